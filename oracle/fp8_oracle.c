@@ -1,0 +1,403 @@
+/*
+ * fp8_oracle.c -- plain, slow, obviously-correct CPU oracle for the FP8 (E4M3)
+ * W8A8 scaled matrix multiply and its activation-quantisation producers.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or call
+ * this file: only the test suite, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header, table or constant with the CUDA
+ * library; every value it uses is derived here from the definitions below.
+ *
+ * What is computed, and where it comes from
+ * -----------------------------------------
+ * The method is the FP8 W8A8 linear layer discussed on the pages
+ *   [P1] "The FP8 tower's cuBLASLt default rests on a false premise: vLLM selects
+ *        FlashInferFP8ScaledMMLinearKernel ..." (vllm.cpp issue #252),
+ *   [P2] "Qwen3.6 NVFP4 baselines (27B and 35B-A3B) must reach vLLM speed parity"
+ *        (vllm.cpp issue #213),
+ *   [P3] "We emit F32 where vLLM emits bf16 on the biggest prefill buffers ..."
+ *        (vllm.cpp issue #417).
+ * The pages name the pieces (E4M3 operands, per-tensor / per-channel /
+ * per-token scales, a bf16 output, a fused RMSNorm -> static FP8 quant that
+ * "quantises once") but print no arithmetic for them, so each function below
+ * writes out the plain definition:
+ *   - E4M3 is the OCP 8-bit floating-point "E4M3" encoding in its finite
+ *     ("fn") variant, the `float8_e4m3fn` / `F8_E4M3` dtype the pages name
+ *     ([P3] "Correction to a claim in the audit"; [P1] "Why it matters").
+ *   - bf16 is IEEE-754 binary32 truncated to 8 significand bits, rounded to
+ *     nearest-even.
+ * Where the pages are silent the readings are:
+ *   R1 round-to-nearest-even everywhere; R2 saturate out-of-range magnitudes to
+ *   +-448 (NaN stays NaN, encoded 0x7F); R3 a quantiser divides by its scale in
+ *   IEEE binary32 (no reciprocal multiply); R4 a per-token scale is
+ *   amax/448 in binary32, and 1.0 for an all-zero row; R5 RMSNorm sums squares
+ *   in binary64, forms 1/sqrt(mean+eps) in binary64, rounds it once to binary32,
+ *   multiplies x*r then *gamma in binary32 and rounds the normalised value to
+ *   bf16 before quantising (this bf16 intermediate is what makes the fused
+ *   producer byte-identical to "RMSNorm to bf16, then static quant", [P3]
+ *   "Ranked follow-ons from the same audit", third bullet); R6 the GEMM
+ *   accumulates exactly (binary64 is exact here, see oracle_gemm_acc_f64),
+ *   multiplies by (double)sa * (double)sb and rounds once to bf16.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fPIC -shared -pthread
+ * (no FMA contraction, IEEE semantics; portable between x86-64 and aarch64).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* E4M3 (OCP FP8, finite variant) decode, straight from the bit fields.      */
+/* ------------------------------------------------------------------------- */
+
+/* Value of one E4M3 code: sign s = bit 7, exponent e = bits 6..3 (bias 7),
+ * mantissa m = bits 2..0.  e == 15 && m == 7 is NaN (0x7F, 0xFF); there is no
+ * infinity.  e == 0 encodes subnormals m * 2^-9.  Normal values are
+ * (1 + m/8) * 2^(e-7) = (8 + m) * 2^(e-10).  Largest finite: 0x7E = 448. */
+double oracle_e4m3_decode(uint8_t code) {
+    int s = (code >> 7) & 1;
+    int e = (code >> 3) & 15;
+    int m = code & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        mag = ldexp((double)m, -9);
+    else
+        mag = ldexp((double)(8 + m), e - 10);
+    return s ? -mag : mag;
+}
+
+void oracle_e4m3_decode_array(const uint8_t *codes, int64_t n, double *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(codes[i]);
+}
+
+/* ------------------------------------------------------------------------- */
+/* E4M3 encode: saturating round-to-nearest-even (readings R1, R2).          */
+/* ------------------------------------------------------------------------- */
+
+/* The 127 non-negative finite E4M3 values, in code order 0x00..0x7E.  Codes
+ * are monotone in value, so the table is sorted; it is filled from the
+ * decoder above, not typed in. */
+static double g_pos_values[127];
+static pthread_once_t g_table_once = PTHREAD_ONCE_INIT;
+
+static void build_table(void) {
+    for (int c = 0; c < 127; ++c) g_pos_values[c] = oracle_e4m3_decode((uint8_t)c);
+}
+
+/* Nearest E4M3 code to the binary32 value v.
+ *   NaN            -> 0x7F (reading R2: the canonical positive NaN code)
+ *   |v| >= 448     -> 0x7E with the sign of v (saturation, covers +-Inf)
+ *   otherwise      -> the nearest table value; on an exact tie between two
+ *                     neighbours, the code whose mantissa LSB (= code LSB) is 0.
+ * The sign of zero is kept: a tiny negative value encodes as 0x80. */
+uint8_t oracle_e4m3_encode(float v) {
+    pthread_once(&g_table_once, build_table);
+    if (isnan(v)) return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    /* largest code c with value <= a (binary search over the sorted table) */
+    int lo = 0, hi = 126;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (g_pos_values[mid] <= a)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    int c = lo;
+    if (g_pos_values[c] != a) {
+        /* a lies strictly between table[c] and table[c+1]; c+1 <= 126 since a < 448 */
+        double below = g_pos_values[c], above = g_pos_values[c + 1];
+        double mid = 0.5 * (below + above); /* exact: both are short dyadic numbers */
+        if (a > mid)
+            c = c + 1;
+        else if (a == mid)
+            c = (c & 1) ? c + 1 : c;
+    }
+    return (uint8_t)(sign | (uint8_t)c);
+}
+
+void oracle_e4m3_encode_array(const float *v, int64_t n, uint8_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(v[i]);
+}
+
+/* Encode the binary32 values whose bit patterns are start, start+1, ...,
+ * start+count-1 (used to sweep whole binades exhaustively). */
+void oracle_e4m3_encode_bits_range(uint32_t start, int64_t count, uint8_t *out) {
+    for (int64_t i = 0; i < count; ++i) {
+        uint32_t bits = start + (uint32_t)i;
+        float v;
+        memcpy(&v, &bits, 4);
+        out[i] = oracle_e4m3_encode(v);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* bf16: round-to-nearest-even from binary64 (and therefore from binary32).  */
+/* ------------------------------------------------------------------------- */
+
+/* bf16 has 8 significand bits (7 stored), the binary32 exponent range, and
+ * subnormals with quantum 2^-133.  The rounding quantum of |v| is
+ * 2^(E-7) for E = floor(log2|v|) >= -126, and 2^-133 below.  |v|/quantum is
+ * < 2^9, rint() rounds it to nearest-even exactly, and the result times the
+ * quantum is an exact bf16 value (or 2^128, which is overflow -> Inf). */
+uint16_t oracle_bf16_rne_f64(double v) {
+    if (isnan(v)) return (uint16_t)(signbit(v) ? 0xFFC0 : 0x7FC0);
+    uint16_t sign = signbit(v) ? 0x8000 : 0x0000;
+    double a = fabs(v);
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80);
+    if (a == 0.0) return sign;
+    int e2;
+    (void)frexp(a, &e2);      /* a = f * 2^e2, 0.5 <= f < 1, so E = e2 - 1 */
+    int E = e2 - 1;
+    if (E < -126) E = -126;   /* subnormal range shares the quantum of 2^-126's binade */
+    double quantum = ldexp(1.0, E - 7);
+    double r = rint(a / quantum) * quantum;
+    if (r >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);
+    float rf = (float)r; /* exact: r is representable in bf16, hence in binary32 */
+    uint32_t bits;
+    memcpy(&bits, &rf, 4);
+    return (uint16_t)(sign | (uint16_t)((bits >> 16) & 0x7FFF));
+}
+
+uint16_t oracle_bf16_rne_f32(float v) { return oracle_bf16_rne_f64((double)v); }
+
+void oracle_bf16_rne_f32_array(const float *v, int64_t n, uint16_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_rne_f32(v[i]);
+}
+
+void oracle_bf16_rne_f64_array(const double *v, int64_t n, uint16_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_rne_f64(v[i]);
+}
+
+/* bf16 bits -> binary32 value (exact: the upper half of a binary32). */
+float oracle_bf16_to_f32(uint16_t b) {
+    uint32_t bits = ((uint32_t)b) << 16;
+    float v;
+    memcpy(&v, &bits, 4);
+    return v;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Activation quantisers ([P3] "Ranked follow-ons": QuantFp8Static and the   */
+/* fused RMSNorm->fp8 producer; [P1] "What is owed" item 2: per-tensor vs     */
+/* per-channel vs per-token granularity, where activation quantisation runs). */
+/* ------------------------------------------------------------------------- */
+
+/* Static per-tensor quantisation: q = enc(fp32(x) / s), division in binary32
+ * (reading R3).  s is the dequantisation multiplier: x ~= dec(q) * s. */
+void oracle_quant_static(const uint16_t *x, float s, int64_t M, int64_t K, uint8_t *q) {
+    for (int64_t i = 0; i < M * K; ++i) {
+        float xv = oracle_bf16_to_f32(x[i]);
+        volatile float t = xv / s; /* one binary32 division, rounded to nearest */
+        q[i] = oracle_e4m3_encode(t);
+    }
+}
+
+/* Dynamic per-token quantisation (reading R4):
+ *   amax_m = max_k |x[m,k]|  (exact; NaN entries are ignored by the max)
+ *   s_m    = fp32(amax_m / 448), or 1.0 if amax_m == 0
+ *   q[m,k] = enc(fp32(x[m,k]) / s_m) */
+void oracle_quant_per_token(const uint16_t *x, int64_t M, int64_t K, uint8_t *q, float *s_out) {
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *row = x + m * K;
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf(oracle_bf16_to_f32(row[k]));
+            if (a > amax) amax = a; /* NaN compares false and is skipped */
+        }
+        volatile float s = amax / 448.0f;
+        float sv = (amax == 0.0f) ? 1.0f : s;
+        s_out[m] = sv;
+        for (int64_t k = 0; k < K; ++k) {
+            volatile float t = oracle_bf16_to_f32(row[k]) / sv;
+            q[m * K + k] = oracle_e4m3_encode(t);
+        }
+    }
+}
+
+/* RMSNorm to bf16 (reading R5), the unfused producer's first half:
+ *   ss    = sum_k (double)x_k^2                       (binary64)
+ *   r64   = 1 / sqrt(ss / K + (double)eps)            (binary64, correctly rounded ops)
+ *   r     = (float) r64
+ *   h_k   = bf16( (fp32(x_k) * r) * fp32(gamma_k) )   (two binary32 multiplies) */
+void oracle_rmsnorm_bf16(const uint16_t *x, const uint16_t *gamma, float eps, int64_t M, int64_t K,
+                         uint16_t *h) {
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *row = x + m * K;
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double xv = (double)oracle_bf16_to_f32(row[k]);
+            ss = ss + xv * xv; /* xv*xv is exact: 16 significand bits */
+        }
+        volatile double mean = ss / (double)K;
+        volatile double denom = sqrt(mean + (double)eps);
+        volatile double r64 = 1.0 / denom;
+        float r = (float)r64;
+        for (int64_t k = 0; k < K; ++k) {
+            volatile float t = oracle_bf16_to_f32(row[k]) * r;
+            volatile float u = t * oracle_bf16_to_f32(gamma[k]);
+            h[m * K + k] = oracle_bf16_rne_f32(u);
+        }
+    }
+}
+
+/* Fused RMSNorm -> static FP8 quant: q = enc(fp32(h) / s) with h from
+ * oracle_rmsnorm_bf16.  Written as the composition on purpose: the fused
+ * producer is defined to equal "norm to bf16, then static quant". */
+void oracle_rmsnorm_quant(const uint16_t *x, const uint16_t *gamma, float eps, float s, int64_t M,
+                          int64_t K, uint8_t *q) {
+    uint16_t *h = (uint16_t *)malloc((size_t)(M * K > 0 ? M * K : 1) * sizeof(uint16_t));
+    oracle_rmsnorm_bf16(x, gamma, eps, M, K, h);
+    oracle_quant_static(h, s, M, K, q);
+    free(h);
+}
+
+/* ------------------------------------------------------------------------- */
+/* The scaled GEMM ([P1] "What is owed" item 2 and "CORRECTION": bmm_fp8(a,  */
+/* b, scale_a, scale_b, out_dtype, ...); [P3] "FINDING 1": out dtype bf16;   */
+/* [P2] "Root-cause theme" item 1: weights stored [N,K], not transposed).    */
+/* ------------------------------------------------------------------------- */
+
+/* Exactness argument: every E4M3 value is an integer multiple of 2^-9 with
+ * magnitude <= 448 = 229376 * 2^-9, so each product is an integer multiple of
+ * 2^-18 below 2^36 * 2^-18, and a sum of K <= 2^15 such products is an integer
+ * multiple of 2^-18 below 2^51 * 2^-18.  binary64 represents every such value
+ * exactly, so the sum is exact in any order and equals the int64 twin below. */
+
+typedef struct {
+    const uint8_t *A, *B;
+    int64_t M, N, K;
+    double *acc;
+    int64_t *acc_i;
+    int tid, nthreads;
+} gemm_job;
+
+static double g_lut[256];
+static int64_t g_lut_i[256];
+static int g_lut_nan[256];
+static pthread_once_t g_lut_once = PTHREAD_ONCE_INIT;
+
+static void build_lut(void) {
+    for (int c = 0; c < 256; ++c) {
+        double v = oracle_e4m3_decode((uint8_t)c);
+        g_lut[c] = v;
+        g_lut_nan[c] = isnan(v) ? 1 : 0;
+        g_lut_i[c] = isnan(v) ? 0 : (int64_t)ldexp(v, 9); /* exact integer */
+    }
+}
+
+static void *gemm_f64_worker(void *p) {
+    gemm_job *j = (gemm_job *)p;
+    for (int64_t m = j->tid; m < j->M; m += j->nthreads) {
+        const uint8_t *a = j->A + m * j->K;
+        for (int64_t n = 0; n < j->N; ++n) {
+            const uint8_t *b = j->B + n * j->K;
+            double s = 0.0;
+            for (int64_t k = 0; k < j->K; ++k) s += g_lut[a[k]] * g_lut[b[k]];
+            j->acc[m * j->N + n] = s;
+        }
+    }
+    return NULL;
+}
+
+static void *gemm_i64_worker(void *p) {
+    gemm_job *j = (gemm_job *)p;
+    for (int64_t m = j->tid; m < j->M; m += j->nthreads) {
+        const uint8_t *a = j->A + m * j->K;
+        for (int64_t n = 0; n < j->N; ++n) {
+            const uint8_t *b = j->B + n * j->K;
+            int64_t s = 0;
+            for (int64_t k = 0; k < j->K; ++k) s += g_lut_i[a[k]] * g_lut_i[b[k]];
+            j->acc_i[m * j->N + n] = s;
+        }
+    }
+    return NULL;
+}
+
+static void run_jobs(void *(*fn)(void *), gemm_job *base, int nthreads) {
+    if (nthreads < 1) nthreads = 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    gemm_job *jobs = (gemm_job *)malloc(sizeof(gemm_job) * (size_t)nthreads);
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = *base;
+        jobs[t].tid = t;
+        jobs[t].nthreads = nthreads;
+        pthread_create(&th[t], NULL, fn, &jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    free(th);
+    free(jobs);
+}
+
+/* acc[m,n] = sum_k dec(A[m,k]) * dec(B[n,k]) in binary64 (exact, see above).
+ * A is [M,K] row-major, B is [N,K] row-major (K contiguous), acc is [M,N]. */
+void oracle_gemm_acc_f64(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
+                         double *acc, int nthreads) {
+    pthread_once(&g_lut_once, build_lut);
+    gemm_job j = {A, B, M, N, K, acc, NULL, 0, 1};
+    run_jobs(gemm_f64_worker, &j, nthreads);
+}
+
+/* Integer twin: acc_i[m,n] = sum_k (dec(A)*2^9) * (dec(B)*2^9), so that
+ * acc = acc_i * 2^-18.  NaN codes contribute 0 here (callers avoid them). */
+void oracle_gemm_acc_i64(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
+                         int64_t *acc_i, int nthreads) {
+    pthread_once(&g_lut_once, build_lut);
+    gemm_job j = {A, B, M, N, K, NULL, acc_i, 0, 1};
+    run_jobs(gemm_i64_worker, &j, nthreads);
+}
+
+/* Scale granularities, as a plain enumeration of which index each scale takes:
+ *   0 per-tensor:           sa[0], sb[0]
+ *   1 per-channel:          sa[0], sb[n]   (per output channel of the weight)
+ *   2 per-token x channel:  sa[m], sb[n]
+ *   3 per-token:            sa[m], sb[0]
+ * ([P1] "What is owed" item 2 names per-tensor, per-channel and per-token.) */
+static double scale_of(const float *sa, const float *sb, int gran, int64_t m, int64_t n) {
+    double a = (double)((gran == 2 || gran == 3) ? sa[m] : sa[0]);
+    double b = (double)((gran == 1 || gran == 2) ? sb[n] : sb[0]);
+    return a * b; /* exact: a 24-bit by 24-bit product fits in 53 bits */
+}
+
+/* y64[m,n] = acc[m,n] * (sa * sb) in binary64, y_bf16 = bf16_rne(y64).
+ * Either output pointer may be NULL. */
+void oracle_scaled_mm(const uint8_t *A, const uint8_t *B, const float *sa, const float *sb, int gran,
+                      int64_t M, int64_t N, int64_t K, double *y64, uint16_t *y_bf16, int nthreads) {
+    double *acc = (double *)malloc(sizeof(double) * (size_t)(M * N > 0 ? M * N : 1));
+    oracle_gemm_acc_f64(A, B, M, N, K, acc, nthreads);
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double y = acc[m * N + n] * scale_of(sa, sb, gran, m, n);
+            if (y64) y64[m * N + n] = y;
+            if (y_bf16) y_bf16[m * N + n] = oracle_bf16_rne_f64(y);
+        }
+    free(acc);
+}
+
+/* The same definition evaluated only at the listed (row, col) pairs, for
+ * checking outputs of shapes too large to compute in full on the CPU. */
+void oracle_scaled_mm_points(const uint8_t *A, const uint8_t *B, const float *sa, const float *sb,
+                             int gran, int64_t M, int64_t N, int64_t K, const int64_t *rows,
+                             const int64_t *cols, int64_t npts, double *y64) {
+    pthread_once(&g_lut_once, build_lut);
+    (void)M;
+    (void)N;
+    for (int64_t i = 0; i < npts; ++i) {
+        const uint8_t *a = A + rows[i] * K;
+        const uint8_t *b = B + cols[i] * K;
+        double s = 0.0;
+        for (int64_t k = 0; k < K; ++k) s += g_lut[a[k]] * g_lut[b[k]];
+        y64[i] = s * scale_of(sa, sb, gran, rows[i], cols[i]);
+    }
+}
+
+int oracle_has_nan_code(const uint8_t *codes, int64_t n) {
+    pthread_once(&g_lut_once, build_lut);
+    for (int64_t i = 0; i < n; ++i)
+        if (g_lut_nan[codes[i]]) return 1;
+    return 0;
+}

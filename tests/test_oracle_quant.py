@@ -1,0 +1,153 @@
+"""Pins for the oracle's quantisers and RMSNorm producer (CPU only)."""
+import math
+
+import numpy as np
+import sympy
+import torch
+
+import workloads
+
+
+def _torch_e4m3(v32: np.ndarray) -> np.ndarray:
+    """Library encoding: torch's RNE float8_e4m3fn cast after clamping to +-448
+    (torch maps magnitudes above 464 to NaN instead of saturating)."""
+    t = torch.from_numpy(np.ascontiguousarray(v32, np.float32)).clamp(-448.0, 448.0)
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _as_f32(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def test_static_quant_vs_torch(orc):
+    g = workloads.rng(10)
+    x = workloads.bf16_normal(g, (16, 512), std=3.0)
+    for s in (np.float32(1 / 56), np.float32(0.01), np.float32(0.37), np.float32(2.5e-3)):
+        q = orc.quant_static(x, float(s))
+        t = torch.from_numpy(_as_f32(x).copy()) / torch.tensor(s)      # IEEE binary32 division
+        assert np.array_equal(q, _torch_e4m3(t.numpy()))
+
+
+def test_static_quant_saturates(orc):
+    x = np.array([[0x4400, 0xC400, 0x7F80, 0xFF80]], np.uint16)  # 512, -512, +inf, -inf
+    q = orc.quant_static(x, 1.0)
+    assert q.tolist() == [[0x7E, 0xFE, 0x7E, 0xFE]]
+
+
+def test_quant_dequant_idempotent(orc):
+    """enc(fp32(dec(q)*s)/s) == q for every finite code over a sweep of scales."""
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    dec = orc.e4m3_decode(codes)
+    for s in np.exp2(np.linspace(-12, 6, 37)).astype(np.float32):
+        v = (dec * float(s)).astype(np.float32)          # fp32(dec * s)
+        back = (v / s).astype(np.float32)
+        assert np.array_equal(orc.e4m3_encode(back), codes), s
+
+
+def test_per_token_properties(orc):
+    g = workloads.rng(11)
+    x = workloads.bf16_normal_with_outliers(g, (64, 640))
+    q, s = orc.quant_per_token(x)
+    xf = _as_f32(x)
+    amax = np.abs(xf).max(axis=1)
+    assert np.array_equal(s, (amax / np.float32(448.0)).astype(np.float32))
+    # the amax element of each row encodes to +-448
+    idx = np.abs(xf).argmax(axis=1)
+    assert np.all((q[np.arange(64), idx] & 0x7F) == 0x7E)
+    # same bytes as torch's encoder on x / s
+    assert np.array_equal(q, _torch_e4m3(xf / s[:, None]))
+
+
+def test_per_token_power_of_two_equivariance(orc):
+    """Scaling a row by 2^k scales its scale by 2^k and leaves the codes alone."""
+    g = workloads.rng(12)
+    x = workloads.bf16_normal(g, (8, 256))
+    q0, s0 = orc.quant_per_token(x)
+    for k in (-5, 3, 9):
+        xk = ((_as_f32(x) * np.float32(2.0 ** k)).view(np.uint32) >> 16).astype(np.uint16)  # exact
+        qk, sk = orc.quant_per_token(xk)
+        assert np.array_equal(qk, q0)
+        assert np.array_equal(sk, (s0 * np.float32(2.0 ** k)).astype(np.float32))
+
+
+def test_per_token_zero_row_and_single_row(orc):
+    x = np.zeros((2, 32), np.uint16)
+    x[1, 5] = 0x3F80  # 1.0
+    q, s = orc.quant_per_token(x)
+    assert s[0] == 1.0 and np.all(q[0] == 0)
+    assert s[1] == np.float32(1.0) / np.float32(448.0)
+    assert q[1, 5] == 0x7E and np.count_nonzero(q[1]) == 1
+
+
+def test_per_token_of_flattened_tensor_is_static_amax_quant(orc):
+    """One-row per-token quant of a flattened tensor == static quant with s = amax/448."""
+    w = workloads.bf16_normal(workloads.rng(13), (64, 128), std=0.02)
+    q1, s1 = orc.quant_per_token(w.reshape(1, -1))
+    q2 = orc.quant_static(w, float(s1[0]))
+    assert np.array_equal(q1.reshape(64, 128), q2)
+
+
+def _rms_exact(xs, eps, gamma, k):
+    """High-precision value of x_k * gamma_k / sqrt(mean(x^2) + eps)."""
+    xs = [sympy.Rational(float(v)) for v in xs]
+    mean = sum(v * v for v in xs) / len(xs)
+    r = 1 / sympy.sqrt(mean + sympy.Rational(float(np.float32(eps))))
+    return float(sympy.N(xs[k] * sympy.Rational(float(gamma)) * r, 40))
+
+
+def test_rmsnorm_closed_forms(orc):
+    """Constant rows and single-spike rows against a 40-digit evaluation: the
+    oracle lands within one bf16 rounding of the exact value."""
+    K = 64
+    cases = []
+    for c in (0x3F80, 0x4040, 0xBE00, 0x0080):         # 1.0, 3.0, -0.125, 2^-126
+        cases.append(np.full(K, c, np.uint16))
+    spike = np.zeros(K, np.uint16)
+    spike[7] = 0x40A0                                   # 5.0
+    cases.append(spike)
+    gamma = np.full(K, 0x3FC0, np.uint16)               # 1.5
+    for eps in (1e-6, 0.0, 0.25):
+        for row in cases:
+            h = orc.rmsnorm_bf16(row[None, :], gamma, eps)[0]
+            hv = _as_f32(h)
+            for k in (0, 7):
+                want = _rms_exact(_as_f32(row), eps, 1.5, k)
+                ulp = 2.0 ** (math.floor(math.log2(abs(want))) - 7) if want != 0 else 0.0
+                assert abs(float(hv[k]) - want) <= ulp, (row[:2], eps, k, hv[k], want)
+
+
+def test_rmsnorm_scale_invariance(orc):
+    """With eps = 0, RMSNorm(2^j x) == RMSNorm(x) exactly (every step scales exactly)."""
+    g = workloads.rng(14)
+    x = workloads.bf16_normal(g, (4, 512))
+    gamma = workloads.bf16_normal(g, (512,), mean=1.0, std=0.1)
+    h0 = orc.rmsnorm_bf16(x, gamma, 0.0)
+    for j in (-7, 4):
+        xj = ((_as_f32(x) * np.float32(2.0 ** j)).view(np.uint32) >> 16).astype(np.uint16)
+        assert np.array_equal(orc.rmsnorm_bf16(xj, gamma, 0.0), h0)
+
+
+def test_rmsnorm_vs_numpy_restatement(orc):
+    """The pinned arithmetic restated with numpy's vectorised ops (different
+    summation order, numpy sqrt) gives the same bf16 bits."""
+    g = workloads.rng(15)
+    x = workloads.bf16_normal(g, (32, 5120))
+    gamma = workloads.bf16_normal(g, (5120,), mean=1.0, std=0.1)
+    h = orc.rmsnorm_bf16(x, gamma, 1e-6)
+    xf = _as_f32(x)
+    ss = np.sum(xf.astype(np.float64) ** 2, axis=1)
+    r = (1.0 / np.sqrt(ss / 5120.0 + float(np.float32(1e-6)))).astype(np.float32)
+    u = (xf * r[:, None]).astype(np.float32) * _as_f32(gamma)[None, :]
+    ref = torch.from_numpy(u.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(h, ref)
+
+
+def test_rmsnorm_quant_is_norm_then_static_quant(orc):
+    g = workloads.rng(16)
+    x = workloads.bf16_normal(g, (8, 1024))
+    gamma = workloads.bf16_normal(g, (1024,), mean=1.0, std=0.1)
+    s = float(np.float32(1 / 56))
+    assert np.array_equal(orc.rmsnorm_quant(x, gamma, 1e-6, s), orc.quant_static(orc.rmsnorm_bf16(x, gamma, 1e-6), s))
+    # zero rows: eps keeps the root finite and every code is zero
+    z = np.zeros((2, 1024), np.uint16)
+    assert np.all(orc.rmsnorm_quant(z, gamma, 1e-6, s) == 0)
