@@ -1,0 +1,367 @@
+"""Benchmark of the FP8 W8A8 decode hot path on GB300.
+
+One step = one pass of the decode fused path over one batch: for each
+M in {1, 2, 4, 8, 16, 32}, the fused RMSNorm -> static E4M3 quantisation of
+x[:M] ([M, 5120] bf16) followed by the merged-QKV FP8 GEMM (N=10240, K=5120,
+per-output-channel weight scales, bf16 out).  Every M uses its own weight copy,
+so a step streams six distinct 52.4 MB weights (315 MB, more than twice the
+129 MB L2) and each GEMM reads its weight from HBM.
+
+The value is algorithmic bytes per step / device time per step, in TB/s
+(weights N*K, activations, outputs, scales, the norm's x and gamma).  The
+step is captured in a CUDA graph and replayed.  See `python bench.py -h`.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas; no data-path collective) and rank 0 prints one JSON line.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "fp8_scaled_mm HBM TB/s (M≤32) & FP8 TFLOPS (prefill), % of GB300 roofline"
+MS = workloads.DECODE_FUSED_MS
+N_QKV, K_HID = workloads.QKV_N, workloads.HIDDEN
+WORKLOAD = ("decode fused path: RMSNorm(eps 1e-6) -> static per-tensor E4M3 quant -> merged-QKV FP8 GEMM "
+            "N=10240 K=5120, per-channel weight scales, bf16 out; one pass per M in {1,2,4,8,16,32}")
+INNER = 20  # steps captured per CUDA graph
+
+
+def gemm_bytes(M, N=N_QKV, K=K_HID):
+    """Algorithmic bytes of one decode GEMM: weights, activations, bf16 output,
+    per-channel weight scales and the scalar activation scale."""
+    return N * K + M * K + 2 * M * N + 4 * N + 4
+
+
+def norm_bytes(M, K=K_HID):
+    """Algorithmic bytes of one fused RMSNorm -> quant: bf16 x and gamma in,
+    E4M3 out, the scale."""
+    return 2 * M * K + 2 * K + M * K + 4
+
+
+def step_bytes():
+    return sum(gemm_bytes(m) + norm_bytes(m) for m in MS)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fp8_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.dev), "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[4:8]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class DecodeFusedStep:
+    """Device buffers and the captured CUDA graph of the decode fused step."""
+
+    def __init__(self, torch, fp8, device, seed=0):
+        self.torch, self.fp8, self.device = torch, fp8, device
+        g = workloads.rng(seed)
+        x = workloads.bf16_normal(g, (32, K_HID))
+        gamma = workloads.bf16_normal(g, (K_HID,), mean=1.0, std=0.1)
+        self.x = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        self.gamma = torch.from_numpy(gamma.view(np.int16)).view(torch.bfloat16).to(device)
+        self.s_a = torch.tensor([float(workloads.STATIC_INPUT_SCALE)], dtype=torch.float32, device=device)
+        self.W, self.sb, self.A, self.Y = [], [], [], []
+        for i, m in enumerate(MS):
+            self.W.append(workloads.device_e4m3_codes(torch, (N_QKV, K_HID), seed=100 + i, device=device)
+                          .view(torch.float8_e4m3fn))
+            self.sb.append(workloads.device_uniform_f32(torch, (N_QKV,), 0.5e-3, 2e-3, seed=200 + i, device=device))
+            self.A.append(torch.empty((m, K_HID), dtype=torch.float8_e4m3fn, device=device))
+            self.Y.append(torch.empty((m, N_QKV), dtype=torch.bfloat16, device=device))
+
+    def launch_step(self):
+        fp8 = self.fp8
+        for i, m in enumerate(MS):
+            fp8.rmsnorm_quant_fp8(self.x[:m], self.gamma, workloads.RMS_EPS, self.s_a, out=self.A[i])
+            fp8.fp8_scaled_mm(self.A[i], self.W[i], self.s_a, self.sb[i], fp8.GRAN_PER_CHANNEL, out=self.Y[i])
+
+    def launch_gemms(self):
+        fp8 = self.fp8
+        for i, m in enumerate(MS):
+            fp8.fp8_scaled_mm(self.A[i], self.W[i], self.s_a, self.sb[i], fp8.GRAN_PER_CHANNEL, out=self.Y[i])
+
+    def capture(self, fn, inner):
+        torch = self.torch
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        torch.cuda.synchronize(self.device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(inner):
+                fn()
+        return graph
+
+
+def time_graph(torch, graph, reps, dist_barrier):
+    """Device time of `reps` replays (CUDA events on the replay stream), max over ranks."""
+    stream = torch.cuda.current_stream()
+    dist_barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier()
+    return t0.elapsed_time(t1)
+
+
+def cpu_baseline_sample(budget_s=10.0):
+    """The oracle, as it stands, on the decode fused step (all six M values,
+    full N), repeated until about `budget_s` seconds of wall time."""
+    import oracle
+    d = workloads.decode_fused(seed=0)
+    nthreads = oracle.default_threads()
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        for m in MS:
+            A = oracle.rmsnorm_quant(d["x"][:m], d["gamma"], d["eps"], float(d["s_a"]))
+            oracle.scaled_mm(A, d["B"], d["s_a"], d["sb"], 1, nthreads=nthreads)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": steps * step_bytes() / el / 1e12, "unit": "TB/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{steps} full decode-fused steps (6 norm-quants + 6 GEMMs 10240x5120, M=1..32), "
+                      f"{el:.1f} s wall"}
+
+
+def run_ours(args, rank, world, dist_barrier, dist_max):
+    import torch
+    import fp8_w8a8_scaled_gb300 as fp8
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    fp8.clear_device_error()
+    step = DecodeFusedStep(torch, fp8, device)
+    step_graph = step.capture(step.launch_step, INNER)
+    gemm_graph = step.capture(step.launch_gemms, INNER)
+    reps = max(1, (args.steps + INNER - 1) // INNER)
+    steps = reps * INNER
+    warm = max(1, (args.warmup + INNER - 1) // INNER)
+
+    for _ in range(warm):
+        step_graph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ms = dist_max(time_graph(torch, step_graph, reps, dist_barrier))
+    clk = clocks.stop()
+    ms_step = ms / steps
+    value = world * step_bytes() / (ms_step * 1e-3) / 1e12
+
+    # roofline of the dominant kernel: the GEMM launches alone, same rotation
+    for _ in range(warm):
+        gemm_graph.replay()
+    ms_g = dist_max(time_graph(torch, gemm_graph, reps, dist_barrier))
+    per_launch_ms = ms_g / (steps * len(MS))
+    gbytes = sum(gemm_bytes(m) for m in MS) / len(MS)
+    achieved = gbytes / (per_launch_ms * 1e-3) / 1e9
+    peak, peak_src = measured_peaks()
+
+    # end to end through the public API with host buffers: H2D of x, the step, D2H of the outputs
+    x_host = step.x.cpu().pin_memory()
+    y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in step.Y]
+    one = step.capture(step.launch_step, 1)
+    e2e_steps = min(steps, 2000)
+    dist_barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        step.x.copy_(x_host, non_blocking=True)
+        one.replay()
+        for yd, yh in zip(step.Y, y_host):
+            yh.copy_(yd, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = dist_max(e0.elapsed_time(e1)) / e2e_steps
+    h2d = step.x.numel() * 2
+    d2h = sum(y.numel() * 2 for y in step.Y)
+    err = fp8.get_device_error()
+    if err:
+        raise RuntimeError(f"device error word {err:#x}")
+
+    out = {
+        "metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": world, "steps": steps,
+        "warmup": warm * INNER, "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "bytes_per_step": step_bytes(), "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: six distinct 52.4 MB weights per step (315 MB)",
+                   "graph": f"{INNER} steps per CUDA graph replay"},
+        "roofline": {"kernel": "decode_gemm_kernel (tcgen05 swap-AB split-K)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": None,
+                     "bytes_per_launch": gbytes, "us_per_launch": round(per_launch_ms * 1e3, 3)},
+        "e2e": {"value": round(world * step_bytes() / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6)},
+        "gpu_launches": steps * 2 * len(MS),
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_sample(args.cpu_seconds)
+    return out
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The oracle timed on the host cores on the same workload and metric: each
+    step is a bounded sample (the first `cols` output channels of every
+    M's GEMM, plus the full norm-quants), sized so the whole run takes about
+    `--ref-seconds` of wall time."""
+    import oracle
+    d = workloads.decode_fused(seed=0)
+    nthreads = oracle.default_threads()
+    A_by_m = {}
+
+    def one_step(cols):
+        for m in MS:
+            A_by_m[m] = oracle.rmsnorm_quant(d["x"][:m], d["gamma"], d["eps"], float(d["s_a"]))
+            oracle.scaled_mm(A_by_m[m], d["B"][:cols], d["s_a"], d["sb"][:cols], 1, nthreads=nthreads)
+
+    def sample_bytes(cols):
+        return sum(gemm_bytes(m, N=cols) + norm_bytes(m) for m in MS)
+
+    t0 = time.perf_counter()
+    one_step(256)
+    per_col = (time.perf_counter() - t0) / 256
+    total = max(1, args.steps + args.warmup)
+    cols = int(max(8, min(N_QKV, args.ref_seconds / total / max(per_col, 1e-9))))
+    cols -= cols % 8
+    for _ in range(args.warmup):
+        one_step(cols)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step(cols)
+    el = time.perf_counter() - t0
+    value = args.steps * sample_bytes(cols) / el / 1e12
+    sample = f"{args.steps} steps, each the norm-quants plus the first {cols} of 10240 GEMM output channels for M=1..32"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 8), "unit": "TB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": round(value, 8), "unit": "TB/s", "cores": nthreads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 8), "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="wall-time budget of the oracle CPU baseline")
+    ap.add_argument("--ref-seconds", type=float, default=60.0, help="wall-time budget of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def dmax(v):
+        if dist is None:
+            return v
+        import torch
+        t = torch.tensor([float(v)], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    out = run_ours(args, rank, world, barrier, dmax)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+"""Python binding of the GB300 FP8 (E4M3) W8A8 scaled-GEMM library.
+
+Argument marshalling only: every function here checks torch tensor dtypes,
+shapes, contiguity and devices, then calls the C ABI of ``libfp8w8a8``
+(``include/fp8w8a8.h``) with raw device pointers and the current torch CUDA
+stream.  All arithmetic happens in the library's CUDA kernels; there is no
+fallback of any kind -- if the library is missing or a call fails, an
+exception is raised.
+
+Functions carry the C names: ``fp8_scaled_mm``, ``rmsnorm_quant_fp8``,
+``quant_fp8_per_token``, ``quant_fp8_static``.
+"""
+import ctypes
+import os
+import platform
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+FP8_OK = 0
+FP8_ERR_INVALID_ARG = 1
+FP8_ERR_ALIGNMENT = 2
+FP8_ERR_UNSUPPORTED = 3
+FP8_ERR_CUDA = 4
+FP8_ERR_DEVICE = 5
+
+GRAN_PER_TENSOR = 0
+GRAN_PER_CHANNEL = 1
+GRAN_PER_TOKEN_CHANNEL = 2
+GRAN_PER_TOKEN = 3
+
+OUT_BF16 = 0
+
+KERNEL_NONE = 0
+KERNEL_DECODE_SPLITK = 1
+KERNEL_PREFILL = 2
+
+E4M3 = torch.float8_e4m3fn
+
+_lib = None
+_current_device = None
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, status, what):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def lib_path() -> str:
+    return os.path.join(HERE, "_build", f"libfp8w8a8_{platform.machine()}.so")
+
+
+def lib():
+    """The loaded C library (ctypes.CDLL) with argument types declared."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libfp8w8a8 is not built ({path} missing): run __graft_entry__.build() "
+                           "or python fp8_w8a8_scaled_gb300/build.py")
+    L = ctypes.CDLL(path)
+    P, I64, I32, F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    L.fp8_scaled_mm.argtypes = [P, P, P, P, I32, I32, I64, I64, I64, P, P]
+    L.fp8_scaled_mm.restype = I32
+    L.rmsnorm_quant_fp8.argtypes = [P, P, F32, P, P, I64, I64, P]
+    L.rmsnorm_quant_fp8.restype = I32
+    L.quant_fp8_per_token.argtypes = [P, P, P, I64, I64, P]
+    L.quant_fp8_per_token.restype = I32
+    L.quant_fp8_static.argtypes = [P, P, P, I64, I64, P]
+    L.quant_fp8_static.restype = I32
+    L.fp8_status_string.argtypes = [I32]
+    L.fp8_status_string.restype = ctypes.c_char_p
+    L.fp8_describe_dispatch.argtypes = [I64, I64, I64, I32]
+    L.fp8_describe_dispatch.restype = I32
+    L.fp8_decode_split.argtypes = [I64, I64, I64]
+    L.fp8_decode_split.restype = I32
+    L.fp8_decode_split_for_sms.argtypes = [I64, I64, I64, I32]
+    L.fp8_decode_split_for_sms.restype = I32
+    L.fp8_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    L.fp8_get_device_error.restype = I32
+    L.fp8_clear_device_error.argtypes = []
+    L.fp8_clear_device_error.restype = I32
+    L.fp8_library_version.argtypes = []
+    L.fp8_library_version.restype = I32
+    L.fp8_set_device.argtypes = [I32]
+    L.fp8_set_device.restype = I32
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().fp8_status_string(int(status)).decode()
+
+
+def _check(status, what):
+    if status != FP8_OK:
+        raise Fp8Error(status, what)
+
+
+def _stream_of(t: torch.Tensor):
+    global _current_device
+    dev = t.device.index if t.device.index is not None else torch.cuda.current_device()
+    if dev != _current_device:
+        _check(lib().fp8_set_device(dev), "fp8_set_device")
+        _current_device = dev
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need(t: torch.Tensor, name: str, dtypes, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, has {t.dim()}")
+
+
+_FP8 = (E4M3, torch.uint8)
+
+
+def fp8_scaled_mm(A, B, scale_a, scale_b, granularity=None, out_dtype=OUT_BF16, out=None):
+    """y = bf16((A @ B.T) * scale_a * scale_b) for E4M3 A [M,K] and B [N,K].
+
+    ``granularity`` defaults from the scale lengths: scale_a has 1 or M
+    elements, scale_b 1 or N."""
+    _need(A, "A", _FP8, 2)
+    _need(B, "B", _FP8, 2)
+    _need(scale_a, "scale_a", (torch.float32,))
+    _need(scale_b, "scale_b", (torch.float32,))
+    M, K = A.shape
+    N, Kb = B.shape
+    if Kb != K:
+        raise ValueError(f"A is [{M},{K}] but B is [{N},{Kb}]")
+    if granularity is None:
+        tok = scale_a.numel() == M and M != 1
+        ch = scale_b.numel() == N and N != 1
+        granularity = {(False, False): 0, (False, True): 1, (True, True): 2, (True, False): 3}[(tok, ch)]
+    want_a = M if granularity in (2, 3) else 1
+    want_b = N if granularity in (1, 2) else 1
+    if scale_a.numel() < want_a or scale_b.numel() < want_b:
+        raise ValueError(f"granularity {granularity} needs scale_a[{want_a}], scale_b[{want_b}]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _need(out, "out", (torch.bfloat16,), 2)
+        if tuple(out.shape) != (M, N):
+            raise ValueError(f"out must be [{M},{N}]")
+    _check(lib().fp8_scaled_mm(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), int(granularity), int(out_dtype),
+                               M, N, K, _ptr(out), _stream_of(A)), "fp8_scaled_mm")
+    return out
+
+
+def rmsnorm_quant_fp8(x, gamma, eps, scale, out=None):
+    """Fused RMSNorm -> static E4M3 quantisation of bf16 x [M,K]."""
+    _need(x, "x", (torch.bfloat16,), 2)
+    _need(gamma, "gamma", (torch.bfloat16,), 1)
+    _need(scale, "scale", (torch.float32,))
+    M, K = x.shape
+    if gamma.numel() != K:
+        raise ValueError("gamma must have K elements")
+    if out is None:
+        out = torch.empty((M, K), dtype=E4M3, device=x.device)
+    else:
+        _need(out, "out", _FP8, 2)
+    _check(lib().rmsnorm_quant_fp8(_ptr(x), _ptr(gamma), float(eps), _ptr(scale), _ptr(out), M, K, _stream_of(x)),
+           "rmsnorm_quant_fp8")
+    return out
+
+
+def quant_fp8_per_token(x, out=None, scale_out=None):
+    """Dynamic per-token E4M3 quantisation of bf16 x [M,K]; returns (q, s[M])."""
+    _need(x, "x", (torch.bfloat16,), 2)
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, K), dtype=E4M3, device=x.device)
+    else:
+        _need(out, "out", _FP8, 2)
+    if scale_out is None:
+        scale_out = torch.empty((M,), dtype=torch.float32, device=x.device)
+    else:
+        _need(scale_out, "scale_out", (torch.float32,))
+    _check(lib().quant_fp8_per_token(_ptr(x), _ptr(out), _ptr(scale_out), M, K, _stream_of(x)),
+           "quant_fp8_per_token")
+    return out, scale_out
+
+
+def quant_fp8_static(x, scale, out=None):
+    """Static per-tensor E4M3 quantisation of bf16 x [M,K] by the device scalar `scale`."""
+    _need(x, "x", (torch.bfloat16,), 2)
+    _need(scale, "scale", (torch.float32,))
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, K), dtype=E4M3, device=x.device)
+    else:
+        _need(out, "out", _FP8, 2)
+    _check(lib().quant_fp8_static(_ptr(x), _ptr(scale), _ptr(out), M, K, _stream_of(x)), "quant_fp8_static")
+    return out
+
+
+def describe_dispatch(M, N, K, granularity=0) -> int:
+    return lib().fp8_describe_dispatch(M, N, K, granularity)
+
+
+def decode_split(M, N, K) -> int:
+    return lib().fp8_decode_split(M, N, K)
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronises the stream and returns the device error word (0 = no error)."""
+    word = ctypes.c_uint32(0)
+    s = ctypes.c_void_p(stream if stream is not None else torch.cuda.current_stream().cuda_stream)
+    st = lib().fp8_get_device_error(s, ctypes.byref(word))
+    if st not in (FP8_OK, FP8_ERR_DEVICE):
+        raise Fp8Error(st, "fp8_get_device_error")
+    return int(word.value)
+
+
+def clear_device_error():
+    _check(lib().fp8_clear_device_error(), "fp8_clear_device_error")

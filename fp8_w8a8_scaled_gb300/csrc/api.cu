@@ -1,0 +1,204 @@
+// api.cu -- the C ABI (include/fp8w8a8.h): argument validation, dispatch,
+// TMA descriptor creation, the device error word.  Every entry point validates
+// everything before touching the GPU, so the validation paths run (and are
+// tested) on a machine without a GPU.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fp8w8a8.h"
+#include "kernels.h"
+
+namespace {
+
+// One error word per device (a module-scope __device__ variable exists once
+// per device that loads the library); host code reaches it only through the
+// address cudaGetSymbolAddress returns with that device current.
+__device__ uint32_t g_error_word;
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kI32Max = 2147483647;
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    uint32_t *err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Per-device state, created on first use with the device current.
+fp8_status device_state(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &st = g_dev[dev];
+    if (!st.ready) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FP8_ERR_CUDA;
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_error_word) != cudaSuccess || addr == nullptr) return FP8_ERR_CUDA;
+        if (g_encode == nullptr) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return FP8_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        st.num_sms = sms;
+        st.err = static_cast<uint32_t *>(addr);
+        st.ready = true;
+    }
+    *out = &st;
+    return FP8_OK;
+}
+
+// 2-D E4M3 tensor [rows, cols] (cols contiguous) read in boxes of
+// box_rows x 128 bytes with the 128-byte swizzle; out-of-range elements read
+// as zero.
+fp8_status make_tmap_e4m3(CUtensorMap *tm, const void *ptr, int64_t rows, int64_t cols, uint32_t box_rows) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    cuuint32_t box[2] = {128u, box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int fp8_library_version(void) { return 100; }
+
+const char *fp8_status_string(int status) {
+    switch (status) {
+        case FP8_OK: return "FP8_OK";
+        case FP8_ERR_INVALID_ARG: return "FP8_ERR_INVALID_ARG: null pointer, bad size or bad enum";
+        case FP8_ERR_ALIGNMENT: return "FP8_ERR_ALIGNMENT: pointer not 16-byte aligned or K/N not a multiple of 16/8";
+        case FP8_ERR_UNSUPPORTED: return "FP8_ERR_UNSUPPORTED: valid request not implemented (e.g. out_dtype)";
+        case FP8_ERR_CUDA: return "FP8_ERR_CUDA: CUDA call or kernel launch failed";
+        case FP8_ERR_DEVICE: return "FP8_ERR_DEVICE: a kernel reported an error (bounded wait ran out)";
+        default: return "unknown fp8_status";
+    }
+}
+
+int fp8_describe_dispatch(int64_t M, int64_t N, int64_t K, int granularity) {
+    if (M < 0 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > kI32Max) return -1;
+    if (granularity < 0 || granularity > 3) return -1;
+    if (M == 0) return FP8_KERNEL_NONE;
+    return FP8_KERNEL_DECODE_SPLITK;
+}
+
+int fp8_decode_split_for_sms(int64_t M, int64_t N, int64_t K, int num_sms) {
+    if (fp8_describe_dispatch(M, N, K, 0) != FP8_KERNEL_DECODE_SPLITK || num_sms < 1) return -1;
+    return fp8k::plan_decode(M, N, K, num_sms).split;
+}
+
+int fp8_decode_split(int64_t M, int64_t N, int64_t K) {
+    DeviceState *st = nullptr;
+    if (fp8_describe_dispatch(M, N, K, 0) != FP8_KERNEL_DECODE_SPLITK) return -1;
+    if (device_state(&st) != FP8_OK) return -1;
+    return fp8k::plan_decode(M, N, K, st->num_sms).split;
+}
+
+fp8_status fp8_scaled_mm(const void *A, const void *B, const float *scale_a, const float *scale_b, int granularity,
+                         int out_dtype, int64_t M, int64_t N, int64_t K, void *out, void *stream) {
+    if (M < 0 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > kI32Max) return FP8_ERR_INVALID_ARG;
+    if (granularity < 0 || granularity > 3) return FP8_ERR_INVALID_ARG;
+    if (out_dtype != FP8_OUT_BF16) return FP8_ERR_UNSUPPORTED;
+    if (M == 0) return FP8_OK;
+    if (!A || !B || !scale_a || !scale_b || !out) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(out) || !aligned4(scale_a) || !aligned4(scale_b))
+        return FP8_ERR_ALIGNMENT;
+    if (K % 16 != 0 || N % 8 != 0) return FP8_ERR_ALIGNMENT;
+
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    const fp8k::DecodePlan plan = fp8k::plan_decode(M, N, K, st->num_sms);
+    CUtensorMap tw, ta;
+    if ((s = make_tmap_e4m3(&tw, B, N, K, fp8k::kDecodeRows)) != FP8_OK) return s;
+    if ((s = make_tmap_e4m3(&ta, A, M, K, static_cast<uint32_t>(plan.tok_pad))) != FP8_OK) return s;
+    return from_cuda(fp8k::launch_decode_gemm(tw, ta, scale_a, scale_b, granularity, M, N, K, out, st->err, plan,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+fp8_status rmsnorm_quant_fp8(const void *x, const void *gamma, float eps, const float *scale, void *out, int64_t M,
+                             int64_t K, void *stream) {
+    if (M < 0 || M > kI32Max || K < 1 || K > 65536) return FP8_ERR_INVALID_ARG;
+    if (M == 0) return FP8_OK;
+    if (!x || !gamma || !scale || !out) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(out) || !aligned4(scale)) return FP8_ERR_ALIGNMENT;
+    if (K % 16 != 0) return FP8_ERR_ALIGNMENT;
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    return from_cuda(
+        fp8k::launch_rmsnorm_quant(x, gamma, eps, scale, out, M, K, st->err, static_cast<cudaStream_t>(stream)));
+}
+
+fp8_status quant_fp8_per_token(const void *x, void *out, float *scale_out, int64_t M, int64_t K, void *stream) {
+    if (M < 0 || M > kI32Max || K < 1 || K > (int64_t(1) << 30)) return FP8_ERR_INVALID_ARG;
+    if (M == 0) return FP8_OK;
+    if (!x || !out || !scale_out) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || !aligned4(scale_out)) return FP8_ERR_ALIGNMENT;
+    if (K % 16 != 0) return FP8_ERR_ALIGNMENT;
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    return from_cuda(fp8k::launch_quant_per_token(x, out, scale_out, M, K, st->err, static_cast<cudaStream_t>(stream)));
+}
+
+fp8_status quant_fp8_static(const void *x, const float *scale, void *out, int64_t M, int64_t K, void *stream) {
+    if (M < 0 || M > kI32Max || K < 1 || K > kI32Max) return FP8_ERR_INVALID_ARG;
+    if (M == 0) return FP8_OK;
+    if (!x || !scale || !out) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || !aligned4(scale)) return FP8_ERR_ALIGNMENT;
+    if (K % 16 != 0) return FP8_ERR_ALIGNMENT;
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    return from_cuda(
+        fp8k::launch_quant_static(x, scale, out, M, K, st->err, static_cast<cudaStream_t>(stream), st->num_sms));
+}
+
+fp8_status fp8_set_device(int device) {
+    if (device < 0 || device >= kMaxDevices) return FP8_ERR_INVALID_ARG;
+    return cudaSetDevice(device) == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status fp8_get_device_error(void *stream, uint32_t *word) {
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8_ERR_CUDA;
+    uint32_t w = 0;
+    if (cudaMemcpy(&w, st->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return FP8_ERR_CUDA;
+    if (word) *word = w;
+    return w ? FP8_ERR_DEVICE : FP8_OK;
+}
+
+fp8_status fp8_clear_device_error(void) {
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    if (cudaMemset(st->err, 0, sizeof(uint32_t)) != cudaSuccess) return FP8_ERR_CUDA;
+    return cudaDeviceSynchronize() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+}  // extern "C"

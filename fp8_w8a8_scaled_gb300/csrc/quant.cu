@@ -1,0 +1,272 @@
+// quant.cu -- the activation producers of the FP8 W8A8 linear layer:
+//   * quant_fp8_static     q = e4m3(x / s)                      (QuantFp8Static)
+//   * quant_fp8_per_token  s_m = amax_m / 448, q = e4m3(x / s_m)
+//   * rmsnorm_quant_fp8    q = e4m3(bf16(x * r * gamma) / s), r = 1/sqrt(mean x^2 + eps)
+// Sources: "We emit F32 where vLLM emits bf16 ..." (vllm.cpp #417), section
+// "Ranked follow-ons from the same audit" (QuantFp8Static, the fused RMSNorm ->
+// fp8 quant, "quantise once"); "The FP8 tower's cuBLASLt default rests on a
+// false premise ..." (vllm.cpp #252), "What is owed" item 2 (per-tensor vs
+// per-token granularity).
+//
+// All three are HBM-bound streaming kernels (2 bytes read + 1 byte written per
+// element): 128-bit coalesced loads of 8 bf16, 64-bit stores of 8 E4M3 codes.
+// The per-row kernels keep the whole row in registers so x is read once.
+//
+// Rounding is pinned so the bytes match the CPU definition exactly: IEEE
+// binary32 division (__fdiv_rn, never a reciprocal multiply), separate
+// binary32 multiplies (no FMA), binary64 sum of squares / mean / sqrt /
+// reciprocal, round-to-nearest-even bf16, and the hardware's saturating
+// round-to-nearest-even E4M3 conversion (cvt.rn.satfinite.e4m3x2.f32).
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fp8k {
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two values -> two E4M3 codes, `a` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Eight bf16 (one 16-byte vector) divided by s -> eight E4M3 codes.
+__device__ __forceinline__ uint2 quant8(const uint4 v, float s) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = e4m3x2(__fdiv_rn(bf16_lo(w[i]), s), __fdiv_rn(bf16_hi(w[i]), s));
+    return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+}
+
+// max |x| over eight bf16; NaN entries are ignored (fmaxf semantics).
+__device__ __forceinline__ float absmax8(const uint4 v, float m) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m = fmaxf(m, __uint_as_float((w[i] << 16) & 0x7FFFFFFFu));
+        m = fmaxf(m, __uint_as_float(w[i] & 0x7FFF0000u));
+    }
+    return m;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+template <int T>
+__device__ __forceinline__ float block_max(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        v = lane < T / 32 ? red[lane] : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+        if (lane == 0) red[0] = v;
+    }
+    __syncthreads();
+    return red[0];
+}
+
+// Sum of the threads' binary64 partial sums.  (Every term is an exact square of
+// a bf16 value; the order only matters if the partial sums need more than 53
+// significand bits, which takes rows spanning ~40 binades.)
+template <int T>
+__device__ __forceinline__ double block_sum_f64(double v, double *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        v = lane < T / 32 ? red[lane] : 0.0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+        if (lane == 0) red[0] = v;
+    }
+    __syncthreads();
+    return red[0];
+}
+
+// ------------------------------------------------------------- static quant --
+
+__global__ void __launch_bounds__(256) quant_static_kernel(const uint4 *__restrict__ x, const float *__restrict__ scale,
+                                                           uint4 *__restrict__ out, int64_t n16) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const float s = __ldg(scale);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) {
+        const uint4 a = ld_stream(x + 2 * i);
+        const uint4 b = ld_stream(x + 2 * i + 1);
+        const uint2 qa = quant8(a, s), qb = quant8(b, s);
+        out[i] = make_uint4(qa.x, qa.y, qb.x, qb.y);
+    }
+}
+
+// ---------------------------------------------------------- per-token quant --
+
+// One CTA per row, the row held in registers: T threads x V vectors of 8.
+template <int T, int V>
+__global__ void __launch_bounds__(T) quant_per_token_kernel(const uint4 *__restrict__ x, uint2 *__restrict__ out,
+                                                            float *__restrict__ scale_out, int nvec) {
+    __shared__ float red[32];
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int64_t row = blockIdx.x;
+    const uint4 *xr = x + row * nvec;
+    uint2 *orow = out + row * nvec;
+    uint4 v[V];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = threadIdx.x + j * T;
+        if (idx < nvec) {
+            v[j] = ld_stream(xr + idx);
+            amax = absmax8(v[j], amax);
+        }
+    }
+    amax = block_max<T>(amax, red);
+    const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    if (threadIdx.x == 0) scale_out[row] = s;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = threadIdx.x + j * T;
+        if (idx < nvec) orow[idx] = quant8(v[j], s);
+    }
+}
+
+// Rows too long for registers: one pass for the max, one to quantise.
+__global__ void __launch_bounds__(512) quant_per_token_long_kernel(const uint4 *__restrict__ x,
+                                                                   uint2 *__restrict__ out,
+                                                                   float *__restrict__ scale_out, int64_t nvec) {
+    __shared__ float red[32];
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int64_t row = blockIdx.x;
+    const uint4 *xr = x + row * nvec;
+    uint2 *orow = out + row * nvec;
+    float amax = 0.0f;
+    for (int64_t i = threadIdx.x; i < nvec; i += 512) amax = absmax8(__ldg(xr + i), amax);
+    amax = block_max<512>(amax, red);
+    const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    if (threadIdx.x == 0) scale_out[row] = s;
+    for (int64_t i = threadIdx.x; i < nvec; i += 512) orow[i] = quant8(__ldg(xr + i), s);
+}
+
+// ---------------------------------------------------- fused RMSNorm -> quant --
+
+template <int T, int V>
+__global__ void __launch_bounds__(T) rmsnorm_quant_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gamma,
+                                                          float eps, const float *__restrict__ scale,
+                                                          uint2 *__restrict__ out, int nvec, int K) {
+    __shared__ double red[32];
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int64_t row = blockIdx.x;
+    const uint4 *xr = x + row * nvec;
+    uint2 *orow = out + row * nvec;
+    uint4 v[V];
+    double ss = 0.0;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = threadIdx.x + j * T;
+        if (idx < nvec) {
+            v[j] = ld_stream(xr + idx);
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const double a = static_cast<double>(bf16_lo(w[i]));
+                const double b = static_cast<double>(bf16_hi(w[i]));
+                ss = __dadd_rn(ss, __dmul_rn(a, a));
+                ss = __dadd_rn(ss, __dmul_rn(b, b));
+            }
+        }
+    }
+    ss = block_sum_f64<T>(ss, red);
+    const double mean = __ddiv_rn(ss, static_cast<double>(K));
+    const double denom = __dsqrt_rn(__dadd_rn(mean, static_cast<double>(eps)));
+    const float r = __double2float_rn(__ddiv_rn(1.0, denom));
+    const float s = __ldg(scale);
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = threadIdx.x + j * T;
+        if (idx < nvec) {
+            const uint4 g = __ldg(gamma + idx);
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+            uint32_t p[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float h0 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(bf16_lo(w[i]), r), bf16_lo(gw[i]))));
+                const float h1 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(bf16_hi(w[i]), r), bf16_hi(gw[i]))));
+                p[i] = e4m3x2(__fdiv_rn(h0, s), __fdiv_rn(h1, s));
+            }
+            orow[idx] = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+        }
+    }
+}
+
+template <int T, int V>
+cudaError_t launch_rows_pt(const void *x, void *out, float *scale_out, int64_t M, int64_t K, cudaStream_t stream) {
+    quant_per_token_kernel<T, V><<<static_cast<unsigned>(M), T, 0, stream>>>(
+        static_cast<const uint4 *>(x), static_cast<uint2 *>(out), scale_out, static_cast<int>(K / 8));
+    return cudaGetLastError();
+}
+
+template <int T, int V>
+cudaError_t launch_rows_rms(const void *x, const void *gamma, float eps, const float *scale, void *out, int64_t M,
+                            int64_t K, cudaStream_t stream) {
+    rmsnorm_quant_kernel<T, V><<<static_cast<unsigned>(M), T, 0, stream>>>(
+        static_cast<const uint4 *>(x), static_cast<const uint4 *>(gamma), eps, scale, static_cast<uint2 *>(out),
+        static_cast<int>(K / 8), static_cast<int>(K));
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quant_static(const void *x, const float *scale, void *out, int64_t M, int64_t K, uint32_t *err,
+                                cudaStream_t stream, int num_sms) {
+    (void)err;
+    const int64_t n16 = M * K / 16;
+    int64_t blocks = (n16 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    quant_static_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<const uint4 *>(x), scale,
+                                                                           static_cast<uint4 *>(out), n16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_per_token(const void *x, void *out, float *scale_out, int64_t M, int64_t K, uint32_t *err,
+                                   cudaStream_t stream) {
+    (void)err;
+    if (K <= 128 * 8 * 8) return launch_rows_pt<128, 8>(x, out, scale_out, M, K, stream);
+    if (K <= 256 * 16 * 8) return launch_rows_pt<256, 16>(x, out, scale_out, M, K, stream);
+    if (K <= 512 * 16 * 8) return launch_rows_pt<512, 16>(x, out, scale_out, M, K, stream);
+    quant_per_token_long_kernel<<<static_cast<unsigned>(M), 512, 0, stream>>>(
+        static_cast<const uint4 *>(x), static_cast<uint2 *>(out), scale_out, K / 8);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_quant(const void *x, const void *gamma, float eps, const float *scale, void *out,
+                                 int64_t M, int64_t K, uint32_t *err, cudaStream_t stream) {
+    (void)err;
+    if (K <= 128 * 8 * 8) return launch_rows_rms<128, 8>(x, gamma, eps, scale, out, M, K, stream);
+    if (K <= 256 * 16 * 8) return launch_rows_rms<256, 16>(x, gamma, eps, scale, out, M, K, stream);
+    return launch_rows_rms<512, 16>(x, gamma, eps, scale, out, M, K, stream);
+}
+
+}  // namespace fp8k

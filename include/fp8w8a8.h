@@ -1,0 +1,197 @@
+/*
+ * fp8w8a8.h -- C ABI of the GB300 (sm_103a) FP8 (E4M3) W8A8 scaled-GEMM library.
+ *
+ * The library computes the linear layer of an FP8 "W8A8" model:
+ *
+ *     y_bf16[m,n] = bf16( (sum_k A[m,k] * B[n,k]) * scale_a[.] * scale_b[.] )
+ *
+ * with A the E4M3 activations [M,K], B the E4M3 weights [N,K] (K contiguous,
+ * one row per output channel), per-tensor / per-output-channel / per-token
+ * scales and a bf16 output, plus the producers that quantise activations to
+ * E4M3: a fused RMSNorm -> static quant, a dynamic per-token quant and a plain
+ * static quant.
+ *
+ * Where each call comes from (page title, then section):
+ *   [P1] "The FP8 tower's cuBLASLt default rests on a false premise: vLLM selects
+ *        FlashInferFP8ScaledMMLinearKernel, not nvjet/cuBLASLt" (vllm.cpp #252)
+ *   [P2] "Qwen3.6 NVFP4 baselines (27B and 35B-A3B) must reach vLLM speed parity"
+ *        (vllm.cpp #213)
+ *   [P3] "We emit F32 where vLLM emits bf16 on the biggest prefill buffers (GDN
+ *        in_proj, attn gate, q/k/v) -- 2x traffic ..." (vllm.cpp #417)
+ *   [P4] "[Kernel] add Flashinfer cutedsl w4a16 linear" (vllm #53014), the
+ *        commit message that references it (Marlin large-M dispatch).
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
+ *     caller owns and allocates every buffer.  The library allocates no device
+ *     memory per call.
+ *   - Row-major layouts.  E4M3 is the OCP FP8 "E4M3" finite encoding
+ *     (torch.float8_e4m3fn): 1 byte, max 448, NaN = 0x7F/0xFF, no Inf.
+ *     bf16 is IEEE binary32's upper half.  Scales are IEEE binary32.
+ *   - Every call validates its arguments first and returns a status.  On any
+ *     error nothing is launched and no memory is written.  M == 0 is a no-op
+ *     that returns FP8_OK.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream), never synchronise the host, and read scales only from
+ *     device memory, so a sequence of calls can be captured in a CUDA graph.
+ *   - No exception crosses this boundary; the functions are thread-safe.
+ *   - Results are deterministic: the same inputs give the same bytes, run
+ *     after run (no floating-point atomics).
+ */
+#ifndef FP8W8A8_H_
+#define FP8W8A8_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8_OK = 0,
+    FP8_ERR_INVALID_ARG = 1,  /* null pointer, negative or too-large size, bad enum */
+    FP8_ERR_ALIGNMENT = 2,    /* pointer not 16-byte aligned, or K / N not a multiple of 16 / 8 */
+    FP8_ERR_UNSUPPORTED = 3,  /* a valid request this library does not implement (e.g. out_dtype) */
+    FP8_ERR_CUDA = 4,         /* a CUDA runtime / driver call or a kernel launch failed */
+    FP8_ERR_DEVICE = 5        /* a kernel reported an error through the device error word */
+} fp8_status;
+
+/* Which scale element multiplies output y[m,n] ([P1] "What is owed", item 2,
+ * names per-tensor, per-channel and per-token scaling). */
+typedef enum {
+    FP8_GRAN_PER_TENSOR = 0,         /* scale_a[1], scale_b[1] */
+    FP8_GRAN_PER_CHANNEL = 1,        /* scale_a[1], scale_b[N]: one scale per output channel */
+    FP8_GRAN_PER_TOKEN_CHANNEL = 2,  /* scale_a[M], scale_b[N] */
+    FP8_GRAN_PER_TOKEN = 3           /* scale_a[M], scale_b[1] */
+} fp8_granularity;
+
+/* Output dtype.  Only bf16: the pages' finding is that an F32 GEMM output
+ * doubles the traffic on the largest activation buffers ([P3] "FINDING 1 --
+ * F32-vs-bf16 output dtype on the fp8 path").  Anything else returns
+ * FP8_ERR_UNSUPPORTED. */
+typedef enum { FP8_OUT_BF16 = 0 } fp8_out_dtype;
+
+/* Kernel identifiers returned by fp8_describe_dispatch. */
+typedef enum {
+    FP8_KERNEL_NONE = 0,          /* M == 0: nothing is launched */
+    FP8_KERNEL_DECODE_SPLITK = 1, /* weight-streaming split-K kernel (small M) */
+    FP8_KERNEL_PREFILL = 2        /* persistent tensor-core tile kernel (large M) */
+} fp8_kernel_id;
+
+/* fp8_scaled_mm -- the FP8 W8A8 scaled GEMM.
+ *
+ * Source: [P1] "CORRECTION -- my headline claim was too strong": the FP8 linear
+ * runs bmm_fp8(a, b, scale_a, scale_b, out_dtype, ...); [P3] "FINDING 1": the
+ * output is the model dtype (bf16), not F32; [P1] "The real finding: shape
+ * and fusion, not library" and [P2] "Lever 2": a merged QKV or gate|up
+ * projection is one call over the row-concatenated weight (and its
+ * concatenated per-channel scales); [P2] "Root-cause theme", item 1: the
+ * weight is kept [N,K], not transposed to [K,N].
+ *
+ *   A        E4M3 [M,K] row-major, 16-byte aligned
+ *   B        E4M3 [N,K] row-major (K contiguous), 16-byte aligned
+ *   scale_a  f32, 1 or M elements by `granularity`
+ *   scale_b  f32, 1 or N elements by `granularity`
+ *   out      bf16 [M,N] row-major, 16-byte aligned, written in full
+ *   M, N, K  0 <= M, 1 <= N, 1 <= K, each below 2^31; K % 16 == 0, N % 8 == 0
+ *
+ * y[m,n] = bf16_rne( fp32(fp32(acc[m,n] * sa) * sb) ) with acc the fp32
+ * tensor-core accumulation of the exact E4M3 products.  Which kernel runs is a
+ * pure function of (M, N, K, granularity), see fp8_describe_dispatch, so a
+ * captured CUDA graph replays the same kernel the eager call would run.
+ * Errors: FP8_ERR_INVALID_ARG, FP8_ERR_ALIGNMENT, FP8_ERR_UNSUPPORTED,
+ * FP8_ERR_CUDA. */
+fp8_status fp8_scaled_mm(const void *A, const void *B, const float *scale_a, const float *scale_b,
+                         int granularity, int out_dtype, int64_t M, int64_t N, int64_t K, void *out,
+                         void *stream);
+
+/* rmsnorm_quant_fp8 -- fused RMSNorm -> static per-tensor E4M3 quantisation,
+ * one pass ("quantise once" per layer).
+ *
+ * Source: [P3] "Ranked follow-ons from the same audit", third bullet: a fused
+ * RMSNorm -> fp8 quant that is byte-exact with the unfused path; [P2] "The GDN
+ * fp8 merge predicate FIRES": the fused producer requires the consumers to share
+ * one bitwise-equal activation input_scale, which is why it takes one scale.
+ *
+ *   x        bf16 [M,K] row-major, 16-byte aligned
+ *   gamma    bf16 [K], 16-byte aligned
+ *   eps      added to mean(x^2) inside the square root
+ *   scale    f32 [1] (device): the static activation scale s (x ~= dec(q) * s)
+ *   out      E4M3 [M,K], 16-byte aligned
+ *   K % 16 == 0, 1 <= K <= 65536
+ *
+ * Per row: ss = sum x^2 in binary64; r = fp32(1 / sqrt(ss/K + eps)) in
+ * binary64; h = bf16_rne((x * r) * gamma) in binary32; q = e4m3_rne_sat(h / s)
+ * with an IEEE binary32 division.  The bytes equal "RMSNorm to bf16, then
+ * quant_fp8_static" exactly. */
+fp8_status rmsnorm_quant_fp8(const void *x, const void *gamma, float eps, const float *scale, void *out,
+                             int64_t M, int64_t K, void *stream);
+
+/* quant_fp8_per_token -- dynamic per-token E4M3 quantisation.
+ *
+ * Source: [P1] "What is owed", item 2 (per-token scaling granularity and where
+ * the activation quantisation happens).
+ *
+ *   x          bf16 [M,K] row-major, 16-byte aligned
+ *   out        E4M3 [M,K], 16-byte aligned
+ *   scale_out  f32 [M]: s_m = amax_m / 448 in binary32 (1.0 for an all-zero
+ *              row); q = e4m3_rne_sat(x / s_m).  NaN entries do not take part
+ *              in the max.
+ *   K % 16 == 0, K <= 2^30.  Applied to a weight [N,K] this is per-output-
+ *   channel weight quantisation; applied to a tensor viewed as one row it is
+ *   per-tensor quantisation with s = amax/448. */
+fp8_status quant_fp8_per_token(const void *x, void *out, float *scale_out, int64_t M, int64_t K,
+                               void *stream);
+
+/* quant_fp8_static -- static per-tensor E4M3 quantisation, q = e4m3_rne_sat(x / s).
+ *
+ * Source: [P3] "Ranked follow-ons from the same audit" (QuantFp8Static).
+ *
+ *   x      bf16 [M,K], 16-byte aligned;  scale f32 [1] (device);
+ *   out    E4M3 [M,K], 16-byte aligned;  K % 16 == 0. */
+fp8_status quant_fp8_static(const void *x, const float *scale, void *out, int64_t M, int64_t K,
+                            void *stream);
+
+/* Human-readable name of a status code (a static string; never NULL). */
+const char *fp8_status_string(int status);
+
+/* Which kernel fp8_scaled_mm runs for this problem (an fp8_kernel_id), or -1
+ * for arguments fp8_scaled_mm would reject.  Host-only, pure: it reads no
+ * device state, so a caller can assert the kernel before capturing a graph.
+ * Source: [P4] commit message: the M-vs-threshold branch is a pure function
+ * of M so that a graph captured at a padded M freezes the branch eager
+ * execution would take. */
+int fp8_describe_dispatch(int64_t M, int64_t N, int64_t K, int granularity);
+
+/* Split-K factor the decode kernel uses for this shape on the current device
+ * (number of CTAs that share one output tile's K range), or -1 if the shape
+ * does not go to the decode kernel.  Host-only. */
+int fp8_decode_split(int64_t M, int64_t N, int64_t K);
+
+/* The same choice for a device with `num_sms` streaming multiprocessors; pure
+ * and host-only (usable without a GPU). */
+int fp8_decode_split_for_sms(int64_t M, int64_t N, int64_t K, int num_sms);
+
+/* Device error word.  Kernels never trap: a bounded wait that runs out sets a
+ * bit here and the kernel returns early.  fp8_get_device_error synchronises
+ * `stream`, copies the word for the current device into *word (host pointer,
+ * may be NULL) and returns FP8_ERR_DEVICE if it is non-zero.  Not for the hot
+ * path.  fp8_clear_device_error zeroes the word (synchronously). */
+fp8_status fp8_get_device_error(void *stream, uint32_t *word);
+fp8_status fp8_clear_device_error(void);
+
+/* Makes `device` the current device of this library's CUDA runtime for the
+ * calling thread (the library links its own copy of the runtime, so a host
+ * program that switches devices through another runtime tells it here).
+ * Returns FP8_ERR_INVALID_ARG for a negative index, FP8_ERR_CUDA if the
+ * runtime refuses the device. */
+fp8_status fp8_set_device(int device);
+
+/* Library version as an integer (major * 10000 + minor * 100 + patch). */
+int fp8_library_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8W8A8_H_ */

@@ -290,11 +290,20 @@ static void build_lut(void) {
     }
 }
 
+/* Each thread owns a contiguous range of output columns n (all rows m), so
+ * that single-row (decode) problems use every thread too. */
+static void col_range(const gemm_job *j, int64_t *n0, int64_t *n1) {
+    *n0 = j->N * j->tid / j->nthreads;
+    *n1 = j->N * (j->tid + 1) / j->nthreads;
+}
+
 static void *gemm_f64_worker(void *p) {
     gemm_job *j = (gemm_job *)p;
-    for (int64_t m = j->tid; m < j->M; m += j->nthreads) {
+    int64_t n0, n1;
+    col_range(j, &n0, &n1);
+    for (int64_t m = 0; m < j->M; ++m) {
         const uint8_t *a = j->A + m * j->K;
-        for (int64_t n = 0; n < j->N; ++n) {
+        for (int64_t n = n0; n < n1; ++n) {
             const uint8_t *b = j->B + n * j->K;
             double s = 0.0;
             for (int64_t k = 0; k < j->K; ++k) s += g_lut[a[k]] * g_lut[b[k]];
@@ -306,9 +315,11 @@ static void *gemm_f64_worker(void *p) {
 
 static void *gemm_i64_worker(void *p) {
     gemm_job *j = (gemm_job *)p;
-    for (int64_t m = j->tid; m < j->M; m += j->nthreads) {
+    int64_t n0, n1;
+    col_range(j, &n0, &n1);
+    for (int64_t m = 0; m < j->M; ++m) {
         const uint8_t *a = j->A + m * j->K;
-        for (int64_t n = 0; n < j->N; ++n) {
+        for (int64_t n = n0; n < n1; ++n) {
             const uint8_t *b = j->B + n * j->K;
             int64_t s = 0;
             for (int64_t k = 0; k < j->K; ++k) s += g_lut_i[a[k]] * g_lut_i[b[k]];

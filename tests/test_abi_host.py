@@ -1,0 +1,126 @@
+"""Host-side tests of the C ABI: the library loads without a GPU, exports every
+function the header declares, and rejects bad arguments with the documented
+status codes before touching any device state (so these run on CPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8w8a8.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from fp8_w8a8_scaled_gb300 import build as b
+    b.build()
+    import fp8_w8a8_scaled_gb300 as f
+    return f.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_abi():
+    names = _declared_functions()
+    for want in ("fp8_scaled_mm", "rmsnorm_quant_fp8", "quant_fp8_per_token", "quant_fp8_static",
+                 "fp8_status_string", "fp8_describe_dispatch", "fp8_get_device_error"):
+        assert want in names, names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    import fp8_w8a8_scaled_gb300 as f
+    for code in range(6):
+        s = f.status_string(code)
+        assert s.startswith("FP8_")
+    assert f.status_string(99) == "unknown fp8_status"
+
+
+P = ctypes.c_void_p
+GOOD = P(0x10000)          # 16-byte aligned fake device addresses: validation never dereferences them
+GOOD2 = P(0x20000)
+GOOD3 = P(0x30000)
+SC = P(0x40000)
+SC2 = P(0x50000)
+
+
+def mm(L, A=GOOD, B=GOOD2, sa=SC, sb=SC2, gran=0, od=0, M=4, N=64, K=64, out=GOOD3):
+    return L.fp8_scaled_mm(A, B, sa, sb, gran, od, M, N, K, out, None)
+
+
+def test_scaled_mm_validation(L):
+    assert mm(L, M=0) == 0                                     # no-op, nothing launched
+    assert mm(L, M=0, A=None, out=None) == 0                   # pointers are not needed for M == 0
+    assert mm(L, M=-1) == 1
+    assert mm(L, N=0) == 1
+    assert mm(L, K=0) == 1
+    assert mm(L, M=2 ** 31) == 1
+    assert mm(L, gran=4) == 1
+    assert mm(L, gran=-1) == 1
+    assert mm(L, od=1) == 3                                    # only bf16 output
+    assert mm(L, A=None) == 1
+    assert mm(L, B=None) == 1
+    assert mm(L, sa=None) == 1
+    assert mm(L, sb=None) == 1
+    assert mm(L, out=None) == 1
+    assert mm(L, A=P(0x10008)) == 2
+    assert mm(L, B=P(0x20001)) == 2
+    assert mm(L, out=P(0x30004)) == 2
+    assert mm(L, sa=P(0x40002)) == 2
+    assert mm(L, K=72) == 2                                    # K % 16
+    assert mm(L, N=68) == 2                                    # N % 8
+
+
+def test_quantiser_validation(L):
+    assert L.quant_fp8_static(GOOD, SC, GOOD2, 0, 64, None) == 0
+    assert L.quant_fp8_static(None, SC, GOOD2, 4, 64, None) == 1
+    assert L.quant_fp8_static(GOOD, None, GOOD2, 4, 64, None) == 1
+    assert L.quant_fp8_static(GOOD, SC, GOOD2, 4, 40, None) == 2
+    assert L.quant_fp8_static(P(0x10002), SC, GOOD2, 4, 64, None) == 2
+    assert L.quant_fp8_static(GOOD, SC, GOOD2, -3, 64, None) == 1
+    assert L.quant_fp8_per_token(GOOD, GOOD2, SC, 0, 64, None) == 0
+    assert L.quant_fp8_per_token(GOOD, GOOD2, None, 4, 64, None) == 1
+    assert L.quant_fp8_per_token(GOOD, P(0x20008), SC, 4, 64, None) == 2
+    assert L.quant_fp8_per_token(GOOD, GOOD2, SC, 4, 0, None) == 1
+    assert L.quant_fp8_per_token(GOOD, GOOD2, SC, 4, 2 ** 31, None) == 1
+    assert L.rmsnorm_quant_fp8(GOOD, GOOD2, ctypes.c_float(1e-6), SC, GOOD3, 0, 64, None) == 0
+    assert L.rmsnorm_quant_fp8(GOOD, None, ctypes.c_float(1e-6), SC, GOOD3, 4, 64, None) == 1
+    assert L.rmsnorm_quant_fp8(GOOD, GOOD2, ctypes.c_float(1e-6), SC, GOOD3, 4, 65536 + 16, None) == 1
+    assert L.rmsnorm_quant_fp8(GOOD, P(0x20004), ctypes.c_float(1e-6), SC, GOOD3, 4, 64, None) == 2
+    assert L.rmsnorm_quant_fp8(GOOD, GOOD2, ctypes.c_float(1e-6), SC, GOOD3, 4, 24, None) == 2
+
+
+def test_describe_dispatch_is_pure(L):
+    assert L.fp8_describe_dispatch(0, 64, 64, 0) == 0
+    assert L.fp8_describe_dispatch(-1, 64, 64, 0) == -1
+    assert L.fp8_describe_dispatch(4, 64, 64, 7) == -1
+    for M in (1, 2, 4, 8, 16, 32, 64):
+        assert L.fp8_describe_dispatch(M, 10240, 5120, 1) == 1
+    # the same question twice gives the same answer (no hidden state)
+    for M in (1, 33, 127, 128, 129, 2048, 8192):
+        assert L.fp8_describe_dispatch(M, 10240, 5120, 2) == L.fp8_describe_dispatch(M, 10240, 5120, 2)
+
+
+def test_decode_split_planner(L):
+    """The planner keeps the grid to one wave on a 152-SM part and splits K
+    into whole 128-wide blocks."""
+    f = L.fp8_decode_split_for_sms
+    for (M, N, K) in ((1, 10240, 5120), (32, 10240, 5120), (64, 34816, 5120), (8, 5120, 8192),
+                      (8, 5120, 17408), (4, 512, 256)):
+        s = f(M, N, K, 152)
+        assert 1 <= s <= 8
+        assert s <= (K + 127) // 128
+    assert f(1, 8, 16, 152) == 1          # one k-block cannot be split
+    assert f(0, 8, 16, 152) == -1
+    # pure: independent of call order
+    assert f(32, 10240, 5120, 152) == f(32, 10240, 5120, 152)

@@ -1,0 +1,247 @@
+"""GPU parity of the FP8 W8A8 scaled GEMM against the CPU oracle, on the
+workload shapes and on ragged random shapes, plus the invariants the method
+guarantees (determinism, graph == eager, merged == split, batch invariance)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from helpers import Guarded, check_gemm, host_bits, scale_product, to_dev_bf16, to_dev_e4m3, to_dev_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp8():
+    import fp8_w8a8_scaled_gb300 as f
+    f.clear_device_error()
+    yield f
+    assert f.get_device_error() == 0
+
+
+def run_mm(fp8, A, B, sa, sb, gran):
+    """A, B: device E4M3 tensors; returns the bf16 output bits, checking the
+    guard bands around the output."""
+    M, N = A.shape[0], B.shape[0]
+    buf = Guarded(M * N * 2)
+    out = buf.view(torch.bfloat16, (M, N))
+    fp8.fp8_scaled_mm(A, B, sa, sb, gran, out=out)
+    torch.cuda.synchronize()
+    assert buf.intact(), "write outside the output buffer"
+    return host_bits(out)
+
+
+def full_check(orc, A_codes, B_codes, sa, sb, gran, y_bits, what):
+    y64, _ = orc.scaled_mm(A_codes, B_codes, sa, sb, gran)
+    M, N = y64.shape
+    rows = np.arange(M)[:, None]
+    cols = np.arange(N)[None, :]
+    return check_gemm(y_bits, y64, scale_product(sa, sb, gran, rows, cols), A_codes.shape[1], what)
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def test_tiny_gemm_per_tensor(fp8, orc):
+    """M=4, K=256, N=512; A and B quantised per tensor with scale amax/448."""
+    d = workloads.tiny_gemm(seed=0)
+    qa, sa = fp8.quant_fp8_per_token(to_dev_bf16(d["x"]).view(1, -1))
+    qb, sb = fp8.quant_fp8_per_token(to_dev_bf16(d["w"]).view(1, -1))
+    wa, wsa = orc.quant_per_token(d["x"].reshape(1, -1))
+    wb, wsb = orc.quant_per_token(d["w"].reshape(1, -1))
+    assert np.array_equal(host_bits(qa).ravel(), wa.ravel()) and np.array_equal(host_bits(sa), wsa)
+    assert np.array_equal(host_bits(qb).ravel(), wb.ravel()) and np.array_equal(host_bits(sb), wsb)
+    A = qa.view(4, 256)
+    B = qb.view(512, 256)
+    y = run_mm(fp8, A, B, sa, sb, 0)
+    full_check(orc, wa.reshape(4, 256), wb.reshape(512, 256), wsa, wsb, 0, y, "tiny")
+
+
+@pytest.fixture(scope="module")
+def decode_fused_case(orc):
+    d = workloads.decode_fused(seed=0)
+    A_all = orc.rmsnorm_quant(d["x"], d["gamma"], d["eps"], float(d["s_a"]))
+    y64, _ = orc.scaled_mm(A_all, d["B"], d["s_a"], d["sb"], 1)
+    return d, A_all, y64
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32])
+def test_decode_fused_qkv(fp8, decode_fused_case, M):
+    """RMSNorm -> static quant -> merged QKV GEMM (N=10240, K=5120), per-channel
+    weight scales; rows 0..M-1 of one [32, 5120] batch."""
+    d, A_all, y64 = decode_fused_case
+    s_a = to_dev_f32(d["s_a"])
+    A = fp8.rmsnorm_quant_fp8(to_dev_bf16(d["x"][:M]), to_dev_bf16(d["gamma"]), d["eps"], s_a)
+    assert np.array_equal(host_bits(A), A_all[:M])
+    assert fp8.describe_dispatch(M, 10240, 5120, 1) == fp8.KERNEL_DECODE_SPLITK
+    y = run_mm(fp8, A, to_dev_e4m3(d["B"]), s_a, to_dev_f32(d["sb"]), 1)
+    sab = scale_product(d["s_a"], d["sb"], 1, np.arange(M)[:, None], np.arange(10240)[None, :])
+    worst, _ = check_gemm(y, y64[:M], sab, 5120, f"decode fused M={M}")
+    print(f"M={M} max err/bound {worst:.4f}")
+
+
+@pytest.fixture(scope="module")
+def gate_up_case(fp8, orc):
+    d = workloads.gate_up_decode(seed=0)
+    qb, sb = fp8.quant_fp8_per_token(to_dev_bf16(d["w"]))
+    wb, wsb = orc.quant_per_token(d["w"])
+    assert np.array_equal(host_bits(qb), wb) and np.array_equal(host_bits(sb), wsb)
+    s_a = float(d["s_a"])
+    qa = fp8.quant_fp8_static(to_dev_bf16(d["x"]), to_dev_f32(s_a))
+    wa = orc.quant_static(d["x"], s_a)
+    assert np.array_equal(host_bits(qa), wa)
+    y64, _ = orc.scaled_mm(wa, wb, [s_a], wsb, 1)
+    return d, qa, qb, sb, wsb, y64
+
+
+@pytest.mark.parametrize("M", [1, 8, 32, 64])
+def test_gate_up_decode(fp8, gate_up_case, M):
+    """Merged gate_up decode GEMM: N=34816, K=5120, per-channel weight scales,
+    per-tensor static activation scale."""
+    d, qa, qb, sb, wsb, y64 = gate_up_case
+    y = run_mm(fp8, qa[:M].contiguous(), qb, to_dev_f32(d["s_a"]), sb, 1)
+    sab = scale_product([d["s_a"]], wsb, 1, np.arange(M)[:, None], np.arange(34816)[None, :])
+    worst, _ = check_gemm(y, y64[:M], sab, 5120, f"gate_up M={M}")
+    print(f"M={M} max err/bound {worst:.4f}")
+
+
+@pytest.mark.parametrize("M,N", [(2048, 10240)])
+def test_prefill_shapes_sampled(fp8, orc, M, N):
+    """Prefill chunk: per-token activation quant (1% outliers x20), per-channel
+    weights; every output of 3 rows plus 20000 random outputs."""
+    d = workloads.prefill(seed=0, m=M, n=N)
+    qa, sa = fp8.quant_fp8_per_token(to_dev_bf16(d["x"]))
+    qb, sb = fp8.quant_fp8_per_token(to_dev_bf16(d["w"]))
+    wa, wsa = orc.quant_per_token(d["x"])
+    wb, wsb = orc.quant_per_token(d["w"])
+    assert np.array_equal(host_bits(qa), wa) and np.array_equal(host_bits(sa), wsa)
+    assert np.array_equal(host_bits(qb), wb) and np.array_equal(host_bits(sb), wsb)
+    y = run_mm(fp8, qa, qb, sa, sb, 2)
+    g = np.random.default_rng(7)
+    rows = np.concatenate([np.repeat([0, M // 2, M - 1], N), g.integers(0, M, 20000)])
+    cols = np.concatenate([np.tile(np.arange(N), 3), g.integers(0, N, 20000)])
+    y64 = orc.scaled_mm_points(wa, wb, wsa, wsb, 2, rows, cols)
+    worst, _ = check_gemm(y[rows, cols], y64, scale_product(wsa, wsb, 2, rows, cols), 5120, f"prefill {M}x{N}")
+    print(f"prefill {M}x{N} max err/bound {worst:.4f}")
+
+
+def test_down_projection_long_k(fp8, orc):
+    """The decode step's down projection: N=5120, K=17408 (random codes)."""
+    M, N, K = 8, 5120, 17408
+    c = workloads.random_gemm(50, M, N, K, 1)
+    y = run_mm(fp8, to_dev_e4m3(c["A"]), to_dev_e4m3(c["B"]), to_dev_f32(c["sa"]), to_dev_f32(c["sb"]), 1)
+    full_check(orc, c["A"], c["B"], c["sa"], c["sb"], 1, y, "down 8x5120x17408")
+
+
+# ----------------------------------------------------------------------------- ragged shapes
+
+SHAPES = [(1, 8, 16), (3, 136, 48), (17, 264, 400), (33, 1000, 272), (64, 1032, 2064), (65, 520, 1040),
+          (127, 392, 784), (129, 256, 512), (200, 8, 4096), (16, 128, 128), (31, 2056, 3088)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("gran", [0, 1, 2, 3])
+def test_random_shapes(fp8, orc, M, N, K, gran):
+    c = workloads.random_gemm(1000 + M * 7 + N * 3 + K + gran, M, N, K, gran)
+    y = run_mm(fp8, to_dev_e4m3(c["A"]), to_dev_e4m3(c["B"]), to_dev_f32(c["sa"]), to_dev_f32(c["sb"]), gran)
+    full_check(orc, c["A"], c["B"], c["sa"], c["sb"], gran, y, f"{M}x{N}x{K} gran {gran}")
+
+
+def test_extreme_codes(fp8, orc):
+    """All-448 operands (largest products), all-ones, and a mix with zeros."""
+    M, N, K = 5, 256, 1024
+    A = np.full((M, K), 0x7E, np.uint8)
+    B = np.full((N, K), 0x7E, np.uint8)
+    B[1::2] = 0xFE
+    A[1] = 0x38
+    A[2] = 0x00
+    y = run_mm(fp8, to_dev_e4m3(A), to_dev_e4m3(B), to_dev_f32([1e-3]), to_dev_f32([2e-3]), 0)
+    full_check(orc, A, B, [1e-3], [2e-3], 0, y, "extreme")
+
+
+def test_nan_code_propagates(fp8):
+    M, N, K = 2, 16, 256
+    A = np.full((M, K), 0x38, np.uint8)
+    B = np.full((N, K), 0x38, np.uint8)
+    B[3, 100] = 0x7F
+    y = run_mm(fp8, to_dev_e4m3(A), to_dev_e4m3(B), to_dev_f32([1.0]), to_dev_f32([1.0]), 0)
+    v = (y.astype(np.uint32) << 16).view(np.float32)
+    assert np.all(np.isnan(v[:, 3]))
+    assert np.all(v[:, [0, 1, 2, 4]] == 256.0)
+
+
+# ----------------------------------------------------------------------------- invariants
+
+def test_rerun_is_bitwise_identical(fp8):
+    for (M, N, K) in ((32, 10240, 5120), (3, 1000, 272)):
+        c = workloads.random_gemm(60, M, N, K, 2)
+        args = (to_dev_e4m3(c["A"]), to_dev_e4m3(c["B"]), to_dev_f32(c["sa"]), to_dev_f32(c["sb"]), 2)
+        y1 = run_mm(fp8, *args)
+        y2 = run_mm(fp8, *args)
+        assert np.array_equal(y1, y2)
+
+
+def test_graph_replay_equals_eager(fp8):
+    M, N, K = 8, 10240, 5120
+    c = workloads.random_gemm(61, M, N, K, 1)
+    A, B = to_dev_e4m3(c["A"]), to_dev_e4m3(c["B"])
+    sa, sb = to_dev_f32(c["sa"]), to_dev_f32(c["sb"])
+    eager = run_mm(fp8, A, B, sa, sb, 1)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fp8.fp8_scaled_mm(A, B, sa, sb, 1, out=out)   # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fp8.fp8_scaled_mm(A, B, sa, sb, 1, out=out)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(out), eager)
+
+
+def test_merged_equals_split(fp8, orc):
+    """QKV as one GEMM over [Wq; Wk; Wv] against three GEMMs: within the bound
+    always, and bitwise when the kernel splits K the same way for all four."""
+    M, K = 8, 5120
+    d = workloads.decode_fused(seed=2)
+    B = d["B"]
+    A = orc.rmsnorm_quant(d["x"][:M], d["gamma"], d["eps"], float(d["s_a"]))
+    sa = to_dev_f32(d["s_a"])
+    Ad = to_dev_e4m3(A)
+    merged = run_mm(fp8, Ad, to_dev_e4m3(B), sa, to_dev_f32(d["sb"]), 1)
+    parts, lo = [], 0
+    for w in (workloads.Q_WIDTH, workloads.KV_WIDTH, workloads.KV_WIDTH):
+        parts.append(run_mm(fp8, Ad, to_dev_e4m3(B[lo:lo + w]), sa, to_dev_f32(d["sb"][lo:lo + w]), 1))
+        lo += w
+    split = np.concatenate(parts, axis=1)
+    same_k_split = len({fp8.decode_split(M, n, K) for n in (10240, 8192, 1024)}) == 1
+    if same_k_split:
+        assert np.array_equal(merged, split)
+    y64, _ = orc.scaled_mm(A, B, d["s_a"], d["sb"], 1)
+    sab = scale_product(d["s_a"], d["sb"], 1, np.arange(M)[:, None], np.arange(10240)[None, :])
+    check_gemm(merged, y64, sab, K, "merged")
+    check_gemm(split, y64, sab, K, "split")
+
+
+def test_batch_rows_independent(fp8):
+    """Row m of an M=16 call against the same row alone (M=1): the kernel
+    pads both to the same token tile and splits K the same way, so bitwise."""
+    N, K = 10240, 5120
+    c = workloads.random_gemm(62, 16, N, K, 1)
+    A = to_dev_e4m3(c["A"])
+    B = to_dev_e4m3(c["B"])
+    sa, sb = to_dev_f32(c["sa"]), to_dev_f32(c["sb"])
+    full = run_mm(fp8, A, B, sa, sb, 1)
+    for m in (0, 7, 15):
+        one = run_mm(fp8, A[m:m + 1].contiguous(), B, sa, sb, 1)
+        if fp8.decode_split(1, N, K) == fp8.decode_split(16, N, K):
+            assert np.array_equal(one[0], full[m])
+
+
+def test_m_zero_is_noop(fp8):
+    A = torch.empty((0, 64), dtype=torch.float8_e4m3fn, device="cuda")
+    B = torch.zeros((64, 64), dtype=torch.float8_e4m3fn, device="cuda")
+    out = fp8.fp8_scaled_mm(A, B, to_dev_f32([1.0]), to_dev_f32([1.0]), 0)
+    assert out.shape == (0, 64)

@@ -1,0 +1,161 @@
+"""GPU parity of the activation quantisers against the CPU oracle: the E4M3
+bytes and the per-token scales must be bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from helpers import Guarded, host_bits, to_dev_bf16, to_dev_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp8():
+    import fp8_w8a8_scaled_gb300 as f
+    f.clear_device_error()
+    yield f
+    assert f.get_device_error() == 0
+
+
+ALL_BF16 = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(4096, 16)
+NAN_MASK = ((ALL_BF16 & 0x7F80) == 0x7F80) & ((ALL_BF16 & 0x7F) != 0)
+
+
+@pytest.mark.parametrize("s", [1.0, 1 / 56, 0.37, 3.3e-3, 2.0 ** -10, 7.5, 1e-30, 1e30, 2.0 ** -130])
+def test_static_quant_every_bf16_value(fp8, orc, s):
+    """Every bf16 bit pattern through q = e4m3(x / s) for a sweep of scales."""
+    s = float(np.float32(s))
+    x = to_dev_bf16(ALL_BF16)
+    q = host_bits(fp8.quant_fp8_static(x, to_dev_f32(s)))
+    want = orc.quant_static(ALL_BF16, s)
+    ok = ~NAN_MASK
+    assert np.array_equal(q[ok], want[ok]), np.argwhere((q != want) & ok)[:10]
+    # NaN inputs: a NaN code (the oracle's reading is 0x7F; record what the hardware emits)
+    assert np.all((q[NAN_MASK] & 0x7F) == 0x7F)
+
+
+def test_static_quant_nan_encoding(fp8):
+    """The hardware conversion's NaN code for a positive and a negative NaN."""
+    x = np.zeros((1, 16), np.uint16)
+    x[0, 0] = 0x7FC0
+    x[0, 1] = 0xFFC0
+    q = host_bits(fp8.quant_fp8_static(to_dev_bf16(x), to_dev_f32(1.0)))
+    print("NaN codes:", hex(int(q[0, 0])), hex(int(q[0, 1])))
+    assert (q[0, 0] & 0x7F) == 0x7F and (q[0, 1] & 0x7F) == 0x7F
+
+
+def test_static_quant_large_and_guarded(fp8, orc):
+    g = workloads.rng(30)
+    x = workloads.bf16_normal(g, (64, 5120))
+    s = float(workloads.STATIC_INPUT_SCALE)
+    buf = Guarded(64 * 5120)
+    out = buf.view(torch.float8_e4m3fn, (64, 5120))
+    fp8.quant_fp8_static(to_dev_bf16(x), to_dev_f32(s), out=out)
+    assert np.array_equal(host_bits(out), orc.quant_static(x, s))
+    assert buf.intact()
+
+
+@pytest.mark.parametrize("M,K", [(1, 16), (3, 48), (7, 5120), (64, 5120), (33, 8192), (5, 8208),
+                                 (9, 17408), (2, 32768), (3, 40000), (2, 65536), (1, 65552), (1, 131072)])
+def test_per_token_shapes(fp8, orc, M, K):
+    """Covers every kernel variant: 128x8, 256x16 and 512x16 register-resident
+    rows and the two-pass path for rows beyond 65536."""
+    g = workloads.rng(31 + M + K)
+    x = workloads.bf16_normal_with_outliers(g, (M, K))
+    x[0, : min(K, 16)] = 0           # a partly-zero row
+    if M > 2:
+        x[2] = 0                     # an all-zero row: scale 1.0, codes 0
+    buf = Guarded(M * K)
+    out = buf.view(torch.float8_e4m3fn, (M, K))
+    q, s = fp8.quant_fp8_per_token(to_dev_bf16(x), out=out)
+    wq, ws = orc.quant_per_token(x)
+    assert np.array_equal(host_bits(s), ws)
+    assert np.array_equal(host_bits(q), wq)
+    assert buf.intact()
+
+
+def test_per_token_prefill_activations(fp8, orc):
+    """Prefill activations: M=2048, K=5120, N(0,1) with 1% outliers x20."""
+    d = workloads.prefill(seed=0, m=2048, n=16)
+    q, s = fp8.quant_fp8_per_token(to_dev_bf16(d["x"]))
+    wq, ws = orc.quant_per_token(d["x"])
+    assert np.array_equal(host_bits(s), ws)
+    assert np.array_equal(host_bits(q), wq)
+
+
+def test_per_channel_weight_quant_gate_up(fp8, orc):
+    """Per-output-channel weight quantisation of the merged gate_up weight
+    [34816, 5120] (quant_fp8_per_token applied to the weight rows)."""
+    d = workloads.gate_up_decode(seed=0)
+    q, s = fp8.quant_fp8_per_token(to_dev_bf16(d["w"]))
+    wq, ws = orc.quant_per_token(d["w"])
+    assert np.array_equal(host_bits(s), ws)
+    assert np.array_equal(host_bits(q), wq)
+
+
+def test_per_token_special_values(fp8, orc):
+    x = np.zeros((4, 32), np.uint16)
+    x[0, :4] = [0x7F80, 0x3F80, 0xBF80, 0x0001]   # +inf in the row: scale inf
+    x[1, :4] = [0x7FC0, 0x4000, 0xC100, 0x0000]   # NaN does not take part in the max
+    x[2, :2] = [0x0001, 0x8002]                   # subnormal-only row
+    x[3, :] = 0x8000                              # negative zeros
+    q, s = fp8.quant_fp8_per_token(to_dev_bf16(x))
+    wq, ws = orc.quant_per_token(x)
+    assert np.array_equal(host_bits(s), ws)
+    qh = host_bits(q)
+    nan_in = ((x & 0x7F80) == 0x7F80) & ((x & 0x7F) != 0)
+    inf_in = (x & 0x7FFF) == 0x7F80
+    ok = ~(nan_in | inf_in)
+    assert np.array_equal(qh[ok], wq[ok])
+    assert np.all((qh[~ok] & 0x7F) == 0x7F)   # inf/inf and NaN/s are NaN
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32])
+def test_rmsnorm_quant_decode_fused(fp8, orc, M):
+    """Decode fused path producer: rows 0..M-1 of x [32, 5120], gamma =
+    1 + N(0, 0.1), eps 1e-6, the static activation scale."""
+    d = workloads.decode_fused(seed=0)
+    x = d["x"][:M]
+    buf = Guarded(M * 5120)
+    out = buf.view(torch.float8_e4m3fn, (M, 5120))
+    q = fp8.rmsnorm_quant_fp8(to_dev_bf16(x), to_dev_bf16(d["gamma"]), d["eps"], to_dev_f32(d["s_a"]), out=out)
+    assert np.array_equal(host_bits(q), orc.rmsnorm_quant(x, d["gamma"], d["eps"], float(d["s_a"])))
+    assert buf.intact()
+
+
+@pytest.mark.parametrize("M,K,eps,s", [(32, 5120, 1e-6, 1 / 112), (5, 16, 1e-6, 1 / 56), (3, 17408, 1e-5, 0.02),
+                                       (2, 65536, 0.0, 0.01), (4, 8192, 1e-6, 1 / 56), (300, 5120, 1e-6, 1 / 56)])
+def test_rmsnorm_quant_shapes(fp8, orc, M, K, eps, s):
+    g = workloads.rng(40 + K)
+    x = workloads.bf16_normal(g, (M, K))
+    gamma = workloads.bf16_normal(g, (K,), mean=1.0, std=0.1)
+    x[0] = 0          # all-zero row: eps keeps the root finite (eps == 0 gives inf * 0 = NaN codes)
+    s = float(np.float32(s))
+    q = host_bits(fp8.rmsnorm_quant_fp8(to_dev_bf16(x), to_dev_bf16(gamma), eps, to_dev_f32(s)))
+    want = orc.rmsnorm_quant(x, gamma, eps, s)
+    if eps == 0.0:
+        assert np.all((q[0] & 0x7F) == 0x7F) and np.all((want[0] & 0x7F) == 0x7F)
+        q, want = q[1:], want[1:]
+    assert np.array_equal(q, want)
+
+
+def test_rmsnorm_fused_equals_unfused(fp8, orc):
+    """Fused norm-quant == static quant of the bf16 norm output, byte for byte
+    (the norm output comes from the oracle; the quant runs on the GPU)."""
+    d = workloads.decode_fused(seed=1)
+    h = orc.rmsnorm_bf16(d["x"], d["gamma"], d["eps"])
+    s = to_dev_f32(d["s_a"])
+    unfused = host_bits(fp8.quant_fp8_static(to_dev_bf16(h), s))
+    fused = host_bits(fp8.rmsnorm_quant_fp8(to_dev_bf16(d["x"]), to_dev_bf16(d["gamma"]), d["eps"], s))
+    assert np.array_equal(fused, unfused)
+
+
+def test_per_token_flattened_equals_static_amax(fp8):
+    """Per-token quant of a tensor viewed as one row == static quant with that
+    row's scale (the tiny workload's per-tensor quantisation)."""
+    d = workloads.tiny_gemm(seed=0)
+    x = to_dev_bf16(d["x"])
+    q1, s1 = fp8.quant_fp8_per_token(x.view(1, -1))
+    q2 = fp8.quant_fp8_static(x, s1)
+    assert np.array_equal(host_bits(q1).reshape(4, 256), host_bits(q2))
