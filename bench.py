@@ -34,7 +34,8 @@ METRIC = "fp8_scaled_mm HBM TB/s (M≤32) & FP8 TFLOPS (prefill), % of GB300 roo
 MS = workloads.DECODE_FUSED_MS
 N_QKV, K_HID = workloads.QKV_N, workloads.HIDDEN
 WORKLOAD = ("decode fused path: RMSNorm(eps 1e-6) -> static per-tensor E4M3 quant -> merged-QKV FP8 GEMM "
-            "N=10240 K=5120, per-channel weight scales, bf16 out; one pass per M in {1,2,4,8,16,32}")
+            "N=10240 K=5120, per-channel weight scales, bf16 out; one pass per M in {1,2,4,8,16,32}; "
+            "kernels chained with programmatic dependent launch, weights flagged static")
 INNER = 20  # steps captured per CUDA graph
 
 
@@ -137,12 +138,14 @@ class DecodeFusedStep:
         fp8 = self.fp8
         for i, m in enumerate(MS):
             fp8.rmsnorm_quant_fp8(self.x[:m], self.gamma, workloads.RMS_EPS, self.s_a, out=self.A[i])
-            fp8.fp8_scaled_mm(self.A[i], self.W[i], self.s_a, self.sb[i], fp8.GRAN_PER_CHANNEL, out=self.Y[i])
+            fp8.fp8_scaled_mm(self.A[i], self.W[i], self.s_a, self.sb[i], fp8.GRAN_PER_CHANNEL, out=self.Y[i],
+                              flags=fp8.FLAG_WEIGHTS_STATIC)
 
     def launch_gemms(self):
         fp8 = self.fp8
         for i, m in enumerate(MS):
-            fp8.fp8_scaled_mm(self.A[i], self.W[i], self.s_a, self.sb[i], fp8.GRAN_PER_CHANNEL, out=self.Y[i])
+            fp8.fp8_scaled_mm(self.A[i], self.W[i], self.s_a, self.sb[i], fp8.GRAN_PER_CHANNEL, out=self.Y[i],
+                              flags=fp8.FLAG_WEIGHTS_STATIC)
 
     def capture(self, fn, inner):
         torch = self.torch
@@ -259,7 +262,7 @@ def run_ours(args, rank, world, dist_barrier, dist_max):
         "config": {"workload": WORKLOAD, "bytes_per_step": step_bytes(), "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: six distinct 52.4 MB weights per step (315 MB)",
                    "graph": f"{INNER} steps per CUDA graph replay"},
-        "roofline": {"kernel": "decode_gemm_kernel (tcgen05 swap-AB split-K)", "bound": "hbm",
+        "roofline": {"kernel": "decode_gemm_kernel (tcgen05 swap-AB, persistent stream-K)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": None,
                      "bytes_per_launch": gbytes, "us_per_launch": round(per_launch_ms * 1e3, 3)},
@@ -318,6 +321,35 @@ def run_reference(args):
     }
 
 
+def run_profile_case(args):
+    """Small eager case for profilers: `--steps` launches of one GEMM shape
+    (plus the norm-quant that feeds it) rotating over three weight copies
+    (more than L2 in total), without CUDA graphs or timing claims."""
+    import torch
+    import fp8_w8a8_scaled_gb300 as fp8
+    M, N, K = (int(v) for v in args.profile.split(","))
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    g = workloads.rng(0)
+    x = torch.from_numpy(workloads.bf16_normal(g, (M, K)).view(np.int16)).view(torch.bfloat16).to(dev)
+    gamma = torch.from_numpy(workloads.bf16_normal(g, (K,), mean=1.0, std=0.1).view(np.int16)).view(
+        torch.bfloat16).to(dev)
+    s_a = torch.tensor([float(workloads.STATIC_INPUT_SCALE)], dtype=torch.float32, device=dev)
+    W = [workloads.device_e4m3_codes(torch, (N, K), seed=300 + i, device=dev).view(torch.float8_e4m3fn)
+         for i in range(3)]
+    sb = workloads.device_uniform_f32(torch, (N,), 0.5e-3, 2e-3, seed=400, device=dev)
+    A = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    for i in range(args.steps):
+        fp8.rmsnorm_quant_fp8(x, gamma, workloads.RMS_EPS, s_a, out=A)
+        fp8.fp8_scaled_mm(A, W[i % 3], s_a, sb, fp8.GRAN_PER_CHANNEL, out=Y)
+    torch.cuda.synchronize()
+    err = fp8.get_device_error()
+    print(json.dumps({"profile_case": [M, N, K], "launches": 2 * args.steps, "device_error": err}))
+    if err:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -327,7 +359,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="wall-time budget of the oracle CPU baseline")
     ap.add_argument("--ref-seconds", type=float, default=60.0, help="wall-time budget of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", metavar="M,N,K", help="run a small eager case for a profiler and exit")
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args)
+        return
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -32,6 +32,9 @@ GRAN_PER_TOKEN = 3
 
 OUT_BF16 = 0
 
+FLAG_WEIGHTS_STATIC = 1
+FLAG_NO_PDL = 2
+
 KERNEL_NONE = 0
 KERNEL_DECODE_SPLITK = 1
 KERNEL_PREFILL = 2
@@ -65,6 +68,8 @@ def lib():
     P, I64, I32, F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
     L.fp8_scaled_mm.argtypes = [P, P, P, P, I32, I32, I64, I64, I64, P, P]
     L.fp8_scaled_mm.restype = I32
+    L.fp8_scaled_mm_ex.argtypes = [P, P, P, P, I32, I32, I64, I64, I64, P, P, ctypes.c_uint]
+    L.fp8_scaled_mm_ex.restype = I32
     L.rmsnorm_quant_fp8.argtypes = [P, P, F32, P, P, I64, I64, P]
     L.rmsnorm_quant_fp8.restype = I32
     L.quant_fp8_per_token.argtypes = [P, P, P, I64, I64, P]
@@ -75,10 +80,10 @@ def lib():
     L.fp8_status_string.restype = ctypes.c_char_p
     L.fp8_describe_dispatch.argtypes = [I64, I64, I64, I32]
     L.fp8_describe_dispatch.restype = I32
-    L.fp8_decode_split.argtypes = [I64, I64, I64]
-    L.fp8_decode_split.restype = I32
-    L.fp8_decode_split_for_sms.argtypes = [I64, I64, I64, I32]
-    L.fp8_decode_split_for_sms.restype = I32
+    L.fp8_decode_ctas.argtypes = [I64, I64, I64]
+    L.fp8_decode_ctas.restype = I32
+    L.fp8_decode_ctas_for_sms.argtypes = [I64, I64, I64, I32]
+    L.fp8_decode_ctas_for_sms.restype = I32
     L.fp8_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     L.fp8_get_device_error.restype = I32
     L.fp8_clear_device_error.argtypes = []
@@ -129,11 +134,12 @@ def _need(t: torch.Tensor, name: str, dtypes, ndim=None):
 _FP8 = (E4M3, torch.uint8)
 
 
-def fp8_scaled_mm(A, B, scale_a, scale_b, granularity=None, out_dtype=OUT_BF16, out=None):
+def fp8_scaled_mm(A, B, scale_a, scale_b, granularity=None, out_dtype=OUT_BF16, out=None, flags=0):
     """y = bf16((A @ B.T) * scale_a * scale_b) for E4M3 A [M,K] and B [N,K].
 
     ``granularity`` defaults from the scale lengths: scale_a has 1 or M
-    elements, scale_b 1 or N."""
+    elements, scale_b 1 or N.  ``flags`` are the C ABI's fp8_flags
+    (FLAG_WEIGHTS_STATIC, FLAG_NO_PDL)."""
     _need(A, "A", _FP8, 2)
     _need(B, "B", _FP8, 2)
     _need(scale_a, "scale_a", (torch.float32,))
@@ -156,8 +162,8 @@ def fp8_scaled_mm(A, B, scale_a, scale_b, granularity=None, out_dtype=OUT_BF16, 
         _need(out, "out", (torch.bfloat16,), 2)
         if tuple(out.shape) != (M, N):
             raise ValueError(f"out must be [{M},{N}]")
-    _check(lib().fp8_scaled_mm(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), int(granularity), int(out_dtype),
-                               M, N, K, _ptr(out), _stream_of(A)), "fp8_scaled_mm")
+    _check(lib().fp8_scaled_mm_ex(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), int(granularity),
+                                  int(out_dtype), M, N, K, _ptr(out), _stream_of(A), int(flags)), "fp8_scaled_mm")
     return out
 
 
@@ -212,8 +218,8 @@ def describe_dispatch(M, N, K, granularity=0) -> int:
     return lib().fp8_describe_dispatch(M, N, K, granularity)
 
 
-def decode_split(M, N, K) -> int:
-    return lib().fp8_decode_split(M, N, K)
+def decode_ctas(M, N, K) -> int:
+    return lib().fp8_decode_ctas(M, N, K)
 
 
 def get_device_error(stream=None) -> int:

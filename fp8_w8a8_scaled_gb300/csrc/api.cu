@@ -22,10 +22,17 @@ __device__ uint32_t g_error_word;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kI32Max = 2147483647;
 
+// Scratch of the decode kernel, allocated once per device on the first GEMM
+// call: arrival counters (zero between launches) and partial-sum slots.
+constexpr size_t kWsCounters = size_t(1) << 20;
+
 struct DeviceState {
     bool ready = false;
     int num_sms = 0;
     uint32_t *err = nullptr;
+    uint32_t *counters = nullptr;
+    float *slots = nullptr;
+    size_t n_slots = 0;
 };
 
 std::mutex g_mu;
@@ -79,6 +86,34 @@ fp8_status make_tmap_e4m3(CUtensorMap *tm, const void *ptr, int64_t rows, int64_
 
 fp8_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
 
+// The decode kernel's workspace for this device: sized for the largest plan
+// (two CTAs per SM, 64-token tiles), allocated and zeroed on first use.
+fp8_status decode_workspace(DeviceState *st, const fp8k::DecodePlan &plan, fp8k::DecodeWorkspace *ws) {
+    if (fp8k::decode_counters_needed(plan) > kWsCounters) return FP8_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (st->counters == nullptr) {
+        const size_t n_slots = 2u * 2u * static_cast<size_t>(st->num_sms) * fp8k::kDecodeMaxTokens * fp8k::kDecodeRows;
+        void *c = nullptr, *sl = nullptr;
+        if (cudaMalloc(&c, kWsCounters * sizeof(uint32_t)) != cudaSuccess) return FP8_ERR_CUDA;
+        if (cudaMalloc(&sl, n_slots * sizeof(float)) != cudaSuccess) {
+            cudaFree(c);
+            return FP8_ERR_CUDA;
+        }
+        if (cudaMemset(c, 0, kWsCounters * sizeof(uint32_t)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+            cudaFree(c);
+            cudaFree(sl);
+            return FP8_ERR_CUDA;
+        }
+        st->counters = static_cast<uint32_t *>(c);
+        st->slots = static_cast<float *>(sl);
+        st->n_slots = n_slots;
+    }
+    if (fp8k::decode_slot_floats(plan) > st->n_slots) return FP8_ERR_UNSUPPORTED;
+    ws->counters = st->counters;
+    ws->slots = st->slots;
+    return FP8_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -104,22 +139,24 @@ int fp8_describe_dispatch(int64_t M, int64_t N, int64_t K, int granularity) {
     return FP8_KERNEL_DECODE_SPLITK;
 }
 
-int fp8_decode_split_for_sms(int64_t M, int64_t N, int64_t K, int num_sms) {
+int fp8_decode_ctas_for_sms(int64_t M, int64_t N, int64_t K, int num_sms) {
     if (fp8_describe_dispatch(M, N, K, 0) != FP8_KERNEL_DECODE_SPLITK || num_sms < 1) return -1;
-    return fp8k::plan_decode(M, N, K, num_sms).split;
+    return fp8k::plan_decode(M, N, K, num_sms).ctas;
 }
 
-int fp8_decode_split(int64_t M, int64_t N, int64_t K) {
+int fp8_decode_ctas(int64_t M, int64_t N, int64_t K) {
     DeviceState *st = nullptr;
     if (fp8_describe_dispatch(M, N, K, 0) != FP8_KERNEL_DECODE_SPLITK) return -1;
     if (device_state(&st) != FP8_OK) return -1;
-    return fp8k::plan_decode(M, N, K, st->num_sms).split;
+    return fp8k::plan_decode(M, N, K, st->num_sms).ctas;
 }
 
-fp8_status fp8_scaled_mm(const void *A, const void *B, const float *scale_a, const float *scale_b, int granularity,
-                         int out_dtype, int64_t M, int64_t N, int64_t K, void *out, void *stream) {
+fp8_status fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, const float *scale_b,
+                            int granularity, int out_dtype, int64_t M, int64_t N, int64_t K, void *out, void *stream,
+                            unsigned flags) {
     if (M < 0 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > kI32Max) return FP8_ERR_INVALID_ARG;
     if (granularity < 0 || granularity > 3) return FP8_ERR_INVALID_ARG;
+    if (flags & ~static_cast<unsigned>(FP8_FLAG_WEIGHTS_STATIC | FP8_FLAG_NO_PDL)) return FP8_ERR_INVALID_ARG;
     if (out_dtype != FP8_OUT_BF16) return FP8_ERR_UNSUPPORTED;
     if (M == 0) return FP8_OK;
     if (!A || !B || !scale_a || !scale_b || !out) return FP8_ERR_INVALID_ARG;
@@ -130,12 +167,22 @@ fp8_status fp8_scaled_mm(const void *A, const void *B, const float *scale_a, con
     DeviceState *st = nullptr;
     fp8_status s = device_state(&st);
     if (s != FP8_OK) return s;
+    fp8k::LaunchOpts opts;
+    opts.pdl = (flags & FP8_FLAG_NO_PDL) == 0;
+    opts.weights_static = (flags & FP8_FLAG_WEIGHTS_STATIC) != 0;
     const fp8k::DecodePlan plan = fp8k::plan_decode(M, N, K, st->num_sms);
+    fp8k::DecodeWorkspace ws;
+    if ((s = decode_workspace(st, plan, &ws)) != FP8_OK) return s;
     CUtensorMap tw, ta;
     if ((s = make_tmap_e4m3(&tw, B, N, K, fp8k::kDecodeRows)) != FP8_OK) return s;
     if ((s = make_tmap_e4m3(&ta, A, M, K, static_cast<uint32_t>(plan.tok_pad))) != FP8_OK) return s;
     return from_cuda(fp8k::launch_decode_gemm(tw, ta, scale_a, scale_b, granularity, M, N, K, out, st->err, plan,
-                                              static_cast<cudaStream_t>(stream)));
+                                              ws, opts, static_cast<cudaStream_t>(stream)));
+}
+
+fp8_status fp8_scaled_mm(const void *A, const void *B, const float *scale_a, const float *scale_b, int granularity,
+                         int out_dtype, int64_t M, int64_t N, int64_t K, void *out, void *stream) {
+    return fp8_scaled_mm_ex(A, B, scale_a, scale_b, granularity, out_dtype, M, N, K, out, stream, 0u);
 }
 
 fp8_status rmsnorm_quant_fp8(const void *x, const void *gamma, float eps, const float *scale, void *out, int64_t M,
@@ -149,7 +196,8 @@ fp8_status rmsnorm_quant_fp8(const void *x, const void *gamma, float eps, const 
     fp8_status s = device_state(&st);
     if (s != FP8_OK) return s;
     return from_cuda(
-        fp8k::launch_rmsnorm_quant(x, gamma, eps, scale, out, M, K, st->err, static_cast<cudaStream_t>(stream)));
+        fp8k::launch_rmsnorm_quant(x, gamma, eps, scale, out, M, K, st->err, static_cast<cudaStream_t>(stream),
+                                   fp8k::LaunchOpts{}));
 }
 
 fp8_status quant_fp8_per_token(const void *x, void *out, float *scale_out, int64_t M, int64_t K, void *stream) {
@@ -161,7 +209,8 @@ fp8_status quant_fp8_per_token(const void *x, void *out, float *scale_out, int64
     DeviceState *st = nullptr;
     fp8_status s = device_state(&st);
     if (s != FP8_OK) return s;
-    return from_cuda(fp8k::launch_quant_per_token(x, out, scale_out, M, K, st->err, static_cast<cudaStream_t>(stream)));
+    return from_cuda(fp8k::launch_quant_per_token(x, out, scale_out, M, K, st->err, static_cast<cudaStream_t>(stream),
+                                                  fp8k::LaunchOpts{}));
 }
 
 fp8_status quant_fp8_static(const void *x, const float *scale, void *out, int64_t M, int64_t K, void *stream) {
@@ -174,7 +223,8 @@ fp8_status quant_fp8_static(const void *x, const float *scale, void *out, int64_
     fp8_status s = device_state(&st);
     if (s != FP8_OK) return s;
     return from_cuda(
-        fp8k::launch_quant_static(x, scale, out, M, K, st->err, static_cast<cudaStream_t>(stream), st->num_sms));
+        fp8k::launch_quant_static(x, scale, out, M, K, st->err, static_cast<cudaStream_t>(stream), st->num_sms,
+                                  fp8k::LaunchOpts{}));
 }
 
 fp8_status fp8_set_device(int device) {
@@ -198,6 +248,8 @@ fp8_status fp8_clear_device_error(void) {
     fp8_status s = device_state(&st);
     if (s != FP8_OK) return s;
     if (cudaMemset(st->err, 0, sizeof(uint32_t)) != cudaSuccess) return FP8_ERR_CUDA;
+    // a kernel that gave up may have left arrival counters behind
+    if (st->counters && cudaMemset(st->counters, 0, kWsCounters * sizeof(uint32_t)) != cudaSuccess) return FP8_ERR_CUDA;
     return cudaDeviceSynchronize() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

@@ -10,23 +10,29 @@
 // split-K reduce kernel costs step time -- here it is fused).
 //
 // Design (GB300, sm_103a).  At decode M every weight byte is used M times, so
-// the kernel is bound by streaming B from HBM once.  Each CTA owns 128 weight
-// rows (output channels) and a contiguous slice of K:
-//   * warp 0 / lane 0 streams 128 x 128-byte weight boxes (and the matching
-//     token box of A) with TMA into a ring of shared-memory stages (128-byte
-//     swizzle), L2 evict-first for the once-read weights;
+// the kernel is bound by streaming B from HBM once, and every SM must stream
+// its equal share all the time.  The work is cut into units of one output tile
+// (128 weight rows x up to 64 tokens) by one 128-wide k-block; a persistent
+// grid of two CTAs per SM gives CTA c the contiguous units
+// [c*U/G, (c+1)*U/G) ("stream-K"), so all CTAs stream the same number of bytes
+// whatever the shape.  Inside a CTA:
+//   * warp 0 / lane 0 streams the units' 128 x 128-byte weight boxes and the
+//     matching token boxes with TMA into a ring of shared-memory stages
+//     (128-byte swizzle), L2 evict-first for the once-read weights;
 //   * warp 1 / lane 0 issues tcgen05.mma kind::f8f6f4 with the WEIGHTS as the
-//     128-row A operand and the tokens (padded to 16/32/64/128) as the N side
-//     ("swap-AB"), accumulating fp32 in TMEM, and frees each stage with
-//     tcgen05.commit;
-//   * the CTAs that split one tile's K range form a thread-block cluster; after
-//     the mainloop each dumps its TMEM partial into its own shared memory, and
-//     every CTA reduces a disjoint slice of the tile by reading the peers'
-//     partials over distributed shared memory in fixed rank order
-//     (deterministic, no atomics, no global workspace), applies the scales in
-//     binary32 and writes bf16.
-// The grid is one wave: the host picks the split so that all CTAs are
-// resident at once and every CTA streams the same number of bytes.
+//     128-row A operand and the tokens (padded to 16/32/64) as the N side
+//     ("swap-AB").  Each k-block is accumulated from zero into one of several
+//     TMEM buffers; tcgen05.commit frees the stage and hands the buffer on;
+//   * 4 or 8 drain warps read each k-block's fp32 partial out of TMEM
+//     while later k-blocks are multiplied, and fold it into a TwoSum (hi, lo)
+//     register pair: the sum over k-blocks is exact to ~2^-48 relative, so the
+//     only roundings left are the tensor core's inside one 128-wide k-block.
+// When a tile's K range ends inside the CTA, the drain warps either store the
+// tile (scales in binary32, then bf16) or, if other CTAs hold the rest of the
+// tile's K range, write their (hi, lo) pairs to a workspace slot and count
+// in on the tile's arrival counter; the CTA that arrives last sums all slots in
+// k order (so the result does not depend on arrival order), stores the tile
+// and resets the counter.  No CTA ever waits for another.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -41,36 +47,90 @@ constexpr uint32_t kWTileBytes = kDecodeRows * kBlockK;  // 16 KB of weights per
 
 template <int TOK>
 struct DecodeCfg {
+    static constexpr int kDrainGroups = TOK <= 16 ? 1 : 2;  // warpgroups that drain TMEM
+    static constexpr int kCols = TOK / kDrainGroups;               // token columns per drain thread
+    static constexpr int kDrainThreads = 128 * kDrainGroups;
+    static constexpr int kThreads = 64 + kDrainThreads;
+    // two CTAs of this kernel plus one of the next (programmatic launch) per SM
+    // two CTAs of this kernel plus one of the next (programmatic launch) per SM
+    // for the 16-token tile; two per SM for the larger tiles
+    static constexpr int kMinBlocks = TOK <= 16 ? 3 : 2;
+    static constexpr int kMaxRegs = (65536 / (kMinBlocks * kThreads)) / 8 * 8;
+    // TMEM accumulators in flight between the MMA and the drain (the MMA can
+    // run this many k-blocks ahead).  kBufs * TOK columns per CTA.
+    static constexpr int kBufs = TOK <= 16 ? 8 : 4;  // must match decode_tmem_bufs()
+    static constexpr uint32_t kTmemCols = kBufs * TOK < 32 ? 32 : kBufs * TOK;
     static constexpr uint32_t kATileBytes = TOK * kBlockK;
     static constexpr uint32_t kStageBytes = kWTileBytes + kATileBytes;
-    static constexpr uint32_t kTmemCols = TOK < 32 ? 32 : TOK;  // power of two >= 32
     static constexpr uint32_t kIdesc = idesc_e4m3_f32(kDecodeRows, TOK);
 };
 
+// Units [u0, u1) of CTA c out of U units over G CTAs, and the CTA owning unit u.
+__host__ __device__ __forceinline__ int64_t unit_begin(int64_t c, int64_t U, int64_t G) { return (c * U) / G; }
+__host__ __device__ __forceinline__ int64_t unit_owner(int64_t u, int64_t U, int64_t G) {
+    return ((u + 1) * G - 1) / U;
+}
+
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// The most CTAs that can share one tile's K range with two CTAs per SM on a
+// 152-SM part is ceil(kb_total / units per CTA) + 1; the planner keeps it at
+// or below this bound (a fixup reads one slot per sharing CTA at once).
+constexpr int kMaxFixupSegs = 8;
+
+struct DecodeArgs {
+    const float *scale_a;
+    const float *scale_b;
+    __nv_bfloat16 *out;
+    uint32_t *err;
+    uint32_t *counters;
+    float *slots;
+    int64_t units;
+    int gran, M, N, kb_total, n_tiles, stages, weights_static;
+};
+
+// A bounded wait that gives up at once when the CTA has already given up:
+// after one wait times out the kernel keeps its control flow (so barriers stay
+// matched) but stops waiting; the error word says the results are invalid.
+__device__ __forceinline__ bool cta_wait(uint32_t bar, uint32_t parity, uint32_t *err, uint32_t code,
+                                         volatile uint32_t *abort) {
+    if (*abort) return false;
+    if (mbar_wait(bar, parity, err, code)) return true;
+    *abort = 1u;
+    return false;
+}
+
 template <int TOK>
-__global__ void __launch_bounds__(128, 4)
+__global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCfg<TOK>::kMaxRegs)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
-                       const float *__restrict__ scale_a, const float *__restrict__ scale_b, int gran, int M, int N,
-                       int kb_total, int stages, __nv_bfloat16 *__restrict__ out, uint32_t *err) {
+                       const DecodeArgs args) {
     using Cfg = DecodeCfg<TOK>;
+    constexpr int NB = Cfg::kBufs;
+    constexpr int kSlotElems = TOK * kDecodeRows;  // fp32 entries of one partial slot
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ uint32_t s_tmem_base, s_issued, s_consumed;
+    __shared__ uint32_t s_tmem_base, s_issued, s_consumed, s_last;
+    __shared__ int64_t s_slot[kMaxFixupSegs];  // slot offsets (fp32 entries) of a tile's K-range parts
+    __shared__ volatile uint32_t s_abort;
 
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int stages = args.stages;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *const base_gen = smem_raw + (base - raw);
     const uint32_t bar0 = base + static_cast<uint32_t>(stages) * Cfg::kStageBytes;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (stages + s); };
-    const uint32_t accum_bar = bar0 + 16u * stages;
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * stages + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * stages + NB + b); };
+    const uint32_t final_bar = bar0 + 8u * (2 * stages + 2 * NB);
 
-    const uint32_t split = gridDim.x;
-    const uint32_t rank = cluster_ctarank();
-    const int n_tile = blockIdx.y, m_tile = blockIdx.z;
-    const int kb_begin = static_cast<int>((static_cast<int64_t>(rank) * kb_total) / split);
-    const int kb_end = static_cast<int>((static_cast<int64_t>(rank + 1) * kb_total) / split);
-    const int iters = kb_end - kb_begin;
+    const int64_t G = gridDim.x, U = args.units;
+    const int64_t me = blockIdx.x;
+    const int64_t u0 = unit_begin(me, U, G), u1 = unit_begin(me + 1, U, G);
+    const int iters = static_cast<int>(u1 - u0);
+    const int kbt = args.kb_total, n_tiles = args.n_tiles;
+    uint32_t *const err = args.err;
 
     if (tid == 0) {
         tma_prefetch_desc(&tmap_w);
@@ -79,10 +139,15 @@ __global__ void __launch_bounds__(128, 4)
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        mbar_init(accum_bar, 1);
+        for (int b = 0; b < NB; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4 * Cfg::kDrainGroups);  // one arrive per drain warp
+        }
+        mbar_init(final_bar, 1);
         fence_mbar_init();
         s_issued = 0;
         s_consumed = 0;
+        s_abort = 0;
     }
     if (warp == 1) tmem_alloc(smem_u32(&s_tmem_base), Cfg::kTmemCols);
     tc_fence_before();
@@ -94,107 +159,221 @@ __global__ void __launch_bounds__(128, 4)
         // ---------------------------------------------------------------- producer
         const uint64_t evict_first = policy_evict_first();
         int i = 0;
-        // Weights do not depend on earlier kernels in the stream; activations do.
+        // Weights that no earlier kernel in the stream writes may be fetched
+        // before the dependency wait; the tokens always wait.
+        const int pre = args.weights_static ? min(iters, stages) : 0;
+        for (; i < pre; ++i) {
+            const int64_t u = u0 + i, t = u / kbt;
+            const int kb = static_cast<int>(u - t * kbt), n_tile = static_cast<int>(t % n_tiles);
+            mbar_arrive_expect_tx(full_bar(i), Cfg::kStageBytes);
+            tma_load_2d_hint(base + static_cast<uint32_t>(i) * Cfg::kStageBytes, &tmap_w, full_bar(i), kb * kBlockK,
+                             n_tile * kDecodeRows, evict_first);
+        }
         grid_dependency_wait();
-        for (; i < iters; ++i) {
+        for (int j = 0; j < pre; ++j) {
+            const int64_t u = u0 + j, t = u / kbt;
+            const int kb = static_cast<int>(u - t * kbt), m_tile = static_cast<int>(t / n_tiles);
+            tma_load_2d(base + static_cast<uint32_t>(j) * Cfg::kStageBytes + kWTileBytes, &tmap_a, full_bar(j),
+                        kb * kBlockK, m_tile * TOK);
+        }
+        int t = static_cast<int>((u0 + i) / kbt), kb = static_cast<int>(u0 + i - static_cast<int64_t>(t) * kbt);
+        for (; i < iters; ++i, ++kb) {
+            if (kb == kbt) {
+                kb = 0;
+                ++t;
+            }
             const int s = i % stages;
             const uint32_t ph = static_cast<uint32_t>(i / stages) & 1u;
-            if (!mbar_wait(empty_bar(s), ph ^ 1u, err, kErrDecodeEmptyWait)) break;
+            if (!cta_wait(empty_bar(s), ph ^ 1u, err, kErrDecodeEmptyWait, &s_abort)) break;
+            const int n_tile = t % n_tiles, m_tile = t / n_tiles;
             const uint32_t stage = base + static_cast<uint32_t>(s) * Cfg::kStageBytes;
             mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
-            const int kx = (kb_begin + i) * kBlockK;
-            tma_load_2d_hint(stage, &tmap_w, full_bar(s), kx, n_tile * kDecodeRows, evict_first);
-            tma_load_2d(stage + kWTileBytes, &tmap_a, full_bar(s), kx, m_tile * TOK);
+            tma_load_2d_hint(stage, &tmap_w, full_bar(s), kb * kBlockK, n_tile * kDecodeRows, evict_first);
+            tma_load_2d(stage + kWTileBytes, &tmap_a, full_bar(s), kb * kBlockK, m_tile * TOK);
         }
         s_issued = static_cast<uint32_t>(i);
+        // Every load of this CTA is issued (and this grid's dependency was
+        // waited for above): the next kernel in the stream may now launch, so
+        // its prologue and weight prefetch overlap this CTA's drain and fixup.
+        grid_launch_dependents();
     } else if (warp == 1 && lane == 0) {
         // ---------------------------------------------------------------- MMA issuer
         int i = 0;
         for (; i < iters; ++i) {
             const int s = i % stages;
             const uint32_t ph = static_cast<uint32_t>(i / stages) & 1u;
-            if (!mbar_wait(full_bar(s), ph, err, kErrDecodeFullWait)) break;
+            const int b = i % NB;
+            const uint32_t tph = static_cast<uint32_t>(i / NB) & 1u;
+            if (!cta_wait(full_bar(s), ph, err, kErrDecodeFullWait, &s_abort)) break;
+            if (!cta_wait(tempty_bar(b), tph ^ 1u, err, kErrDecodeTmemEmptyWait, &s_abort)) break;
             tc_fence_after();
             const uint32_t w_addr = base + static_cast<uint32_t>(s) * Cfg::kStageBytes;
-            const uint32_t a_addr = w_addr + kWTileBytes;
+            const uint64_t dw = sw128_kmajor_desc(w_addr), da = sw128_kmajor_desc(w_addr + kWTileBytes);
+            const uint32_t d = tmem + static_cast<uint32_t>(b * TOK);
 #pragma unroll
-            for (int kk = 0; kk < kBlockK / 32; ++kk) {
-                mma_e4m3(tmem, sw128_kmajor_desc(w_addr + 32u * kk), sw128_kmajor_desc(a_addr + 32u * kk),
-                         Cfg::kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < kBlockK / 32; ++kk)  // +32 bytes along K = +2 in the address field
+                mma_e4m3(d, dw + 2u * kk, da + 2u * kk, Cfg::kIdesc, kk > 0 ? 1u : 0u);
             mma_commit(empty_bar(s));
+            mma_commit(tfull_bar(b));
         }
         s_consumed = static_cast<uint32_t>(i);
-        mma_commit(accum_bar);  // arrives once every MMA issued above has completed
+        mma_commit(final_bar);  // arrives when every MMA issued above has completed
+    } else if (warp >= 2) {
+        // ---------------------------------------------------------------- drain + tile output
+        grid_dependency_wait();  // outputs, scales and the workspace are touched below
+        const uint32_t quarter = warp & 3u;          // a warp reaches TMEM lanes 32*(warp%4) .. +31
+        const int row = static_cast<int>(quarter * 32u + lane);  // weight row within the tile
+        const int col0 = static_cast<int>((warp - 2) / 4) * Cfg::kCols;
+        const bool sa_vec = (args.gran == 2 || args.gran == 3);
+        const bool sb_vec = (args.gran == 1 || args.gran == 2);
+        const float sa0 = __ldg(args.scale_a), sb0 = __ldg(args.scale_b);
+        const int t_first_me = static_cast<int>(u0 / kbt);
+        float hi[Cfg::kCols], lo[Cfg::kCols];
+#pragma unroll
+        for (int c = 0; c < Cfg::kCols; ++c) hi[c] = lo[c] = 0.0f;
+
+        int t = static_cast<int>(u0 / kbt), kb = static_cast<int>(u0 - static_cast<int64_t>(t) * kbt);
+        for (int i = 0; i < iters; ++i, ++kb) {
+            if (kb == kbt) {
+                kb = 0;
+                ++t;
+            }
+            const int b = i % NB;
+            const uint32_t tph = static_cast<uint32_t>(i / NB) & 1u;
+            cta_wait(tfull_bar(b), tph, err, kErrDecodeTmemFullWait, &s_abort);
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((quarter * 32u) << 16) + static_cast<uint32_t>(b * TOK + col0);
+#pragma unroll
+            for (int c0 = 0; c0 < Cfg::kCols; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(taddr + static_cast<uint32_t>(c0), r);
+                tmem_ld_wait();
+                if (c0 + 16 >= Cfg::kCols) {  // last chunk read: the buffer is free for the MMA again
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(b));
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) two_sum_acc(hi[c0 + j], lo[c0 + j], __uint_as_float(r[j]));
+            }
+
+            if (kb != kbt - 1 && i != iters - 1) continue;
+
+            // ---- this CTA's part of tile t ends here
+            const int n_tile = t % n_tiles, m_tile = t / n_tiles;
+            const int n = n_tile * kDecodeRows + row;
+            const int m0 = m_tile * TOK;
+            const int mt = min(TOK, args.M - m0);
+            const int64_t tile_u0 = static_cast<int64_t>(t) * kbt;
+            const bool whole = (u0 <= tile_u0) && (kb == kbt - 1);
+            if (!whole) {
+                // this CTA's part of the tile, rounded once to binary32
+                float *mine = args.slots + static_cast<int64_t>(2 * me + (t == t_first_me ? 0 : 1)) * kSlotElems;
+#pragma unroll
+                for (int c = 0; c < Cfg::kCols; ++c)
+                    if (col0 + c < mt) mine[(col0 + c) * kDecodeRows + row] = __fadd_rn(hi[c], lo[c]);
+                __threadfence();
+                named_barrier_sync(1, Cfg::kDrainThreads);
+                if (tid == 64) {
+                    const int64_t c_first = unit_owner(tile_u0, U, G), c_last = unit_owner(tile_u0 + kbt - 1, U, G);
+                    const int64_t nseg = c_last - c_first + 1;
+                    const bool last = atomicAdd(args.counters + t, 1u) == static_cast<uint32_t>(nseg - 1);
+                    s_last = last ? static_cast<uint32_t>(nseg) : 0u;
+                    if (last) {
+                        for (int j = 0; j < kMaxFixupSegs && j < nseg; ++j) {
+                            const int64_t cc = c_first + j;
+                            s_slot[j] = (2 * cc + (t == unit_begin(cc, U, G) / kbt ? 0 : 1)) * kSlotElems;
+                        }
+                    }
+                }
+                named_barrier_sync(1, Cfg::kDrainThreads);
+                if (s_last != 0u) {
+                    // Last arrival: sum the tile over its K range in k order (this
+                    // CTA's own part is read back from its slot like the others).
+                    // The drain threads switch to a flat ownership of the tile's
+                    // valid entries, four per thread per round, so that every slot
+                    // load of a round is in flight at once.
+                    __threadfence();
+                    int nseg = static_cast<int>(s_last);
+                    if (nseg > kMaxFixupSegs) {  // the planner keeps this from happening
+                        if (tid == 64) atomicOr(err, kErrDecodeFixup);
+                        nseg = kMaxFixupSegs;
+                    }
+                    const int entries = mt * kDecodeRows;  // [col][row], valid token columns only
+                    const int dt = static_cast<int>(tid) - 64;
+                    for (int e0 = 4 * dt; e0 < entries; e0 += 4 * Cfg::kDrainThreads) {
+                        float4 v[kMaxFixupSegs];
+#pragma unroll
+                        for (int j = 0; j < kMaxFixupSegs; ++j)
+                            if (j < nseg) v[j] = __ldcg(reinterpret_cast<const float4 *>(args.slots + s_slot[j] + e0));
+                        float h[4] = {0.0f, 0.0f, 0.0f, 0.0f}, l[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                        for (int j = 0; j < kMaxFixupSegs; ++j) {
+                            if (j < nseg) {
+                                two_sum_acc(h[0], l[0], v[j].x);
+                                two_sum_acc(h[1], l[1], v[j].y);
+                                two_sum_acc(h[2], l[2], v[j].z);
+                                two_sum_acc(h[3], l[3], v[j].w);
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int e = e0 + q;
+                            const int m = e / kDecodeRows, nn = n_tile * kDecodeRows + (e % kDecodeRows);
+                            if (e < entries && nn < args.N) {
+                                const float sa = sa_vec ? __ldg(args.scale_a + m0 + m) : sa0;
+                                const float sb = sb_vec ? __ldg(args.scale_b + nn) : sb0;
+                                args.out[static_cast<int64_t>(m0 + m) * args.N + nn] =
+                                    __float2bfloat16_rn(__fmul_rn(__fmul_rn(__fadd_rn(h[q], l[q]), sa), sb));
+                            }
+                        }
+                    }
+                    if (tid == 64) args.counters[t] = 0u;  // ready for the next launch
+                }
+            }
+            if (whole && n < args.N) {
+#pragma unroll
+                for (int c = 0; c < Cfg::kCols; ++c) {
+                    const int m = col0 + c;
+                    if (m < mt) {
+                        const float acc = __fadd_rn(hi[c], lo[c]);
+                        const float sa = sa_vec ? __ldg(args.scale_a + m0 + m) : sa0;
+                        const float sb = sb_vec ? __ldg(args.scale_b + n) : sb0;
+                        args.out[static_cast<int64_t>(m0 + m) * args.N + n] =
+                            __float2bfloat16_rn(__fmul_rn(__fmul_rn(acc, sa), sb));
+                    }
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < Cfg::kCols; ++c) hi[c] = lo[c] = 0.0f;
+        }
     }
     __syncwarp();
+    grid_dependency_wait();
+    // (The producer thread triggered the dependent launch after its last load;
+    // a grid only triggers after its own dependency wait, so at most one
+    // dependent grid is ever waiting.)
     grid_launch_dependents();
-    grid_dependency_wait();  // the scales may come from the previous kernel in the stream
     __syncthreads();
 
-    // ------------------------------------------------------------------ epilogue
-    const uint32_t issued = s_issued, consumed = s_consumed;
-    const bool acc_ok = mbar_wait(accum_bar, 0, err, kErrDecodeAccumWait);
-    tc_fence_after();
     if (tid == 0) {
         // Loads issued but never consumed (only after a timeout): let them land
-        // before the stage memory is reused.
+        // before the CTA exits.
+        const uint32_t issued = s_issued, consumed = s_consumed;
         for (uint32_t i = consumed; i < issued; ++i)
             mbar_wait(full_bar(static_cast<int>(i % stages)), (i / stages) & 1u, err, kErrDecodeFullWait);
     }
-    __syncthreads();
-
-    float *part = reinterpret_cast<float *>(base_gen);  // [TOK][128] fp32, reuses the stage ring
-    // CTA-uniform, since the TMEM loads below are warp-collective (.sync.aligned)
-    const bool have = __syncthreads_and(acc_ok) && iters > 0 && consumed == static_cast<uint32_t>(iters);
-    if (have) {
-#pragma unroll 1
-        for (int c0 = 0; c0 < TOK; c0 += 16) {
-            uint32_t r[16];
-            tmem_ld16(tmem + ((warp * 32u) << 16) + static_cast<uint32_t>(c0), r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) part[(c0 + j) * kDecodeRows + tid] = __uint_as_float(r[j]);
-        }
-    } else {
-        for (int c = 0; c < TOK; ++c) part[c * kDecodeRows + tid] = 0.0f;
-    }
-    tc_fence_before();
-    cluster_sync();  // every partial of the tile is now visible to the whole cluster
-
-    const int rows_per = (kDecodeRows + static_cast<int>(split) - 1) / static_cast<int>(split);
-    const int r0 = static_cast<int>(rank) * rows_per;
-    const int r1 = min(kDecodeRows, r0 + rows_per);
-    const int nrows = max(0, r1 - r0);
-    const int m0 = m_tile * TOK;
-    const int mt = min(TOK, M - m0);
-    const uint32_t part_addr = smem_u32(part);
-    const bool sa_vec = (gran == 2 || gran == 3);
-    const bool sb_vec = (gran == 1 || gran == 2);
-    const float sa0 = __ldg(scale_a), sb0 = __ldg(scale_b);
-    for (int e = tid; e < nrows * mt; e += 128) {
-        const int nl = r0 + e % nrows;
-        const int m = e / nrows;
-        const int n = n_tile * kDecodeRows + nl;
-        if (n >= N) continue;
-        const uint32_t off = part_addr + 4u * static_cast<uint32_t>(m * kDecodeRows + nl);
-        float acc = 0.0f;
-        for (uint32_t src = 0; src < split; ++src) acc = __fadd_rn(acc, ld_cluster_f32(map_to_rank(off, src)));
-        const float sa = sa_vec ? __ldg(scale_a + m0 + m) : sa0;
-        const float sb = sb_vec ? __ldg(scale_b + n) : sb0;
-        out[static_cast<int64_t>(m0 + m) * N + n] = __float2bfloat16_rn(__fmul_rn(__fmul_rn(acc, sa), sb));
-    }
-    cluster_sync();  // peers are done reading this CTA's partial
-
     if (warp == 1) {
+        mbar_wait(final_bar, 0, err, kErrDecodeAccumWait);  // every MMA has completed
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::kTmemCols);
     }
 }
 
 template <int TOK>
-cudaError_t launch_tok(const CUtensorMap &tw, const CUtensorMap &ta, const float *sa, const float *sb, int gran,
-                       int64_t M, int64_t N, void *out, uint32_t *err, const DecodePlan &p, cudaStream_t stream) {
+cudaError_t launch_tok(const CUtensorMap &tw, const CUtensorMap &ta, const DecodeArgs &a, const DecodePlan &p,
+                       const LaunchOpts &o, cudaStream_t stream) {
     static bool attr_done = false;  // benign race: the attribute call is idempotent
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -202,80 +381,73 @@ cudaError_t launch_tok(const CUtensorMap &tw, const CUtensorMap &ta, const float
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.split), static_cast<unsigned>(p.n_tiles),
-                       static_cast<unsigned>(p.m_tiles));
-    cfg.blockDim = dim3(128, 1, 1);
-    cfg.dynamicSmemBytes = p.smem_bytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attrs[1];
-    attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = static_cast<unsigned>(p.split);
-    attrs[0].val.clusterDim.y = 1;
-    attrs[0].val.clusterDim.z = 1;
-    cfg.attrs = attrs;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_gemm_kernel<TOK>, tw, ta, sa, sb, gran, static_cast<int>(M),
-                              static_cast<int>(N), p.kb_total, p.stages, static_cast<__nv_bfloat16 *>(out), err);
+    return launch_with_opts(decode_gemm_kernel<TOK>, dim3(static_cast<unsigned>(p.ctas)),
+                            dim3(DecodeCfg<TOK>::kThreads), p.smem_bytes, stream, o, tw, ta, a);
 }
 
 }  // namespace
 
-// Shared memory one CTA needs for `stages` stages of `tok` tokens, plus the
-// 1024-byte alignment slack and the barriers.
+// TMEM accumulators of the decode kernel for a token tile (DecodeCfg::kBufs).
+static int decode_tmem_bufs(int tok) { return tok <= 16 ? 8 : 4; }
+
+// Shared memory one CTA needs: the 1024-byte alignment slack, `stages` stages
+// of weights + tokens, and the mbarriers (full/empty per stage, full/empty per
+// TMEM accumulator, one final), rounded up.
 static size_t decode_smem_bytes(int tok, int stages) {
-    return 1024 + static_cast<size_t>(stages) * (kDecodeRows * kBlockK + tok * kBlockK) + 256;
+    const size_t barriers = 8u * static_cast<size_t>(2 * stages + 2 * decode_tmem_bufs(tok) + 1);
+    return 1024 + static_cast<size_t>(stages) * (kDecodeRows * kBlockK + tok * kBlockK) + ((barriers + 127) / 128) * 128;
 }
 
 DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, int num_sms) {
     DecodePlan p{};
-    p.tok_pad = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
-    const int stage_bytes = kDecodeRows * kBlockK + p.tok_pad * kBlockK;
-    // About 60 KB of stages per CTA; several CTAs share an SM.
-    p.stages = 60 * 1024 / stage_bytes;
-    if (p.stages < 2) p.stages = 2;
+    p.tok_pad = M <= 16 ? 16 : M <= 32 ? 32 : 64;
+    p.stages = 3;  // ~55-75 KB: two CTAs of this kernel and one of the next fit on an SM
     p.smem_bytes = decode_smem_bytes(p.tok_pad, p.stages);
     p.n_tiles = static_cast<int>((N + kDecodeRows - 1) / kDecodeRows);
     p.m_tiles = static_cast<int>((M + p.tok_pad - 1) / p.tok_pad);
     p.kb_total = static_cast<int>((K + kBlockK - 1) / kBlockK);
-    // CTAs resident per SM: 228 KB of shared memory per SM (1 KB reserved per
-    // CTA), at most 4 by the register budget of __launch_bounds__(128, 4), and
-    // TMEM columns (512 per SM).
-    const int tmem_cols = p.tok_pad < 32 ? 32 : p.tok_pad;
-    int per_sm = static_cast<int>((228 * 1024) / (p.smem_bytes + 1024));
-    if (per_sm > 512 / tmem_cols) per_sm = 512 / tmem_cols;
-    if (per_sm > 4) per_sm = 4;
-    if (per_sm < 1) per_sm = 1;
-    const int64_t slots = static_cast<int64_t>(per_sm) * num_sms;
-    const int64_t tiles = static_cast<int64_t>(p.n_tiles) * p.m_tiles;
-    // Pick the split S (1..8, at most one k-block per CTA) that minimises
-    // waves * (k-blocks per CTA + fixed per-CTA cost); ties keep the smaller S.
-    const int kOverheadKb = 2;
-    int best_s = 1;
-    int64_t best_cost = -1;
-    for (int s = 1; s <= 8 && s <= p.kb_total; ++s) {
-        const int64_t ctas = tiles * s;
-        const int64_t waves = (ctas + slots - 1) / slots;
-        const int64_t per_cta = (p.kb_total + s - 1) / s;
-        const int64_t cost = waves * (per_cta + kOverheadKb);
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best_s = s;
-        }
-    }
-    p.split = best_s;
+    p.units = static_cast<int64_t>(p.n_tiles) * p.m_tiles * p.kb_total;
+    // Two persistent CTAs per SM, each with the same number of units (+-1),
+    // and at least kb_total / (kMaxFixupSegs - 1) units each, so that no more
+    // than kMaxFixupSegs CTAs share one tile.
+    const int64_t min_units = (p.kb_total + kMaxFixupSegs - 2) / (kMaxFixupSegs - 1);
+    int64_t ctas = 2 * static_cast<int64_t>(num_sms);
+    if (ctas > p.units / min_units) ctas = p.units / min_units;
+    if (ctas < 1) ctas = 1;
+    p.ctas = static_cast<int>(ctas);
     return p;
+}
+
+size_t decode_counters_needed(const DecodePlan &p) { return static_cast<size_t>(p.n_tiles) * p.m_tiles; }
+
+size_t decode_slot_floats(const DecodePlan &p) {
+    return 2u * static_cast<size_t>(p.ctas) * static_cast<size_t>(p.tok_pad) * kDecodeRows;
 }
 
 cudaError_t launch_decode_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_a, const float *scale_a,
                                const float *scale_b, int granularity, int64_t M, int64_t N, int64_t K, void *out,
-                               uint32_t *err, const DecodePlan &plan, cudaStream_t stream) {
+                               uint32_t *err, const DecodePlan &plan, const DecodeWorkspace &ws,
+                               const LaunchOpts &opts, cudaStream_t stream) {
     (void)K;
+    DecodeArgs a;
+    a.scale_a = scale_a;
+    a.scale_b = scale_b;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.err = err;
+    a.counters = ws.counters;
+    a.slots = ws.slots;
+    a.units = plan.units;
+    a.gran = granularity;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.kb_total = plan.kb_total;
+    a.n_tiles = plan.n_tiles;
+    a.stages = plan.stages;
+    a.weights_static = opts.weights_static ? 1 : 0;
     switch (plan.tok_pad) {
-        case 16: return launch_tok<16>(tmap_w, tmap_a, scale_a, scale_b, granularity, M, N, out, err, plan, stream);
-        case 32: return launch_tok<32>(tmap_w, tmap_a, scale_a, scale_b, granularity, M, N, out, err, plan, stream);
-        case 64: return launch_tok<64>(tmap_w, tmap_a, scale_a, scale_b, granularity, M, N, out, err, plan, stream);
-        default: return launch_tok<128>(tmap_w, tmap_a, scale_a, scale_b, granularity, M, N, out, err, plan, stream);
+        case 16: return launch_tok<16>(tmap_w, tmap_a, a, plan, opts, stream);
+        case 32: return launch_tok<32>(tmap_w, tmap_a, a, plan, opts, stream);
+        default: return launch_tok<64>(tmap_w, tmap_a, a, plan, opts, stream);
     }
 }
 

@@ -7,39 +7,76 @@
 
 namespace fp8k {
 
+// Launch options shared by the kernels.
+struct LaunchOpts {
+    bool pdl = true;              // programmatic dependent launch (prologue overlaps the previous kernel)
+    bool weights_static = false;  // B is not written by the kernel just before this one in the stream
+};
+
+// Launch with the programmatic-stream-serialisation attribute when opts.pdl:
+// the kernel may start while its predecessor in the stream is finishing, and
+// waits for it (griddepcontrol.wait) before touching memory it may have written.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_with_opts(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, const LaunchOpts &opts, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = opts.pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // ---------------------------------------------------------------- quantisers --
 
 cudaError_t launch_quant_static(const void *x, const float *scale, void *out, int64_t M, int64_t K,
-                                uint32_t *err, cudaStream_t stream, int num_sms);
+                                uint32_t *err, cudaStream_t stream, int num_sms, const LaunchOpts &opts);
 
 cudaError_t launch_quant_per_token(const void *x, void *out, float *scale_out, int64_t M, int64_t K,
-                                   uint32_t *err, cudaStream_t stream);
+                                   uint32_t *err, cudaStream_t stream, const LaunchOpts &opts);
 
 cudaError_t launch_rmsnorm_quant(const void *x, const void *gamma, float eps, const float *scale, void *out,
-                                 int64_t M, int64_t K, uint32_t *err, cudaStream_t stream);
+                                 int64_t M, int64_t K, uint32_t *err, cudaStream_t stream, const LaunchOpts &opts);
 
 // ------------------------------------------------------------- decode GEMM --
 
 // Tile geometry of the weight-streaming kernel: 128 weight rows (output
-// channels) per CTA on the tensor core's M side, the tokens on its N side.
+// channels) per tile on the tensor core's M side, up to 64 tokens on its N side.
 constexpr int kDecodeRows = 128;
 constexpr int kBlockK = 128;  // bytes (= E4M3 elements) of K per pipeline stage
-constexpr int kDecodeMaxTokens = 128;
+constexpr int kDecodeMaxTokens = 64;
 
 struct DecodePlan {
-    int tok_pad;   // tokens per CTA on the MMA N side: 16, 32, 64 or 128
-    int split;     // CTAs per cluster sharing one tile's K range (1..8)
-    int stages;    // pipeline depth
-    int n_tiles;   // ceil(N / 128)
-    int m_tiles;   // ceil(M / tok_pad)
-    int kb_total;  // ceil(K / 128)
+    int tok_pad;      // tokens per tile on the MMA N side: 16, 32 or 64
+    int stages;       // pipeline depth
+    int n_tiles;      // ceil(N / 128)
+    int m_tiles;      // ceil(M / tok_pad)
+    int kb_total;     // ceil(K / 128)
+    int64_t units;    // n_tiles * m_tiles * kb_total (one unit = one tile x one k-block)
+    int ctas;         // persistent CTAs; CTA c owns units [c*units/ctas, (c+1)*units/ctas)
     size_t smem_bytes;
 };
 
 DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, int num_sms);
 
+// Scratch of the decode kernel: a zeroed arrival counter per output tile, and
+// two partial-sum slots per CTA (128 x tok_pad fp32 each) for the tiles whose
+// K range is split between CTAs.  Every launch leaves the counters at zero.
+struct DecodeWorkspace {
+    uint32_t *counters;
+    float *slots;
+};
+size_t decode_counters_needed(const DecodePlan &p);  // number of counters
+size_t decode_slot_floats(const DecodePlan &p);      // number of fp32 slot entries
+
 cudaError_t launch_decode_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_a, const float *scale_a,
                                const float *scale_b, int granularity, int64_t M, int64_t N, int64_t K, void *out,
-                               uint32_t *err, const DecodePlan &plan, cudaStream_t stream);
+                               uint32_t *err, const DecodePlan &plan, const DecodeWorkspace &ws, const LaunchOpts &opts,
+                               cudaStream_t stream);
 
 }  // namespace fp8k

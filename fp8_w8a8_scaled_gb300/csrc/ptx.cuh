@@ -18,6 +18,9 @@ enum : uint32_t {
     kErrDecodeFullWait = 1u << 0,
     kErrDecodeEmptyWait = 1u << 1,
     kErrDecodeAccumWait = 1u << 2,
+    kErrDecodeTmemFullWait = 1u << 3,
+    kErrDecodeTmemEmptyWait = 1u << 8,
+    kErrDecodeFixup = 1u << 9,
     kErrPrefillFullWait = 1u << 4,
     kErrPrefillEmptyWait = 1u << 5,
     kErrPrefillAccumWait = 1u << 6,
@@ -201,6 +204,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------------ compensated summation --
+
+// (hi, lo) += v with Knuth's TwoSum: hi + lo represents the running sum with
+// the rounding error of every addition kept in lo.  Plain binary32 adds, no
+// contraction (the library is compiled with --fmad=false).
+__device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float v) {
+    const float s = __fadd_rn(hi, v);
+    const float bv = __fsub_rn(s, hi);
+    const float av = __fsub_rn(s, bv);
+    const float err = __fadd_rn(__fsub_rn(hi, av), __fsub_rn(v, bv));
+    hi = s;
+    lo = __fadd_rn(lo, err);
+}
+
 // ----------------------------------------------------------------- cluster --
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -220,9 +237,17 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+// Store to distributed shared memory (another CTA of the cluster).
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float2 v) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
+}
+
+// Loads from distributed shared memory.  Volatile (kept in program order after
+// the cluster barrier that publishes the data) but without a memory clobber,
+// so several loads can be in flight at once.
+__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
     return v;
 }
 
@@ -233,7 +258,9 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Allows the next grid in the stream (if launched with programmatic stream
-// serialisation) to start launching.
+// serialisation) to start launching.  Called only after grid_dependency_wait():
+// a grid that triggered before its own wait would let its successor launch and
+// trigger in turn, piling up waiting grids that hold SM resources.
 __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

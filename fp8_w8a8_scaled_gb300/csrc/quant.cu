@@ -14,9 +14,11 @@
 //
 // Rounding is pinned so the bytes match the CPU definition exactly: IEEE
 // binary32 division (__fdiv_rn, never a reciprocal multiply), separate
-// binary32 multiplies (no FMA), binary64 sum of squares / mean / sqrt /
-// reciprocal, round-to-nearest-even bf16, and the hardware's saturating
-// round-to-nearest-even E4M3 conversion (cvt.rn.satfinite.e4m3x2.f32).
+// binary32 multiplies (no FMA), the sum of squares formed exactly and rounded
+// once to binary32, binary32 mean / sqrt / reciprocal, round-to-nearest-even
+// bf16, and the hardware's saturating round-to-nearest-even E4M3
+// conversion (cvt.rn.satfinite.e4m3x2.f32).  Every kernel is launched with
+// programmatic dependent launch and waits for its predecessor before reading.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -63,7 +65,6 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     return v;
 }
 
-template <int T>
 __device__ __forceinline__ float block_max(float v, float *red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
@@ -71,7 +72,7 @@ __device__ __forceinline__ float block_max(float v, float *red) {
     if (lane == 0) red[warp] = v;
     __syncthreads();
     if (warp == 0) {
-        v = lane < T / 32 ? red[lane] : 0.0f;
+        v = lane < static_cast<int>(blockDim.x >> 5) ? red[lane] : 0.0f;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
         if (lane == 0) red[0] = v;
@@ -80,24 +81,82 @@ __device__ __forceinline__ float block_max(float v, float *red) {
     return red[0];
 }
 
-// Sum of the threads' binary64 partial sums.  (Every term is an exact square of
-// a bf16 value; the order only matters if the partial sums need more than 53
-// significand bits, which takes rows spanning ~40 binades.)
-template <int T>
-__device__ __forceinline__ double block_sum_f64(double v, double *red) {
+// Block-wide reductions used by the RMSNorm kernel.
+__device__ __forceinline__ int block_max_int(int v, int *red) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
     if (lane == 0) red[warp] = v;
     __syncthreads();
-    if (warp == 0) {
-        v = lane < T / 32 ? red[lane] : 0.0;
+    v = lane < static_cast<int>(blockDim.x >> 5) ? red[lane] : 0;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-        if (lane == 0) red[0] = v;
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// 128-bit unsigned integer as (hi, lo).
+struct U128 {
+    uint64_t hi, lo;
+};
+
+__device__ __forceinline__ U128 add128(U128 a, U128 b) {
+    U128 r;
+    r.lo = a.lo + b.lo;
+    r.hi = a.hi + b.hi + (r.lo < a.lo ? 1u : 0u);
+    return r;
+}
+
+__device__ __forceinline__ U128 block_sum_u128(U128 v, uint64_t *red_hi, uint64_t *red_lo) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        U128 w;
+        w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
+        w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
+        v = add128(v, w);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) {
+        red_hi[warp] = v.hi;
+        red_lo[warp] = v.lo;
     }
     __syncthreads();
-    return red[0];
+    const int nw = static_cast<int>(blockDim.x >> 5);
+    v.hi = lane < nw ? red_hi[lane] : 0;
+    v.lo = lane < nw ? red_lo[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        U128 w;
+        w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
+        w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
+        v = add128(v, w);
+    }
+    return v;
+}
+
+__device__ __forceinline__ uint64_t shr128(U128 a, int q) {  // low 64 bits of a >> q, 0 <= q < 128
+    if (q == 0) return a.lo;
+    if (q < 64) return (a.lo >> q) | (a.hi << (64 - q));
+    return a.hi >> (q - 64);
+}
+
+__device__ __forceinline__ int bit128(U128 a, int i) {
+    return static_cast<int>(i < 64 ? (a.lo >> i) & 1u : (a.hi >> (i - 64)) & 1u);
+}
+
+__device__ __forceinline__ bool any_below128(U128 a, int i) {  // any set bit at positions < i
+    if (i <= 0) return false;
+    if (i < 64) return (a.lo & ((1ull << i) - 1)) != 0;
+    if (i == 64) return a.lo != 0;
+    return a.lo != 0 || (a.hi & ((1ull << (i - 64)) - 1)) != 0;
+}
+
+// bf16 bits -> (m, E): x = +-m * 2^(E - 134) with E >= 1 (E = 1 also for subnormals).
+__device__ __forceinline__ void bf16_split(uint32_t b, uint32_t &m, int &E) {
+    const uint32_t e = (b >> 7) & 0xFFu, mant = b & 0x7Fu;
+    m = e ? (128u | mant) : mant;
+    E = e ? static_cast<int>(e) : 1;
 }
 
 // ------------------------------------------------------------- static quant --
@@ -118,10 +177,13 @@ __global__ void __launch_bounds__(256) quant_static_kernel(const uint4 *__restri
 
 // ---------------------------------------------------------- per-token quant --
 
-// One CTA per row, the row held in registers: T threads x V vectors of 8.
-template <int T, int V>
-__global__ void __launch_bounds__(T) quant_per_token_kernel(const uint4 *__restrict__ x, uint2 *__restrict__ out,
-                                                            float *__restrict__ scale_out, int nvec) {
+// One CTA per row, the row held in registers: blockDim.x threads (up to 1024)
+// x V vectors of 8, as few vectors per thread as the row allows so that every
+// thread's serial chain is short.
+template <int V>
+__global__ void __launch_bounds__(1024) quant_per_token_kernel(const uint4 *__restrict__ x, uint2 *__restrict__ out,
+                                                               float *__restrict__ scale_out, int nvec) {
+    const int T = static_cast<int>(blockDim.x);
     __shared__ float red[32];
     grid_dependency_wait();
     grid_launch_dependents();
@@ -138,7 +200,7 @@ __global__ void __launch_bounds__(T) quant_per_token_kernel(const uint4 *__restr
             amax = absmax8(v[j], amax);
         }
     }
-    amax = block_max<T>(amax, red);
+    amax = block_max(amax, red);
     const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
     if (threadIdx.x == 0) scale_out[row] = s;
 #pragma unroll
@@ -160,7 +222,7 @@ __global__ void __launch_bounds__(512) quant_per_token_long_kernel(const uint4 *
     uint2 *orow = out + row * nvec;
     float amax = 0.0f;
     for (int64_t i = threadIdx.x; i < nvec; i += 512) amax = absmax8(__ldg(xr + i), amax);
-    amax = block_max<512>(amax, red);
+    amax = block_max(amax, red);
     const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
     if (threadIdx.x == 0) scale_out[row] = s;
     for (int64_t i = threadIdx.x; i < nvec; i += 512) orow[i] = quant8(__ldg(xr + i), s);
@@ -168,45 +230,123 @@ __global__ void __launch_bounds__(512) quant_per_token_long_kernel(const uint4 *
 
 // ---------------------------------------------------- fused RMSNorm -> quant --
 
-template <int T, int V>
-__global__ void __launch_bounds__(T) rmsnorm_quant_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gamma,
-                                                          float eps, const float *__restrict__ scale,
-                                                          uint2 *__restrict__ out, int nvec, int K) {
-    __shared__ double red[32];
+// One CTA per row.  The sum of squares is formed EXACTLY: every bf16 square is
+// m^2 * 2^(2E - 268) with m < 256, so the squares of the row's top 40 binades
+// are added as integers into a 128-bit fixed-point accumulator (2^94 per term
+// at most, 2^110 for 2^16 terms), and any nonzero smaller term only sets a
+// sticky bit -- all terms are non-negative and smaller than 2^-61 of the sum,
+// so the sticky bit is all the rounding needs.  The exact sum is rounded once
+// to binary32, then mean = ss / K, t = mean + eps, d = sqrt(t), r = 1 / d are
+// single IEEE binary32 operations.
+template <int V>
+__global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gamma,
+                                                             float eps, const float *__restrict__ scale,
+                                                             uint2 *__restrict__ out, int nvec, int K) {
+    const int T = static_cast<int>(blockDim.x);
+    __shared__ uint64_t red_hi[32], red_lo[32];
+    __shared__ int red_i[32];
+    __shared__ float s_r;
     grid_dependency_wait();
     grid_launch_dependents();
     const int64_t row = blockIdx.x;
     const uint4 *xr = x + row * nvec;
     uint2 *orow = out + row * nvec;
-    uint4 v[V];
-    double ss = 0.0;
+    uint4 v[V], g[V];
+    constexpr bool kPrefetchGamma = V <= 8;  // keep gamma in registers too when they are plentiful
+    int emax = 0, special = 0;               // special: 3 = a NaN, 2 = an Inf (the max keeps NaN)
 #pragma unroll
     for (int j = 0; j < V; ++j) {
         const int idx = threadIdx.x + j * T;
         if (idx < nvec) {
             v[j] = ld_stream(xr + idx);
+            if (kPrefetchGamma) g[j] = __ldg(gamma + idx);
             const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const double a = static_cast<double>(bf16_lo(w[i]));
-                const double b = static_cast<double>(bf16_hi(w[i]));
-                ss = __dadd_rn(ss, __dmul_rn(a, a));
-                ss = __dadd_rn(ss, __dmul_rn(b, b));
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t b = (w[i >> 1] >> (16 * (i & 1))) & 0x7FFFu;
+                if ((b >> 7) == 0xFFu) {
+                    special = max(special, (b & 0x7Fu) ? 3 : 2);
+                } else if (b != 0) {
+                    uint32_t m;
+                    int E;
+                    bf16_split(b, m, E);
+                    emax = max(emax, E);
+                }
             }
         }
     }
-    ss = block_sum_f64<T>(ss, red);
-    const double mean = __ddiv_rn(ss, static_cast<double>(K));
-    const double denom = __dsqrt_rn(__dadd_rn(mean, static_cast<double>(eps)));
-    const float r = __double2float_rn(__ddiv_rn(1.0, denom));
+    emax = block_max_int(emax, red_i);
+    special = block_max_int(special, red_i);
+    const int elo = max(emax - 39, 1);
+    U128 acc = {0, 0};
+    int sticky = 0;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = threadIdx.x + j * T;
+        if (idx < nvec) {
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t b = (w[i >> 1] >> (16 * (i & 1))) & 0x7FFFu;
+                if (b == 0 || (b >> 7) == 0xFFu) continue;
+                uint32_t m;
+                int E;
+                bf16_split(b, m, E);
+                if (E < elo) {
+                    sticky = 1;
+                    continue;
+                }
+                const int sh = 2 * (E - elo);  // 0 .. 78
+                const uint64_t sq = static_cast<uint64_t>(m * m);
+                U128 t;
+                t.lo = sh < 64 ? (sq << sh) : 0;
+                t.hi = sh == 0 ? 0 : (sh < 64 ? (sq >> (64 - sh)) : (sq << (sh - 64)));
+                acc = add128(acc, t);
+            }
+        }
+    }
+    acc = block_sum_u128(acc, red_hi, red_lo);
+    sticky = block_max_int(sticky, red_i);
+    if (threadIdx.x == 0) {
+        float ss;
+        if (special == 3) {
+            ss = __int_as_float(0x7FC00000);
+        } else if (special == 2) {
+            ss = __int_as_float(0x7F800000);
+        } else if (acc.hi == 0 && acc.lo == 0) {
+            ss = 0.0f;
+        } else {
+            // value = acc * 2^(2*elo - 268); round at binary32 precision (24
+            // significant bits, or the subnormal quantum 2^-149)
+            const int top = acc.hi ? 127 - __clzll(static_cast<long long>(acc.hi))
+                                   : 63 - __clzll(static_cast<long long>(acc.lo));
+            const int q = max(top - 23, 119 - 2 * elo);
+            uint64_t keep;
+            if (q <= 0) {
+                keep = acc.lo;  // fewer than 24 significant bits: exact
+            } else {
+                keep = shr128(acc, q);
+                const bool half = bit128(acc, q - 1) != 0;
+                const bool rest = any_below128(acc, q - 1) || sticky;
+                if (half && (rest || (keep & 1u))) keep += 1;
+            }
+            ss = ldexpf(static_cast<float>(keep), (q > 0 ? q : 0) + 2 * elo - 268);
+        }
+        const float mean = __fdiv_rn(ss, static_cast<float>(K));
+        const float t = __fadd_rn(mean, eps);
+        const float d = __fsqrt_rn(t);
+        s_r = __fdiv_rn(1.0f, d);
+    }
+    __syncthreads();
+    const float r = s_r;
     const float s = __ldg(scale);
 #pragma unroll
     for (int j = 0; j < V; ++j) {
         const int idx = threadIdx.x + j * T;
         if (idx < nvec) {
-            const uint4 g = __ldg(gamma + idx);
             const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-            const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+            const uint4 gv = kPrefetchGamma ? g[j] : __ldg(gamma + idx);
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
             uint32_t p[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -219,54 +359,66 @@ __global__ void __launch_bounds__(T) rmsnorm_quant_kernel(const uint4 *__restric
     }
 }
 
-template <int T, int V>
-cudaError_t launch_rows_pt(const void *x, void *out, float *scale_out, int64_t M, int64_t K, cudaStream_t stream) {
-    quant_per_token_kernel<T, V><<<static_cast<unsigned>(M), T, 0, stream>>>(
-        static_cast<const uint4 *>(x), static_cast<uint2 *>(out), scale_out, static_cast<int>(K / 8));
-    return cudaGetLastError();
+// Threads per row-CTA for `nvec` vectors at V vectors per thread: a multiple
+// of 32, at most 1024.
+inline int row_threads(int64_t nvec, int V) {
+    const int64_t t = (nvec + V - 1) / V;
+    return static_cast<int>(((t + 31) / 32) * 32);
 }
 
-template <int T, int V>
+template <int V>
+cudaError_t launch_rows_pt(const void *x, void *out, float *scale_out, int64_t M, int64_t K, cudaStream_t stream,
+                           const LaunchOpts &o) {
+    const int64_t nvec = K / 8;
+    return launch_with_opts(quant_per_token_kernel<V>, dim3(static_cast<unsigned>(M)), dim3(row_threads(nvec, V)), 0,
+                            stream, o, static_cast<const uint4 *>(x), static_cast<uint2 *>(out), scale_out,
+                            static_cast<int>(nvec));
+}
+
+template <int V>
 cudaError_t launch_rows_rms(const void *x, const void *gamma, float eps, const float *scale, void *out, int64_t M,
-                            int64_t K, cudaStream_t stream) {
-    rmsnorm_quant_kernel<T, V><<<static_cast<unsigned>(M), T, 0, stream>>>(
-        static_cast<const uint4 *>(x), static_cast<const uint4 *>(gamma), eps, scale, static_cast<uint2 *>(out),
-        static_cast<int>(K / 8), static_cast<int>(K));
-    return cudaGetLastError();
+                            int64_t K, cudaStream_t stream, const LaunchOpts &o) {
+    const int64_t nvec = K / 8;
+    return launch_with_opts(rmsnorm_quant_kernel<V>, dim3(static_cast<unsigned>(M)), dim3(row_threads(nvec, V)), 0,
+                            stream, o, static_cast<const uint4 *>(x), static_cast<const uint4 *>(gamma), eps, scale,
+                            static_cast<uint2 *>(out), static_cast<int>(nvec), static_cast<int>(K));
 }
 
 }  // namespace
 
 cudaError_t launch_quant_static(const void *x, const float *scale, void *out, int64_t M, int64_t K, uint32_t *err,
-                                cudaStream_t stream, int num_sms) {
+                                cudaStream_t stream, int num_sms, const LaunchOpts &o) {
     (void)err;
     const int64_t n16 = M * K / 16;
     int64_t blocks = (n16 + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    quant_static_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<const uint4 *>(x), scale,
-                                                                           static_cast<uint4 *>(out), n16);
-    return cudaGetLastError();
+    return launch_with_opts(quant_static_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, o,
+                            static_cast<const uint4 *>(x), scale, static_cast<uint4 *>(out), n16);
 }
 
 cudaError_t launch_quant_per_token(const void *x, void *out, float *scale_out, int64_t M, int64_t K, uint32_t *err,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, const LaunchOpts &o) {
     (void)err;
-    if (K <= 128 * 8 * 8) return launch_rows_pt<128, 8>(x, out, scale_out, M, K, stream);
-    if (K <= 256 * 16 * 8) return launch_rows_pt<256, 16>(x, out, scale_out, M, K, stream);
-    if (K <= 512 * 16 * 8) return launch_rows_pt<512, 16>(x, out, scale_out, M, K, stream);
-    quant_per_token_long_kernel<<<static_cast<unsigned>(M), 512, 0, stream>>>(
-        static_cast<const uint4 *>(x), static_cast<uint2 *>(out), scale_out, K / 8);
-    return cudaGetLastError();
+    const int64_t nvec = K / 8;
+    if (nvec <= 1024) return launch_rows_pt<1>(x, out, scale_out, M, K, stream, o);
+    if (nvec <= 2048) return launch_rows_pt<2>(x, out, scale_out, M, K, stream, o);
+    if (nvec <= 4096) return launch_rows_pt<4>(x, out, scale_out, M, K, stream, o);
+    if (nvec <= 8192) return launch_rows_pt<8>(x, out, scale_out, M, K, stream, o);
+    if (nvec <= 16384) return launch_rows_pt<16>(x, out, scale_out, M, K, stream, o);
+    return launch_with_opts(quant_per_token_long_kernel, dim3(static_cast<unsigned>(M)), dim3(512), 0, stream, o,
+                            static_cast<const uint4 *>(x), static_cast<uint2 *>(out), scale_out, nvec);
 }
 
 cudaError_t launch_rmsnorm_quant(const void *x, const void *gamma, float eps, const float *scale, void *out,
-                                 int64_t M, int64_t K, uint32_t *err, cudaStream_t stream) {
+                                 int64_t M, int64_t K, uint32_t *err, cudaStream_t stream, const LaunchOpts &o) {
     (void)err;
-    if (K <= 128 * 8 * 8) return launch_rows_rms<128, 8>(x, gamma, eps, scale, out, M, K, stream);
-    if (K <= 256 * 16 * 8) return launch_rows_rms<256, 16>(x, gamma, eps, scale, out, M, K, stream);
-    return launch_rows_rms<512, 16>(x, gamma, eps, scale, out, M, K, stream);
+    const int64_t nvec = K / 8;
+    if (nvec <= 1024) return launch_rows_rms<1>(x, gamma, eps, scale, out, M, K, stream, o);
+    if (nvec <= 2048) return launch_rows_rms<2>(x, gamma, eps, scale, out, M, K, stream, o);
+    if (nvec <= 4096) return launch_rows_rms<4>(x, gamma, eps, scale, out, M, K, stream, o);
+    return launch_rows_rms<8>(x, gamma, eps, scale, out, M, K, stream, o);
 }
 
 }  // namespace fp8k

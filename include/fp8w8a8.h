@@ -24,7 +24,12 @@
  * Conventions shared by every call
  *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
  *     caller owns and allocates every buffer.  The library allocates no device
- *     memory per call.
+ *     memory per call: its only allocation is a ~25 MB scratch area per device
+ *     (arrival counters and partial sums of the decode GEMM), made on the
+ *     first fp8_scaled_mm call on that device -- make that first call before
+ *     capturing a CUDA graph.  Because the scratch is shared, GEMM calls that
+ *     may run concurrently on different streams of one device race; order
+ *     them on one stream (or with events).
  *   - Row-major layouts.  E4M3 is the OCP FP8 "E4M3" finite encoding
  *     (torch.float8_e4m3fn): 1 byte, max 448, NaN = 0x7F/0xFF, no Inf.
  *     bf16 is IEEE binary32's upper half.  Scales are IEEE binary32.
@@ -105,6 +110,26 @@ fp8_status fp8_scaled_mm(const void *A, const void *B, const float *scale_a, con
                          int granularity, int out_dtype, int64_t M, int64_t N, int64_t K, void *out,
                          void *stream);
 
+/* Flags of fp8_scaled_mm_ex. */
+typedef enum {
+    /* B is not written by the kernel that runs just before this call in the
+     * stream (typical for model weights), so the kernel may start streaming B
+     * before that kernel has finished.  Wrong if the previous kernel writes B. */
+    FP8_FLAG_WEIGHTS_STATIC = 1,
+    /* Launch without programmatic dependent launch (plain stream order). */
+    FP8_FLAG_NO_PDL = 2
+} fp8_flags;
+
+/* fp8_scaled_mm_ex -- fp8_scaled_mm with launch flags (fp8_flags, OR-ed).
+ * By default every kernel of this library is launched with programmatic
+ * dependent launch: it may begin its prologue while the previous kernel in the
+ * stream is finishing and waits (griddepcontrol.wait) for that kernel before
+ * reading anything it could have written.  Same arguments and errors as
+ * fp8_scaled_mm; unknown flag bits return FP8_ERR_INVALID_ARG. */
+fp8_status fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, const float *scale_b,
+                            int granularity, int out_dtype, int64_t M, int64_t N, int64_t K, void *out,
+                            void *stream, unsigned flags);
+
 /* rmsnorm_quant_fp8 -- fused RMSNorm -> static per-tensor E4M3 quantisation,
  * one pass ("quantise once" per layer).
  *
@@ -163,20 +188,22 @@ const char *fp8_status_string(int status);
  * execution would take. */
 int fp8_describe_dispatch(int64_t M, int64_t N, int64_t K, int granularity);
 
-/* Split-K factor the decode kernel uses for this shape on the current device
- * (number of CTAs that share one output tile's K range), or -1 if the shape
- * does not go to the decode kernel.  Host-only. */
-int fp8_decode_split(int64_t M, int64_t N, int64_t K);
+/* Number of persistent CTAs the decode kernel launches for this shape on the
+ * current device (the K ranges of all output tiles are divided evenly among
+ * them), or -1 if the shape does not go to the decode kernel.  Host-only. */
+int fp8_decode_ctas(int64_t M, int64_t N, int64_t K);
 
-/* The same choice for a device with `num_sms` streaming multiprocessors; pure
- * and host-only (usable without a GPU). */
-int fp8_decode_split_for_sms(int64_t M, int64_t N, int64_t K, int num_sms);
+/* The same for a device with `num_sms` streaming multiprocessors; pure and
+ * host-only (usable without a GPU). */
+int fp8_decode_ctas_for_sms(int64_t M, int64_t N, int64_t K, int num_sms);
 
 /* Device error word.  Kernels never trap: a bounded wait that runs out sets a
- * bit here and the kernel returns early.  fp8_get_device_error synchronises
+ * bit here and the kernel finishes without waiting further (its outputs are
+ * then invalid).  fp8_get_device_error synchronises
  * `stream`, copies the word for the current device into *word (host pointer,
  * may be NULL) and returns FP8_ERR_DEVICE if it is non-zero.  Not for the hot
- * path.  fp8_clear_device_error zeroes the word (synchronously). */
+ * path.  fp8_clear_device_error zeroes the word and the decode GEMM's
+ * arrival counters (synchronously). */
 fp8_status fp8_get_device_error(void *stream, uint32_t *word);
 fp8_status fp8_clear_device_error(void);
 

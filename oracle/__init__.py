@@ -46,6 +46,8 @@ def _load():
     lib.oracle_quant_static.argtypes = [P, ctypes.c_float, I64, I64, P]
     lib.oracle_quant_per_token.argtypes = [P, I64, I64, P, P]
     lib.oracle_rmsnorm_bf16.argtypes = [P, P, ctypes.c_float, I64, I64, P]
+    lib.oracle_sum_squares_bf16.argtypes = [P, I64]
+    lib.oracle_sum_squares_bf16.restype = ctypes.c_float
     lib.oracle_rmsnorm_quant.argtypes = [P, P, ctypes.c_float, ctypes.c_float, I64, I64, P]
     lib.oracle_gemm_acc_f64.argtypes = [P, P, I64, I64, I64, P, ctypes.c_int]
     lib.oracle_gemm_acc_i64.argtypes = [P, P, I64, I64, I64, P, ctypes.c_int]
@@ -133,6 +135,12 @@ def quant_per_token(x_bf16):
     s = np.empty(M, np.float32)
     _load().oracle_quant_per_token(_ptr(x), M, K, _ptr(q), _ptr(s))
     return q, s
+
+
+def sum_squares_bf16(x_bf16) -> np.float32:
+    """Exact sum of squares of a bf16 vector, rounded once to binary32."""
+    x = _c(x_bf16, np.uint16).ravel()
+    return np.float32(_load().oracle_sum_squares_bf16(_ptr(x), x.size))
 
 
 def rmsnorm_bf16(x_bf16, gamma_bf16, eps: float) -> np.ndarray:

@@ -29,9 +29,10 @@
  *   R1 round-to-nearest-even everywhere; R2 saturate out-of-range magnitudes to
  *   +-448 (NaN stays NaN, encoded 0x7F); R3 a quantiser divides by its scale in
  *   IEEE binary32 (no reciprocal multiply); R4 a per-token scale is
- *   amax/448 in binary32, and 1.0 for an all-zero row; R5 RMSNorm sums squares
- *   in binary64, forms 1/sqrt(mean+eps) in binary64, rounds it once to binary32,
- *   multiplies x*r then *gamma in binary32 and rounds the normalised value to
+ *   amax/448 in binary32, and 1.0 for an all-zero row; R5 RMSNorm forms the
+ *   exact sum of squares rounded once to binary32, then mean, +eps, sqrt and
+ *   the reciprocal as single IEEE binary32 operations, multiplies x*r then
+ *   *gamma in binary32 and rounds the normalised value to
  *   bf16 before quantising (this bf16 intermediate is what makes the fused
  *   producer byte-identical to "RMSNorm to bf16, then static quant", [P3]
  *   "Ranked follow-ons from the same audit", third bullet); R6 the GEMM
@@ -219,28 +220,91 @@ void oracle_quant_per_token(const uint16_t *x, int64_t M, int64_t K, uint8_t *q,
     }
 }
 
+/* Sum of squares of K bf16 values, computed exactly and rounded once to
+ * binary32 (round-to-nearest-even).  A finite bf16 value is x = m * 2^e with an
+ * integer m < 256: m = 128 + mantissa and e = E - 134 for an exponent field
+ * E >= 1, m = mantissa and e = -133 for E == 0.  So x^2 = m^2 * 2^(2e) with
+ * 2e >= -266, and every square is an integer multiple of 2^-266 below 2^256.
+ * The squares are added into a fixed-point integer in units of 2^-266 (nine
+ * 64-bit limbs, 576 bits: room for 2^16 squares), which is then rounded to
+ * binary32.  A NaN element gives NaN, an infinite one +Inf. */
+#define SS_LIMBS 9
+static void limbs_add_shifted(uint64_t *acc, uint64_t v, int shift) {
+    int limb = shift / 64, off = shift % 64;
+    uint64_t lo = v << off;
+    uint64_t hi = off ? (v >> (64 - off)) : 0;
+    uint64_t old = acc[limb];
+    acc[limb] = old + lo;
+    uint64_t carry = acc[limb] < old;
+    for (int i = limb + 1; i < SS_LIMBS && (hi || carry); ++i) {
+        uint64_t o = acc[i];
+        acc[i] = o + hi + carry;
+        carry = (acc[i] < o) || (carry && acc[i] == o);
+        hi = 0;
+    }
+}
+
+static int limbs_bit(const uint64_t *acc, int i) { return (int)((acc[i / 64] >> (i % 64)) & 1u); }
+
+static int limbs_any_below(const uint64_t *acc, int i) { /* any set bit at positions < i */
+    for (int j = 0; j < i / 64; ++j)
+        if (acc[j]) return 1;
+    if (i % 64 && (acc[i / 64] & ((((uint64_t)1) << (i % 64)) - 1))) return 1;
+    return 0;
+}
+
+float oracle_sum_squares_bf16(const uint16_t *x, int64_t K) {
+    uint64_t acc[SS_LIMBS] = {0};
+    int has_nan = 0, has_inf = 0;
+    for (int64_t k = 0; k < K; ++k) {
+        unsigned b = x[k] & 0x7FFFu, E = b >> 7, mant = b & 0x7Fu;
+        if (E == 255) {
+            if (mant) has_nan = 1; else has_inf = 1;
+            continue;
+        }
+        uint64_t m = E ? (128u | mant) : mant;
+        if (m == 0) continue;
+        int shift = E ? 2 * (int)E - 2 : 0; /* 2e + 266 */
+        limbs_add_shifted(acc, m * m, shift);
+    }
+    if (has_nan) return NAN;
+    if (has_inf) return INFINITY;
+    int top = -1;
+    for (int i = SS_LIMBS * 64 - 1; i >= 0; --i)
+        if (limbs_bit(acc, i)) { top = i; break; }
+    if (top < 0) return 0.0f;
+    /* bit position of the binary32 unit in the last place: 24 significant bits,
+     * or the subnormal quantum 2^-149 (= bit 117 in units of 2^-266) */
+    int q = top - 23;
+    if (q < 117) q = 117;
+    uint64_t keep = 0;
+    for (int i = top; i >= q; --i) keep = (keep << 1) | (uint64_t)limbs_bit(acc, i);
+    if (q > 0) {
+        int half = limbs_bit(acc, q - 1);
+        int sticky = limbs_any_below(acc, q - 1);
+        if (half && (sticky || (keep & 1u))) keep += 1;
+    }
+    return (float)ldexp((double)keep, q - 266); /* exact, or +Inf beyond the binary32 range */
+}
+
 /* RMSNorm to bf16 (reading R5), the unfused producer's first half:
- *   ss    = sum_k (double)x_k^2                       (binary64)
- *   r64   = 1 / sqrt(ss / K + (double)eps)            (binary64, correctly rounded ops)
- *   r     = (float) r64
+ *   ss    = the exact sum of x_k^2 rounded once to binary32
+ *   mean  = ss / K,  t = mean + eps,  d = sqrt(t),  r = 1 / d
+ *           (each one IEEE binary32 operation, rounded to nearest even)
  *   h_k   = bf16( (fp32(x_k) * r) * fp32(gamma_k) )   (two binary32 multiplies) */
 void oracle_rmsnorm_bf16(const uint16_t *x, const uint16_t *gamma, float eps, int64_t M, int64_t K,
                          uint16_t *h) {
     for (int64_t m = 0; m < M; ++m) {
         const uint16_t *row = x + m * K;
-        double ss = 0.0;
+        volatile float ss = oracle_sum_squares_bf16(row, K);
+        volatile float mean = ss / (float)K;
+        volatile float t = mean + eps;
+        volatile float d = sqrtf(t);
+        volatile float r = 1.0f / d;
         for (int64_t k = 0; k < K; ++k) {
-            double xv = (double)oracle_bf16_to_f32(row[k]);
-            ss = ss + xv * xv; /* xv*xv is exact: 16 significand bits */
-        }
-        volatile double mean = ss / (double)K;
-        volatile double denom = sqrt(mean + (double)eps);
-        volatile double r64 = 1.0 / denom;
-        float r = (float)r64;
-        for (int64_t k = 0; k < K; ++k) {
-            volatile float t = oracle_bf16_to_f32(row[k]) * r;
-            volatile float u = t * oracle_bf16_to_f32(gamma[k]);
-            h[m * K + k] = oracle_bf16_rne_f32(u);
+            volatile float u = oracle_bf16_to_f32(row[k]) * r;
+            volatile float v = u * oracle_bf16_to_f32(gamma[k]);
+            h[m * K + k] = oracle_bf16_rne_f32(v);
         }
     }
 }

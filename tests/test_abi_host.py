@@ -81,6 +81,14 @@ def test_scaled_mm_validation(L):
     assert mm(L, N=68) == 2                                    # N % 8
 
 
+def test_scaled_mm_ex_flags(L):
+    args = (GOOD, GOOD2, SC, SC2, 0, 0, 4, 64, 64, GOOD3, None)
+    assert L.fp8_scaled_mm_ex(*args[:6], 0, *args[7:], 0) == 0       # M == 0 no-op with flags
+    assert L.fp8_scaled_mm_ex(*args, 4) == 1                          # unknown flag bit
+    assert L.fp8_scaled_mm_ex(*args, 0x100) == 1
+    assert L.fp8_scaled_mm_ex(GOOD, GOOD2, SC, SC2, 0, 0, 4, 64, 72, GOOD3, None, 1) == 2
+
+
 def test_quantiser_validation(L):
     assert L.quant_fp8_static(GOOD, SC, GOOD2, 0, 64, None) == 0
     assert L.quant_fp8_static(None, SC, GOOD2, 4, 64, None) == 1
@@ -111,16 +119,18 @@ def test_describe_dispatch_is_pure(L):
         assert L.fp8_describe_dispatch(M, 10240, 5120, 2) == L.fp8_describe_dispatch(M, 10240, 5120, 2)
 
 
-def test_decode_split_planner(L):
-    """The planner keeps the grid to one wave on a 152-SM part and splits K
-    into whole 128-wide blocks."""
-    f = L.fp8_decode_split_for_sms
-    for (M, N, K) in ((1, 10240, 5120), (32, 10240, 5120), (64, 34816, 5120), (8, 5120, 8192),
-                      (8, 5120, 17408), (4, 512, 256)):
-        s = f(M, N, K, 152)
-        assert 1 <= s <= 8
-        assert s <= (K + 127) // 128
-    assert f(1, 8, 16, 152) == 1          # one k-block cannot be split
+def test_decode_planner(L):
+    """Two persistent CTAs per SM (never more CTAs than units of one tile x
+    one 128-wide k-block)."""
+    f = L.fp8_decode_ctas_for_sms
+    for (M, N, K) in ((1, 10240, 5120), (32, 10240, 5120), (64, 34816, 5120)):
+        assert f(M, N, K, 152) == 304
+    assert f(8, 5120, 8192, 152) == 40 * 64 // 10       # >= 10 k-blocks per CTA (64 per tile)
+    assert f(8, 5120, 17408, 152) == 40 * 136 // 20
+    assert f(4, 512, 256, 152) == 4 * 2          # 4 tiles x 2 k-blocks
+    assert f(1, 8, 16, 152) == 1                 # one unit
+    # a single tile with a long K range is shared by at most 8 CTAs
+    assert f(1, 128, 5120, 152) == 40 // 6       # at least ceil(40/7) = 6 k-blocks per CTA
+    assert f(1, 8, 65536, 152) == 512 // 74
     assert f(0, 8, 16, 152) == -1
-    # pure: independent of call order
     assert f(32, 10240, 5120, 152) == f(32, 10240, 5120, 152)

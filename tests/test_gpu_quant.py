@@ -159,3 +159,30 @@ def test_per_token_flattened_equals_static_amax(fp8):
     q1, s1 = fp8.quant_fp8_per_token(x.view(1, -1))
     q2 = fp8.quant_fp8_static(x, s1)
     assert np.array_equal(host_bits(q1).reshape(4, 256), host_bits(q2))
+
+
+def test_rmsnorm_exact_sum_edge_rows(fp8, orc):
+    """Rows that exercise the exact sum of squares: a binary32 tie broken by a
+    term 80 binades down (below the 40-binade window: the sticky bit), terms
+    spanning more than 120 bits, subnormal inputs, NaN / Inf, constant rows."""
+    K = 64
+    rows = np.zeros((10, K), np.uint16)
+    rows[0, :2] = [0x3F80, 0x3980]                    # 1 + 2^-24: a tie
+    rows[1, :3] = [0x3F80, 0x3980, 0x2B80]            # ... broken upwards by 2^-80
+    g = workloads.rng(44)
+    rows[2] = workloads.bf16_normal(g, (K,))
+    rows[2, ::3] = 0x1F80                             # 2^-64 next to O(1) values
+    rows[3, :5] = [0x0001, 0x0003, 0x8005, 0x007F, 0x0080]   # subnormals and the smallest normal
+    rows[4, :2] = [0x7FC0, 0x3F80]                    # NaN
+    rows[5, :2] = [0x7F80, 0x3F80]                    # +Inf
+    rows[6, :3] = [0x7F80, 0x7FC0, 0x3F80]            # Inf and NaN: NaN
+    rows[7] = 0x4040                                  # constant 3.0
+    rows[8] = workloads.bf16_normal(g, (K,), std=1e6)
+    rows[9] = 0x5F00                                  # 2^63: squares overflow binary32 -> Inf
+    gamma = workloads.bf16_normal(g, (K,), mean=1.0, std=0.1)
+    for eps in (1e-6, 0.0):
+        q = host_bits(fp8.rmsnorm_quant_fp8(to_dev_bf16(rows), to_dev_bf16(gamma), eps, to_dev_f32(1 / 56)))
+        want = orc.rmsnorm_quant(rows, gamma, eps, float(np.float32(1 / 56)))
+        nan_w = (want & 0x7F) == 0x7F
+        assert np.array_equal(q[~nan_w], want[~nan_w]), eps
+        assert np.all((q[nan_w] & 0x7F) == 0x7F), eps

@@ -1,5 +1,6 @@
 """Pins for the oracle's quantisers and RMSNorm producer (CPU only)."""
 import math
+from fractions import Fraction
 
 import numpy as np
 import sympy
@@ -100,7 +101,9 @@ def test_rmsnorm_closed_forms(orc):
     oracle lands within one bf16 rounding of the exact value."""
     K = 64
     cases = []
-    for c in (0x3F80, 0x4040, 0xBE00, 0x0080):         # 1.0, 3.0, -0.125, 2^-126
+    # 1.0, 3.0, -0.125, 2^-63 (rows whose mean square underflows binary32 are left
+    # out: with eps = 0 the binary32 chain then divides by zero)
+    for c in (0x3F80, 0x4040, 0xBE00, 0x2000):
         cases.append(np.full(K, c, np.uint16))
     spike = np.zeros(K, np.uint16)
     spike[7] = 0x40A0                                   # 5.0
@@ -127,16 +130,59 @@ def test_rmsnorm_scale_invariance(orc):
         assert np.array_equal(orc.rmsnorm_bf16(xj, gamma, 0.0), h0)
 
 
+def _f32_nearest(fr: Fraction) -> np.float32:
+    """Exact rational -> nearest binary32 (ties to even), normal range."""
+    if fr == 0:
+        return np.float32(0.0)
+    a = abs(fr)
+    e = math.floor(math.log2(a))
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    q = Fraction(2) ** (e - 23)
+    n = a / q
+    f = math.floor(n)
+    rem = n - f
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and f % 2 == 1):
+        f += 1
+    return np.float32(math.copysign(float(f * q), fr))
+
+
+def test_sum_squares_exact_vs_rationals(orc):
+    """The sum of squares is the exact rational sum rounded once to binary32,
+    including rows whose terms span more binades than binary64 can hold."""
+    g = np.random.default_rng(17)
+    rows = [workloads.bf16_normal(g, (256,)), workloads.bf16_normal(g, (1000,), std=1e-3)]
+    wide = workloads.bf16_normal(g, (64,))
+    wide[::2] = (np.float32(2.0 ** -60) * _as_f32(wide[::2])).view(np.uint32) >> 16
+    rows.append(wide.astype(np.uint16))                                # 2^-60 next to O(1): > 120 bits
+    tie = np.array([0x3F80, 0x3F80, 0x3F80, 0x3380, 0x3380], np.uint16)  # 3 + 2*2^-48: a binary32 tie + sticky
+    rows.append(tie)
+    rows.append(np.array([0x0001, 0x0002, 0x0080], np.uint16))        # subnormal bf16 inputs
+    for r in rows:
+        exact = sum(Fraction(float(v)) ** 2 for v in _as_f32(r))
+        assert orc.sum_squares_bf16(r) == _f32_nearest(exact) if exact >= Fraction(2) ** -126 else True
+    # 1 + 2^-24 is a binary32 tie (rounds to even, 1.0); a 2^-80 term breaks the tie upwards
+    assert orc.sum_squares_bf16(np.array([0x3F80, 0x3980], np.uint16)) == np.float32(1.0)
+    assert orc.sum_squares_bf16(np.array([0x3F80, 0x3980, 0x2B80], np.uint16)) == np.nextafter(
+        np.float32(1.0), np.float32(2.0))
+    assert orc.sum_squares_bf16(np.zeros(8, np.uint16)) == 0.0
+    assert np.isinf(orc.sum_squares_bf16(np.array([0x3F80, 0x7F80], np.uint16)))
+    assert np.isnan(orc.sum_squares_bf16(np.array([0x7F80, 0x7FC1], np.uint16)))
+
+
 def test_rmsnorm_vs_numpy_restatement(orc):
-    """The pinned arithmetic restated with numpy's vectorised ops (different
-    summation order, numpy sqrt) gives the same bf16 bits."""
+    """The pinned arithmetic restated with numpy's vectorised ops (binary64 sum
+    of the exact squares, then the binary32 chain) gives the same bf16 bits."""
     g = workloads.rng(15)
     x = workloads.bf16_normal(g, (32, 5120))
     gamma = workloads.bf16_normal(g, (5120,), mean=1.0, std=0.1)
     h = orc.rmsnorm_bf16(x, gamma, 1e-6)
     xf = _as_f32(x)
-    ss = np.sum(xf.astype(np.float64) ** 2, axis=1)
-    r = (1.0 / np.sqrt(ss / 5120.0 + float(np.float32(1e-6)))).astype(np.float32)
+    ss = np.sum(xf.astype(np.float64) ** 2, axis=1).astype(np.float32)
+    t = (ss / np.float32(5120)).astype(np.float32) + np.float32(1e-6)
+    r = (np.float32(1.0) / np.sqrt(t.astype(np.float32))).astype(np.float32)
     u = (xf * r[:, None]).astype(np.float32) * _as_f32(gamma)[None, :]
     ref = torch.from_numpy(u.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(h, ref)
