@@ -114,6 +114,34 @@ fp8_status decode_workspace(DeviceState *st, const fp8k::DecodePlan &plan, fp8k:
     return FP8_OK;
 }
 
+// ---------------------------------------------------------------- fixed scratch
+// Scratch of fp8_scaled_mm_noalloc: arrival counters then partial-sum slots
+// of the decode kernel, in one file-scope device array.  The module holds one
+// copy per device that loads the library, from load until the process exits.
+// In host code the array's name is only a host-side stand-in: its device
+// address comes from cudaGetSymbolAddress with the device current.
+constexpr size_t kNoAllocCounters = 16384;                 // output tiles
+constexpr size_t kNoAllocSlotFloats = 384u * 2u * 16u * 128u;  // 384 CTAs x 2 slots x 16 tokens x 128 rows
+constexpr size_t kNoAllocBytes = kNoAllocCounters * sizeof(uint32_t) + kNoAllocSlotFloats * sizeof(float);
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the fixed scratch for the current device (looked up once).
+fp8_status noalloc_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FP8_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return FP8_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -128,6 +156,7 @@ const char *fp8_status_string(int status) {
         case FP8_ERR_UNSUPPORTED: return "FP8_ERR_UNSUPPORTED: valid request not implemented (e.g. out_dtype)";
         case FP8_ERR_CUDA: return "FP8_ERR_CUDA: CUDA call or kernel launch failed";
         case FP8_ERR_DEVICE: return "FP8_ERR_DEVICE: a kernel reported an error (bounded wait ran out)";
+        case FP8_ERR_TOO_LARGE: return "FP8_ERR_TOO_LARGE: problem exceeds the fixed scratch of fp8_scaled_mm_noalloc";
         default: return "unknown fp8_status";
     }
 }
@@ -183,6 +212,41 @@ fp8_status fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, 
 fp8_status fp8_scaled_mm(const void *A, const void *B, const float *scale_a, const float *scale_b, int granularity,
                          int out_dtype, int64_t M, int64_t N, int64_t K, void *out, void *stream) {
     return fp8_scaled_mm_ex(A, B, scale_a, scale_b, granularity, out_dtype, M, N, K, out, stream, 0u);
+}
+
+fp8_status fp8_scaled_mm_noalloc(const void *A, const void *B, const float *scale_a, const float *scale_b,
+                                 int granularity, int out_dtype, int64_t M, int64_t N, int64_t K, void *out,
+                                 void *stream) {
+    if (M < 0 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > kI32Max) return FP8_ERR_INVALID_ARG;
+    if (granularity < 0 || granularity > 3) return FP8_ERR_INVALID_ARG;
+    if (out_dtype != FP8_OUT_BF16) return FP8_ERR_UNSUPPORTED;
+    if (M == 0) return FP8_OK;
+    if (!A || !B || !scale_a || !scale_b || !out) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(out) || !aligned4(scale_a) || !aligned4(scale_b))
+        return FP8_ERR_ALIGNMENT;
+    if (K % 16 != 0 || N % 8 != 0) return FP8_ERR_ALIGNMENT;
+    if (M > 16) return FP8_ERR_TOO_LARGE;
+
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    const fp8k::DecodePlan plan = fp8k::plan_decode(M, N, K, st->num_sms);
+    const size_t n_counters = fp8k::decode_counters_needed(plan);
+    if (n_counters > kNoAllocCounters || fp8k::decode_slot_floats(plan) > kNoAllocSlotFloats)
+        return FP8_ERR_TOO_LARGE;
+    void *scratch = nullptr;
+    if ((s = noalloc_scratch(&scratch)) != FP8_OK) return s;
+    fp8k::DecodeWorkspace ws;
+    ws.counters = static_cast<uint32_t *>(scratch);
+    ws.slots = reinterpret_cast<float *>(static_cast<unsigned char *>(scratch) + kNoAllocCounters * sizeof(uint32_t));
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // the counters must start at zero; the previous call may have been cut short
+    if (cudaMemsetAsync(ws.counters, 0, n_counters * sizeof(uint32_t), cs) != cudaSuccess) return FP8_ERR_CUDA;
+    CUtensorMap tw, ta;
+    if ((s = make_tmap_e4m3(&tw, B, N, K, fp8k::kDecodeRows)) != FP8_OK) return s;
+    if ((s = make_tmap_e4m3(&ta, A, M, K, static_cast<uint32_t>(plan.tok_pad))) != FP8_OK) return s;
+    return from_cuda(fp8k::launch_decode_gemm(tw, ta, scale_a, scale_b, granularity, M, N, K, out, st->err, plan,
+                                              ws, fp8k::LaunchOpts{}, cs));
 }
 
 fp8_status rmsnorm_quant_fp8(const void *x, const void *gamma, float eps, const float *scale, void *out, int64_t M,

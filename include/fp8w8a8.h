@@ -58,7 +58,8 @@ typedef enum {
     FP8_ERR_ALIGNMENT = 2,    /* pointer not 16-byte aligned, or K / N not a multiple of 16 / 8 */
     FP8_ERR_UNSUPPORTED = 3,  /* a valid request this library does not implement (e.g. out_dtype) */
     FP8_ERR_CUDA = 4,         /* a CUDA runtime / driver call or a kernel launch failed */
-    FP8_ERR_DEVICE = 5        /* a kernel reported an error through the device error word */
+    FP8_ERR_DEVICE = 5,       /* a kernel reported an error through the device error word */
+    FP8_ERR_TOO_LARGE = 6     /* the problem needs more scratch than fp8_scaled_mm_noalloc's fixed area */
 } fp8_status;
 
 /* Which scale element multiplies output y[m,n] ([P1] "What is owed", item 2,
@@ -129,6 +130,35 @@ typedef enum {
 fp8_status fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, const float *scale_b,
                             int granularity, int out_dtype, int64_t M, int64_t N, int64_t K, void *out,
                             void *stream, unsigned flags);
+
+/* fp8_scaled_mm_noalloc -- fp8_scaled_mm for callers that cannot allocate.
+ *
+ * The pages have no counterpart of this call; it exists for callers that may
+ * not call cudaMalloc at all: code running inside a memory pool or arena
+ * that must own every device allocation, hosts whose allocator is locked
+ * while a CUDA graph is being built, or embedders that forbid hidden
+ * allocations.  fp8_scaled_mm allocates its ~25 MB scratch on first use; this
+ * entry point instead uses a fixed scratch area compiled into the library (a
+ * file-scope device array of 6 MB + 64 KB that every GPU which loads the
+ * library holds until the process exits), and never calls cudaMalloc,
+ * cudaFree or any allocating routine.
+ *
+ * Arguments, layouts and results are those of fp8_scaled_mm (same kernel, so
+ * the same bytes).  Limits of the fixed area: M <= 16, at most 16384 output
+ * tiles of 128 rows (N <= 2,097,152), and at most 384 streaming CTAs (any
+ * GPU with up to 192 SMs); larger problems return FP8_ERR_TOO_LARGE without
+ * launching anything.
+ *
+ * The first call on a device looks up the device address of the scratch area
+ * for that device (cudaGetSymbolAddress), so make the first call on each
+ * device before capturing a CUDA graph.  Every call zeroes the area's arrival
+ * counters on `stream` before its kernel.  All calls share the one area and
+ * it keeps the last call's contents: calls that may run at the same time on
+ * the GPU (different streams, no ordering) race and give wrong results;
+ * order them.  Errors: those of fp8_scaled_mm, plus FP8_ERR_TOO_LARGE. */
+fp8_status fp8_scaled_mm_noalloc(const void *A, const void *B, const float *scale_a, const float *scale_b,
+                                 int granularity, int out_dtype, int64_t M, int64_t N, int64_t K, void *out,
+                                 void *stream);
 
 /* rmsnorm_quant_fp8 -- fused RMSNorm -> static per-tensor E4M3 quantisation,
  * one pass ("quantise once" per layer).
