@@ -113,6 +113,39 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+DECODE_KERNEL_SOURCES = ("fp8_w8a8_scaled_gb300/csrc/gemm_decode.cu", "fp8_w8a8_scaled_gb300/csrc/ptx.cuh")
+TRAFFIC_RECORD = "profiles/decode_gemm_qkv_10240x5120.md"
+
+
+def decode_kernel_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in DECODE_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per GEMM launch from the committed ncu summary, or None when
+    the summary is missing or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, TRAFFIC_RECORD)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.split(":", 1)[0] in ("traffic_bytes_per_launch", "kernel_source_digest"):
+                k, v = line.split(":", 1)
+                fields[k] = v.strip()
+    if fields.get("kernel_source_digest") != decode_kernel_digest():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 # ----------------------------------------------------------------------------- our arm
 
 class DecodeFusedStep:
@@ -264,7 +297,8 @@ def run_ours(args, rank, world, dist_barrier, dist_max):
                    "graph": f"{INNER} steps per CUDA graph replay"},
         "roofline": {"kernel": "decode_gemm_kernel (tcgen05 swap-AB, persistent stream-K)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": None,
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": recorded_traffic(),
+                     "traffic_source": TRAFFIC_RECORD,
                      "bytes_per_launch": gbytes, "us_per_launch": round(per_launch_ms * 1e3, 3)},
         "e2e": {"value": round(world * step_bytes() / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6)},
