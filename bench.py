@@ -230,6 +230,91 @@ def cpu_baseline_sample(budget_s=10.0):
                       f"{el:.1f} s wall"}
 
 
+PREFILL_SHAPES = [(m, n) for m in workloads.PREFILL_MS for n in workloads.PREFILL_NS]
+
+
+def fp8_dense_peak():
+    """FP8 dense tensor peak (TFLOP/s): the measured bf16 GEMM rate times the
+    nominal FP8 / bf16 ratio (4.5 / 2.25 PFLOP/s dense)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return 2.0 * float(p["bf16_tflops"]), "measured bf16 burst x 2 (nominal fp8/bf16 ratio)"
+    return 2.0 * 1900.0, "fallback bf16 1.9 PFLOP/s x 2 (nominal fp8/bf16 ratio)"
+
+
+def run_prefill(torch, fp8, device, dist_barrier, dist_max, seconds_per_shape=0.25):
+    """The prefill-chunk GEMMs (M in {2048, 8192} x N in {10240, 34816},
+    K = 5120, per-token x per-channel scales, bf16 out), each timed alone as a
+    CUDA graph of launches rotating over three weight copies (so inputs plus
+    outputs exceed L2), and the per-token activation quantisation of the same
+    chunks.  Returns the prefill object of the JSON line."""
+    K = K_HID
+    shapes, tot_flop, tot_ms = [], 0.0, 0.0
+    quant = []
+    launches = 0
+    for (M, N) in PREFILL_SHAPES:
+        x = workloads.device_bf16_normal(torch, (M, K), seed=500 + M, device=device)
+        A = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=device)
+        sa = torch.empty((M,), dtype=torch.float32, device=device)
+        Bs = [workloads.device_e4m3_codes(torch, (N, K), seed=600 + i, device=device).view(torch.float8_e4m3fn)
+              for i in range(3)]
+        sb = workloads.device_uniform_f32(torch, (N,), 0.5e-3, 2e-3, seed=700, device=device)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        fp8.quant_fp8_per_token(x, out=A, scale_out=sa)
+
+        def gemms():
+            for i in range(3):
+                fp8.fp8_scaled_mm(A, Bs[i], sa, sb, fp8.GRAN_PER_TOKEN_CHANNEL, out=Y)
+
+        def quants():
+            for _ in range(3):
+                fp8.quant_fp8_per_token(x, out=A, scale_out=sa)
+
+        flop = 2.0 * M * N * K
+        res = {}
+        for name, fn, per in (("gemm", gemms, 3), ("quant", quants, 3)):
+            s = torch.cuda.Stream(device=device)
+            s.wait_stream(torch.cuda.current_stream(device))
+            with torch.cuda.stream(s):
+                fn()
+            torch.cuda.current_stream(device).wait_stream(s)
+            torch.cuda.synchronize(device)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                fn()
+            for _ in range(3):
+                graph.replay()
+            torch.cuda.synchronize(device)
+            t = time_graph(torch, graph, 1, dist_barrier) / per
+            reps = max(3, int(seconds_per_shape * 1e3 / max(t * per, 1e-3)))
+            res[name] = dist_max(time_graph(torch, graph, reps, dist_barrier)) / (reps * per)
+            launches += reps * per
+        ms = res["gemm"]
+        shapes.append({"M": M, "N": N, "K": K, "ms": round(ms, 5), "tflops": round(flop / ms / 1e9, 1)})
+        quant.append({"M": M, "K": K, "us": round(res["quant"] * 1e3, 2),
+                      "tbps": round(3.0 * M * K / (res["quant"] * 1e-3) / 1e12, 3)})
+        tot_flop += flop
+        tot_ms += ms
+        del x, A, sa, Bs, sb, Y
+    peak, src = fp8_dense_peak()
+    achieved = tot_flop / tot_ms / 1e9
+    return {
+        "metric": "prefill FP8 GEMM TFLOP/s (M in {2048, 8192}, K 5120, N in {10240, 34816}, per-token x "
+                  "per-channel scales, bf16 out)",
+        "value": round(achieved, 1), "unit": "TFLOP/s", "shapes": shapes,
+        "roofline": {"kernel": "prefill_gemm_kernel (tcgen05 128x256 tiles, persistent)", "bound": "tensor",
+                     "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_source": src, "traffic": None},
+        "quant_per_token": quant,
+        "gpu_launches": launches,
+        "l2": "three weight copies rotated per graph (inputs + outputs > 129 MB L2)",
+        "data": "synthetic: device-random N(0,1) activations (quantised per token in the graph) and uniform "
+                "E4M3 weight codes; values do not change the tensor-core time",
+    }
+
+
 def run_ours(args, rank, world, dist_barrier, dist_max):
     import torch
     import fp8_w8a8_scaled_gb300 as fp8
@@ -305,6 +390,15 @@ def run_ours(args, rank, world, dist_barrier, dist_max):
         "gpu_launches": steps * 2 * len(MS),
         "clocks": clk,
     }
+    if not args.no_prefill:
+        clocks_p = ClockSampler(local)
+        clocks_p.start()
+        time.sleep(0.2)
+        out["prefill"] = run_prefill(torch, fp8, device, dist_barrier, dist_max)
+        out["prefill"]["clocks"] = clocks_p.stop()
+        err = fp8.get_device_error()
+        if err:
+            raise RuntimeError(f"device error word {err:#x}")
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_sample(args.cpu_seconds)
     return out
@@ -393,6 +487,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="wall-time budget of the oracle CPU baseline")
     ap.add_argument("--ref-seconds", type=float, default=60.0, help="wall-time budget of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-chunk GEMM measurement")
     ap.add_argument("--profile", metavar="M,N,K", help="run a small eager case for a profiler and exit")
     args = ap.parse_args()
     if args.profile:

@@ -165,7 +165,7 @@ int fp8_describe_dispatch(int64_t M, int64_t N, int64_t K, int granularity) {
     if (M < 0 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > kI32Max) return -1;
     if (granularity < 0 || granularity > 3) return -1;
     if (M == 0) return FP8_KERNEL_NONE;
-    return FP8_KERNEL_DECODE_SPLITK;
+    return M >= fp8k::kPrefillMinM ? FP8_KERNEL_PREFILL : FP8_KERNEL_DECODE_SPLITK;
 }
 
 int fp8_decode_ctas_for_sms(int64_t M, int64_t N, int64_t K, int num_sms) {
@@ -199,6 +199,15 @@ fp8_status fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, 
     fp8k::LaunchOpts opts;
     opts.pdl = (flags & FP8_FLAG_NO_PDL) == 0;
     opts.weights_static = (flags & FP8_FLAG_WEIGHTS_STATIC) != 0;
+    if (fp8_describe_dispatch(M, N, K, granularity) == FP8_KERNEL_PREFILL) {
+        const fp8k::PrefillPlan plan = fp8k::plan_prefill(M, N, K, st->num_sms);
+        if (static_cast<int64_t>(plan.m_tiles) * plan.n_tiles > kI32Max) return FP8_ERR_UNSUPPORTED;
+        CUtensorMap ta, tb;
+        if ((s = make_tmap_e4m3(&ta, A, M, K, fp8k::kPrefillBM)) != FP8_OK) return s;
+        if ((s = make_tmap_e4m3(&tb, B, N, K, fp8k::kPrefillBN)) != FP8_OK) return s;
+        return from_cuda(fp8k::launch_prefill_gemm(ta, tb, scale_a, scale_b, granularity, M, N, K, out, st->err,
+                                                   plan, opts, static_cast<cudaStream_t>(stream)));
+    }
     const fp8k::DecodePlan plan = fp8k::plan_decode(M, N, K, st->num_sms);
     fp8k::DecodeWorkspace ws;
     if ((s = decode_workspace(st, plan, &ws)) != FP8_OK) return s;

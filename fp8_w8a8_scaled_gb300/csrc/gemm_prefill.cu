@@ -1,0 +1,345 @@
+// gemm_prefill.cu -- FP8 W8A8 scaled GEMM for large M (prefill).
+//
+// y[m,n] = bf16( (sum_k A[m,k] * B[n,k]) * sa * sb ), A E4M3 [M,K] (tokens),
+// B E4M3 [N,K] (weights), per-tensor / per-token sa, per-tensor / per-channel sb.
+// Sources: "[Kernel] add Flashinfer cutedsl w4a16 linear" (vllm #53014), the
+// commit message on the large-M dequant + 16-bit GEMM dispatch (at prefill M
+// the GEMM is compute-bound, so a dense tensor-core tile wins there); "We emit
+// F32 where vLLM emits bf16 on the biggest prefill buffers ..." (vllm.cpp
+// #417), FINDING 1 (the prefill outputs are the largest activation buffers and
+// must be written as bf16, not F32).
+//
+// Design (GB300, sm_103a).  At prefill M every weight byte feeds >= 128 tokens
+// and the kernel is bound by the FP8 tensor-core rate.  One persistent CTA per
+// SM walks the 128-token x 256-channel output tiles t = blockIdx.x + i*gridDim.x
+// (token tile fastest, so the CTAs resident at one time share their weight
+// rows through L2 and the whole token matrix stays L2-resident):
+//   * warp 0 / lane 0 loads, per 128-byte k-block, the 128 x 128-byte token box
+//     and the 256 x 128-byte weight box with TMA (128-byte swizzle) into a ring
+//     of 48 KB shared-memory stages;
+//   * warp 1 / lane 0 issues four tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32)
+//     per k-block.  A tile's K range is cut into groups of kPrefillDrainKb
+//     k-blocks; each group accumulates from zero into one of two 256-column
+//     TMEM accumulators, so the MMAs of one group overlap the epilogue's work
+//     on the previous one;
+//   * warps 2..9 are the epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (one
+//     token row per thread) and half of the 256 columns, adds each group's
+//     partial sums into binary32 registers, and at the end of the tile applies
+//     the scales in binary32 ((acc * sa) * sb), rounds to bf16 and stores.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fp8k {
+namespace {
+
+constexpr int kPrefillThreads = 64 + 256;  // producer warp, MMA warp, 8 epilogue warps
+constexpr int kPrefillEpiWarps = 8;
+constexpr uint32_t kPrefillATile = kPrefillBM * kBlockK;  // 16 KB of tokens per stage
+constexpr uint32_t kPrefillBTile = kPrefillBN * kBlockK;  // 32 KB of weights per stage
+constexpr uint32_t kPrefillStageBytes = kPrefillATile + kPrefillBTile;
+constexpr uint32_t kPrefillTmemCols = 2 * kPrefillBN;  // two accumulators: all 512 columns
+constexpr uint32_t kPrefillIdesc = idesc_e4m3_f32(kPrefillBM, kPrefillBN);
+constexpr int kPrefillMaxStages = 4;
+// k-blocks (of 128) the tensor core accumulates in TMEM before the epilogue
+// adds the partial sum into fp32 registers (0 = a tile's whole K range in one
+// TMEM accumulation).  The tensor core's accumulation is less exact than
+// binary32 round-to-nearest over many MMAs: on prefill-chunk data (M 2048,
+// N 10240, K 5120) one accumulation over all 160 MMAs left 5 of 2.1e7 outputs
+// beyond the acceptance bound (max 1.25 of it), groups of 20 k-blocks reached
+// 0.87 of it and groups of 10 k-blocks 0.49 (bf16 rounding alone: 0.39), for
+// about 3% of the throughput of one accumulation.
+constexpr int kPrefillDrainKb = 10;
+
+struct PrefillArgs {
+    const float *scale_a;
+    const float *scale_b;
+    __nv_bfloat16 *out;
+    uint32_t *err;
+    int gran, M, N, kb_total, m_tiles, tiles, stages, drain_kb;
+};
+
+// Bounded wait of one thread; gives up at once once the CTA has given up.
+__device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, uint32_t *err, uint32_t code,
+                                        volatile uint32_t *abort) {
+    if (*abort) return false;
+    if (mbar_wait(bar, parity, err, code)) return true;
+    *abort = 1u;
+    return false;
+}
+
+// The same wait taken by lane 0 for the whole warp: the warp's control flow
+// stays uniform, which tcgen05.ld (a .sync.aligned instruction) requires.
+__device__ __forceinline__ bool pf_warp_wait(uint32_t bar, uint32_t parity, uint32_t *err, uint32_t code,
+                                             volatile uint32_t *abort, uint32_t lane) {
+    uint32_t ok = 0;
+    if (lane == 0) ok = pf_wait(bar, parity, err, code, abort) ? 1u : 0u;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat16 a = __float2bfloat16_rn(lo), b = __float2bfloat16_rn(hi);
+    return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+}
+
+__global__ void __launch_bounds__(kPrefillThreads, 1)
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                        const PrefillArgs args) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem_base, s_issued, s_consumed;
+    __shared__ volatile uint32_t s_abort;
+
+    const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int stages = args.stages;
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t bar0 = base + static_cast<uint32_t>(stages) * kPrefillStageBytes;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (stages + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * stages + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * stages + 2 + b); };
+    const uint32_t final_bar = bar0 + 8u * (2 * stages + 4);
+
+    const int kbt = args.kb_total, m_tiles = args.m_tiles, tiles = args.tiles, dkb = args.drain_kb;
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    uint32_t *const err = args.err;
+
+    if (tid == 0) {
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), kPrefillEpiWarps);  // one arrive per epilogue warp
+        }
+        mbar_init(final_bar, 1);
+        fence_mbar_init();
+        s_issued = 0;
+        s_consumed = 0;
+        s_abort = 0;
+    }
+    if (warp == 1) tmem_alloc(smem_u32(&s_tmem_base), kPrefillTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------------------- producer
+        grid_dependency_wait();  // the tokens (and possibly the weights) come from earlier kernels
+        uint32_t it = 0;
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int t = c; t < tiles && ok; t += G) {
+            const int m_tile = t % m_tiles, n_tile = t / m_tiles;
+            for (int kb = 0; kb < kbt; ++kb) {
+                if (!pf_wait(empty_bar(s), ph ^ 1u, err, kErrPrefillEmptyWait, &s_abort)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t stage = base + static_cast<uint32_t>(s) * kPrefillStageBytes;
+                mbar_arrive_expect_tx(full_bar(s), kPrefillStageBytes);
+                tma_load_2d(stage, &tmap_a, full_bar(s), kb * kBlockK, m_tile * kPrefillBM);
+                tma_load_2d(stage + kPrefillATile, &tmap_b, full_bar(s), kb * kBlockK, n_tile * kPrefillBN);
+                ++it;
+                if (++s == stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        s_issued = it;
+        grid_launch_dependents();
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------------------- MMA issuer
+        // Each tile's K range is cut into groups of drain_kb k-blocks; every
+        // group accumulates from zero into the next TMEM accumulator (two in
+        // rotation) and is handed to the epilogue, which adds it into fp32
+        // registers.
+        uint32_t it = 0;
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t dc = 0;  // groups issued so far (accumulator = dc & 1)
+        bool ok = true;
+        for (int t = c; t < tiles && ok; t += G) {
+            for (int kb0 = 0; kb0 < kbt && ok; kb0 += dkb, ++dc) {
+                const int acc = static_cast<int>(dc & 1u);
+                if (!pf_wait(tempty_bar(acc), ((dc >> 1) & 1u) ^ 1u, err, kErrPrefillAccumEmptyWait, &s_abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * kPrefillBN);
+                const int kb1 = min(kb0 + dkb, kbt);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!pf_wait(full_bar(s), ph, err, kErrPrefillFullWait, &s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t stage = base + static_cast<uint32_t>(s) * kPrefillStageBytes;
+                    const uint64_t da = sw128_kmajor_desc(stage), db = sw128_kmajor_desc(stage + kPrefillATile);
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / 32; ++kk)  // +32 bytes along K = +2 in the address field
+                        mma_e4m3(d, da + 2u * kk, db + 2u * kk, kPrefillIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    mma_commit(empty_bar(s));
+                    ++it;
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok) mma_commit(tfull_bar(acc));
+            }
+        }
+        s_consumed = it;
+        mma_commit(final_bar);  // arrives when every MMA issued above has completed
+    } else if (warp >= 2) {
+        // ---------------------------------------------------------------- epilogue
+        grid_dependency_wait();  // scales may come from the previous kernel; the output may be read by it
+        const uint32_t quarter = warp & 3u;
+        const int half = static_cast<int>(warp - 2) >> 2;
+        const int row = static_cast<int>(quarter * 32u + lane);
+        const bool sa_vec = (args.gran == 2 || args.gran == 3);
+        const bool sb_vec = (args.gran == 1 || args.gran == 2);
+        const float sa0 = __ldg(args.scale_a), sb0 = __ldg(args.scale_b);
+        const int M = args.M, N = args.N;
+        constexpr int kCols = kPrefillBN / 2;  // columns of one thread
+        uint32_t dc = 0;
+        bool ok = true;
+        for (int t = c; t < tiles && ok; t += G) {
+            float y[kCols];
+#pragma unroll
+            for (int j = 0; j < kCols; ++j) y[j] = 0.0f;
+            for (int kb0 = 0; kb0 < kbt; kb0 += dkb, ++dc) {
+                const int acc = static_cast<int>(dc & 1u);
+                if (!pf_warp_wait(tfull_bar(acc), (dc >> 1) & 1u, err, kErrPrefillAccumWait, &s_abort, lane)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tbase = tmem + ((quarter * 32u) << 16) +
+                                       static_cast<uint32_t>(acc * kPrefillBN + half * kCols);
+#pragma unroll
+                for (int j = 0; j < kCols; j += 32) {
+                    uint32_t v[32];
+                    tmem_ld16(tbase + static_cast<uint32_t>(j), *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld16(tbase + static_cast<uint32_t>(j + 16), *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) y[j + q] = __fadd_rn(y[j + q], __uint_as_float(v[q]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
+            }
+            if (!ok) break;
+            const int m_tile = t % m_tiles, n_tile = t / m_tiles;
+            const int m = m_tile * kPrefillBM + row;
+            if (m < M) {
+                const float sa = sa_vec ? __ldg(args.scale_a + m) : sa0;
+                const int nbase = n_tile * kPrefillBN + half * kCols;
+                __nv_bfloat16 *const yrow = args.out + static_cast<int64_t>(m) * N;
+#pragma unroll
+                for (int j = 0; j < kCols; j += 8) {
+                    const int n = nbase + j;
+                    if (n < N) {  // N % 8 == 0: a group of 8 columns is all in or all out
+                        uint32_t p[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float b0 = sb_vec ? __ldg(args.scale_b + n + 2 * q) : sb0;
+                            const float b1 = sb_vec ? __ldg(args.scale_b + n + 2 * q + 1) : sb0;
+                            p[q] = pack_bf16x2(__fmul_rn(__fmul_rn(y[j + 2 * q], sa), b0),
+                                               __fmul_rn(__fmul_rn(y[j + 2 * q + 1], sa), b1));
+                        }
+                        *reinterpret_cast<uint4 *>(yrow + n) = make_uint4(p[0], p[1], p[2], p[3]);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    }
+
+    // Every thread triggers only here, after the producer's dependency wait
+    // (the producer triggered once more right after its last load).
+    __syncthreads();
+    grid_launch_dependents();
+
+    if (tid == 0) {
+        // Loads issued but never consumed (only after a timeout): let them land
+        // before the CTA exits.
+        const uint32_t issued = s_issued, consumed = s_consumed;
+        for (uint32_t i = consumed; i < issued; ++i)
+            mbar_wait(full_bar(static_cast<int>(i % static_cast<uint32_t>(stages))),
+                      (i / static_cast<uint32_t>(stages)) & 1u, err, kErrPrefillFullWait);
+    }
+    if (warp == 1) {
+        mbar_wait(final_bar, 0, err, kErrPrefillAccumWait);  // every MMA has completed
+        tc_fence_after();
+        tmem_dealloc(tmem, kPrefillTmemCols);
+    }
+}
+
+}  // namespace
+
+// Shared memory of one CTA: alignment slack, the stages, the mbarriers
+// (full/empty per stage, full/empty per accumulator, one final), rounded up.
+static size_t prefill_smem_bytes(int stages) {
+    const size_t barriers = 8u * static_cast<size_t>(2 * stages + 5);
+    return 1024 + static_cast<size_t>(stages) * kPrefillStageBytes + ((barriers + 127) / 128) * 128;
+}
+
+PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms) {
+    PrefillPlan p{};
+    p.m_tiles = static_cast<int>((M + kPrefillBM - 1) / kPrefillBM);
+    p.n_tiles = static_cast<int>((N + kPrefillBN - 1) / kPrefillBN);
+    p.kb_total = static_cast<int>((K + kBlockK - 1) / kBlockK);
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    p.ctas = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    if (p.ctas < 1) p.ctas = 1;
+    p.stages = kPrefillMaxStages;
+    p.drain_kb = (kPrefillDrainKb > 0 && kPrefillDrainKb < p.kb_total) ? kPrefillDrainKb : p.kb_total;
+    p.smem_bytes = prefill_smem_bytes(p.stages);
+    return p;
+}
+
+cudaError_t launch_prefill_gemm(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b, const float *scale_a,
+                                const float *scale_b, int granularity, int64_t M, int64_t N, int64_t K, void *out,
+                                uint32_t *err, const PrefillPlan &plan, const LaunchOpts &opts,
+                                cudaStream_t stream) {
+    (void)K;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool attr_done[64] = {};  // benign race: the attribute call is idempotent
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(prefill_smem_bytes(kPrefillMaxStages)));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    PrefillArgs a;
+    a.scale_a = scale_a;
+    a.scale_b = scale_b;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.err = err;
+    a.gran = granularity;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.kb_total = plan.kb_total;
+    a.m_tiles = plan.m_tiles;
+    a.tiles = plan.m_tiles * plan.n_tiles;
+    a.stages = plan.stages;
+    a.drain_kb = plan.drain_kb;
+    return launch_with_opts(prefill_gemm_kernel, dim3(static_cast<unsigned>(plan.ctas)), dim3(kPrefillThreads),
+                            plan.smem_bytes, stream, opts, tmap_a, tmap_b, a);
+}
+
+}  // namespace fp8k

@@ -79,4 +79,26 @@ cudaError_t launch_decode_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tma
                                uint32_t *err, const DecodePlan &plan, const DecodeWorkspace &ws, const LaunchOpts &opts,
                                cudaStream_t stream);
 
+// ------------------------------------------------------------ prefill GEMM --
+
+// Tile geometry of the large-M kernel: 128 tokens (MMA M) x 256 output
+// channels (MMA N) per tile, 128-byte k-blocks.
+constexpr int kPrefillBM = 128;
+constexpr int kPrefillBN = 256;
+constexpr int64_t kPrefillMinM = 65;  // fp8_scaled_mm sends M >= this to the prefill kernel
+
+struct PrefillPlan {
+    int m_tiles, n_tiles, kb_total;
+    int ctas;       // persistent CTAs (one per SM at most)
+    int stages;
+    int drain_kb;   // k-blocks accumulated in TMEM before the epilogue folds them into registers
+    size_t smem_bytes;
+};
+
+PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms);
+
+cudaError_t launch_prefill_gemm(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b, const float *scale_a,
+                                const float *scale_b, int granularity, int64_t M, int64_t N, int64_t K, void *out,
+                                uint32_t *err, const PrefillPlan &plan, const LaunchOpts &opts, cudaStream_t stream);
+
 }  // namespace fp8k

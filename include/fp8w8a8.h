@@ -104,7 +104,11 @@ typedef enum {
  * y[m,n] = bf16_rne( fp32(fp32(acc[m,n] * sa) * sb) ) with acc the fp32
  * tensor-core accumulation of the exact E4M3 products.  Which kernel runs is a
  * pure function of (M, N, K, granularity), see fp8_describe_dispatch, so a
- * captured CUDA graph replays the same kernel the eager call would run.
+ * captured CUDA graph replays the same kernel the eager call would run:
+ * M <= 64 the weight-streaming decode kernel (uses the library's scratch
+ * area), M >= 65 the tensor-core tile kernel (uses no scratch).  For a fixed
+ * M the result is deterministic (bitwise the same on every run); on the tile
+ * kernel row m does not depend on the other rows of A.
  * Errors: FP8_ERR_INVALID_ARG, FP8_ERR_ALIGNMENT, FP8_ERR_UNSUPPORTED,
  * FP8_ERR_CUDA. */
 fp8_status fp8_scaled_mm(const void *A, const void *B, const float *scale_a, const float *scale_b,
@@ -213,6 +217,7 @@ const char *fp8_status_string(int status);
 /* Which kernel fp8_scaled_mm runs for this problem (an fp8_kernel_id), or -1
  * for arguments fp8_scaled_mm would reject.  Host-only, pure: it reads no
  * device state, so a caller can assert the kernel before capturing a graph.
+ * FP8_KERNEL_DECODE_SPLITK for 1 <= M <= 64, FP8_KERNEL_PREFILL for M >= 65.
  * Source: [P4] commit message: the M-vs-threshold branch is a pure function
  * of M so that a graph captured at a padded M freezes the branch eager
  * execution would take. */

@@ -65,6 +65,36 @@ def check_gemm(y_bits: np.ndarray, y64: np.ndarray, sab: np.ndarray, K: int, wha
     return worst, int(bad.size)
 
 
+def tc_accumulation_bound(abs_sum: np.ndarray, sab: np.ndarray, K: int) -> np.ndarray:
+    """Worst-case error of accumulating the K exact E4M3 products in binary32
+    on the tensor core, from the arithmetic alone: the sum is formed as
+    ceil(K/32) chunk sums added one after another into a binary32 accumulator,
+    each step (including the chunk's own reduction) off by at most one unit
+    in the last place of a partial sum whose magnitude is at most
+    sum_k |a_k * b_k|; so |error| <= (ceil(K/32) + 1) * 2^-23 * sum_k |a_k * b_k|,
+    times the scales.  `abs_sum` is sum_k |a_k * b_k| in code units."""
+    steps = -(-K // 32) + 1
+    return steps * 2.0 ** -23 * np.abs(sab) * abs_sum
+
+
+def check_gemm_tc(y_bits, y64, sab, K, abs_sum, what=""):
+    """For outputs of the large-M kernel on stress inputs (uniformly random
+    codes, outlier-free activations) whose partial sums are large next to the
+    acceptance bound's absolute term: asserts |y - ref| <= bound + the binary32
+    accumulation bound above.  Returns (max err / acceptance bound,
+    max err / (bound + accumulation bound))."""
+    y = bf16_bits_to_f64(y_bits)
+    err = np.abs(y - y64)
+    bound = gemm_bound(y64, sab, K)
+    total = bound + tc_accumulation_bound(abs_sum, sab, K)
+    assert not np.any(np.isnan(y[~np.isnan(y64)])), f"{what}: NaN in GPU output"
+    bad = ~(err <= total)
+    r_acc = float(np.max(err / np.where(bound > 0, bound, np.inf))) if err.size else 0.0
+    r_tot = float(np.max(err / np.where(total > 0, total, np.inf))) if err.size else 0.0
+    assert int(bad.sum()) == 0, f"{what}: {int(bad.sum())} outputs outside bound + accumulation bound ({r_tot:.3g})"
+    return r_acc, r_tot
+
+
 class Guarded:
     """A device buffer of `nbytes` with canary bands on both sides."""
 

@@ -114,6 +114,9 @@ def test_describe_dispatch_is_pure(L):
     assert L.fp8_describe_dispatch(4, 64, 64, 7) == -1
     for M in (1, 2, 4, 8, 16, 32, 64):
         assert L.fp8_describe_dispatch(M, 10240, 5120, 1) == 1
+    for M in (65, 128, 2048, 8192):
+        assert L.fp8_describe_dispatch(M, 10240, 5120, 1) == 2
+        assert L.fp8_describe_dispatch(M, 34816, 5120, 2) == 2
     # the same question twice gives the same answer (no hidden state)
     for M in (1, 33, 127, 128, 129, 2048, 8192):
         assert L.fp8_describe_dispatch(M, 10240, 5120, 2) == L.fp8_describe_dispatch(M, 10240, 5120, 2)

@@ -1,0 +1,136 @@
+"""GPU parity of the large-M (prefill) GEMM kernel against the CPU oracle:
+prefill-chunk data at the acceptance bound (ragged shapes and the largest
+workload shape), stress inputs (outlier-free activations, uniformly random
+codes) at the acceptance bound plus the binary32 accumulation bound, more
+tiles than SMs (each persistent CTA walks several tiles through both TMEM
+accumulators), every scale granularity, the decode/prefill dispatch
+boundary, and the invariants the kernel's fixed accumulation order gives
+(rerun, graph replay and row independence are bitwise)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from helpers import check_gemm, host_bits, scale_product, to_dev_bf16, to_dev_e4m3, to_dev_f32
+from test_gpu_gemm import full_check, quantised_operands, run_mm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp8():
+    import fp8_w8a8_scaled_gb300 as f
+    f.clear_device_error()
+    yield f
+    assert f.get_device_error() == 0
+
+
+# (M, N, K): ragged M (not a multiple of 128), ragged N (not a multiple of 256,
+# and N % 16 == 8 for a half 16-column chunk), ragged K (not a multiple of 128).
+SHAPES = [(65, 264, 400), (128, 256, 128), (300, 776, 1040), (257, 1288, 2064), (1000, 520, 5120)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("gran", [0, 1, 2, 3])
+def test_prefill_quantised_operands(fp8, orc, M, N, K, gran):
+    assert fp8.describe_dispatch(M, N, K, gran) == fp8.KERNEL_PREFILL
+    qa, qb, sa, sb, wa, wb, wsa, wsb = quantised_operands(fp8, orc, M, N, K, gran, 5000 + M + N + K + gran)
+    y = run_mm(fp8, qa, qb, sa, sb, gran)
+    full_check(orc, wa, wb, wsa, wsb, gran, y, f"prefill {M}x{N}x{K} gran {gran}", tc_bound=True)
+
+
+@pytest.mark.parametrize("M,N,K", [(65, 264, 400), (300, 776, 1040)])
+def test_prefill_random_codes(fp8, orc, M, N, K):
+    """Uniformly random codes (every E4M3 value, short K)."""
+    c = workloads.random_gemm(5100 + M + N + K, M, N, K, 2)
+    y = run_mm(fp8, to_dev_e4m3(c["A"]), to_dev_e4m3(c["B"]), to_dev_f32(c["sa"]), to_dev_f32(c["sb"]), 2)
+    full_check(orc, c["A"], c["B"], c["sa"], c["sb"], 2, y, f"codes {M}x{N}x{K}", tc_bound=True)
+
+
+def test_prefill_more_tiles_than_sms(fp8, orc):
+    """1024 x 8192 outputs = 256 tiles: each CTA runs two or more tiles, so
+    both accumulators and the ring phases wrap."""
+    M, N, K = 1024, 8192, 1024
+    qa, qb, sa, sb, wa, wb, wsa, wsb = quantised_operands(fp8, orc, M, N, K, 2, 5200)
+    y = run_mm(fp8, qa, qb, sa, sb, 2)
+    full_check(orc, wa, wb, wsa, wsb, 2, y, "1024x8192x1024", tc_bound=True)
+
+
+@pytest.mark.parametrize("M", [64, 65])
+def test_dispatch_boundary(fp8, orc, M):
+    """The last decode M and the first prefill M give results within the bound
+    on the same operands."""
+    N, K = 1032, 2064
+    want = fp8.KERNEL_DECODE_SPLITK if M <= 64 else fp8.KERNEL_PREFILL
+    assert fp8.describe_dispatch(M, N, K, 2) == want
+    qa, qb, sa, sb, wa, wb, wsa, wsb = quantised_operands(fp8, orc, M, N, K, 2, 5300)
+    y = run_mm(fp8, qa, qb, sa, sb, 2)
+    full_check(orc, wa, wb, wsa, wsb, 2, y, f"boundary M={M}", tc_bound=M > 64)
+
+
+@pytest.mark.parametrize("M,N", [(1000, 1288), (257, 10240)])
+def test_prefill_chunk_data_full(fp8, orc, M, N):
+    """Prefill-chunk data (per-token activations with 1% outliers x20,
+    per-channel weights, K = 5120) on ragged shapes, every output against the
+    oracle at the acceptance bound."""
+    d = workloads.prefill(seed=2, m=M, n=N)
+    qa, sa = fp8.quant_fp8_per_token(to_dev_bf16(d["x"]))
+    qb, sb = fp8.quant_fp8_per_token(to_dev_bf16(d["w"]))
+    wa, wsa = orc.quant_per_token(d["x"])
+    wb, wsb = orc.quant_per_token(d["w"])
+    assert np.array_equal(host_bits(qa), wa) and np.array_equal(host_bits(sa), wsa)
+    assert np.array_equal(host_bits(qb), wb) and np.array_equal(host_bits(sb), wsb)
+    y = run_mm(fp8, qa, qb, sa, sb, 2)
+    worst, _ = full_check(orc, wa, wb, wsa, wsb, 2, y, f"prefill chunk {M}x{N}")
+    print(f"prefill chunk {M}x{N}: max err/bound {worst:.4f}")
+
+
+@pytest.mark.parametrize("M,N", [(8192, 34816)])
+def test_prefill_gate_up_sampled(fp8, orc, M, N):
+    """The largest prefill shape: per-token activations (1% outliers x20) into
+    the merged gate_up weight, per-channel scales; 3 full rows plus 20000
+    random outputs against the oracle."""
+    d = workloads.prefill(seed=1, m=M, n=N)
+    qa, sa = fp8.quant_fp8_per_token(to_dev_bf16(d["x"]))
+    qb, sb = fp8.quant_fp8_per_token(to_dev_bf16(d["w"]))
+    wa, wsa = orc.quant_per_token(d["x"])
+    wb, wsb = orc.quant_per_token(d["w"])
+    assert np.array_equal(host_bits(sa), wsa) and np.array_equal(host_bits(sb), wsb)
+    y = fp8.fp8_scaled_mm(qa, qb, sa, sb, 2)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(8)
+    rows = np.concatenate([np.repeat([0, M // 2 + 1, M - 1], N), g.integers(0, M, 20000)])
+    cols = np.concatenate([np.tile(np.arange(N), 3), g.integers(0, N, 20000)])
+    yb = host_bits(y[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()])
+    y64 = orc.scaled_mm_points(wa, wb, wsa, wsb, 2, rows, cols)
+    worst, _ = check_gemm(yb, y64, scale_product(wsa, wsb, 2, rows, cols), 5120, f"prefill {M}x{N}")
+    print(f"prefill {M}x{N}: max err/bound {worst:.4f}")
+
+
+def test_prefill_invariants(fp8):
+    """Rerun, CUDA-graph replay and a row computed inside a larger M are all
+    bitwise equal: each output is accumulated over K in one fixed order by one
+    CTA whatever M is."""
+    M, N, K = 300, 1288, 2064
+    c = workloads.random_gemm(5400, 1000, N, K, 2)
+    A_big, B = to_dev_e4m3(c["A"]), to_dev_e4m3(c["B"])
+    sa_big, sb = to_dev_f32(c["sa"]), to_dev_f32(c["sb"])
+    A, sa = A_big[:M].contiguous(), sa_big[:M].contiguous()
+    y1 = run_mm(fp8, A, B, sa, sb, 2)
+    y2 = run_mm(fp8, A, B, sa, sb, 2)
+    assert np.array_equal(y1, y2)
+    big = run_mm(fp8, A_big, B, sa_big, sb, 2)
+    assert np.array_equal(big[:M], y1)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fp8.fp8_scaled_mm(A, B, sa, sb, 2, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fp8.fp8_scaled_mm(A, B, sa, sb, 2, out=out)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(out), y1)
