@@ -23,16 +23,20 @@
 //     128-row A operand and the tokens (padded to 16/32/64) as the N side
 //     ("swap-AB").  Each k-block is accumulated from zero into one of several
 //     TMEM buffers; tcgen05.commit frees the stage and hands the buffer on;
-//   * 4 or 8 drain warps read each k-block's fp32 partial out of TMEM
+//   * 4 drain warps (8 for the 64-token tile) read each k-block's fp32 partial out of TMEM
 //     while later k-blocks are multiplied, and fold it into a TwoSum (hi, lo)
 //     register pair: the sum over k-blocks is exact to ~2^-48 relative, so the
 //     only roundings left are the tensor core's inside one 128-wide k-block.
 // When a tile's K range ends inside the CTA, the drain warps either store the
 // tile (scales in binary32, then bf16) or, if other CTAs hold the rest of the
-// tile's K range, write their (hi, lo) pairs to a workspace slot and count
-// in on the tile's arrival counter; the CTA that arrives last sums all slots in
-// k order (so the result does not depend on arrival order), stores the tile
-// and resets the counter.  No CTA ever waits for another.
+// tile's K range, write their part (hi + lo, rounded once to binary32) to a
+// workspace slot and count in on the tile's arrival counter (a barrier, then
+// one thread's release fence and atomic add); the CTA that arrives last
+// acquires, sums all slots in k order (so the result does not depend on
+// arrival order), stores the tile and resets the counter.  Which CTAs share
+// the first and last tile of a CTA's range, and where their slots are, is
+// worked out while the first loads are in flight.  No CTA ever waits for
+// another.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -47,11 +51,13 @@ constexpr uint32_t kWTileBytes = kDecodeRows * kBlockK;  // 16 KB of weights per
 
 template <int TOK>
 struct DecodeCfg {
-    static constexpr int kDrainGroups = TOK <= 16 ? 1 : 2;  // warpgroups that drain TMEM
-    static constexpr int kCols = TOK / kDrainGroups;               // token columns per drain thread
+    // warpgroups that drain TMEM: one for the 16- and 32-token tiles (up to 32
+    // token columns per thread: fewer, fatter threads keep the 32-token tile's
+    // drain free of register spills), two for the 64-token tile
+    static constexpr int kDrainGroups = TOK <= 32 ? 1 : 2;
+    static constexpr int kCols = TOK / kDrainGroups;  // token columns per drain thread
     static constexpr int kDrainThreads = 128 * kDrainGroups;
     static constexpr int kThreads = 64 + kDrainThreads;
-    // two CTAs of this kernel plus one of the next (programmatic launch) per SM
     // two CTAs of this kernel plus one of the next (programmatic launch) per SM
     // for the 16-token tile; two per SM for the larger tiles
     static constexpr int kMinBlocks = TOK <= 16 ? 3 : 2;
@@ -80,6 +86,7 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthread
 // or below this bound (a fixup reads one slot per sharing CTA at once).
 constexpr int kMaxFixupSegs = 8;
 
+
 struct DecodeArgs {
     const float *scale_a;
     const float *scale_b;
@@ -102,6 +109,58 @@ __device__ __forceinline__ bool cta_wait(uint32_t bar, uint32_t parity, uint32_t
     return false;
 }
 
+// The last-arriving CTA's sum of a tile's K-range parts: every valid entry
+// ([token column][weight row] of the tile) summed over the parts in k order
+// (TwoSum), scaled, rounded to bf16 and stored.  Thread dt of NT owns VEC
+// float4 groups of entries per round, and all SEGS x VEC loads of a round are
+// issued before any is used.
+template <int SEGS, int VEC, int NT>
+__device__ __forceinline__ void fixup_sum(const DecodeArgs &args, const int64_t *slot, int nseg, int entries, int dt,
+                                          int n_tile, int m0, bool sa_vec, bool sb_vec, float sa0, float sb0) {
+    for (int e0 = 4 * VEC * dt; e0 < entries; e0 += 4 * VEC * NT) {
+        float sa_e[4 * VEC], sb_e[4 * VEC];  // the scales, requested before the slots
+#pragma unroll
+        for (int q = 0; q < 4 * VEC; ++q) {
+            const int e = min(e0 + q, entries - 1);
+            const int m = e / kDecodeRows, nn = n_tile * kDecodeRows + (e % kDecodeRows);
+            sa_e[q] = sa_vec ? __ldg(args.scale_a + m0 + m) : sa0;
+            sb_e[q] = (sb_vec && nn < args.N) ? __ldg(args.scale_b + nn) : sb0;
+        }
+        float4 v[SEGS][VEC];
+#pragma unroll
+        for (int j = 0; j < SEGS; ++j)
+#pragma unroll
+            for (int c = 0; c < VEC; ++c)
+                if (j < nseg && e0 + 4 * c < entries)
+                    v[j][c] = __ldcg(reinterpret_cast<const float4 *>(args.slots + slot[j] + e0 + 4 * c));
+        float h[4 * VEC], l[4 * VEC];
+#pragma unroll
+        for (int q = 0; q < 4 * VEC; ++q) h[q] = l[q] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < SEGS; ++j) {
+            if (j < nseg) {
+#pragma unroll
+                for (int c = 0; c < VEC; ++c) {
+                    if (e0 + 4 * c < entries) {
+                        two_sum_acc(h[4 * c + 0], l[4 * c + 0], v[j][c].x);
+                        two_sum_acc(h[4 * c + 1], l[4 * c + 1], v[j][c].y);
+                        two_sum_acc(h[4 * c + 2], l[4 * c + 2], v[j][c].z);
+                        two_sum_acc(h[4 * c + 3], l[4 * c + 3], v[j][c].w);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4 * VEC; ++q) {
+            const int e = e0 + q;
+            const int m = e / kDecodeRows, nn = n_tile * kDecodeRows + (e % kDecodeRows);
+            if (e < entries && nn < args.N)
+                args.out[static_cast<int64_t>(m0 + m) * args.N + nn] =
+                    __float2bfloat16_rn(__fmul_rn(__fmul_rn(__fadd_rn(h[q], l[q]), sa_e[q]), sb_e[q]));
+        }
+    }
+}
+
 template <int TOK>
 __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCfg<TOK>::kMaxRegs)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
@@ -111,7 +170,10 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
     constexpr int kSlotElems = TOK * kDecodeRows;  // fp32 entries of one partial slot
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t s_tmem_base, s_issued, s_consumed, s_last;
-    __shared__ int64_t s_slot[kMaxFixupSegs];  // slot offsets (fp32 entries) of a tile's K-range parts
+    // slot offsets (fp32 entries) of the K-range parts of this CTA's first and
+    // last tile (the only tiles it can share with other CTAs), and their counts
+    __shared__ int64_t s_slot[2][kMaxFixupSegs];
+    __shared__ int s_nseg[2];
     __shared__ volatile uint32_t s_abort;
 
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -228,6 +290,21 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
         const bool sb_vec = (args.gran == 1 || args.gran == 2);
         const float sa0 = __ldg(args.scale_a), sb0 = __ldg(args.scale_b);
         const int t_first_me = static_cast<int>(u0 / kbt);
+        if (tid == 64 && iters > 0) {
+            // Which CTAs hold the other parts of this CTA's first and last tile
+            // and where their partial sums go, worked out while the first
+            // loads are in flight.
+            for (int w = 0; w < 2; ++w) {
+                const int64_t t = (w == 0 ? u0 : u1 - 1) / kbt, tile_u0 = t * kbt;
+                const int64_t c_first = unit_owner(tile_u0, U, G), c_last = unit_owner(tile_u0 + kbt - 1, U, G);
+                const int nseg = static_cast<int>(c_last - c_first + 1);
+                s_nseg[w] = nseg;
+                for (int j = 0; j < kMaxFixupSegs && j < nseg; ++j) {
+                    const int64_t cc = c_first + j;
+                    s_slot[w][j] = (2 * cc + (t == unit_begin(cc, U, G) / kbt ? 0 : 1)) * kSlotElems;
+                }
+            }
+        }
         float hi[Cfg::kCols], lo[Cfg::kCols];
 #pragma unroll
         for (int c = 0; c < Cfg::kCols; ++c) hi[c] = lo[c] = 0.0f;
@@ -273,28 +350,26 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
 #pragma unroll
                 for (int c = 0; c < Cfg::kCols; ++c)
                     if (col0 + c < mt) mine[(col0 + c) * kDecodeRows + row] = __fadd_rn(hi[c], lo[c]);
-                __threadfence();
+                // Arrival: the barrier orders every drain thread's slot writes
+                // before tid 64's release fence and count (the usual
+                // barrier + single-thread release pattern); the last of the
+                // tile's parts to arrive acquires and sums them all.
                 named_barrier_sync(1, Cfg::kDrainThreads);
+                const int w = (t == t_first_me) ? 0 : 1;
                 if (tid == 64) {
-                    const int64_t c_first = unit_owner(tile_u0, U, G), c_last = unit_owner(tile_u0 + kbt - 1, U, G);
-                    const int64_t nseg = c_last - c_first + 1;
+                    const int nseg = s_nseg[w];
+                    __threadfence();
                     const bool last = atomicAdd(args.counters + t, 1u) == static_cast<uint32_t>(nseg - 1);
+                    if (last) __threadfence();
                     s_last = last ? static_cast<uint32_t>(nseg) : 0u;
-                    if (last) {
-                        for (int j = 0; j < kMaxFixupSegs && j < nseg; ++j) {
-                            const int64_t cc = c_first + j;
-                            s_slot[j] = (2 * cc + (t == unit_begin(cc, U, G) / kbt ? 0 : 1)) * kSlotElems;
-                        }
-                    }
                 }
                 named_barrier_sync(1, Cfg::kDrainThreads);
                 if (s_last != 0u) {
                     // Last arrival: sum the tile over its K range in k order (this
                     // CTA's own part is read back from its slot like the others).
                     // The drain threads switch to a flat ownership of the tile's
-                    // valid entries, four per thread per round, so that every slot
-                    // load of a round is in flight at once.
-                    __threadfence();
+                    // valid entries, 4 * kVec per thread per round, so that every
+                    // slot load of a round is in flight at once.
                     int nseg = static_cast<int>(s_last);
                     if (nseg > kMaxFixupSegs) {  // the planner keeps this from happening
                         if (tid == 64) atomicOr(err, kErrDecodeFixup);
@@ -302,33 +377,8 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
                     }
                     const int entries = mt * kDecodeRows;  // [col][row], valid token columns only
                     const int dt = static_cast<int>(tid) - 64;
-                    for (int e0 = 4 * dt; e0 < entries; e0 += 4 * Cfg::kDrainThreads) {
-                        float4 v[kMaxFixupSegs];
-#pragma unroll
-                        for (int j = 0; j < kMaxFixupSegs; ++j)
-                            if (j < nseg) v[j] = __ldcg(reinterpret_cast<const float4 *>(args.slots + s_slot[j] + e0));
-                        float h[4] = {0.0f, 0.0f, 0.0f, 0.0f}, l[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                        for (int j = 0; j < kMaxFixupSegs; ++j) {
-                            if (j < nseg) {
-                                two_sum_acc(h[0], l[0], v[j].x);
-                                two_sum_acc(h[1], l[1], v[j].y);
-                                two_sum_acc(h[2], l[2], v[j].z);
-                                two_sum_acc(h[3], l[3], v[j].w);
-                            }
-                        }
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int e = e0 + q;
-                            const int m = e / kDecodeRows, nn = n_tile * kDecodeRows + (e % kDecodeRows);
-                            if (e < entries && nn < args.N) {
-                                const float sa = sa_vec ? __ldg(args.scale_a + m0 + m) : sa0;
-                                const float sb = sb_vec ? __ldg(args.scale_b + nn) : sb0;
-                                args.out[static_cast<int64_t>(m0 + m) * args.N + nn] =
-                                    __float2bfloat16_rn(__fmul_rn(__fmul_rn(__fadd_rn(h[q], l[q]), sa), sb));
-                            }
-                        }
-                    }
+                    fixup_sum<kMaxFixupSegs, 1, Cfg::kDrainThreads>(args, s_slot[w], nseg, entries, dt, n_tile, m0,
+                                                                     sa_vec, sb_vec, sa0, sb0);
                     if (tid == 64) args.counters[t] = 0u;  // ready for the next launch
                 }
             }
