@@ -315,6 +315,140 @@ def run_prefill(torch, fp8, device, dist_barrier, dist_max, seconds_per_shape=0.
     }
 
 
+def gemm_bytes_gran(M, N, K, per_token):
+    """Algorithmic bytes of one GEMM whose activation scale is per token
+    (M floats) or per tensor (one float); per-channel weight scales."""
+    return N * K + M * K + 2 * M * N + 4 * N + (4 * M if per_token else 4)
+
+
+def quant_bytes(M, K):
+    """Per-token quantisation: bf16 in, E4M3 out, one f32 scale per row."""
+    return 2 * M * K + M * K + 4 * M
+
+
+def graph_of(torch, device, fn, inner):
+    s = torch.cuda.Stream(device=device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        fn(0)
+    torch.cuda.current_stream(device).wait_stream(s)
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(inner):
+            fn(i)
+    return graph
+
+
+def run_gate_up(torch, fp8, device, dist_barrier, dist_max, reps=40):
+    """Merged gate_up decode GEMM (N 34816, K 5120, per-channel weight scales,
+    per-tensor activation scale) at M in {1, 8, 32, 64}: 20 launches per graph
+    alternating two 178 MB weights (inputs > L2)."""
+    N, K = workloads.GATE_UP_N, K_HID
+    W = [workloads.device_e4m3_codes(torch, (N, K), seed=800 + i, device=device).view(torch.float8_e4m3fn)
+         for i in range(2)]
+    sb = workloads.device_uniform_f32(torch, (N,), 0.5e-3, 2e-3, seed=802, device=device)
+    s_a = torch.tensor([float(workloads.STATIC_INPUT_SCALE)], dtype=torch.float32, device=device)
+    peak, _ = measured_peaks()
+    rows, launches = [], 0
+    for M in workloads.GATE_UP_MS:
+        A = workloads.device_e4m3_codes(torch, (M, K), seed=803, device=device).view(torch.float8_e4m3fn)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        g = graph_of(torch, device, lambda i: fp8.fp8_scaled_mm(A, W[i % 2], s_a, sb, fp8.GRAN_PER_CHANNEL, out=Y,
+                                                                 flags=fp8.FLAG_WEIGHTS_STATIC), 20)
+        for _ in range(3):
+            g.replay()
+        us = dist_max(time_graph(torch, g, reps, dist_barrier)) * 1e3 / (20 * reps)
+        launches += 20 * reps
+        b = gemm_bytes_gran(M, N, K, False)
+        gbps = b / (us * 1e-6) / 1e9
+        rows.append({"M": M, "us": round(us, 3), "GBps": round(gbps, 1), "frac": round(gbps / peak, 4),
+                     "kernel": "decode" if fp8.describe_dispatch(M, N, K, 1) == fp8.KERNEL_DECODE_SPLITK else "prefill"})
+    del W
+    return {"workload": "merged gate_up decode GEMM N=34816 K=5120, per-channel weight scales, per-tensor "
+                        "activation scale, bf16 out; two 178 MB weights alternated", "unit": "GB/s",
+            "peak": peak, "per_M": rows, "gpu_launches": launches}
+
+
+def run_decode_step(torch, fp8, device, dist_barrier, dist_max, reps=20):
+    """Synthetic 64-layer decode step at M in {1, 4, 8}: per layer RMSNorm ->
+    static quant -> QKV (10240x5120), per-token quant of an [M, 8192] stub ->
+    O (5120x8192), gate_up (34816x5120) on the same normalised input, per-token
+    quant of an [M, 17408] stub -> down (5120x17408); distinct weights per
+    layer (23.15 GB), the whole step one CUDA graph."""
+    L_ = workloads.STEP_LAYERS
+    shapes = workloads.LayerShapes()
+    K = K_HID
+    Wl = []
+    for layer in range(L_):
+        ws = []
+        for j, (n, k) in enumerate((shapes.qkv, shapes.o, shapes.gate_up, shapes.down)):
+            w = workloads.device_e4m3_codes(torch, (n, k), seed=10000 + 8 * layer + j, device=device)
+            ws.append((w.view(torch.float8_e4m3fn),
+                       workloads.device_uniform_f32(torch, (n,), 0.5e-3, 2e-3, seed=20000 + 8 * layer + j,
+                                                    device=device)))
+        Wl.append(ws)
+    gamma = workloads.device_bf16_normal(torch, (K,), seed=30000, device=device, std=0.1)
+    s_a = torch.tensor([float(workloads.STATIC_INPUT_SCALE)], dtype=torch.float32, device=device)
+    peak, _ = measured_peaks()
+    rows, launches = [], 0
+    for M in workloads.STEP_MS:
+        x = workloads.device_bf16_normal(torch, (M, K), seed=30001, device=device)
+        o_in = workloads.device_bf16_normal(torch, (M, workloads.O_K), seed=30002, device=device)
+        d_in = workloads.device_bf16_normal(torch, (M, workloads.DOWN_K), seed=30003, device=device)
+        a = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=device)
+        a_o = torch.empty((M, workloads.O_K), dtype=torch.float8_e4m3fn, device=device)
+        a_d = torch.empty((M, workloads.DOWN_K), dtype=torch.float8_e4m3fn, device=device)
+        s_o = torch.empty((M,), dtype=torch.float32, device=device)
+        s_d = torch.empty((M,), dtype=torch.float32, device=device)
+        y = [torch.empty((M, n), dtype=torch.bfloat16, device=device)
+             for (n, _) in (shapes.qkv, shapes.o, shapes.gate_up, shapes.down)]
+        st = fp8.FLAG_WEIGHTS_STATIC
+
+        def step(_i):
+            for ws in Wl:
+                fp8.rmsnorm_quant_fp8(x, gamma, workloads.RMS_EPS, s_a, out=a)
+                fp8.fp8_scaled_mm(a, ws[0][0], s_a, ws[0][1], fp8.GRAN_PER_CHANNEL, out=y[0], flags=st)
+                fp8.quant_fp8_per_token(o_in, out=a_o, scale_out=s_o)
+                fp8.fp8_scaled_mm(a_o, ws[1][0], s_o, ws[1][1], fp8.GRAN_PER_TOKEN_CHANNEL, out=y[1], flags=st)
+                fp8.fp8_scaled_mm(a, ws[2][0], s_a, ws[2][1], fp8.GRAN_PER_CHANNEL, out=y[2], flags=st)
+                fp8.quant_fp8_per_token(d_in, out=a_d, scale_out=s_d)
+                fp8.fp8_scaled_mm(a_d, ws[3][0], s_d, ws[3][1], fp8.GRAN_PER_TOKEN_CHANNEL, out=y[3], flags=st)
+
+        g = graph_of(torch, device, step, 1)
+        for _ in range(3):
+            g.replay()
+        ms = dist_max(time_graph(torch, g, reps, dist_barrier)) / reps
+        launches += reps * 7 * L_
+        layer_bytes = (norm_bytes(M) + gemm_bytes_gran(M, *shapes.qkv, False)
+                       + quant_bytes(M, workloads.O_K) + gemm_bytes_gran(M, *shapes.o, True)
+                       + gemm_bytes_gran(M, *shapes.gate_up, False)
+                       + quant_bytes(M, workloads.DOWN_K) + gemm_bytes_gran(M, *shapes.down, True))
+        tbps = L_ * layer_bytes / (ms * 1e-3) / 1e12
+        rows.append({"M": M, "ms_per_step": round(ms, 4), "bytes_per_step": L_ * layer_bytes, "TBps": round(tbps, 4),
+                     "frac": round(tbps * 1e3 / peak, 4)})
+    del Wl
+    torch.cuda.empty_cache()
+    return {"workload": "64-layer synthetic decode step (norm-quant, QKV, per-token quant, O, gate_up, per-token "
+                        "quant, down per layer; 361.76 MB of distinct weights per layer), one CUDA graph",
+            "unit": "TB/s", "peak_GBps": peak, "per_M": rows, "gpu_launches": launches}
+
+
+def run_tiny(torch, fp8, device, dist_barrier, dist_max, reps=200):
+    """The tiny GEMM (M 4, K 256, N 512, per-tensor scales): microseconds per
+    call inside a CUDA graph of 20 calls."""
+    A = workloads.device_e4m3_codes(torch, (4, 256), seed=900, device=device).view(torch.float8_e4m3fn)
+    B = workloads.device_e4m3_codes(torch, (512, 256), seed=901, device=device).view(torch.float8_e4m3fn)
+    s = torch.tensor([1e-2], dtype=torch.float32, device=device)
+    Y = torch.empty((4, 512), dtype=torch.bfloat16, device=device)
+    g = graph_of(torch, device, lambda i: fp8.fp8_scaled_mm(A, B, s, s, fp8.GRAN_PER_TENSOR, out=Y), 20)
+    for _ in range(3):
+        g.replay()
+    us = dist_max(time_graph(torch, g, reps, dist_barrier)) * 1e3 / (20 * reps)
+    return {"workload": "tiny GEMM M=4 K=256 N=512 per-tensor", "us_per_call": round(us, 3),
+            "gpu_launches": 20 * reps}
+
+
 def run_ours(args, rank, world, dist_barrier, dist_max):
     import torch
     import fp8_w8a8_scaled_gb300 as fp8
@@ -396,6 +530,13 @@ def run_ours(args, rank, world, dist_barrier, dist_max):
         time.sleep(0.2)
         out["prefill"] = run_prefill(torch, fp8, device, dist_barrier, dist_max)
         out["prefill"]["clocks"] = clocks_p.stop()
+        err = fp8.get_device_error()
+        if err:
+            raise RuntimeError(f"device error word {err:#x}")
+    if not args.no_extras:
+        out["gate_up"] = run_gate_up(torch, fp8, device, dist_barrier, dist_max)
+        out["decode_step"] = run_decode_step(torch, fp8, device, dist_barrier, dist_max)
+        out["tiny"] = run_tiny(torch, fp8, device, dist_barrier, dist_max)
         err = fp8.get_device_error()
         if err:
             raise RuntimeError(f"device error word {err:#x}")
@@ -488,6 +629,8 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=60.0, help="wall-time budget of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-chunk GEMM measurement")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the gate_up decode, 64-layer decode step and tiny GEMM measurements")
     ap.add_argument("--profile", metavar="M,N,K", help="run a small eager case for a profiler and exit")
     args = ap.parse_args()
     if args.profile:
