@@ -12,7 +12,7 @@
 // Design (GB300, sm_103a).  At decode M every weight byte is used M times, so
 // the kernel is bound by streaming B from HBM once, and every SM must stream
 // its equal share all the time.  The work is cut into units of one output tile
-// (128 weight rows x up to 64 tokens) by one 128-wide k-block; a persistent
+// (128 weight rows x up to 32 tokens) by one 128-wide k-block; a persistent
 // grid of two CTAs per SM gives CTA c the contiguous units
 // [c*U/G, (c+1)*U/G) ("stream-K"), so all CTAs stream the same number of bytes
 // whatever the shape.  Inside a CTA:
@@ -20,10 +20,10 @@
 //     matching token boxes with TMA into a ring of shared-memory stages
 //     (128-byte swizzle), L2 evict-first for the once-read weights;
 //   * warp 1 / lane 0 issues tcgen05.mma kind::f8f6f4 with the WEIGHTS as the
-//     128-row A operand and the tokens (padded to 16/32/64) as the N side
+//     128-row A operand and the tokens (padded to 16/32) as the N side
 //     ("swap-AB").  Each k-block is accumulated from zero into one of several
 //     TMEM buffers; tcgen05.commit frees the stage and hands the buffer on;
-//   * 4 drain warps (8 for the 64-token tile) read each k-block's fp32 partial out of TMEM
+//   * 4 drain warps read each k-block's fp32 partial out of TMEM
 //     while later k-blocks are multiplied, and fold it into a TwoSum (hi, lo)
 //     register pair: the sum over k-blocks is exact to ~2^-48 relative, so the
 //     only roundings left are the tensor core's inside one 128-wide k-block.
@@ -51,10 +51,9 @@ constexpr uint32_t kWTileBytes = kDecodeRows * kBlockK;  // 16 KB of weights per
 
 template <int TOK>
 struct DecodeCfg {
-    // warpgroups that drain TMEM: one for the 16- and 32-token tiles (up to 32
-    // token columns per thread: fewer, fatter threads keep the 32-token tile's
-    // drain free of register spills), two for the 64-token tile
-    static constexpr int kDrainGroups = TOK <= 32 ? 1 : 2;
+    // one warpgroup drains TMEM (up to 32 token columns per thread: fewer,
+    // fatter threads keep the 32-token tile's drain free of register spills)
+    static constexpr int kDrainGroups = 1;
     static constexpr int kCols = TOK / kDrainGroups;  // token columns per drain thread
     static constexpr int kDrainThreads = 128 * kDrainGroups;
     static constexpr int kThreads = 64 + kDrainThreads;
@@ -450,7 +449,7 @@ static size_t decode_smem_bytes(int tok, int stages) {
 
 DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, int num_sms) {
     DecodePlan p{};
-    p.tok_pad = M <= 16 ? 16 : M <= 32 ? 32 : 64;
+    p.tok_pad = M <= 16 ? 16 : 32;
     p.stages = 3;  // ~55-75 KB: two CTAs of this kernel and one of the next fit on an SM
     p.smem_bytes = decode_smem_bytes(p.tok_pad, p.stages);
     p.n_tiles = static_cast<int>((N + kDecodeRows - 1) / kDecodeRows);
@@ -496,8 +495,7 @@ cudaError_t launch_decode_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tma
     a.weights_static = opts.weights_static ? 1 : 0;
     switch (plan.tok_pad) {
         case 16: return launch_tok<16>(tmap_w, tmap_a, a, plan, opts, stream);
-        case 32: return launch_tok<32>(tmap_w, tmap_a, a, plan, opts, stream);
-        default: return launch_tok<64>(tmap_w, tmap_a, a, plan, opts, stream);
+        default: return launch_tok<32>(tmap_w, tmap_a, a, plan, opts, stream);
     }
 }
 

@@ -45,14 +45,21 @@ constexpr uint32_t kPrefillTmemCols = 2 * kPrefillBN;  // two accumulators: all 
 constexpr uint32_t kPrefillIdesc = idesc_e4m3_f32(kPrefillBM, kPrefillBN);
 constexpr int kPrefillMaxStages = 4;
 // k-blocks (of 128) the tensor core accumulates in TMEM before the epilogue
-// adds the partial sum into fp32 registers (0 = a tile's whole K range in one
-// TMEM accumulation).  The tensor core's accumulation is less exact than
-// binary32 round-to-nearest over many MMAs: on prefill-chunk data (M 2048,
-// N 10240, K 5120) one accumulation over all 160 MMAs left 5 of 2.1e7 outputs
-// beyond the acceptance bound (max 1.25 of it), groups of 20 k-blocks reached
-// 0.87 of it and groups of 10 k-blocks 0.49 (bf16 rounding alone: 0.39), for
-// about 3% of the throughput of one accumulation.
+// adds the partial sum into fp32 registers.  The tensor core's accumulation is
+// less exact than binary32 round-to-nearest over many MMAs: on prefill-chunk
+// data (M 2048, N 10240, K 5120) one accumulation over all 160 MMAs left 5 of
+// 2.1e7 outputs beyond the acceptance bound (max 1.25 of it), groups of 20
+// k-blocks reached 0.87 of it and groups of 10 k-blocks 0.49 (bf16 rounding
+// alone: 0.39), for about 3% of the throughput of one accumulation.  At small
+// M the kernel is bound by streaming the weights, not by the tensor core, and
+// draining more often costs little (only the warps holding valid token rows
+// read TMEM); there the weights may be uniformly random codes, whose partial
+// sums are large next to the bound (groups of 10 k-blocks: 1.95 of it on the
+// 32-token decode data, groups of 2: 0.54), so M <= kPrefillSmallM drains
+// every kPrefillDrainKbSmall k-blocks.
 constexpr int kPrefillDrainKb = 10;
+constexpr int kPrefillDrainKbSmall = 2;
+constexpr int64_t kPrefillSmallM = 128;
 
 struct PrefillArgs {
     const float *scale_a;
@@ -218,6 +225,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             float y[kCols];
 #pragma unroll
             for (int j = 0; j < kCols; ++j) y[j] = 0.0f;
+            // a warp whose 32 token rows all lie beyond M (small M) only takes
+            // part in the hand-shake
+            const bool live = (t % m_tiles) * kPrefillBM + static_cast<int>(quarter * 32u) < M;
             for (int kb0 = 0; kb0 < kbt; kb0 += dkb, ++dc) {
                 const int acc = static_cast<int>(dc & 1u);
                 if (!pf_warp_wait(tfull_bar(acc), (dc >> 1) & 1u, err, kErrPrefillAccumWait, &s_abort, lane)) {
@@ -225,6 +235,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     break;
                 }
                 tc_fence_after();
+                if (live) {
                 const uint32_t tbase = tmem + ((quarter * 32u) << 16) +
                                        static_cast<uint32_t>(acc * kPrefillBN + half * kCols);
 #pragma unroll
@@ -235,6 +246,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     tmem_ld_wait();
 #pragma unroll
                     for (int q = 0; q < 32; ++q) y[j + q] = __fadd_rn(y[j + q], __uint_as_float(v[q]));
+                }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -305,7 +317,8 @@ PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms) {
     p.ctas = static_cast<int>(tiles < num_sms ? tiles : num_sms);
     if (p.ctas < 1) p.ctas = 1;
     p.stages = kPrefillMaxStages;
-    p.drain_kb = (kPrefillDrainKb > 0 && kPrefillDrainKb < p.kb_total) ? kPrefillDrainKb : p.kb_total;
+    const int dkb = M <= kPrefillSmallM ? kPrefillDrainKbSmall : kPrefillDrainKb;
+    p.drain_kb = (dkb > 0 && dkb < p.kb_total) ? dkb : p.kb_total;
     p.smem_bytes = prefill_smem_bytes(p.stages);
     return p;
 }

@@ -49,10 +49,10 @@ cudaError_t launch_rmsnorm_quant(const void *x, const void *gamma, float eps, co
 // channels) per tile on the tensor core's M side, up to 64 tokens on its N side.
 constexpr int kDecodeRows = 128;
 constexpr int kBlockK = 128;  // bytes (= E4M3 elements) of K per pipeline stage
-constexpr int kDecodeMaxTokens = 64;
+constexpr int kDecodeMaxTokens = 32;
 
 struct DecodePlan {
-    int tok_pad;      // tokens per tile on the MMA N side: 16, 32 or 64
+    int tok_pad;      // tokens per tile on the MMA N side: 16 or 32
     int stages;       // pipeline depth
     int n_tiles;      // ceil(N / 128)
     int m_tiles;      // ceil(M / tok_pad)
@@ -85,7 +85,7 @@ cudaError_t launch_decode_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tma
 // channels (MMA N) per tile, 128-byte k-blocks.
 constexpr int kPrefillBM = 128;
 constexpr int kPrefillBN = 256;
-constexpr int64_t kPrefillMinM = 65;  // fp8_scaled_mm sends M >= this to the prefill kernel
+constexpr int64_t kPrefillMinM = 33;  // fp8_scaled_mm sends M >= this to the prefill kernel
 
 struct PrefillPlan {
     int m_tiles, n_tiles, kb_total;

@@ -24,7 +24,7 @@
  * Conventions shared by every call
  *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
  *     caller owns and allocates every buffer.  The library allocates no device
- *     memory per call: its only allocation is a ~25 MB scratch area per device
+ *     memory per call: its only allocation is a ~14 MB scratch area per device
  *     (arrival counters and partial sums of the decode GEMM), made on the
  *     first fp8_scaled_mm call on that device -- make that first call before
  *     capturing a CUDA graph.  Because the scratch is shared, GEMM calls that
@@ -105,8 +105,8 @@ typedef enum {
  * tensor-core accumulation of the exact E4M3 products.  Which kernel runs is a
  * pure function of (M, N, K, granularity), see fp8_describe_dispatch, so a
  * captured CUDA graph replays the same kernel the eager call would run:
- * M <= 64 the weight-streaming decode kernel (uses the library's scratch
- * area), M >= 65 the tensor-core tile kernel (uses no scratch).  For a fixed
+ * M <= 32 the weight-streaming decode kernel (uses the library's scratch
+ * area), M >= 33 the tensor-core tile kernel (uses no scratch).  For a fixed
  * M the result is deterministic (bitwise the same on every run); on the tile
  * kernel row m does not depend on the other rows of A.
  * Errors: FP8_ERR_INVALID_ARG, FP8_ERR_ALIGNMENT, FP8_ERR_UNSUPPORTED,
@@ -141,7 +141,7 @@ fp8_status fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, 
  * not call cudaMalloc at all: code running inside a memory pool or arena
  * that must own every device allocation, hosts whose allocator is locked
  * while a CUDA graph is being built, or embedders that forbid hidden
- * allocations.  fp8_scaled_mm allocates its ~25 MB scratch on first use; this
+ * allocations.  fp8_scaled_mm allocates its ~14 MB scratch on first use; this
  * entry point instead uses a fixed scratch area compiled into the library (a
  * file-scope device array of 6 MB + 64 KB that every GPU which loads the
  * library holds until the process exits), and never calls cudaMalloc,
@@ -217,7 +217,7 @@ const char *fp8_status_string(int status);
 /* Which kernel fp8_scaled_mm runs for this problem (an fp8_kernel_id), or -1
  * for arguments fp8_scaled_mm would reject.  Host-only, pure: it reads no
  * device state, so a caller can assert the kernel before capturing a graph.
- * FP8_KERNEL_DECODE_SPLITK for 1 <= M <= 64, FP8_KERNEL_PREFILL for M >= 65.
+ * FP8_KERNEL_DECODE_SPLITK for 1 <= M <= 32, FP8_KERNEL_PREFILL for M >= 33.
  * Source: [P4] commit message: the M-vs-threshold branch is a pure function
  * of M so that a graph captured at a padded M freezes the branch eager
  * execution would take. */

@@ -112,9 +112,9 @@ def test_describe_dispatch_is_pure(L):
     assert L.fp8_describe_dispatch(0, 64, 64, 0) == 0
     assert L.fp8_describe_dispatch(-1, 64, 64, 0) == -1
     assert L.fp8_describe_dispatch(4, 64, 64, 7) == -1
-    for M in (1, 2, 4, 8, 16, 32, 64):
+    for M in (1, 2, 4, 8, 16, 32):
         assert L.fp8_describe_dispatch(M, 10240, 5120, 1) == 1
-    for M in (65, 128, 2048, 8192):
+    for M in (33, 64, 65, 128, 2048, 8192):
         assert L.fp8_describe_dispatch(M, 10240, 5120, 1) == 2
         assert L.fp8_describe_dispatch(M, 34816, 5120, 2) == 2
     # the same question twice gives the same answer (no hidden state)
@@ -126,7 +126,7 @@ def test_decode_planner(L):
     """Two persistent CTAs per SM (never more CTAs than units of one tile x
     one 128-wide k-block)."""
     f = L.fp8_decode_ctas_for_sms
-    for (M, N, K) in ((1, 10240, 5120), (32, 10240, 5120), (64, 34816, 5120)):
+    for (M, N, K) in ((1, 10240, 5120), (32, 10240, 5120), (32, 34816, 5120)):
         assert f(M, N, K, 152) == 304
     assert f(8, 5120, 8192, 152) == 40 * 64 // 10       # >= 10 k-blocks per CTA (64 per tile)
     assert f(8, 5120, 17408, 152) == 40 * 136 // 20
