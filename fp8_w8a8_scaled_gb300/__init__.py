@@ -70,6 +70,8 @@ def lib():
     L.fp8_scaled_mm.restype = I32
     L.fp8_scaled_mm_ex.argtypes = [P, P, P, P, I32, I32, I64, I64, I64, P, P, ctypes.c_uint]
     L.fp8_scaled_mm_ex.restype = I32
+    L.fp8_rmsnorm_quant_scaled_mm.argtypes = [P, P, F32, P, P, P, I32, I32, I64, I64, I64, P, P, P, ctypes.c_uint]
+    L.fp8_rmsnorm_quant_scaled_mm.restype = I32
     L.rmsnorm_quant_fp8.argtypes = [P, P, F32, P, P, I64, I64, P]
     L.rmsnorm_quant_fp8.restype = I32
     L.quant_fp8_per_token.argtypes = [P, P, P, I64, I64, P]
@@ -182,6 +184,39 @@ def rmsnorm_quant_fp8(x, gamma, eps, scale, out=None):
     _check(lib().rmsnorm_quant_fp8(_ptr(x), _ptr(gamma), float(eps), _ptr(scale), _ptr(out), M, K, _stream_of(x)),
            "rmsnorm_quant_fp8")
     return out
+
+
+def rmsnorm_quant_scaled_mm(x, gamma, eps, scale_a, B, scale_b, granularity=None, a_out=None, out=None, flags=0):
+    """rmsnorm_quant_fp8(x) into a_out, then fp8_scaled_mm(a_out, B) into out,
+    as one call (one launch at decode M); returns (a_out, out).  The activation
+    scale is per tensor; ``granularity`` (0 or 1) defaults from scale_b."""
+    _need(x, "x", (torch.bfloat16,), 2)
+    _need(gamma, "gamma", (torch.bfloat16,), 1)
+    _need(scale_a, "scale_a", (torch.float32,))
+    _need(B, "B", _FP8, 2)
+    _need(scale_b, "scale_b", (torch.float32,))
+    M, K = x.shape
+    N, Kb = B.shape
+    if Kb != K or gamma.numel() != K:
+        raise ValueError(f"x is [{M},{K}], B is [{N},{Kb}], gamma has {gamma.numel()} elements")
+    if granularity is None:
+        granularity = 1 if (scale_b.numel() == N and N != 1) else 0
+    if scale_b.numel() < (N if granularity == 1 else 1):
+        raise ValueError(f"granularity {granularity} needs scale_b[{N if granularity == 1 else 1}]")
+    if a_out is None:
+        a_out = torch.empty((M, K), dtype=E4M3, device=x.device)
+    else:
+        _need(a_out, "a_out", _FP8, 2)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(out, "out", (torch.bfloat16,), 2)
+        if tuple(out.shape) != (M, N):
+            raise ValueError(f"out must be [{M},{N}]")
+    _check(lib().fp8_rmsnorm_quant_scaled_mm(_ptr(x), _ptr(gamma), float(eps), _ptr(scale_a), _ptr(B), _ptr(scale_b),
+                                             int(granularity), OUT_BF16, M, N, K, _ptr(a_out), _ptr(out),
+                                             _stream_of(x), int(flags)), "fp8_rmsnorm_quant_scaled_mm")
+    return a_out, out
 
 
 def quant_fp8_per_token(x, out=None, scale_out=None):

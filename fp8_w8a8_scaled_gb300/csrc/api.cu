@@ -258,6 +258,26 @@ fp8_status fp8_scaled_mm_noalloc(const void *A, const void *B, const float *scal
                                               ws, fp8k::LaunchOpts{}, cs));
 }
 
+fp8_status fp8_rmsnorm_quant_scaled_mm(const void *x, const void *gamma, float eps, const float *scale_a,
+                                       const void *B, const float *scale_b, int granularity, int out_dtype, int64_t M,
+                                       int64_t N, int64_t K, void *a_out, void *out, void *stream, unsigned flags) {
+    if (M < 0 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > 65536) return FP8_ERR_INVALID_ARG;
+    if (granularity != FP8_GRAN_PER_TENSOR && granularity != FP8_GRAN_PER_CHANNEL) return FP8_ERR_INVALID_ARG;
+    if (flags & ~static_cast<unsigned>(FP8_FLAG_WEIGHTS_STATIC | FP8_FLAG_NO_PDL)) return FP8_ERR_INVALID_ARG;
+    if (out_dtype != FP8_OUT_BF16) return FP8_ERR_UNSUPPORTED;
+    if (M == 0) return FP8_OK;
+    if (!x || !gamma || !scale_a || !B || !scale_b || !a_out || !out) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(a_out) || !aligned16(B) || !aligned16(out) ||
+        !aligned4(scale_a) || !aligned4(scale_b))
+        return FP8_ERR_ALIGNMENT;
+    if (K % 16 != 0 || N % 8 != 0) return FP8_ERR_ALIGNMENT;
+    // Every argument is valid for both calls, so the first cannot succeed and
+    // the second then fail validation.
+    fp8_status s = rmsnorm_quant_fp8(x, gamma, eps, scale_a, a_out, M, K, stream);
+    if (s != FP8_OK) return s;
+    return fp8_scaled_mm_ex(a_out, B, scale_a, scale_b, granularity, out_dtype, M, N, K, out, stream, flags);
+}
+
 fp8_status rmsnorm_quant_fp8(const void *x, const void *gamma, float eps, const float *scale, void *out, int64_t M,
                              int64_t K, void *stream) {
     if (M < 0 || M > kI32Max || K < 1 || K > 65536) return FP8_ERR_INVALID_ARG;

@@ -1,0 +1,311 @@
+// norm_row.cuh -- the fused RMSNorm -> static E4M3 quantisation of ONE row by
+// a group of threads, shared by the standalone rmsnorm_quant_fp8 kernel (a CTA
+// per row) and the decode GEMM's fused prologue (the drain warpgroup of the
+// first M CTAs), so both produce the same bytes.
+//
+// Source: "We emit F32 where vLLM emits bf16 on the biggest prefill buffers
+// ..." (vllm.cpp #417), "Ranked follow-ons from the same audit": the fused
+// RMSNorm -> fp8 quant, byte-exact with the unfused norm-then-quant ("quantise
+// once").
+//
+//   q = e4m3( bf16((x * r) * gamma) / s ),   r = 1 / sqrt(ss / K + eps)
+//
+// The sum of squares ss is formed EXACTLY: every bf16 square is
+// m^2 * 2^(2E - 268) with m < 256, so the squares of the row's top 40 binades
+// are added as integers into a 128-bit fixed-point accumulator (2^94 per term
+// at most, 2^110 for 2^16 terms), and any nonzero smaller term only sets a
+// sticky bit -- all terms are non-negative and smaller than 2^-61 of the sum,
+// so the sticky bit is all the rounding needs.  The exact sum is rounded once
+// to binary32, then mean = ss / K, t = mean + eps, d = sqrt(t), r = 1 / d are
+// single IEEE binary32 operations; the two multiplies are separate binary32
+// operations (the library is compiled without FMA contraction), bf16 and E4M3
+// conversions round to nearest even (the E4M3 one saturating).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include <cstdint>
+
+namespace fp8k {
+namespace norm {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two values -> two E4M3 codes, `a` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// 128-bit unsigned integer as (hi, lo).
+struct U128 {
+    uint64_t hi, lo;
+};
+
+__device__ __forceinline__ U128 add128(U128 a, U128 b) {
+    U128 r;
+    r.lo = a.lo + b.lo;
+    r.hi = a.hi + b.hi + (r.lo < a.lo ? 1u : 0u);
+    return r;
+}
+
+__device__ __forceinline__ uint64_t shr128(U128 a, int q) {  // low 64 bits of a >> q, 0 <= q < 128
+    if (q == 0) return a.lo;
+    if (q < 64) return (a.lo >> q) | (a.hi << (64 - q));
+    return a.hi >> (q - 64);
+}
+
+__device__ __forceinline__ int bit128(U128 a, int i) {
+    return static_cast<int>(i < 64 ? (a.lo >> i) & 1u : (a.hi >> (i - 64)) & 1u);
+}
+
+__device__ __forceinline__ bool any_below128(U128 a, int i) {  // any set bit at positions < i
+    if (i <= 0) return false;
+    if (i < 64) return (a.lo & ((1ull << i) - 1)) != 0;
+    if (i == 64) return a.lo != 0;
+    return a.lo != 0 || (a.hi & ((1ull << (i - 64)) - 1)) != 0;
+}
+
+// bf16 bits -> (m, E): x = +-m * 2^(E - 134) with E >= 1 (E = 1 also for subnormals).
+__device__ __forceinline__ void bf16_split(uint32_t b, uint32_t &m, int &E) {
+    const uint32_t e = (b >> 7) & 0xFFu, mant = b & 0x7Fu;
+    m = e ? (128u | mant) : mant;
+    E = e ? static_cast<int>(e) : 1;
+}
+
+// Shared scratch of one row group's reductions (one entry per warp).
+struct RowScratch {
+    uint64_t red_hi[32], red_lo[32];
+    int red_i[32];
+    float r;
+};
+
+// A group of T threads (T a multiple of 32, at most 1024), thread ti of it,
+// synchronised by `sync()` (a CTA barrier or a named barrier of exactly the
+// group's threads).
+struct Group {
+    int ti, T;
+};
+
+template <class Sync>
+__device__ __forceinline__ int group_max_int(int v, const Group g, RowScratch *sc, Sync sync) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    const int warp = g.ti >> 5, lane = g.ti & 31;
+    sync();
+    if (lane == 0) sc->red_i[warp] = v;
+    sync();
+    v = lane < (g.T >> 5) ? sc->red_i[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+template <class Sync>
+__device__ __forceinline__ U128 group_sum_u128(U128 v, const Group g, RowScratch *sc, Sync sync) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        U128 w;
+        w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
+        w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
+        v = add128(v, w);
+    }
+    const int warp = g.ti >> 5, lane = g.ti & 31;
+    sync();
+    if (lane == 0) {
+        sc->red_hi[warp] = v.hi;
+        sc->red_lo[warp] = v.lo;
+    }
+    sync();
+    const int nw = g.T >> 5;
+    v.hi = lane < nw ? sc->red_hi[lane] : 0;
+    v.lo = lane < nw ? sc->red_lo[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        U128 w;
+        w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
+        w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
+        v = add128(v, w);
+    }
+    return v;
+}
+
+// The exact sum (acc * 2^(2*elo - 268), plus a sticky bit for smaller terms)
+// rounded to binary32 at 24 significant bits or the subnormal quantum 2^-149;
+// NaN / Inf inputs (special 3 / 2) give NaN / Inf.
+__device__ __forceinline__ float round_sum_to_f32(U128 acc, int elo, int sticky, int special) {
+    if (special == 3) return __int_as_float(0x7FC00000);
+    if (special == 2) return __int_as_float(0x7F800000);
+    if (acc.hi == 0 && acc.lo == 0) return 0.0f;
+    const int top = acc.hi ? 127 - __clzll(static_cast<long long>(acc.hi)) : 63 - __clzll(static_cast<long long>(acc.lo));
+    const int q = max(top - 23, 119 - 2 * elo);
+    uint64_t keep;
+    if (q <= 0) {
+        keep = acc.lo;  // fewer than 24 significant bits: exact
+    } else {
+        keep = shr128(acc, q);
+        const bool half = bit128(acc, q - 1) != 0;
+        const bool rest = any_below128(acc, q - 1) || sticky;
+        if (half && (rest || (keep & 1u))) keep += 1;
+    }
+    return ldexpf(static_cast<float>(keep), (q > 0 ? q : 0) + 2 * elo - 268);
+}
+
+// Max of two ints over the group (one pair of barriers for both).
+template <class Sync>
+__device__ __forceinline__ int2 group_max2(int2 v, const Group g, RowScratch *sc, Sync sync) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        v.x = max(v.x, __shfl_xor_sync(0xFFFFFFFFu, v.x, o));
+        v.y = max(v.y, __shfl_xor_sync(0xFFFFFFFFu, v.y, o));
+    }
+    const int warp = g.ti >> 5, lane = g.ti & 31;
+    sync();
+    if (lane == 0) {
+        sc->red_i[warp] = v.x;
+        sc->red_hi[warp] = static_cast<uint64_t>(static_cast<uint32_t>(v.y));
+    }
+    sync();
+    const int nw = g.T >> 5;
+    v.x = lane < nw ? sc->red_i[lane] : 0;
+    v.y = lane < nw ? static_cast<int>(sc->red_hi[lane]) : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        v.x = max(v.x, __shfl_xor_sync(0xFFFFFFFFu, v.x, o));
+        v.y = max(v.y, __shfl_xor_sync(0xFFFFFFFFu, v.y, o));
+    }
+    return v;
+}
+
+// Exponent field of the largest |element| of a vector of 8 bf16 (0 for zeros
+// and subnormals; 0xFF when an Inf or NaN is present), two lanes at a time.
+__device__ __forceinline__ uint32_t vec_max_exp(const uint4 v) {
+    uint32_t r = __vmaxu2(__vmaxu2(v.x & 0x7F807F80u, v.y & 0x7F807F80u), __vmaxu2(v.z & 0x7F807F80u, v.w & 0x7F807F80u));
+    r = max(r & 0xFFFFu, r >> 16);
+    return r >> 7;
+}
+
+// 3 = some element is a NaN, 2 = some element is an Inf, 0 = neither.
+__device__ __forceinline__ int vec_special(const uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    int sp = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t b = (w[i >> 1] >> (16 * (i & 1))) & 0x7FFFu;
+        if ((b >> 7) == 0xFFu) sp = max(sp, (b & 0x7Fu) ? 3 : 2);
+    }
+    return sp;
+}
+
+// The squares of one vector's elements of binade E >= elo, added exactly as
+// integers (element m * 2^(E - 134) contributes m^2 * 2^(2 (E - elo)) units)
+// into three 64-bit partial sums at 32-bit offsets (each contribution is
+// below 2^47 and a thread adds at most 2^16 of them, so none overflows);
+// smaller nonzero elements only set the sticky bit.
+__device__ __forceinline__ void vec_sum_squares(const uint4 v, int elo, uint64_t &a0, uint64_t &a1, uint64_t &a2,
+                                                int &sticky) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t b = (w[i >> 1] >> (16 * (i & 1))) & 0x7FFFu;
+        const uint32_t e = b >> 7, mant = b & 0x7Fu;
+        const uint32_t m = e ? (mant | 0x80u) : mant;
+        const int E = e ? static_cast<int>(e) : 1;
+        const bool nz = b != 0;
+        const bool in = nz && E >= elo;
+        sticky |= (nz && E < elo) ? 1 : 0;
+        const int sh = in ? 2 * (E - elo) : 0;
+        const uint64_t c = in ? (static_cast<uint64_t>(m * m) << (sh & 31)) : 0ull;
+        const int k = sh >> 5;
+        a0 += (k == 0) ? c : 0ull;
+        a1 += (k == 1) ? c : 0ull;
+        a2 += (k == 2) ? c : 0ull;
+    }
+}
+
+// One row: xr / gamma / orow hold nvec vectors of 8 elements (K = 8 * nvec);
+// thread ti handles vectors ti, ti + T, ... (at most V of them).  Every
+// thread of the group must call this (it synchronises the group).
+template <int V, bool kPrefetchGamma, class Sync>
+__device__ __forceinline__ void rmsnorm_quant_row(const uint4 *__restrict__ xr, const uint4 *__restrict__ gamma,
+                                                  float eps, float s, uint2 *__restrict__ orow, int nvec, int K,
+                                                  const Group g, RowScratch *sc, Sync sync) {
+    uint4 v[V], gm[kPrefetchGamma ? V : 1];
+    uint32_t efield = 0;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = g.ti + j * g.T;
+        if (idx < nvec) {
+            v[j] = ld_stream(xr + idx);
+            if (kPrefetchGamma) gm[j] = __ldg(gamma + idx);
+            efield = max(efield, vec_max_exp(v[j]));
+        }
+    }
+    int special = 0;  // 3 = a NaN, 2 = an Inf (the max keeps NaN)
+    if (efield == 0xFFu) {
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int idx = g.ti + j * g.T;
+            if (idx < nvec) special = max(special, vec_special(v[j]));
+        }
+    }
+    const int2 red = group_max2(make_int2(static_cast<int>(efield), special), g, sc, sync);
+    special = red.y;
+    // The largest binade of a finite element (subnormals count as binade 1;
+    // an all-subnormal or all-zero row gives the same window as binade 1).
+    const int emax = special ? 0 : red.x;
+    const int elo = max(emax - 39, 1);
+    uint64_t a0 = 0, a1 = 0, a2 = 0;
+    int sticky = 0;
+    if (!special) {
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int idx = g.ti + j * g.T;
+            if (idx < nvec) vec_sum_squares(v[j], elo, a0, a1, a2, sticky);
+        }
+    }
+    // a0 + a1 * 2^32 + a2 * 2^64 as one 128-bit number
+    U128 acc = {a2, a0};
+    acc = add128(acc, U128{a1 >> 32, a1 << 32});
+    acc = group_sum_u128(acc, g, sc, sync);
+    sticky = group_max_int(sticky, g, sc, sync);
+    if (g.ti == 0) {
+        const float ss = round_sum_to_f32(acc, elo, sticky, special);
+        const float mean = __fdiv_rn(ss, static_cast<float>(K));
+        const float t = __fadd_rn(mean, eps);
+        const float d = __fsqrt_rn(t);
+        sc->r = __fdiv_rn(1.0f, d);
+    }
+    sync();
+    const float r = sc->r;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = g.ti + j * g.T;
+        if (idx < nvec) {
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            const uint4 gv = kPrefetchGamma ? gm[j] : __ldg(gamma + idx);
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            uint32_t p[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float h0 =
+                    __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(bf16_lo(w[i]), r), bf16_lo(gw[i]))));
+                const float h1 =
+                    __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(bf16_hi(w[i]), r), bf16_hi(gw[i]))));
+                p[i] = e4m3x2(__fdiv_rn(h0, s), __fdiv_rn(h1, s));
+            }
+            orow[idx] = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+        }
+    }
+}
+
+}  // namespace norm
+}  // namespace fp8k

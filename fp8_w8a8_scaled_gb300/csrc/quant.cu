@@ -24,18 +24,17 @@
 #include <cuda_runtime.h>
 
 #include "kernels.h"
+#include "norm_row.cuh"
 #include "ptx.cuh"
 
 namespace fp8k {
 namespace {
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+using norm::bf16_hi;
+using norm::bf16_lo;
+using norm::e4m3x2;
+using norm::ld_stream;
 
-// Two values -> two E4M3 codes, `a` in the low byte.
-__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
-    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
-}
 
 // Eight bf16 (one 16-byte vector) divided by s -> eight E4M3 codes.
 __device__ __forceinline__ uint2 quant8(const uint4 v, float s) {
@@ -57,14 +56,6 @@ __device__ __forceinline__ float absmax8(const uint4 v, float m) {
     return m;
 }
 
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ float block_max(float v, float *red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
@@ -79,84 +70,6 @@ __device__ __forceinline__ float block_max(float v, float *red) {
     }
     __syncthreads();
     return red[0];
-}
-
-// Block-wide reductions used by the RMSNorm kernel.
-__device__ __forceinline__ int block_max_int(int v, int *red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    v = lane < static_cast<int>(blockDim.x >> 5) ? red[lane] : 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    return v;
-}
-
-// 128-bit unsigned integer as (hi, lo).
-struct U128 {
-    uint64_t hi, lo;
-};
-
-__device__ __forceinline__ U128 add128(U128 a, U128 b) {
-    U128 r;
-    r.lo = a.lo + b.lo;
-    r.hi = a.hi + b.hi + (r.lo < a.lo ? 1u : 0u);
-    return r;
-}
-
-__device__ __forceinline__ U128 block_sum_u128(U128 v, uint64_t *red_hi, uint64_t *red_lo) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        U128 w;
-        w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
-        w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
-        v = add128(v, w);
-    }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();
-    if (lane == 0) {
-        red_hi[warp] = v.hi;
-        red_lo[warp] = v.lo;
-    }
-    __syncthreads();
-    const int nw = static_cast<int>(blockDim.x >> 5);
-    v.hi = lane < nw ? red_hi[lane] : 0;
-    v.lo = lane < nw ? red_lo[lane] : 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        U128 w;
-        w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
-        w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
-        v = add128(v, w);
-    }
-    return v;
-}
-
-__device__ __forceinline__ uint64_t shr128(U128 a, int q) {  // low 64 bits of a >> q, 0 <= q < 128
-    if (q == 0) return a.lo;
-    if (q < 64) return (a.lo >> q) | (a.hi << (64 - q));
-    return a.hi >> (q - 64);
-}
-
-__device__ __forceinline__ int bit128(U128 a, int i) {
-    return static_cast<int>(i < 64 ? (a.lo >> i) & 1u : (a.hi >> (i - 64)) & 1u);
-}
-
-__device__ __forceinline__ bool any_below128(U128 a, int i) {  // any set bit at positions < i
-    if (i <= 0) return false;
-    if (i < 64) return (a.lo & ((1ull << i) - 1)) != 0;
-    if (i == 64) return a.lo != 0;
-    return a.lo != 0 || (a.hi & ((1ull << (i - 64)) - 1)) != 0;
-}
-
-// bf16 bits -> (m, E): x = +-m * 2^(E - 134) with E >= 1 (E = 1 also for subnormals).
-__device__ __forceinline__ void bf16_split(uint32_t b, uint32_t &m, int &E) {
-    const uint32_t e = (b >> 7) & 0xFFu, mant = b & 0x7Fu;
-    m = e ? (128u | mant) : mant;
-    E = e ? static_cast<int>(e) : 1;
 }
 
 // ------------------------------------------------------------- static quant --
@@ -230,133 +143,24 @@ __global__ void __launch_bounds__(512) quant_per_token_long_kernel(const uint4 *
 
 // ---------------------------------------------------- fused RMSNorm -> quant --
 
-// One CTA per row.  The sum of squares is formed EXACTLY: every bf16 square is
-// m^2 * 2^(2E - 268) with m < 256, so the squares of the row's top 40 binades
-// are added as integers into a 128-bit fixed-point accumulator (2^94 per term
-// at most, 2^110 for 2^16 terms), and any nonzero smaller term only sets a
-// sticky bit -- all terms are non-negative and smaller than 2^-61 of the sum,
-// so the sticky bit is all the rounding needs.  The exact sum is rounded once
-// to binary32, then mean = ss / K, t = mean + eps, d = sqrt(t), r = 1 / d are
-// single IEEE binary32 operations.
+struct CtaSync {
+    __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+// One CTA per row; the row arithmetic (exact sum of squares, binary32 chain)
+// is norm::rmsnorm_quant_row, shared with the decode GEMM's fused prologue.
 template <int V>
 __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gamma,
                                                              float eps, const float *__restrict__ scale,
                                                              uint2 *__restrict__ out, int nvec, int K) {
-    const int T = static_cast<int>(blockDim.x);
-    __shared__ uint64_t red_hi[32], red_lo[32];
-    __shared__ int red_i[32];
-    __shared__ float s_r;
+    __shared__ norm::RowScratch sc;
     grid_dependency_wait();
     grid_launch_dependents();
     const int64_t row = blockIdx.x;
-    const uint4 *xr = x + row * nvec;
-    uint2 *orow = out + row * nvec;
-    uint4 v[V], g[V];
-    constexpr bool kPrefetchGamma = V <= 8;  // keep gamma in registers too when they are plentiful
-    int emax = 0, special = 0;               // special: 3 = a NaN, 2 = an Inf (the max keeps NaN)
-#pragma unroll
-    for (int j = 0; j < V; ++j) {
-        const int idx = threadIdx.x + j * T;
-        if (idx < nvec) {
-            v[j] = ld_stream(xr + idx);
-            if (kPrefetchGamma) g[j] = __ldg(gamma + idx);
-            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t b = (w[i >> 1] >> (16 * (i & 1))) & 0x7FFFu;
-                if ((b >> 7) == 0xFFu) {
-                    special = max(special, (b & 0x7Fu) ? 3 : 2);
-                } else if (b != 0) {
-                    uint32_t m;
-                    int E;
-                    bf16_split(b, m, E);
-                    emax = max(emax, E);
-                }
-            }
-        }
-    }
-    emax = block_max_int(emax, red_i);
-    special = block_max_int(special, red_i);
-    const int elo = max(emax - 39, 1);
-    U128 acc = {0, 0};
-    int sticky = 0;
-#pragma unroll
-    for (int j = 0; j < V; ++j) {
-        const int idx = threadIdx.x + j * T;
-        if (idx < nvec) {
-            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t b = (w[i >> 1] >> (16 * (i & 1))) & 0x7FFFu;
-                if (b == 0 || (b >> 7) == 0xFFu) continue;
-                uint32_t m;
-                int E;
-                bf16_split(b, m, E);
-                if (E < elo) {
-                    sticky = 1;
-                    continue;
-                }
-                const int sh = 2 * (E - elo);  // 0 .. 78
-                const uint64_t sq = static_cast<uint64_t>(m * m);
-                U128 t;
-                t.lo = sh < 64 ? (sq << sh) : 0;
-                t.hi = sh == 0 ? 0 : (sh < 64 ? (sq >> (64 - sh)) : (sq << (sh - 64)));
-                acc = add128(acc, t);
-            }
-        }
-    }
-    acc = block_sum_u128(acc, red_hi, red_lo);
-    sticky = block_max_int(sticky, red_i);
-    if (threadIdx.x == 0) {
-        float ss;
-        if (special == 3) {
-            ss = __int_as_float(0x7FC00000);
-        } else if (special == 2) {
-            ss = __int_as_float(0x7F800000);
-        } else if (acc.hi == 0 && acc.lo == 0) {
-            ss = 0.0f;
-        } else {
-            // value = acc * 2^(2*elo - 268); round at binary32 precision (24
-            // significant bits, or the subnormal quantum 2^-149)
-            const int top = acc.hi ? 127 - __clzll(static_cast<long long>(acc.hi))
-                                   : 63 - __clzll(static_cast<long long>(acc.lo));
-            const int q = max(top - 23, 119 - 2 * elo);
-            uint64_t keep;
-            if (q <= 0) {
-                keep = acc.lo;  // fewer than 24 significant bits: exact
-            } else {
-                keep = shr128(acc, q);
-                const bool half = bit128(acc, q - 1) != 0;
-                const bool rest = any_below128(acc, q - 1) || sticky;
-                if (half && (rest || (keep & 1u))) keep += 1;
-            }
-            ss = ldexpf(static_cast<float>(keep), (q > 0 ? q : 0) + 2 * elo - 268);
-        }
-        const float mean = __fdiv_rn(ss, static_cast<float>(K));
-        const float t = __fadd_rn(mean, eps);
-        const float d = __fsqrt_rn(t);
-        s_r = __fdiv_rn(1.0f, d);
-    }
-    __syncthreads();
-    const float r = s_r;
     const float s = __ldg(scale);
-#pragma unroll
-    for (int j = 0; j < V; ++j) {
-        const int idx = threadIdx.x + j * T;
-        if (idx < nvec) {
-            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-            const uint4 gv = kPrefetchGamma ? g[j] : __ldg(gamma + idx);
-            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-            uint32_t p[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float h0 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(bf16_lo(w[i]), r), bf16_lo(gw[i]))));
-                const float h1 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(bf16_hi(w[i]), r), bf16_hi(gw[i]))));
-                p[i] = e4m3x2(__fdiv_rn(h0, s), __fdiv_rn(h1, s));
-            }
-            orow[idx] = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
-        }
-    }
+    norm::rmsnorm_quant_row<V, (V <= 8)>(x + row * nvec, gamma, eps, s, out + row * nvec, nvec, K,
+                                         norm::Group{static_cast<int>(threadIdx.x), static_cast<int>(blockDim.x)}, &sc,
+                                         CtaSync{});
 }
 
 // Threads per row-CTA for `nvec` vectors at V vectors per thread: a multiple

@@ -186,6 +186,35 @@ fp8_status fp8_scaled_mm_noalloc(const void *A, const void *B, const float *scal
 fp8_status rmsnorm_quant_fp8(const void *x, const void *gamma, float eps, const float *scale, void *out,
                              int64_t M, int64_t K, void *stream);
 
+/* fp8_rmsnorm_quant_scaled_mm -- rmsnorm_quant_fp8 followed by fp8_scaled_mm
+ * on its output, as one call ("quantise once": the normalised, quantised
+ * activations are written to a_out for the layer's other projections, and
+ * this projection consumes them at once).
+ *
+ * Source: [P3] "Ranked follow-ons from the same audit" (the fused RMSNorm ->
+ * fp8 quant feeding the FP8 GEMMs of a layer, quantise once); [P1] "SETTLED
+ * BY PAIRED TRACE" (at decode M the cost is per launch and per weight byte).
+ *
+ *   x, gamma, eps   as rmsnorm_quant_fp8 (x bf16 [M,K], gamma bf16 [K])
+ *   scale_a         f32 [1] (device): the static activation scale, used both
+ *                   to quantise and as the GEMM's activation scale
+ *   B, scale_b      as fp8_scaled_mm; granularity FP8_GRAN_PER_TENSOR or
+ *                   FP8_GRAN_PER_CHANNEL (the activation scale is one value)
+ *   a_out           E4M3 [M,K], 16-byte aligned: written with exactly the bytes
+ *                   rmsnorm_quant_fp8 writes
+ *   out             bf16 [M,N]: exactly the bytes fp8_scaled_mm(a_out, ...)
+ *                   writes
+ *   flags           as fp8_scaled_mm_ex
+ *   K % 16 == 0, 1 <= K <= 65536, N % 8 == 0
+ *
+ * It runs the norm kernel and then the GEMM kernel, chained with programmatic
+ * dependent launch (the GEMM's CTAs launch early, fetch their first weights
+ * and wait for the normalised rows).  Errors: those of the two calls; an
+ * argument error is reported before anything is launched. */
+fp8_status fp8_rmsnorm_quant_scaled_mm(const void *x, const void *gamma, float eps, const float *scale_a,
+                                       const void *B, const float *scale_b, int granularity, int out_dtype, int64_t M,
+                                       int64_t N, int64_t K, void *a_out, void *out, void *stream, unsigned flags);
+
 /* quant_fp8_per_token -- dynamic per-token E4M3 quantisation.
  *
  * Source: [P1] "What is owed", item 2 (per-token scaling granularity and where

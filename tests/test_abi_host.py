@@ -89,6 +89,31 @@ def test_scaled_mm_ex_flags(L):
     assert L.fp8_scaled_mm_ex(GOOD, GOOD2, SC, SC2, 0, 0, 4, 64, 72, GOOD3, None, 1) == 2
 
 
+def test_fused_norm_mm_validation(L):
+    f = L.fp8_rmsnorm_quant_scaled_mm
+    G4, G5 = P(0x60000), P(0x70000)
+
+    def call(x=GOOD, gamma=GOOD2, sa=SC, B=GOOD3, sb=SC2, gran=1, od=0, M=4, N=64, K=64, a=G4, out=G5, flags=0):
+        return f(x, gamma, ctypes.c_float(1e-6), sa, B, sb, gran, od, M, N, K, a, out, None, flags)
+
+    assert call(M=0) == 0
+    assert call(M=0, x=None, a=None, out=None) == 0
+    assert call(gran=2) == 1            # the activation scale is per tensor
+    assert call(gran=3) == 1
+    assert call(M=-1) == 1
+    assert call(K=65552) == 1
+    assert call(flags=4) == 1
+    assert call(od=1) == 3
+    assert call(x=None) == 1
+    assert call(gamma=None) == 1
+    assert call(a=None) == 1
+    assert call(out=None) == 1
+    assert call(a=P(0x60008)) == 2
+    assert call(gamma=P(0x20004)) == 2
+    assert call(K=72) == 2
+    assert call(N=68) == 2
+
+
 def test_quantiser_validation(L):
     assert L.quant_fp8_static(GOOD, SC, GOOD2, 0, 64, None) == 0
     assert L.quant_fp8_static(None, SC, GOOD2, 4, 64, None) == 1
