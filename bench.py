@@ -326,6 +326,11 @@ def quant_bytes(M, K):
     return 2 * M * K + M * K + 4 * M
 
 
+def silu_quant_bytes(M, I):
+    """SiLU(gate) * up -> per-token quant: bf16 [M, 2I] in, E4M3 [M, I] out, scales."""
+    return 2 * M * 2 * I + M * I + 4 * M
+
+
 def graph_of(torch, device, fn, inner):
     s = torch.cuda.Stream(device=device)
     s.wait_stream(torch.cuda.current_stream(device))
@@ -372,9 +377,10 @@ def run_gate_up(torch, fp8, device, dist_barrier, dist_max, reps=40):
 
 def run_decode_step(torch, fp8, device, dist_barrier, dist_max, reps=20):
     """Synthetic 64-layer decode step at M in {1, 4, 8}: per layer RMSNorm ->
-    static quant -> QKV (10240x5120), per-token quant of an [M, 8192] stub ->
-    O (5120x8192), gate_up (34816x5120) on the same normalised input, per-token
-    quant of an [M, 17408] stub -> down (5120x17408); distinct weights per
+    static quant -> QKV (10240x5120), per-token quant of an [M, 8192] stub
+    (the attention output, not on this path) -> O (5120x8192), gate_up
+    (34816x5120) on the same normalised input, SiLU(gate) * up -> per-token
+    quant of the gate_up output -> down (5120x17408); distinct weights per
     layer (23.15 GB), the whole step one CUDA graph."""
     L_ = workloads.STEP_LAYERS
     shapes = workloads.LayerShapes()
@@ -395,7 +401,6 @@ def run_decode_step(torch, fp8, device, dist_barrier, dist_max, reps=20):
     for M in workloads.STEP_MS:
         x = workloads.device_bf16_normal(torch, (M, K), seed=30001, device=device)
         o_in = workloads.device_bf16_normal(torch, (M, workloads.O_K), seed=30002, device=device)
-        d_in = workloads.device_bf16_normal(torch, (M, workloads.DOWN_K), seed=30003, device=device)
         a = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=device)
         a_o = torch.empty((M, workloads.O_K), dtype=torch.float8_e4m3fn, device=device)
         a_d = torch.empty((M, workloads.DOWN_K), dtype=torch.float8_e4m3fn, device=device)
@@ -412,7 +417,7 @@ def run_decode_step(torch, fp8, device, dist_barrier, dist_max, reps=20):
                 fp8.quant_fp8_per_token(o_in, out=a_o, scale_out=s_o)
                 fp8.fp8_scaled_mm(a_o, ws[1][0], s_o, ws[1][1], fp8.GRAN_PER_TOKEN_CHANNEL, out=y[1], flags=st)
                 fp8.fp8_scaled_mm(a, ws[2][0], s_a, ws[2][1], fp8.GRAN_PER_CHANNEL, out=y[2], flags=st)
-                fp8.quant_fp8_per_token(d_in, out=a_d, scale_out=s_d)
+                fp8.silu_mul_quant_per_token(y[2], out=a_d, scale_out=s_d)
                 fp8.fp8_scaled_mm(a_d, ws[3][0], s_d, ws[3][1], fp8.GRAN_PER_TOKEN_CHANNEL, out=y[3], flags=st)
 
         g = graph_of(torch, device, step, 1)
@@ -423,14 +428,15 @@ def run_decode_step(torch, fp8, device, dist_barrier, dist_max, reps=20):
         layer_bytes = (norm_bytes(M) + gemm_bytes_gran(M, *shapes.qkv, False)
                        + quant_bytes(M, workloads.O_K) + gemm_bytes_gran(M, *shapes.o, True)
                        + gemm_bytes_gran(M, *shapes.gate_up, False)
-                       + quant_bytes(M, workloads.DOWN_K) + gemm_bytes_gran(M, *shapes.down, True))
+                       + silu_quant_bytes(M, workloads.DOWN_K) + gemm_bytes_gran(M, *shapes.down, True))
         tbps = L_ * layer_bytes / (ms * 1e-3) / 1e12
         rows.append({"M": M, "ms_per_step": round(ms, 4), "bytes_per_step": L_ * layer_bytes, "TBps": round(tbps, 4),
                      "frac": round(tbps * 1e3 / peak, 4)})
     del Wl
     torch.cuda.empty_cache()
-    return {"workload": "64-layer synthetic decode step (norm-quant, QKV, per-token quant, O, gate_up, per-token "
-                        "quant, down per layer; 361.76 MB of distinct weights per layer), one CUDA graph",
+    return {"workload": "64-layer synthetic decode step (norm-quant, QKV, per-token quant of an attention-output "
+                        "stub, O, gate_up, SiLU(gate)*up -> per-token quant, down per layer; 361.76 MB of distinct "
+                        "weights per layer), one CUDA graph",
             "unit": "TB/s", "peak_GBps": peak, "per_M": rows, "gpu_launches": launches}
 
 

@@ -72,6 +72,10 @@ def lib():
     L.fp8_scaled_mm_ex.restype = I32
     L.fp8_rmsnorm_quant_scaled_mm.argtypes = [P, P, F32, P, P, P, I32, I32, I64, I64, I64, P, P, P, ctypes.c_uint]
     L.fp8_rmsnorm_quant_scaled_mm.restype = I32
+    L.fp8_silu_mul_quant_per_token.argtypes = [P, P, P, I64, I64, P]
+    L.fp8_silu_mul_quant_per_token.restype = I32
+    L.fp8_add_rmsnorm_quant.argtypes = [P, P, P, F32, P, P, I64, I64, P]
+    L.fp8_add_rmsnorm_quant.restype = I32
     L.rmsnorm_quant_fp8.argtypes = [P, P, F32, P, P, I64, I64, P]
     L.rmsnorm_quant_fp8.restype = I32
     L.quant_fp8_per_token.argtypes = [P, P, P, I64, I64, P]
@@ -217,6 +221,46 @@ def rmsnorm_quant_scaled_mm(x, gamma, eps, scale_a, B, scale_b, granularity=None
                                              int(granularity), OUT_BF16, M, N, K, _ptr(a_out), _ptr(out),
                                              _stream_of(x), int(flags)), "fp8_rmsnorm_quant_scaled_mm")
     return a_out, out
+
+
+def add_rmsnorm_quant_fp8(x, residual, gamma, eps, scale, out=None):
+    """residual <- bf16(x + residual) in place, then the fused RMSNorm -> static
+    E4M3 quantisation of it; returns the E4M3 [M,K] output."""
+    _need(x, "x", (torch.bfloat16,), 2)
+    _need(residual, "residual", (torch.bfloat16,), 2)
+    _need(gamma, "gamma", (torch.bfloat16,), 1)
+    _need(scale, "scale", (torch.float32,))
+    M, K = x.shape
+    if tuple(residual.shape) != (M, K) or gamma.numel() != K:
+        raise ValueError("residual must match x; gamma must have K elements")
+    if out is None:
+        out = torch.empty((M, K), dtype=E4M3, device=x.device)
+    else:
+        _need(out, "out", _FP8, 2)
+    _check(lib().fp8_add_rmsnorm_quant(_ptr(x), _ptr(residual), _ptr(gamma), float(eps), _ptr(scale), _ptr(out), M,
+                                       K, _stream_of(x)), "fp8_add_rmsnorm_quant")
+    return out
+
+
+def silu_mul_quant_per_token(gate_up, out=None, scale_out=None):
+    """silu(gate) * up for bf16 rows [gate | up] ([M, 2I]), quantised per token;
+    returns (q E4M3 [M, I], s f32 [M])."""
+    _need(gate_up, "gate_up", (torch.bfloat16,), 2)
+    M, W = gate_up.shape
+    if W % 2:
+        raise ValueError("gate_up rows must hold [gate | up]")
+    I = W // 2
+    if out is None:
+        out = torch.empty((M, I), dtype=E4M3, device=gate_up.device)
+    else:
+        _need(out, "out", _FP8, 2)
+    if scale_out is None:
+        scale_out = torch.empty((M,), dtype=torch.float32, device=gate_up.device)
+    else:
+        _need(scale_out, "scale_out", (torch.float32,))
+    _check(lib().fp8_silu_mul_quant_per_token(_ptr(gate_up), _ptr(out), _ptr(scale_out), M, I,
+                                              _stream_of(gate_up)), "fp8_silu_mul_quant_per_token")
+    return out, scale_out
 
 
 def quant_fp8_per_token(x, out=None, scale_out=None):

@@ -290,7 +290,37 @@ fp8_status rmsnorm_quant_fp8(const void *x, const void *gamma, float eps, const 
     if (s != FP8_OK) return s;
     return from_cuda(
         fp8k::launch_rmsnorm_quant(x, gamma, eps, scale, out, M, K, st->err, static_cast<cudaStream_t>(stream),
-                                   fp8k::LaunchOpts{}));
+                                   st->num_sms, fp8k::LaunchOpts{}));
+}
+
+fp8_status fp8_add_rmsnorm_quant(const void *x, void *residual, const void *gamma, float eps, const float *scale,
+                                 void *out, int64_t M, int64_t K, void *stream) {
+    if (M < 0 || M > kI32Max || K < 1 || K > 65536) return FP8_ERR_INVALID_ARG;
+    if (M == 0) return FP8_OK;
+    if (!x || !residual || !gamma || !scale || !out) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(residual) || !aligned16(gamma) || !aligned16(out) || !aligned4(scale))
+        return FP8_ERR_ALIGNMENT;
+    if (K % 16 != 0) return FP8_ERR_ALIGNMENT;
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    return from_cuda(fp8k::launch_rmsnorm_quant(x, gamma, eps, scale, out, M, K, st->err,
+                                                static_cast<cudaStream_t>(stream), st->num_sms, fp8k::LaunchOpts{},
+                                                residual));
+}
+
+fp8_status fp8_silu_mul_quant_per_token(const void *gate_up, void *out, float *scale_out, int64_t M, int64_t I,
+                                        void *stream) {
+    if (M < 0 || M > kI32Max || I < 1 || I > 131072) return FP8_ERR_INVALID_ARG;
+    if (M == 0) return FP8_OK;
+    if (!gate_up || !out || !scale_out) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(gate_up) || !aligned16(out) || !aligned4(scale_out)) return FP8_ERR_ALIGNMENT;
+    if (I % 16 != 0) return FP8_ERR_ALIGNMENT;
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    return from_cuda(fp8k::launch_silu_mul_quant(gate_up, out, scale_out, M, I, st->err,
+                                                 static_cast<cudaStream_t>(stream), st->num_sms, fp8k::LaunchOpts{}));
 }
 
 fp8_status quant_fp8_per_token(const void *x, void *out, float *scale_out, int64_t M, int64_t K, void *stream) {
@@ -303,7 +333,7 @@ fp8_status quant_fp8_per_token(const void *x, void *out, float *scale_out, int64
     fp8_status s = device_state(&st);
     if (s != FP8_OK) return s;
     return from_cuda(fp8k::launch_quant_per_token(x, out, scale_out, M, K, st->err, static_cast<cudaStream_t>(stream),
-                                                  fp8k::LaunchOpts{}));
+                                                  st->num_sms, fp8k::LaunchOpts{}));
 }
 
 fp8_status quant_fp8_static(const void *x, const float *scale, void *out, int64_t M, int64_t K, void *stream) {

@@ -38,10 +38,16 @@ cudaError_t launch_quant_static(const void *x, const float *scale, void *out, in
                                 uint32_t *err, cudaStream_t stream, int num_sms, const LaunchOpts &opts);
 
 cudaError_t launch_quant_per_token(const void *x, void *out, float *scale_out, int64_t M, int64_t K,
-                                   uint32_t *err, cudaStream_t stream, const LaunchOpts &opts);
+                                   uint32_t *err, cudaStream_t stream, int num_sms, const LaunchOpts &opts);
 
+// gate_up [M, 2I] bf16 rows [gate | up] -> E4M3 [M, I] of silu(gate) * up, per-token scales.
+cudaError_t launch_silu_mul_quant(const void *gate_up, void *out, float *scale_out, int64_t M, int64_t I,
+                                  uint32_t *err, cudaStream_t stream, int num_sms, const LaunchOpts &opts);
+
+// resid != nullptr: the row is bf16(x + resid) (which replaces resid) before the norm.
 cudaError_t launch_rmsnorm_quant(const void *x, const void *gamma, float eps, const float *scale, void *out,
-                                 int64_t M, int64_t K, uint32_t *err, cudaStream_t stream, const LaunchOpts &opts);
+                                 int64_t M, int64_t K, uint32_t *err, cudaStream_t stream, int num_sms,
+                                 const LaunchOpts &opts, void *resid = nullptr);
 
 // ------------------------------------------------------------- decode GEMM --
 

@@ -234,10 +234,21 @@ __device__ __forceinline__ void vec_sum_squares(const uint4 v, int elo, uint64_t
 // One row: xr / gamma / orow hold nvec vectors of 8 elements (K = 8 * nvec);
 // thread ti handles vectors ti, ti + T, ... (at most V of them).  Every
 // thread of the group must call this (it synchronises the group).
-template <int V, bool kPrefetchGamma, class Sync>
+// bf16( fp32(a) + fp32(b) ) for the two bf16 halves of a pair of words.
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(bf16_lo(a), bf16_lo(b))));
+    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(bf16_hi(a), bf16_hi(b))));
+    return lo | (hi << 16);
+}
+
+template <int V, bool kPrefetchGamma, bool kResidual = false, class Sync>
 __device__ __forceinline__ void rmsnorm_quant_row(const uint4 *__restrict__ xr, const uint4 *__restrict__ gamma,
                                                   float eps, float s, uint2 *__restrict__ orow, int nvec, int K,
-                                                  const Group g, RowScratch *sc, Sync sync) {
+                                                  const Group g, RowScratch *sc, Sync sync,
+                                                  uint4 *resid = nullptr) {
+    // With kResidual the row is first replaced by h = bf16(fp32(x) + fp32(res))
+    // (one binary32 addition, rounded to bf16), which is also written back
+    // over the residual row `resid` (each element by the thread that read it).
     uint4 v[V], gm[kPrefetchGamma ? V : 1];
     uint32_t efield = 0;
 #pragma unroll
@@ -245,6 +256,12 @@ __device__ __forceinline__ void rmsnorm_quant_row(const uint4 *__restrict__ xr, 
         const int idx = g.ti + j * g.T;
         if (idx < nvec) {
             v[j] = ld_stream(xr + idx);
+            if (kResidual) {
+                const uint4 rv = resid[idx];
+                v[j] = make_uint4(add_bf16x2(v[j].x, rv.x), add_bf16x2(v[j].y, rv.y), add_bf16x2(v[j].z, rv.z),
+                                  add_bf16x2(v[j].w, rv.w));
+                resid[idx] = v[j];
+            }
             if (kPrefetchGamma) gm[j] = __ldg(gamma + idx);
             efield = max(efield, vec_max_exp(v[j]));
         }

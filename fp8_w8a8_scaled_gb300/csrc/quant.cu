@@ -141,6 +141,86 @@ __global__ void __launch_bounds__(512) quant_per_token_long_kernel(const uint4 *
     for (int64_t i = threadIdx.x; i < nvec; i += 512) orow[i] = quant8(__ldg(xr + i), s);
 }
 
+// ------------------------------------------- SiLU(gate) * up -> per-token quant --
+
+// exp in binary32: Cody and Waite's argument reduction (W. J. Cody and W.
+// Waite, "Software Manual for the Elementary Functions", 1980) --
+// n = rint(y log2 e), r = (y - n C1) - n C2 with C1 + C2 = ln 2 and C1 short
+// enough that n C1 is exact -- then e^r by its Taylor series to degree 7 in
+// Horner form, times 2^n.  Every step is one IEEE binary32 operation (no
+// fused multiply-add), so the result is a fixed function of y; it is within a
+// few units in the last place of exp.  y < -87 gives 0 and y > 88 gives +inf
+// (every 2^n is then a normal number), NaN gives NaN.
+__device__ __forceinline__ float exp_f32(float y) {
+    if (y != y) return y;
+    if (y < -87.0f) return 0.0f;
+    if (y > 88.0f) return __int_as_float(0x7F800000);
+    const float kLog2e = 1.44269504088896340736f;   // log2(e) rounded to binary32
+    const float kLn2Hi = 0.693145751953125f;        // 0x3F317200: ln 2 to 16 bits
+    const float kLn2Lo = 1.428606765330187045e-06f; // ln 2 - kLn2Hi, rounded
+    const float n = rintf(__fmul_rn(y, kLog2e));
+    const float r = __fsub_rn(__fsub_rn(y, __fmul_rn(n, kLn2Hi)), __fmul_rn(n, kLn2Lo));
+    float p = 1.0f / 5040.0f;
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 720.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 120.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 24.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 6.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    const float two_n = __int_as_float((static_cast<int>(n) + 127) << 23);
+    return __fmul_rn(p, two_n);
+}
+
+// bf16( silu(g) * u ) with silu(g) = g / (1 + exp(-g)), binary32 throughout.
+__device__ __forceinline__ uint32_t silu_mul_bf16(float g, float u) {
+    const float s = __fdiv_rn(g, __fadd_rn(1.0f, exp_f32(-g)));
+    return __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(s, u)));
+}
+
+__device__ __forceinline__ uint4 silu_mul8(const uint4 g, const uint4 u) {
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+    uint32_t a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        a[i] = silu_mul_bf16(bf16_lo(gw[i]), bf16_lo(uw[i])) | (silu_mul_bf16(bf16_hi(gw[i]), bf16_hi(uw[i])) << 16);
+    return make_uint4(a[0], a[1], a[2], a[3]);
+}
+
+// One CTA per row of [gate (I) | up (I)]: a = bf16(silu(gate) * up) held in
+// registers, then the per-token quantisation of a (the same arithmetic as
+// quant_per_token_kernel on a materialised a).
+template <int V>
+__global__ void __launch_bounds__(1024) silu_mul_quant_kernel(const uint4 *__restrict__ gate_up, uint2 *__restrict__ out,
+                                                              float *__restrict__ scale_out, int nvec) {
+    const int T = static_cast<int>(blockDim.x);
+    __shared__ float red[32];
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int64_t row = blockIdx.x;
+    const uint4 *gr = gate_up + row * 2 * nvec;
+    const uint4 *ur = gr + nvec;
+    uint2 *orow = out + row * nvec;
+    uint4 a[V];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = threadIdx.x + j * T;
+        if (idx < nvec) {
+            a[j] = silu_mul8(ld_stream(gr + idx), ld_stream(ur + idx));
+            amax = absmax8(a[j], amax);
+        }
+    }
+    amax = block_max(amax, red);
+    const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    if (threadIdx.x == 0) scale_out[row] = s;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = threadIdx.x + j * T;
+        if (idx < nvec) orow[idx] = quant8(a[j], s);
+    }
+}
+
 // ---------------------------------------------------- fused RMSNorm -> quant --
 
 struct CtaSync {
@@ -148,19 +228,20 @@ struct CtaSync {
 };
 
 // One CTA per row; the row arithmetic (exact sum of squares, binary32 chain)
-// is norm::rmsnorm_quant_row, shared with the decode GEMM's fused prologue.
-template <int V>
+// is norm::rmsnorm_quant_row.  With R the row is first the residual sum
+// bf16(x + resid), which also replaces the residual row.
+template <int V, bool R>
 __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gamma,
                                                              float eps, const float *__restrict__ scale,
-                                                             uint2 *__restrict__ out, int nvec, int K) {
+                                                             uint2 *__restrict__ out, int nvec, int K, uint4 *resid) {
     __shared__ norm::RowScratch sc;
     grid_dependency_wait();
     grid_launch_dependents();
     const int64_t row = blockIdx.x;
     const float s = __ldg(scale);
-    norm::rmsnorm_quant_row<V, (V <= 8)>(x + row * nvec, gamma, eps, s, out + row * nvec, nvec, K,
-                                         norm::Group{static_cast<int>(threadIdx.x), static_cast<int>(blockDim.x)}, &sc,
-                                         CtaSync{});
+    norm::rmsnorm_quant_row<V, (V <= 8), R>(x + row * nvec, gamma, eps, s, out + row * nvec, nvec, K,
+                                            norm::Group{static_cast<int>(threadIdx.x), static_cast<int>(blockDim.x)},
+                                            &sc, CtaSync{}, R ? resid + row * nvec : nullptr);
 }
 
 // Threads per row-CTA for `nvec` vectors at V vectors per thread: a multiple
@@ -180,12 +261,26 @@ cudaError_t launch_rows_pt(const void *x, void *out, float *scale_out, int64_t M
 }
 
 template <int V>
+cudaError_t launch_rows_silu(const void *gate_up, void *out, float *scale_out, int64_t M, int64_t I,
+                             cudaStream_t stream, const LaunchOpts &o) {
+    const int64_t nvec = I / 8;
+    return launch_with_opts(silu_mul_quant_kernel<V>, dim3(static_cast<unsigned>(M)), dim3(row_threads(nvec, V)), 0,
+                            stream, o, static_cast<const uint4 *>(gate_up), static_cast<uint2 *>(out), scale_out,
+                            static_cast<int>(nvec));
+}
+
+template <int V>
 cudaError_t launch_rows_rms(const void *x, const void *gamma, float eps, const float *scale, void *out, int64_t M,
-                            int64_t K, cudaStream_t stream, const LaunchOpts &o) {
+                            int64_t K, cudaStream_t stream, const LaunchOpts &o, void *resid) {
     const int64_t nvec = K / 8;
-    return launch_with_opts(rmsnorm_quant_kernel<V>, dim3(static_cast<unsigned>(M)), dim3(row_threads(nvec, V)), 0,
-                            stream, o, static_cast<const uint4 *>(x), static_cast<const uint4 *>(gamma), eps, scale,
-                            static_cast<uint2 *>(out), static_cast<int>(nvec), static_cast<int>(K));
+    const dim3 grid(static_cast<unsigned>(M)), block(row_threads(nvec, V));
+    if (resid != nullptr)
+        return launch_with_opts(rmsnorm_quant_kernel<V, true>, grid, block, 0, stream, o, static_cast<const uint4 *>(x),
+                                static_cast<const uint4 *>(gamma), eps, scale, static_cast<uint2 *>(out),
+                                static_cast<int>(nvec), static_cast<int>(K), static_cast<uint4 *>(resid));
+    return launch_with_opts(rmsnorm_quant_kernel<V, false>, grid, block, 0, stream, o, static_cast<const uint4 *>(x),
+                            static_cast<const uint4 *>(gamma), eps, scale, static_cast<uint2 *>(out),
+                            static_cast<int>(nvec), static_cast<int>(K), static_cast<uint4 *>(nullptr));
 }
 
 }  // namespace
@@ -202,10 +297,17 @@ cudaError_t launch_quant_static(const void *x, const float *scale, void *out, in
                             static_cast<const uint4 *>(x), scale, static_cast<uint4 *>(out), n16);
 }
 
+// Rows per launch from which the per-row kernels trade latency for bytes in
+// flight: with few rows, one 16-byte vector per thread makes each row's serial
+// chain shortest; with many rows, fewer (and busier) threads per row let more
+// rows, and so more loads, be resident on each SM at once.
+inline bool many_rows(int64_t M, int num_sms) { return M >= 4 * static_cast<int64_t>(num_sms); }
+
 cudaError_t launch_quant_per_token(const void *x, void *out, float *scale_out, int64_t M, int64_t K, uint32_t *err,
-                                   cudaStream_t stream, const LaunchOpts &o) {
+                                   cudaStream_t stream, int num_sms, const LaunchOpts &o) {
     (void)err;
     const int64_t nvec = K / 8;
+    if (many_rows(M, num_sms) && nvec <= 1024) return launch_rows_pt<4>(x, out, scale_out, M, K, stream, o);
     if (nvec <= 1024) return launch_rows_pt<1>(x, out, scale_out, M, K, stream, o);
     if (nvec <= 2048) return launch_rows_pt<2>(x, out, scale_out, M, K, stream, o);
     if (nvec <= 4096) return launch_rows_pt<4>(x, out, scale_out, M, K, stream, o);
@@ -215,14 +317,29 @@ cudaError_t launch_quant_per_token(const void *x, void *out, float *scale_out, i
                             static_cast<const uint4 *>(x), static_cast<uint2 *>(out), scale_out, nvec);
 }
 
+cudaError_t launch_silu_mul_quant(const void *gate_up, void *out, float *scale_out, int64_t M, int64_t I,
+                                  uint32_t *err, cudaStream_t stream, int num_sms, const LaunchOpts &o) {
+    (void)err;
+    const int64_t nvec = I / 8;
+    if (many_rows(M, num_sms) && nvec <= 1024) return launch_rows_silu<4>(gate_up, out, scale_out, M, I, stream, o);
+    if (nvec <= 1024) return launch_rows_silu<1>(gate_up, out, scale_out, M, I, stream, o);
+    if (nvec <= 2048) return launch_rows_silu<2>(gate_up, out, scale_out, M, I, stream, o);
+    if (nvec <= 4096) return launch_rows_silu<4>(gate_up, out, scale_out, M, I, stream, o);
+    if (nvec <= 8192) return launch_rows_silu<8>(gate_up, out, scale_out, M, I, stream, o);
+    return launch_rows_silu<16>(gate_up, out, scale_out, M, I, stream, o);
+}
+
 cudaError_t launch_rmsnorm_quant(const void *x, const void *gamma, float eps, const float *scale, void *out,
-                                 int64_t M, int64_t K, uint32_t *err, cudaStream_t stream, const LaunchOpts &o) {
+                                 int64_t M, int64_t K, uint32_t *err, cudaStream_t stream, int num_sms,
+                                 const LaunchOpts &o, void *resid) {
     (void)err;
     const int64_t nvec = K / 8;
-    if (nvec <= 1024) return launch_rows_rms<1>(x, gamma, eps, scale, out, M, K, stream, o);
-    if (nvec <= 2048) return launch_rows_rms<2>(x, gamma, eps, scale, out, M, K, stream, o);
-    if (nvec <= 4096) return launch_rows_rms<4>(x, gamma, eps, scale, out, M, K, stream, o);
-    return launch_rows_rms<8>(x, gamma, eps, scale, out, M, K, stream, o);
+    if (many_rows(M, num_sms) && nvec <= 1024)
+        return launch_rows_rms<4>(x, gamma, eps, scale, out, M, K, stream, o, resid);
+    if (nvec <= 1024) return launch_rows_rms<1>(x, gamma, eps, scale, out, M, K, stream, o, resid);
+    if (nvec <= 2048) return launch_rows_rms<2>(x, gamma, eps, scale, out, M, K, stream, o, resid);
+    if (nvec <= 4096) return launch_rows_rms<4>(x, gamma, eps, scale, out, M, K, stream, o, resid);
+    return launch_rows_rms<8>(x, gamma, eps, scale, out, M, K, stream, o, resid);
 }
 
 }  // namespace fp8k

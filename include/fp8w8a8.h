@@ -186,6 +186,45 @@ fp8_status fp8_scaled_mm_noalloc(const void *A, const void *B, const float *scal
 fp8_status rmsnorm_quant_fp8(const void *x, const void *gamma, float eps, const float *scale, void *out,
                              int64_t M, int64_t K, void *stream);
 
+/* fp8_add_rmsnorm_quant -- residual add, then rmsnorm_quant_fp8, one pass.
+ *
+ * Source: [P3] "Ranked follow-ons from the same audit", second bullet: each
+ * FP8 projection's input should leave its producer already quantised; a
+ * decoder layer's norm input is the residual stream plus the previous block's
+ * output, so the add is folded into the norm-quant producer.
+ *
+ *   x         bf16 [M,K] (the block output), 16-byte aligned
+ *   residual  bf16 [M,K], 16-byte aligned: read, then overwritten IN PLACE
+ *             with h = bf16_rne( fp32(x) + fp32(residual) ) (one binary32
+ *             addition, round to nearest even), the updated residual stream
+ *   gamma, eps, scale, out, M, K   as rmsnorm_quant_fp8, applied to h
+ *
+ * out holds exactly the bytes rmsnorm_quant_fp8(h, ...) would write.  x and
+ * residual must not overlap.  Errors: as rmsnorm_quant_fp8. */
+fp8_status fp8_add_rmsnorm_quant(const void *x, void *residual, const void *gamma, float eps, const float *scale,
+                                 void *out, int64_t M, int64_t K, void *stream);
+
+/* fp8_silu_mul_quant_per_token -- SiLU(gate) * up, then dynamic per-token
+ * E4M3 quantisation: the producer of the down projection's input.
+ *
+ * Source: [P3] "Ranked follow-ons from the same audit", second bullet: every
+ * FP8 projection's input should leave its producer already quantised (here
+ * the MLP's activation, which feeds the down projection).
+ *
+ *   gate_up    bf16 [M, 2I] row-major, 16-byte aligned: each row is
+ *              [gate (I) | up (I)] (the merged gate_up GEMM's output)
+ *   out        E4M3 [M, I], 16-byte aligned
+ *   scale_out  f32 [M] (device): s_m = amax_m / 448 (1.0 for an all-zero row)
+ *   I % 16 == 0, 1 <= I <= 131072
+ *
+ * a = bf16_rne( silu(g) * u ) with silu(g) = g / (1 + e(-g)) in binary32 and
+ * e a fixed binary32 exp (Cody-Waite argument reduction, degree-7 Taylor
+ * polynomial, one IEEE operation per step, within a few ulp of exp); then
+ * out = e4m3(a / s_m) exactly as quant_fp8_per_token on a.
+ * Errors: FP8_ERR_INVALID_ARG, FP8_ERR_ALIGNMENT, FP8_ERR_CUDA. */
+fp8_status fp8_silu_mul_quant_per_token(const void *gate_up, void *out, float *scale_out, int64_t M, int64_t I,
+                                        void *stream);
+
 /* fp8_rmsnorm_quant_scaled_mm -- rmsnorm_quant_fp8 followed by fp8_scaled_mm
  * on its output, as one call ("quantise once": the normalised, quantised
  * activations are written to a_out for the layer's other projections, and

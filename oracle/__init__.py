@@ -49,6 +49,16 @@ def _load():
     lib.oracle_sum_squares_bf16.argtypes = [P, I64]
     lib.oracle_sum_squares_bf16.restype = ctypes.c_float
     lib.oracle_rmsnorm_quant.argtypes = [P, P, ctypes.c_float, ctypes.c_float, I64, I64, P]
+    lib.oracle_residual_add_bf16.argtypes = [P, P, I64, P]
+    lib.oracle_exp_f32.argtypes = [ctypes.c_float]
+    lib.oracle_exp_f32.restype = ctypes.c_float
+    lib.oracle_exp_f32_array.argtypes = [P, I64, P]
+    lib.oracle_silu_f32.argtypes = [ctypes.c_float]
+    lib.oracle_silu_f32.restype = ctypes.c_float
+    lib.oracle_silu_f32_array.argtypes = [P, I64, P]
+    lib.oracle_silu_mul_bf16.argtypes = [P, I64, I64, P]
+    lib.oracle_silu_mul_quant_per_token.argtypes = [P, I64, I64, P, P]
+    lib.oracle_add_rmsnorm_quant.argtypes = [P, P, P, ctypes.c_float, ctypes.c_float, I64, I64, P, P]
     lib.oracle_gemm_acc_f64.argtypes = [P, P, I64, I64, I64, P, ctypes.c_int]
     lib.oracle_gemm_acc_i64.argtypes = [P, P, I64, I64, I64, P, ctypes.c_int]
     lib.oracle_scaled_mm.argtypes = [P, P, P, P, ctypes.c_int, I64, I64, I64, P, P, ctypes.c_int]
@@ -159,6 +169,68 @@ def rmsnorm_quant(x_bf16, gamma_bf16, eps: float, s: float) -> np.ndarray:
     q = np.empty((M, K), np.uint8)
     _load().oracle_rmsnorm_quant(_ptr(x), _ptr(g), ctypes.c_float(eps), ctypes.c_float(s), M, K, _ptr(q))
     return q
+
+
+def residual_add_bf16(x_bf16, r_bf16) -> np.ndarray:
+    x = _c(x_bf16, np.uint16)
+    r = _c(r_bf16, np.uint16)
+    if x.shape != r.shape:
+        raise ValueError("x and r must have the same shape")
+    h = np.empty(x.shape, np.uint16)
+    _load().oracle_residual_add_bf16(_ptr(x), _ptr(r), x.size, _ptr(h))
+    return h
+
+
+def add_rmsnorm_quant(x_bf16, r_bf16, gamma_bf16, eps: float, s: float):
+    """Returns (q E4M3 codes [M,K], h bf16 bits [M,K] = the updated residual)."""
+    x = _c(x_bf16, np.uint16)
+    r = _c(r_bf16, np.uint16)
+    g = _c(gamma_bf16, np.uint16)
+    M, K = x.shape
+    if r.shape != x.shape:
+        raise ValueError("x and r must have the same shape")
+    q = np.empty((M, K), np.uint8)
+    h = np.empty((M, K), np.uint16)
+    _load().oracle_add_rmsnorm_quant(_ptr(x), _ptr(r), _ptr(g), ctypes.c_float(eps), ctypes.c_float(s), M, K,
+                                     _ptr(q), _ptr(h))
+    return q, h
+
+
+def exp_f32(y) -> np.ndarray:
+    y = _c(np.atleast_1d(y), np.float32)
+    out = np.empty(y.shape, np.float32)
+    _load().oracle_exp_f32_array(_ptr(y), y.size, _ptr(out))
+    return out
+
+
+def silu_f32(g) -> np.ndarray:
+    g = _c(np.atleast_1d(g), np.float32)
+    out = np.empty(g.shape, np.float32)
+    _load().oracle_silu_f32_array(_ptr(g), g.size, _ptr(out))
+    return out
+
+
+def silu_mul_bf16(gate_up_bf16) -> np.ndarray:
+    """bf16 bits [M, I] of silu(gate) * up for rows [gate | up] ([M, 2I])."""
+    x = _c(gate_up_bf16, np.uint16)
+    M, W = x.shape
+    if W % 2:
+        raise ValueError("gate_up rows must have an even width")
+    a = np.empty((M, W // 2), np.uint16)
+    _load().oracle_silu_mul_bf16(_ptr(x), M, W // 2, _ptr(a))
+    return a
+
+
+def silu_mul_quant_per_token(gate_up_bf16):
+    """(E4M3 codes [M, I], per-token scales [M]) of silu(gate) * up."""
+    x = _c(gate_up_bf16, np.uint16)
+    M, W = x.shape
+    if W % 2:
+        raise ValueError("gate_up rows must have an even width")
+    q = np.empty((M, W // 2), np.uint8)
+    s = np.empty((M,), np.float32)
+    _load().oracle_silu_mul_quant_per_token(_ptr(x), M, W // 2, _ptr(q), _ptr(s))
+    return q, s
 
 
 # --- GEMM --------------------------------------------------------------------

@@ -320,6 +320,115 @@ void oracle_rmsnorm_quant(const uint16_t *x, const uint16_t *gamma, float eps, f
     free(h);
 }
 
+/* Residual add in front of the norm (reading R18): the layer's norm input is
+ * the residual stream plus the block's output, h_k = bf16( fp32(x_k) +
+ * fp32(r_k) ) -- one IEEE binary32 addition (round to nearest even), then bf16
+ * round to nearest even.  [P3] "Ranked follow-ons from the same audit",
+ * second bullet: every FP8 projection's input should come out of its producer
+ * already quantised ("quantise once"), the input norm of a decoder layer
+ * being that producer. */
+void oracle_residual_add_bf16(const uint16_t *x, const uint16_t *r, int64_t n, uint16_t *h) {
+    for (int64_t i = 0; i < n; ++i) {
+        volatile float a = oracle_bf16_to_f32(x[i]);
+        volatile float b = oracle_bf16_to_f32(r[i]);
+        volatile float c = a + b;
+        h[i] = oracle_bf16_rne_f32(c);
+    }
+}
+
+/* Fused residual add -> RMSNorm -> static FP8 quant: h as above (also
+ * returned: it is the updated residual stream), then oracle_rmsnorm_quant(h). */
+void oracle_add_rmsnorm_quant(const uint16_t *x, const uint16_t *r, const uint16_t *gamma, float eps, float s,
+                              int64_t M, int64_t K, uint8_t *q, uint16_t *h) {
+    oracle_residual_add_bf16(x, r, M * K, h);
+    oracle_rmsnorm_quant(h, gamma, eps, s, M, K, q);
+}
+
+/* SiLU(gate) * up -> dynamic per-token FP8 quant: the producer of the down
+ * projection's input (reading R19).  [P3] "Ranked follow-ons from the same
+ * audit", second bullet: every FP8 projection's input should leave its
+ * producer already quantised.  The pages print no formula, so:
+ *   e(y)   = exp(y) in binary32 by the method below,
+ *   s(g)   = g / (1 + e(-g))               (binary32 add and division),
+ *   a      = bf16_rne( s(g) * u )           (binary32 multiply; bf16 intermediate,
+ *                                            so fused == "SiLU-mul to bf16, then
+ *                                            per-token quant" byte for byte),
+ *   q, s_m = the per-token quantisation of the bf16 row a (R4).
+ * gate_up rows hold [gate (I) | up (I)].
+ *
+ * exp in binary32 (Cody and Waite's argument reduction, W. J. Cody and W.
+ * Waite, "Software Manual for the Elementary Functions", 1980): n =
+ * rint(y * log2(e)); r = (y - n * C1) - n * C2 with C1 + C2 = ln 2 and C1 a
+ * short constant (so n * C1 is exact for |n| <= 128); e^r by its Taylor
+ * series to degree 7 in Horner form; times 2^n.  Every step is one IEEE
+ * binary32 operation (round to nearest even; no fused multiply-add).  Inputs
+ * below -87 give 0 and above 88 give +inf (so every 2^n is a normal number);
+ * NaN gives NaN.  It is within a few units in the last place of exp (pinned
+ * against binary64 exp by the tests). */
+static const float kLog2e = 1.44269504088896340736f;   /* log2(e) rounded to binary32 */
+static const float kLn2Hi = 0.693145751953125f;         /* 0x3F317200: ln 2 to 16 bits */
+static const float kLn2Lo = 1.428606765330187045e-06f;  /* ln 2 - kLn2Hi, rounded */
+
+float oracle_exp_f32(float y) {
+    if (y != y) return y;
+    if (y < -87.0f) return 0.0f;
+    if (y > 88.0f) return INFINITY;
+    volatile float t = y * kLog2e;
+    const float n = rintf(t);
+    volatile float a = n * kLn2Hi;
+    volatile float r1 = y - a;
+    volatile float b = n * kLn2Lo;
+    volatile float r = r1 - b;
+    /* 1 + r + r^2/2! + ... + r^7/7!, Horner: ((((((c7 r + c6) r + c5) r + c4) r + c3) r + c2) r + 1) r + 1 */
+    static const float c[8] = {1.0f, 1.0f, 0.5f, 1.0f / 6.0f, 1.0f / 24.0f, 1.0f / 120.0f, 1.0f / 720.0f,
+                               1.0f / 5040.0f};
+    volatile float p = c[7];
+    for (int i = 6; i >= 0; --i) {
+        volatile float pr = p * r;
+        p = pr + c[i];
+    }
+    const int ni = (int)n;
+    uint32_t bits = (uint32_t)(ni + 127) << 23;
+    float two_n;
+    memcpy(&two_n, &bits, sizeof two_n);
+    volatile float out = p * two_n;
+    return out;
+}
+
+void oracle_exp_f32_array(const float *y, int64_t n, float *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_exp_f32(y[i]);
+}
+
+float oracle_silu_f32(float g) {
+    volatile float e = oracle_exp_f32(-g);
+    volatile float d = 1.0f + e;
+    volatile float s = g / d;
+    return s;
+}
+
+void oracle_silu_f32_array(const float *g, int64_t n, float *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_silu_f32(g[i]);
+}
+
+/* a = bf16( silu(gate) * up ) for rows [gate | up] of width 2I. */
+void oracle_silu_mul_bf16(const uint16_t *gate_up, int64_t M, int64_t I, uint16_t *a) {
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *row = gate_up + m * 2 * I;
+        for (int64_t k = 0; k < I; ++k) {
+            volatile float s = oracle_silu_f32(oracle_bf16_to_f32(row[k]));
+            volatile float v = s * oracle_bf16_to_f32(row[I + k]);
+            a[m * I + k] = oracle_bf16_rne_f32(v);
+        }
+    }
+}
+
+void oracle_silu_mul_quant_per_token(const uint16_t *gate_up, int64_t M, int64_t I, uint8_t *q, float *s_out) {
+    uint16_t *a = (uint16_t *)malloc((size_t)(M * I > 0 ? M * I : 1) * sizeof(uint16_t));
+    oracle_silu_mul_bf16(gate_up, M, I, a);
+    oracle_quant_per_token(a, M, I, q, s_out);
+    free(a);
+}
+
 /* ------------------------------------------------------------------------- */
 /* The scaled GEMM ([P1] "What is owed" item 2 and "CORRECTION": bmm_fp8(a,  */
 /* b, scale_a, scale_b, out_dtype, ...); [P3] "FINDING 1": out dtype bf16;   */

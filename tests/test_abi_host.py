@@ -114,6 +114,28 @@ def test_fused_norm_mm_validation(L):
     assert call(N=68) == 2
 
 
+def test_add_rmsnorm_validation(L):
+    f = L.fp8_add_rmsnorm_quant
+    e = ctypes.c_float(1e-6)
+    R = P(0x60000)
+    assert f(GOOD, R, GOOD2, e, SC, GOOD3, 0, 64, None) == 0
+    assert f(GOOD, None, GOOD2, e, SC, GOOD3, 4, 64, None) == 1
+    assert f(GOOD, R, GOOD2, e, SC, GOOD3, 4, 65552, None) == 1
+    assert f(GOOD, P(0x60008), GOOD2, e, SC, GOOD3, 4, 64, None) == 2
+    assert f(GOOD, R, GOOD2, e, SC, GOOD3, 4, 40, None) == 2
+
+
+def test_silu_mul_quant_validation(L):
+    f = L.fp8_silu_mul_quant_per_token
+    assert f(GOOD, GOOD2, SC, 0, 64, None) == 0
+    assert f(None, GOOD2, SC, 4, 64, None) == 1
+    assert f(GOOD, GOOD2, None, 4, 64, None) == 1
+    assert f(GOOD, GOOD2, SC, 4, 131072 + 16, None) == 1
+    assert f(GOOD, GOOD2, SC, 4, 0, None) == 1
+    assert f(GOOD, GOOD2, SC, 4, 40, None) == 2
+    assert f(GOOD, P(0x20008), SC, 4, 64, None) == 2
+
+
 def test_quantiser_validation(L):
     assert L.quant_fp8_static(GOOD, SC, GOOD2, 0, 64, None) == 0
     assert L.quant_fp8_static(None, SC, GOOD2, 4, 64, None) == 1

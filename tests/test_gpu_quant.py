@@ -56,7 +56,7 @@ def test_static_quant_large_and_guarded(fp8, orc):
     assert buf.intact()
 
 
-@pytest.mark.parametrize("M,K", [(1, 16), (3, 48), (7, 5120), (64, 5120), (33, 8192), (5, 8208),
+@pytest.mark.parametrize("M,K", [(1, 16), (3, 48), (7, 5120), (64, 5120), (33, 8192), (5, 8208), (700, 8192), (999, 48),
                                  (9, 17408), (2, 32768), (3, 40000), (2, 65536), (1, 65552), (1, 131072)])
 def test_per_token_shapes(fp8, orc, M, K):
     """Covers every kernel variant: 128x8, 256x16 and 512x16 register-resident
@@ -125,7 +125,8 @@ def test_rmsnorm_quant_decode_fused(fp8, orc, M):
 
 
 @pytest.mark.parametrize("M,K,eps,s", [(32, 5120, 1e-6, 1 / 112), (5, 16, 1e-6, 1 / 56), (3, 17408, 1e-5, 0.02),
-                                       (2, 65536, 0.0, 0.01), (4, 8192, 1e-6, 1 / 56), (300, 5120, 1e-6, 1 / 56)])
+                                       (2, 65536, 0.0, 0.01), (4, 8192, 1e-6, 1 / 56), (300, 5120, 1e-6, 1 / 56),
+                                       (1000, 5120, 1e-6, 1 / 56), (640, 8192, 1e-5, 0.02)])
 def test_rmsnorm_quant_shapes(fp8, orc, M, K, eps, s):
     g = workloads.rng(40 + K)
     x = workloads.bf16_normal(g, (M, K))
@@ -186,3 +187,70 @@ def test_rmsnorm_exact_sum_edge_rows(fp8, orc):
         nan_w = (want & 0x7F) == 0x7F
         assert np.array_equal(q[~nan_w], want[~nan_w]), eps
         assert np.all((q[nan_w] & 0x7F) == 0x7F), eps
+
+
+@pytest.mark.parametrize("M,K", [(1, 5120), (8, 5120), (32, 5120), (3, 17408), (1000, 5120), (5, 16)])
+def test_add_rmsnorm_quant(fp8, orc, M, K):
+    """Residual add -> RMSNorm -> static quant: the E4M3 bytes and the updated
+    residual (in place) bit-exact against the oracle, including residual
+    values that overflow the sum and signed zeros."""
+    g = workloads.rng(80 + M + K)
+    x = workloads.bf16_normal(g, (M, K))
+    r = workloads.bf16_normal(g, (M, K), std=4.0)
+    gamma = workloads.bf16_normal(g, (K,), mean=1.0, std=0.1)
+    r[0, :4] = [0x8000, 0x0000, 0x7F7F, 0xFF7F]
+    x[0, :4] = [0x8000, 0x8000, 0x7F7F, 0x3F80]
+    s = float(np.float32(1 / 56))
+    want_q, want_h = orc.add_rmsnorm_quant(x, r, gamma, 1e-6, s)
+    rd = to_dev_bf16(r)
+    q = fp8.add_rmsnorm_quant_fp8(to_dev_bf16(x), rd, to_dev_bf16(gamma), 1e-6, to_dev_f32(s))
+    assert np.array_equal(host_bits(rd), want_h)
+    qh = host_bits(q)
+    nan_w = (want_q & 0x7F) == 0x7F
+    assert np.array_equal(qh[~nan_w], want_q[~nan_w])
+    assert np.all((qh[nan_w] & 0x7F) == 0x7F)
+
+
+def test_add_rmsnorm_equals_add_then_norm(fp8, orc):
+    """Fused == the residual sum materialised, then rmsnorm_quant_fp8 on it."""
+    d = workloads.decode_fused(seed=9)
+    g = workloads.rng(90)
+    r = workloads.bf16_normal(g, d["x"].shape, std=0.5)
+    s = to_dev_f32(d["s_a"])
+    rd = to_dev_bf16(r)
+    q = host_bits(fp8.add_rmsnorm_quant_fp8(to_dev_bf16(d["x"]), rd, to_dev_bf16(d["gamma"]), d["eps"], s))
+    h = orc.residual_add_bf16(d["x"], r)
+    q2 = host_bits(fp8.rmsnorm_quant_fp8(to_dev_bf16(h), to_dev_bf16(d["gamma"]), d["eps"], s))
+    assert np.array_equal(q, q2)
+    assert np.array_equal(host_bits(rd), h)
+
+
+@pytest.mark.parametrize("M,I", [(1, 17408), (8, 17408), (3, 16), (1000, 1024), (5, 2064), (2, 65536)])
+def test_silu_mul_quant_per_token(fp8, orc, M, I):
+    """SiLU(gate) * up -> per-token quant, bit-exact (codes and scales) against
+    the oracle on MLP-like rows ([gate | up], N(0,1) with 1% outliers x20),
+    including all-zero rows and large negative gates."""
+    g = workloads.rng(100 + M + I)
+    gu = workloads.bf16_normal_with_outliers(g, (M, 2 * I))
+    if M > 2:
+        gu[2] = 0
+    gu[0, :8] = [0xC2C8, 0x42C8, 0xFF80, 0x7F80, 0x0001, 0x8001, 0x3F80, 0xBF80]   # -100, 100, -inf, inf, ...
+    q, s = fp8.silu_mul_quant_per_token(to_dev_bf16(gu))
+    wq, ws = orc.silu_mul_quant_per_token(gu)
+    sh, qh = host_bits(s), host_bits(q)
+    ok_rows = np.isfinite(ws)
+    assert np.array_equal(sh[ok_rows], ws[ok_rows])
+    assert np.all(np.isnan(sh[~ok_rows]) | np.isinf(sh[~ok_rows]))
+    nan_w = (wq & 0x7F) == 0x7F
+    assert np.array_equal(qh[ok_rows][~nan_w[ok_rows]], wq[ok_rows][~nan_w[ok_rows]])
+
+
+def test_silu_mul_quant_equals_unfused(fp8, orc):
+    """Fused == the bf16 intermediate materialised (oracle), then the GPU's
+    per-token quantiser on it."""
+    g = workloads.rng(101)
+    gu = workloads.bf16_normal(g, (16, 2 * 4096), std=2.0)
+    q, s = fp8.silu_mul_quant_per_token(to_dev_bf16(gu))
+    a = orc.silu_mul_bf16(gu)
+    q2, s2 = fp8.quant_fp8_per_token(to_dev_bf16(a))
+    assert np.array_equal(host_bits(q), host_bits(q2)) and np.array_equal(host_bits(s), host_bits(s2))

@@ -197,3 +197,156 @@ def test_rmsnorm_quant_is_norm_then_static_quant(orc):
     # zero rows: eps keeps the root finite and every code is zero
     z = np.zeros((2, 1024), np.uint16)
     assert np.all(orc.rmsnorm_quant(z, gamma, 1e-6, s) == 0)
+
+
+# --------------------------------------------------------------------------- residual add (R18)
+
+def _bf16_bits_of_f32(v32):
+    """float32 -> bf16 bits by torch's round-to-nearest-even cast (a library
+    primitive, pinned separately against exact rationals)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(v32, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_residual_add_is_f32_sum_then_bf16(orc):
+    """h = bf16(fp32(x) + fp32(r)): against numpy's IEEE binary32 addition
+    followed by torch's RNE cast, on random pairs with every exponent gap
+    (exact fp32 sums and rounded ones), both signs, zeros and subnormals."""
+    g = np.random.default_rng(70)
+    x = workloads.bf16_normal(g, (4096,), std=1.0)
+    r = workloads.bf16_normal(g, (4096,), std=1.0)
+    scale = (2.0 ** g.integers(-40, 40, 4096)).astype(np.float32)
+    r = (((r.astype(np.uint32) << 16).view(np.float32) * scale).view(np.uint32) >> 16).astype(np.uint16)
+    r[:16] = [0, 0x8000, 0x0001, 0x8001, 0x7F7F, 0xFF7F, 0x3F80, 0xBF80] * 2
+    x[:16] = [0, 0, 0x0001, 0x0001, 0x7F7F, 0x7F7F, 0xBF80, 0x3F80] + [0x4000] * 8
+    with np.errstate(over="ignore"):
+        want = _bf16_bits_of_f32((x.astype(np.uint32) << 16).view(np.float32)
+                                 + (r.astype(np.uint32) << 16).view(np.float32))
+    h = orc.residual_add_bf16(x, r)
+    assert np.array_equal(h, want)
+    assert np.array_equal(orc.residual_add_bf16(r, x), h)          # commutative
+    assert h[4] == 0x7F80                                          # max + max overflows to +inf
+    assert h[6] == 0x0000                                          # -1 + 1 = +0 (round to nearest)
+
+
+def test_residual_add_exact_rationals(orc):
+    """Where the binary32 sum is exact (exponent gap <= 16), h is the exact
+    rational sum rounded once to bf16 (ties to even), computed with fractions."""
+    from fractions import Fraction
+    g = np.random.default_rng(71)
+    xs = workloads.bf16_normal(g, (300,))
+    rs = workloads.bf16_normal(g, (300,), std=0.05)
+    h = orc.residual_add_bf16(xs, rs)
+
+    def val(b):
+        return Fraction(float((np.uint32(b) << np.uint32(16)).view(np.float32)))
+
+    def bf16_rne(q):
+        if q == 0:
+            return 0.0
+        sgn = -1 if q < 0 else 1
+        a = abs(q)
+        e = 0
+        while a >= 2:
+            a /= 2
+            e += 1
+        while a < 1:
+            a *= 2
+            e -= 1
+        unit = Fraction(1, 128)
+        k = a / unit
+        lo = int(k)
+        rem = k - lo
+        if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and lo % 2 == 1):
+            lo += 1
+        return sgn * float(lo * unit * Fraction(2) ** e)
+
+    checked = 0
+    for a, b, got in zip(xs, rs, h):
+        fa, fb = val(a), val(b)
+        if fa == 0 or fb == 0:
+            continue
+        ea = int(np.floor(np.log2(abs(float(fa)))))
+        eb = int(np.floor(np.log2(abs(float(fb)))))
+        if abs(ea - eb) > 16:
+            continue
+        want = bf16_rne(fa + fb)
+        assert float((np.uint32(got) << np.uint32(16)).view(np.float32)) == want
+        checked += 1
+    assert checked > 200
+
+
+def test_add_rmsnorm_quant_composition(orc):
+    """The fused producer is residual add, then the pinned RMSNorm -> quant;
+    a zero residual gives exactly rmsnorm_quant(x) (x has no negative zeros,
+    which the add would turn into +0)."""
+    d = workloads.decode_fused(seed=7)
+    g = np.random.default_rng(72)
+    r = workloads.bf16_normal(g, d["x"].shape, std=0.5)
+    s = float(d["s_a"])
+    q, h = orc.add_rmsnorm_quant(d["x"], r, d["gamma"], d["eps"], s)
+    assert np.array_equal(h, orc.residual_add_bf16(d["x"], r))
+    assert np.array_equal(q, orc.rmsnorm_quant(h, d["gamma"], d["eps"], s))
+    z = np.zeros_like(d["x"])
+    q0, h0 = orc.add_rmsnorm_quant(d["x"], z, d["gamma"], d["eps"], s)
+    assert np.array_equal(q0, orc.rmsnorm_quant(d["x"], d["gamma"], d["eps"], s))
+
+
+# --------------------------------------------------------------------------- SiLU * up -> per-token quant (R19)
+
+def test_exp_f32_within_two_ulp_of_binary64(orc):
+    y = np.linspace(-87.0, 88.0, 400001).astype(np.float32)
+    e = orc.exp_f32(y).astype(np.float64)
+    t = np.exp(y.astype(np.float64))
+    ulp = np.spacing(t.astype(np.float32)).astype(np.float64)
+    assert np.max(np.abs(e - t) / ulp) <= 2.0
+    assert np.all(np.diff(e) >= 0)                       # monotone on the sweep
+    assert orc.exp_f32(np.float32(0.0))[0] == 1.0
+    assert orc.exp_f32(np.float32(1.0))[0] == np.float32(np.e)
+    sp = orc.exp_f32(np.array([np.nan, -100.0, -87.5, 100.0, np.inf, -np.inf], np.float32))
+    assert np.isnan(sp[0]) and sp[1] == 0.0 and sp[2] == 0.0 and np.isinf(sp[3]) and np.isinf(sp[4])
+    assert sp[5] == 0.0
+
+
+def test_silu_against_binary64(orc):
+    """silu(g) = g / (1 + e(-g)) within 4 ulp of the binary64 value
+    g / (1 + exp(-g)) over [-80, 80], exact special cases."""
+    g = np.linspace(-80.0, 80.0, 200001).astype(np.float32)
+    got = orc.silu_f32(g).astype(np.float64)
+    ref = g.astype(np.float64) / (1.0 + np.exp(-g.astype(np.float64)))
+    ulp = np.maximum(np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64), 1e-45)
+    assert np.max(np.abs(got - ref) / ulp) <= 4.0
+    sp = orc.silu_f32(np.array([0.0, np.inf, -100.0, np.nan], np.float32))
+    assert sp[0] == 0.0 and sp[1] == np.inf
+    assert sp[2] == 0.0 and np.signbit(sp[2])            # -100 / inf = -0
+    assert np.isnan(sp[3])
+
+
+def test_silu_mul_bf16_definition(orc):
+    """a = bf16(silu(g) * u): the binary32 product of the pinned silu and u,
+    rounded by torch's RNE cast; gate is the first half of each row."""
+    import torch
+    g = np.random.default_rng(73)
+    gu = workloads.bf16_normal(g, (3, 2 * 64), std=3.0)
+    a = orc.silu_mul_bf16(gu)
+    gate = (gu[:, :64].astype(np.uint32) << 16).view(np.float32)
+    up = (gu[:, 64:].astype(np.uint32) << 16).view(np.float32)
+    s = orc.silu_f32(gate).reshape(gate.shape)
+    want = torch.from_numpy(s * up).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(a, want)
+
+
+def test_silu_mul_quant_composition(orc):
+    """The fused producer equals the per-token quantisation of the bf16
+    intermediate; its amax element maps to +-448."""
+    g = np.random.default_rng(74)
+    gu = workloads.bf16_normal_with_outliers(g, (4, 2 * 256))
+    gu[1] = 0
+    q, s = orc.silu_mul_quant_per_token(gu)
+    a = orc.silu_mul_bf16(gu)
+    q2, s2 = orc.quant_per_token(a)
+    assert np.array_equal(q, q2) and np.array_equal(s, s2)
+    assert s[1] == 1.0 and np.all(q[1] == 0)
+    for m in (0, 2, 3):
+        assert np.max(q[m] & 0x7F) == 0x7E
