@@ -72,6 +72,8 @@ def lib():
     L.fp8_scaled_mm_ex.restype = I32
     L.fp8_rmsnorm_quant_scaled_mm.argtypes = [P, P, F32, P, P, P, I32, I32, I64, I64, I64, P, P, P, ctypes.c_uint]
     L.fp8_rmsnorm_quant_scaled_mm.restype = I32
+    L.fp8_requant_merge.argtypes = [P, P, P, I32, I64, P, P, P]
+    L.fp8_requant_merge.restype = I32
     L.fp8_silu_mul_quant_per_token.argtypes = [P, P, P, I64, I64, P]
     L.fp8_silu_mul_quant_per_token.restype = I32
     L.fp8_add_rmsnorm_quant.argtypes = [P, P, P, F32, P, P, I64, I64, P]
@@ -260,6 +262,35 @@ def silu_mul_quant_per_token(gate_up, out=None, scale_out=None):
         _need(scale_out, "scale_out", (torch.float32,))
     _check(lib().fp8_silu_mul_quant_per_token(_ptr(gate_up), _ptr(out), _ptr(scale_out), M, I,
                                               _stream_of(gate_up)), "fp8_silu_mul_quant_per_token")
+    return out, scale_out
+
+
+def requant_merge(shards, scales, out=None, scale_out=None):
+    """Merge E4M3 weight shards [rows_j, K] with per-tensor scales (1-element
+    f32 tensors) into one [sum rows_j, K] weight requantised to the largest
+    scale; returns (merged, scale)."""
+    if not shards or len(shards) != len(scales):
+        raise ValueError("one scale per shard")
+    K = shards[0].shape[1]
+    for w, sc in zip(shards, scales):
+        _need(w, "shard", _FP8, 2)
+        _need(sc, "scale", (torch.float32,))
+        if w.shape[1] != K:
+            raise ValueError("every shard must have K columns")
+    n = len(shards)
+    rows = (ctypes.c_int64 * n)(*[int(w.shape[0]) for w in shards])
+    ptrs = (ctypes.c_void_p * n)(*[w.data_ptr() for w in shards])
+    sptrs = (ctypes.c_void_p * n)(*[sc.data_ptr() for sc in scales])
+    total = sum(int(w.shape[0]) for w in shards)
+    if out is None:
+        out = torch.empty((total, K), dtype=E4M3, device=shards[0].device)
+    else:
+        _need(out, "out", _FP8, 2)
+    if scale_out is None:
+        scale_out = torch.empty((1,), dtype=torch.float32, device=shards[0].device)
+    _check(lib().fp8_requant_merge(ctypes.cast(ptrs, ctypes.c_void_p), ctypes.cast(sptrs, ctypes.c_void_p),
+                                   ctypes.cast(rows, ctypes.c_void_p), n, K, _ptr(out), _ptr(scale_out),
+                                   _stream_of(shards[0])), "fp8_requant_merge")
     return out, scale_out
 
 

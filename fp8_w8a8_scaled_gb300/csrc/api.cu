@@ -204,7 +204,7 @@ fp8_status fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, 
         if (static_cast<int64_t>(plan.m_tiles) * plan.n_tiles > kI32Max) return FP8_ERR_UNSUPPORTED;
         CUtensorMap ta, tb;
         if ((s = make_tmap_e4m3(&ta, A, M, K, fp8k::kPrefillBM)) != FP8_OK) return s;
-        if ((s = make_tmap_e4m3(&tb, B, N, K, fp8k::kPrefillBN)) != FP8_OK) return s;
+        if ((s = make_tmap_e4m3(&tb, B, N, K, static_cast<uint32_t>(plan.bn))) != FP8_OK) return s;
         return from_cuda(fp8k::launch_prefill_gemm(ta, tb, scale_a, scale_b, granularity, M, N, K, out, st->err,
                                                    plan, opts, static_cast<cudaStream_t>(stream)));
     }
@@ -321,6 +321,35 @@ fp8_status fp8_silu_mul_quant_per_token(const void *gate_up, void *out, float *s
     if (s != FP8_OK) return s;
     return from_cuda(fp8k::launch_silu_mul_quant(gate_up, out, scale_out, M, I, st->err,
                                                  static_cast<cudaStream_t>(stream), st->num_sms, fp8k::LaunchOpts{}));
+}
+
+fp8_status fp8_requant_merge(const void *const *shards, const float *const *scales, const int64_t *rows,
+                             int n_shards, int64_t K, void *out, float *scale_out, void *stream) {
+    if (!shards || !scales || !rows || !out || !scale_out) return FP8_ERR_INVALID_ARG;
+    if (n_shards < 1 || n_shards > fp8k::kMaxMergeShards || K < 1 || K > kI32Max) return FP8_ERR_INVALID_ARG;
+    if (K % 16 != 0) return FP8_ERR_ALIGNMENT;
+    if (!aligned16(out) || !aligned4(scale_out)) return FP8_ERR_ALIGNMENT;
+    fp8k::MergeArgs a{};
+    int64_t total_rows = 0;
+    for (int j = 0; j < n_shards; ++j) {
+        if (rows[j] < 0 || rows[j] > kI32Max) return FP8_ERR_INVALID_ARG;
+        if (rows[j] > 0 && (!shards[j] || !scales[j])) return FP8_ERR_INVALID_ARG;
+        if (!scales[j]) return FP8_ERR_INVALID_ARG;
+        if ((shards[j] && !aligned16(shards[j])) || !aligned4(scales[j])) return FP8_ERR_ALIGNMENT;
+        total_rows += rows[j];
+        a.src[j] = static_cast<const uint4 *>(shards[j]);
+        a.scale[j] = scales[j];
+        a.end16[j] = total_rows * K / 16;
+    }
+    if (total_rows > kI32Max) return FP8_ERR_INVALID_ARG;
+    a.n = n_shards;
+    a.out = static_cast<uint4 *>(out);
+    a.scale_out = scale_out;
+    a.n16 = total_rows * K / 16;
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    return from_cuda(fp8k::launch_requant_merge(a, static_cast<cudaStream_t>(stream), st->num_sms, fp8k::LaunchOpts{}));
 }
 
 fp8_status quant_fp8_per_token(const void *x, void *out, float *scale_out, int64_t M, int64_t K, void *stream) {

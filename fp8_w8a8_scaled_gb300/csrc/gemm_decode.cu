@@ -12,7 +12,7 @@
 // Design (GB300, sm_103a).  At decode M every weight byte is used M times, so
 // the kernel is bound by streaming B from HBM once, and every SM must stream
 // its equal share all the time.  The work is cut into units of one output tile
-// (128 weight rows x up to 32 tokens) by one 128-wide k-block; a persistent
+// (128 weight rows x up to 16 tokens) by one 128-wide k-block; a persistent
 // grid of two CTAs per SM gives CTA c the contiguous units
 // [c*U/G, (c+1)*U/G) ("stream-K"), so all CTAs stream the same number of bytes
 // whatever the shape.  Inside a CTA:
@@ -20,7 +20,7 @@
 //     matching token boxes with TMA into a ring of shared-memory stages
 //     (128-byte swizzle), L2 evict-first for the once-read weights;
 //   * warp 1 / lane 0 issues tcgen05.mma kind::f8f6f4 with the WEIGHTS as the
-//     128-row A operand and the tokens (padded to 16/32) as the N side
+//     128-row A operand and the tokens (padded to 16) as the N side
 //     ("swap-AB").  Each k-block is accumulated from zero into one of several
 //     TMEM buffers; tcgen05.commit frees the stage and hands the buffer on;
 //   * 4 drain warps read each k-block's fp32 partial out of TMEM
@@ -51,8 +51,7 @@ constexpr uint32_t kWTileBytes = kDecodeRows * kBlockK;  // 16 KB of weights per
 
 template <int TOK>
 struct DecodeCfg {
-    // one warpgroup drains TMEM (up to 32 token columns per thread: fewer,
-    // fatter threads keep the 32-token tile's drain free of register spills)
+    // one warpgroup drains TMEM, all TOK token columns per thread
     static constexpr int kDrainGroups = 1;
     static constexpr int kCols = TOK / kDrainGroups;  // token columns per drain thread
     static constexpr int kDrainThreads = 128 * kDrainGroups;
@@ -449,7 +448,7 @@ static size_t decode_smem_bytes(int tok, int stages) {
 
 DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, int num_sms) {
     DecodePlan p{};
-    p.tok_pad = M <= 16 ? 16 : 32;
+    p.tok_pad = 16;
     p.stages = 3;  // ~55-75 KB: two CTAs of this kernel and one of the next fit on an SM
     p.smem_bytes = decode_smem_bytes(p.tok_pad, p.stages);
     p.n_tiles = static_cast<int>((N + kDecodeRows - 1) / kDecodeRows);
@@ -493,10 +492,7 @@ cudaError_t launch_decode_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tma
     a.n_tiles = plan.n_tiles;
     a.stages = plan.stages;
     a.weights_static = opts.weights_static ? 1 : 0;
-    switch (plan.tok_pad) {
-        case 16: return launch_tok<16>(tmap_w, tmap_a, a, plan, opts, stream);
-        default: return launch_tok<32>(tmap_w, tmap_a, a, plan, opts, stream);
-    }
+    return launch_tok<16>(tmap_w, tmap_a, a, plan, opts, stream);
 }
 
 }  // namespace fp8k

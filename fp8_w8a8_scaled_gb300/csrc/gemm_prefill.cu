@@ -12,6 +12,9 @@
 // Design (GB300, sm_103a).  At prefill M every weight byte feeds >= 128 tokens
 // and the kernel is bound by the FP8 tensor-core rate.  One persistent CTA per
 // SM walks the 128-token x 256-channel output tiles t = blockIdx.x + i*gridDim.x
+// (128-channel tiles when M is small and 256-channel ones would leave most SMs
+// idle: there the time goes into streaming the weights, and twice the CTAs
+// stream them twice as fast)
 // (token tile fastest, so the CTAs resident at one time share their weight
 // rows through L2 and the whole token matrix stays L2-resident):
 //   * warp 0 / lane 0 loads, per 128-byte k-block, the 128 x 128-byte token box
@@ -39,11 +42,16 @@ namespace {
 constexpr int kPrefillThreads = 64 + 256;  // producer warp, MMA warp, 8 epilogue warps
 constexpr int kPrefillEpiWarps = 8;
 constexpr uint32_t kPrefillATile = kPrefillBM * kBlockK;  // 16 KB of tokens per stage
-constexpr uint32_t kPrefillBTile = kPrefillBN * kBlockK;  // 32 KB of weights per stage
-constexpr uint32_t kPrefillStageBytes = kPrefillATile + kPrefillBTile;
-constexpr uint32_t kPrefillTmemCols = 2 * kPrefillBN;  // two accumulators: all 512 columns
-constexpr uint32_t kPrefillIdesc = idesc_e4m3_f32(kPrefillBM, kPrefillBN);
-constexpr int kPrefillMaxStages = 4;
+// The output tile is 128 tokens x BN channels, BN = 256 (the largest MMA N) or
+// 128 (twice the CTAs for small M, whose time goes into streaming weights).
+template <int BN>
+struct PrefillCfg {
+    static constexpr uint32_t kBTile = BN * kBlockK;             // weights per stage
+    static constexpr uint32_t kStageBytes = kPrefillATile + kBTile;
+    static constexpr uint32_t kTmemCols = 2 * BN;                 // two accumulators
+    static constexpr uint32_t kIdesc = idesc_e4m3_f32(kPrefillBM, BN);
+    static constexpr int kStages = BN == 256 ? 4 : 6;             // 192 KB of stages either way
+};
 // k-blocks (of 128) the tensor core accumulates in TMEM before the epilogue
 // adds the partial sum into fp32 registers.  The tensor core's accumulation is
 // less exact than binary32 round-to-nearest over many MMAs: on prefill-chunk
@@ -92,6 +100,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                         const PrefillArgs args) {
@@ -103,7 +112,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int stages = args.stages;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t bar0 = base + static_cast<uint32_t>(stages) * kPrefillStageBytes;
+    using Cfg = PrefillCfg<BN>;
+    const uint32_t bar0 = base + static_cast<uint32_t>(stages) * Cfg::kStageBytes;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (stages + s); };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * stages + b); };
@@ -131,7 +141,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         s_consumed = 0;
         s_abort = 0;
     }
-    if (warp == 1) tmem_alloc(smem_u32(&s_tmem_base), kPrefillTmemCols);
+    if (warp == 1) tmem_alloc(smem_u32(&s_tmem_base), Cfg::kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -151,10 +161,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t stage = base + static_cast<uint32_t>(s) * kPrefillStageBytes;
-                mbar_arrive_expect_tx(full_bar(s), kPrefillStageBytes);
+                const uint32_t stage = base + static_cast<uint32_t>(s) * Cfg::kStageBytes;
+                mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
                 tma_load_2d(stage, &tmap_a, full_bar(s), kb * kBlockK, m_tile * kPrefillBM);
-                tma_load_2d(stage + kPrefillATile, &tmap_b, full_bar(s), kb * kBlockK, n_tile * kPrefillBN);
+                tma_load_2d(stage + kPrefillATile, &tmap_b, full_bar(s), kb * kBlockK, n_tile * BN);
                 ++it;
                 if (++s == stages) {
                     s = 0;
@@ -183,7 +193,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + static_cast<uint32_t>(acc * kPrefillBN);
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
                 const int kb1 = min(kb0 + dkb, kbt);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!pf_wait(full_bar(s), ph, err, kErrPrefillFullWait, &s_abort)) {
@@ -191,11 +201,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t stage = base + static_cast<uint32_t>(s) * kPrefillStageBytes;
+                    const uint32_t stage = base + static_cast<uint32_t>(s) * Cfg::kStageBytes;
                     const uint64_t da = sw128_kmajor_desc(stage), db = sw128_kmajor_desc(stage + kPrefillATile);
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 32; ++kk)  // +32 bytes along K = +2 in the address field
-                        mma_e4m3(d, da + 2u * kk, db + 2u * kk, kPrefillIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        mma_e4m3(d, da + 2u * kk, db + 2u * kk, Cfg::kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
                     mma_commit(empty_bar(s));
                     ++it;
                     if (++s == stages) {
@@ -218,7 +228,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const bool sb_vec = (args.gran == 1 || args.gran == 2);
         const float sa0 = __ldg(args.scale_a), sb0 = __ldg(args.scale_b);
         const int M = args.M, N = args.N;
-        constexpr int kCols = kPrefillBN / 2;  // columns of one thread
+        constexpr int kCols = BN / 2;  // columns of one thread
         uint32_t dc = 0;
         bool ok = true;
         for (int t = c; t < tiles && ok; t += G) {
@@ -237,7 +247,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 tc_fence_after();
                 if (live) {
                 const uint32_t tbase = tmem + ((quarter * 32u) << 16) +
-                                       static_cast<uint32_t>(acc * kPrefillBN + half * kCols);
+                                       static_cast<uint32_t>(acc * BN + half * kCols);
 #pragma unroll
                 for (int j = 0; j < kCols; j += 32) {
                     uint32_t v[32];
@@ -257,7 +267,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const int m = m_tile * kPrefillBM + row;
             if (m < M) {
                 const float sa = sa_vec ? __ldg(args.scale_a + m) : sa0;
-                const int nbase = n_tile * kPrefillBN + half * kCols;
+                const int nbase = n_tile * BN + half * kCols;
                 __nv_bfloat16 *const yrow = args.out + static_cast<int64_t>(m) * N;
 #pragma unroll
                 for (int j = 0; j < kCols; j += 8) {
@@ -295,7 +305,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     if (warp == 1) {
         mbar_wait(final_bar, 0, err, kErrPrefillAccumWait);  // every MMA has completed
         tc_fence_after();
-        tmem_dealloc(tmem, kPrefillTmemCols);
+        tmem_dealloc(tmem, Cfg::kTmemCols);
     }
 }
 
@@ -303,24 +313,46 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
 // Shared memory of one CTA: alignment slack, the stages, the mbarriers
 // (full/empty per stage, full/empty per accumulator, one final), rounded up.
-static size_t prefill_smem_bytes(int stages) {
+static size_t prefill_smem_bytes(int stages, int bn) {
     const size_t barriers = 8u * static_cast<size_t>(2 * stages + 5);
-    return 1024 + static_cast<size_t>(stages) * kPrefillStageBytes + ((barriers + 127) / 128) * 128;
+    const size_t stage = static_cast<size_t>(kPrefillBM + bn) * kBlockK;
+    return 1024 + static_cast<size_t>(stages) * stage + ((barriers + 127) / 128) * 128;
 }
 
 PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms) {
     PrefillPlan p{};
     p.m_tiles = static_cast<int>((M + kPrefillBM - 1) / kPrefillBM);
-    p.n_tiles = static_cast<int>((N + kPrefillBN - 1) / kPrefillBN);
+    // 256-channel tiles, unless they would leave most SMs idle while the
+    // kernel is bound by streaming the weights (small M): then 128 channels.
+    const int64_t tiles256 = static_cast<int64_t>(p.m_tiles) * ((N + 255) / 256);
+    p.bn = (M <= kPrefillSmallM && 2 * tiles256 <= num_sms) ? 128 : 256;
+    p.n_tiles = static_cast<int>((N + p.bn - 1) / p.bn);
     p.kb_total = static_cast<int>((K + kBlockK - 1) / kBlockK);
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     p.ctas = static_cast<int>(tiles < num_sms ? tiles : num_sms);
     if (p.ctas < 1) p.ctas = 1;
-    p.stages = kPrefillMaxStages;
+    p.stages = p.bn == 256 ? PrefillCfg<256>::kStages : PrefillCfg<128>::kStages;
     const int dkb = M <= kPrefillSmallM ? kPrefillDrainKbSmall : kPrefillDrainKb;
     p.drain_kb = (dkb > 0 && dkb < p.kb_total) ? dkb : p.kb_total;
-    p.smem_bytes = prefill_smem_bytes(p.stages);
+    p.smem_bytes = prefill_smem_bytes(p.stages, p.bn);
     return p;
+}
+
+template <int BN>
+static cudaError_t launch_bn(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b, const PrefillArgs &a,
+                             const PrefillPlan &plan, const LaunchOpts &opts, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool attr_done[64] = {};  // benign race: the attribute call is idempotent
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(prefill_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(prefill_smem_bytes(PrefillCfg<BN>::kStages, BN)));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    return launch_with_opts(prefill_gemm_kernel<BN>, dim3(static_cast<unsigned>(plan.ctas)), dim3(kPrefillThreads),
+                            plan.smem_bytes, stream, opts, tmap_a, tmap_b, a);
 }
 
 cudaError_t launch_prefill_gemm(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b, const float *scale_a,
@@ -328,16 +360,6 @@ cudaError_t launch_prefill_gemm(const CUtensorMap &tmap_a, const CUtensorMap &tm
                                 uint32_t *err, const PrefillPlan &plan, const LaunchOpts &opts,
                                 cudaStream_t stream) {
     (void)K;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    static bool attr_done[64] = {};  // benign race: the attribute call is idempotent
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(prefill_smem_bytes(kPrefillMaxStages)));
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_done[dev] = true;
-    }
     PrefillArgs a;
     a.scale_a = scale_a;
     a.scale_b = scale_b;
@@ -351,8 +373,8 @@ cudaError_t launch_prefill_gemm(const CUtensorMap &tmap_a, const CUtensorMap &tm
     a.tiles = plan.m_tiles * plan.n_tiles;
     a.stages = plan.stages;
     a.drain_kb = plan.drain_kb;
-    return launch_with_opts(prefill_gemm_kernel, dim3(static_cast<unsigned>(plan.ctas)), dim3(kPrefillThreads),
-                            plan.smem_bytes, stream, opts, tmap_a, tmap_b, a);
+    if (plan.bn == 128) return launch_bn<128>(tmap_a, tmap_b, a, plan, opts, stream);
+    return launch_bn<256>(tmap_a, tmap_b, a, plan, opts, stream);
 }
 
 }  // namespace fp8k

@@ -11,6 +11,7 @@ namespace fp8k {
 struct LaunchOpts {
     bool pdl = true;              // programmatic dependent launch (prologue overlaps the previous kernel)
     bool weights_static = false;  // B is not written by the kernel just before this one in the stream
+    int cluster_x = 1;            // CTAs per thread-block cluster (along x); 1 = no clusters
 };
 
 // Launch with the programmatic-stream-serialisation attribute when opts.pdl:
@@ -24,11 +25,18 @@ inline cudaError_t launch_with_opts(void (*kernel)(KArgs...), dim3 grid, dim3 bl
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = opts.pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (opts.cluster_x > 1) {  // thread-block clusters of cluster_x CTAs along x
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(opts.cluster_x);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
@@ -39,6 +47,20 @@ cudaError_t launch_quant_static(const void *x, const float *scale, void *out, in
 
 cudaError_t launch_quant_per_token(const void *x, void *out, float *scale_out, int64_t M, int64_t K,
                                    uint32_t *err, cudaStream_t stream, int num_sms, const LaunchOpts &opts);
+
+// Weight shards (each [rows_j, K] E4M3 with a per-tensor scale) merged into one
+// weight requantised to the largest scale.
+constexpr int kMaxMergeShards = 16;
+struct MergeArgs {
+    const uint4 *src[kMaxMergeShards];
+    const float *scale[kMaxMergeShards];
+    int64_t end16[kMaxMergeShards];  // cumulative end of each shard, in 16-byte vectors
+    int n;
+    uint4 *out;
+    float *scale_out;
+    int64_t n16;
+};
+cudaError_t launch_requant_merge(const MergeArgs &a, cudaStream_t stream, int num_sms, const LaunchOpts &opts);
 
 // gate_up [M, 2I] bf16 rows [gate | up] -> E4M3 [M, I] of silu(gate) * up, per-token scales.
 cudaError_t launch_silu_mul_quant(const void *gate_up, void *out, float *scale_out, int64_t M, int64_t I,
@@ -55,10 +77,10 @@ cudaError_t launch_rmsnorm_quant(const void *x, const void *gamma, float eps, co
 // channels) per tile on the tensor core's M side, up to 64 tokens on its N side.
 constexpr int kDecodeRows = 128;
 constexpr int kBlockK = 128;  // bytes (= E4M3 elements) of K per pipeline stage
-constexpr int kDecodeMaxTokens = 32;
+constexpr int kDecodeMaxTokens = 16;
 
 struct DecodePlan {
-    int tok_pad;      // tokens per tile on the MMA N side: 16 or 32
+    int tok_pad;      // tokens per tile on the MMA N side: 16
     int stages;       // pipeline depth
     int n_tiles;      // ceil(N / 128)
     int m_tiles;      // ceil(M / tok_pad)
@@ -91,9 +113,10 @@ cudaError_t launch_decode_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tma
 // channels (MMA N) per tile, 128-byte k-blocks.
 constexpr int kPrefillBM = 128;
 constexpr int kPrefillBN = 256;
-constexpr int64_t kPrefillMinM = 33;  // fp8_scaled_mm sends M >= this to the prefill kernel
+constexpr int64_t kPrefillMinM = 17;  // fp8_scaled_mm sends M >= this to the prefill kernel
 
 struct PrefillPlan {
+    int bn;  // output channels per tile: 256, or 128 for small M with few tiles
     int m_tiles, n_tiles, kb_total;
     int ctas;       // persistent CTAs (one per SM at most)
     int stages;

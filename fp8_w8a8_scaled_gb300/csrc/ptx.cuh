@@ -259,6 +259,14 @@ __device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float2 v) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
 }
 
+// One float from distributed shared memory (after the cluster barrier that
+// publishes it).
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Loads from distributed shared memory.  Volatile (kept in program order after
 // the cluster barrier that publishes the data) but without a memory clobber,
 // so several loads can be in flight at once.

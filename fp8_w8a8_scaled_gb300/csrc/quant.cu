@@ -20,6 +20,7 @@
 // conversion (cvt.rn.satfinite.e4m3x2.f32).  Every kernel is launched with
 // programmatic dependent launch and waits for its predecessor before reading.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -221,6 +222,96 @@ __global__ void __launch_bounds__(1024) silu_mul_quant_kernel(const uint4 *__res
     }
 }
 
+// Small M: a row of [gate | up] split over a cluster of CS CTAs (one CTA per
+// SM for M rows would leave almost every SM idle and give each thread many
+// exp / divisions in series).  Each CTA takes a contiguous chunk of the row;
+// the row's amax is the max of the CTAs' maxima, exchanged through
+// distributed shared memory between two cluster barriers (max is exact and
+// order-free, so every CTA gets the same scale and the bytes equal the
+// one-CTA kernel's).
+template <int V, int CS>
+__global__ void __launch_bounds__(256) silu_mul_quant_cluster_kernel(const uint4 *__restrict__ gate_up,
+                                                                     uint2 *__restrict__ out,
+                                                                     float *__restrict__ scale_out, int nvec) {
+    __shared__ float red[32];
+    __shared__ float s_amax;
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const uint32_t rank = cluster_ctarank();
+    const int64_t row = blockIdx.x / CS;
+    const int chunk = (nvec + CS - 1) / CS;
+    const int v0 = static_cast<int>(rank) * chunk, v1 = min(nvec, v0 + chunk);
+    const uint4 *gr = gate_up + row * 2 * nvec;
+    const uint4 *ur = gr + nvec;
+    uint2 *orow = out + row * nvec;
+    const int T = static_cast<int>(blockDim.x);
+    uint4 a[V];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = v0 + static_cast<int>(threadIdx.x) + j * T;
+        if (idx < v1) {
+            a[j] = silu_mul8(ld_stream(gr + idx), ld_stream(ur + idx));
+            amax = absmax8(a[j], amax);
+        }
+    }
+    amax = block_max(amax, red);
+    if (threadIdx.x == 0) s_amax = amax;
+    cluster_sync();
+    float m = 0.0f;
+    const uint32_t my = smem_u32(&s_amax);
+#pragma unroll
+    for (int r = 0; r < CS; ++r) m = fmaxf(m, ld_cluster_f32(map_to_rank(my, static_cast<uint32_t>(r))));
+    cluster_sync();  // no CTA leaves while another may still read its s_amax
+    const float s = (m == 0.0f) ? 1.0f : __fdiv_rn(m, 448.0f);
+    if (rank == 0 && threadIdx.x == 0) scale_out[row] = s;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = v0 + static_cast<int>(threadIdx.x) + j * T;
+        if (idx < v1) orow[idx] = quant8(a[j], s);
+    }
+}
+
+// ---------------------------------------------------- shard requantisation --
+
+// Shards [rows_j, K] of E4M3 weights with per-tensor scales s_j, merged into
+// one [sum rows_j, K] weight with the scale s_max = max_j s_j: every code
+// becomes e4m3( fp32(dec(q) * s_j) / s_max ).  16 codes per thread step (a
+// shard's byte size is a multiple of 16, so no vector straddles two shards).
+__global__ void __launch_bounds__(256) requant_merge_kernel(const MergeArgs a) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    float smax = 0.0f;
+    for (int j = 0; j < a.n; ++j) smax = fmaxf(smax, __ldg(a.scale[j]));
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.scale_out = smax;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < a.n16; i += stride) {
+        int j = 0;
+        while (j + 1 < a.n && i >= a.end16[j]) ++j;
+        const int64_t start = j ? a.end16[j - 1] : 0;
+        const uint4 v = ld_stream(a.src[j] + (i - start));
+        const float s_in = __ldg(a.scale[j]);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t packed = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const __nv_fp8x2_storage_t two = static_cast<__nv_fp8x2_storage_t>((w[k] >> (16 * h)) & 0xFFFFu);
+                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
+                const float d0 = __half2float(__half(__half_raw{hr.x}));
+                const float d1 = __half2float(__half(__half_raw{hr.y}));
+                const float v0 = __fdiv_rn(__fmul_rn(d0, s_in), smax);
+                const float v1 = __fdiv_rn(__fmul_rn(d1, s_in), smax);
+                packed |= e4m3x2(v0, v1) << (16 * h);
+            }
+            o[k] = packed;
+        }
+        a.out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 // ---------------------------------------------------- fused RMSNorm -> quant --
 
 struct CtaSync {
@@ -317,10 +408,27 @@ cudaError_t launch_quant_per_token(const void *x, void *out, float *scale_out, i
                             static_cast<const uint4 *>(x), static_cast<uint2 *>(out), scale_out, nvec);
 }
 
+cudaError_t launch_requant_merge(const MergeArgs &a, cudaStream_t stream, int num_sms, const LaunchOpts &o) {
+    int64_t blocks = (a.n16 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return launch_with_opts(requant_merge_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, o, a);
+}
+
 cudaError_t launch_silu_mul_quant(const void *gate_up, void *out, float *scale_out, int64_t M, int64_t I,
                                   uint32_t *err, cudaStream_t stream, int num_sms, const LaunchOpts &o) {
     (void)err;
     const int64_t nvec = I / 8;
+    // Few long rows: 8-CTA clusters per row, 256 threads x up to 4 vectors each.
+    constexpr int kCS = 8;
+    if (M * kCS <= 2 * static_cast<int64_t>(num_sms) && nvec >= kCS * 256 && nvec <= kCS * 256 * 4) {
+        LaunchOpts oc = o;
+        oc.cluster_x = kCS;
+        return launch_with_opts(silu_mul_quant_cluster_kernel<4, kCS>, dim3(static_cast<unsigned>(M * kCS)), dim3(256),
+                                0, stream, oc, static_cast<const uint4 *>(gate_up), static_cast<uint2 *>(out),
+                                scale_out, static_cast<int>(nvec));
+    }
     if (many_rows(M, num_sms) && nvec <= 1024) return launch_rows_silu<4>(gate_up, out, scale_out, M, I, stream, o);
     if (nvec <= 1024) return launch_rows_silu<1>(gate_up, out, scale_out, M, I, stream, o);
     if (nvec <= 2048) return launch_rows_silu<2>(gate_up, out, scale_out, M, I, stream, o);

@@ -24,7 +24,7 @@
  * Conventions shared by every call
  *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
  *     caller owns and allocates every buffer.  The library allocates no device
- *     memory per call: its only allocation is a ~14 MB scratch area per device
+ *     memory per call: its only allocation is a ~9 MB scratch area per device
  *     (arrival counters and partial sums of the decode GEMM), made on the
  *     first fp8_scaled_mm call on that device -- make that first call before
  *     capturing a CUDA graph.  Because the scratch is shared, GEMM calls that
@@ -105,8 +105,8 @@ typedef enum {
  * tensor-core accumulation of the exact E4M3 products.  Which kernel runs is a
  * pure function of (M, N, K, granularity), see fp8_describe_dispatch, so a
  * captured CUDA graph replays the same kernel the eager call would run:
- * M <= 32 the weight-streaming decode kernel (uses the library's scratch
- * area), M >= 33 the tensor-core tile kernel (uses no scratch).  For a fixed
+ * M <= 16 the weight-streaming decode kernel (uses the library's scratch
+ * area), M >= 17 the tensor-core tile kernel (uses no scratch).  For a fixed
  * M the result is deterministic (bitwise the same on every run); on the tile
  * kernel row m does not depend on the other rows of A.
  * Errors: FP8_ERR_INVALID_ARG, FP8_ERR_ALIGNMENT, FP8_ERR_UNSUPPORTED,
@@ -141,7 +141,7 @@ fp8_status fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, 
  * not call cudaMalloc at all: code running inside a memory pool or arena
  * that must own every device allocation, hosts whose allocator is locked
  * while a CUDA graph is being built, or embedders that forbid hidden
- * allocations.  fp8_scaled_mm allocates its ~14 MB scratch on first use; this
+ * allocations.  fp8_scaled_mm allocates its ~9 MB scratch on first use; this
  * entry point instead uses a fixed scratch area compiled into the library (a
  * file-scope device array of 6 MB + 64 KB that every GPU which loads the
  * library holds until the process exits), and never calls cudaMalloc,
@@ -225,6 +225,29 @@ fp8_status fp8_add_rmsnorm_quant(const void *x, void *residual, const void *gamm
 fp8_status fp8_silu_mul_quant_per_token(const void *gate_up, void *out, float *scale_out, int64_t M, int64_t I,
                                         void *stream);
 
+/* fp8_requant_merge -- merge weight shards that carry different per-tensor
+ * scales into one weight with one scale, the largest (max_w_scale).
+ *
+ * Source: [P3] "Ranked follow-ons from the same audit", first bullet: a merged
+ * QKV projection is one physical GEMM, and shards whose per-tensor scales
+ * differ are requantised to the largest scale (lossy), instead of declining
+ * to merge.  (With per-output-channel scales, concatenating the shards and
+ * their scales merges them losslessly and needs no requantisation.)
+ *
+ *   shards     HOST array of n_shards DEVICE pointers, shard j E4M3
+ *              [rows[j], K] row-major, 16-byte aligned (may be NULL if
+ *              rows[j] == 0)
+ *   scales     HOST array of n_shards DEVICE pointers to f32 [1]: s_j
+ *   rows       HOST array of n_shards row counts
+ *   out        E4M3 [sum rows, K], 16-byte aligned: the shards in order,
+ *              code q of shard j becoming e4m3( fp32(dec(q) * s_j) / s_max )
+ *   scale_out  f32 [1] (device): s_max = max_j s_j (must not alias an input)
+ *   1 <= n_shards <= 16, K % 16 == 0, sum rows < 2^31
+ *
+ * Errors: FP8_ERR_INVALID_ARG, FP8_ERR_ALIGNMENT, FP8_ERR_CUDA. */
+fp8_status fp8_requant_merge(const void *const *shards, const float *const *scales, const int64_t *rows,
+                             int n_shards, int64_t K, void *out, float *scale_out, void *stream);
+
 /* fp8_rmsnorm_quant_scaled_mm -- rmsnorm_quant_fp8 followed by fp8_scaled_mm
  * on its output, as one call ("quantise once": the normalised, quantised
  * activations are written to a_out for the layer's other projections, and
@@ -285,7 +308,7 @@ const char *fp8_status_string(int status);
 /* Which kernel fp8_scaled_mm runs for this problem (an fp8_kernel_id), or -1
  * for arguments fp8_scaled_mm would reject.  Host-only, pure: it reads no
  * device state, so a caller can assert the kernel before capturing a graph.
- * FP8_KERNEL_DECODE_SPLITK for 1 <= M <= 32, FP8_KERNEL_PREFILL for M >= 33.
+ * FP8_KERNEL_DECODE_SPLITK for 1 <= M <= 16, FP8_KERNEL_PREFILL for M >= 17.
  * Source: [P4] commit message: the M-vs-threshold branch is a pure function
  * of M so that a graph captured at a padded M freezes the branch eager
  * execution would take. */

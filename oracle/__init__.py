@@ -50,6 +50,7 @@ def _load():
     lib.oracle_sum_squares_bf16.restype = ctypes.c_float
     lib.oracle_rmsnorm_quant.argtypes = [P, P, ctypes.c_float, ctypes.c_float, I64, I64, P]
     lib.oracle_residual_add_bf16.argtypes = [P, P, I64, P]
+    lib.oracle_requant.argtypes = [P, I64, ctypes.c_float, ctypes.c_float, P]
     lib.oracle_exp_f32.argtypes = [ctypes.c_float]
     lib.oracle_exp_f32.restype = ctypes.c_float
     lib.oracle_exp_f32_array.argtypes = [P, I64, P]
@@ -231,6 +232,13 @@ def silu_mul_quant_per_token(gate_up_bf16):
     s = np.empty((M,), np.float32)
     _load().oracle_silu_mul_quant_per_token(_ptr(x), M, W // 2, _ptr(q), _ptr(s))
     return q, s
+
+
+def requant(q_codes, s_in: float, s_out: float) -> np.ndarray:
+    q = _c(q_codes, np.uint8)
+    out = np.empty(q.shape, np.uint8)
+    _load().oracle_requant(_ptr(q), q.size, ctypes.c_float(s_in), ctypes.c_float(s_out), _ptr(out))
+    return out
 
 
 # --- GEMM --------------------------------------------------------------------

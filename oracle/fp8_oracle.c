@@ -429,6 +429,21 @@ void oracle_silu_mul_quant_per_token(const uint16_t *gate_up, int64_t M, int64_t
     free(a);
 }
 
+/* Requantisation of a weight shard from its per-tensor scale s_in to another
+ * scale s_out (reading R20): w = fp32(dec(q) * s_in) (one binary32 multiply;
+ * dec(q) is exact in binary32), q' = enc(w / s_out) (R2, R3).  [P3] "Ranked
+ * follow-ons from the same audit", first bullet: a merged QKV projection whose
+ * shards carry different per-tensor scales is requantised to the largest of
+ * them (max_w_scale), which is lossy. */
+void oracle_requant(const uint8_t *q, int64_t n, float s_in, float s_out, uint8_t *out) {
+    for (int64_t i = 0; i < n; ++i) {
+        volatile float d = (float)oracle_e4m3_decode(q[i]);
+        volatile float w = d * s_in;
+        volatile float v = w / s_out;
+        out[i] = oracle_e4m3_encode(v);
+    }
+}
+
 /* ------------------------------------------------------------------------- */
 /* The scaled GEMM ([P1] "What is owed" item 2 and "CORRECTION": bmm_fp8(a,  */
 /* b, scale_a, scale_b, out_dtype, ...); [P3] "FINDING 1": out dtype bf16;   */

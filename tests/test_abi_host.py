@@ -136,6 +136,28 @@ def test_silu_mul_quant_validation(L):
     assert f(GOOD, P(0x20008), SC, 4, 64, None) == 2
 
 
+def test_requant_merge_validation(L):
+    f = L.fp8_requant_merge
+    I64 = ctypes.c_int64
+
+    def call(ptrs, scales, rows, K=64, out=GOOD3, so=SC):
+        n = len(rows)
+        pa = (ctypes.c_void_p * n)(*ptrs)
+        sa = (ctypes.c_void_p * n)(*scales)
+        ra = (I64 * n)(*rows)
+        return f(ctypes.cast(pa, P), ctypes.cast(sa, P), ctypes.cast(ra, P), n, K, out, so, None)
+
+    # (only invalid calls here: the fake addresses must never reach a launch)
+    assert call([0x10000], [0x40000], [4], K=40) == 2
+    assert call([0x10008], [0x40000], [4]) == 2
+    assert call([0x10000], [0x40002], [4]) == 2
+    assert call([0x10000], [0], [4]) == 1
+    assert call([0], [0x40000], [4]) == 1
+    assert call([0x10000], [0x40000], [-1]) == 1
+    assert call([0x10000] * 17, [0x40000] * 17, [1] * 17) == 1
+    assert call([0x10000], [0x40000], [4], out=None) == 1
+
+
 def test_quantiser_validation(L):
     assert L.quant_fp8_static(GOOD, SC, GOOD2, 0, 64, None) == 0
     assert L.quant_fp8_static(None, SC, GOOD2, 4, 64, None) == 1
@@ -159,9 +181,9 @@ def test_describe_dispatch_is_pure(L):
     assert L.fp8_describe_dispatch(0, 64, 64, 0) == 0
     assert L.fp8_describe_dispatch(-1, 64, 64, 0) == -1
     assert L.fp8_describe_dispatch(4, 64, 64, 7) == -1
-    for M in (1, 2, 4, 8, 16, 32):
+    for M in (1, 2, 4, 8, 16):
         assert L.fp8_describe_dispatch(M, 10240, 5120, 1) == 1
-    for M in (33, 64, 65, 128, 2048, 8192):
+    for M in (17, 32, 33, 64, 65, 128, 2048, 8192):
         assert L.fp8_describe_dispatch(M, 10240, 5120, 1) == 2
         assert L.fp8_describe_dispatch(M, 34816, 5120, 2) == 2
     # the same question twice gives the same answer (no hidden state)
@@ -173,7 +195,7 @@ def test_decode_planner(L):
     """Two persistent CTAs per SM (never more CTAs than units of one tile x
     one 128-wide k-block)."""
     f = L.fp8_decode_ctas_for_sms
-    for (M, N, K) in ((1, 10240, 5120), (32, 10240, 5120), (32, 34816, 5120)):
+    for (M, N, K) in ((1, 10240, 5120), (16, 10240, 5120), (16, 34816, 5120)):
         assert f(M, N, K, 152) == 304
     assert f(8, 5120, 8192, 152) == 40 * 64 // 10       # >= 10 k-blocks per CTA (64 per tile)
     assert f(8, 5120, 17408, 152) == 40 * 136 // 20

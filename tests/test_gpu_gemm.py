@@ -82,7 +82,8 @@ def test_decode_fused_qkv(fp8, decode_fused_case, M):
     s_a = to_dev_f32(d["s_a"])
     A = fp8.rmsnorm_quant_fp8(to_dev_bf16(d["x"][:M]), to_dev_bf16(d["gamma"]), d["eps"], s_a)
     assert np.array_equal(host_bits(A), A_all[:M])
-    assert fp8.describe_dispatch(M, 10240, 5120, 1) == fp8.KERNEL_DECODE_SPLITK
+    want = fp8.KERNEL_DECODE_SPLITK if M <= 16 else fp8.KERNEL_PREFILL
+    assert fp8.describe_dispatch(M, 10240, 5120, 1) == want
     y = run_mm(fp8, A, to_dev_e4m3(d["B"]), s_a, to_dev_f32(d["sb"]), 1)
     sab = scale_product(d["s_a"], d["sb"], 1, np.arange(M)[:, None], np.arange(10240)[None, :])
     worst, _ = check_gemm(y, y64[:M], sab, 5120, f"decode fused M={M}")

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import workloads
-from helpers import Guarded, host_bits, to_dev_bf16, to_dev_f32
+from helpers import Guarded, host_bits, to_dev_bf16, to_dev_e4m3, to_dev_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -254,3 +254,26 @@ def test_silu_mul_quant_equals_unfused(fp8, orc):
     a = orc.silu_mul_bf16(gu)
     q2, s2 = fp8.quant_fp8_per_token(to_dev_bf16(a))
     assert np.array_equal(host_bits(q), host_bits(q2)) and np.array_equal(host_bits(s), host_bits(s2))
+
+
+def test_requant_merge_qkv_shards(fp8, orc):
+    """Three shards (q 8192, k 1024, v 1024 rows of K 512) with different
+    per-tensor scales merged at the largest: codes bit-exact against the
+    oracle (NaN codes stay NaN codes), the scale is the maximum."""
+    g = workloads.rng(110)
+    K = 512
+    rows = (workloads.Q_WIDTH, workloads.KV_WIDTH, workloads.KV_WIDTH)
+    shards = [workloads.e4m3_codes(g, (r, K)) for r in rows]
+    shards[1][0, :4] = [0x7F, 0xFF, 0x7E, 0xFE]
+    scales = [np.float32(2.1e-3), np.float32(3.3e-3), np.float32(1.7e-3)]
+    merged, s = fp8.requant_merge([to_dev_e4m3(w) for w in shards], [to_dev_f32(x) for x in scales])
+    smax = max(scales)
+    assert host_bits(s)[0] == smax
+    want = np.concatenate([orc.requant(w, float(x), float(smax)) for w, x in zip(shards, scales)])
+    got = host_bits(merged)
+    nan_w = (want & 0x7F) == 0x7F
+    assert np.array_equal(got[~nan_w], want[~nan_w])
+    assert np.all((got[nan_w] & 0x7F) == 0x7F)
+    # the shard at the largest scale is unchanged
+    assert np.array_equal(got[rows[0]:rows[0] + rows[1]][~nan_w[rows[0]:rows[0] + rows[1]]],
+                          shards[1][~nan_w[rows[0]:rows[0] + rows[1]]])

@@ -350,3 +350,43 @@ def test_silu_mul_quant_composition(orc):
     assert s[1] == 1.0 and np.all(q[1] == 0)
     for m in (0, 2, 3):
         assert np.max(q[m] & 0x7F) == 0x7E
+
+
+# --------------------------------------------------------------------------- shard requantisation (R20)
+
+ALL_CODES = np.arange(256, dtype=np.uint8)
+NAN_CODES = (ALL_CODES & 0x7F) == 0x7F
+
+
+def test_requant_identity_and_powers_of_two(orc):
+    """Same scale: every code maps to itself.  Twice the scale: every code
+    maps to the code of half its value (exact in E4M3 down to the smallest
+    normals; subnormal halves round to nearest even)."""
+    for s in (1.0, 3.7e-3, 2.0 ** -20, 123.0):
+        s = float(np.float32(s))
+        q = orc.requant(ALL_CODES, s, s)
+        assert np.array_equal(q[~NAN_CODES], ALL_CODES[~NAN_CODES])
+        assert np.all((q[NAN_CODES] & 0x7F) == 0x7F)
+    dec = orc.e4m3_decode(ALL_CODES)
+    half = orc.requant(ALL_CODES, 0.5, 1.0)
+    want = orc.e4m3_encode((dec / 2).astype(np.float32))
+    assert np.array_equal(half[~NAN_CODES], want[~NAN_CODES])
+    exact = (~NAN_CODES) & ((ALL_CODES & 0x78) >= 0x10)          # exponent field >= 2: halving stays normal
+    assert np.array_equal(orc.e4m3_decode(half[exact]), dec[exact] / 2)
+
+
+def test_requant_to_max_scale_is_monotone_and_close(orc):
+    """Requantising to a larger scale keeps the order of the values and each
+    result is the nearest E4M3 value to dec(q) * s_in / s_out (brute force
+    over the 254 finite values)."""
+    s_in, s_out = float(np.float32(1.3e-3)), float(np.float32(2.9e-3))
+    q = orc.requant(ALL_CODES, s_in, s_out)
+    dec = orc.e4m3_decode(ALL_CODES)
+    fin = ~NAN_CODES
+    order = np.argsort(dec[fin], kind="stable")
+    got = orc.e4m3_decode(q[fin])[order]
+    assert np.all(np.diff(got) >= 0)
+    grid = np.unique(orc.e4m3_decode(ALL_CODES[fin]))
+    target = (np.float32(dec[fin]) * np.float32(s_in)) / np.float32(s_out)
+    nearest = np.abs(grid[None, :] - target.astype(np.float64)[:, None]).min(axis=1)
+    assert np.all(np.abs(orc.e4m3_decode(q[fin]) - target) <= nearest + 1e-12)
