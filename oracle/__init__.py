@@ -64,6 +64,9 @@ def _load():
     lib.oracle_gemm_acc_i64.argtypes = [P, P, I64, I64, I64, P, ctypes.c_int]
     lib.oracle_scaled_mm.argtypes = [P, P, P, P, ctypes.c_int, I64, I64, I64, P, P, ctypes.c_int]
     lib.oracle_scaled_mm_points.argtypes = [P, P, P, P, ctypes.c_int, I64, I64, I64, P, P, I64, P]
+    lib.oracle_quant_per_token_group.argtypes = [P, I64, I64, P, P]
+    lib.oracle_quant_weight_block.argtypes = [P, I64, I64, P, P]
+    lib.oracle_scaled_mm_block_points.argtypes = [P, P, P, P, I64, I64, I64, P, P, I64, P]
     lib.oracle_has_nan_code.argtypes = [P, I64]
     lib.oracle_has_nan_code.restype = ctypes.c_int
     _lib = lib
@@ -232,6 +235,46 @@ def silu_mul_quant_per_token(gate_up_bf16):
     s = np.empty((M,), np.float32)
     _load().oracle_silu_mul_quant_per_token(_ptr(x), M, W // 2, _ptr(q), _ptr(s))
     return q, s
+
+
+BLOCK = 128
+
+
+def quant_per_token_group(x_bf16):
+    """(codes [M,K], scales [M, ceil(K/128)]): every 128-wide group of a row
+    quantised on its own."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((M, -(-K // BLOCK)), np.float32)
+    _load().oracle_quant_per_token_group(_ptr(x), M, K, _ptr(q), _ptr(s))
+    return q, s
+
+
+def quant_weight_block(w_bf16):
+    """(codes [N,K], scales [ceil(N/128), ceil(K/128)]): one scale per 128 x 128 block."""
+    w = _c(w_bf16, np.uint16)
+    N, K = w.shape
+    q = np.empty((N, K), np.uint8)
+    s = np.empty((-(-N // BLOCK), -(-K // BLOCK)), np.float32)
+    _load().oracle_quant_weight_block(_ptr(w), N, K, _ptr(q), _ptr(s))
+    return q, s
+
+
+def scaled_mm_block_points(A, B, sa, sb, rows, cols) -> np.ndarray:
+    """The blockwise GEMM (scales [M, KB] and [NB, KB]) at (rows[i], cols[i])."""
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    sa = _c(sa, np.float32)
+    sb = _c(sb, np.float32)
+    rows = _c(rows, np.int64)
+    cols = _c(cols, np.int64)
+    M, K = A.shape
+    N = B.shape[0]
+    y = np.empty(rows.shape, np.float64)
+    _load().oracle_scaled_mm_block_points(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), M, N, K, _ptr(rows), _ptr(cols),
+                                          rows.size, _ptr(y))
+    return y
 
 
 def requant(q_codes, s_in: float, s_out: float) -> np.ndarray:

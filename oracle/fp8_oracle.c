@@ -594,6 +594,74 @@ void oracle_scaled_mm_points(const uint8_t *A, const uint8_t *B, const float *sa
     }
 }
 
+/* ------------------------------------------------------------------------- */
+/* Blockwise scaling (reading R21): weights carry one scale per 128 x 128     */
+/* block, activations one per token per 128-wide group of K, so the GEMM is    */
+/*   y[m,n] = sum_g  sa[m,g] * sb[n/128, g] * sum_{k in group g} A[m,k] B[n,k]  */
+/* ([P4] "[Kernel] add Flashinfer cutedsl w4a16 linear": the commit message    */
+/* sets "dense FP8 non-blockwise" apart, so a blockwise FP8 variant exists).  */
+/* ------------------------------------------------------------------------- */
+
+#define ORACLE_BLOCK 128
+
+/* Per-token-group quantisation: every 128-wide group of a row quantised on
+ * its own, exactly as oracle_quant_per_token on that group (s = amax/448,
+ * 1.0 for an all-zero group).  s_out is [M, ceil(K/128)]. */
+void oracle_quant_per_token_group(const uint16_t *x, int64_t M, int64_t K, uint8_t *q, float *s_out) {
+    const int64_t KB = (K + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t g = 0; g < KB; ++g) {
+            const int64_t k0 = g * ORACLE_BLOCK, len = (K - k0 < ORACLE_BLOCK) ? K - k0 : ORACLE_BLOCK;
+            oracle_quant_per_token(x + m * K + k0, 1, len, q + m * K + k0, s_out + m * KB + g);
+        }
+}
+
+/* Per-block weight quantisation: s[nb, g] = amax over the 128 x 128 block /
+ * 448 (1.0 for an all-zero block; NaN entries do not take part), then
+ * q = enc(fp32(w) / s) (R3).  s_out is [ceil(N/128), ceil(K/128)]. */
+void oracle_quant_weight_block(const uint16_t *w, int64_t N, int64_t K, uint8_t *q, float *s_out) {
+    const int64_t KB = (K + ORACLE_BLOCK - 1) / ORACLE_BLOCK, NB = (N + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
+    for (int64_t nb = 0; nb < NB; ++nb)
+        for (int64_t g = 0; g < KB; ++g) {
+            const int64_t n0 = nb * ORACLE_BLOCK, n1 = (n0 + ORACLE_BLOCK < N) ? n0 + ORACLE_BLOCK : N;
+            const int64_t k0 = g * ORACLE_BLOCK, k1 = (k0 + ORACLE_BLOCK < K) ? k0 + ORACLE_BLOCK : K;
+            float amax = 0.0f;
+            for (int64_t n = n0; n < n1; ++n)
+                for (int64_t k = k0; k < k1; ++k) {
+                    const float a = fabsf(oracle_bf16_to_f32(w[n * K + k]));
+                    if (a > amax) amax = a; /* NaN compares false: ignored */
+                }
+            volatile float sv = amax / 448.0f;
+            const float sc = (amax == 0.0f) ? 1.0f : sv;
+            s_out[nb * KB + g] = sc;
+            for (int64_t n = n0; n < n1; ++n) oracle_quant_static(w + n * K + k0, sc, 1, k1 - k0, q + n * K + k0);
+        }
+}
+
+/* y64 of the blockwise GEMM at the listed (row, col) pairs: each group's sum
+ * exact in binary64 (as in the per-tensor case), times sa * sb (exact
+ * product), summed over the groups in binary64. */
+void oracle_scaled_mm_block_points(const uint8_t *A, const uint8_t *B, const float *sa, const float *sb, int64_t M,
+                                   int64_t N, int64_t K, const int64_t *rows, const int64_t *cols, int64_t npts,
+                                   double *y64) {
+    pthread_once(&g_lut_once, build_lut);
+    (void)M;
+    (void)N;
+    const int64_t KB = (K + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
+    for (int64_t i = 0; i < npts; ++i) {
+        const uint8_t *a = A + rows[i] * K;
+        const uint8_t *b = B + cols[i] * K;
+        double y = 0.0;
+        for (int64_t g = 0; g < KB; ++g) {
+            double acc = 0.0;
+            const int64_t k1 = (g + 1) * ORACLE_BLOCK < K ? (g + 1) * ORACLE_BLOCK : K;
+            for (int64_t k = g * ORACLE_BLOCK; k < k1; ++k) acc += g_lut[a[k]] * g_lut[b[k]];
+            y += acc * ((double)sa[rows[i] * KB + g] * (double)sb[(cols[i] / ORACLE_BLOCK) * KB + g]);
+        }
+        y64[i] = y;
+    }
+}
+
 int oracle_has_nan_code(const uint8_t *codes, int64_t n) {
     pthread_once(&g_lut_once, build_lut);
     for (int64_t i = 0; i < n; ++i)

@@ -137,3 +137,85 @@ def test_pages_weight_stream_accounting():
         assert abs(rate - gibs) <= 1e-3 * gibs, (rate, gibs)
     total_b, gib = totals[0]
     assert abs(total_b / 2 ** 30 - gib) < 5e-5
+
+
+# --------------------------------------------------------------------------- blockwise scaling (R21)
+
+def _dec(orc, codes):
+    return orc.e4m3_decode(codes).astype(np.float64)
+
+
+def test_block_gemm_matches_groupwise_numpy(orc):
+    """The blockwise GEMM against numpy's float64 matmul of the decoded
+    operands, one 128-wide K group at a time, each group's product scaled by
+    sa[m, g] * sb[n // 128, g] (ragged K and N, distinct scales per block)."""
+    g = np.random.default_rng(120)
+    M, N, K = 5, 300, 400
+    A = workloads.e4m3_codes(g, (M, K))
+    B = workloads.e4m3_codes(g, (N, K))
+    KB, NB = -(-K // 128), -(-N // 128)
+    sa = g.uniform(0.5, 2.0, (M, KB)).astype(np.float32)
+    sb = g.uniform(0.5, 2.0, (NB, KB)).astype(np.float32)
+    Ad, Bd = _dec(orc, A), _dec(orc, B)
+    want = np.zeros((M, N))
+    for gi in range(KB):
+        k0, k1 = gi * 128, min(K, gi * 128 + 128)
+        part = Ad[:, k0:k1] @ Bd[:, k0:k1].T
+        want += part * (sa[:, gi].astype(np.float64)[:, None] * sb[np.arange(N) // 128, gi].astype(np.float64)[None, :])
+    rows, cols = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    got = orc.scaled_mm_block_points(A, B, sa, sb, rows.ravel(), cols.ravel()).reshape(M, N)
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-9)
+
+
+def test_block_gemm_with_uniform_scales_is_token_channel(orc):
+    """Scales constant along K reduce the blockwise GEMM to the per-token x
+    per-channel one (gran 2) of the same operands."""
+    g = np.random.default_rng(121)
+    M, N, K = 3, 256, 512
+    A = workloads.e4m3_codes(g, (M, K))
+    B = workloads.e4m3_codes(g, (N, K))
+    a = g.uniform(0.5, 2.0, M).astype(np.float32)
+    b = g.uniform(0.5, 2.0, 2).astype(np.float32)
+    sa = np.repeat(a[:, None], 4, axis=1)
+    sb = np.repeat(b[:, None], 4, axis=1)
+    rows, cols = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    got = orc.scaled_mm_block_points(A, B, sa, sb, rows.ravel(), cols.ravel())
+    want = orc.scaled_mm_points(A, B, a, np.repeat(b, 128), 2, rows.ravel(), cols.ravel())
+    assert np.allclose(got, want, rtol=1e-13, atol=0)
+
+
+def test_per_token_group_quant_is_per_token_on_groups(orc):
+    """Each 128-wide group quantised exactly like a per-token row of its own
+    (the rows reshaped so that each group is a row), ragged last group."""
+    g = np.random.default_rng(122)
+    x = workloads.bf16_normal_with_outliers(g, (4, 512))
+    q, s = orc.quant_per_token_group(x)
+    q2, s2 = orc.quant_per_token(x.reshape(16, 128))
+    assert np.array_equal(q, q2.reshape(4, 512)) and np.array_equal(s, s2.reshape(4, 4))
+    x3 = workloads.bf16_normal(g, (2, 400))
+    q3, s3 = orc.quant_per_token_group(x3)
+    assert s3.shape == (2, 4)
+    qt, st = orc.quant_per_token(x3[:, 384:])
+    assert np.array_equal(q3[:, 384:], qt) and np.array_equal(s3[:, 3], st)
+
+
+def test_weight_block_quant(orc):
+    """Block scales from numpy's per-block amax / 448 in binary32, codes the
+    static quantisation of each block by its scale; the amax element of every
+    block maps to +-448; an all-zero block gets scale 1 and zero codes."""
+    g = np.random.default_rng(123)
+    w = workloads.bf16_normal(g, (256, 384), std=0.02)
+    w[:128, 128:256] = 0
+    q, s = orc.quant_weight_block(w)
+    wf = (w.astype(np.uint32) << 16).view(np.float32)
+    amax = np.abs(wf).reshape(2, 128, 3, 128).max(axis=(1, 3))
+    want_s = np.where(amax == 0, np.float32(1.0), amax / np.float32(448.0)).astype(np.float32)
+    assert np.array_equal(s, want_s)
+    for nb in range(2):
+        for gb in range(3):
+            blk = w[nb * 128:(nb + 1) * 128, gb * 128:(gb + 1) * 128]
+            assert np.array_equal(q[nb * 128:(nb + 1) * 128, gb * 128:(gb + 1) * 128],
+                                  orc.quant_static(blk, float(s[nb, gb])))
+            if amax[nb, gb] > 0:
+                assert np.max(q[nb * 128:(nb + 1) * 128, gb * 128:(gb + 1) * 128] & 0x7F) == 0x7E
+    assert s[0, 1] == 1.0 and np.all(q[:128, 128:256] == 0)
