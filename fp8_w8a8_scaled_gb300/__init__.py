@@ -8,7 +8,8 @@ fallback of any kind -- if the library is missing or a call fails, an
 exception is raised.
 
 Functions carry the C names: ``fp8_scaled_mm``, ``rmsnorm_quant_fp8``,
-``quant_fp8_per_token``, ``quant_fp8_static``.
+``quant_fp8_per_token``, ``quant_fp8_static``, and the blockwise-scaling
+quantisers ``quant_per_token_group`` / ``quant_weight_block``.
 """
 import ctypes
 import os
@@ -29,6 +30,8 @@ GRAN_PER_TENSOR = 0
 GRAN_PER_CHANNEL = 1
 GRAN_PER_TOKEN_CHANNEL = 2
 GRAN_PER_TOKEN = 3
+GRAN_BLOCK_128 = 4
+BLOCK = 128
 
 OUT_BF16 = 0
 
@@ -82,6 +85,10 @@ def lib():
     L.rmsnorm_quant_fp8.restype = I32
     L.quant_fp8_per_token.argtypes = [P, P, P, I64, I64, P]
     L.quant_fp8_per_token.restype = I32
+    L.fp8_quant_per_token_group.argtypes = [P, P, P, I64, I64, P]
+    L.fp8_quant_per_token_group.restype = I32
+    L.fp8_quant_weight_block.argtypes = [P, P, P, I64, I64, P]
+    L.fp8_quant_weight_block.restype = I32
     L.quant_fp8_static.argtypes = [P, P, P, I64, I64, P]
     L.quant_fp8_static.restype = I32
     L.fp8_status_string.argtypes = [I32]
@@ -145,9 +152,10 @@ _FP8 = (E4M3, torch.uint8)
 def fp8_scaled_mm(A, B, scale_a, scale_b, granularity=None, out_dtype=OUT_BF16, out=None, flags=0):
     """y = bf16((A @ B.T) * scale_a * scale_b) for E4M3 A [M,K] and B [N,K].
 
-    ``granularity`` defaults from the scale lengths: scale_a has 1 or M
-    elements, scale_b 1 or N.  ``flags`` are the C ABI's fp8_flags
-    (FLAG_WEIGHTS_STATIC, FLAG_NO_PDL)."""
+    ``granularity`` defaults from the scales: 2-D scales [M, ceil(K/128)] and
+    [ceil(N/128), ceil(K/128)] select the blockwise form, otherwise scale_a
+    has 1 or M elements and scale_b 1 or N.  ``flags`` are the C ABI's
+    fp8_flags (FLAG_WEIGHTS_STATIC, FLAG_NO_PDL)."""
     _need(A, "A", _FP8, 2)
     _need(B, "B", _FP8, 2)
     _need(scale_a, "scale_a", (torch.float32,))
@@ -156,12 +164,18 @@ def fp8_scaled_mm(A, B, scale_a, scale_b, granularity=None, out_dtype=OUT_BF16, 
     N, Kb = B.shape
     if Kb != K:
         raise ValueError(f"A is [{M},{K}] but B is [{N},{Kb}]")
+    if granularity is None and (scale_a.dim() == 2 or scale_b.dim() == 2):
+        granularity = GRAN_BLOCK_128
     if granularity is None:
         tok = scale_a.numel() == M and M != 1
         ch = scale_b.numel() == N and N != 1
         granularity = {(False, False): 0, (False, True): 1, (True, True): 2, (True, False): 3}[(tok, ch)]
-    want_a = M if granularity in (2, 3) else 1
-    want_b = N if granularity in (1, 2) else 1
+    KB = (K + BLOCK - 1) // BLOCK
+    if granularity == GRAN_BLOCK_128:
+        want_a, want_b = M * KB, ((N + BLOCK - 1) // BLOCK) * KB
+    else:
+        want_a = M if granularity in (2, 3) else 1
+        want_b = N if granularity in (1, 2) else 1
     if scale_a.numel() < want_a or scale_b.numel() < want_b:
         raise ValueError(f"granularity {granularity} needs scale_a[{want_a}], scale_b[{want_b}]")
     if out is None:
@@ -308,6 +322,48 @@ def quant_fp8_per_token(x, out=None, scale_out=None):
         _need(scale_out, "scale_out", (torch.float32,))
     _check(lib().quant_fp8_per_token(_ptr(x), _ptr(out), _ptr(scale_out), M, K, _stream_of(x)),
            "quant_fp8_per_token")
+    return out, scale_out
+
+
+def quant_per_token_group(x, out=None, scale_out=None):
+    """E4M3 quantisation of bf16 x [M,K] per token and per 128-wide group of K;
+    returns (q, s[M, ceil(K/128)])."""
+    _need(x, "x", (torch.bfloat16,), 2)
+    M, K = x.shape
+    KB = (K + BLOCK - 1) // BLOCK
+    if out is None:
+        out = torch.empty((M, K), dtype=E4M3, device=x.device)
+    else:
+        _need(out, "out", _FP8, 2)
+    if scale_out is None:
+        scale_out = torch.empty((M, KB), dtype=torch.float32, device=x.device)
+    else:
+        _need(scale_out, "scale_out", (torch.float32,))
+        if scale_out.numel() < M * KB:
+            raise ValueError(f"scale_out needs {M * KB} elements")
+    _check(lib().fp8_quant_per_token_group(_ptr(x), _ptr(out), _ptr(scale_out), M, K, _stream_of(x)),
+           "fp8_quant_per_token_group")
+    return out, scale_out
+
+
+def quant_weight_block(w, out=None, scale_out=None):
+    """E4M3 quantisation of a bf16 weight w [N,K] with one scale per 128 x 128
+    block; returns (q, s[ceil(N/128), ceil(K/128)])."""
+    _need(w, "w", (torch.bfloat16,), 2)
+    N, K = w.shape
+    KB, NB = (K + BLOCK - 1) // BLOCK, (N + BLOCK - 1) // BLOCK
+    if out is None:
+        out = torch.empty((N, K), dtype=E4M3, device=w.device)
+    else:
+        _need(out, "out", _FP8, 2)
+    if scale_out is None:
+        scale_out = torch.empty((NB, KB), dtype=torch.float32, device=w.device)
+    else:
+        _need(scale_out, "scale_out", (torch.float32,))
+        if scale_out.numel() < NB * KB:
+            raise ValueError(f"scale_out needs {NB * KB} elements")
+    _check(lib().fp8_quant_weight_block(_ptr(w), _ptr(out), _ptr(scale_out), N, K, _stream_of(w)),
+           "fp8_quant_weight_block")
     return out, scale_out
 
 

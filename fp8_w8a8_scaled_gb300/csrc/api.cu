@@ -163,7 +163,7 @@ const char *fp8_status_string(int status) {
 
 int fp8_describe_dispatch(int64_t M, int64_t N, int64_t K, int granularity) {
     if (M < 0 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > kI32Max) return -1;
-    if (granularity < 0 || granularity > 3) return -1;
+    if (granularity < 0 || granularity > FP8_GRAN_BLOCK_128) return -1;
     if (M == 0) return FP8_KERNEL_NONE;
     return M >= fp8k::kPrefillMinM ? FP8_KERNEL_PREFILL : FP8_KERNEL_DECODE_SPLITK;
 }
@@ -184,7 +184,7 @@ fp8_status fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, 
                             int granularity, int out_dtype, int64_t M, int64_t N, int64_t K, void *out, void *stream,
                             unsigned flags) {
     if (M < 0 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > kI32Max) return FP8_ERR_INVALID_ARG;
-    if (granularity < 0 || granularity > 3) return FP8_ERR_INVALID_ARG;
+    if (granularity < 0 || granularity > FP8_GRAN_BLOCK_128) return FP8_ERR_INVALID_ARG;
     if (flags & ~static_cast<unsigned>(FP8_FLAG_WEIGHTS_STATIC | FP8_FLAG_NO_PDL)) return FP8_ERR_INVALID_ARG;
     if (out_dtype != FP8_OUT_BF16) return FP8_ERR_UNSUPPORTED;
     if (M == 0) return FP8_OK;
@@ -227,7 +227,7 @@ fp8_status fp8_scaled_mm_noalloc(const void *A, const void *B, const float *scal
                                  int granularity, int out_dtype, int64_t M, int64_t N, int64_t K, void *out,
                                  void *stream) {
     if (M < 0 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > kI32Max) return FP8_ERR_INVALID_ARG;
-    if (granularity < 0 || granularity > 3) return FP8_ERR_INVALID_ARG;
+    if (granularity < 0 || granularity > FP8_GRAN_BLOCK_128) return FP8_ERR_INVALID_ARG;
     if (out_dtype != FP8_OUT_BF16) return FP8_ERR_UNSUPPORTED;
     if (M == 0) return FP8_OK;
     if (!A || !B || !scale_a || !scale_b || !out) return FP8_ERR_INVALID_ARG;
@@ -363,6 +363,32 @@ fp8_status quant_fp8_per_token(const void *x, void *out, float *scale_out, int64
     if (s != FP8_OK) return s;
     return from_cuda(fp8k::launch_quant_per_token(x, out, scale_out, M, K, st->err, static_cast<cudaStream_t>(stream),
                                                   st->num_sms, fp8k::LaunchOpts{}));
+}
+
+fp8_status fp8_quant_per_token_group(const void *x, void *out, float *scale_out, int64_t M, int64_t K, void *stream) {
+    if (M < 0 || M > kI32Max || K < 1 || K > (int64_t(1) << 30)) return FP8_ERR_INVALID_ARG;
+    if (M == 0) return FP8_OK;
+    if (!x || !out || !scale_out) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || !aligned4(scale_out)) return FP8_ERR_ALIGNMENT;
+    if (K % 16 != 0) return FP8_ERR_ALIGNMENT;
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    return from_cuda(fp8k::launch_quant_per_token_group(x, out, scale_out, M, K, static_cast<cudaStream_t>(stream),
+                                                        fp8k::LaunchOpts{}));
+}
+
+fp8_status fp8_quant_weight_block(const void *w, void *out, float *scale_out, int64_t N, int64_t K, void *stream) {
+    if (N < 0 || N > kI32Max || K < 1 || K > (int64_t(1) << 30)) return FP8_ERR_INVALID_ARG;
+    if (N == 0) return FP8_OK;
+    if (!w || !out || !scale_out) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(out) || !aligned4(scale_out)) return FP8_ERR_ALIGNMENT;
+    if (K % 16 != 0) return FP8_ERR_ALIGNMENT;
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    return from_cuda(fp8k::launch_quant_weight_block(w, out, scale_out, N, K, static_cast<cudaStream_t>(stream),
+                                                     fp8k::LaunchOpts{}));
 }
 
 fp8_status quant_fp8_static(const void *x, const float *scale, void *out, int64_t M, int64_t K, void *stream) {

@@ -159,7 +159,11 @@ __device__ __forceinline__ void fixup_sum(const DecodeArgs &args, const int64_t 
     }
 }
 
-template <int TOK>
+// kBlk: blockwise scaling (one activation scale per token per k-block, one
+// weight scale per 128-row tile per k-block).  Every k-block's partial sum is
+// multiplied by its scale product as it leaves TMEM, and the tile's output
+// takes no further scale.
+template <int TOK, bool kBlk>
 __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCfg<TOK>::kMaxRegs)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                        const DecodeArgs args) {
@@ -284,9 +288,9 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
         const uint32_t quarter = warp & 3u;          // a warp reaches TMEM lanes 32*(warp%4) .. +31
         const int row = static_cast<int>(quarter * 32u + lane);  // weight row within the tile
         const int col0 = static_cast<int>((warp - 2) / 4) * Cfg::kCols;
-        const bool sa_vec = (args.gran == 2 || args.gran == 3);
-        const bool sb_vec = (args.gran == 1 || args.gran == 2);
-        const float sa0 = __ldg(args.scale_a), sb0 = __ldg(args.scale_b);
+        const bool sa_vec = !kBlk && (args.gran == 2 || args.gran == 3);
+        const bool sb_vec = !kBlk && (args.gran == 1 || args.gran == 2);
+        const float sa0 = kBlk ? 1.0f : __ldg(args.scale_a), sb0 = kBlk ? 1.0f : __ldg(args.scale_b);
         const int t_first_me = static_cast<int>(u0 / kbt);
         if (tid == 64 && iters > 0) {
             // Which CTAs hold the other parts of this CTA's first and last tile
@@ -315,6 +319,16 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
             }
             const int b = i % NB;
             const uint32_t tph = static_cast<uint32_t>(i / NB) & 1u;
+            float bs[kBlk ? Cfg::kCols : 1];  // scale products of this k-block, per token column
+            if constexpr (kBlk) {
+                // requested before the wait so that the loads overlap it
+                const int nt = t % n_tiles, mb = (t / n_tiles) * TOK + col0;
+                const float sbk = __ldg(args.scale_b + static_cast<int64_t>(nt) * kbt + kb);
+#pragma unroll
+                for (int c = 0; c < Cfg::kCols; ++c)
+                    bs[c] = mb + c < args.M ? __fmul_rn(__ldg(args.scale_a + static_cast<int64_t>(mb + c) * kbt + kb), sbk)
+                                            : 0.0f;
+            }
             cta_wait(tfull_bar(b), tph, err, kErrDecodeTmemFullWait, &s_abort);
             __syncwarp();
             tc_fence_after();
@@ -330,7 +344,11 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
                     if (lane == 0) mbar_arrive(tempty_bar(b));
                 }
 #pragma unroll
-                for (int j = 0; j < 16; ++j) two_sum_acc(hi[c0 + j], lo[c0 + j], __uint_as_float(r[j]));
+                for (int j = 0; j < 16; ++j) {
+                    float p = __uint_as_float(r[j]);
+                    if constexpr (kBlk) p = __fmul_rn(p, bs[c0 + j]);
+                    two_sum_acc(hi[c0 + j], lo[c0 + j], p);
+                }
             }
 
             if (kb != kbt - 1 && i != iters - 1) continue;
@@ -419,17 +437,17 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
     }
 }
 
-template <int TOK>
+template <int TOK, bool kBlk>
 cudaError_t launch_tok(const CUtensorMap &tw, const CUtensorMap &ta, const DecodeArgs &a, const DecodePlan &p,
                        const LaunchOpts &o, cudaStream_t stream) {
     static bool attr_done = false;  // benign race: the attribute call is idempotent
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             200 * 1024);
+        cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<TOK, kBlk>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    return launch_with_opts(decode_gemm_kernel<TOK>, dim3(static_cast<unsigned>(p.ctas)),
+    return launch_with_opts(decode_gemm_kernel<TOK, kBlk>, dim3(static_cast<unsigned>(p.ctas)),
                             dim3(DecodeCfg<TOK>::kThreads), p.smem_bytes, stream, o, tw, ta, a);
 }
 
@@ -492,7 +510,8 @@ cudaError_t launch_decode_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tma
     a.n_tiles = plan.n_tiles;
     a.stages = plan.stages;
     a.weights_static = opts.weights_static ? 1 : 0;
-    return launch_tok<16>(tmap_w, tmap_a, a, plan, opts, stream);
+    if (granularity == kGranBlock128) return launch_tok<16, true>(tmap_w, tmap_a, a, plan, opts, stream);
+    return launch_tok<16, false>(tmap_w, tmap_a, a, plan, opts, stream);
 }
 
 }  // namespace fp8k

@@ -100,7 +100,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
-template <int BN>
+// kBlk: blockwise scaling.  The K range is drained after every k-block
+// (drain_kb == 1) and each k-block's partial sum is multiplied by its scale
+// product sa[m, kb] * sb[n / 128, kb] as it is added into the registers; the
+// tile's output then takes no further scale.
+template <int BN, bool kBlk>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                         const PrefillArgs args) {
@@ -224,9 +228,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const uint32_t quarter = warp & 3u;
         const int half = static_cast<int>(warp - 2) >> 2;
         const int row = static_cast<int>(quarter * 32u + lane);
-        const bool sa_vec = (args.gran == 2 || args.gran == 3);
-        const bool sb_vec = (args.gran == 1 || args.gran == 2);
-        const float sa0 = __ldg(args.scale_a), sb0 = __ldg(args.scale_b);
+        const bool sa_vec = !kBlk && (args.gran == 2 || args.gran == 3);
+        const bool sb_vec = !kBlk && (args.gran == 1 || args.gran == 2);
+        const float sa0 = kBlk ? 1.0f : __ldg(args.scale_a), sb0 = kBlk ? 1.0f : __ldg(args.scale_b);
         const int M = args.M, N = args.N;
         constexpr int kCols = BN / 2;  // columns of one thread
         uint32_t dc = 0;
@@ -238,8 +242,19 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             // a warp whose 32 token rows all lie beyond M (small M) only takes
             // part in the hand-shake
             const bool live = (t % m_tiles) * kPrefillBM + static_cast<int>(quarter * 32u) < M;
+            const int m_row = (t % m_tiles) * kPrefillBM + row;                  // this thread's token row
+            const int n_col = (t / m_tiles) * BN + half * kCols;                 // its first channel
             for (int kb0 = 0; kb0 < kbt; kb0 += dkb, ++dc) {
                 const int acc = static_cast<int>(dc & 1u);
+                float bsc = 0.0f;  // blockwise: scale product of k-block kb0, requested before the wait
+                if constexpr (kBlk) {
+                    if (live) {
+                        const float a = m_row < M ? __ldg(args.scale_a + static_cast<int64_t>(m_row) * kbt + kb0) : 0.0f;
+                        const float b =
+                            n_col < N ? __ldg(args.scale_b + static_cast<int64_t>(n_col / 128) * kbt + kb0) : 0.0f;
+                        bsc = __fmul_rn(a, b);
+                    }
+                }
                 if (!pf_warp_wait(tfull_bar(acc), (dc >> 1) & 1u, err, kErrPrefillAccumWait, &s_abort, lane)) {
                     ok = false;
                     break;
@@ -255,7 +270,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     tmem_ld16(tbase + static_cast<uint32_t>(j + 16), *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) y[j + q] = __fadd_rn(y[j + q], __uint_as_float(v[q]));
+                    for (int q = 0; q < 32; ++q) {
+                        if constexpr (kBlk)
+                            y[j + q] = __fmaf_rn(__uint_as_float(v[q]), bsc, y[j + q]);
+                        else
+                            y[j + q] = __fadd_rn(y[j + q], __uint_as_float(v[q]));
+                    }
                 }
                 }
                 tc_fence_before();
@@ -338,7 +358,7 @@ PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms) {
     return p;
 }
 
-template <int BN>
+template <int BN, bool kBlk>
 static cudaError_t launch_bn(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b, const PrefillArgs &a,
                              const PrefillPlan &plan, const LaunchOpts &opts, cudaStream_t stream) {
     int dev = 0;
@@ -346,12 +366,12 @@ static cudaError_t launch_bn(const CUtensorMap &tmap_a, const CUtensorMap &tmap_
     if (e != cudaSuccess) return e;
     static bool attr_done[64] = {};  // benign race: the attribute call is idempotent
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(prefill_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(prefill_gemm_kernel<BN, kBlk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(prefill_smem_bytes(PrefillCfg<BN>::kStages, BN)));
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
-    return launch_with_opts(prefill_gemm_kernel<BN>, dim3(static_cast<unsigned>(plan.ctas)), dim3(kPrefillThreads),
+    return launch_with_opts(prefill_gemm_kernel<BN, kBlk>, dim3(static_cast<unsigned>(plan.ctas)), dim3(kPrefillThreads),
                             plan.smem_bytes, stream, opts, tmap_a, tmap_b, a);
 }
 
@@ -373,8 +393,14 @@ cudaError_t launch_prefill_gemm(const CUtensorMap &tmap_a, const CUtensorMap &tm
     a.tiles = plan.m_tiles * plan.n_tiles;
     a.stages = plan.stages;
     a.drain_kb = plan.drain_kb;
-    if (plan.bn == 128) return launch_bn<128>(tmap_a, tmap_b, a, plan, opts, stream);
-    return launch_bn<256>(tmap_a, tmap_b, a, plan, opts, stream);
+    if (granularity == kGranBlock128) {
+        // every k-block has its own scales: drain after each one
+        a.drain_kb = 1;
+        if (plan.bn == 128) return launch_bn<128, true>(tmap_a, tmap_b, a, plan, opts, stream);
+        return launch_bn<256, true>(tmap_a, tmap_b, a, plan, opts, stream);
+    }
+    if (plan.bn == 128) return launch_bn<128, false>(tmap_a, tmap_b, a, plan, opts, stream);
+    return launch_bn<256, false>(tmap_a, tmap_b, a, plan, opts, stream);
 }
 
 }  // namespace fp8k

@@ -48,6 +48,13 @@ cudaError_t launch_quant_static(const void *x, const float *scale, void *out, in
 cudaError_t launch_quant_per_token(const void *x, void *out, float *scale_out, int64_t M, int64_t K,
                                    uint32_t *err, cudaStream_t stream, int num_sms, const LaunchOpts &opts);
 
+// Blockwise quantisers: 128-wide token groups (scales [M, ceil(K/128)]) and
+// 128 x 128 weight blocks (scales [ceil(N/128), ceil(K/128)]).
+cudaError_t launch_quant_per_token_group(const void *x, void *out, float *scale_out, int64_t M, int64_t K,
+                                         cudaStream_t stream, const LaunchOpts &opts);
+cudaError_t launch_quant_weight_block(const void *w, void *out, float *scale_out, int64_t N, int64_t K,
+                                      cudaStream_t stream, const LaunchOpts &opts);
+
 // Weight shards (each [rows_j, K] E4M3 with a per-tensor scale) merged into one
 // weight requantised to the largest scale.
 constexpr int kMaxMergeShards = 16;
@@ -75,6 +82,9 @@ cudaError_t launch_rmsnorm_quant(const void *x, const void *gamma, float eps, co
 
 // Tile geometry of the weight-streaming kernel: 128 weight rows (output
 // channels) per tile on the tensor core's M side, up to 64 tokens on its N side.
+// Granularity code of blockwise scaling (fp8_granularity FP8_GRAN_BLOCK_128):
+// scales per 128-wide k-block, per token and per 128-row weight block.
+constexpr int kGranBlock128 = 4;
 constexpr int kDecodeRows = 128;
 constexpr int kBlockK = 128;  // bytes (= E4M3 elements) of K per pipeline stage
 constexpr int kDecodeMaxTokens = 16;

@@ -272,6 +272,83 @@ __global__ void __launch_bounds__(256) silu_mul_quant_cluster_kernel(const uint4
     }
 }
 
+// ------------------------------------------------------ blockwise quantisers --
+
+// Per-token-group quantisation: each 128-wide group of a row is quantised on
+// its own (s = amax/448, 1.0 for an all-zero group).  A half-warp owns a group
+// (16 lanes x one 16-byte vector of 8 bf16), so a warp does two groups and a
+// CTA of 8 warps sixteen groups of one row; the group max is a 16-lane
+// shuffle reduction.  Work item b (grid-stride) is row b / chunks, groups
+// 16 * (b % chunks) onwards.
+__global__ void __launch_bounds__(256) quant_per_token_group_kernel(const uint4 *__restrict__ x,
+                                                                    uint2 *__restrict__ out,
+                                                                    float *__restrict__ scale_out, int64_t items,
+                                                                    int chunks, int nvec, int KB) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    for (int64_t b = blockIdx.x; b < items; b += gridDim.x) {
+        const int64_t row = b / chunks;
+        const int grp = static_cast<int>(b - row * chunks) * 16 + static_cast<int>(threadIdx.x >> 4);
+        const int vec = grp * 16 + (lane & 15);
+        const bool ok = grp < KB && vec < nvec;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        float amax = 0.0f;
+        if (ok) {
+            v = ld_stream(x + row * nvec + vec);
+            amax = absmax8(v, 0.0f);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+        if (ok) {
+            out[row * nvec + vec] = quant8(v, s);
+            if ((lane & 15) == 0) scale_out[row * KB + grp] = s;
+        }
+    }
+}
+
+// Per-block weight quantisation: one CTA per 128 x 128 block (2048 vectors of
+// 8, eight per thread), s = amax/448 of the block (1.0 if all zero).  Work
+// item b (grid-stride) is block row b / KB, k-group b % KB.
+__global__ void __launch_bounds__(256) quant_weight_block_kernel(const uint4 *__restrict__ w, uint2 *__restrict__ out,
+                                                                 float *__restrict__ scale_out, int64_t N,
+                                                                 int64_t items, int nvec, int KB) {
+    __shared__ float red[32];
+    grid_dependency_wait();
+    grid_launch_dependents();
+    for (int64_t b = blockIdx.x; b < items; b += gridDim.x) {
+        const int64_t nb = b / KB;
+        const int g = static_cast<int>(b - nb * KB);
+        uint4 v[8];
+        bool ok[8];
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int t = static_cast<int>(threadIdx.x) + j * 256;
+            const int64_t n = nb * 128 + (t >> 4);
+            const int kv = g * 16 + (t & 15);
+            ok[j] = n < N && kv < nvec;
+            v[j] = make_uint4(0, 0, 0, 0);
+            if (ok[j]) {
+                v[j] = ld_stream(w + n * nvec + kv);
+                amax = absmax8(v[j], amax);
+            }
+        }
+        amax = block_max(amax, red);
+        const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+        if (threadIdx.x == 0) scale_out[nb * KB + g] = s;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int t = static_cast<int>(threadIdx.x) + j * 256;
+            const int64_t n = nb * 128 + (t >> 4);
+            const int kv = g * 16 + (t & 15);
+            if (ok[j]) out[n * nvec + kv] = quant8(v[j], s);
+        }
+        __syncthreads();  // red[] is reused by the next item
+    }
+}
+
 // ---------------------------------------------------- shard requantisation --
 
 // Shards [rows_j, K] of E4M3 weights with per-tensor scales s_j, merged into
@@ -406,6 +483,26 @@ cudaError_t launch_quant_per_token(const void *x, void *out, float *scale_out, i
     if (nvec <= 16384) return launch_rows_pt<16>(x, out, scale_out, M, K, stream, o);
     return launch_with_opts(quant_per_token_long_kernel, dim3(static_cast<unsigned>(M)), dim3(512), 0, stream, o,
                             static_cast<const uint4 *>(x), static_cast<uint2 *>(out), scale_out, nvec);
+}
+
+cudaError_t launch_quant_per_token_group(const void *x, void *out, float *scale_out, int64_t M, int64_t K,
+                                         cudaStream_t stream, const LaunchOpts &o) {
+    const int nvec = static_cast<int>(K / 8), KB = static_cast<int>((K + 127) / 128);
+    const int chunks = (KB + 15) / 16;
+    const int64_t items = M * chunks;
+    const unsigned grid = static_cast<unsigned>(items < (int64_t(1) << 20) ? items : (int64_t(1) << 20));
+    return launch_with_opts(quant_per_token_group_kernel, dim3(grid), dim3(256), 0, stream, o,
+                            static_cast<const uint4 *>(x), static_cast<uint2 *>(out), scale_out, items, chunks, nvec,
+                            KB);
+}
+
+cudaError_t launch_quant_weight_block(const void *w, void *out, float *scale_out, int64_t N, int64_t K,
+                                      cudaStream_t stream, const LaunchOpts &o) {
+    const int nvec = static_cast<int>(K / 8), KB = static_cast<int>((K + 127) / 128);
+    const int64_t items = ((N + 127) / 128) * KB;
+    const unsigned grid = static_cast<unsigned>(items < (int64_t(1) << 20) ? items : (int64_t(1) << 20));
+    return launch_with_opts(quant_weight_block_kernel, dim3(grid), dim3(256), 0, stream, o,
+                            static_cast<const uint4 *>(w), static_cast<uint2 *>(out), scale_out, N, items, nvec, KB);
 }
 
 cudaError_t launch_requant_merge(const MergeArgs &a, cudaStream_t stream, int num_sms, const LaunchOpts &o) {

@@ -68,7 +68,13 @@ typedef enum {
     FP8_GRAN_PER_TENSOR = 0,         /* scale_a[1], scale_b[1] */
     FP8_GRAN_PER_CHANNEL = 1,        /* scale_a[1], scale_b[N]: one scale per output channel */
     FP8_GRAN_PER_TOKEN_CHANNEL = 2,  /* scale_a[M], scale_b[N] */
-    FP8_GRAN_PER_TOKEN = 3           /* scale_a[M], scale_b[1] */
+    FP8_GRAN_PER_TOKEN = 3,          /* scale_a[M], scale_b[1] */
+    /* Blockwise: scale_a[M][ceil(K/128)] (one per token per 128-wide group of
+     * K), scale_b[ceil(N/128)][ceil(K/128)] (one per 128 x 128 weight block),
+     * both row-major; y[m,n] = sum_g sa[m,g] * sb[n/128,g] * acc_g[m,n] with
+     * acc_g the group's sum of products ([P4] commit message: "dense FP8
+     * non-blockwise" implies a blockwise FP8 variant). */
+    FP8_GRAN_BLOCK_128 = 4
 } fp8_granularity;
 
 /* Output dtype.  Only bf16: the pages' finding is that an F32 GEMM output
@@ -292,6 +298,37 @@ fp8_status fp8_rmsnorm_quant_scaled_mm(const void *x, const void *gamma, float e
  *   per-tensor quantisation with s = amax/448. */
 fp8_status quant_fp8_per_token(const void *x, void *out, float *scale_out, int64_t M, int64_t K,
                                void *stream);
+
+/* fp8_quant_per_token_group -- dynamic E4M3 quantisation per token and per
+ * 128-wide group of K, the activation side of FP8_GRAN_BLOCK_128.
+ *
+ * Source: [P4] commit message ("dense FP8 non-blockwise" sets a blockwise
+ * variant apart); the group width 128 is this library's reading.
+ *
+ *   x          bf16 [M,K] row-major, 16-byte aligned
+ *   out        E4M3 [M,K], 16-byte aligned
+ *   scale_out  f32 [M][ceil(K/128)] row-major: each group quantised exactly as
+ *              quant_fp8_per_token would quantise that group alone (the last
+ *              group of a row may be narrower than 128).
+ *   K % 16 == 0, K <= 2^30.
+ * Errors: FP8_ERR_INVALID_ARG, FP8_ERR_ALIGNMENT, FP8_ERR_CUDA. */
+fp8_status fp8_quant_per_token_group(const void *x, void *out, float *scale_out, int64_t M, int64_t K,
+                                     void *stream);
+
+/* fp8_quant_weight_block -- E4M3 quantisation of a weight [N,K] with one scale
+ * per 128 x 128 block, the weight side of FP8_GRAN_BLOCK_128.
+ *
+ * Source: as fp8_quant_per_token_group.
+ *
+ *   w          bf16 [N,K] row-major, 16-byte aligned
+ *   out        E4M3 [N,K], 16-byte aligned
+ *   scale_out  f32 [ceil(N/128)][ceil(K/128)] row-major: s = amax over the
+ *              block / 448 in binary32 (1.0 for an all-zero block; NaN
+ *              entries do not take part); q = e4m3_rne_sat(w / s).  Edge
+ *              blocks cover what is left of N and K.
+ *   K % 16 == 0, K <= 2^30, N < 2^31.
+ * Errors: FP8_ERR_INVALID_ARG, FP8_ERR_ALIGNMENT, FP8_ERR_CUDA. */
+fp8_status fp8_quant_weight_block(const void *w, void *out, float *scale_out, int64_t N, int64_t K, void *stream);
 
 /* quant_fp8_static -- static per-tensor E4M3 quantisation, q = e4m3_rne_sat(x / s).
  *

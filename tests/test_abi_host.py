@@ -65,7 +65,9 @@ def test_scaled_mm_validation(L):
     assert mm(L, N=0) == 1
     assert mm(L, K=0) == 1
     assert mm(L, M=2 ** 31) == 1
-    assert mm(L, gran=4) == 1
+    assert mm(L, gran=5) == 1
+    assert mm(L, gran=4, M=0) == 0                             # blockwise is a valid granularity
+    assert mm(L, gran=4, K=72) == 2
     assert mm(L, gran=-1) == 1
     assert mm(L, od=1) == 3                                    # only bf16 output
     assert mm(L, A=None) == 1
@@ -170,6 +172,18 @@ def test_quantiser_validation(L):
     assert L.quant_fp8_per_token(GOOD, P(0x20008), SC, 4, 64, None) == 2
     assert L.quant_fp8_per_token(GOOD, GOOD2, SC, 4, 0, None) == 1
     assert L.quant_fp8_per_token(GOOD, GOOD2, SC, 4, 2 ** 31, None) == 1
+    for fn in (L.fp8_quant_per_token_group, L.fp8_quant_weight_block):
+        assert fn(GOOD, GOOD2, SC, 0, 64, None) == 0              # no rows: nothing launched
+        assert fn(None, GOOD2, SC, 4, 64, None) == 1
+        assert fn(GOOD, None, SC, 4, 64, None) == 1
+        assert fn(GOOD, GOOD2, None, 4, 64, None) == 1
+        assert fn(GOOD, GOOD2, SC, -1, 64, None) == 1
+        assert fn(GOOD, GOOD2, SC, 4, 0, None) == 1
+        assert fn(GOOD, GOOD2, SC, 4, 2 ** 31, None) == 1
+        assert fn(GOOD, GOOD2, SC, 4, 72, None) == 2             # K % 16
+        assert fn(P(0x10008), GOOD2, SC, 4, 64, None) == 2
+        assert fn(GOOD, P(0x20004), SC, 4, 64, None) == 2
+        assert fn(GOOD, GOOD2, P(0x40002), 4, 64, None) == 2
     assert L.rmsnorm_quant_fp8(GOOD, GOOD2, ctypes.c_float(1e-6), SC, GOOD3, 0, 64, None) == 0
     assert L.rmsnorm_quant_fp8(GOOD, None, ctypes.c_float(1e-6), SC, GOOD3, 4, 64, None) == 1
     assert L.rmsnorm_quant_fp8(GOOD, GOOD2, ctypes.c_float(1e-6), SC, GOOD3, 4, 65536 + 16, None) == 1
@@ -181,6 +195,9 @@ def test_describe_dispatch_is_pure(L):
     assert L.fp8_describe_dispatch(0, 64, 64, 0) == 0
     assert L.fp8_describe_dispatch(-1, 64, 64, 0) == -1
     assert L.fp8_describe_dispatch(4, 64, 64, 7) == -1
+    assert L.fp8_describe_dispatch(4, 64, 64, 5) == -1
+    assert L.fp8_describe_dispatch(16, 10240, 5120, 4) == 1        # blockwise: same split as the others
+    assert L.fp8_describe_dispatch(17, 10240, 5120, 4) == 2
     for M in (1, 2, 4, 8, 16):
         assert L.fp8_describe_dispatch(M, 10240, 5120, 1) == 1
     for M in (17, 32, 33, 64, 65, 128, 2048, 8192):

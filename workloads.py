@@ -142,14 +142,18 @@ def prefill(seed: int = 0, m: int = 2048, n: int = QKV_N, k: int = HIDDEN):
 def random_gemm(seed: int, M: int, N: int, K: int, gran: int):
     """Random E4M3 operands and positive scales for a GEMM of the given shape
     and granularity (0 per-tensor, 1 per-channel, 2 per-token x channel,
-    3 per-token)."""
+    3 per-token, 4 blockwise: sa [M, ceil(K/128)], sb [ceil(N/128), ceil(K/128)])."""
     g = rng(seed)
     A = e4m3_codes(g, (M, K))
     B = e4m3_codes(g, (N, K))
-    na = M if gran in (2, 3) else 1
-    nb = N if gran in (1, 2) else 1
-    sa = uniform_f32(g, (na,), 0.25, 4.0) * np.float32(1e-2)
-    sb = uniform_f32(g, (nb,), 0.25, 4.0) * np.float32(1e-3)
+    if gran == 4:
+        na = (M, -(-K // 128))
+        nb = (-(-N // 128), -(-K // 128))
+    else:
+        na = (M if gran in (2, 3) else 1,)
+        nb = (N if gran in (1, 2) else 1,)
+    sa = uniform_f32(g, na, 0.25, 4.0) * np.float32(1e-2)
+    sb = uniform_f32(g, nb, 0.25, 4.0) * np.float32(1e-3)
     return dict(A=A, B=B, sa=sa.astype(np.float32), sb=sb.astype(np.float32))
 
 
