@@ -529,8 +529,9 @@ def run_ours(args, rank, world, dist_barrier, dist_max):
         "config": {"workload": WORKLOAD, "bytes_per_step": step_bytes(), "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: six distinct 52.4 MB weights per step (315 MB)",
                    "graph": f"{INNER} steps per CUDA graph replay"},
-        "roofline": {"kernel": "decode_gemm_kernel (tcgen05 swap-AB, persistent stream-K), the M = "
-                               + "/".join(str(m) for m in dms) + " GEMMs of the step (M = 32 runs the tile kernel)",
+        "roofline": {"kernel": "decode_gemm_kernel (tcgen05 swap-AB; 3-CTA clusters per 128-channel tile on QKV, "
+                               "partial sums reduced through distributed shared memory), the M = "
+                               + "/".join(str(m) for m in dms) + " GEMMs of the step",
                      "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": recorded_traffic(),

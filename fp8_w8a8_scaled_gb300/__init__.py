@@ -97,6 +97,8 @@ def lib():
     L.fp8_describe_dispatch.restype = I32
     L.fp8_decode_ctas.argtypes = [I64, I64, I64]
     L.fp8_decode_ctas.restype = I32
+    L.fp8_decode_split_for_sms.argtypes = [I64, I64, I64, I32]
+    L.fp8_decode_split_for_sms.restype = I32
     L.fp8_decode_ctas_for_sms.argtypes = [I64, I64, I64, I32]
     L.fp8_decode_ctas_for_sms.restype = I32
     L.fp8_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
@@ -386,6 +388,14 @@ def describe_dispatch(M, N, K, granularity=0) -> int:
 
 def decode_ctas(M, N, K) -> int:
     return lib().fp8_decode_ctas(M, N, K)
+
+
+def decode_split(M, N, K, num_sms=None) -> int:
+    """The decode kernel's mode: S >= 1 CTAs per output tile (clusters), 0 for
+    the persistent stream-K grid, -1 if the shape does not go to it."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return lib().fp8_decode_split_for_sms(M, N, K, int(num_sms))
 
 
 def get_device_error(stream=None) -> int:

@@ -173,6 +173,11 @@ int fp8_decode_ctas_for_sms(int64_t M, int64_t N, int64_t K, int num_sms) {
     return fp8k::plan_decode(M, N, K, num_sms).ctas;
 }
 
+int fp8_decode_split_for_sms(int64_t M, int64_t N, int64_t K, int num_sms) {
+    if (fp8_describe_dispatch(M, N, K, 0) != FP8_KERNEL_DECODE_SPLITK || num_sms < 1) return -1;
+    return fp8k::plan_decode(M, N, K, num_sms).split;
+}
+
 int fp8_decode_ctas(int64_t M, int64_t N, int64_t K) {
     DeviceState *st = nullptr;
     if (fp8_describe_dispatch(M, N, K, 0) != FP8_KERNEL_DECODE_SPLITK) return -1;

@@ -12,10 +12,17 @@
 // Design (GB300, sm_103a).  At decode M every weight byte is used M times, so
 // the kernel is bound by streaming B from HBM once, and every SM must stream
 // its equal share all the time.  The work is cut into units of one output tile
-// (128 weight rows x up to 16 tokens) by one 128-wide k-block; a persistent
-// grid of two CTAs per SM gives CTA c the contiguous units
-// [c*U/G, (c+1)*U/G) ("stream-K"), so all CTAs stream the same number of bytes
-// whatever the shape.  Inside a CTA:
+// (128 weight rows x up to 16 tokens) by one 128-wide k-block, and given out
+// in one of two ways:
+//   * cluster mode (enough tiles: N >= ~3840 on 152 SMs): a cluster of S CTAs
+//     per tile, CTA r taking k-blocks [r*kb/S, (r+1)*kb/S), with S chosen so
+//     the grid is ~1.6 CTAs per SM; the S parts are summed through
+//     distributed shared memory (below).  S = 1 (as many tiles as ~1.6 x SMs)
+//     is whole tiles, nothing to sum;
+//   * stream-K (few tiles with long K ranges): a persistent grid of two CTAs
+//     per SM gives CTA c the contiguous units [c*U/G, (c+1)*U/G), so all CTAs
+//     stream the same number of bytes whatever the shape.
+// Inside a CTA:
 //   * warp 0 / lane 0 streams the units' 128 x 128-byte weight boxes and the
 //     matching token boxes with TMA into a ring of shared-memory stages
 //     (128-byte swizzle), L2 evict-first for the once-read weights;
@@ -29,7 +36,10 @@
 //     only roundings left are the tensor core's inside one 128-wide k-block.
 // When a tile's K range ends inside the CTA, the drain warps either store the
 // tile (scales in binary32, then bf16) or, if other CTAs hold the rest of the
-// tile's K range, write their part (hi + lo, rounded once to binary32) to a
+// tile's K range: in cluster mode, store their part of each row into the
+// shared memory of the cluster CTA that sums that row, and after one cluster
+// barrier every CTA sums its rows over the S parts in k order; in stream-K
+// mode, write their part (hi + lo, rounded once to binary32) to a
 // workspace slot and count in on the tile's arrival counter (a barrier, then
 // one thread's release fence and atomic add); the CTA that arrives last
 // acquires, sums all slots in k order (so the result does not depend on
@@ -94,7 +104,12 @@ struct DecodeArgs {
     float *slots;
     int64_t units;
     int gran, M, N, kb_total, n_tiles, stages, weights_static;
+    int split;  // cluster mode: CTAs (one cluster) per tile; 0 in stream-K mode
 };
+
+// Cluster mode: rows [red_row_begin(q, S), red_row_begin(q + 1, S)) of a tile
+// are summed by CTA q of the tile's cluster; at most ceil(128 / S) of them.
+__host__ __device__ __forceinline__ int red_row_begin(int q, int S) { return (q * kDecodeRows + S - 1) / S; }
 
 // A bounded wait that gives up at once when the CTA has already given up:
 // after one wait times out the kernel keeps its control flow (so barriers stay
@@ -162,8 +177,17 @@ __device__ __forceinline__ void fixup_sum(const DecodeArgs &args, const int64_t 
 // kBlk: blockwise scaling (one activation scale per token per k-block, one
 // weight scale per 128-row tile per k-block).  Every k-block's partial sum is
 // multiplied by its scale product as it leaves TMEM, and the tile's output
-// takes no further scale.
-template <int TOK, bool kBlk>
+// takes no further scale.  Lanes 1..TOK of warp 0 write the scale products of
+// each unit into a shared-memory slot beside its TMEM accumulator, up to
+// kBufs units ahead of the drain (so the scale loads' latency is hidden), and
+// the accumulator's "full" barrier waits for them as well as for the MMA.
+// kCluster: the grid is one cluster of `split` CTAs per output tile, CTA r of
+// the cluster taking k-blocks [r*kb/S, (r+1)*kb/S) of the tile; the parts are
+// summed through distributed shared memory instead of the workspace: every CTA
+// stores its fp32 part of rows [red_row_begin(q), red_row_begin(q+1)) into
+// CTA q's reduction area, one cluster barrier, then CTA q sums its rows over
+// the S parts in rank (= k) order and stores them.
+template <int TOK, bool kBlk, bool kCluster>
 __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCfg<TOK>::kMaxRegs)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                        const DecodeArgs args) {
@@ -177,6 +201,7 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
     __shared__ int64_t s_slot[2][kMaxFixupSegs];
     __shared__ int s_nseg[2];
     __shared__ volatile uint32_t s_abort;
+    __shared__ float s_bscale[kBlk ? NB : 1][TOK];  // blockwise: scale products per accumulator
 
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int stages = args.stages;
@@ -191,7 +216,15 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
 
     const int64_t G = gridDim.x, U = args.units;
     const int64_t me = blockIdx.x;
-    const int64_t u0 = unit_begin(me, U, G), u1 = unit_begin(me + 1, U, G);
+    const int S = kCluster ? args.split : 1;
+    const int c_rank = kCluster ? static_cast<int>(me % S) : 0;  // == %cluster_ctarank (clusters along x)
+    const int64_t u0 = kCluster ? (me / S) * args.kb_total + (static_cast<int64_t>(c_rank) * args.kb_total) / S
+                                : unit_begin(me, U, G);
+    const int64_t u1 = kCluster ? (me / S) * args.kb_total + (static_cast<int64_t>(c_rank + 1) * args.kb_total) / S
+                                : unit_begin(me + 1, U, G);
+    const int red_rows = (kDecodeRows + S - 1) / S;  // cluster mode: rows per reduction slot
+    // cluster mode: the reduction area, [S parts][TOK tokens][red_rows rows] fp32, after the barriers
+    const uint32_t red_base = bar0 + ((8u * static_cast<uint32_t>(2 * stages + 2 * NB + 1) + 127u) & ~127u);
     const int iters = static_cast<int>(u1 - u0);
     const int kbt = args.kb_total, n_tiles = args.n_tiles;
     uint32_t *const err = args.err;
@@ -204,7 +237,7 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
             mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < NB; ++b) {
-            mbar_init(tfull_bar(b), 1);
+            mbar_init(tfull_bar(b), kBlk ? 2 : 1);  // MMA commit (+ scale writer)
             mbar_init(tempty_bar(b), 4 * Cfg::kDrainGroups);  // one arrive per drain warp
         }
         mbar_init(final_bar, 1);
@@ -218,6 +251,10 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem_base;
+    // Cluster mode: a first cluster barrier, waited for before the first store
+    // into another CTA's shared memory, so that every CTA of the cluster is
+    // known to be running by then.
+    if (kCluster && S > 1) cluster_arrive_relaxed();
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------------- producer
@@ -260,6 +297,36 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
         // waited for above): the next kernel in the stream may now launch, so
         // its prologue and weight prefetch overlap this CTA's drain and fixup.
         grid_launch_dependents();
+    } else if (kBlk && warp == 0 && lane >= 1 && lane <= 16) {
+        // ---------------------------------------------------------------- scale writer (blockwise)
+        constexpr unsigned kMask = 0xFFFFu << 1;  // lanes 1..16, token columns lane-1 (+16)
+        grid_dependency_wait();  // the scales may come from the previous kernel
+        const int c0 = static_cast<int>(lane) - 1;
+        int t = static_cast<int>(u0 / kbt), kb = static_cast<int>(u0 - static_cast<int64_t>(t) * kbt);
+        for (int i = 0; i < iters; ++i, ++kb) {
+            if (kb == kbt) {
+                kb = 0;
+                ++t;
+            }
+            const int b = i % NB;
+            const uint32_t tph = static_cast<uint32_t>(i / NB) & 1u;
+            const int nt = t % n_tiles, m0 = (t / n_tiles) * TOK;
+            const float sbk = __ldg(args.scale_b + static_cast<int64_t>(nt) * kbt + kb);
+            float sak[TOK / 16];
+#pragma unroll
+            for (int j = 0; j < TOK / 16; ++j) {
+                const int m = m0 + c0 + 16 * j;
+                sak[j] = m < args.M ? __ldg(args.scale_a + static_cast<int64_t>(m) * kbt + kb) : 0.0f;
+            }
+            uint32_t ok = 1;
+            if (lane == 1) ok = cta_wait(tempty_bar(b), tph ^ 1u, err, kErrDecodeTmemEmptyWait, &s_abort) ? 1u : 0u;
+            ok = __shfl_sync(kMask, ok, 1);
+            if (!ok) break;
+#pragma unroll
+            for (int j = 0; j < TOK / 16; ++j) s_bscale[b][c0 + 16 * j] = __fmul_rn(sak[j], sbk);
+            __syncwarp(kMask);  // every lane's slot write before lane 1's (release) arrival
+            if (lane == 1) mbar_arrive(tfull_bar(b));
+        }
     } else if (warp == 1 && lane == 0) {
         // ---------------------------------------------------------------- MMA issuer
         int i = 0;
@@ -292,7 +359,7 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
         const bool sb_vec = !kBlk && (args.gran == 1 || args.gran == 2);
         const float sa0 = kBlk ? 1.0f : __ldg(args.scale_a), sb0 = kBlk ? 1.0f : __ldg(args.scale_b);
         const int t_first_me = static_cast<int>(u0 / kbt);
-        if (tid == 64 && iters > 0) {
+        if (!kCluster && tid == 64 && iters > 0) {
             // Which CTAs hold the other parts of this CTA's first and last tile
             // and where their partial sums go, worked out while the first
             // loads are in flight.
@@ -319,16 +386,6 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
             }
             const int b = i % NB;
             const uint32_t tph = static_cast<uint32_t>(i / NB) & 1u;
-            float bs[kBlk ? Cfg::kCols : 1];  // scale products of this k-block, per token column
-            if constexpr (kBlk) {
-                // requested before the wait so that the loads overlap it
-                const int nt = t % n_tiles, mb = (t / n_tiles) * TOK + col0;
-                const float sbk = __ldg(args.scale_b + static_cast<int64_t>(nt) * kbt + kb);
-#pragma unroll
-                for (int c = 0; c < Cfg::kCols; ++c)
-                    bs[c] = mb + c < args.M ? __fmul_rn(__ldg(args.scale_a + static_cast<int64_t>(mb + c) * kbt + kb), sbk)
-                                            : 0.0f;
-            }
             cta_wait(tfull_bar(b), tph, err, kErrDecodeTmemFullWait, &s_abort);
             __syncwarp();
             tc_fence_after();
@@ -338,7 +395,7 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
                 uint32_t r[16];
                 tmem_ld16(taddr + static_cast<uint32_t>(c0), r);
                 tmem_ld_wait();
-                if (c0 + 16 >= Cfg::kCols) {  // last chunk read: the buffer is free for the MMA again
+                if (!kBlk && c0 + 16 >= Cfg::kCols) {  // last chunk read: the buffer is free for the MMA again
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(tempty_bar(b));
@@ -346,9 +403,14 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     float p = __uint_as_float(r[j]);
-                    if constexpr (kBlk) p = __fmul_rn(p, bs[c0 + j]);
+                    if constexpr (kBlk) p = __fmul_rn(p, s_bscale[b][col0 + c0 + j]);
                     two_sum_acc(hi[c0 + j], lo[c0 + j], p);
                 }
+            }
+            if constexpr (kBlk) {  // TMEM and the scale slot both free: the writer may refill it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(b));
             }
 
             if (kb != kbt - 1 && i != iters - 1) continue;
@@ -360,7 +422,19 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
             const int mt = min(TOK, args.M - m0);
             const int64_t tile_u0 = static_cast<int64_t>(t) * kbt;
             const bool whole = (u0 <= tile_u0) && (kb == kbt - 1);
-            if (!whole) {
+            if (kCluster && !whole) {
+                // this CTA's part of the tile, rounded once to binary32, into
+                // the reduction area of the CTA that sums this row
+                cluster_wait();  // (the drain warps' half of the first cluster barrier)
+                const int q = (row * S) / kDecodeRows;
+                const int lr = row - red_row_begin(q, S);
+                const uint32_t dst = map_to_rank(
+                    red_base + 4u * static_cast<uint32_t>((c_rank * TOK) * red_rows + lr), static_cast<uint32_t>(q));
+#pragma unroll
+                for (int c = 0; c < Cfg::kCols; ++c)
+                    if (col0 + c < mt) st_cluster_f32(dst + 4u * static_cast<uint32_t>((col0 + c) * red_rows),
+                                                      __fadd_rn(hi[c], lo[c]));
+            } else if (!kCluster && !whole) {
                 // this CTA's part of the tile, rounded once to binary32
                 float *mine = args.slots + static_cast<int64_t>(2 * me + (t == t_first_me ? 0 : 1)) * kSlotElems;
 #pragma unroll
@@ -423,6 +497,36 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
     grid_launch_dependents();
     __syncthreads();
 
+    if constexpr (kCluster) {
+        if (S > 1) {
+            if (warp < 2) cluster_wait();  // the other warps' half of the first cluster barrier
+            // every part of every row this CTA sums has landed (and no CTA of
+            // the cluster touches another's shared memory after this point)
+            cluster_sync();
+            if (warp >= 2) {
+                const int tile = static_cast<int>(me / S);
+                const int rb = red_row_begin(c_rank, S), nr = red_row_begin(c_rank + 1, S) - rb;
+                const int mt = min(TOK, args.M);
+                const bool sa_vec = !kBlk && (args.gran == 2 || args.gran == 3);
+                const bool sb_vec = !kBlk && (args.gran == 1 || args.gran == 2);
+                const float sa0 = kBlk ? 1.0f : __ldg(args.scale_a), sb0 = kBlk ? 1.0f : __ldg(args.scale_b);
+                const float *red = reinterpret_cast<const float *>(smem_raw + (red_base - raw));
+                for (int e = static_cast<int>(tid) - 64; e < nr * mt; e += Cfg::kDrainThreads) {
+                    const int m = e / nr, lr = e - m * nr;  // consecutive threads: consecutive channels
+                    const int n = tile * kDecodeRows + rb + lr;
+                    float h = 0.0f, l = 0.0f;
+                    for (int src = 0; src < S; ++src) two_sum_acc(h, l, red[(src * TOK + m) * red_rows + lr]);
+                    if (n < args.N) {
+                        const float sa = sa_vec ? __ldg(args.scale_a + m) : sa0;
+                        const float sb = sb_vec ? __ldg(args.scale_b + n) : sb0;
+                        args.out[static_cast<int64_t>(m) * args.N + n] =
+                            __float2bfloat16_rn(__fmul_rn(__fmul_rn(__fadd_rn(h, l), sa), sb));
+                    }
+                }
+            }
+        }
+    }
+
     if (tid == 0) {
         // Loads issued but never consumed (only after a timeout): let them land
         // before the CTA exits.
@@ -437,18 +541,23 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
     }
 }
 
-template <int TOK, bool kBlk>
+template <int TOK, bool kBlk, bool kCluster>
 cudaError_t launch_tok(const CUtensorMap &tw, const CUtensorMap &ta, const DecodeArgs &a, const DecodePlan &p,
                        const LaunchOpts &o, cudaStream_t stream) {
-    static bool attr_done = false;  // benign race: the attribute call is idempotent
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<TOK, kBlk>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool attr_done[64] = {};  // benign race: the attribute call is idempotent
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(decode_gemm_kernel<TOK, kBlk, kCluster>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 200 * 1024);
         if (e != cudaSuccess) return e;
-        attr_done = true;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
-    return launch_with_opts(decode_gemm_kernel<TOK, kBlk>, dim3(static_cast<unsigned>(p.ctas)),
-                            dim3(DecodeCfg<TOK>::kThreads), p.smem_bytes, stream, o, tw, ta, a);
+    LaunchOpts oc = o;
+    oc.cluster_x = kCluster ? p.split : 1;
+    return launch_with_opts(decode_gemm_kernel<TOK, kBlk, kCluster>, dim3(static_cast<unsigned>(p.ctas)),
+                            dim3(DecodeCfg<TOK>::kThreads), p.smem_bytes, stream, oc, tw, ta, a);
 }
 
 }  // namespace
@@ -457,22 +566,45 @@ cudaError_t launch_tok(const CUtensorMap &tw, const CUtensorMap &ta, const Decod
 static int decode_tmem_bufs(int tok) { return tok <= 16 ? 8 : 4; }
 
 // Shared memory one CTA needs: the 1024-byte alignment slack, `stages` stages
-// of weights + tokens, and the mbarriers (full/empty per stage, full/empty per
-// TMEM accumulator, one final), rounded up.
-static size_t decode_smem_bytes(int tok, int stages) {
+// of weights + tokens, the mbarriers (full/empty per stage, full/empty per
+// TMEM accumulator, one final) rounded up to 128 bytes, and in cluster mode
+// (split > 1) the reduction area of S parts x tok tokens x ceil(128/S) rows.
+static size_t decode_smem_bytes(int tok, int stages, int split) {
     const size_t barriers = 8u * static_cast<size_t>(2 * stages + 2 * decode_tmem_bufs(tok) + 1);
-    return 1024 + static_cast<size_t>(stages) * (kDecodeRows * kBlockK + tok * kBlockK) + ((barriers + 127) / 128) * 128;
+    const size_t red = split > 1 ? 4u * static_cast<size_t>(split) * tok * ((kDecodeRows + split - 1) / split) : 0;
+    return 1024 + static_cast<size_t>(stages) * (kDecodeRows * kBlockK + tok * kBlockK) + ((barriers + 127) / 128) * 128 +
+           red;
 }
+
+// Cluster mode: S = (8 * SMs / 5) / tiles CTAs per tile (at least 1, at most
+// the tile's k-blocks), used when S <= kMaxClusterSplit; with fewer tiles (a
+// long K range over few channels) the persistent stream-K grid keeps every SM
+// streaming.  The grid is kept near 1.6 CTAs per SM because of how clusters
+// are placed: on the QKV shape (80 tiles) 3-CTA clusters (240 CTAs) took 13.7
+// us per launch and 4-CTA ones (320 CTAs) 22 us, the latter leaving SMs idle
+// and starting some clusters only after others had finished; on N 5120 (40
+// tiles) 6-CTA clusters took 12.0 us and 8-CTA ones 19.4 us.
+constexpr int kMaxClusterSplit = 8;
 
 DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, int num_sms) {
     DecodePlan p{};
-    p.tok_pad = 16;
+    p.tok_pad = M <= 16 ? 16 : 32;
     p.stages = 3;  // ~55-75 KB: two CTAs of this kernel and one of the next fit on an SM
-    p.smem_bytes = decode_smem_bytes(p.tok_pad, p.stages);
     p.n_tiles = static_cast<int>((N + kDecodeRows - 1) / kDecodeRows);
     p.m_tiles = static_cast<int>((M + p.tok_pad - 1) / p.tok_pad);
     p.kb_total = static_cast<int>((K + kBlockK - 1) / kBlockK);
     p.units = static_cast<int64_t>(p.n_tiles) * p.m_tiles * p.kb_total;
+    int64_t split = (8 * static_cast<int64_t>(num_sms) / 5) / p.n_tiles;
+    if (split < 1) split = 1;
+    if (split > p.kb_total) split = p.kb_total;
+    if (p.m_tiles == 1 && split <= kMaxClusterSplit) {
+        p.split = static_cast<int>(split);
+        p.ctas = static_cast<int>(static_cast<int64_t>(p.n_tiles) * split);
+        p.smem_bytes = decode_smem_bytes(p.tok_pad, p.stages, p.split);
+        return p;
+    }
+    p.split = 0;
+    p.smem_bytes = decode_smem_bytes(p.tok_pad, p.stages, 0);
     // Two persistent CTAs per SM, each with the same number of units (+-1),
     // and at least kb_total / (kMaxFixupSegs - 1) units each, so that no more
     // than kMaxFixupSegs CTAs share one tile.
@@ -484,10 +616,12 @@ DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, int num_sms) {
     return p;
 }
 
-size_t decode_counters_needed(const DecodePlan &p) { return static_cast<size_t>(p.n_tiles) * p.m_tiles; }
+size_t decode_counters_needed(const DecodePlan &p) {
+    return p.split > 0 ? 0 : static_cast<size_t>(p.n_tiles) * p.m_tiles;
+}
 
 size_t decode_slot_floats(const DecodePlan &p) {
-    return 2u * static_cast<size_t>(p.ctas) * static_cast<size_t>(p.tok_pad) * kDecodeRows;
+    return p.split > 0 ? 0 : 2u * static_cast<size_t>(p.ctas) * static_cast<size_t>(p.tok_pad) * kDecodeRows;
 }
 
 cudaError_t launch_decode_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_a, const float *scale_a,
@@ -510,8 +644,20 @@ cudaError_t launch_decode_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tma
     a.n_tiles = plan.n_tiles;
     a.stages = plan.stages;
     a.weights_static = opts.weights_static ? 1 : 0;
-    if (granularity == kGranBlock128) return launch_tok<16, true>(tmap_w, tmap_a, a, plan, opts, stream);
-    return launch_tok<16, false>(tmap_w, tmap_a, a, plan, opts, stream);
+    a.split = plan.split;
+    const bool blk = granularity == kGranBlock128;
+    if (plan.tok_pad == 32) {
+        if (plan.split > 0)
+            return blk ? launch_tok<32, true, true>(tmap_w, tmap_a, a, plan, opts, stream)
+                       : launch_tok<32, false, true>(tmap_w, tmap_a, a, plan, opts, stream);
+        return blk ? launch_tok<32, true, false>(tmap_w, tmap_a, a, plan, opts, stream)
+                   : launch_tok<32, false, false>(tmap_w, tmap_a, a, plan, opts, stream);
+    }
+    if (plan.split > 0)
+        return blk ? launch_tok<16, true, true>(tmap_w, tmap_a, a, plan, opts, stream)
+                   : launch_tok<16, false, true>(tmap_w, tmap_a, a, plan, opts, stream);
+    return blk ? launch_tok<16, true, false>(tmap_w, tmap_a, a, plan, opts, stream)
+               : launch_tok<16, false, false>(tmap_w, tmap_a, a, plan, opts, stream);
 }
 
 }  // namespace fp8k

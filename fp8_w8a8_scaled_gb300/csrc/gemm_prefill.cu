@@ -244,15 +244,32 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const bool live = (t % m_tiles) * kPrefillBM + static_cast<int>(quarter * 32u) < M;
             const int m_row = (t % m_tiles) * kPrefillBM + row;                  // this thread's token row
             const int n_col = (t / m_tiles) * BN + half * kCols;                 // its first channel
+            // Blockwise: the scales of k-block kb (sa of this row, sb of this
+            // column block) are requested two k-blocks ahead of their use, so
+            // that their latency hides behind the epilogue's work.
+            const float *const sa_row = args.scale_a + static_cast<int64_t>(m_row < M ? m_row : 0) * kbt;
+            const float *const sb_row = args.scale_b + static_cast<int64_t>(n_col < N ? n_col / 128 : 0) * kbt;
+            const bool sc_ok = kBlk && live && m_row < M && n_col < N;
+            // (a, b) pairs for k-blocks kb0 + 1 and kb0 + 2; the product is taken at the use
+            float pa1 = 0.0f, pb1 = 0.0f, pa2 = 0.0f, pb2 = 0.0f;
+            if (kBlk && sc_ok) {
+                pa1 = __ldg(sa_row);
+                pb1 = __ldg(sb_row);
+                if (kbt > 1) {
+                    pa2 = __ldg(sa_row + 1);
+                    pb2 = __ldg(sb_row + 1);
+                }
+            }
             for (int kb0 = 0; kb0 < kbt; kb0 += dkb, ++dc) {
                 const int acc = static_cast<int>(dc & 1u);
-                float bsc = 0.0f;  // blockwise: scale product of k-block kb0, requested before the wait
+                float bsc = 0.0f;  // blockwise: scale product of k-block kb0 (drain_kb == 1)
                 if constexpr (kBlk) {
-                    if (live) {
-                        const float a = m_row < M ? __ldg(args.scale_a + static_cast<int64_t>(m_row) * kbt + kb0) : 0.0f;
-                        const float b =
-                            n_col < N ? __ldg(args.scale_b + static_cast<int64_t>(n_col / 128) * kbt + kb0) : 0.0f;
-                        bsc = __fmul_rn(a, b);
+                    bsc = __fmul_rn(pa1, pb1);
+                    pa1 = pa2;
+                    pb1 = pb2;
+                    if (sc_ok && kb0 + 2 < kbt) {
+                        pa2 = __ldg(sa_row + kb0 + 2);
+                        pb2 = __ldg(sb_row + kb0 + 2);
                     }
                 }
                 if (!pf_warp_wait(tfull_bar(acc), (dc >> 1) & 1u, err, kErrPrefillAccumWait, &s_abort, lane)) {
@@ -263,18 +280,22 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 if (live) {
                 const uint32_t tbase = tmem + ((quarter * 32u) << 16) +
                                        static_cast<uint32_t>(acc * BN + half * kCols);
+                // 16-column chunks, the next one loading while the current one
+                // is added (paired FP32 instructions)
+                uint32_t v[2][16];
+                tmem_ld16(tbase, v[0]);
 #pragma unroll
-                for (int j = 0; j < kCols; j += 32) {
-                    uint32_t v[32];
-                    tmem_ld16(tbase + static_cast<uint32_t>(j), *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                    tmem_ld16(tbase + static_cast<uint32_t>(j + 16), *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                for (int j = 0; j < kCols; j += 16) {
+                    const int cur = (j / 16) & 1;
                     tmem_ld_wait();
+                    if (j + 16 < kCols) tmem_ld16(tbase + static_cast<uint32_t>(j + 16), v[cur ^ 1]);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
+                    for (int q = 0; q < 16; q += 2) {
+                        const float a0 = __uint_as_float(v[cur][q]), a1 = __uint_as_float(v[cur][q + 1]);
                         if constexpr (kBlk)
-                            y[j + q] = __fmaf_rn(__uint_as_float(v[q]), bsc, y[j + q]);
+                            fma2_rn(y[j + q], y[j + q + 1], a0, a1, bsc);
                         else
-                            y[j + q] = __fadd_rn(y[j + q], __uint_as_float(v[q]));
+                            add2_rn(y[j + q], y[j + q + 1], a0, a1);
                     }
                 }
                 }

@@ -87,16 +87,18 @@ cudaError_t launch_rmsnorm_quant(const void *x, const void *gamma, float eps, co
 constexpr int kGranBlock128 = 4;
 constexpr int kDecodeRows = 128;
 constexpr int kBlockK = 128;  // bytes (= E4M3 elements) of K per pipeline stage
-constexpr int kDecodeMaxTokens = 16;
+constexpr int kDecodeMaxTokens = 32;
 
 struct DecodePlan {
-    int tok_pad;      // tokens per tile on the MMA N side: 16
+    int tok_pad;      // tokens per tile on the MMA N side: 16 (M <= 16) or 32
     int stages;       // pipeline depth
     int n_tiles;      // ceil(N / 128)
     int m_tiles;      // ceil(M / tok_pad)
     int kb_total;     // ceil(K / 128)
     int64_t units;    // n_tiles * m_tiles * kb_total (one unit = one tile x one k-block)
-    int ctas;         // persistent CTAs; CTA c owns units [c*units/ctas, (c+1)*units/ctas)
+    int ctas;         // stream-K: persistent CTAs, CTA c owning units [c*units/ctas, (c+1)*units/ctas);
+                      // cluster mode: n_tiles * split
+    int split;        // cluster mode: CTAs (one cluster) per output tile; 0 = stream-K
     size_t smem_bytes;
 };
 
@@ -123,7 +125,7 @@ cudaError_t launch_decode_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tma
 // channels (MMA N) per tile, 128-byte k-blocks.
 constexpr int kPrefillBM = 128;
 constexpr int kPrefillBN = 256;
-constexpr int64_t kPrefillMinM = 17;  // fp8_scaled_mm sends M >= this to the prefill kernel
+constexpr int64_t kPrefillMinM = 33;  // fp8_scaled_mm sends M >= this to the prefill kernel
 
 struct PrefillPlan {
     int bn;  // output channels per tile: 256, or 128 for small M with few tiles

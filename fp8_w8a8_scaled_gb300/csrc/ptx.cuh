@@ -221,6 +221,30 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Two binary32 fused multiply-adds in one instruction (Blackwell's paired FP32
+// pipe): (y0, y1) = (a0 * s + y0, a1 * s + y1), each rounded once to nearest.
+__device__ __forceinline__ void fma2_rn(float &y0, float &y1, float a0, float a1, float s) {
+    asm("{\n\t.reg .b64 ra, rs, ry;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rs, {%4, %4};\n\t"
+        "mov.b64 ry, {%0, %1};\n\t"
+        "fma.rn.f32x2 ry, ra, rs, ry;\n\t"
+        "mov.b64 {%0, %1}, ry;\n\t}"
+        : "+f"(y0), "+f"(y1)
+        : "f"(a0), "f"(a1), "f"(s));
+}
+
+// (y0, y1) += (a0, a1), each add rounded once to nearest, in one instruction.
+__device__ __forceinline__ void add2_rn(float &y0, float &y1, float a0, float a1) {
+    asm("{\n\t.reg .b64 ra, ry;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 ry, {%0, %1};\n\t"
+        "add.rn.f32x2 ry, ry, ra;\n\t"
+        "mov.b64 {%0, %1}, ry;\n\t}"
+        : "+f"(y0), "+f"(y1)
+        : "f"(a0), "f"(a1));
+}
+
 // ------------------------------------------------------ compensated summation --
 
 // (hi, lo) += v with Knuth's TwoSum: hi + lo represents the running sum with
@@ -252,6 +276,18 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
+}
+
+// Cluster barrier halves: `arrive` (relaxed: orders nothing) and `wait`, for a
+// first barrier that only establishes that every CTA of the cluster is running.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+// Store one float to distributed shared memory (another CTA of the cluster).
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // Store to distributed shared memory (another CTA of the cluster).

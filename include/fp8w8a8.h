@@ -111,10 +111,12 @@ typedef enum {
  * tensor-core accumulation of the exact E4M3 products.  Which kernel runs is a
  * pure function of (M, N, K, granularity), see fp8_describe_dispatch, so a
  * captured CUDA graph replays the same kernel the eager call would run:
- * M <= 16 the weight-streaming decode kernel (uses the library's scratch
- * area), M >= 17 the tensor-core tile kernel (uses no scratch).  For a fixed
- * M the result is deterministic (bitwise the same on every run); on the tile
- * kernel row m does not depend on the other rows of A.
+ * M <= 32 the weight-streaming decode kernel (16-token tile for M <= 16,
+ * 32-token tile above; its stream-K mode uses the library's scratch area),
+ * M >= 33 the tensor-core tile kernel (uses no scratch).  For a fixed M the
+ * result is deterministic (bitwise the same on every run); on the tile kernel
+ * row m does not depend on the other rows of A, and on the decode kernel
+ * neither within one token tile size (M <= 16, or 17 <= M <= 32).
  * Errors: FP8_ERR_INVALID_ARG, FP8_ERR_ALIGNMENT, FP8_ERR_UNSUPPORTED,
  * FP8_ERR_CUDA. */
 fp8_status fp8_scaled_mm(const void *A, const void *B, const float *scale_a, const float *scale_b,
@@ -345,20 +347,31 @@ const char *fp8_status_string(int status);
 /* Which kernel fp8_scaled_mm runs for this problem (an fp8_kernel_id), or -1
  * for arguments fp8_scaled_mm would reject.  Host-only, pure: it reads no
  * device state, so a caller can assert the kernel before capturing a graph.
- * FP8_KERNEL_DECODE_SPLITK for 1 <= M <= 16, FP8_KERNEL_PREFILL for M >= 17.
+ * FP8_KERNEL_DECODE_SPLITK for 1 <= M <= 32, FP8_KERNEL_PREFILL for M >= 33.
  * Source: [P4] commit message: the M-vs-threshold branch is a pure function
  * of M so that a graph captured at a padded M freezes the branch eager
  * execution would take. */
 int fp8_describe_dispatch(int64_t M, int64_t N, int64_t K, int granularity);
 
-/* Number of persistent CTAs the decode kernel launches for this shape on the
- * current device (the K ranges of all output tiles are divided evenly among
- * them), or -1 if the shape does not go to the decode kernel.  Host-only. */
+/* Number of CTAs the decode kernel launches for this shape on the current
+ * device, or -1 if the shape does not go to the decode kernel.  Host-only.
+ * The decode kernel runs in one of two modes (see fp8_decode_split_for_sms):
+ * clusters of S CTAs per 128-channel output tile, each CTA taking 1/S of the
+ * tile's K range (ctas = ceil(N/128) * S), or a persistent grid over which the
+ * K ranges of all tiles are divided evenly (stream-K). */
 int fp8_decode_ctas(int64_t M, int64_t N, int64_t K);
 
 /* The same for a device with `num_sms` streaming multiprocessors; pure and
  * host-only (usable without a GPU). */
 int fp8_decode_ctas_for_sms(int64_t M, int64_t N, int64_t K, int num_sms);
+
+/* The decode kernel's mode for this shape on a device with `num_sms` SMs: S >=
+ * 1 for clusters of S CTAs per output tile (S = 1: whole tiles, nothing to
+ * sum), 0 for the persistent stream-K grid, -1 if the shape does not go to the
+ * decode kernel.  With tiles = ceil(N/128), S = floor(floor(8 * num_sms / 5) /
+ * tiles), at least 1 and at most ceil(K/128); clusters when S <= 8, stream-K
+ * otherwise.  Pure and host-only. */
+int fp8_decode_split_for_sms(int64_t M, int64_t N, int64_t K, int num_sms);
 
 /* Device error word.  Kernels never trap: a bounded wait that runs out sets a
  * bit here and the kernel finishes without waiting further (its outputs are

@@ -196,11 +196,11 @@ def test_describe_dispatch_is_pure(L):
     assert L.fp8_describe_dispatch(-1, 64, 64, 0) == -1
     assert L.fp8_describe_dispatch(4, 64, 64, 7) == -1
     assert L.fp8_describe_dispatch(4, 64, 64, 5) == -1
-    assert L.fp8_describe_dispatch(16, 10240, 5120, 4) == 1        # blockwise: same split as the others
-    assert L.fp8_describe_dispatch(17, 10240, 5120, 4) == 2
-    for M in (1, 2, 4, 8, 16):
+    assert L.fp8_describe_dispatch(32, 10240, 5120, 4) == 1        # blockwise: same split as the others
+    assert L.fp8_describe_dispatch(33, 10240, 5120, 4) == 2
+    for M in (1, 2, 4, 8, 16, 17, 24, 32):
         assert L.fp8_describe_dispatch(M, 10240, 5120, 1) == 1
-    for M in (17, 32, 33, 64, 65, 128, 2048, 8192):
+    for M in (33, 64, 65, 128, 2048, 8192):
         assert L.fp8_describe_dispatch(M, 10240, 5120, 1) == 2
         assert L.fp8_describe_dispatch(M, 34816, 5120, 2) == 2
     # the same question twice gives the same answer (no hidden state)
@@ -209,17 +209,29 @@ def test_describe_dispatch_is_pure(L):
 
 
 def test_decode_planner(L):
-    """Two persistent CTAs per SM (never more CTAs than units of one tile x
-    one 128-wide k-block)."""
+    """Cluster mode (S = floor(floor(8 * SMs / 5) / tiles) CTAs per
+    128-channel tile, at least 1, at most the tile's k-blocks) when S <= 8;
+    else two persistent CTAs per SM (stream-K; never more CTAs than units of
+    one tile x one 128-wide k-block, and at most 8 CTAs per tile)."""
     f = L.fp8_decode_ctas_for_sms
-    for (M, N, K) in ((1, 10240, 5120), (16, 10240, 5120), (16, 34816, 5120)):
-        assert f(M, N, K, 152) == 304
-    assert f(8, 5120, 8192, 152) == 40 * 64 // 10       # >= 10 k-blocks per CTA (64 per tile)
-    assert f(8, 5120, 17408, 152) == 40 * 136 // 20
-    assert f(4, 512, 256, 152) == 4 * 2          # 4 tiles x 2 k-blocks
-    assert f(1, 8, 16, 152) == 1                 # one unit
-    # a single tile with a long K range is shared by at most 8 CTAs
-    assert f(1, 128, 5120, 152) == 40 // 6       # at least ceil(40/7) = 6 k-blocks per CTA
-    assert f(1, 8, 65536, 152) == 512 // 74
-    assert f(0, 8, 16, 152) == -1
+    sp = L.fp8_decode_split_for_sms
+    # cluster mode (243 CTAs' worth of tiles on 152 SMs)
+    for M in (1, 16):
+        assert sp(M, 10240, 5120, 152) == 3 and f(M, 10240, 5120, 152) == 80 * 3
+    assert sp(16, 34816, 5120, 152) == 1 and f(16, 34816, 5120, 152) == 272    # whole tiles, no reduction
+    assert sp(8, 5120, 8192, 152) == 6 and f(8, 5120, 8192, 152) == 40 * 6
+    assert sp(8, 5120, 17408, 152) == 6
+    assert sp(1, 8192, 5120, 152) == 3 and sp(1, 7168, 5120, 152) == 4 and sp(1, 6144, 5120, 152) == 5
+    assert sp(1, 4096, 5120, 152) == 7 and sp(1, 3840, 5120, 152) == 8 and sp(1, 3456, 5120, 152) == 0
+    assert sp(1, 10240, 256, 152) == 2                      # capped at the 2 k-blocks of K
+    assert sp(4, 512, 256, 152) == 2 and f(4, 512, 256, 152) == 4 * 2
+    assert sp(1, 8, 16, 152) == 1 and f(1, 8, 16, 152) == 1  # one unit
+    # stream-K: few tiles with long K ranges
+    assert sp(1, 128, 5120, 152) == 0
+    assert f(1, 128, 5120, 152) == 40 // 6                   # at least ceil(40/7) = 6 k-blocks per CTA
+    assert sp(1, 8, 65536, 152) == 0 and f(1, 8, 65536, 152) == 512 // 74
+    assert sp(16, 2048, 5120, 152) == 0 and f(16, 2048, 5120, 152) == 16 * 40 // 6
+    assert sp(5, 1032, 5120, 152) == 0
+    assert f(0, 8, 16, 152) == -1 and sp(0, 8, 16, 152) == -1 and sp(33, 10240, 5120, 152) == -1
+    assert sp(32, 10240, 5120, 152) == 3 and f(17, 10240, 5120, 152) == 240   # the 32-token tile, same plan
     assert f(32, 10240, 5120, 152) == f(32, 10240, 5120, 152)

@@ -1,6 +1,6 @@
 """GPU parity of blockwise FP8 scaling (128 x 128 weight blocks, 128-wide token
 groups) against the CPU oracle: the two quantisers byte-exact, and the GEMM
-with FP8_GRAN_BLOCK_128 on both kernels (decode M <= 16, tile M >= 17) within
+with FP8_GRAN_BLOCK_128 on both kernels (decode M <= 32, tile M >= 33) within
 the acceptance bound, every output of the small cases and sampled outputs of
 the workload-sized ones."""
 import numpy as np
@@ -140,13 +140,13 @@ def test_quantisers_empty(fp8):
 # ------------------------------------------------------------------ GEMM, random codes
 
 SHAPES = [(1, 136, 400), (3, 8, 16), (5, 1032, 5120), (16, 264, 272), (16, 128, 128),
-          (17, 264, 400), (33, 1000, 272), (129, 520, 1040), (200, 8, 4096), (300, 1032, 2064)]
+          (17, 264, 400), (32, 10240, 1040), (33, 1000, 272), (129, 520, 1040), (200, 8, 4096), (300, 1032, 2064)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_block_gemm_random_codes(fp8, orc, M, N, K):
     c = workloads.random_gemm(8000 + M * 7 + N * 3 + K, M, N, K, GRAN_BLOCK)
-    want = fp8.KERNEL_DECODE_SPLITK if M <= 16 else fp8.KERNEL_PREFILL
+    want = fp8.KERNEL_DECODE_SPLITK if M <= 32 else fp8.KERNEL_PREFILL
     assert fp8.describe_dispatch(M, N, K, GRAN_BLOCK) == want
     y = run_block_mm(fp8, to_dev_e4m3(c["A"]), to_dev_e4m3(c["B"]), dev_scales(c["sa"]), dev_scales(c["sb"]))
     block_check(orc, c["A"], c["B"], c["sa"], c["sb"], y, f"{M}x{N}x{K} blockwise")
@@ -161,7 +161,7 @@ def test_block_gemm_scales_select_blocks(fp8, orc):
     sb = np.zeros((3, 4), np.float32)
     sa[2, 1] = 0.5
     sb[1, 1] = 0.25
-    for m_rows in (M, 40):  # decode kernel, then tile kernel
+    for m_rows in (M, 24, 40):  # decode kernel (16- and 32-token tiles), then tile kernel
         A = np.resize(c["A"], (m_rows, K))
         sam = np.zeros((m_rows, 4), np.float32)
         sam[2, 1] = 0.5
@@ -201,7 +201,7 @@ def quantised_block_operands(fp8, orc, M, N, K, seed):
     return qa, qb, sa, sb, wa, wb, wsa, wsb
 
 
-@pytest.mark.parametrize("M", [1, 8, 16])
+@pytest.mark.parametrize("M", [1, 8, 16, 32])
 def test_block_qkv_decode(fp8, orc, M):
     """Merged QKV (N 10240, K 5120) at decode M, every output."""
     qa, qb, sa, sb, wa, wb, wsa, wsb = quantised_block_operands(fp8, orc, M, 10240, 5120, 8300 + M)

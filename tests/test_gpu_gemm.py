@@ -32,9 +32,11 @@ def run_mm(fp8, A, B, sa, sb, gran):
 
 
 def full_check(orc, A_codes, B_codes, sa, sb, gran, y_bits, what, tc_bound=False):
-    """Every output against the oracle.  With tc_bound (stress inputs on the
-    large-M kernel) the binary32 accumulation bound is added to the acceptance
-    bound; the ratio to the acceptance bound alone is still reported."""
+    """Every output against the oracle.  With tc_bound (stress inputs:
+    uniformly random codes, or outlier-free data on the large-M kernel's long
+    accumulation groups) the binary32 accumulation bound is added to the
+    acceptance bound; the ratio to the acceptance bound alone is still
+    reported."""
     y64, _ = orc.scaled_mm(A_codes, B_codes, sa, sb, gran)
     M, N = y64.shape
     rows = np.arange(M)[:, None]
@@ -82,7 +84,7 @@ def test_decode_fused_qkv(fp8, decode_fused_case, M):
     s_a = to_dev_f32(d["s_a"])
     A = fp8.rmsnorm_quant_fp8(to_dev_bf16(d["x"][:M]), to_dev_bf16(d["gamma"]), d["eps"], s_a)
     assert np.array_equal(host_bits(A), A_all[:M])
-    want = fp8.KERNEL_DECODE_SPLITK if M <= 16 else fp8.KERNEL_PREFILL
+    want = fp8.KERNEL_DECODE_SPLITK if M <= 32 else fp8.KERNEL_PREFILL
     assert fp8.describe_dispatch(M, 10240, 5120, 1) == want
     y = run_mm(fp8, A, to_dev_e4m3(d["B"]), s_a, to_dev_f32(d["sb"]), 1)
     sab = scale_product(d["s_a"], d["sb"], 1, np.arange(M)[:, None], np.arange(10240)[None, :])
@@ -140,6 +142,37 @@ def test_down_projection_long_k(fp8, orc):
     print(f"down max err/bound {worst:.4f}")
 
 
+# ----------------------------------------------------------------------------- decode modes
+
+# (M, N, K, S): the decode kernel's mode for the shape on a 152-SM GB300 --
+# clusters of S CTAs per 128-channel tile (every S from 1 to 8, rows split
+# unevenly among the S CTAs for S = 3, 5, 6, 7; a ragged last tile; K ranges
+# split unevenly), or 0 for the persistent stream-K grid.
+DECODE_MODES = [(1, 34816, 1040, 1), (16, 10240, 256, 2), (3, 13312, 2064, 2), (16, 10232, 5136, 3),
+                (7, 8192, 1552, 3), (2, 7168, 4096, 4), (16, 6144, 1040, 5), (5, 5120, 8192, 6),
+                (4, 4096, 2064, 7), (11, 3840, 1552, 8),
+                (1, 128, 5120, 0), (16, 2048, 5120, 0), (9, 1032, 17408, 0),
+                # the 32-token tile (17 <= M <= 32)
+                (32, 10240, 5120, 3), (24, 34816, 1040, 1), (17, 5120, 8192, 6), (32, 2048, 5120, 0),
+                (20, 1032, 4096, 0)]
+
+
+@pytest.mark.parametrize("M,N,K,S", DECODE_MODES)
+def test_decode_modes(fp8, orc, M, N, K, S):
+    """Every output of both decode modes against the oracle, per-token x
+    per-channel scales.  Uniformly random codes are stress inputs: their
+    128-wide k-block sums are large next to the acceptance bound's absolute
+    term, and the tensor core's binary32 accumulation inside a k-block is
+    allowed its own bound (as on the tile kernel)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms == 152:
+        assert fp8.decode_split(M, N, K, sms) == S
+    c = workloads.random_gemm(7000 + M + N + K, M, N, K, 2)
+    y = run_mm(fp8, to_dev_e4m3(c["A"]), to_dev_e4m3(c["B"]), to_dev_f32(c["sa"]), to_dev_f32(c["sb"]), 2)
+    worst, _ = full_check(orc, c["A"], c["B"], c["sa"], c["sb"], 2, y, f"{M}x{N}x{K} split {S}", tc_bound=True)
+    print(f"{M}x{N}x{K} split {fp8.decode_split(M, N, K)}: max err/bound {worst:.4f}")
+
+
 # ----------------------------------------------------------------------------- ragged shapes
 
 # Uniformly random E4M3 codes: every code value, with a heavier magnitude tail
@@ -153,8 +186,7 @@ SHAPES_CODES = [(1, 8, 16), (3, 136, 48), (17, 264, 400), (33, 1000, 272), (65, 
 def test_random_codes(fp8, orc, M, N, K, gran):
     c = workloads.random_gemm(1000 + M * 7 + N * 3 + K + gran, M, N, K, gran)
     y = run_mm(fp8, to_dev_e4m3(c["A"]), to_dev_e4m3(c["B"]), to_dev_f32(c["sa"]), to_dev_f32(c["sb"]), gran)
-    full_check(orc, c["A"], c["B"], c["sa"], c["sb"], gran, y, f"{M}x{N}x{K} gran {gran}",
-               tc_bound=fp8.describe_dispatch(M, N, K, gran) == fp8.KERNEL_PREFILL)
+    full_check(orc, c["A"], c["B"], c["sa"], c["sb"], gran, y, f"{M}x{N}x{K} gran {gran}", tc_bound=True)
 
 
 def quantised_operands(fp8, orc, M, N, K, gran, seed):

@@ -27,7 +27,7 @@ def fp8():
 
 # (M, N, K): ragged M (not a multiple of 128), ragged N (not a multiple of 256,
 # and N % 16 == 8 for a half 16-column chunk), ragged K (not a multiple of 128).
-SHAPES = [(17, 136, 272), (33, 136, 272), (65, 264, 400), (128, 256, 128), (300, 776, 1040), (257, 1288, 2064), (1000, 520, 5120)]
+SHAPES = [(40, 136, 272), (33, 136, 272), (65, 264, 400), (128, 256, 128), (300, 776, 1040), (257, 1288, 2064), (1000, 520, 5120)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -56,16 +56,16 @@ def test_prefill_more_tiles_than_sms(fp8, orc):
     full_check(orc, wa, wb, wsa, wsb, 2, y, "1024x8192x1024", tc_bound=True)
 
 
-@pytest.mark.parametrize("M", [16, 17])
+@pytest.mark.parametrize("M", [16, 17, 32, 33])
 def test_dispatch_boundary(fp8, orc, M):
-    """The last decode M and the first prefill M give results within the bound
-    on the same operands."""
+    """The token tiles' boundary (16 / 17) and the last decode M and the first
+    prefill M (32 / 33) give results within the bound on the same operands."""
     N, K = 1032, 2064
-    want = fp8.KERNEL_DECODE_SPLITK if M <= 16 else fp8.KERNEL_PREFILL
+    want = fp8.KERNEL_DECODE_SPLITK if M <= 32 else fp8.KERNEL_PREFILL
     assert fp8.describe_dispatch(M, N, K, 2) == want
     qa, qb, sa, sb, wa, wb, wsa, wsb = quantised_operands(fp8, orc, M, N, K, 2, 5300)
     y = run_mm(fp8, qa, qb, sa, sb, 2)
-    full_check(orc, wa, wb, wsa, wsb, 2, y, f"boundary M={M}", tc_bound=M > 16)
+    full_check(orc, wa, wb, wsa, wsb, 2, y, f"boundary M={M}", tc_bound=M > 32)
 
 
 @pytest.mark.parametrize("M,N", [(1000, 1288), (257, 10240)])
