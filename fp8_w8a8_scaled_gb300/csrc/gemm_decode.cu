@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
     __shared__ int s_nseg[2];
     __shared__ volatile uint32_t s_abort;
     __shared__ float s_bscale[kBlk ? NB : 1][TOK];  // blockwise: scale products per accumulator
+    __shared__ float s_red_sa[kCluster ? TOK : 1], s_red_sb[kCluster ? kDecodeRows : 1];  // cluster-mode scales
 
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int stages = args.stages;
@@ -499,29 +500,33 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
 
     if constexpr (kCluster) {
         if (S > 1) {
+            const int tile = static_cast<int>(me / S);
+            const int rb = red_row_begin(c_rank, S), nr = red_row_begin(c_rank + 1, S) - rb;
+            const int mt = min(TOK, args.M);
+            if (warp >= 2) {
+                // the scales of this CTA's rows and of the tokens, staged in
+                // shared memory while the other CTAs of the cluster finish
+                const int dt = static_cast<int>(tid) - 64;
+                const bool sa_vec = !kBlk && (args.gran == 2 || args.gran == 3);
+                const bool sb_vec = !kBlk && (args.gran == 1 || args.gran == 2);
+                if (dt < mt) s_red_sa[dt] = kBlk ? 1.0f : __ldg(args.scale_a + (sa_vec ? dt : 0));
+                const int n = tile * kDecodeRows + rb + dt;
+                if (dt < nr) s_red_sb[dt] = kBlk ? 1.0f : __ldg(args.scale_b + (sb_vec && n < args.N ? n : 0));
+            }
             if (warp < 2) cluster_wait();  // the other warps' half of the first cluster barrier
             // every part of every row this CTA sums has landed (and no CTA of
             // the cluster touches another's shared memory after this point)
             cluster_sync();
             if (warp >= 2) {
-                const int tile = static_cast<int>(me / S);
-                const int rb = red_row_begin(c_rank, S), nr = red_row_begin(c_rank + 1, S) - rb;
-                const int mt = min(TOK, args.M);
-                const bool sa_vec = !kBlk && (args.gran == 2 || args.gran == 3);
-                const bool sb_vec = !kBlk && (args.gran == 1 || args.gran == 2);
-                const float sa0 = kBlk ? 1.0f : __ldg(args.scale_a), sb0 = kBlk ? 1.0f : __ldg(args.scale_b);
                 const float *red = reinterpret_cast<const float *>(smem_raw + (red_base - raw));
                 for (int e = static_cast<int>(tid) - 64; e < nr * mt; e += Cfg::kDrainThreads) {
                     const int m = e / nr, lr = e - m * nr;  // consecutive threads: consecutive channels
                     const int n = tile * kDecodeRows + rb + lr;
                     float h = 0.0f, l = 0.0f;
                     for (int src = 0; src < S; ++src) two_sum_acc(h, l, red[(src * TOK + m) * red_rows + lr]);
-                    if (n < args.N) {
-                        const float sa = sa_vec ? __ldg(args.scale_a + m) : sa0;
-                        const float sb = sb_vec ? __ldg(args.scale_b + n) : sb0;
+                    if (n < args.N)
                         args.out[static_cast<int64_t>(m) * args.N + n] =
-                            __float2bfloat16_rn(__fmul_rn(__fmul_rn(__fadd_rn(h, l), sa), sb));
-                    }
+                            __float2bfloat16_rn(__fmul_rn(__fmul_rn(__fadd_rn(h, l), s_red_sa[m]), s_red_sb[lr]));
                 }
             }
         }

@@ -95,45 +95,37 @@ struct Group {
     int ti, T;
 };
 
+// Sum of a 128-bit value and OR of a flag over the group (one pair of
+// barriers for both).
 template <class Sync>
-__device__ __forceinline__ int group_max_int(int v, const Group g, RowScratch *sc, Sync sync) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    const int warp = g.ti >> 5, lane = g.ti & 31;
-    sync();
-    if (lane == 0) sc->red_i[warp] = v;
-    sync();
-    v = lane < (g.T >> 5) ? sc->red_i[lane] : 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    return v;
-}
-
-template <class Sync>
-__device__ __forceinline__ U128 group_sum_u128(U128 v, const Group g, RowScratch *sc, Sync sync) {
+__device__ __forceinline__ U128 group_sum_u128_or(U128 v, int &flag, const Group g, RowScratch *sc, Sync sync) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         U128 w;
         w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
         w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
         v = add128(v, w);
+        flag |= __shfl_xor_sync(0xFFFFFFFFu, flag, o);
     }
     const int warp = g.ti >> 5, lane = g.ti & 31;
     sync();
     if (lane == 0) {
         sc->red_hi[warp] = v.hi;
         sc->red_lo[warp] = v.lo;
+        sc->red_i[warp] = flag;
     }
     sync();
     const int nw = g.T >> 5;
     v.hi = lane < nw ? sc->red_hi[lane] : 0;
     v.lo = lane < nw ? sc->red_lo[lane] : 0;
+    flag = lane < nw ? sc->red_i[lane] : 0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         U128 w;
         w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
         w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
         v = add128(v, w);
+        flag |= __shfl_xor_sync(0xFFFFFFFFu, flag, o);
     }
     return v;
 }
@@ -292,8 +284,7 @@ __device__ __forceinline__ void rmsnorm_quant_row(const uint4 *__restrict__ xr, 
     // a0 + a1 * 2^32 + a2 * 2^64 as one 128-bit number
     U128 acc = {a2, a0};
     acc = add128(acc, U128{a1 >> 32, a1 << 32});
-    acc = group_sum_u128(acc, g, sc, sync);
-    sticky = group_max_int(sticky, g, sc, sync);
+    acc = group_sum_u128_or(acc, sticky, g, sc, sync);
     if (g.ti == 0) {
         const float ss = round_sum_to_f32(acc, elo, sticky, special);
         const float mean = __fdiv_rn(ss, static_cast<float>(K));
