@@ -67,6 +67,9 @@ def _load():
     lib.oracle_quant_per_token_group.argtypes = [P, I64, I64, P, P]
     lib.oracle_quant_weight_block.argtypes = [P, I64, I64, P, P]
     lib.oracle_scaled_mm_block_points.argtypes = [P, P, P, P, I64, I64, I64, P, P, I64, P]
+    lib.oracle_w8a16_mm.argtypes = [P, P, P, ctypes.c_int, I64, I64, I64, P, P, ctypes.c_int]
+    lib.oracle_w8a16_points.argtypes = [P, P, P, ctypes.c_int, I64, P, P, I64, P]
+    lib.oracle_dequant_weight_bf16.argtypes = [P, P, ctypes.c_int, I64, I64, P]
     lib.oracle_has_nan_code.argtypes = [P, I64]
     lib.oracle_has_nan_code.restype = ctypes.c_int
     _lib = lib
@@ -335,6 +338,44 @@ def scaled_mm_points(A, B, sa, sb, gran: int, rows, cols) -> np.ndarray:
     _load().oracle_scaled_mm_points(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), gran, M, N, K, _ptr(rows),
                                     _ptr(cols), rows.size, _ptr(y))
     return y
+
+
+def w8a16_mm(x_bf16, W, sb, per_channel: bool, nthreads=None):
+    """Weight-only FP8 GEMM: (y64 float64 [M,N], y_bf16 uint16 [M,N]) for bf16
+    x [M,K], E4M3 codes W [N,K], scales sb [N] (per channel) or [1]."""
+    x = _c(x_bf16, np.uint16)
+    W = _c(W, np.uint8)
+    sb = _c(np.atleast_1d(sb), np.float32)
+    M, K = x.shape
+    N = W.shape[0]
+    y64 = np.empty((M, N), np.float64)
+    yb = np.empty((M, N), np.uint16)
+    _load().oracle_w8a16_mm(_ptr(x), _ptr(W), _ptr(sb), int(bool(per_channel)), M, N, K, _ptr(y64), _ptr(yb),
+                            nthreads or default_threads())
+    return y64, yb
+
+
+def w8a16_points(x_bf16, W, sb, per_channel: bool, rows, cols) -> np.ndarray:
+    """The weight-only GEMM at the (rows[i], cols[i]) outputs."""
+    x = _c(x_bf16, np.uint16)
+    W = _c(W, np.uint8)
+    sb = _c(np.atleast_1d(sb), np.float32)
+    rows = _c(rows, np.int64)
+    cols = _c(cols, np.int64)
+    y = np.empty(rows.shape, np.float64)
+    _load().oracle_w8a16_points(_ptr(x), _ptr(W), _ptr(sb), int(bool(per_channel)), x.shape[1], _ptr(rows),
+                                _ptr(cols), rows.size, _ptr(y))
+    return y
+
+
+def dequant_weight_bf16(W, sb, per_channel: bool) -> np.ndarray:
+    """The large-M branch's bf16 weight: bf16_rne(fp32(dec(W) * sb)), uint16 [N,K]."""
+    W = _c(W, np.uint8)
+    sb = _c(np.atleast_1d(sb), np.float32)
+    N, K = W.shape
+    out = np.empty((N, K), np.uint16)
+    _load().oracle_dequant_weight_bf16(_ptr(W), _ptr(sb), int(bool(per_channel)), N, K, _ptr(out))
+    return out
 
 
 def has_nan_code(codes) -> bool:

@@ -662,6 +662,90 @@ void oracle_scaled_mm_block_points(const uint8_t *A, const uint8_t *B, const flo
     }
 }
 
+/* ------------------------------------------------------------------------- */
+/* Weight-only FP8 (W8A16, reading R22): bf16 activations, E4M3 weights with  */
+/* a per-tensor or per-output-channel binary32 scale, bf16 output:            */
+/*   y[m,n] = ( sum_k x[m,k] * dec(W[n,k]) ) * sb[n]                          */
+/* ([P4] "[Kernel] add Flashinfer cutedsl w4a16 linear": the FP8 channelwise  */
+/* weight-only half -- E4M3 weights, 16-bit activations -- and its large-M     */
+/* branch that dequantises the weight to 16 bits for a dense 16-bit GEMM.)    */
+/* A product of a bf16 value (8 significant bits) and an E4M3 value (4) has   */
+/* at most 12 significant bits and is exact in binary64; the products are    */
+/* summed in binary64 in k order (error at most K * 2^-53 * sum |x w|, far     */
+/* below the acceptance bound), the sum is multiplied by the scale in binary64 */
+/* and rounded to bf16.                                                        */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    const uint16_t *x;
+    const uint8_t *W;
+    const float *sb;
+    int per_channel;
+    int64_t M, N, K;
+    double *y64;
+    uint16_t *ybf;
+    int tid, nthreads;
+} w8a16_job;
+
+static double w8a16_dot(const uint16_t *xr, const uint8_t *wr, int64_t K) {
+    double s = 0.0;
+    for (int64_t k = 0; k < K; ++k) s += (double)oracle_bf16_to_f32(xr[k]) * g_lut[wr[k]];
+    return s;
+}
+
+static void *w8a16_worker(void *p) {
+    w8a16_job *j = (w8a16_job *)p;
+    const int64_t n0 = j->N * j->tid / j->nthreads, n1 = j->N * (j->tid + 1) / j->nthreads;
+    for (int64_t m = 0; m < j->M; ++m)
+        for (int64_t n = n0; n < n1; ++n) {
+            const double y = w8a16_dot(j->x + m * j->K, j->W + n * j->K, j->K) *
+                             (double)(j->per_channel ? j->sb[n] : j->sb[0]);
+            if (j->y64) j->y64[m * j->N + n] = y;
+            if (j->ybf) j->ybf[m * j->N + n] = oracle_bf16_rne_f64(y);
+        }
+    return NULL;
+}
+
+/* y64 / y_bf16 [M,N] (either may be NULL); x bf16 [M,K], W codes [N,K]. */
+void oracle_w8a16_mm(const uint16_t *x, const uint8_t *W, const float *sb, int per_channel, int64_t M, int64_t N,
+                     int64_t K, double *y64, uint16_t *y_bf16, int nthreads) {
+    pthread_once(&g_lut_once, build_lut);
+    if (nthreads < 1) nthreads = 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    w8a16_job *jobs = (w8a16_job *)malloc(sizeof(w8a16_job) * (size_t)nthreads);
+    for (int t = 0; t < nthreads; ++t) {
+        w8a16_job jb = {x, W, sb, per_channel, M, N, K, y64, y_bf16, t, nthreads};
+        jobs[t] = jb;
+        pthread_create(&th[t], NULL, w8a16_worker, &jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    free(th);
+    free(jobs);
+}
+
+/* The same definition at the listed (row, col) pairs. */
+void oracle_w8a16_points(const uint16_t *x, const uint8_t *W, const float *sb, int per_channel, int64_t K,
+                         const int64_t *rows, const int64_t *cols, int64_t npts, double *y64) {
+    pthread_once(&g_lut_once, build_lut);
+    for (int64_t i = 0; i < npts; ++i)
+        y64[i] = w8a16_dot(x + rows[i] * K, W + cols[i] * K, K) * (double)(per_channel ? sb[cols[i]] : sb[0]);
+}
+
+/* The large-M branch's 16-bit weight: w16[n,k] = bf16_rne( fp32(dec(W) * sb) ),
+ * one binary32 multiply (dec(W) is exact in binary32) rounded to nearest, then
+ * rounded to bf16 (R22). */
+void oracle_dequant_weight_bf16(const uint8_t *W, const float *sb, int per_channel, int64_t N, int64_t K,
+                                uint16_t *out) {
+    pthread_once(&g_lut_once, build_lut);
+    for (int64_t n = 0; n < N; ++n) {
+        const float s = per_channel ? sb[n] : sb[0];
+        for (int64_t k = 0; k < K; ++k) {
+            volatile float v = (float)g_lut[W[n * K + k]] * s;
+            out[n * K + k] = oracle_bf16_rne_f32(v);
+        }
+    }
+}
+
 int oracle_has_nan_code(const uint8_t *codes, int64_t n) {
     pthread_once(&g_lut_once, build_lut);
     for (int64_t i = 0; i < n; ++i)
