@@ -383,6 +383,54 @@ def run_gate_up(torch, fp8, device, dist_barrier, dist_max, reps=40):
             "peak": peak, "per_M": rows, "gpu_launches": launches}
 
 
+def run_w8a16(torch, fp8, device, dist_barrier, dist_max, reps=40):
+    """Weight-only FP8 GEMM on the merged QKV shape (N 10240, K 5120, bf16
+    activations, per-channel weight scales): the widen-on-chip decode kernel at
+    M in {1, 8, 16, 32} (weight bytes per launch / time, against the HBM peak;
+    20 launches per graph over eight 52.4 MB weights) and the large-M branch
+    (widen + dense bf16 GEMM + scale) at M 2048 in TFLOP/s."""
+    N, K = N_QKV, K_HID
+    W = [workloads.device_e4m3_codes(torch, (N, K), seed=900 + i, device=device).view(torch.float8_e4m3fn)
+         for i in range(8)]
+    sb = workloads.device_uniform_f32(torch, (N,), 0.5e-3, 2e-3, seed=908, device=device)
+    peak, _ = measured_peaks()
+    rows, launches = [], 0
+    for M in (1, 8, 16, 32):
+        x = workloads.device_bf16_normal(torch, (M, K), seed=909, device=device)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        g = graph_of(torch, device, lambda i: fp8.w8a16_mm(x, W[i % 8], sb, fp8.GRAN_PER_CHANNEL, out=Y,
+                                                          flags=fp8.FLAG_WEIGHTS_STATIC), 20)
+        for _ in range(3):
+            g.replay()
+        us = dist_max(time_graph(torch, g, reps, dist_barrier)) * 1e3 / (20 * reps)
+        launches += 20 * reps
+        b = N * K + 2 * M * K + 2 * M * N + 4 * N
+        gbps = b / (us * 1e-6) / 1e9
+        rows.append({"M": M, "us": round(us, 3), "GBps": round(gbps, 1), "frac": round(gbps / peak, 4)})
+    M = 2048
+    x = workloads.device_bf16_normal(torch, (M, K), seed=910, device=device)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    # eager launches (the branch calls cuBLAS): each call is ~100 us of GPU
+    # work, far above the host's enqueue time, so the events time the GPU
+    for i in range(3):
+        fp8.w8a16_mm(x, W[i % 8], sb, fp8.GRAN_PER_CHANNEL, out=Y)
+    torch.cuda.synchronize(device)
+    dist_barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(40):
+        fp8.w8a16_mm(x, W[i % 8], sb, fp8.GRAN_PER_CHANNEL, out=Y)
+    e1.record()
+    torch.cuda.synchronize(device)
+    us = dist_max(e0.elapsed_time(e1)) * 1e3 / 40
+    dense = {"M": M, "us": round(us, 2), "tflops": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1),
+             "path": "widen (E4M3 -> bf16, exact) + cuBLAS bf16 GEMM + per-channel scale"}
+    del W
+    return {"workload": "weight-only FP8 (W8A16) merged QKV N=10240 K=5120, bf16 activations, per-channel "
+                        "weight scales, bf16 out; eight 52.4 MB weights rotated", "unit": "GB/s", "peak": peak,
+            "per_M": rows, "dense_m2048": dense, "gpu_launches": launches}
+
+
 def run_decode_step(torch, fp8, device, dist_barrier, dist_max, reps=20):
     """Synthetic 64-layer decode step at M in {1, 4, 8}: per layer RMSNorm ->
     static quant -> QKV (10240x5120), per-token quant of an [M, 8192] stub
@@ -553,6 +601,7 @@ def run_ours(args, rank, world, dist_barrier, dist_max):
             raise RuntimeError(f"device error word {err:#x}")
     if not args.no_extras:
         out["gate_up"] = run_gate_up(torch, fp8, device, dist_barrier, dist_max)
+        out["w8a16"] = run_w8a16(torch, fp8, device, dist_barrier, dist_max)
         out["decode_step"] = run_decode_step(torch, fp8, device, dist_barrier, dist_max)
         out["tiny"] = run_tiny(torch, fp8, device, dist_barrier, dist_max)
         err = fp8.get_device_error()

@@ -41,6 +41,8 @@ FLAG_NO_PDL = 2
 KERNEL_NONE = 0
 KERNEL_DECODE_SPLITK = 1
 KERNEL_PREFILL = 2
+KERNEL_W16_DECODE = 3
+KERNEL_W16_DENSE = 4
 
 E4M3 = torch.float8_e4m3fn
 
@@ -85,6 +87,14 @@ def lib():
     L.rmsnorm_quant_fp8.restype = I32
     L.quant_fp8_per_token.argtypes = [P, P, P, I64, I64, P]
     L.quant_fp8_per_token.restype = I32
+    L.fp8_w8a16_mm.argtypes = [P, P, P, I32, I32, I64, I64, I64, P, P]
+    L.fp8_w8a16_mm.restype = I32
+    L.fp8_w8a16_mm_ex.argtypes = [P, P, P, I32, I32, I64, I64, I64, P, P, ctypes.c_uint]
+    L.fp8_w8a16_mm_ex.restype = I32
+    L.fp8_w8a16_describe_dispatch.argtypes = [I64, I64, I64]
+    L.fp8_w8a16_describe_dispatch.restype = I32
+    L.fp8_widen_weight.argtypes = [P, P, I32, I64, I64, P, P]
+    L.fp8_widen_weight.restype = I32
     L.fp8_quant_per_token_group.argtypes = [P, P, P, I64, I64, P]
     L.fp8_quant_per_token_group.restype = I32
     L.fp8_quant_weight_block.argtypes = [P, P, P, I64, I64, P]
@@ -325,6 +335,52 @@ def quant_fp8_per_token(x, out=None, scale_out=None):
     _check(lib().quant_fp8_per_token(_ptr(x), _ptr(out), _ptr(scale_out), M, K, _stream_of(x)),
            "quant_fp8_per_token")
     return out, scale_out
+
+
+def w8a16_mm(x, W, scale_b, granularity=None, out=None, flags=0):
+    """Weight-only FP8 GEMM: y = bf16((x @ dec(W).T) * scale_b) for bf16 x
+    [M,K] and E4M3 W [N,K]; ``granularity`` (0 per-tensor, 1 per-channel)
+    defaults from the length of scale_b."""
+    _need(x, "x", (torch.bfloat16,), 2)
+    _need(W, "W", _FP8, 2)
+    _need(scale_b, "scale_b", (torch.float32,))
+    M, K = x.shape
+    N, Kw = W.shape
+    if Kw != K:
+        raise ValueError(f"x is [{M},{K}] but W is [{N},{Kw}]")
+    if granularity is None:
+        granularity = GRAN_PER_CHANNEL if (scale_b.numel() == N and N != 1) else GRAN_PER_TENSOR
+    if scale_b.numel() < (N if granularity == GRAN_PER_CHANNEL else 1):
+        raise ValueError("scale_b too short for the granularity")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(out, "out", (torch.bfloat16,), 2)
+        if tuple(out.shape) != (M, N):
+            raise ValueError(f"out must be [{M},{N}]")
+    _check(lib().fp8_w8a16_mm_ex(_ptr(x), _ptr(W), _ptr(scale_b), int(granularity), OUT_BF16, M, N, K, _ptr(out),
+                                 _stream_of(x), int(flags)), "fp8_w8a16_mm")
+    return out
+
+
+def w8a16_describe_dispatch(M, N, K) -> int:
+    return lib().fp8_w8a16_describe_dispatch(M, N, K)
+
+
+def widen_weight(W, scale_b, granularity=None, out=None):
+    """bf16 [N,K] = bf16_rne(fp32(dec(W) * s)), the weight-only large-M branch's weight."""
+    _need(W, "W", _FP8, 2)
+    _need(scale_b, "scale_b", (torch.float32,))
+    N, K = W.shape
+    if granularity is None:
+        granularity = GRAN_PER_CHANNEL if (scale_b.numel() == N and N != 1) else GRAN_PER_TENSOR
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.bfloat16, device=W.device)
+    else:
+        _need(out, "out", (torch.bfloat16,), 2)
+    _check(lib().fp8_widen_weight(_ptr(W), _ptr(scale_b), int(granularity), N, K, _ptr(out), _stream_of(W)),
+           "fp8_widen_weight")
+    return out
 
 
 def quant_per_token_group(x, out=None, scale_out=None):

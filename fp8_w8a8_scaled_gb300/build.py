@@ -16,8 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "quant.cu", "gemm_decode.cu", "gemm_prefill.cu"]
-HEADERS = ["ptx.cuh", "kernels.h"]
+SOURCES = ["api.cu", "quant.cu", "gemm_decode.cu", "gemm_prefill.cu", "gemm_w8a16.cu"]
+HEADERS = ["ptx.cuh", "kernels.h", "splitk.cuh", "norm_row.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-I", os.path.join(ROOT, "include")]

@@ -2,9 +2,11 @@
 // TMA descriptor creation, the device error word.  Every entry point validates
 // everything before touching the GPU, so the validation paths run (and are
 // tested) on a machine without a GPU.
+#include <cublas_v2.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <dlfcn.h>
 
 #include <cstdint>
 #include <mutex>
@@ -33,7 +35,22 @@ struct DeviceState {
     uint32_t *counters = nullptr;
     float *slots = nullptr;
     size_t n_slots = 0;
+    void *w16 = nullptr;  // the weight-only large-M branch's bf16 weight (grow-only)
+    size_t w16_bytes = 0;
+    cublasHandle_t blas = nullptr;
 };
+
+// cuBLAS, for the weight-only large-M branch's dense bf16 GEMM only, opened
+// on first use so that the library loads where cuBLAS is absent.
+struct Blas {
+    bool tried = false;
+    cublasStatus_t (*create)(cublasHandle_t *) = nullptr;
+    cublasStatus_t (*set_stream)(cublasHandle_t, cudaStream_t) = nullptr;
+    cublasStatus_t (*gemm_ex)(cublasHandle_t, cublasOperation_t, cublasOperation_t, int, int, int, const void *,
+                              const void *, cudaDataType, int, const void *, cudaDataType, int, const void *, void *,
+                              cudaDataType, int, cublasComputeType_t, cublasGemmAlgo_t) = nullptr;
+};
+Blas g_blas;
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -84,7 +101,60 @@ fp8_status make_tmap_e4m3(CUtensorMap *tm, const void *ptr, int64_t rows, int64_
     return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
 }
 
+// 2-D bf16 tensor [rows, cols] (cols contiguous) read in boxes of
+// box_rows x 64 elements (128 bytes) with the 128-byte swizzle; out-of-range
+// elements read as zero.
+fp8_status make_tmap_bf16(CUtensorMap *tm, const void *ptr, int64_t rows, int64_t cols, uint32_t box_rows) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2u};
+    cuuint32_t box[2] = {64u, box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
+}
+
 fp8_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
+
+// The cuBLAS handle of this device (cuBLAS opened on first use).
+fp8_status blas_handle(DeviceState *st, cublasHandle_t *h) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_blas.tried) {
+        g_blas.tried = true;
+        void *lib = dlopen("libcublas.so.13", RTLD_NOW | RTLD_GLOBAL);
+        if (!lib) lib = dlopen("libcublas.so", RTLD_NOW | RTLD_GLOBAL);
+        if (lib) {
+            g_blas.create = reinterpret_cast<decltype(g_blas.create)>(dlsym(lib, "cublasCreate_v2"));
+            g_blas.set_stream = reinterpret_cast<decltype(g_blas.set_stream)>(dlsym(lib, "cublasSetStream_v2"));
+            g_blas.gemm_ex = reinterpret_cast<decltype(g_blas.gemm_ex)>(dlsym(lib, "cublasGemmEx"));
+        }
+    }
+    if (!g_blas.create || !g_blas.set_stream || !g_blas.gemm_ex) return FP8_ERR_UNSUPPORTED;
+    if (st->blas == nullptr && g_blas.create(&st->blas) != CUBLAS_STATUS_SUCCESS) {
+        st->blas = nullptr;
+        return FP8_ERR_CUDA;
+    }
+    *h = st->blas;
+    return FP8_OK;
+}
+
+// The bf16 weight buffer of the large-M branch, grown to `bytes` if needed.
+fp8_status w16_buffer(DeviceState *st, size_t bytes, void **out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (st->w16_bytes < bytes) {
+        if (st->w16 && cudaFree(st->w16) != cudaSuccess) return FP8_ERR_CUDA;
+        st->w16 = nullptr;
+        st->w16_bytes = 0;
+        if (cudaMalloc(&st->w16, bytes) != cudaSuccess) {
+            st->w16 = nullptr;
+            return FP8_ERR_CUDA;
+        }
+        st->w16_bytes = bytes;
+    }
+    *out = st->w16;
+    return FP8_OK;
+}
 
 // The decode kernel's workspace for this device: sized for the largest plan
 // (two CTAs per SM, 64-token tiles), allocated and zeroed on first use.
@@ -368,6 +438,81 @@ fp8_status quant_fp8_per_token(const void *x, void *out, float *scale_out, int64
     if (s != FP8_OK) return s;
     return from_cuda(fp8k::launch_quant_per_token(x, out, scale_out, M, K, st->err, static_cast<cudaStream_t>(stream),
                                                   st->num_sms, fp8k::LaunchOpts{}));
+}
+
+int fp8_w8a16_describe_dispatch(int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > kI32Max) return -1;
+    if (M == 0) return FP8_KERNEL_NONE;
+    return M >= fp8k::kPrefillMinM ? FP8_KERNEL_W16_DENSE : FP8_KERNEL_W16_DECODE;
+}
+
+fp8_status fp8_widen_weight(const void *W, const float *scale_b, int granularity, int64_t N, int64_t K, void *out,
+                            void *stream) {
+    if (N < 0 || N > kI32Max || K < 1 || K > kI32Max) return FP8_ERR_INVALID_ARG;
+    if (granularity != FP8_GRAN_PER_TENSOR && granularity != FP8_GRAN_PER_CHANNEL) return FP8_ERR_INVALID_ARG;
+    if (N == 0) return FP8_OK;
+    if (!W || !scale_b || !out) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(out) || !aligned4(scale_b)) return FP8_ERR_ALIGNMENT;
+    if (K % 16 != 0) return FP8_ERR_ALIGNMENT;
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    return from_cuda(fp8k::launch_widen_weight(W, scale_b, granularity == FP8_GRAN_PER_CHANNEL ? 1 : 0, N, K, out,
+                                               static_cast<cudaStream_t>(stream), st->num_sms, fp8k::LaunchOpts{}));
+}
+
+fp8_status fp8_w8a16_mm_ex(const void *x, const void *W, const float *scale_b, int granularity, int out_dtype,
+                           int64_t M, int64_t N, int64_t K, void *out, void *stream, unsigned flags) {
+    if (M < 0 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > kI32Max) return FP8_ERR_INVALID_ARG;
+    if (granularity != FP8_GRAN_PER_TENSOR && granularity != FP8_GRAN_PER_CHANNEL) return FP8_ERR_INVALID_ARG;
+    if (flags & ~static_cast<unsigned>(FP8_FLAG_WEIGHTS_STATIC | FP8_FLAG_NO_PDL)) return FP8_ERR_INVALID_ARG;
+    if (out_dtype != FP8_OUT_BF16) return FP8_ERR_UNSUPPORTED;
+    if (M == 0) return FP8_OK;
+    if (!x || !W || !scale_b || !out) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(out) || !aligned4(scale_b)) return FP8_ERR_ALIGNMENT;
+    if (K % 16 != 0 || N % 8 != 0) return FP8_ERR_ALIGNMENT;
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    fp8k::LaunchOpts opts;
+    opts.pdl = (flags & FP8_FLAG_NO_PDL) == 0;
+    opts.weights_static = (flags & FP8_FLAG_WEIGHTS_STATIC) != 0;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int per_channel = granularity == FP8_GRAN_PER_CHANNEL ? 1 : 0;
+    if (fp8_w8a16_describe_dispatch(M, N, K) == FP8_KERNEL_W16_DENSE) {
+        // Large M: the weight widened to bf16 (exact: every E4M3 value is a
+        // bf16 value), a dense bf16 GEMM (cuBLAS; y^T [N,M] = W16 [N,K] x^T,
+        // column-major) into out, then the scale applied in place.
+        cublasHandle_t h = nullptr;
+        if ((s = blas_handle(st, &h)) != FP8_OK) return s;
+        void *w16 = nullptr;
+        if ((s = w16_buffer(st, static_cast<size_t>(N) * static_cast<size_t>(K) * 2u, &w16)) != FP8_OK) return s;
+        if ((s = from_cuda(fp8k::launch_widen_weight(W, nullptr, 0, N, K, w16, cs, st->num_sms, opts))) != FP8_OK)
+            return s;
+        {
+            std::lock_guard<std::mutex> lock(g_mu);
+            const float one = 1.0f, zero = 0.0f;
+            if (g_blas.set_stream(h, cs) != CUBLAS_STATUS_SUCCESS) return FP8_ERR_CUDA;
+            const cublasStatus_t b = g_blas.gemm_ex(
+                h, CUBLAS_OP_T, CUBLAS_OP_N, static_cast<int>(N), static_cast<int>(M), static_cast<int>(K), &one, w16,
+                CUDA_R_16BF, static_cast<int>(K), x, CUDA_R_16BF, static_cast<int>(K), &zero, out, CUDA_R_16BF,
+                static_cast<int>(N), CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+            if (b != CUBLAS_STATUS_SUCCESS) return FP8_ERR_CUDA;
+        }
+        return from_cuda(fp8k::launch_scale_columns(out, scale_b, per_channel, M, N, cs, st->num_sms, opts));
+    }
+    const fp8k::DecodePlan plan = fp8k::plan_w8a16(M, N, K, st->num_sms);
+    fp8k::DecodeWorkspace ws;
+    if ((s = decode_workspace(st, plan, &ws)) != FP8_OK) return s;
+    CUtensorMap tw, tx;
+    if ((s = make_tmap_e4m3(&tw, W, N, K, fp8k::kDecodeRows)) != FP8_OK) return s;
+    if ((s = make_tmap_bf16(&tx, x, M, K, static_cast<uint32_t>(plan.tok_pad))) != FP8_OK) return s;
+    return from_cuda(fp8k::launch_w8a16_gemm(tw, tx, scale_b, per_channel, M, N, K, out, st->err, plan, ws, opts, cs));
+}
+
+fp8_status fp8_w8a16_mm(const void *x, const void *W, const float *scale_b, int granularity, int out_dtype, int64_t M,
+                        int64_t N, int64_t K, void *out, void *stream) {
+    return fp8_w8a16_mm_ex(x, W, scale_b, granularity, out_dtype, M, N, K, out, stream, 0u);
 }
 
 fp8_status fp8_quant_per_token_group(const void *x, void *out, float *scale_out, int64_t M, int64_t K, void *stream) {

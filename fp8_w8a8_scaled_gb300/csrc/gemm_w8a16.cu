@@ -1,0 +1,562 @@
+// gemm_w8a16.cu -- weight-only FP8 GEMM (W8A16) for small M: bf16 activations
+// x [M,K], E4M3 weights W [N,K] with a per-tensor or per-output-channel scale,
+// bf16 out:  y[m,n] = bf16( (sum_k x[m,k] * dec(W[n,k])) * sb ).
+// Sources: "[Kernel] add Flashinfer cutedsl w4a16 linear" (vllm #53014): the
+// FP8 channelwise half of the weight-only path (the weight stays E4M3 in HBM
+// and is widened on chip; at decode M the kernel is bound by the weight
+// bytes), and its large-M branch (widen the weight to 16 bits once, then a
+// dense 16-bit GEMM), which lives in api.cu.
+//
+// Design (GB300, sm_103a).  The tensor core's kind::f16 takes both operands in
+// one 16-bit type, so the E4M3 weight tile is widened to bf16 (exact: every
+// E4M3 value is a bf16 value) in shared memory before the MMA reads it.
+// Units are (128-row output tile) x (128-wide k-block), divided among one
+// persistent CTA per SM as in the W8A8 kernel's stream-K mode (one CTA per SM:
+// the widened tiles take 128 KB of shared memory beside the ring).  Inside a
+// CTA:
+//   * warp 0 / lane 0 streams each unit's 128 x 128-byte E4M3 weight box and
+//     its two TOK x 64-element bf16 token boxes with TMA into a ring of stages
+//     (128-byte swizzle);
+//   * warps 6-13 (two warpgroups, half of each weight row per thread; one
+//     warpgroup, whole rows, for the 32-token tile) widen
+//     each unit's E4M3 tile into one of four bf16 A tiles, laid out as the MMA
+//     reads them (two 64-element K halves of 128 rows x 128 bytes, 128-byte
+//     swizzled), up to four units ahead of the MMA;
+//   * warps 2-5 drain each unit's fp32 partial out of TMEM into TwoSum
+//     registers -- the same drain, tile store and stream-K fix-up as the W8A8
+//     decode kernel;
+//   * warp 1 / lane 0 issues eight tcgen05.mma kind::f16 (BF16 x BF16 -> F32,
+//     M = 128 weight rows, N = TOK tokens, K = 16) per unit into one of
+//     several TMEM accumulators.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "splitk.cuh"
+
+namespace fp8k {
+namespace {
+
+constexpr uint32_t kW16WeightBytes = kDecodeRows * kBlockK;    // 16 KB of E4M3 per stage
+constexpr uint32_t kW16Region = kDecodeRows * 128;             // 64 bf16 of K for 128 rows: 16 KB
+constexpr uint32_t kW16ATileBytes = 2 * kW16Region;            // the widened 128 x 128 tile: 32 KB
+
+template <int TOK>
+struct W16Cfg {
+    // producer warp, MMA warp, one drain warpgroup, kWidenGroups widening
+    // warpgroups (each thread widens its row's share of the 8 chunks); one for
+    // the 32-token tile, whose drain needs the registers of a 10-warp CTA
+    static constexpr int kWidenGroups = TOK <= 16 ? 2 : 1;
+    static constexpr int kThreads = 64 + 128 + 128 * kWidenGroups;
+    // registers a thread may use with one CTA per SM: a sub-partition holds
+    // ceil(warps / 4) of its warps, 16384 registers each
+    static constexpr int kMaxRegs = (16384 / (32 * ((kThreads / 32 + 3) / 4))) / 8 * 8;
+    static constexpr int kDrainThreads = 128;
+    static constexpr int kBufs = TOK <= 16 ? 8 : 4;              // TMEM accumulators (must match w16_tmem_bufs)
+    static constexpr uint32_t kTmemCols = kBufs * TOK < 32 ? 32 : kBufs * TOK;
+    static constexpr uint32_t kXRegion = TOK * 128;              // 64 bf16 of K for TOK tokens
+    static constexpr uint32_t kXStageBytes = 2 * kXRegion;       // one unit's token tile
+    static constexpr int kXStages = 8;                           // token ring (>= the weight ring)
+    static constexpr int kABufs = TOK <= 16 ? 3 : 2;             // widened tiles ahead of the MMA
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(kDecodeRows, TOK);
+};
+
+// Two E4M3 codes (the first in the low byte) -> two bf16 (the first in the low
+// half); exact, NaN codes give NaN.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t pair) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair), __NV_E4M3);
+    const float2 f = __half22float2(__half2(h));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    return static_cast<uint32_t>(__bfloat16_as_ushort(b.x)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b.y)) << 16);
+}
+
+// Chunks [J0, J0 + NJ) of row r of a 128 x 128-byte E4M3 box (128-byte
+// swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)) widened into
+// the bf16 A tile: K elements 64h .. 64h+63 go to region h, whose rows are 128
+// bytes of 8-element chunks swizzled the same way.
+template <int NJ>
+__device__ __forceinline__ void widen_row(const uint8_t *src, uint8_t *dst, int r, int J0) {
+    const int sw = r & 7;
+    const uint8_t *srow = src + r * 128;
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) {
+        const int j = J0 + jj;
+        const uint4 q = *reinterpret_cast<const uint4 *>(srow + ((j ^ sw) << 4));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            o[2 * t] = e4m3x2_to_bf16x2(w[t] & 0xFFFFu);
+            o[2 * t + 1] = e4m3x2_to_bf16x2(w[t] >> 16);
+        }
+        uint8_t *drow = dst + (j >> 2) * kW16Region + r * 128;
+        const int c0 = (j & 3) * 2;
+        *reinterpret_cast<uint4 *>(drow + ((c0 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4 *>(drow + (((c0 + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// (No __launch_bounds__: the register cap is set from the warp count.)
+template <int TOK>
+__global__ void __maxnreg__(W16Cfg<TOK>::kMaxRegs)
+    w8a16_decode_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                        const DecodeArgs args) {
+    using Cfg = W16Cfg<TOK>;
+    constexpr int NB = Cfg::kBufs;
+    constexpr int kSlotElems = TOK * kDecodeRows;  // fp32 entries of one partial slot
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem_base, s_last;
+    __shared__ uint32_t s_w_issued, s_w_consumed, s_x_issued, s_x_consumed;  // loads requested / used
+    __shared__ int64_t s_slot[2][kMaxFixupSegs];
+    __shared__ int s_nseg[2];
+    __shared__ volatile uint32_t s_abort;
+
+    const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int stages = args.stages;  // the weight ring
+    constexpr int NX = Cfg::kXStages;
+    constexpr int NA = Cfg::kABufs;
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    // [weight ring: stages x 16 KB][token ring: NX x TOK*256 B][widened tiles: NA x 32 KB][barriers]
+    const uint32_t xbase = base + static_cast<uint32_t>(stages) * kW16WeightBytes;
+    const uint32_t abuf0 = xbase + static_cast<uint32_t>(NX) * Cfg::kXStageBytes;
+    const uint32_t bar0 = abuf0 + static_cast<uint32_t>(NA) * kW16ATileBytes;
+    auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
+    auto wempty_bar = [&](int s) { return bar0 + 8u * (stages + s); };
+    auto xfull_bar = [&](int s) { return bar0 + 8u * (2 * stages + s); };
+    auto xempty_bar = [&](int s) { return bar0 + 8u * (2 * stages + NX + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * stages + 2 * NX + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * stages + 2 * NX + NB + b); };
+    auto afull_bar = [&](int a) { return bar0 + 8u * (2 * stages + 2 * NX + 2 * NB + a); };
+    auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * stages + 2 * NX + 2 * NB + NA + a); };
+    const uint32_t final_bar = bar0 + 8u * (2 * stages + 2 * NX + 2 * NB + 2 * NA);
+
+    const int64_t G = gridDim.x, U = args.units;
+    const int64_t me = blockIdx.x;
+    const int64_t u0 = unit_begin(me, U, G), u1 = unit_begin(me + 1, U, G);
+    const int iters = static_cast<int>(u1 - u0);
+    const int kbt = args.kb_total, n_tiles = args.n_tiles;
+    uint32_t *const err = args.err;
+
+    if (tid == 0) {
+        tma_prefetch_desc(&tmap_w);
+        tma_prefetch_desc(&tmap_x);
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(wfull_bar(s), 1);
+            mbar_init(wempty_bar(s), 4 * Cfg::kWidenGroups);  // one arrive per widening warp
+        }
+        for (int s = 0; s < NX; ++s) {
+            mbar_init(xfull_bar(s), 1);
+            mbar_init(xempty_bar(s), 1);  // the MMA's commit
+        }
+        for (int b = 0; b < NB; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4);  // one arrive per drain warp
+        }
+        for (int a = 0; a < NA; ++a) {
+            mbar_init(afull_bar(a), 4 * Cfg::kWidenGroups);  // one arrive per widening warp
+            mbar_init(aempty_bar(a), 1);                      // the MMA's commit
+        }
+        mbar_init(final_bar, 1);
+        fence_mbar_init();
+        s_w_issued = s_w_consumed = s_x_issued = s_x_consumed = 0;
+        s_abort = 0;
+    }
+    if (warp == 1) tmem_alloc(smem_u32(&s_tmem_base), Cfg::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------------------- producer
+        // The weight ring is released by the widening warps as soon as they
+        // have read a stage, the token ring by the MMA; each runs ahead on its own.
+        const uint64_t evict_first = policy_evict_first();
+        int i = 0;
+        // Weights that no earlier kernel in the stream writes may be fetched
+        // before the dependency wait; the tokens always wait.
+        const int pre = args.weights_static ? min(iters, stages) : 0;
+        for (; i < pre; ++i) {
+            const int64_t u = u0 + i, t = u / kbt;
+            const int kb = static_cast<int>(u - t * kbt), n_tile = static_cast<int>(t % n_tiles);
+            mbar_arrive_expect_tx(wfull_bar(i), kW16WeightBytes);
+            tma_load_2d_hint(base + static_cast<uint32_t>(i) * kW16WeightBytes, &tmap_w, wfull_bar(i), kb * kBlockK,
+                             n_tile * kDecodeRows, evict_first);
+        }
+        s_w_issued = static_cast<uint32_t>(i);
+        grid_dependency_wait();
+        int wi = i, xi = 0;  // units whose weights / tokens are requested
+        int wt = static_cast<int>((u0 + wi) / kbt), wkb = static_cast<int>(u0 + wi - static_cast<int64_t>(wt) * kbt);
+        int xt = static_cast<int>(u0 / kbt), xkb = static_cast<int>(u0 - static_cast<int64_t>(xt) * kbt);
+        bool ok = true;
+        while (ok && (wi < iters || xi < iters)) {
+            // tokens first while they trail the weights (the MMA needs both)
+            if (xi < iters && (xi < wi || wi == iters)) {
+                if (xkb == kbt) {
+                    xkb = 0;
+                    ++xt;
+                }
+                const int s = xi % NX;
+                if (!cta_wait(xempty_bar(s), (static_cast<uint32_t>(xi / NX) & 1u) ^ 1u, err, kErrDecodeEmptyWait,
+                              &s_abort)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t xs = xbase + static_cast<uint32_t>(s) * Cfg::kXStageBytes;
+                const int m_tile = xt / n_tiles;
+                mbar_arrive_expect_tx(xfull_bar(s), Cfg::kXStageBytes);
+                tma_load_2d(xs, &tmap_x, xfull_bar(s), xkb * kBlockK, m_tile * TOK);
+                tma_load_2d(xs + Cfg::kXRegion, &tmap_x, xfull_bar(s), xkb * kBlockK + 64, m_tile * TOK);
+                ++xi;
+                ++xkb;
+                s_x_issued = static_cast<uint32_t>(xi);
+            } else {
+                if (wkb == kbt) {
+                    wkb = 0;
+                    ++wt;
+                }
+                const int s = wi % stages;
+                if (!cta_wait(wempty_bar(s), (static_cast<uint32_t>(wi / stages) & 1u) ^ 1u, err,
+                              kErrDecodeEmptyWait, &s_abort)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(wfull_bar(s), kW16WeightBytes);
+                tma_load_2d_hint(base + static_cast<uint32_t>(s) * kW16WeightBytes, &tmap_w, wfull_bar(s),
+                                 wkb * kBlockK, (wt % n_tiles) * kDecodeRows, evict_first);
+                ++wi;
+                ++wkb;
+                s_w_issued = static_cast<uint32_t>(wi);
+            }
+        }
+        grid_launch_dependents();
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------------------- MMA issuer
+        int i = 0;
+        for (; i < iters; ++i) {
+            const int s = i % NX, b = i % NB, a = i % NA;
+            const uint32_t ph = static_cast<uint32_t>(i / NX) & 1u, tph = static_cast<uint32_t>(i / NB) & 1u,
+                           aph = static_cast<uint32_t>(i / NA) & 1u;
+            if (!cta_wait(xfull_bar(s), ph, err, kErrDecodeFullWait, &s_abort)) break;
+            if (!cta_wait(afull_bar(a), aph, err, kErrW16AFullWait, &s_abort)) break;
+            if (!cta_wait(tempty_bar(b), tph ^ 1u, err, kErrDecodeTmemEmptyWait, &s_abort)) break;
+            tc_fence_after();
+            const uint32_t xs = xbase + static_cast<uint32_t>(s) * Cfg::kXStageBytes;
+            const uint32_t as = abuf0 + static_cast<uint32_t>(a) * kW16ATileBytes;
+            const uint32_t d = tmem + static_cast<uint32_t>(b * TOK);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {  // K = 16 bf16 = 32 bytes per MMA: +2 in the address field
+                const uint32_t h = static_cast<uint32_t>(kk >> 2), o = 2u * static_cast<uint32_t>(kk & 3);
+                mma_bf16(d, sw128_kmajor_desc(as + h * kW16Region) + o, sw128_kmajor_desc(xs + h * Cfg::kXRegion) + o,
+                         Cfg::kIdesc, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(xempty_bar(s));
+            mma_commit(aempty_bar(a));
+            mma_commit(tfull_bar(b));
+        }
+        s_x_consumed = static_cast<uint32_t>(i);
+        mma_commit(final_bar);  // arrives when every MMA issued above has completed
+    } else if (warp >= 6) {
+        // ---------------------------------------------------------------- widening
+        // Unit j's E4M3 weights widened into A tile j % NA once the stage has
+        // landed and the MMA of unit j - NA has finished reading the tile; the
+        // weight stage is released right after.  Warpgroup g widens chunks
+        // [g*8/WG, (g+1)*8/WG) of every row.
+        constexpr int kNJ = 8 / Cfg::kWidenGroups;
+        const int row = static_cast<int>((warp & 3u) * 32u + lane);
+        const int j0 = static_cast<int>((warp - 6) / 4) * kNJ;
+        int j = 0;
+        for (; j < iters; ++j) {
+            const int s = j % stages, a = j % NA;
+            if (!cta_wait(wfull_bar(s), static_cast<uint32_t>(j / stages) & 1u, err, kErrW16FullWait, &s_abort))
+                break;
+            if (!cta_wait(aempty_bar(a), (static_cast<uint32_t>(j / NA) & 1u) ^ 1u, err, kErrW16AEmptyWait,
+                          &s_abort))
+                break;
+            widen_row<kNJ>(smem_raw + (base + static_cast<uint32_t>(s) * kW16WeightBytes - raw),
+                           smem_raw + (abuf0 + static_cast<uint32_t>(a) * kW16ATileBytes - raw), row, j0);
+            fence_proxy_async_smem();  // the writes, before the tensor core reads them
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(afull_bar(a));
+                mbar_arrive(wempty_bar(s));
+            }
+        }
+        if (warp == 6 && lane == 0) s_w_consumed = static_cast<uint32_t>(j);
+    } else if (warp >= 2) {
+        // ---------------------------------------------------------------- drain + tile output
+        const uint32_t quarter = warp & 3u;                      // TMEM lanes 32*(warp%4) .. +31
+        const int row = static_cast<int>(quarter * 32u + lane);  // weight row within the tile
+        grid_dependency_wait();  // outputs, scales and the workspace are touched below
+        const bool sb_vec = args.gran == 1;
+        const float sb0 = __ldg(args.scale_b);
+        const int t_first_me = static_cast<int>(u0 / kbt);
+        if (tid == 64 && iters > 0) {
+            // Which CTAs hold the other parts of this CTA's first and last tile
+            // and where their partial sums go.
+            for (int w = 0; w < 2; ++w) {
+                const int64_t t = (w == 0 ? u0 : u1 - 1) / kbt, tile_u0 = t * kbt;
+                const int64_t c_first = unit_owner(tile_u0, U, G), c_last = unit_owner(tile_u0 + kbt - 1, U, G);
+                const int nseg = static_cast<int>(c_last - c_first + 1);
+                s_nseg[w] = nseg;
+                for (int j = 0; j < kMaxFixupSegs && j < nseg; ++j) {
+                    const int64_t cc = c_first + j;
+                    s_slot[w][j] = (2 * cc + (t == unit_begin(cc, U, G) / kbt ? 0 : 1)) * kSlotElems;
+                }
+            }
+        }
+        float hi[TOK], lo[TOK];
+#pragma unroll
+        for (int c = 0; c < TOK; ++c) hi[c] = lo[c] = 0.0f;
+
+        int t = static_cast<int>(u0 / kbt), kb = static_cast<int>(u0 - static_cast<int64_t>(t) * kbt);
+        for (int i = 0; i < iters; ++i, ++kb) {
+            if (kb == kbt) {
+                kb = 0;
+                ++t;
+            }
+            const int b = i % NB;
+            const uint32_t tph = static_cast<uint32_t>(i / NB) & 1u;
+            cta_wait(tfull_bar(b), tph, err, kErrDecodeTmemFullWait, &s_abort);
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((quarter * 32u) << 16) + static_cast<uint32_t>(b * TOK);
+#pragma unroll
+            for (int c0 = 0; c0 < TOK; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(taddr + static_cast<uint32_t>(c0), r);
+                tmem_ld_wait();
+                if (c0 + 16 >= TOK) {  // last chunk read: the accumulator is free for the MMA again
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(b));
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) two_sum_acc(hi[c0 + j], lo[c0 + j], __uint_as_float(r[j]));
+            }
+
+            if (kb != kbt - 1 && i != iters - 1) continue;
+
+            // ---- this CTA's part of tile t ends here
+            const int n_tile = t % n_tiles, m_tile = t / n_tiles;
+            const int n = n_tile * kDecodeRows + row;
+            const int m0 = m_tile * TOK;
+            const int mt = min(TOK, args.M - m0);
+            const int64_t tile_u0 = static_cast<int64_t>(t) * kbt;
+            const bool whole = (u0 <= tile_u0) && (kb == kbt - 1);
+            if (!whole) {
+                // this CTA's part of the tile, rounded once to binary32, then
+                // the arrival count; the last of the tile's parts sums them all
+                float *mine = args.slots + static_cast<int64_t>(2 * me + (t == t_first_me ? 0 : 1)) * kSlotElems;
+#pragma unroll
+                for (int c = 0; c < TOK; ++c)
+                    if (c < mt) mine[c * kDecodeRows + row] = __fadd_rn(hi[c], lo[c]);
+                named_barrier_sync(1, Cfg::kDrainThreads);
+                const int w = (t == t_first_me) ? 0 : 1;
+                if (tid == 64) {
+                    const int nseg = s_nseg[w];
+                    __threadfence();
+                    const bool last = atomicAdd(args.counters + t, 1u) == static_cast<uint32_t>(nseg - 1);
+                    if (last) __threadfence();
+                    s_last = last ? static_cast<uint32_t>(nseg) : 0u;
+                }
+                named_barrier_sync(1, Cfg::kDrainThreads);
+                if (s_last != 0u) {
+                    int nseg = static_cast<int>(s_last);
+                    if (nseg > kMaxFixupSegs) {  // the planner keeps this from happening
+                        if (tid == 64) atomicOr(err, kErrDecodeFixup);
+                        nseg = kMaxFixupSegs;
+                    }
+                    fixup_sum<kMaxFixupSegs, 1, Cfg::kDrainThreads>(args, s_slot[w], nseg, mt * kDecodeRows,
+                                                                     static_cast<int>(tid) - 64, n_tile, m0, false,
+                                                                     sb_vec, 1.0f, sb0);
+                    if (tid == 64) args.counters[t] = 0u;  // ready for the next launch
+                }
+            } else if (n < args.N) {
+                const float sb = sb_vec ? __ldg(args.scale_b + n) : sb0;
+#pragma unroll
+                for (int c = 0; c < TOK; ++c)
+                    if (c < mt)
+                        args.out[static_cast<int64_t>(m0 + c) * args.N + n] =
+                            __float2bfloat16_rn(__fmul_rn(__fadd_rn(hi[c], lo[c]), sb));
+            }
+#pragma unroll
+            for (int c = 0; c < TOK; ++c) hi[c] = lo[c] = 0.0f;
+        }
+    }
+    __syncwarp();
+    grid_dependency_wait();
+    grid_launch_dependents();
+    __syncthreads();
+
+    if (tid == 0) {
+        // Loads issued but never consumed (only after a timeout): let them land
+        // before the CTA exits.
+        for (uint32_t i = s_w_consumed; i < s_w_issued; ++i)
+            mbar_wait(wfull_bar(static_cast<int>(i % stages)), (i / stages) & 1u, err, kErrW16FullWait);
+        for (uint32_t i = s_x_consumed; i < s_x_issued; ++i)
+            mbar_wait(xfull_bar(static_cast<int>(i % NX)), (i / NX) & 1u, err, kErrDecodeFullWait);
+    }
+    if (warp == 1) {
+        mbar_wait(final_bar, 0, err, kErrDecodeAccumWait);  // every MMA has completed
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+}
+
+template <int TOK>
+cudaError_t launch_w16(const CUtensorMap &tw, const CUtensorMap &tx, const DecodeArgs &a, const DecodePlan &p,
+                       const LaunchOpts &o, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool attr_done[64] = {};  // benign race: the attribute call is idempotent
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(w8a16_decode_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(p.smem_bytes));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    return launch_with_opts(w8a16_decode_kernel<TOK>, dim3(static_cast<unsigned>(p.ctas)),
+                            dim3(W16Cfg<TOK>::kThreads), p.smem_bytes, stream, o, tw, tx, a);
+}
+
+// w16[n,k] = bf16_rne(fp32(dec(W[n,k]) * s)), one binary32 multiply rounded
+// to nearest, then rounded to bf16 (s = 1 when `scale` is null: the exact
+// E4M3 value); 16 codes per thread, grid-stride.
+__global__ void __launch_bounds__(256) widen_weight_kernel(const uint4 *__restrict__ w, uint4 *__restrict__ out,
+                                                           const float *__restrict__ scale, int per_channel,
+                                                           int64_t n16, int k16) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const float s = scale ? __ldg(scale + (per_channel ? i / k16 : 0)) : 1.0f;
+        const uint4 q = __ldg(w + i);
+        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>((wv[t >> 1] >> (16 * (t & 1))) & 0xFFFFu), __NV_E4M3);
+            const float2 f = __half22float2(__half2(h));
+            const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(f.x, s), __fmul_rn(f.y, s));
+            o[t] = static_cast<uint32_t>(__bfloat16_as_ushort(b.x)) |
+                   (static_cast<uint32_t>(__bfloat16_as_ushort(b.y)) << 16);
+        }
+        out[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+        out[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// y[m,n] = bf16_rne(fp32(y[m,n]) * s), s = scale[n] (per channel) or
+// scale[0], in place over a bf16 [M,N] matrix; 8 elements per thread.
+__global__ void __launch_bounds__(256) scale_columns_kernel(uint4 *__restrict__ y, const float *__restrict__ scale,
+                                                            int per_channel, int64_t n8, int N8) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int n0 = static_cast<int>(i % N8) * 8;
+        const uint4 v = y[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float s0 = __ldg(scale + (per_channel ? n0 + 2 * t : 0));
+            const float s1 = __ldg(scale + (per_channel ? n0 + 2 * t + 1 : 0));
+            const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(w[t] << 16), s0),
+                                                           __fmul_rn(__uint_as_float(w[t] & 0xFFFF0000u), s1));
+            o[t] = static_cast<uint32_t>(__bfloat16_as_ushort(b.x)) |
+                   (static_cast<uint32_t>(__bfloat16_as_ushort(b.y)) << 16);
+        }
+        y[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+}  // namespace
+
+// Shared memory of one CTA: alignment slack, the weight ring, the token ring,
+// the widened weight tiles and the mbarriers (rounded up).
+static size_t w16_smem_bytes(int tok, int stages) {
+    const int nb = tok <= 16 ? 8 : 4, nx = W16Cfg<16>::kXStages, na = tok <= 16 ? W16Cfg<16>::kABufs
+                                                                                 : W16Cfg<32>::kABufs;
+    const size_t barriers = 8u * static_cast<size_t>(2 * stages + 2 * nx + 2 * nb + 2 * na + 1);
+    return 1024 + static_cast<size_t>(stages) * kW16WeightBytes + static_cast<size_t>(nx) * 2u * tok * 128u +
+           static_cast<size_t>(na) * kW16ATileBytes + ((barriers + 127) / 128) * 128;
+}
+
+DecodePlan plan_w8a16(int64_t M, int64_t N, int64_t K, int num_sms) {
+    DecodePlan p{};
+    p.tok_pad = M <= 16 ? 16 : 32;
+    p.stages = 6;  // 96 KB of weights in flight: 225 KB of shared memory with the token ring and widened tiles
+    p.smem_bytes = w16_smem_bytes(p.tok_pad, p.stages);
+    p.n_tiles = static_cast<int>((N + kDecodeRows - 1) / kDecodeRows);
+    p.m_tiles = static_cast<int>((M + p.tok_pad - 1) / p.tok_pad);
+    p.kb_total = static_cast<int>((K + kBlockK - 1) / kBlockK);
+    p.units = static_cast<int64_t>(p.n_tiles) * p.m_tiles * p.kb_total;
+    p.split = 0;
+    // One persistent CTA per SM, at least kb_total / (kMaxFixupSegs - 1)
+    // units each (at most kMaxFixupSegs CTAs share a tile).
+    const int64_t min_units = (p.kb_total + kMaxFixupSegs - 2) / (kMaxFixupSegs - 1);
+    int64_t ctas = num_sms;
+    if (ctas > p.units / min_units) ctas = p.units / min_units;
+    if (ctas < 1) ctas = 1;
+    p.ctas = static_cast<int>(ctas);
+    return p;
+}
+
+cudaError_t launch_w8a16_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, const float *scale_b,
+                              int per_channel, int64_t M, int64_t N, int64_t K, void *out, uint32_t *err,
+                              const DecodePlan &plan, const DecodeWorkspace &ws, const LaunchOpts &opts,
+                              cudaStream_t stream) {
+    (void)K;
+    DecodeArgs a{};
+    a.scale_a = nullptr;
+    a.scale_b = scale_b;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.err = err;
+    a.counters = ws.counters;
+    a.slots = ws.slots;
+    a.units = plan.units;
+    a.gran = per_channel ? 1 : 0;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.kb_total = plan.kb_total;
+    a.n_tiles = plan.n_tiles;
+    a.stages = plan.stages;
+    a.weights_static = opts.weights_static ? 1 : 0;
+    a.split = 0;
+    if (plan.tok_pad == 32) return launch_w16<32>(tmap_w, tmap_x, a, plan, opts, stream);
+    return launch_w16<16>(tmap_w, tmap_x, a, plan, opts, stream);
+}
+
+cudaError_t launch_scale_columns(void *y, const float *scale, int per_channel, int64_t M, int64_t N,
+                                 cudaStream_t stream, int num_sms, const LaunchOpts &opts) {
+    const int64_t n8 = M * N / 8;
+    int64_t blocks = (n8 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return launch_with_opts(scale_columns_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, opts,
+                            static_cast<uint4 *>(y), scale, per_channel, n8, static_cast<int>(N / 8));
+}
+
+cudaError_t launch_widen_weight(const void *w, const float *scale, int per_channel, int64_t N, int64_t K, void *out,
+                                cudaStream_t stream, int num_sms, const LaunchOpts &opts) {
+    const int64_t n16 = N * K / 16;
+    int64_t blocks = (n16 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return launch_with_opts(widen_weight_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, opts,
+                            static_cast<const uint4 *>(w), static_cast<uint4 *>(out), scale, per_channel, n16,
+                            static_cast<int>(K / 16));
+}
+
+}  // namespace fp8k

@@ -119,6 +119,24 @@ cudaError_t launch_decode_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tma
                                uint32_t *err, const DecodePlan &plan, const DecodeWorkspace &ws, const LaunchOpts &opts,
                                cudaStream_t stream);
 
+// ------------------------------------------------------- weight-only GEMM --
+
+// The W8A16 decode kernel (bf16 activations, E4M3 weights, M <= 32): the
+// decode plan's fields with one persistent CTA per SM (stream-K, split = 0);
+// tmap_x is a bf16 tensor map with 64-element x tok_pad boxes.
+DecodePlan plan_w8a16(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_w8a16_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, const float *scale_b,
+                              int per_channel, int64_t M, int64_t N, int64_t K, void *out, uint32_t *err,
+                              const DecodePlan &plan, const DecodeWorkspace &ws, const LaunchOpts &opts,
+                              cudaStream_t stream);
+// w16 [N,K] bf16 = bf16_rne(fp32(dec(W) * s)) (K % 16 == 0); scale == nullptr
+// gives the exact E4M3 values (the large-M branch's weight).
+cudaError_t launch_widen_weight(const void *w, const float *scale, int per_channel, int64_t N, int64_t K, void *out,
+                                cudaStream_t stream, int num_sms, const LaunchOpts &opts);
+// y [M,N] bf16 <- bf16_rne(fp32(y) * s[n]) in place (N % 8 == 0).
+cudaError_t launch_scale_columns(void *y, const float *scale, int per_channel, int64_t M, int64_t N,
+                                 cudaStream_t stream, int num_sms, const LaunchOpts &opts);
+
 // ------------------------------------------------------------ prefill GEMM --
 
 // Tile geometry of the large-M kernel: 128 tokens (MMA M) x 256 output

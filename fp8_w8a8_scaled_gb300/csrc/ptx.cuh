@@ -21,6 +21,9 @@ enum : uint32_t {
     kErrDecodeTmemFullWait = 1u << 3,
     kErrDecodeTmemEmptyWait = 1u << 8,
     kErrDecodeFixup = 1u << 9,
+    kErrW16FullWait = 1u << 10,     // weight-only kernel: a stage's TMA loads
+    kErrW16AEmptyWait = 1u << 11,   // weight-only kernel: a widened weight tile freed by the MMA
+    kErrW16AFullWait = 1u << 12,    // weight-only kernel: a widened weight tile written
     kErrPrefillFullWait = 1u << 4,
     kErrPrefillEmptyWait = 1u << 5,
     kErrPrefillAccumWait = 1u << 6,
@@ -188,6 +191,36 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t m, uint32_t n) {
            | (0u << 16)         // B K-major
            | ((n >> 3) << 17)   // N / 8, bits 17-22
            | ((m >> 4) << 24);  // M / 16, bits 24-28
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16 with BF16 A and B, both
+// K-major, an FP32 accumulator, and an M x N tile.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
+    return (1u << 4)            // D format: F32
+           | (1u << 7)          // A format: BF16
+           | (1u << 10)         // B format: BF16
+           | (0u << 15)         // A K-major
+           | (0u << 16)         // B K-major
+           | ((n >> 3) << 17)   // N / 8, bits 17-22
+           | ((m >> 4) << 24);  // M / 16, bits 24-28
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T for BF16 operands (K = 16 per instruction),
+// issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy reads of them (a tcgen05.mma operand written by threads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.

@@ -87,7 +87,9 @@ typedef enum { FP8_OUT_BF16 = 0 } fp8_out_dtype;
 typedef enum {
     FP8_KERNEL_NONE = 0,          /* M == 0: nothing is launched */
     FP8_KERNEL_DECODE_SPLITK = 1, /* weight-streaming split-K kernel (small M) */
-    FP8_KERNEL_PREFILL = 2        /* persistent tensor-core tile kernel (large M) */
+    FP8_KERNEL_PREFILL = 2,       /* persistent tensor-core tile kernel (large M) */
+    FP8_KERNEL_W16_DECODE = 3,    /* weight-only: widen-on-chip split-K kernel (M <= 32) */
+    FP8_KERNEL_W16_DENSE = 4      /* weight-only: widened bf16 weight + dense bf16 GEMM (M >= 33) */
 } fp8_kernel_id;
 
 /* fp8_scaled_mm -- the FP8 W8A8 scaled GEMM.
@@ -331,6 +333,51 @@ fp8_status fp8_quant_per_token_group(const void *x, void *out, float *scale_out,
  *   K % 16 == 0, K <= 2^30, N < 2^31.
  * Errors: FP8_ERR_INVALID_ARG, FP8_ERR_ALIGNMENT, FP8_ERR_CUDA. */
 fp8_status fp8_quant_weight_block(const void *w, void *out, float *scale_out, int64_t N, int64_t K, void *stream);
+
+/* fp8_w8a16_mm -- weight-only FP8 GEMM: bf16 activations, E4M3 weights.
+ *
+ * Source: [P4] "[Kernel] add Flashinfer cutedsl w4a16 linear" (vllm #53014):
+ * the FP8 channelwise half of the weight-only path, and its large-M branch
+ * that widens the weight to 16 bits for a dense 16-bit GEMM.
+ *
+ *   x        bf16 [M,K] row-major, 16-byte aligned
+ *   W        E4M3 [N,K] row-major (K contiguous), 16-byte aligned
+ *   scale_b  f32, 1 (FP8_GRAN_PER_TENSOR) or N (FP8_GRAN_PER_CHANNEL) elements
+ *   out      bf16 [M,N], 16-byte aligned, written in full
+ *   M, N, K  as fp8_scaled_mm (K % 16 == 0, N % 8 == 0)
+ *
+ * y[m,n] = bf16( (sum_k x[m,k] * dec(W[n,k])) * sb ).  M <= 32: a split-K
+ * kernel that widens each E4M3 weight tile to bf16 in shared memory (exact)
+ * and multiplies on the tensor core (fp32 accumulation inside 128-wide
+ * k-blocks, TwoSum across them, the scale in binary32 at the end); it shares
+ * the decode kernel's scratch area.  M >= 33: the weight widened to bf16
+ * (exact) into a library-owned buffer of N*K*2 bytes (grown on demand, one per
+ * device, so overlapping large-M calls on different streams race on it), a
+ * dense bf16 GEMM from cuBLAS (fp32 accumulation, bf16 result; cuBLAS is
+ * opened on first use, FP8_ERR_UNSUPPORTED where it is absent), then
+ * y = bf16(fp32(y) * sb) in place.  fp8_w8a16_describe_dispatch tells which.
+ * Errors: FP8_ERR_INVALID_ARG (also a granularity other than per-tensor /
+ * per-channel), FP8_ERR_ALIGNMENT, FP8_ERR_UNSUPPORTED, FP8_ERR_CUDA. */
+fp8_status fp8_w8a16_mm(const void *x, const void *W, const float *scale_b, int granularity, int out_dtype,
+                        int64_t M, int64_t N, int64_t K, void *out, void *stream);
+
+/* fp8_w8a16_mm with launch flags (fp8_flags), as fp8_scaled_mm_ex. */
+fp8_status fp8_w8a16_mm_ex(const void *x, const void *W, const float *scale_b, int granularity, int out_dtype,
+                           int64_t M, int64_t N, int64_t K, void *out, void *stream, unsigned flags);
+
+/* FP8_KERNEL_W16_DECODE for 1 <= M <= 32, FP8_KERNEL_W16_DENSE for M >= 33,
+ * FP8_KERNEL_NONE for M == 0, -1 for sizes fp8_w8a16_mm rejects.  Pure. */
+int fp8_w8a16_describe_dispatch(int64_t M, int64_t N, int64_t K);
+
+/* fp8_widen_weight -- out[n,k] = bf16_rne( fp32(dec(W[n,k]) * s) ), s =
+ * scale_b[0] (FP8_GRAN_PER_TENSOR) or scale_b[n] (FP8_GRAN_PER_CHANNEL): one
+ * binary32 multiply rounded to nearest, then rounded to bf16 (the weight the
+ * pages' large-M branch dequantises; fp8_w8a16_mm's own branch widens with s
+ * = 1, exactly, and scales the result instead).  W E4M3 [N,K], out bf16
+ * [N,K], both 16-byte aligned; K % 16 == 0.
+ * Errors: FP8_ERR_INVALID_ARG, FP8_ERR_ALIGNMENT, FP8_ERR_CUDA. */
+fp8_status fp8_widen_weight(const void *W, const float *scale_b, int granularity, int64_t N, int64_t K, void *out,
+                            void *stream);
 
 /* quant_fp8_static -- static per-tensor E4M3 quantisation, q = e4m3_rne_sat(x / s).
  *

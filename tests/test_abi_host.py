@@ -191,6 +191,30 @@ def test_quantiser_validation(L):
     assert L.rmsnorm_quant_fp8(GOOD, GOOD2, ctypes.c_float(1e-6), SC, GOOD3, 4, 24, None) == 2
 
 
+def test_w8a16_validation(L):
+    def w16(x=GOOD, W=GOOD2, sb=SC, gran=1, od=0, M=4, N=64, K=64, out=GOOD3, flags=0):
+        return L.fp8_w8a16_mm_ex(x, W, sb, gran, od, M, N, K, out, None, flags)
+    assert w16(M=0) == 0 and w16(M=0, x=None, out=None) == 0       # no-op, nothing launched
+    assert w16(M=-1) == 1 and w16(N=0) == 1 and w16(K=0) == 1 and w16(M=2 ** 31) == 1
+    assert w16(gran=2) == 1 and w16(gran=3) == 1 and w16(gran=4) == 1 and w16(gran=-1) == 1
+    assert w16(od=1) == 3
+    assert w16(flags=4) == 1
+    assert w16(x=None) == 1 and w16(W=None) == 1 and w16(sb=None) == 1 and w16(out=None) == 1
+    assert w16(x=P(0x10008)) == 2 and w16(W=P(0x20001)) == 2 and w16(out=P(0x30004)) == 2
+    assert w16(sb=P(0x40002)) == 2 and w16(K=72) == 2 and w16(N=68) == 2
+    assert L.fp8_w8a16_mm(GOOD, GOOD2, SC, 0, 0, 0, 64, 64, GOOD3, None) == 0
+    d = L.fp8_w8a16_describe_dispatch
+    assert d(0, 64, 64) == 0 and d(-1, 64, 64) == -1 and d(4, 0, 64) == -1
+    assert all(d(M, 10240, 5120) == 3 for M in (1, 16, 17, 32))
+    assert all(d(M, 10240, 5120) == 4 for M in (33, 64, 2048))
+    wd = L.fp8_widen_weight
+    assert wd(GOOD, SC, 1, 0, 64, GOOD3, None) == 0
+    assert wd(None, SC, 1, 4, 64, GOOD3, None) == 1 and wd(GOOD, None, 1, 4, 64, GOOD3, None) == 1
+    assert wd(GOOD, SC, 1, 4, 64, None, None) == 1 and wd(GOOD, SC, 2, 4, 64, GOOD3, None) == 1
+    assert wd(GOOD, SC, 1, -1, 64, GOOD3, None) == 1 and wd(GOOD, SC, 1, 4, 0, GOOD3, None) == 1
+    assert wd(GOOD, SC, 1, 4, 72, GOOD3, None) == 2 and wd(P(0x10008), SC, 1, 4, 64, GOOD3, None) == 2
+
+
 def test_describe_dispatch_is_pure(L):
     assert L.fp8_describe_dispatch(0, 64, 64, 0) == 0
     assert L.fp8_describe_dispatch(-1, 64, 64, 0) == -1

@@ -1,0 +1,169 @@
+"""GPU parity of the weight-only FP8 GEMM (W8A16: bf16 activations, E4M3
+weights) against the CPU oracle: the widen-on-chip decode kernel (M <= 32,
+every output), the large-M branch (the widened bf16 weight byte-exact, then
+the dense bf16 GEMM), and the invariants (determinism, dispatch, NaN codes)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from helpers import Guarded, bf16_bits_to_f64, host_bits, to_dev_bf16, to_dev_e4m3, to_dev_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp8():
+    import fp8_w8a8_scaled_gb300 as f
+    f.clear_device_error()
+    yield f
+    assert f.get_device_error() == 0
+
+
+def run_w16(fp8, x, W, sb, gran, flags=0):
+    M, N = x.shape[0], W.shape[0]
+    buf = Guarded(M * N * 2)
+    out = buf.view(torch.bfloat16, (M, N))
+    fp8.w8a16_mm(x, W, sb, gran, out=out, flags=flags)
+    torch.cuda.synchronize()
+    assert buf.intact(), "write outside the output buffer"
+    return host_bits(out)
+
+
+def _dec_bf16(bits):
+    return bf16_bits_to_f64(bits)
+
+
+def w16_bound(x_bits, W_codes, sb, per_channel, y64, orc, K, mma_k):
+    """Acceptance bound of the weight-only GEMM: 1e-2 |ref| + 1e-3 sa sb sqrt(K)
+    with sa = max_k |x[m,k]| / 448 (the scale a per-token quantisation of the
+    row would take), plus the binary32 accumulation bound of the tensor core's
+    sums of mma_k-wide chunks (ceil(K/mma_k) + 1) 2^-23 sb sum_k |x w|."""
+    xa = np.abs(_dec_bf16(x_bits))
+    sa = xa.max(axis=1) / 448.0
+    sbv = np.asarray(sb, np.float64).reshape(-1)
+    sbn = sbv if per_channel else np.full(W_codes.shape[0], sbv[0])
+    wabs = np.abs(orc.e4m3_decode(W_codes))
+    abs_sum = (xa @ wabs.T) * sbn[None, :]
+    acc = (-(-K // mma_k) + 1) * 2.0 ** -23 * abs_sum
+    return 1e-2 * np.abs(y64) + 1e-3 * sa[:, None] * sbn[None, :] * np.sqrt(K), acc
+
+
+def operands(seed, M, N, K, per_channel=True, weights="codes"):
+    g = workloads.rng(seed)
+    x = workloads.bf16_normal_with_outliers(g, (M, K))
+    if weights == "codes":
+        W = workloads.e4m3_codes(g, (N, K))
+        sb = workloads.uniform_f32(g, (N if per_channel else 1,), 0.5, 2.0) * np.float32(1e-3)
+    else:  # N(0, 0.02) weights quantised per channel by the oracle (amax / 448)
+        import oracle
+        w = workloads.bf16_normal(g, (N, K), std=0.02)
+        W, sb = oracle.quant_per_token(w if per_channel else w.reshape(1, -1))
+        W = W.reshape(N, K)
+    return x, W, np.asarray(sb, np.float32)
+
+
+def check(fp8, orc, x, W, sb, per_channel, what, flags=0):
+    M, K = x.shape
+    y = run_w16(fp8, to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb), 1 if per_channel else 0, flags)
+    y64, _ = orc.w8a16_mm(x, W, sb, per_channel)
+    bound, acc = w16_bound(x, W, sb, per_channel, y64, orc, K, 16)
+    yf = bf16_bits_to_f64(y)
+    err = np.abs(yf - y64)
+    assert not np.any(np.isnan(yf)), f"{what}: NaN"
+    bad = ~(err <= bound + acc)
+    ratio = float(np.max(err / np.where(bound > 0, bound, np.inf)))
+    assert int(bad.sum()) == 0, f"{what}: {int(bad.sum())} of {err.size} outside the bound (max {ratio:.3g})"
+    print(f"{what}: max err/bound {ratio:.4f}")
+    return y
+
+
+# ------------------------------------------------------------------ decode kernel (M <= 32)
+
+SHAPES = [(1, 8, 16), (3, 136, 272), (16, 128, 128), (5, 1032, 5120), (16, 264, 1040), (17, 136, 400),
+          (32, 1032, 2064), (24, 520, 1552)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("per_channel", [True, False])
+def test_w16_decode_random_codes(fp8, orc, M, N, K, per_channel):
+    assert fp8.w8a16_describe_dispatch(M, N, K) == fp8.KERNEL_W16_DECODE
+    x, W, sb = operands(9000 + M + N + K, M, N, K, per_channel)
+    check(fp8, orc, x, W, sb, per_channel, f"w16 {M}x{N}x{K} pc={per_channel}")
+
+
+@pytest.mark.parametrize("M", [1, 8, 16, 32])
+def test_w16_decode_qkv(fp8, orc, M):
+    """Merged QKV (N 10240, K 5120), per-channel quantised N(0, 0.02) weights,
+    every output."""
+    x, W, sb = operands(9100 + M, M, 10240, 5120, True, weights="quant")
+    check(fp8, orc, x, W, sb, True, f"w16 QKV M={M}", flags=fp8.FLAG_WEIGHTS_STATIC)
+
+
+def test_w16_decode_rerun_bitwise(fp8):
+    x, W, sb = operands(9200, 8, 2048, 5120)
+    xd, Wd, sbd = to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb)
+    y0 = run_w16(fp8, xd, Wd, sbd, 1)
+    for _ in range(3):
+        assert np.array_equal(run_w16(fp8, xd, Wd, sbd, 1), y0)
+
+
+def test_w16_rows_independent(fp8):
+    """Row m of an M=16 call against the same row alone: same tile, same K
+    division, so bitwise."""
+    x, W, sb = operands(9300, 16, 1032, 2064)
+    xd, Wd, sbd = to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb)
+    full = run_w16(fp8, xd, Wd, sbd, 1)
+    for m in (0, 9, 15):
+        assert np.array_equal(run_w16(fp8, xd[m:m + 1].contiguous(), Wd, sbd, 1)[0], full[m])
+
+
+def test_w16_nan_weight_code(fp8, orc):
+    x, W, sb = operands(9400, 4, 136, 272)
+    W[7, 100] = 0x7F
+    y = run_w16(fp8, to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb), 1)
+    assert np.all(np.isnan(bf16_bits_to_f64(y[:, 7])))
+    assert not np.any(np.isnan(bf16_bits_to_f64(np.delete(y, 7, axis=1))))
+
+
+def test_w16_m_zero(fp8):
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((64, 64), dtype=torch.float8_e4m3fn, device="cuda")
+    y = fp8.w8a16_mm(x, W, to_dev_f32([1.0]), 0)
+    assert y.shape == (0, 64)
+
+
+# ------------------------------------------------------------------ large-M branch
+
+@pytest.mark.parametrize("per_channel", [True, False])
+def test_widen_weight_bitexact(fp8, orc, per_channel):
+    g = workloads.rng(9500)
+    W = workloads.e4m3_codes(g, (300, 400))
+    W[3, 5] = 0x7F
+    W[4, 6] = 0xFF
+    sb = (g.uniform(0.25, 4.0, 300 if per_channel else 1) * 1e-3).astype(np.float32)
+    out = fp8.widen_weight(to_dev_e4m3(W), to_dev_f32(sb), 1 if per_channel else 0)
+    torch.cuda.synchronize()
+    want = orc.dequant_weight_bf16(W, sb, per_channel)
+    got = host_bits(out)
+    nan_w = (want & 0x7F80) == 0x7F80
+    assert np.array_equal(got[~nan_w], want[~nan_w])
+    assert np.all((got[nan_w] & 0x7F80) == 0x7F80) and np.all((got[nan_w] & 0x7F) != 0)
+
+
+@pytest.mark.parametrize("M,N,K", [(33, 136, 272), (64, 1032, 2064), (300, 520, 1040)])
+@pytest.mark.parametrize("per_channel", [True, False])
+def test_w16_dense_branch(fp8, orc, M, N, K, per_channel):
+    """Large M: the exactly widened weight in a dense bf16 GEMM (fp32
+    accumulation, bf16 result), then the scale: against the method's exact
+    result with the acceptance bound, plus the recursive-summation bound of the
+    GEMM's binary32 accumulation ((K + 1) 2^-23 sb sum |x w|), plus one bf16
+    rounding of the unscaled result (2^-8 of it, before the scale)."""
+    assert fp8.w8a16_describe_dispatch(M, N, K) == fp8.KERNEL_W16_DENSE
+    x, W, sb = operands(9600 + M, M, N, K, per_channel, weights="quant")
+    y = bf16_bits_to_f64(run_w16(fp8, to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb), 1 if per_channel else 0))
+    y64, _ = orc.w8a16_mm(x, W, sb, per_channel)
+    bound, acc = w16_bound(x, W, sb, per_channel, y64, orc, K, 1)
+    err = np.abs(y - y64)
+    assert np.all(err <= bound + acc + 2.0 ** -8 * np.abs(y64))
+    print(f"w16 dense {M}x{N}x{K} pc={per_channel}: max err/acceptance bound {float(np.max(err / bound)):.4f}")
