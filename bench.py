@@ -113,7 +113,8 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-DECODE_KERNEL_SOURCES = ("fp8_w8a8_scaled_gb300/csrc/gemm_decode.cu", "fp8_w8a8_scaled_gb300/csrc/ptx.cuh")
+DECODE_KERNEL_SOURCES = ("fp8_w8a8_scaled_gb300/csrc/gemm_decode.cu", "fp8_w8a8_scaled_gb300/csrc/splitk.cuh",
+                         "fp8_w8a8_scaled_gb300/csrc/ptx.cuh")
 TRAFFIC_RECORD = "profiles/decode_gemm_qkv_10240x5120.md"
 
 

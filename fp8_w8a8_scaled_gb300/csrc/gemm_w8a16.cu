@@ -10,18 +10,17 @@
 // Design (GB300, sm_103a).  The tensor core's kind::f16 takes both operands in
 // one 16-bit type, so the E4M3 weight tile is widened to bf16 (exact: every
 // E4M3 value is a bf16 value) in shared memory before the MMA reads it.
-// Units are (128-row output tile) x (128-wide k-block), divided among one
-// persistent CTA per SM as in the W8A8 kernel's stream-K mode (one CTA per SM:
-// the widened tiles take 128 KB of shared memory beside the ring).  Inside a
+// Units are (128-row output tile) x (128-wide k-block), divided among
+// persistent CTAs as in the W8A8 kernel's stream-K mode: two per SM for the
+// 16-token tile (one widened tile each), one for the 32-token tile.  Inside a
 // CTA:
 //   * warp 0 / lane 0 streams each unit's 128 x 128-byte E4M3 weight box and
 //     its two TOK x 64-element bf16 token boxes with TMA into a ring of stages
 //     (128-byte swizzle);
-//   * warps 6-13 (two warpgroups, half of each weight row per thread; one
-//     warpgroup, whole rows, for the 32-token tile) widen
-//     each unit's E4M3 tile into one of four bf16 A tiles, laid out as the MMA
-//     reads them (two 64-element K halves of 128 rows x 128 bytes, 128-byte
-//     swizzled), up to four units ahead of the MMA;
+//   * warps 6-9, one weight row per thread, widen each unit's E4M3 tile into
+//     a bf16 A tile (one or two in flight), laid out as the MMA reads them
+//     (two 64-element K halves of 128 rows x 128 bytes, 128-byte swizzled),
+//     and release the weight stage at once;
 //   * warps 2-5 drain each unit's fp32 partial out of TMEM into TwoSum
 //     registers -- the same drain, tile store and stream-K fix-up as the W8A8
 //     decode kernel;
@@ -47,21 +46,23 @@ constexpr uint32_t kW16ATileBytes = 2 * kW16Region;            // the widened 12
 
 template <int TOK>
 struct W16Cfg {
-    // producer warp, MMA warp, one drain warpgroup, kWidenGroups widening
-    // warpgroups (each thread widens its row's share of the 8 chunks); one for
-    // the 32-token tile, whose drain needs the registers of a 10-warp CTA
-    static constexpr int kWidenGroups = TOK <= 16 ? 2 : 1;
+    // producer warp, MMA warp, one drain warpgroup, one widening warpgroup
+    // (each thread widens one weight row); kWidenGroups > 1 splits the rows'
+    // chunks between several (two were slower than two CTAs per SM of one)
+    static constexpr int kWidenGroups = 1;
     static constexpr int kThreads = 64 + 128 + 128 * kWidenGroups;
     // registers a thread may use with one CTA per SM: a sub-partition holds
     // ceil(warps / 4) of its warps, 16384 registers each
-    static constexpr int kMaxRegs = (16384 / (32 * ((kThreads / 32 + 3) / 4))) / 8 * 8;
+    // registers per thread: two CTAs per SM for the 16-token tile (10 warps
+    // each: 5 per sub-partition), one for the 32-token tile, whose drain needs more
+    static constexpr int kMaxRegs = TOK <= 16 ? 96 : 168;
     static constexpr int kDrainThreads = 128;
     static constexpr int kBufs = TOK <= 16 ? 8 : 4;              // TMEM accumulators (must match w16_tmem_bufs)
     static constexpr uint32_t kTmemCols = kBufs * TOK < 32 ? 32 : kBufs * TOK;
     static constexpr uint32_t kXRegion = TOK * 128;              // 64 bf16 of K for TOK tokens
     static constexpr uint32_t kXStageBytes = 2 * kXRegion;       // one unit's token tile
-    static constexpr int kXStages = 8;                           // token ring (>= the weight ring)
-    static constexpr int kABufs = TOK <= 16 ? 3 : 2;             // widened tiles ahead of the MMA
+    static constexpr int kXStages = TOK <= 16 ? 4 : 8;          // token ring (>= the weight ring)
+    static constexpr int kABufs = TOK <= 16 ? 1 : 2;             // widened tiles ahead of the MMA
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kDecodeRows, TOK);
 };
 
@@ -484,7 +485,7 @@ __global__ void __launch_bounds__(256) scale_columns_kernel(uint4 *__restrict__ 
 // Shared memory of one CTA: alignment slack, the weight ring, the token ring,
 // the widened weight tiles and the mbarriers (rounded up).
 static size_t w16_smem_bytes(int tok, int stages) {
-    const int nb = tok <= 16 ? 8 : 4, nx = W16Cfg<16>::kXStages, na = tok <= 16 ? W16Cfg<16>::kABufs
+    const int nb = tok <= 16 ? 8 : 4, nx = tok <= 16 ? W16Cfg<16>::kXStages : W16Cfg<32>::kXStages, na = tok <= 16 ? W16Cfg<16>::kABufs
                                                                                  : W16Cfg<32>::kABufs;
     const size_t barriers = 8u * static_cast<size_t>(2 * stages + 2 * nx + 2 * nb + 2 * na + 1);
     return 1024 + static_cast<size_t>(stages) * kW16WeightBytes + static_cast<size_t>(nx) * 2u * tok * 128u +
@@ -494,17 +495,19 @@ static size_t w16_smem_bytes(int tok, int stages) {
 DecodePlan plan_w8a16(int64_t M, int64_t N, int64_t K, int num_sms) {
     DecodePlan p{};
     p.tok_pad = M <= 16 ? 16 : 32;
-    p.stages = 6;  // 96 KB of weights in flight: 225 KB of shared memory with the token ring and widened tiles
+    // 16 tokens: 3 weight stages, 4 token stages, one widened tile (97 KB, two
+    // CTAs per SM); 32 tokens: 6, 8 and two (225 KB, one CTA per SM)
+    p.stages = p.tok_pad == 16 ? 3 : 6;
     p.smem_bytes = w16_smem_bytes(p.tok_pad, p.stages);
     p.n_tiles = static_cast<int>((N + kDecodeRows - 1) / kDecodeRows);
     p.m_tiles = static_cast<int>((M + p.tok_pad - 1) / p.tok_pad);
     p.kb_total = static_cast<int>((K + kBlockK - 1) / kBlockK);
     p.units = static_cast<int64_t>(p.n_tiles) * p.m_tiles * p.kb_total;
     p.split = 0;
-    // One persistent CTA per SM, at least kb_total / (kMaxFixupSegs - 1)
-    // units each (at most kMaxFixupSegs CTAs share a tile).
+    // Persistent CTAs (two or one per SM), at least kb_total / (kMaxFixupSegs
+    // - 1) units each (at most kMaxFixupSegs CTAs share a tile).
     const int64_t min_units = (p.kb_total + kMaxFixupSegs - 2) / (kMaxFixupSegs - 1);
-    int64_t ctas = num_sms;
+    int64_t ctas = p.tok_pad == 16 ? 2 * static_cast<int64_t>(num_sms) : num_sms;
     if (ctas > p.units / min_units) ctas = p.units / min_units;
     if (ctas < 1) ctas = 1;
     p.ctas = static_cast<int>(ctas);
