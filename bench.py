@@ -677,12 +677,23 @@ def run_profile_case(args):
     sb = workloads.device_uniform_f32(torch, (N,), 0.5e-3, 2e-3, seed=400, device=dev)
     A = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    kind = args.profile_kind
+    if kind == "blockwise":  # per-token-group activations x 128x128-block weights
+        sag = torch.empty((M, (K + 127) // 128), dtype=torch.float32, device=dev)
+        sbb = workloads.device_uniform_f32(torch, ((N + 127) // 128, (K + 127) // 128), 0.5e-3, 2e-3, seed=401,
+                                           device=dev)
     for i in range(args.steps):
-        fp8.rmsnorm_quant_fp8(x, gamma, workloads.RMS_EPS, s_a, out=A)
-        fp8.fp8_scaled_mm(A, W[i % 3], s_a, sb, fp8.GRAN_PER_CHANNEL, out=Y)
+        if kind == "w8a16":  # bf16 activations, E4M3 weights: no activation quantisation
+            fp8.w8a16_mm(x, W[i % 3], sb, fp8.GRAN_PER_CHANNEL, out=Y)
+        elif kind == "blockwise":
+            fp8.quant_per_token_group(x, out=A, scale_out=sag)
+            fp8.fp8_scaled_mm(A, W[i % 3], sag, sbb, fp8.GRAN_BLOCK_128, out=Y)
+        else:
+            fp8.rmsnorm_quant_fp8(x, gamma, workloads.RMS_EPS, s_a, out=A)
+            fp8.fp8_scaled_mm(A, W[i % 3], s_a, sb, fp8.GRAN_PER_CHANNEL, out=Y)
     torch.cuda.synchronize()
     err = fp8.get_device_error()
-    print(json.dumps({"profile_case": [M, N, K], "launches": 2 * args.steps, "device_error": err}))
+    print(json.dumps({"profile_case": [M, N, K], "kind": kind, "device_error": err}))
     if err:
         raise SystemExit(1)
 
@@ -700,6 +711,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the gate_up decode, 64-layer decode step and tiny GEMM measurements")
     ap.add_argument("--profile", metavar="M,N,K", help="run a small eager case for a profiler and exit")
+    ap.add_argument("--profile-kind", choices=("w8a8", "w8a16", "blockwise"), default="w8a8",
+                    help="the GEMM of the --profile case: per-channel W8A8 after the norm-quant (default), "
+                         "weight-only W8A16, or blockwise-scaled W8A8 after the per-token-group quant")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args)

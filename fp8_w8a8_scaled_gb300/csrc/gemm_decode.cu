@@ -425,14 +425,34 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
             cluster_sync();
             if (warp >= 2) {
                 const float *red = reinterpret_cast<const float *>(smem_raw + (red_base - raw));
-                for (int e = static_cast<int>(tid) - 64; e < nr * mt; e += Cfg::kDrainThreads) {
-                    const int m = e / nr, lr = e - m * nr;  // consecutive threads: consecutive channels
-                    const int n = tile * kDecodeRows + rb + lr;
-                    float h = 0.0f, l = 0.0f;
-                    for (int src = 0; src < S; ++src) two_sum_acc(h, l, red[(src * TOK + m) * red_rows + lr]);
-                    if (n < args.N)
-                        args.out[static_cast<int64_t>(m) * args.N + n] =
-                            __float2bfloat16_rn(__fmul_rn(__fmul_rn(__fadd_rn(h, l), s_red_sa[m]), s_red_sb[lr]));
+                // kR entries per thread per round, all their shared-memory
+                // reads issued before any sum (the parts of one entry form a
+                // dependent chain); consecutive threads: consecutive channels
+                constexpr int kR = 4;
+                const int entries = nr * mt;
+                for (int e0 = static_cast<int>(tid) - 64; e0 < entries; e0 += kR * Cfg::kDrainThreads) {
+                    float v[kR][kMaxClusterParts];
+                    int mm[kR], ll[kR];
+#pragma unroll
+                    for (int q = 0; q < kR; ++q) {
+                        const int e = min(e0 + q * Cfg::kDrainThreads, entries - 1);
+                        mm[q] = e / nr;
+                        ll[q] = e - mm[q] * nr;
+#pragma unroll
+                        for (int src = 0; src < kMaxClusterParts; ++src)
+                            if (src < S) v[q][src] = red[(src * TOK + mm[q]) * red_rows + ll[q]];
+                    }
+#pragma unroll
+                    for (int q = 0; q < kR; ++q) {
+                        float h = 0.0f, l = 0.0f;
+#pragma unroll
+                        for (int src = 0; src < kMaxClusterParts; ++src)
+                            if (src < S) two_sum_acc(h, l, v[q][src]);
+                        const int n = tile * kDecodeRows + rb + ll[q];
+                        if (e0 + q * Cfg::kDrainThreads < entries && n < args.N)
+                            args.out[static_cast<int64_t>(mm[q]) * args.N + n] = __float2bfloat16_rn(
+                                __fmul_rn(__fmul_rn(__fadd_rn(h, l), s_red_sa[mm[q]]), s_red_sb[ll[q]]));
+                    }
                 }
             }
         }
@@ -495,7 +515,7 @@ static size_t decode_smem_bytes(int tok, int stages, int split) {
 // us per launch and 4-CTA ones (320 CTAs) 22 us, the latter leaving SMs idle
 // and starting some clusters only after others had finished; on N 5120 (40
 // tiles) 6-CTA clusters took 12.0 us and 8-CTA ones 19.4 us.
-constexpr int kMaxClusterSplit = 8;
+constexpr int kMaxClusterSplit = kMaxClusterParts;
 
 DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, int num_sms) {
     DecodePlan p{};

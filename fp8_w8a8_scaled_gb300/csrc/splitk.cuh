@@ -41,6 +41,9 @@ struct DecodeArgs {
     int split;  // cluster mode: CTAs (one cluster) per tile; 0 in stream-K mode
 };
 
+// Cluster mode: at most this many CTAs (parts) per tile.
+constexpr int kMaxClusterParts = 8;
+
 // Cluster mode: rows [red_row_begin(q, S), red_row_begin(q + 1, S)) of a tile
 // are summed by CTA q of the tile's cluster; at most ceil(128 / S) of them.
 __host__ __device__ __forceinline__ int red_row_begin(int q, int S) { return (q * kDecodeRows + S - 1) / S; }
