@@ -540,7 +540,7 @@ def run_ours(args, rank, world, dist_barrier, dist_max):
     ms = dist_max(time_graph(torch, step_graph, reps, dist_barrier))
     clk = clocks.stop()
     ms_step = ms / steps
-    value = world * step_bytes() / (ms_step * 1e-3) / 1e12
+    value = whole_job_tbps(world, step_bytes(), ms_step)
 
     # roofline of the dominant kernel: the GEMM launches alone, same rotation
     for _ in range(warm):
@@ -596,7 +596,7 @@ def run_ours(args, rank, world, dist_barrier, dist_max):
                      "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": recorded_traffic(),
                      "traffic_source": TRAFFIC_RECORD,
                      "bytes_per_launch": gbytes, "us_per_launch": round(per_launch_ms * 1e3, 3)},
-        "e2e": {"value": round(world * step_bytes() / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TB/s",
+        "e2e": {"value": round(whole_job_tbps(world, step_bytes(), e2e_ms), 4), "unit": "TB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6)},
         "gpu_launches": steps * 2 * len(MS),
         "clocks": clk,
@@ -708,6 +708,31 @@ def run_profile_case(args):
         raise SystemExit(1)
 
 
+def whole_job_tbps(world, bytes_per_step, ms_per_step):
+    """The whole job's rate: every rank runs the same step (replicas), so the
+    bytes of all ranks over the slowest rank's step time."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e12
+
+
+def dist_ops(dist, device):
+    """A barrier and a max over ranks of one float, through the process group
+    `dist` (None: one process); `device` holds the reduced tensor ("cuda" for
+    NCCL, "cpu" for gloo)."""
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def dmax(v):
+        if dist is None:
+            return v
+        import torch
+        t = torch.tensor([float(v)], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    return barrier, dmax
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -744,18 +769,7 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
-    def dmax(v):
-        if dist is None:
-            return v
-        import torch
-        t = torch.tensor([float(v)], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
+    barrier, dmax = dist_ops(dist, "cuda")
     out = run_ours(args, rank, world, barrier, dmax)
     if rank == 0:
         print(json.dumps(out), flush=True)
