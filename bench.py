@@ -160,24 +160,30 @@ class DecodeFusedStep:
         self.x = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
         self.gamma = torch.from_numpy(gamma.view(np.int16)).view(torch.bfloat16).to(device)
         self.s_a = torch.tensor([float(workloads.STATIC_INPUT_SCALE)], dtype=torch.float32, device=device)
-        self.W, self.sb, self.A, self.Y = [], [], [], []
-        # the outputs of all M are rows of one buffer, so that one copy reads them back
-        self.Y_all = torch.empty((sum(MS), N_QKV), dtype=torch.bfloat16, device=device)
+        self.W, self.sb, self.A = [], [], []
+        # the outputs of all M are rows of one buffer, so that one copy reads
+        # them back; two such buffers, so that a step's read-back can overlap
+        # the next step (the end-to-end loop alternates them)
+        self.Y_all = [torch.empty((sum(MS), N_QKV), dtype=torch.bfloat16, device=device) for _ in range(2)]
+        self.Y2 = [[], []]
         row = 0
         for i, m in enumerate(MS):
             self.W.append(workloads.device_e4m3_codes(torch, (N_QKV, K_HID), seed=100 + i, device=device)
                           .view(torch.float8_e4m3fn))
             self.sb.append(workloads.device_uniform_f32(torch, (N_QKV,), 0.5e-3, 2e-3, seed=200 + i, device=device))
             self.A.append(torch.empty((m, K_HID), dtype=torch.float8_e4m3fn, device=device))
-            self.Y.append(self.Y_all[row:row + m])
+            for b in range(2):
+                self.Y2[b].append(self.Y_all[b][row:row + m])
             row += m
+        self.Y = self.Y2[0]
 
-    def launch_step(self):
+    def launch_step(self, buf=0, x=None):
         fp8 = self.fp8
+        x = self.x if x is None else x
         for i, m in enumerate(MS):
-            fp8.rmsnorm_quant_fp8(self.x[:m], self.gamma, workloads.RMS_EPS, self.s_a, out=self.A[i])
-            fp8.fp8_scaled_mm(self.A[i], self.W[i], self.s_a, self.sb[i], fp8.GRAN_PER_CHANNEL, out=self.Y[i],
-                              flags=fp8.FLAG_WEIGHTS_STATIC)
+            fp8.rmsnorm_quant_fp8(x[:m], self.gamma, workloads.RMS_EPS, self.s_a, out=self.A[i])
+            fp8.fp8_scaled_mm(self.A[i], self.W[i], self.s_a, self.sb[i], fp8.GRAN_PER_CHANNEL,
+                              out=self.Y2[buf][i], flags=fp8.FLAG_WEIGHTS_STATIC)
 
     def decode_ms(self):
         """The M values the weight-streaming decode kernel serves."""
@@ -192,6 +198,20 @@ class DecodeFusedStep:
                 continue
             fp8.fp8_scaled_mm(self.A[i], self.W[i], self.s_a, self.sb[i], fp8.GRAN_PER_CHANNEL, out=self.Y[i],
                               flags=fp8.FLAG_WEIGHTS_STATIC)
+
+    def capture_once(self, fn):
+        """fn (which records INNER steps itself) run once, then captured."""
+        torch = self.torch
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        torch.cuda.synchronize(self.device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        return graph
 
     def capture(self, fn, inner):
         torch = self.torch
@@ -553,16 +573,50 @@ def run_ours(args, rank, world, dist_barrier, dist_max):
     peak, peak_src = measured_peaks()
 
     # end to end through the public API with host buffers: every step copies
-    # x in from pinned host memory, runs the step and copies all its outputs
-    # back (one copy each way, captured with the step in the replayed graph)
+    # its x in from pinned host memory, runs and copies all its outputs back
+    # (one copy each way), captured with the steps in the replayed graph.  The
+    # copies run on a second stream and overlap the neighbouring steps' work,
+    # as a serving loop would: step j reads input buffer j % 2 (copied in
+    # while step j - 1 computes) and writes output buffer j % 2 (copied out
+    # while step j + 1 computes).
     x_host = step.x.cpu().pin_memory()
-    y_host = torch.empty(step.Y_all.shape, dtype=step.Y_all.dtype).pin_memory()
+    x_dev = [step.x, torch.empty_like(step.x)]
+    y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in step.Y_all]
+    side = torch.cuda.Stream(device=device)
+    read_back = [torch.cuda.Event(), torch.cuda.Event()]  # output buffer b copied to the host
+    loaded = [torch.cuda.Event(), torch.cuda.Event()]     # input buffer b copied from the host
+    consumed = [torch.cuda.Event(), torch.cuda.Event()]   # the step that read input buffer b is done
 
-    def e2e_step():
-        step.x.copy_(x_host, non_blocking=True)
-        step.launch_step()
-        y_host.copy_(step.Y_all, non_blocking=True)
-    one = step.capture(e2e_step, INNER)
+    def copy_in(j):
+        b = j % 2
+        with torch.cuda.stream(side):
+            if j >= 2:
+                side.wait_event(consumed[b])  # step j - 2 has finished reading buffer b
+            x_dev[b].copy_(x_host, non_blocking=True)
+            loaded[b].record(side)
+
+    def e2e_step(j):
+        b = j % 2
+        main = torch.cuda.current_stream(device)
+        main.wait_event(loaded[b])
+        if j >= 2:
+            main.wait_event(read_back[b])  # step j - 2's outputs have left output buffer b
+        if j + 1 < INNER:
+            copy_in(j + 1)                 # the next step's input, while this step computes
+        step.launch_step(b, x_dev[b])
+        consumed[b].record(main)
+        side.wait_event(consumed[b])
+        with torch.cuda.stream(side):
+            y_host[b].copy_(step.Y_all[b], non_blocking=True)
+            read_back[b].record(side)
+
+    def e2e_steps():
+        side.wait_stream(torch.cuda.current_stream(device))
+        copy_in(0)
+        for j in range(INNER):
+            e2e_step(j)
+        torch.cuda.current_stream(device).wait_stream(side)
+    one = step.capture_once(e2e_steps)
     for _ in range(warm):
         one.replay()
     e2e_reps = max(1, min(reps, 2000 // INNER))
@@ -576,7 +630,7 @@ def run_ours(args, rank, world, dist_barrier, dist_max):
     torch.cuda.synchronize()
     e2e_ms = dist_max(e0.elapsed_time(e1)) / (e2e_reps * INNER)
     h2d = step.x.numel() * 2
-    d2h = step.Y_all.numel() * 2
+    d2h = step.Y_all[0].numel() * 2
     err = fp8.get_device_error()
     if err:
         raise RuntimeError(f"device error word {err:#x}")
