@@ -423,35 +423,29 @@ __global__ void __launch_bounds__(DecodeCfg<TOK>::kThreads) __maxnreg__(DecodeCf
             // every part of every row this CTA sums has landed (and no CTA of
             // the cluster touches another's shared memory after this point)
             cluster_sync();
-            if (warp >= 2) {
-                const float *red = reinterpret_cast<const float *>(smem_raw + (red_base - raw));
-                // kR entries per thread per round, all their shared-memory
-                // reads issued before any sum (the parts of one entry form a
-                // dependent chain); consecutive threads: consecutive channels
-                constexpr int kR = 4;
-                const int entries = nr * mt;
-                for (int e0 = static_cast<int>(tid) - 64; e0 < entries; e0 += kR * Cfg::kDrainThreads) {
-                    float v[kR][kMaxClusterParts];
-                    int mm[kR], ll[kR];
-#pragma unroll
-                    for (int q = 0; q < kR; ++q) {
-                        const int e = min(e0 + q * Cfg::kDrainThreads, entries - 1);
-                        mm[q] = e / nr;
-                        ll[q] = e - mm[q] * nr;
+            {
+                // Every thread of the CTA (the producer and MMA warps are done
+                // too) takes one of this CTA's rows and every g-th token
+                // column; consecutive threads: consecutive channels.
+                const int groups = Cfg::kThreads / nr;  // nr <= 64 < kThreads
+                const int lr = static_cast<int>(tid) % nr, m0 = static_cast<int>(tid) / nr;
+                const int n = tile * kDecodeRows + rb + lr;
+                if (m0 < groups && n < args.N) {
+                    const float sb = s_red_sb[lr];
+                    __nv_bfloat16 *o = args.out + static_cast<int64_t>(m0) * args.N + n;
+                    const int64_t ostep = static_cast<int64_t>(groups) * args.N;
+#pragma unroll 4
+                    for (int m = m0; m < mt; m += groups, o += ostep) {
+                        float v[kMaxClusterParts];
 #pragma unroll
                         for (int src = 0; src < kMaxClusterParts; ++src)
-                            if (src < S) v[q][src] = red[(src * TOK + mm[q]) * red_rows + ll[q]];
-                    }
-#pragma unroll
-                    for (int q = 0; q < kR; ++q) {
+                            if (src < S)
+                                v[src] = lds_f32(red_base + 4u * static_cast<uint32_t>((src * TOK + m) * red_rows + lr));
                         float h = 0.0f, l = 0.0f;
 #pragma unroll
                         for (int src = 0; src < kMaxClusterParts; ++src)
-                            if (src < S) two_sum_acc(h, l, v[q][src]);
-                        const int n = tile * kDecodeRows + rb + ll[q];
-                        if (e0 + q * Cfg::kDrainThreads < entries && n < args.N)
-                            args.out[static_cast<int64_t>(mm[q]) * args.N + n] = __float2bfloat16_rn(
-                                __fmul_rn(__fmul_rn(__fadd_rn(h, l), s_red_sa[mm[q]]), s_red_sb[ll[q]]));
+                            if (src < S) two_sum_acc(h, l, v[src]);
+                        *o = __float2bfloat16_rn(__fmul_rn(__fmul_rn(__fadd_rn(h, l), s_red_sa[m]), sb));
                     }
                 }
             }
