@@ -113,6 +113,8 @@ def lib():
     L.fp8_decode_ctas_for_sms.restype = I32
     L.fp8_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     L.fp8_get_device_error.restype = I32
+    L.fp8_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P]
+    L.fp8_selftest_bounded_wait.restype = I32
     L.fp8_clear_device_error.argtypes = []
     L.fp8_clear_device_error.restype = I32
     L.fp8_library_version.argtypes = []
@@ -452,6 +454,13 @@ def decode_split(M, N, K, num_sms=None) -> int:
     if num_sms is None:
         num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     return lib().fp8_decode_split_for_sms(M, N, K, int(num_sms))
+
+
+def selftest_bounded_wait(timeout_us=1000):
+    """Launch the failure-path self-test (a bounded wait nothing completes)."""
+    dev = torch.cuda.current_device()
+    _check(lib().fp8_selftest_bounded_wait(int(timeout_us), ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)),
+           "fp8_selftest_bounded_wait")
 
 
 def get_device_error(stream=None) -> int:

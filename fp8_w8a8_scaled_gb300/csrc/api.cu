@@ -13,6 +13,7 @@
 
 #include "../../include/fp8w8a8.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -20,6 +21,20 @@ namespace {
 // per device that loads the library); host code reaches it only through the
 // address cudaGetSymbolAddress returns with that device current.
 __device__ uint32_t g_error_word;
+
+// fp8_selftest_bounded_wait's kernel: one thread waits, with the kernels'
+// bounded wait, on an mbarrier phase that nothing completes; the wait gives up
+// after timeout_ns, sets kErrSelfTestWait in the error word and the kernel
+// returns normally.
+__global__ void bounded_wait_probe_kernel(uint32_t *err, unsigned long long timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        const uint32_t b = fp8k::smem_u32(&bar);
+        fp8k::mbar_init(b, 1);  // one arrival would complete phase 0; none comes
+        fp8k::fence_mbar_init();
+        fp8k::mbar_wait_for(b, 0, err, fp8k::kErrSelfTestWait, timeout_ns);
+    }
+}
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kI32Max = 2147483647;
@@ -569,6 +584,16 @@ fp8_status fp8_get_device_error(void *stream, uint32_t *word) {
     if (cudaMemcpy(&w, st->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return FP8_ERR_CUDA;
     if (word) *word = w;
     return w ? FP8_ERR_DEVICE : FP8_OK;
+}
+
+fp8_status fp8_selftest_bounded_wait(uint32_t timeout_us, void *stream) {
+    if (timeout_us < 1 || timeout_us > 2000000u) return FP8_ERR_INVALID_ARG;
+    DeviceState *st = nullptr;
+    fp8_status s = device_state(&st);
+    if (s != FP8_OK) return s;
+    bounded_wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        st->err, static_cast<unsigned long long>(timeout_us) * 1000ull);
+    return from_cuda(cudaGetLastError());
 }
 
 fp8_status fp8_clear_device_error(void) {

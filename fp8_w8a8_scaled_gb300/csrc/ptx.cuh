@@ -24,6 +24,7 @@ enum : uint32_t {
     kErrW16FullWait = 1u << 10,     // weight-only kernel: a stage's TMA loads
     kErrW16AEmptyWait = 1u << 11,   // weight-only kernel: a widened weight tile freed by the MMA
     kErrW16AFullWait = 1u << 12,    // weight-only kernel: a widened weight tile written
+    kErrSelfTestWait = 1u << 13,    // fp8_selftest_bounded_wait: the wait nothing completes
     kErrPrefillFullWait = 1u << 4,
     kErrPrefillEmptyWait = 1u << 5,
     kErrPrefillAccumWait = 1u << 6,
@@ -87,22 +88,28 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 }
 
 // Waits for the phase with the given parity to complete.  Returns false (and
-// sets `code` in *err) if it has not completed after kWaitTimeoutNs.  Waiting
+// sets `code` in *err) if it has not completed after timeout_ns (mbar_wait:
+// kWaitTimeoutNs).  Waiting
 // threads sleep in the barrier instead of spinning, so they take no issue
 // slots from the warps that do the work (the hardware wakes them when the
 // phase completes).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err, uint32_t code) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint32_t *err, uint32_t code,
+                                              unsigned long long timeout_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
             if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        if (globaltimer_ns() - t0 > timeout_ns) {
             atomicOr(err, code);
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err, uint32_t code) {
+    return mbar_wait_for(bar, parity, err, code, kWaitTimeoutNs);
 }
 
 // --------------------------------------------------------------------- TMA --

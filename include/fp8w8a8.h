@@ -430,6 +430,14 @@ int fp8_decode_split_for_sms(int64_t M, int64_t N, int64_t K, int num_sms);
 fp8_status fp8_get_device_error(void *stream, uint32_t *word);
 fp8_status fp8_clear_device_error(void);
 
+/* Self-test of the failure path: launches one thread that waits, with the
+ * kernels' own bounded wait, for an mbarrier phase that nothing completes.
+ * After timeout_us (1 .. 2,000,000) it gives up, sets bit 13 (0x2000) of the
+ * device error word and returns, so the context stays usable; a following
+ * fp8_get_device_error reports FP8_ERR_DEVICE with that bit.  No fault, trap
+ * or hang is involved.  Errors: FP8_ERR_INVALID_ARG, FP8_ERR_CUDA. */
+fp8_status fp8_selftest_bounded_wait(uint32_t timeout_us, void *stream);
+
 /* Makes `device` the current device of this library's CUDA runtime for the
  * calling thread (the library links its own copy of the runtime, so a host
  * program that switches devices through another runtime tells it here).

@@ -215,6 +215,12 @@ def test_w8a16_validation(L):
     assert wd(GOOD, SC, 1, 4, 72, GOOD3, None) == 2 and wd(P(0x10008), SC, 1, 4, 64, GOOD3, None) == 2
 
 
+def test_selftest_validation(L):
+    L.fp8_selftest_bounded_wait.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
+    assert L.fp8_selftest_bounded_wait(0, None) == 1
+    assert L.fp8_selftest_bounded_wait(3000000, None) == 1
+
+
 def test_describe_dispatch_is_pure(L):
     assert L.fp8_describe_dispatch(0, 64, 64, 0) == 0
     assert L.fp8_describe_dispatch(-1, 64, 64, 0) == -1
