@@ -172,7 +172,7 @@ fp8_status w16_buffer(DeviceState *st, size_t bytes, void **out) {
 }
 
 // The decode kernel's workspace for this device: sized for the largest plan
-// (two CTAs per SM, 64-token tiles), allocated and zeroed on first use.
+// (two CTAs per SM, 32-token tiles), allocated and zeroed on first use.
 fp8_status decode_workspace(DeviceState *st, const fp8k::DecodePlan &plan, fp8k::DecodeWorkspace *ws) {
     if (fp8k::decode_counters_needed(plan) > kWsCounters) return FP8_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mu);

@@ -68,7 +68,7 @@ struct DecodeCfg {
     static constexpr int kDrainThreads = 128 * kDrainGroups;
     static constexpr int kThreads = 64 + kDrainThreads;
     // two CTAs of this kernel plus one of the next (programmatic launch) per SM
-    // for the 16-token tile; two per SM for the larger tiles
+    // for the 16-token tile; two per SM for the 32-token tile
     static constexpr int kMinBlocks = TOK <= 16 ? 3 : 2;
     static constexpr int kMaxRegs = (65536 / (kMinBlocks * kThreads)) / 8 * 8;
     // TMEM accumulators in flight between the MMA and the drain (the MMA can
