@@ -14,9 +14,14 @@
 // m^2 * 2^(2E - 268) with m < 256, so the squares of the row's top 40 binades
 // are added as integers into a 128-bit fixed-point accumulator (2^94 per term
 // at most, 2^110 for 2^16 terms), and any nonzero smaller term only sets a
-// sticky bit -- all terms are non-negative and smaller than 2^-61 of the sum,
-// so the sticky bit is all the rounding needs.  The exact sum is rounded once
-// to binary32, then mean = ss / K, t = mean + eps, d = sqrt(t), r = 1 / d are
+// sticky bit.  The smaller terms add up to less than K * 2^14 units of the
+// window's lowest bit, far below the rounding position (at least 2^69 units
+// once a term lies below the window), so they can change the rounding only by
+// a carry through a run of one bits from just below the guard bit down to
+// that bound.  That case -- astronomically rare in data, but constructible --
+// is detected, and the row is then summed exactly by one thread over the full
+// exponent range (sticky_may_carry, exact_row_sum_squares).  The exact sum is
+// rounded once to binary32, then mean = ss / K, t = mean + eps, d = sqrt(t), r = 1 / d are
 // single IEEE binary32 operations; the two multiplies are separate binary32
 // operations (the library is compiled without FMA contraction), bf16 and E4M3
 // conversions round to nearest even (the E4M3 one saturating).
@@ -83,8 +88,9 @@ __device__ __forceinline__ void bf16_split(uint32_t b, uint32_t &m, int &E) {
 
 // Shared scratch of one row group's reductions (one entry per warp).
 struct RowScratch {
-    uint64_t red_hi[32], red_lo[32];
-    int red_i[32];
+    uint32_t red_limb[5][32];  // per warp: 24-bit limbs of its partial sum
+    uint32_t exact[17];        // the exact fallback's limbs (kExactLimbs)
+    uint32_t red_a[32], red_b[32];
     float r;
 };
 
@@ -95,39 +101,54 @@ struct Group {
     int ti, T;
 };
 
+// A 128-bit value below 2^120 as five 24-bit limbs, and back: a sum of up
+// to 32 such limbs stays below 2^29, so each limb of a group sum is one
+// 32-bit warp reduction (redux.sync), the carries propagated afterwards.
+__device__ __forceinline__ void to_limbs(U128 v, uint32_t (&l)[5]) {
+    l[0] = static_cast<uint32_t>(v.lo) & 0xFFFFFFu;
+    l[1] = static_cast<uint32_t>(v.lo >> 24) & 0xFFFFFFu;
+    l[2] = (static_cast<uint32_t>(v.lo >> 48) | (static_cast<uint32_t>(v.hi) << 16)) & 0xFFFFFFu;
+    l[3] = static_cast<uint32_t>(v.hi >> 8) & 0xFFFFFFu;
+    l[4] = static_cast<uint32_t>(v.hi >> 32) & 0xFFFFFFu;
+}
+
+__device__ __forceinline__ void warp_sum_limbs(uint32_t (&l)[5]) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const uint32_t t = __reduce_add_sync(0xFFFFFFFFu, l[k]) + c;
+        l[k] = k < 4 ? (t & 0xFFFFFFu) : t;
+        c = t >> 24;
+    }
+}
+
 // Sum of a 128-bit value and OR of a flag over the group (one pair of
-// barriers for both).
+// barriers for both).  Every partial and the total are below 2^120 (the
+// row's sum of squares in window units is below K * 2^94 <= 2^110).
 template <class Sync>
 __device__ __forceinline__ U128 group_sum_u128_or(U128 v, int &flag, const Group g, RowScratch *sc, Sync sync) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        U128 w;
-        w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
-        w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
-        v = add128(v, w);
-        flag |= __shfl_xor_sync(0xFFFFFFFFu, flag, o);
-    }
+    uint32_t l[5];
+    to_limbs(v, l);
+    warp_sum_limbs(l);
+    uint32_t f = __reduce_or_sync(0xFFFFFFFFu, static_cast<uint32_t>(flag));
     const int warp = g.ti >> 5, lane = g.ti & 31;
     sync();
     if (lane == 0) {
-        sc->red_hi[warp] = v.hi;
-        sc->red_lo[warp] = v.lo;
-        sc->red_i[warp] = flag;
+#pragma unroll
+        for (int k = 0; k < 5; ++k) sc->red_limb[k][warp] = l[k];
+        sc->red_a[warp] = f;
     }
     sync();
     const int nw = g.T >> 5;
-    v.hi = lane < nw ? sc->red_hi[lane] : 0;
-    v.lo = lane < nw ? sc->red_lo[lane] : 0;
-    flag = lane < nw ? sc->red_i[lane] : 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        U128 w;
-        w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
-        w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
-        v = add128(v, w);
-        flag |= __shfl_xor_sync(0xFFFFFFFFu, flag, o);
-    }
-    return v;
+    for (int k = 0; k < 5; ++k) l[k] = lane < nw ? sc->red_limb[k][lane] : 0u;
+    f = lane < nw ? sc->red_a[lane] : 0u;
+    warp_sum_limbs(l);
+    flag = static_cast<int>(__reduce_or_sync(0xFFFFFFFFu, f));
+    U128 r;
+    r.lo = static_cast<uint64_t>(l[0]) | (static_cast<uint64_t>(l[1]) << 24) | (static_cast<uint64_t>(l[2]) << 48);
+    r.hi = static_cast<uint64_t>(l[2] >> 16) | (static_cast<uint64_t>(l[3]) << 8) | (static_cast<uint64_t>(l[4]) << 32);
+    return r;
 }
 
 // The exact sum (acc * 2^(2*elo - 268), plus a sticky bit for smaller terms)
@@ -151,30 +172,86 @@ __device__ __forceinline__ float round_sum_to_f32(U128 acc, int elo, int sticky,
     return ldexpf(static_cast<float>(keep), (q > 0 ? q : 0) + 2 * elo - 268);
 }
 
-// Max of two ints over the group (one pair of barriers for both).
+// True when the squares below the window (sticky set) could carry into the
+// rounding of the windowed sum acc: the guard bit is 0 and every bit from
+// just below it down to 2^p, p = 14 + bitlen(K), is 1 (the small terms sum to
+// less than K * 2^14 < 2^p units, each being m^2 * 4^(E - elo) < 2^16 / 4).
+// With the guard bit 1 the windowed sum already rounds up, as the exact sum
+// does whether or not a carry reaches it.
+__device__ __forceinline__ bool sticky_may_carry(U128 acc, int elo, int K) {
+    if (acc.hi == 0 && acc.lo == 0) return true;
+    const int top = acc.hi ? 127 - __clzll(static_cast<long long>(acc.hi)) : 63 - __clzll(static_cast<long long>(acc.lo));
+    const int q = max(top - 23, 119 - 2 * elo);
+    if (q < 2) return true;
+    if (bit128(acc, q - 1)) return false;
+    const int p = 14 + (32 - __clz(K));
+    for (int i = q - 2; i >= p; --i)
+        if (!bit128(acc, i)) return false;
+    return true;
+}
+
+// The exact sum of squares of a finite row by one thread, over the whole
+// exponent range: 17 limbs of 32 bits in shared memory (`limb`), bit i worth
+// 2^(i - 266) (a square is m^2 * 2^(2E - 2) such units, E >= 1, below 2^522;
+// 2^16 of them below 2^538), rounded once to binary32 at 24 significant bits
+// or the subnormal quantum 2^-149 (= 2^117 units).  Slow (tens of
+// microseconds for K = 5120); taken only when sticky_may_carry says the
+// windowed sum cannot decide the rounding.  The limbs live in shared memory so
+// that this rare path needs no local-memory frame in the kernel.
+constexpr int kExactLimbs = 17;
+
+__device__ __noinline__ float exact_row_sum_squares(const uint4 *row, int nvec, uint32_t *limb) {
+    for (int i = 0; i < kExactLimbs; ++i) limb[i] = 0;
+    for (int i = 0; i < nvec; ++i) {
+        const uint4 v = row[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+            uint32_t m;
+            int E;
+            bf16_split((w[h >> 1] >> (16 * (h & 1))) & 0x7FFFu, m, E);
+            if (m == 0) continue;
+            const int sh = 2 * E - 2;
+            uint64_t add = static_cast<uint64_t>(m * m) << (sh & 31);  // below 2^47
+            for (int k = sh >> 5; add != 0 && k < kExactLimbs; ++k) {
+                const uint64_t t = static_cast<uint64_t>(limb[k]) + (add & 0xFFFFFFFFull);
+                limb[k] = static_cast<uint32_t>(t);
+                add = (add >> 32) + (t >> 32);
+            }
+        }
+    }
+    int top = -1;
+    for (int k = kExactLimbs - 1; k >= 0 && top < 0; --k)
+        if (limb[k]) top = 32 * k + 31 - __clz(static_cast<int>(limb[k]));
+    if (top < 0) return 0.0f;
+    const int q = max(top - 23, 117);
+    uint32_t keep = 0;
+    for (int i = top; i >= q; --i) keep = (keep << 1) | ((limb[i >> 5] >> (i & 31)) & 1u);
+    const uint32_t half = (limb[(q - 1) >> 5] >> ((q - 1) & 31)) & 1u;
+    bool rest = false;
+    for (int i = q - 2; i >= 0 && !rest; --i) rest = ((limb[i >> 5] >> (i & 31)) & 1u) != 0;
+    if (half && (rest || (keep & 1u))) keep += 1;
+    return ldexpf(static_cast<float>(keep), q - 266);
+}
+
+// Max of two non-negative ints over the group (one pair of barriers for
+// both).
 template <class Sync>
 __device__ __forceinline__ int2 group_max2(int2 v, const Group g, RowScratch *sc, Sync sync) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        v.x = max(v.x, __shfl_xor_sync(0xFFFFFFFFu, v.x, o));
-        v.y = max(v.y, __shfl_xor_sync(0xFFFFFFFFu, v.y, o));
-    }
+    uint32_t a = __reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(v.x));
+    uint32_t b = __reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(v.y));
     const int warp = g.ti >> 5, lane = g.ti & 31;
     sync();
     if (lane == 0) {
-        sc->red_i[warp] = v.x;
-        sc->red_hi[warp] = static_cast<uint64_t>(static_cast<uint32_t>(v.y));
+        sc->red_a[warp] = a;
+        sc->red_b[warp] = b;
     }
     sync();
     const int nw = g.T >> 5;
-    v.x = lane < nw ? sc->red_i[lane] : 0;
-    v.y = lane < nw ? static_cast<int>(sc->red_hi[lane]) : 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        v.x = max(v.x, __shfl_xor_sync(0xFFFFFFFFu, v.x, o));
-        v.y = max(v.y, __shfl_xor_sync(0xFFFFFFFFu, v.y, o));
-    }
-    return v;
+    a = lane < nw ? sc->red_a[lane] : 0u;
+    b = lane < nw ? sc->red_b[lane] : 0u;
+    return make_int2(static_cast<int>(__reduce_max_sync(0xFFFFFFFFu, a)),
+                     static_cast<int>(__reduce_max_sync(0xFFFFFFFFu, b)));
 }
 
 // Exponent field of the largest |element| of a vector of 8 bf16 (0 for zeros
@@ -286,7 +363,11 @@ __device__ __forceinline__ void rmsnorm_quant_row(const uint4 *__restrict__ xr, 
     acc = add128(acc, U128{a1 >> 32, a1 << 32});
     acc = group_sum_u128_or(acc, sticky, g, sc, sync);
     if (g.ti == 0) {
-        const float ss = round_sum_to_f32(acc, elo, sticky, special);
+        // (with kResidual the summed row is already in `resid`: every thread
+        // wrote its vectors before the group's barriers above)
+        const float ss = (!special && sticky && sticky_may_carry(acc, elo, K))
+                             ? exact_row_sum_squares(kResidual ? resid : xr, nvec, sc->exact)
+                             : round_sum_to_f32(acc, elo, sticky, special);
         const float mean = __fdiv_rn(ss, static_cast<float>(K));
         const float t = __fadd_rn(mean, eps);
         const float d = __fsqrt_rn(t);

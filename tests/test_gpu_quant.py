@@ -189,6 +189,35 @@ def test_rmsnorm_exact_sum_edge_rows(fp8, orc):
         assert np.all((q[nan_w] & 0x7F) == 0x7F), eps
 
 
+@pytest.mark.parametrize("K", [64, 5120])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_rmsnorm_carry_rows(fp8, orc, K, seed):
+    """Rows whose squares below the 40-binade window carry into the rounding
+    of the windowed sum (constructed: guard bit 0, a run of ones below it):
+    the windowed rule alone rounds the sum of squares one ulp low and the
+    probe's E4M3 code one step high; the kernel must detect the case and sum
+    the row exactly.  Between two ordinary rows; also through the residual
+    path, the row arriving as the residual (x = 0) so that the exact sum must
+    read the summed row."""
+    import norm_cases
+    d = norm_cases.carry_row(K=K, seed=seed)
+    assert d["ss_exact"] != d["ss_window"]
+    g = workloads.rng(70 + seed)
+    rows = workloads.bf16_normal(g, (3, K))
+    rows[1] = d["row"]
+    s = float(np.float32(d["s"]))
+    want = orc.rmsnorm_quant(rows, d["gamma"], d["eps"], s)
+    q = host_bits(fp8.rmsnorm_quant_fp8(to_dev_bf16(rows), to_dev_bf16(d["gamma"]), d["eps"], to_dev_f32(s)))
+    assert np.array_equal(q, want)
+    zeros = np.zeros_like(rows)
+    want_q, want_h = orc.add_rmsnorm_quant(zeros, rows, d["gamma"], d["eps"], s)
+    assert np.array_equal(want_q, want)
+    rd = to_dev_bf16(rows)
+    q2 = host_bits(fp8.add_rmsnorm_quant_fp8(to_dev_bf16(zeros), rd, to_dev_bf16(d["gamma"]), d["eps"],
+                                             to_dev_f32(s)))
+    assert np.array_equal(q2, want) and np.array_equal(host_bits(rd), want_h)
+
+
 @pytest.mark.parametrize("M,K", [(1, 5120), (8, 5120), (32, 5120), (3, 17408), (1000, 5120), (5, 16)])
 def test_add_rmsnorm_quant(fp8, orc, M, K):
     """Residual add -> RMSNorm -> static quant: the E4M3 bytes and the updated

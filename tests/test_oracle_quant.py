@@ -172,6 +172,24 @@ def test_sum_squares_exact_vs_rationals(orc):
     assert np.isnan(orc.sum_squares_bf16(np.array([0x7F80, 0x7FC1], np.uint16)))
 
 
+def test_sum_squares_carry_rows(orc):
+    """Constructed rows where the squares below the row's top 40 binades carry
+    into the rounding (a run of one bits under a zero guard bit): the oracle's
+    sum is the exact integer sum rounded once (Python integers), which here
+    differs from the windowed sum with only a sticky bit for the small squares;
+    and the probe element's E4M3 code follows the exact sum."""
+    import norm_cases
+    for K, seed in ((64, 0), (64, 1), (5120, 2), (64, 3)):
+        d = norm_cases.carry_row(K=K, seed=seed)
+        exact = norm_cases.round_units_f32(norm_cases.exact_units(d["row"]))
+        assert orc.sum_squares_bf16(d["row"]) == exact == d["ss_exact"]
+        assert exact != norm_cases.window_f32(d["row"])
+        frac = sum(Fraction(float(v)) ** 2 for v in _as_f32(d["row"]))
+        assert exact == _f32_nearest(frac)
+        q = orc.rmsnorm_quant(d["row"][None, :], d["gamma"], d["eps"], d["s"])[0]
+        assert q[d["probe"]] == 0x38        # 1.0: the boundary 1.0625 lies between the exact and windowed h / s
+
+
 def test_rmsnorm_vs_numpy_restatement(orc):
     """The pinned arithmetic restated with numpy's vectorised ops (binary64 sum
     of the exact squares, then the binary32 chain) gives the same bf16 bits."""
