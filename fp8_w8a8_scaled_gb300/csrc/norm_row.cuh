@@ -1,7 +1,6 @@
 // norm_row.cuh -- the fused RMSNorm -> static E4M3 quantisation of ONE row by
-// a group of threads, shared by the standalone rmsnorm_quant_fp8 kernel (a CTA
-// per row) and the decode GEMM's fused prologue (the drain warpgroup of the
-// first M CTAs), so both produce the same bytes.
+// a group of threads: the row arithmetic of the rmsnorm_quant_fp8 and
+// add_rmsnorm_quant_fp8 kernels (a CTA per row).
 //
 // Source: "We emit F32 where vLLM emits bf16 on the biggest prefill buffers
 // ..." (vllm.cpp #417), "Ranked follow-ons from the same audit": the fused
@@ -90,7 +89,7 @@ __device__ __forceinline__ void bf16_split(uint32_t b, uint32_t &m, int &E) {
 struct RowScratch {
     uint32_t red_limb[5][32];  // per warp: 24-bit limbs of its partial sum
     uint32_t exact[17];        // the exact fallback's limbs (kExactLimbs)
-    uint32_t red_a[32], red_b[32];
+    uint32_t red_a[32], red_b[32], red_f[32];
     float r;
 };
 
@@ -122,8 +121,8 @@ __device__ __forceinline__ void warp_sum_limbs(uint32_t (&l)[5]) {
     }
 }
 
-// Sum of a 128-bit value and OR of a flag over the group (one pair of
-// barriers for both).  Every partial and the total are below 2^120 (the
+// Sum of a 128-bit value and OR of a flag over the group (one barrier for
+// both; the scratch fields it writes are written once per row).  Every partial and the total are below 2^120 (the
 // row's sum of squares in window units is below K * 2^94 <= 2^110).
 template <class Sync>
 __device__ __forceinline__ U128 group_sum_u128_or(U128 v, int &flag, const Group g, RowScratch *sc, Sync sync) {
@@ -132,17 +131,16 @@ __device__ __forceinline__ U128 group_sum_u128_or(U128 v, int &flag, const Group
     warp_sum_limbs(l);
     uint32_t f = __reduce_or_sync(0xFFFFFFFFu, static_cast<uint32_t>(flag));
     const int warp = g.ti >> 5, lane = g.ti & 31;
-    sync();
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < 5; ++k) sc->red_limb[k][warp] = l[k];
-        sc->red_a[warp] = f;
+        sc->red_f[warp] = f;
     }
     sync();
     const int nw = g.T >> 5;
 #pragma unroll
     for (int k = 0; k < 5; ++k) l[k] = lane < nw ? sc->red_limb[k][lane] : 0u;
-    f = lane < nw ? sc->red_a[lane] : 0u;
+    f = lane < nw ? sc->red_f[lane] : 0u;
     warp_sum_limbs(l);
     flag = static_cast<int>(__reduce_or_sync(0xFFFFFFFFu, f));
     U128 r;
@@ -234,14 +232,13 @@ __device__ __noinline__ float exact_row_sum_squares(const uint4 *row, int nvec, 
     return ldexpf(static_cast<float>(keep), q - 266);
 }
 
-// Max of two non-negative ints over the group (one pair of barriers for
-// both).
+// Max of two non-negative ints over the group (one barrier for both; the
+// scratch fields it writes are written once per row).
 template <class Sync>
 __device__ __forceinline__ int2 group_max2(int2 v, const Group g, RowScratch *sc, Sync sync) {
     uint32_t a = __reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(v.x));
     uint32_t b = __reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(v.y));
     const int warp = g.ti >> 5, lane = g.ti & 31;
-    sync();
     if (lane == 0) {
         sc->red_a[warp] = a;
         sc->red_b[warp] = b;

@@ -189,6 +189,44 @@ def test_rmsnorm_exact_sum_edge_rows(fp8, orc):
         assert np.all((q[nan_w] & 0x7F) == 0x7F), eps
 
 
+def test_rmsnorm_warp_windows(fp8, orc):
+    """Rows of 5120 (20 warps of one vector per thread) whose warps see very
+    different largest binades, so that aligning the warps' window sums to the
+    row's window shifts bits out: large values in one warp's elements only,
+    tiny ones elsewhere (squares below the row's window, some of them exact
+    multiples of its unit), an Inf or a NaN in a single warp, subnormals around
+    one normal value."""
+    K = 5120
+    g = workloads.rng(77)
+    rows = np.zeros((8, K), np.uint16)
+    big = workloads.bf16_normal(g, (K,))
+    tiny = workloads.bf16_normal(g, (K,), std=2.0 ** -50)
+    rows[0] = tiny
+    rows[0, :256] = big[:256]                          # warp 0 large, the rest 2^-50
+    rows[1] = tiny
+    rows[1, 4000:4256] = big[4000:4256]                # a late warp large
+    rows[2] = 0x2000                                   # 2^-63: squares exact in the row's unit
+    rows[2, 300] = 0x4000                              # one 2.0
+    rows[3] = big
+    rows[3, 2000] = 0x7F80                             # Inf in one warp
+    rows[4] = big
+    rows[4, 5119] = 0x7FC1                             # NaN in the last warp
+    rows[5] = g.integers(1, 128, K).astype(np.uint16)  # subnormals ...
+    rows[5, 4321] = 0x0080                             # ... and the smallest normal
+    rows[6] = tiny
+    rows[6, ::640] = 0x4B00                            # a few 2^23 values, every other warp
+    rows[7] = big
+    rows[7, 1:K:7] = 0x0001                            # a subnormal every 7th element
+    gamma = workloads.bf16_normal(g, (K,), mean=1.0, std=0.1)
+    for eps in (1e-6, 0.0):
+        s = float(np.float32(1 / 56))
+        q = host_bits(fp8.rmsnorm_quant_fp8(to_dev_bf16(rows), to_dev_bf16(gamma), eps, to_dev_f32(s)))
+        want = orc.rmsnorm_quant(rows, gamma, eps, s)
+        nan_w = (want & 0x7F) == 0x7F
+        assert np.array_equal(q[~nan_w], want[~nan_w]), eps
+        assert np.all((q[nan_w] & 0x7F) == 0x7F), eps
+
+
 @pytest.mark.parametrize("K", [64, 5120])
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_rmsnorm_carry_rows(fp8, orc, K, seed):
@@ -203,8 +241,13 @@ def test_rmsnorm_carry_rows(fp8, orc, K, seed):
     d = norm_cases.carry_row(K=K, seed=seed)
     assert d["ss_exact"] != d["ss_window"]
     g = workloads.rng(70 + seed)
-    rows = workloads.bf16_normal(g, (3, K))
+    rows = workloads.bf16_normal(g, (4, K))
     rows[1] = d["row"]
+    # the same elements scattered over the row (other warps, other windows);
+    # the probe stays where its gamma is
+    perm = np.concatenate([[d["probe"]], g.permutation(np.delete(np.arange(K), d["probe"]))])
+    rows[3] = 0
+    rows[3][perm] = d["row"][np.concatenate([[d["probe"]], np.delete(np.arange(K), d["probe"])])]
     s = float(np.float32(d["s"]))
     want = orc.rmsnorm_quant(rows, d["gamma"], d["eps"], s)
     q = host_bits(fp8.rmsnorm_quant_fp8(to_dev_bf16(rows), to_dev_bf16(d["gamma"]), d["eps"], to_dev_f32(s)))
