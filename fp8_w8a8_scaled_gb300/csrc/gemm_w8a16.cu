@@ -9,24 +9,26 @@
 //
 // Design (GB300, sm_103a).  The tensor core's kind::f16 takes both operands in
 // one 16-bit type, so the E4M3 weight tile is widened to bf16 (exact: every
-// E4M3 value is a bf16 value) in shared memory before the MMA reads it.
-// Units are (128-row output tile) x (128-wide k-block), divided among
-// persistent CTAs as in the W8A8 kernel's stream-K mode: two per SM for the
-// 16-token tile (one widened tile each), one for the 32-token tile.  Inside a
-// CTA:
+// E4M3 value is a bf16 value) before the MMA reads it -- into tensor memory,
+// which the MMA can take its A operand from, so that shared memory carries
+// only the E4M3 box and the tokens (widening into shared memory tripled its
+// traffic per k-block and bounded the kernel).  Units are (128-row output
+// tile) x (128-wide k-block), divided among persistent CTAs as in the W8A8
+// kernel's stream-K mode: two per SM for the 16-token tile, one for the
+// 32-token tile.  Inside a CTA:
 //   * warp 0 / lane 0 streams each unit's 128 x 128-byte E4M3 weight box and
 //     its two TOK x 64-element bf16 token boxes with TMA into a ring of stages
 //     (128-byte swizzle);
-//   * warps 6-9, one weight row per thread, widen each unit's E4M3 tile into
-//     a bf16 A tile (one or two in flight), laid out as the MMA reads them
-//     (two 64-element K halves of 128 rows x 128 bytes, 128-byte swizzled),
-//     and release the weight stage at once;
+//   * warps 6-9, one weight row per thread (the row of the thread's TMEM
+//     lane), widen each unit's E4M3 row into 64 TMEM columns of one of two
+//     A tiles (two K elements per column) and release the weight stage at
+//     once;
 //   * warps 2-5 drain each unit's fp32 partial out of TMEM into TwoSum
 //     registers -- the same drain, tile store and stream-K fix-up as the W8A8
 //     decode kernel;
 //   * warp 1 / lane 0 issues eight tcgen05.mma kind::f16 (BF16 x BF16 -> F32,
-//     M = 128 weight rows, N = TOK tokens, K = 16) per unit into one of
-//     several TMEM accumulators.
+//     M = 128 weight rows from TMEM, N = TOK tokens from shared memory,
+//     K = 16) per unit into one of several TMEM accumulators.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -41,8 +43,6 @@ namespace fp8k {
 namespace {
 
 constexpr uint32_t kW16WeightBytes = kDecodeRows * kBlockK;    // 16 KB of E4M3 per stage
-constexpr uint32_t kW16Region = kDecodeRows * 128;             // 64 bf16 of K for 128 rows: 16 KB
-constexpr uint32_t kW16ATileBytes = 2 * kW16Region;            // the widened 128 x 128 tile: 32 KB
 
 template <int TOK>
 struct W16Cfg {
@@ -57,12 +57,15 @@ struct W16Cfg {
     // each: 5 per sub-partition), one for the 32-token tile, whose drain needs more
     static constexpr int kMaxRegs = TOK <= 16 ? 96 : 168;
     static constexpr int kDrainThreads = 128;
-    static constexpr int kBufs = TOK <= 16 ? 8 : 4;              // TMEM accumulators (must match w16_tmem_bufs)
-    static constexpr uint32_t kTmemCols = kBufs * TOK < 32 ? 32 : kBufs * TOK;
+    static constexpr int kBufs = TOK <= 16 ? 8 : 4;              // TMEM accumulators
+    // widened tiles ahead of the MMA, in TMEM after the accumulators: 64
+    // columns each (128 rows x 128 bf16)
+    static constexpr int kABufs = 2;
+    static constexpr uint32_t kACol0 = kBufs * TOK;
+    static constexpr uint32_t kTmemCols = 256;  // kACol0 + kABufs * 64 = 256 for both tiles; two CTAs per SM at most
     static constexpr uint32_t kXRegion = TOK * 128;              // 64 bf16 of K for TOK tokens
     static constexpr uint32_t kXStageBytes = 2 * kXRegion;       // one unit's token tile
     static constexpr int kXStages = TOK <= 16 ? 4 : 8;          // token ring (>= the weight ring)
-    static constexpr int kABufs = TOK <= 16 ? 1 : 2;             // widened tiles ahead of the MMA
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kDecodeRows, TOK);
 };
 
@@ -75,29 +78,58 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t pair) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(b.x)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b.y)) << 16);
 }
 
-// Chunks [J0, J0 + NJ) of row r of a 128 x 128-byte E4M3 box (128-byte
-// swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)) widened into
-// the bf16 A tile: K elements 64h .. 64h+63 go to region h, whose rows are 128
-// bytes of 8-element chunks swizzled the same way.
+// Each thread of the warp writes 32 consecutive 32-bit TMEM columns of its
+// lane (lane = the warp's 32-lane quarter + thread index).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem]^T for BF16 operands (K = 16 per instruction):
+// A's 128 rows in the 128 TMEM lanes, two K elements per 32-bit column (the
+// lower K index in the low half), 8 columns per instruction.
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Row r of a 128 x 128-byte E4M3 box (128-byte swizzle: 16-byte chunk j of
+// row r sits at chunk j ^ (r % 8)), chunks [J0, J0 + NJ), widened into the
+// calling thread's TMEM lane: K elements 2c, 2c + 1 in column c of the tile
+// at `trow` (this lane's address of the tile's first column).
 template <int NJ>
-__device__ __forceinline__ void widen_row(const uint8_t *src, uint8_t *dst, int r, int J0) {
+__device__ __forceinline__ void widen_row_tmem(const uint8_t *src, uint32_t trow, int r, int J0) {
+    static_assert(NJ % 4 == 0, "whole 64-element halves");
     const int sw = r & 7;
     const uint8_t *srow = src + r * 128;
 #pragma unroll
-    for (int jj = 0; jj < NJ; ++jj) {
-        const int j = J0 + jj;
-        const uint4 q = *reinterpret_cast<const uint4 *>(srow + ((j ^ sw) << 4));
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-        uint32_t o[8];
+    for (int h = 0; h < NJ / 4; ++h) {
+        uint32_t o[32];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            o[2 * t] = e4m3x2_to_bf16x2(w[t] & 0xFFFFu);
-            o[2 * t + 1] = e4m3x2_to_bf16x2(w[t] >> 16);
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = J0 + 4 * h + jj;
+            const uint4 q = *reinterpret_cast<const uint4 *>(srow + ((j ^ sw) << 4));
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                o[8 * jj + 2 * t] = e4m3x2_to_bf16x2(w[t] & 0xFFFFu);
+                o[8 * jj + 2 * t + 1] = e4m3x2_to_bf16x2(w[t] >> 16);
+            }
         }
-        uint8_t *drow = dst + (j >> 2) * kW16Region + r * 128;
-        const int c0 = (j & 3) * 2;
-        *reinterpret_cast<uint4 *>(drow + ((c0 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4 *>(drow + (((c0 + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        tmem_st32(trow + static_cast<uint32_t>(J0 * 8 + 32 * h), o);
     }
 }
 
@@ -122,10 +154,10 @@ __global__ void __maxnreg__(W16Cfg<TOK>::kMaxRegs)
     constexpr int NA = Cfg::kABufs;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    // [weight ring: stages x 16 KB][token ring: NX x TOK*256 B][widened tiles: NA x 32 KB][barriers]
+    // [weight ring: stages x 16 KB][token ring: NX x TOK*256 B][barriers]; the
+    // widened tiles live in TMEM
     const uint32_t xbase = base + static_cast<uint32_t>(stages) * kW16WeightBytes;
-    const uint32_t abuf0 = xbase + static_cast<uint32_t>(NX) * Cfg::kXStageBytes;
-    const uint32_t bar0 = abuf0 + static_cast<uint32_t>(NA) * kW16ATileBytes;
+    const uint32_t bar0 = xbase + static_cast<uint32_t>(NX) * Cfg::kXStageBytes;
     auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
     auto wempty_bar = [&](int s) { return bar0 + 8u * (stages + s); };
     auto xfull_bar = [&](int s) { return bar0 + 8u * (2 * stages + s); };
@@ -248,13 +280,13 @@ __global__ void __maxnreg__(W16Cfg<TOK>::kMaxRegs)
             if (!cta_wait(tempty_bar(b), tph ^ 1u, err, kErrDecodeTmemEmptyWait, &s_abort)) break;
             tc_fence_after();
             const uint32_t xs = xbase + static_cast<uint32_t>(s) * Cfg::kXStageBytes;
-            const uint32_t as = abuf0 + static_cast<uint32_t>(a) * kW16ATileBytes;
+            const uint32_t at = tmem + Cfg::kACol0 + static_cast<uint32_t>(a) * 64u;
             const uint32_t d = tmem + static_cast<uint32_t>(b * TOK);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {  // K = 16 bf16 = 32 bytes per MMA: +2 in the address field
+            for (int kk = 0; kk < 8; ++kk) {  // K = 16 bf16 per MMA: 8 TMEM columns of A, 32 bytes of the token tile
                 const uint32_t h = static_cast<uint32_t>(kk >> 2), o = 2u * static_cast<uint32_t>(kk & 3);
-                mma_bf16(d, sw128_kmajor_desc(as + h * kW16Region) + o, sw128_kmajor_desc(xs + h * Cfg::kXRegion) + o,
-                         Cfg::kIdesc, kk > 0 ? 1u : 0u);
+                mma_bf16_tmem_a(d, at + 8u * static_cast<uint32_t>(kk), sw128_kmajor_desc(xs + h * Cfg::kXRegion) + o,
+                                Cfg::kIdesc, kk > 0 ? 1u : 0u);
             }
             mma_commit(xempty_bar(s));
             mma_commit(aempty_bar(a));
@@ -274,14 +306,19 @@ __global__ void __maxnreg__(W16Cfg<TOK>::kMaxRegs)
         int j = 0;
         for (; j < iters; ++j) {
             const int s = j % stages, a = j % NA;
-            if (!cta_wait(wfull_bar(s), static_cast<uint32_t>(j / stages) & 1u, err, kErrW16FullWait, &s_abort))
-                break;
-            if (!cta_wait(aempty_bar(a), (static_cast<uint32_t>(j / NA) & 1u) ^ 1u, err, kErrW16AEmptyWait,
-                          &s_abort))
-                break;
-            widen_row<kNJ>(smem_raw + (base + static_cast<uint32_t>(s) * kW16WeightBytes - raw),
-                           smem_raw + (abuf0 + static_cast<uint32_t>(a) * kW16ATileBytes - raw), row, j0);
-            fence_proxy_async_smem();  // the writes, before the tensor core reads them
+            // the TMEM stores below are warp-collective: the warp goes on only
+            // if every lane's wait succeeded
+            bool ok = cta_wait(wfull_bar(s), static_cast<uint32_t>(j / stages) & 1u, err, kErrW16FullWait, &s_abort);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            ok = cta_wait(aempty_bar(a), (static_cast<uint32_t>(j / NA) & 1u) ^ 1u, err, kErrW16AEmptyWait, &s_abort);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            widen_row_tmem<kNJ>(smem_raw + (base + static_cast<uint32_t>(s) * kW16WeightBytes - raw),
+                                tmem + ((static_cast<uint32_t>(warp & 3u) * 32u) << 16) + Cfg::kACol0 +
+                                    static_cast<uint32_t>(a) * 64u,
+                                row, j0);
+            tmem_st_wait();  // the stores, before the tensor core reads them
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(afull_bar(a));
@@ -482,22 +519,23 @@ __global__ void __launch_bounds__(256) scale_columns_kernel(uint4 *__restrict__ 
 
 }  // namespace
 
-// Shared memory of one CTA: alignment slack, the weight ring, the token ring,
-// the widened weight tiles and the mbarriers (rounded up).
+// Shared memory of one CTA: alignment slack, the weight ring, the token ring
+// and the mbarriers (rounded up); the widened tiles are in TMEM.
 static size_t w16_smem_bytes(int tok, int stages) {
-    const int nb = tok <= 16 ? 8 : 4, nx = tok <= 16 ? W16Cfg<16>::kXStages : W16Cfg<32>::kXStages, na = tok <= 16 ? W16Cfg<16>::kABufs
-                                                                                 : W16Cfg<32>::kABufs;
+    const int nb = tok <= 16 ? W16Cfg<16>::kBufs : W16Cfg<32>::kBufs;
+    const int nx = tok <= 16 ? W16Cfg<16>::kXStages : W16Cfg<32>::kXStages;
+    const int na = tok <= 16 ? W16Cfg<16>::kABufs : W16Cfg<32>::kABufs;
     const size_t barriers = 8u * static_cast<size_t>(2 * stages + 2 * nx + 2 * nb + 2 * na + 1);
     return 1024 + static_cast<size_t>(stages) * kW16WeightBytes + static_cast<size_t>(nx) * 2u * tok * 128u +
-           static_cast<size_t>(na) * kW16ATileBytes + ((barriers + 127) / 128) * 128;
+           ((barriers + 127) / 128) * 128;
 }
 
 DecodePlan plan_w8a16(int64_t M, int64_t N, int64_t K, int num_sms) {
     DecodePlan p{};
     p.tok_pad = M <= 16 ? 16 : 32;
-    // 16 tokens: 3 weight stages, 4 token stages, one widened tile (97 KB, two
-    // CTAs per SM); 32 tokens: 6, 8 and two (225 KB, one CTA per SM)
-    p.stages = p.tok_pad == 16 ? 3 : 6;
+    // 16 tokens: 5 weight stages and 4 token stages (~98 KB, two CTAs per SM);
+    // 32 tokens: 8 and 8 (~194 KB, one CTA per SM)
+    p.stages = p.tok_pad == 16 ? 5 : 8;
     p.smem_bytes = w16_smem_bytes(p.tok_pad, p.stages);
     p.n_tiles = static_cast<int>((N + kDecodeRows - 1) / kDecodeRows);
     p.m_tiles = static_cast<int>((M + p.tok_pad - 1) / p.tok_pad);
