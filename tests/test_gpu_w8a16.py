@@ -92,6 +92,20 @@ def test_w16_decode_random_codes(fp8, orc, M, N, K, per_channel):
     check(fp8, orc, x, W, sb, per_channel, f"w16 {M}x{N}x{K} pc={per_channel}")
 
 
+# (M, N, K) with 29 to 100 output tiles (tiles shared by 3 to 10 CTAs of the
+# persistent grid), one with a ragged last tile and a ragged k-block
+TILE_COUNT_SHAPES = [(3, 12800, 512), (5, 6400, 640), (8, 5632, 768), (2, 4608, 1024), (16, 4104, 1040),
+                     (1, 3712, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", TILE_COUNT_SHAPES)
+def test_w16_decode_tile_counts(fp8, orc, M, N, K):
+    """Every output against the oracle, and a rerun bitwise."""
+    x, W, sb = operands(9050 + N, M, N, K, True)
+    y = check(fp8, orc, x, W, sb, True, f"w16 {M}x{N}x{K}")
+    assert np.array_equal(run_w16(fp8, to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb), 1), y)
+
+
 @pytest.mark.parametrize("M", [1, 8, 16, 32])
 def test_w16_decode_qkv(fp8, orc, M):
     """Merged QKV (N 10240, K 5120), per-channel quantised N(0, 0.02) weights,
