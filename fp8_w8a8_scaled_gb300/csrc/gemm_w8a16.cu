@@ -51,10 +51,8 @@ struct W16Cfg {
     // chunks between several (two were slower than two CTAs per SM of one)
     static constexpr int kWidenGroups = 1;
     static constexpr int kThreads = 64 + 128 + 128 * kWidenGroups;
-    // registers a thread may use with one CTA per SM: a sub-partition holds
-    // ceil(warps / 4) of its warps, 16384 registers each
     // registers per thread: two CTAs per SM for the 16-token tile (10 warps
-    // each: 5 per sub-partition), one for the 32-token tile, whose drain needs more
+    // each), one for the 32-token tile, whose drain needs more
     static constexpr int kMaxRegs = TOK <= 16 ? 96 : 168;
     static constexpr int kDrainThreads = 128;
     static constexpr int kBufs = TOK <= 16 ? 8 : 4;              // TMEM accumulators
@@ -65,8 +63,9 @@ struct W16Cfg {
     static constexpr uint32_t kTmemCols = 256;  // kACol0 + kABufs * 64 = 256 for both tiles; two CTAs per SM at most
     static constexpr uint32_t kXRegion = TOK * 128;              // 64 bf16 of K for TOK tokens
     static constexpr uint32_t kXStageBytes = 2 * kXRegion;       // one unit's token tile
-    static constexpr int kXStages = TOK <= 16 ? 4 : 8;          // token ring (>= the weight ring)
+    static constexpr int kXStages = TOK <= 16 ? 4 : 8;          // token ring
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kDecodeRows, TOK);
+    static_assert(kACol0 + kABufs * 64 <= kTmemCols, "accumulators and widened tiles fit the allocation");
 };
 
 // Two E4M3 codes (the first in the low byte) -> two bf16 (the first in the low
