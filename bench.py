@@ -456,18 +456,12 @@ def run_w8a16(torch, fp8, device, dist_barrier, dist_max, reps=40):
             "per_M": rows, "dense_m2048": dense, "gpu_launches": launches}
 
 
-def run_decode_step(torch, fp8, device, dist_barrier, dist_max, reps=20):
-    """Synthetic 64-layer decode step at M in {1, 4, 8}: per layer RMSNorm ->
-    static quant -> QKV (10240x5120), per-token quant of an [M, 8192] stub
-    (the attention output, not on this path) -> O (5120x8192), gate_up
-    (34816x5120) on the same normalised input, SiLU(gate) * up -> per-token
-    quant of the gate_up output -> down (5120x17408); distinct weights per
-    layer (23.15 GB), the whole step one CUDA graph."""
-    L_ = workloads.STEP_LAYERS
+def decode_step_weights(torch, device):
+    """Distinct weights and per-channel scales of the 64 layers of the
+    synthetic decode step: (QKV, O, gate_up, down) per layer, 23.15 GB."""
     shapes = workloads.LayerShapes()
-    K = K_HID
     Wl = []
-    for layer in range(L_):
+    for layer in range(workloads.STEP_LAYERS):
         ws = []
         for j, (n, k) in enumerate((shapes.qkv, shapes.o, shapes.gate_up, shapes.down)):
             w = workloads.device_e4m3_codes(torch, (n, k), seed=10000 + 8 * layer + j, device=device)
@@ -475,32 +469,53 @@ def run_decode_step(torch, fp8, device, dist_barrier, dist_max, reps=20):
                        workloads.device_uniform_f32(torch, (n,), 0.5e-3, 2e-3, seed=20000 + 8 * layer + j,
                                                     device=device)))
         Wl.append(ws)
+    return Wl
+
+
+def decode_step_fn(torch, fp8, device, Wl, M):
+    """One synthetic decode step at M tokens over the layers' weights Wl:
+    per layer RMSNorm -> static quant -> QKV, per-token quant of an [M, 8192]
+    stub (the attention output, not on this path) -> O, gate_up on the same
+    normalised input, SiLU(gate) * up -> per-token quant -> down (7 launches
+    per layer)."""
+    shapes = workloads.LayerShapes()
+    K = K_HID
     gamma = workloads.device_bf16_normal(torch, (K,), seed=30000, device=device, std=0.1)
     s_a = torch.tensor([float(workloads.STATIC_INPUT_SCALE)], dtype=torch.float32, device=device)
+    x = workloads.device_bf16_normal(torch, (M, K), seed=30001, device=device)
+    o_in = workloads.device_bf16_normal(torch, (M, workloads.O_K), seed=30002, device=device)
+    a = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=device)
+    a_o = torch.empty((M, workloads.O_K), dtype=torch.float8_e4m3fn, device=device)
+    a_d = torch.empty((M, workloads.DOWN_K), dtype=torch.float8_e4m3fn, device=device)
+    s_o = torch.empty((M,), dtype=torch.float32, device=device)
+    s_d = torch.empty((M,), dtype=torch.float32, device=device)
+    y = [torch.empty((M, n), dtype=torch.bfloat16, device=device)
+         for (n, _) in (shapes.qkv, shapes.o, shapes.gate_up, shapes.down)]
+    st = fp8.FLAG_WEIGHTS_STATIC
+
+    def step(_i):
+        for ws in Wl:
+            fp8.rmsnorm_quant_fp8(x, gamma, workloads.RMS_EPS, s_a, out=a)
+            fp8.fp8_scaled_mm(a, ws[0][0], s_a, ws[0][1], fp8.GRAN_PER_CHANNEL, out=y[0], flags=st)
+            fp8.quant_fp8_per_token(o_in, out=a_o, scale_out=s_o)
+            fp8.fp8_scaled_mm(a_o, ws[1][0], s_o, ws[1][1], fp8.GRAN_PER_TOKEN_CHANNEL, out=y[1], flags=st)
+            fp8.fp8_scaled_mm(a, ws[2][0], s_a, ws[2][1], fp8.GRAN_PER_CHANNEL, out=y[2], flags=st)
+            fp8.silu_mul_quant_per_token(y[2], out=a_d, scale_out=s_d)
+            fp8.fp8_scaled_mm(a_d, ws[3][0], s_d, ws[3][1], fp8.GRAN_PER_TOKEN_CHANNEL, out=y[3], flags=st)
+
+    return step
+
+
+def run_decode_step(torch, fp8, device, dist_barrier, dist_max, reps=20):
+    """Synthetic 64-layer decode step at M in {1, 4, 8} (decode_step_fn),
+    distinct weights per layer (23.15 GB), the whole step one CUDA graph."""
+    L_ = workloads.STEP_LAYERS
+    shapes = workloads.LayerShapes()
+    Wl = decode_step_weights(torch, device)
     peak, _ = measured_peaks()
     rows, launches = [], 0
     for M in workloads.STEP_MS:
-        x = workloads.device_bf16_normal(torch, (M, K), seed=30001, device=device)
-        o_in = workloads.device_bf16_normal(torch, (M, workloads.O_K), seed=30002, device=device)
-        a = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=device)
-        a_o = torch.empty((M, workloads.O_K), dtype=torch.float8_e4m3fn, device=device)
-        a_d = torch.empty((M, workloads.DOWN_K), dtype=torch.float8_e4m3fn, device=device)
-        s_o = torch.empty((M,), dtype=torch.float32, device=device)
-        s_d = torch.empty((M,), dtype=torch.float32, device=device)
-        y = [torch.empty((M, n), dtype=torch.bfloat16, device=device)
-             for (n, _) in (shapes.qkv, shapes.o, shapes.gate_up, shapes.down)]
-        st = fp8.FLAG_WEIGHTS_STATIC
-
-        def step(_i):
-            for ws in Wl:
-                fp8.rmsnorm_quant_fp8(x, gamma, workloads.RMS_EPS, s_a, out=a)
-                fp8.fp8_scaled_mm(a, ws[0][0], s_a, ws[0][1], fp8.GRAN_PER_CHANNEL, out=y[0], flags=st)
-                fp8.quant_fp8_per_token(o_in, out=a_o, scale_out=s_o)
-                fp8.fp8_scaled_mm(a_o, ws[1][0], s_o, ws[1][1], fp8.GRAN_PER_TOKEN_CHANNEL, out=y[1], flags=st)
-                fp8.fp8_scaled_mm(a, ws[2][0], s_a, ws[2][1], fp8.GRAN_PER_CHANNEL, out=y[2], flags=st)
-                fp8.silu_mul_quant_per_token(y[2], out=a_d, scale_out=s_d)
-                fp8.fp8_scaled_mm(a_d, ws[3][0], s_d, ws[3][1], fp8.GRAN_PER_TOKEN_CHANNEL, out=y[3], flags=st)
-
+        step = decode_step_fn(torch, fp8, device, Wl, M)
         g = graph_of(torch, device, step, 1)
         for _ in range(3):
             g.replay()
@@ -731,6 +746,16 @@ def run_profile_case(args):
     M, N, K = (int(v) for v in args.profile.split(","))
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(0)
+    if args.profile_kind == "step":  # the 64-layer decode step at M tokens (N, K unused), eagerly
+        step = decode_step_fn(torch, fp8, dev, decode_step_weights(torch, dev), M)
+        for i in range(args.steps):
+            step(i)
+        torch.cuda.synchronize()
+        err = fp8.get_device_error()
+        print(json.dumps({"profile_case": [M, N, K], "kind": "step", "device_error": err}))
+        if err:
+            raise SystemExit(1)
+        return
     g = workloads.rng(0)
     x = torch.from_numpy(workloads.bf16_normal(g, (M, K)).view(np.int16)).view(torch.bfloat16).to(dev)
     gamma = torch.from_numpy(workloads.bf16_normal(g, (K,), mean=1.0, std=0.1).view(np.int16)).view(
@@ -800,9 +825,10 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the gate_up decode, 64-layer decode step and tiny GEMM measurements")
     ap.add_argument("--profile", metavar="M,N,K", help="run a small eager case for a profiler and exit")
-    ap.add_argument("--profile-kind", choices=("w8a8", "w8a16", "blockwise"), default="w8a8",
+    ap.add_argument("--profile-kind", choices=("w8a8", "w8a16", "blockwise", "step"), default="w8a8",
                     help="the GEMM of the --profile case: per-channel W8A8 after the norm-quant (default), "
-                         "weight-only W8A16, or blockwise-scaled W8A8 after the per-token-group quant")
+                         "weight-only W8A16, or blockwise-scaled W8A8 after the per-token-group quant; or "
+                         "'step': the 64-layer decode step at M tokens (N, K ignored)")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args)
