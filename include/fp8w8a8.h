@@ -416,8 +416,9 @@ int fp8_decode_ctas_for_sms(int64_t M, int64_t N, int64_t K, int num_sms);
  * 1 for clusters of S CTAs per output tile (S = 1: whole tiles, nothing to
  * sum), 0 for the persistent stream-K grid, -1 if the shape does not go to the
  * decode kernel.  With tiles = ceil(N/128), S = floor(floor(8 * num_sms / 5) /
- * tiles), at least 1 and at most ceil(K/128); clusters when S <= 8, stream-K
- * otherwise.  Pure and host-only. */
+ * tiles), at least 1 and at most ceil(K/128), and 1 when K <= 256 (two
+ * k-blocks at most: whole tiles); clusters when S <= 8, stream-K otherwise.
+ * Pure and host-only. */
 int fp8_decode_split_for_sms(int64_t M, int64_t N, int64_t K, int num_sms);
 
 /* Device error word.  Kernels never trap: a bounded wait that runs out sets a

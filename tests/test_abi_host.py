@@ -240,7 +240,8 @@ def test_describe_dispatch_is_pure(L):
 
 def test_decode_planner(L):
     """Cluster mode (S = floor(floor(8 * SMs / 5) / tiles) CTAs per
-    128-channel tile, at least 1, at most the tile's k-blocks) when S <= 8;
+    128-channel tile, at least 1, at most the tile's k-blocks, 1 when K has
+    at most two k-blocks) when S <= 8;
     else two persistent CTAs per SM (stream-K; never more CTAs than units of
     one tile x one 128-wide k-block, and at most 8 CTAs per tile)."""
     f = L.fp8_decode_ctas_for_sms
@@ -253,8 +254,10 @@ def test_decode_planner(L):
     assert sp(8, 5120, 17408, 152) == 6
     assert sp(1, 8192, 5120, 152) == 3 and sp(1, 7168, 5120, 152) == 4 and sp(1, 6144, 5120, 152) == 5
     assert sp(1, 4096, 5120, 152) == 7 and sp(1, 3840, 5120, 152) == 8 and sp(1, 3456, 5120, 152) == 0
-    assert sp(1, 10240, 256, 152) == 2                      # capped at the 2 k-blocks of K
-    assert sp(4, 512, 256, 152) == 2 and f(4, 512, 256, 152) == 4 * 2
+    assert sp(1, 10240, 384, 152) == 3                      # capped at the 3 k-blocks of K
+    assert sp(1, 12800, 384, 152) == 2
+    assert sp(1, 10240, 256, 152) == 1 and f(1, 10240, 256, 152) == 80    # K of 1-2 k-blocks: whole tiles
+    assert sp(4, 512, 256, 152) == 1 and f(4, 512, 256, 152) == 4
     assert sp(1, 8, 16, 152) == 1 and f(1, 8, 16, 152) == 1  # one unit
     # stream-K: few tiles with long K ranges
     assert sp(1, 128, 5120, 152) == 0

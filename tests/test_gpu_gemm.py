@@ -148,7 +148,7 @@ def test_down_projection_long_k(fp8, orc):
 # clusters of S CTAs per 128-channel tile (every S from 1 to 8, rows split
 # unevenly among the S CTAs for S = 3, 5, 6, 7; a ragged last tile; K ranges
 # split unevenly), or 0 for the persistent stream-K grid.
-DECODE_MODES = [(1, 34816, 1040, 1), (16, 10240, 256, 2), (3, 13312, 2064, 2), (16, 10232, 5136, 3),
+DECODE_MODES = [(1, 34816, 1040, 1), (16, 10240, 256, 1), (16, 12800, 400, 2), (3, 13312, 2064, 2), (16, 10232, 5136, 3),
                 (7, 8192, 1552, 3), (2, 7168, 4096, 4), (16, 6144, 1040, 5), (5, 5120, 8192, 6),
                 (4, 4096, 2064, 7), (11, 3840, 1552, 8),
                 (1, 128, 5120, 0), (16, 2048, 5120, 0), (9, 1032, 17408, 0),
