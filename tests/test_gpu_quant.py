@@ -35,6 +35,35 @@ def test_static_quant_every_bf16_value(fp8, orc, s):
     assert np.all((q[NAN_MASK] & 0x7F) == 0x7F)
 
 
+def test_static_quant_near_midpoints(fp8, orc):
+    """Quotients x / s within a few binary32 units of an E4M3 rounding midpoint
+    (where a reciprocal multiply could pick the other code): for 64 bf16 x and
+    midpoints across the whole range (the subnormal steps, 2^-10 next to zero,
+    the normal binades up to 432 below the saturation at 448), s is chosen so
+    that x0 / s lands 0, +-1, +-2 or +-4 units from the midpoint; every x of
+    the vector, the ones near midpoints and the others, bit-exact."""
+    g = workloads.rng(33)
+    xs = workloads.bf16_normal(g, (1, 64))
+    xs[0, :4] = [0x3F80, 0x4140, 0xBF80, 0x3C23]      # 1, 12, -1, ~0.01
+    e4 = orc.e4m3_decode(np.arange(0x00, 0x7F, dtype=np.uint8))   # 0 .. 448, ascending
+    mids = (e4[:-1] + e4[1:]) / 2.0
+    pick = np.unique(np.concatenate([mids[:10], mids[10::7], mids[-3:]]))
+    dev_x = to_dev_bf16(xs)
+    x_f = orc.bf16_to_f32(xs[0])
+    checked = 0
+    for j, m in enumerate(pick):
+        x0 = float(x_f[j % 4])
+        base = np.float32(abs(x0) / m)
+        for k in (0, 1, -1, 2, -2, 4, -4):
+            s = base
+            for _ in range(abs(k)):
+                s = np.nextafter(s, np.float32(np.inf) if k > 0 else np.float32(0), dtype=np.float32)
+            q = host_bits(fp8.quant_fp8_static(dev_x, to_dev_f32(float(s))))
+            assert np.array_equal(q, orc.quant_static(xs, float(s))), (m, k, float(s))
+            checked += 1
+    assert checked == 7 * len(pick)
+
+
 def test_static_quant_nan_encoding(fp8):
     """The hardware conversion's NaN code for a positive and a negative NaN."""
     x = np.zeros((1, 16), np.uint16)
