@@ -268,3 +268,29 @@ def test_decode_planner(L):
     assert f(0, 8, 16, 152) == -1 and sp(0, 8, 16, 152) == -1 and sp(33, 10240, 5120, 152) == -1
     assert sp(32, 10240, 5120, 152) == 3 and f(17, 10240, 5120, 152) == 240   # the 32-token tile, same plan
     assert f(32, 10240, 5120, 152) == f(32, 10240, 5120, 152)
+
+
+def test_decode_planner_properties(L):
+    """Random decode shapes and SM counts: cluster mode takes S = the floor
+    rule (at least 1, at most the k-blocks, 1 when K has at most two
+    k-blocks) with ceil(N/128) * S CTAs whenever that S is at most 8; else
+    stream-K with at most two CTAs per SM, never more CTAs than units, and at
+    least ceil(kb / 7) units per CTA (so at most 8 CTAs share a tile)."""
+    import random
+    rnd = random.Random(5)
+    f, sp = L.fp8_decode_ctas_for_sms, L.fp8_decode_split_for_sms
+    seen = set()
+    for _ in range(3000):
+        M, N, K = rnd.randint(1, 32), 8 * rnd.randint(1, 8000), 16 * rnd.randint(1, 4096)
+        sms = rnd.choice((1, 8, 132, 148, 152, 160))
+        tiles, kb = -(-N // 128), -(-K // 128)
+        S, c = sp(M, N, K, sms), f(M, N, K, sms)
+        rule = 1 if kb <= 2 else max(1, min((8 * sms // 5) // tiles, kb))
+        if rule <= 8:
+            assert (S, c) == (rule, tiles * rule), (M, N, K, sms)
+        else:
+            units = tiles * kb
+            assert S == 0 and 1 <= c <= min(2 * sms, units), (M, N, K, sms)
+            assert units // c >= -(-kb // 7), (M, N, K, sms)
+        seen.add(min(S, 2))
+    assert seen == {0, 1, 2}
