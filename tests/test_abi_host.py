@@ -294,3 +294,32 @@ def test_decode_planner_properties(L):
             assert units // c >= -(-kb // 7), (M, N, K, sms)
         seen.add(min(S, 2))
     assert seen == {0, 1, 2}
+
+
+def test_product_path_is_independent_of_the_oracle():
+    """The package never imports the oracle (no CPU fallback exists), and a
+    missing library is an error, not a silent alternative: loading the
+    binding and the library in a fresh interpreter leaves `oracle` unloaded,
+    and with the library file pointed elsewhere lib() raises."""
+    import subprocess
+    import sys
+    from fp8_w8a8_scaled_gb300 import build as b
+    b.build()
+    pkg = os.path.join(ROOT, "fp8_w8a8_scaled_gb300")
+    for name in os.listdir(pkg):
+        if name.endswith(".py"):
+            text = open(os.path.join(pkg, name)).read()
+            assert not re.search(r"^\s*(from|import)\s+oracle\b", text, flags=re.M), name
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "import fp8_w8a8_scaled_gb300 as f\n"
+            "f.lib()\n"
+            "assert 'oracle' not in sys.modules, 'oracle imported by the product path'\n"
+            "f._lib = None\n"
+            "f.lib_path = lambda: '/nonexistent/libfp8w8a8.so'\n"
+            "try:\n"
+            "    f.lib()\n"
+            "except RuntimeError:\n"
+            "    print('raised')\n" % ROOT)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip().endswith("raised"), r.stdout
