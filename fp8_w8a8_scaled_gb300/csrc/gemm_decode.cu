@@ -12,13 +12,13 @@
 // Design (GB300, sm_103a).  At decode M every weight byte is used M times, so
 // the kernel is bound by streaming B from HBM once, and every SM must stream
 // its equal share all the time.  The work is cut into units of one output tile
-// (128 weight rows x up to 16 tokens) by one 128-wide k-block, and given out
-// in one of two ways:
+// (128 weight rows x a 16- or 32-token tile) by one 128-wide k-block, and
+// given out in one of two ways:
 //   * cluster mode (enough tiles: N >= ~3840 on 152 SMs): a cluster of S CTAs
 //     per tile, CTA r taking k-blocks [r*kb/S, (r+1)*kb/S), with S chosen so
 //     the grid is ~1.6 CTAs per SM; the S parts are summed through
-//     distributed shared memory (below).  S = 1 (as many tiles as ~1.6 x SMs)
-//     is whole tiles, nothing to sum;
+//     distributed shared memory (below).  S = 1 (as many tiles as ~1.6 x SMs,
+//     or a K range of at most two k-blocks) is whole tiles, nothing to sum;
 //   * stream-K (few tiles with long K ranges): a persistent grid of two CTAs
 //     per SM gives CTA c the contiguous units [c*U/G, (c+1)*U/G), so all CTAs
 //     stream the same number of bytes whatever the shape.
@@ -27,7 +27,7 @@
 //     matching token boxes with TMA into a ring of shared-memory stages
 //     (128-byte swizzle), L2 evict-first for the once-read weights;
 //   * warp 1 / lane 0 issues tcgen05.mma kind::f8f6f4 with the WEIGHTS as the
-//     128-row A operand and the tokens (padded to 16) as the N side
+//     128-row A operand and the tokens (padded to 16 or 32) as the N side
 //     ("swap-AB").  Each k-block is accumulated from zero into one of several
 //     TMEM buffers; tcgen05.commit frees the stage and hands the buffer on;
 //   * 4 drain warps read each k-block's fp32 partial out of TMEM
@@ -45,8 +45,9 @@
 // acquires, sums all slots in k order (so the result does not depend on
 // arrival order), stores the tile and resets the counter.  Which CTAs share
 // the first and last tile of a CTA's range, and where their slots are, is
-// worked out while the first loads are in flight.  No CTA ever waits for
-// another.
+// worked out while the first loads are in flight.  No CTA ever spins on
+// another: the only cross-CTA wait is the hardware cluster barrier among the
+// co-scheduled CTAs of one cluster.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
