@@ -107,10 +107,12 @@ def lib():
     L.fp8_describe_dispatch.restype = I32
     L.fp8_decode_ctas.argtypes = [I64, I64, I64]
     L.fp8_decode_ctas.restype = I32
-    L.fp8_decode_split_for_sms.argtypes = [I64, I64, I64, I32]
+    L.fp8_decode_split_for_sms.argtypes = [I64, I64, I64, I32, I32]
     L.fp8_decode_split_for_sms.restype = I32
-    L.fp8_decode_ctas_for_sms.argtypes = [I64, I64, I64, I32]
+    L.fp8_decode_ctas_for_sms.argtypes = [I64, I64, I64, I32, I32]
     L.fp8_decode_ctas_for_sms.restype = I32
+    L.fp8_decode_exact_for_sms.argtypes = [I64, I64, I64, I32, I32]
+    L.fp8_decode_exact_for_sms.restype = I32
     L.fp8_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     L.fp8_get_device_error.restype = I32
     L.fp8_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P]
@@ -448,12 +450,23 @@ def decode_ctas(M, N, K) -> int:
     return lib().fp8_decode_ctas(M, N, K)
 
 
-def decode_split(M, N, K, num_sms=None) -> int:
-    """The decode kernel's mode: S >= 1 CTAs per output tile (clusters), 0 for
-    the persistent stream-K grid, -1 if the shape does not go to it."""
+def _sms(num_sms):
     if num_sms is None:
         num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    return lib().fp8_decode_split_for_sms(M, N, K, int(num_sms))
+    return int(num_sms)
+
+
+def decode_split(M, N, K, num_sms=None, granularity=GRAN_PER_CHANNEL) -> int:
+    """The decode kernel's mode: S >= 1 CTAs per output tile (clusters, blockwise
+    scaling only), 0 for a persistent stream-K grid, -1 if the shape does not
+    go to it."""
+    return lib().fp8_decode_split_for_sms(M, N, K, int(granularity), _sms(num_sms))
+
+
+def decode_exact(M, N, K, num_sms=None, granularity=GRAN_PER_CHANNEL) -> int:
+    """1 if the shape runs the exact-sum decode kernel, 0 for the TwoSum one,
+    -1 if it does not go to the decode kernel."""
+    return lib().fp8_decode_exact_for_sms(M, N, K, int(granularity), _sms(num_sms))
 
 
 def selftest_bounded_wait(timeout_us=1000):

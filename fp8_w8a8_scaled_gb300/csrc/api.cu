@@ -8,6 +8,7 @@
 #include <cudaTypedefs.h>
 #include <dlfcn.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -132,6 +133,12 @@ fp8_status make_tmap_bf16(CUtensorMap *tm, const void *ptr, int64_t rows, int64_
 
 fp8_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
 
+// Rows of the decode kernel's token boxes: the M real rows (the rest of its
+// token tiles stays zero).
+uint32_t decode_token_box_rows(const fp8k::DecodePlan &plan, int64_t M) {
+    return static_cast<uint32_t>(std::min<int64_t>(M, plan.tok_pad));
+}
+
 // The cuBLAS handle of this device (cuBLAS opened on first use).
 fp8_status blas_handle(DeviceState *st, cublasHandle_t *h) {
     std::lock_guard<std::mutex> lock(g_mu);
@@ -250,17 +257,26 @@ int fp8_describe_dispatch(int64_t M, int64_t N, int64_t K, int granularity) {
     if (M < 0 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > kI32Max) return -1;
     if (granularity < 0 || granularity > FP8_GRAN_BLOCK_128) return -1;
     if (M == 0) return FP8_KERNEL_NONE;
-    return M >= fp8k::kPrefillMinM ? FP8_KERNEL_PREFILL : FP8_KERNEL_DECODE_SPLITK;
+    if (M >= fp8k::kPrefillMinM) return FP8_KERNEL_PREFILL;
+    // the decode kernel's exact k-block sum holds fewer than 2^20 k-blocks
+    if (granularity != FP8_GRAN_BLOCK_128 && (K + fp8k::kBlockK - 1) / fp8k::kBlockK >= fp8k::kExactMaxKb)
+        return FP8_KERNEL_PREFILL;
+    return FP8_KERNEL_DECODE_SPLITK;
 }
 
-int fp8_decode_ctas_for_sms(int64_t M, int64_t N, int64_t K, int num_sms) {
-    if (fp8_describe_dispatch(M, N, K, 0) != FP8_KERNEL_DECODE_SPLITK || num_sms < 1) return -1;
-    return fp8k::plan_decode(M, N, K, num_sms).ctas;
+int fp8_decode_ctas_for_sms(int64_t M, int64_t N, int64_t K, int granularity, int num_sms) {
+    if (fp8_describe_dispatch(M, N, K, granularity) != FP8_KERNEL_DECODE_SPLITK || num_sms < 1) return -1;
+    return fp8k::plan_decode(M, N, K, num_sms, granularity == FP8_GRAN_BLOCK_128).ctas;
 }
 
-int fp8_decode_split_for_sms(int64_t M, int64_t N, int64_t K, int num_sms) {
-    if (fp8_describe_dispatch(M, N, K, 0) != FP8_KERNEL_DECODE_SPLITK || num_sms < 1) return -1;
-    return fp8k::plan_decode(M, N, K, num_sms).split;
+int fp8_decode_split_for_sms(int64_t M, int64_t N, int64_t K, int granularity, int num_sms) {
+    if (fp8_describe_dispatch(M, N, K, granularity) != FP8_KERNEL_DECODE_SPLITK || num_sms < 1) return -1;
+    return fp8k::plan_decode(M, N, K, num_sms, granularity == FP8_GRAN_BLOCK_128).split;
+}
+
+int fp8_decode_exact_for_sms(int64_t M, int64_t N, int64_t K, int granularity, int num_sms) {
+    if (fp8_describe_dispatch(M, N, K, granularity) != FP8_KERNEL_DECODE_SPLITK || num_sms < 1) return -1;
+    return fp8k::plan_decode(M, N, K, num_sms, granularity == FP8_GRAN_BLOCK_128).exact;
 }
 
 int fp8_decode_ctas(int64_t M, int64_t N, int64_t K) {
@@ -298,12 +314,12 @@ fp8_status fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, 
         return from_cuda(fp8k::launch_prefill_gemm(ta, tb, scale_a, scale_b, granularity, M, N, K, out, st->err,
                                                    plan, opts, static_cast<cudaStream_t>(stream)));
     }
-    const fp8k::DecodePlan plan = fp8k::plan_decode(M, N, K, st->num_sms);
+    const fp8k::DecodePlan plan = fp8k::plan_decode(M, N, K, st->num_sms, granularity == FP8_GRAN_BLOCK_128);
     fp8k::DecodeWorkspace ws;
     if ((s = decode_workspace(st, plan, &ws)) != FP8_OK) return s;
     CUtensorMap tw, ta;
     if ((s = make_tmap_e4m3(&tw, B, N, K, fp8k::kDecodeRows)) != FP8_OK) return s;
-    if ((s = make_tmap_e4m3(&ta, A, M, K, static_cast<uint32_t>(plan.tok_pad))) != FP8_OK) return s;
+    if ((s = make_tmap_e4m3(&ta, A, M, K, decode_token_box_rows(plan, M))) != FP8_OK) return s;
     return from_cuda(fp8k::launch_decode_gemm(tw, ta, scale_a, scale_b, granularity, M, N, K, out, st->err, plan,
                                               ws, opts, static_cast<cudaStream_t>(stream)));
 }
@@ -329,7 +345,7 @@ fp8_status fp8_scaled_mm_noalloc(const void *A, const void *B, const float *scal
     DeviceState *st = nullptr;
     fp8_status s = device_state(&st);
     if (s != FP8_OK) return s;
-    const fp8k::DecodePlan plan = fp8k::plan_decode(M, N, K, st->num_sms);
+    const fp8k::DecodePlan plan = fp8k::plan_decode(M, N, K, st->num_sms, granularity == FP8_GRAN_BLOCK_128);
     const size_t n_counters = fp8k::decode_counters_needed(plan);
     if (n_counters > kNoAllocCounters || fp8k::decode_slot_floats(plan) > kNoAllocSlotFloats)
         return FP8_ERR_TOO_LARGE;
@@ -343,7 +359,7 @@ fp8_status fp8_scaled_mm_noalloc(const void *A, const void *B, const float *scal
     if (cudaMemsetAsync(ws.counters, 0, n_counters * sizeof(uint32_t), cs) != cudaSuccess) return FP8_ERR_CUDA;
     CUtensorMap tw, ta;
     if ((s = make_tmap_e4m3(&tw, B, N, K, fp8k::kDecodeRows)) != FP8_OK) return s;
-    if ((s = make_tmap_e4m3(&ta, A, M, K, static_cast<uint32_t>(plan.tok_pad))) != FP8_OK) return s;
+    if ((s = make_tmap_e4m3(&ta, A, M, K, decode_token_box_rows(plan, M))) != FP8_OK) return s;
     return from_cuda(fp8k::launch_decode_gemm(tw, ta, scale_a, scale_b, granularity, M, N, K, out, st->err, plan,
                                               ws, fp8k::LaunchOpts{}, cs));
 }

@@ -88,6 +88,10 @@ constexpr int kGranBlock128 = 4;
 constexpr int kDecodeRows = 128;
 constexpr int kBlockK = 128;  // bytes (= E4M3 elements) of K per pipeline stage
 constexpr int kDecodeMaxTokens = 32;
+// The decode kernel's exact 32-bit accumulators hold the sums of fewer than
+// 2048 k-blocks (K <= 262,016); longer K goes to the tile kernel (blockwise
+// scaling, summed in binary32 TwoSum pairs, has no such limit).
+constexpr int64_t kExactMaxKb = 2048;
 
 struct DecodePlan {
     int tok_pad;      // tokens per tile on the MMA N side: 16 (M <= 16) or 32
@@ -99,14 +103,21 @@ struct DecodePlan {
     int ctas;         // stream-K: persistent CTAs, CTA c owning units [c*units/ctas, (c+1)*units/ctas);
                       // cluster mode: n_tiles * split
     int split;        // cluster mode: CTAs (one cluster) per output tile; 0 = stream-K
+    int exact;        // 1: the k-block partials are summed exactly as integers (every granularity but
+                      // blockwise), so the result does not depend on how K is divided among CTAs
     size_t smem_bytes;
 };
 
-DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, int num_sms);
+// The decode kernel's plan, a pure function of the shape, the scaling kind and
+// the SM count (the grid and its division of K are the same for both kinds;
+// blockwise scaling sums TwoSum parts, every other granularity exact ones).
+DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, int num_sms, bool blockwise = false);
 
 // Scratch of the decode kernel: a zeroed arrival counter per output tile, and
-// two partial-sum slots per CTA (128 x tok_pad fp32 each) for the tiles whose
-// K range is split between CTAs.  Every launch leaves the counters at zero.
+// two partial-sum slots per CTA (128 x tok_pad entries each: 64-bit integer
+// exact parts -- two floats' room -- or binary32 TwoSum parts for blockwise
+// scaling) for the tiles whose K range is split between CTAs under stream-K.
+// Every launch leaves the counters at zero.
 struct DecodeWorkspace {
     uint32_t *counters;
     float *slots;

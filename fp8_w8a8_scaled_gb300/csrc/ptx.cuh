@@ -138,6 +138,12 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// Orders this thread's earlier generic-proxy writes to shared memory before
+// later async-proxy accesses (TMA, tcgen05.mma operand reads) of it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

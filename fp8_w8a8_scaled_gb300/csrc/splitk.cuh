@@ -39,6 +39,7 @@ struct DecodeArgs {
     int64_t units;
     int gran, M, N, kb_total, n_tiles, stages, weights_static;
     int split;  // cluster mode: CTAs (one cluster) per tile; 0 in stream-K mode
+    int tok_rows;     // token rows a token box carries (M); the rest of the token tile stays zero
 };
 
 // Cluster mode: at most this many CTAs (parts) per tile.

@@ -401,25 +401,33 @@ const char *fp8_status_string(int status);
 int fp8_describe_dispatch(int64_t M, int64_t N, int64_t K, int granularity);
 
 /* Number of CTAs the decode kernel launches for this shape on the current
- * device, or -1 if the shape does not go to the decode kernel.  Host-only.
- * The decode kernel runs in one of two modes (see fp8_decode_split_for_sms):
- * clusters of S CTAs per 128-channel output tile, each CTA taking 1/S of the
- * tile's K range (ctas = ceil(N/128) * S), or a persistent grid over which the
- * K ranges of all tiles are divided evenly (stream-K). */
+ * device with per-tensor / per-channel / per-token scales, or -1 if the shape
+ * does not go to the decode kernel.  Host-only. */
 int fp8_decode_ctas(int64_t M, int64_t N, int64_t K);
 
-/* The same for a device with `num_sms` streaming multiprocessors; pure and
- * host-only (usable without a GPU). */
-int fp8_decode_ctas_for_sms(int64_t M, int64_t N, int64_t K, int num_sms);
-
-/* The decode kernel's mode for this shape on a device with `num_sms` SMs: S >=
- * 1 for clusters of S CTAs per output tile (S = 1: whole tiles, nothing to
- * sum), 0 for the persistent stream-K grid, -1 if the shape does not go to the
- * decode kernel.  With tiles = ceil(N/128), S = floor(floor(8 * num_sms / 5) /
- * tiles), at least 1 and at most ceil(K/128), and 1 when K <= 256 (two
- * k-blocks at most: whole tiles); clusters when S <= 8, stream-K otherwise.
- * Pure and host-only. */
-int fp8_decode_split_for_sms(int64_t M, int64_t N, int64_t K, int num_sms);
+/* The decode kernel's plan for this shape and granularity on a device with
+ * `num_sms` streaming multiprocessors; each returns -1 if the arguments do not
+ * go to the decode kernel.  Pure and host-only (usable without a GPU).
+ *
+ * The kernel runs in one of two modes: clusters of S CTAs per 128-row output
+ * tile, each CTA taking 1/S of the tile's K range (ctas = ceil(N/128) * S;
+ * fp8_decode_split_for_sms returns S), or a persistent stream-K grid of at
+ * most two CTAs per SM over which the (tile x 128-wide k-block) units are
+ * divided evenly (split returns 0; ctas = min(2 * num_sms, units /
+ * ceil(kb/7)) with kb = ceil(K/128), so at most 8 CTAs share a tile).  S =
+ * floor(floor(8 * num_sms / 5) / tiles), at least 1 and at most kb, and 1 when
+ * K <= 256; clusters when S <= 8, stream-K otherwise.  The plan is the same
+ * for every granularity.
+ *
+ * fp8_decode_exact_for_sms returns 1 when the tile sums are exact (every
+ * granularity but blockwise, K <= 262,016): each 128-wide k-block's binary32
+ * tensor-core partial is added as an integer multiple of 2^-18, so the result
+ * does not depend on how K is divided among CTAs (merged and split
+ * projections, and a token alone or in any batch of up to 32, give the same
+ * bits); 0 for blockwise scaling (k-block parts added with TwoSum). */
+int fp8_decode_ctas_for_sms(int64_t M, int64_t N, int64_t K, int granularity, int num_sms);
+int fp8_decode_split_for_sms(int64_t M, int64_t N, int64_t K, int granularity, int num_sms);
+int fp8_decode_exact_for_sms(int64_t M, int64_t N, int64_t K, int granularity, int num_sms);
 
 /* Device error word.  Kernels never trap: a bounded wait that runs out sets a
  * bit here and the kernel finishes without waiting further (its outputs are

@@ -233,6 +233,11 @@ def test_describe_dispatch_is_pure(L):
     for M in (33, 64, 65, 128, 2048, 8192):
         assert L.fp8_describe_dispatch(M, 10240, 5120, 1) == 2
         assert L.fp8_describe_dispatch(M, 34816, 5120, 2) == 2
+    # the decode kernel's exact sum holds fewer than 2048 k-blocks; longer K
+    # goes to the tile kernel (blockwise scaling keeps the decode kernel)
+    assert L.fp8_describe_dispatch(1, 8, 2048 * 128, 1) == 2
+    assert L.fp8_describe_dispatch(1, 8, 2047 * 128, 1) == 1
+    assert L.fp8_describe_dispatch(1, 8, 2048 * 128, 4) == 1
     # the same question twice gives the same answer (no hidden state)
     for M in (1, 33, 127, 128, 129, 2048, 8192):
         assert L.fp8_describe_dispatch(M, 10240, 5120, 2) == L.fp8_describe_dispatch(M, 10240, 5120, 2)
@@ -241,50 +246,57 @@ def test_describe_dispatch_is_pure(L):
 def test_decode_planner(L):
     """Cluster mode (S = floor(floor(8 * SMs / 5) / tiles) CTAs per
     128-channel tile, at least 1, at most the tile's k-blocks, 1 when K has
-    at most two k-blocks) when S <= 8;
-    else two persistent CTAs per SM (stream-K; never more CTAs than units of
-    one tile x one 128-wide k-block, and at most 8 CTAs per tile)."""
-    f = L.fp8_decode_ctas_for_sms
-    sp = L.fp8_decode_split_for_sms
-    # cluster mode (243 CTAs' worth of tiles on 152 SMs)
-    for M in (1, 16):
-        assert sp(M, 10240, 5120, 152) == 3 and f(M, 10240, 5120, 152) == 80 * 3
-    assert sp(16, 34816, 5120, 152) == 1 and f(16, 34816, 5120, 152) == 272    # whole tiles, no reduction
-    assert sp(8, 5120, 8192, 152) == 6 and f(8, 5120, 8192, 152) == 40 * 6
-    assert sp(8, 5120, 17408, 152) == 6
-    assert sp(1, 8192, 5120, 152) == 3 and sp(1, 7168, 5120, 152) == 4 and sp(1, 6144, 5120, 152) == 5
-    assert sp(1, 4096, 5120, 152) == 7 and sp(1, 3840, 5120, 152) == 8 and sp(1, 3456, 5120, 152) == 0
-    assert sp(1, 10240, 384, 152) == 3                      # capped at the 3 k-blocks of K
-    assert sp(1, 12800, 384, 152) == 2
-    assert sp(1, 10240, 256, 152) == 1 and f(1, 10240, 256, 152) == 80    # K of 1-2 k-blocks: whole tiles
-    assert sp(4, 512, 256, 152) == 1 and f(4, 512, 256, 152) == 4
-    assert sp(1, 8, 16, 152) == 1 and f(1, 8, 16, 152) == 1  # one unit
-    # stream-K: few tiles with long K ranges
-    assert sp(1, 128, 5120, 152) == 0
-    assert f(1, 128, 5120, 152) == 40 // 6                   # at least ceil(40/7) = 6 k-blocks per CTA
-    assert sp(1, 8, 65536, 152) == 0 and f(1, 8, 65536, 152) == 512 // 74
-    assert sp(16, 2048, 5120, 152) == 0 and f(16, 2048, 5120, 152) == 16 * 40 // 6
-    assert sp(5, 1032, 5120, 152) == 0
-    assert f(0, 8, 16, 152) == -1 and sp(0, 8, 16, 152) == -1 and sp(33, 10240, 5120, 152) == -1
-    assert sp(32, 10240, 5120, 152) == 3 and f(17, 10240, 5120, 152) == 240   # the 32-token tile, same plan
-    assert f(32, 10240, 5120, 152) == f(32, 10240, 5120, 152)
+    at most two k-blocks) when S <= 8; else two persistent CTAs per SM
+    (stream-K; never more CTAs than units of one tile x one 128-wide k-block,
+    and at most 8 CTAs per tile).  The same plan for every granularity; the
+    k-block sums are exact for all but blockwise scaling."""
+    f, sp, ex = L.fp8_decode_ctas_for_sms, L.fp8_decode_split_for_sms, L.fp8_decode_exact_for_sms
+    for g in (0, 1, 2, 3, 4):
+        assert ex(1, 10240, 5120, g, 152) == (0 if g == 4 else 1)
+        # cluster mode (243 CTAs' worth of tiles on 152 SMs)
+        for M in (1, 16):
+            assert sp(M, 10240, 5120, g, 152) == 3 and f(M, 10240, 5120, g, 152) == 80 * 3
+        assert sp(16, 34816, 5120, g, 152) == 1 and f(16, 34816, 5120, g, 152) == 272    # whole tiles
+        assert sp(8, 5120, 8192, g, 152) == 6 and f(8, 5120, 8192, g, 152) == 40 * 6
+        assert sp(8, 5120, 17408, g, 152) == 6
+        assert sp(1, 8192, 5120, g, 152) == 3 and sp(1, 7168, 5120, g, 152) == 4 and sp(1, 6144, 5120, g, 152) == 5
+        assert sp(1, 4096, 5120, g, 152) == 7 and sp(1, 3840, 5120, g, 152) == 8 and sp(1, 3456, 5120, g, 152) == 0
+        assert sp(1, 10240, 384, g, 152) == 3                     # capped at the 3 k-blocks of K
+        assert sp(1, 12800, 384, g, 152) == 2
+        assert sp(1, 10240, 256, g, 152) == 1 and f(1, 10240, 256, g, 152) == 80   # K of 1-2 k-blocks: whole tiles
+        assert sp(4, 512, 256, g, 152) == 1 and f(4, 512, 256, g, 152) == 4
+        assert sp(1, 8, 16, g, 152) == 1 and f(1, 8, 16, g, 152) == 1           # one unit
+        # stream-K: few tiles with long K ranges
+        assert sp(1, 128, 5120, g, 152) == 0
+        assert f(1, 128, 5120, g, 152) == 40 // 6                 # at least ceil(40/7) = 6 k-blocks per CTA
+        assert sp(1, 8, 65536, g, 152) == 0 and f(1, 8, 65536, g, 152) == 512 // 74
+        assert sp(16, 2048, 5120, g, 152) == 0 and f(16, 2048, 5120, g, 152) == 16 * 40 // 6
+        assert sp(5, 1032, 5120, g, 152) == 0
+        assert sp(32, 10240, 5120, g, 152) == 3 and f(17, 10240, 5120, g, 152) == 240   # the 32-token tile
+    assert f(0, 8, 16, 1, 152) == -1 and sp(0, 8, 16, 1, 152) == -1 and sp(33, 10240, 5120, 1, 152) == -1
+    assert ex(1, 8, 2048 * 128, 1, 152) == -1                 # 2048 k-blocks: the tile kernel
+    assert ex(1, 8, 2047 * 128, 1, 152) == 1
+    assert ex(1, 8, 2048 * 128, 4, 152) == 0                  # blockwise has no such limit
 
 
 def test_decode_planner_properties(L):
-    """Random decode shapes and SM counts: cluster mode takes S = the floor
-    rule (at least 1, at most the k-blocks, 1 when K has at most two
-    k-blocks) with ceil(N/128) * S CTAs whenever that S is at most 8; else
-    stream-K with at most two CTAs per SM, never more CTAs than units, and at
-    least ceil(kb / 7) units per CTA (so at most 8 CTAs share a tile)."""
+    """Random decode shapes, granularities and SM counts: cluster mode takes
+    S = the floor rule (at least 1, at most the k-blocks, 1 when K has at
+    most two k-blocks) with ceil(N/128) * S CTAs whenever that S is at most
+    8; else stream-K with at most two CTAs per SM, never more CTAs than units,
+    and at least ceil(kb / 7) units per CTA (so at most 8 CTAs share a tile);
+    exact sums for every granularity but blockwise."""
     import random
     rnd = random.Random(5)
-    f, sp = L.fp8_decode_ctas_for_sms, L.fp8_decode_split_for_sms
+    f, sp, ex = L.fp8_decode_ctas_for_sms, L.fp8_decode_split_for_sms, L.fp8_decode_exact_for_sms
     seen = set()
     for _ in range(3000):
         M, N, K = rnd.randint(1, 32), 8 * rnd.randint(1, 8000), 16 * rnd.randint(1, 4096)
         sms = rnd.choice((1, 8, 132, 148, 152, 160))
+        g = rnd.choice((0, 1, 2, 3, 4))
         tiles, kb = -(-N // 128), -(-K // 128)
-        S, c = sp(M, N, K, sms), f(M, N, K, sms)
+        S, c = sp(M, N, K, g, sms), f(M, N, K, g, sms)
+        assert ex(M, N, K, g, sms) == (0 if g == 4 else 1)
         rule = 1 if kb <= 2 else max(1, min((8 * sms // 5) // tiles, kb))
         if rule <= 8:
             assert (S, c) == (rule, tiles * rule), (M, N, K, sms)

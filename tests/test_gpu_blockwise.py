@@ -152,6 +152,26 @@ def test_block_gemm_random_codes(fp8, orc, M, N, K):
     block_check(orc, c["A"], c["B"], c["sa"], c["sb"], y, f"{M}x{N}x{K} blockwise")
 
 
+@pytest.mark.parametrize("M,N,K,S", [(1, 34816, 1040, 1), (16, 10240, 256, 1), (16, 12800, 400, 2),
+                                     (16, 10232, 5136, 3), (2, 7168, 4096, 4), (16, 6144, 1040, 5),
+                                     (5, 5120, 8192, 6), (4, 4096, 2064, 7), (11, 3840, 1552, 8),
+                                     (1, 128, 5120, 0), (9, 1032, 17408, 0), (32, 10240, 5120, 3),
+                                     (17, 5120, 8192, 6), (20, 1032, 4096, 0)])
+def test_block_decode_modes(fp8, orc, M, N, K, S):
+    """The blockwise decode kernel's modes on a 152-SM GB300 -- clusters of S
+    CTAs per 128-channel tile for every S from 1 to 8 (rows split unevenly
+    among the S CTAs for S = 3, 5, 6, 7; ragged last tiles; K ranges split
+    unevenly) and the stream-K grid (S = 0) -- every output against the
+    oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms == 152:
+        assert fp8.decode_split(M, N, K, sms, granularity=GRAN_BLOCK) == S
+    assert fp8.decode_exact(M, N, K, granularity=GRAN_BLOCK) == 0
+    c = workloads.random_gemm(8600 + M + N + K, M, N, K, GRAN_BLOCK)
+    y = run_block_mm(fp8, to_dev_e4m3(c["A"]), to_dev_e4m3(c["B"]), dev_scales(c["sa"]), dev_scales(c["sb"]))
+    block_check(orc, c["A"], c["B"], c["sa"], c["sb"], y, f"{M}x{N}x{K} blockwise split {S}")
+
+
 def test_block_gemm_scales_select_blocks(fp8, orc):
     """Scales zero everywhere but one (token, k-group) and one (weight block,
     k-group): only that group's products survive, in that block's outputs."""

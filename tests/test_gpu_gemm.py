@@ -160,17 +160,19 @@ DECODE_MODES = [(1, 34816, 1040, 1), (16, 10240, 256, 1), (16, 12800, 400, 2), (
 @pytest.mark.parametrize("M,N,K,S", DECODE_MODES)
 def test_decode_modes(fp8, orc, M, N, K, S):
     """Every output of both decode modes against the oracle, per-token x
-    per-channel scales.  Uniformly random codes are stress inputs: their
-    128-wide k-block sums are large next to the acceptance bound's absolute
-    term, and the tensor core's binary32 accumulation inside a k-block is
-    allowed its own bound (as on the tile kernel)."""
+    per-channel scales (exact k-block sums).  Uniformly random codes are
+    stress inputs: their 128-wide k-block sums are large next to the
+    acceptance bound's absolute term, and the tensor core's binary32
+    accumulation inside a k-block is allowed its own bound (as on the tile
+    kernel)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     if sms == 152:
-        assert fp8.decode_split(M, N, K, sms) == S
+        assert fp8.decode_split(M, N, K, sms, granularity=2) == S
+    assert fp8.decode_exact(M, N, K, granularity=2) == 1
     c = workloads.random_gemm(7000 + M + N + K, M, N, K, 2)
     y = run_mm(fp8, to_dev_e4m3(c["A"]), to_dev_e4m3(c["B"]), to_dev_f32(c["sa"]), to_dev_f32(c["sb"]), 2)
     worst, _ = full_check(orc, c["A"], c["B"], c["sa"], c["sb"], 2, y, f"{M}x{N}x{K} split {S}", tc_bound=True)
-    print(f"{M}x{N}x{K} split {fp8.decode_split(M, N, K)}: max err/bound {worst:.4f}")
+    print(f"{M}x{N}x{K} split {fp8.decode_split(M, N, K, granularity=2)}: max err/bound {worst:.4f}")
 
 
 # ----------------------------------------------------------------------------- ragged shapes
@@ -276,8 +278,10 @@ def test_graph_replay_equals_eager(fp8):
 
 
 def test_merged_equals_split(fp8, orc):
-    """QKV as one GEMM over [Wq; Wk; Wv] against three GEMMs: both within the
-    bound of the oracle (the K ranges are divided differently, so not bitwise)."""
+    """QKV as one GEMM over [Wq; Wk; Wv] against three GEMMs: bitwise equal
+    (the decode kernel sums each tile's k-block partials exactly, so how the
+    K ranges are divided among CTAs -- different for the three shapes -- does
+    not change a bit), and both within the bound of the oracle."""
     M, K = 8, 5120
     d = workloads.decode_fused(seed=2)
     B = d["B"]
@@ -292,8 +296,9 @@ def test_merged_equals_split(fp8, orc):
     split = np.concatenate(parts, axis=1)
     y64, _ = orc.scaled_mm(A, B, d["s_a"], d["sb"], 1)
     sab = scale_product(d["s_a"], d["sb"], 1, np.arange(M)[:, None], np.arange(10240)[None, :])
+    assert fp8.decode_split(M, 10240, K) != fp8.decode_split(M, workloads.KV_WIDTH, K)
+    assert np.array_equal(merged, split)
     check_gemm(merged, y64, sab, K, "merged")
-    check_gemm(split, y64, sab, K, "split")
 
 
 def test_batch_rows_independent(fp8):
@@ -309,6 +314,22 @@ def test_batch_rows_independent(fp8):
         one = run_mm(fp8, A[m:m + 1].contiguous(), B, sa, sb, 1)
         assert fp8.decode_ctas(1, N, K) == fp8.decode_ctas(16, N, K)
         assert np.array_equal(one[0], full[m])
+
+
+def test_batch_rows_independent_across_token_tiles(fp8):
+    """Row m of an M=32 call (32-token tile) against the same row alone (M=1,
+    16-token tile): the k-block partials come from MMAs of different widths
+    but the same operands, and the exact sum makes the division of K
+    irrelevant, so the decode kernel is batch-invariant over M <= 32."""
+    N, K = 10240, 5120
+    c = workloads.random_gemm(64, 32, N, K, 2)
+    A = to_dev_e4m3(c["A"])
+    B = to_dev_e4m3(c["B"])
+    sa, sb = to_dev_f32(c["sa"]), to_dev_f32(c["sb"])
+    full = run_mm(fp8, A, B, sa, sb, 2)
+    for m in (0, 16, 31):
+        one = run_mm(fp8, A[m:m + 1].contiguous(), B, sa[m:m + 1].contiguous(), sb, 2)
+        assert np.array_equal(one[0], full[m]), m
 
 
 def test_m_zero_is_noop(fp8):
