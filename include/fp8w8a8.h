@@ -189,10 +189,14 @@ fp8_status fp8_scaled_mm_noalloc(const void *A, const void *B, const float *scal
  *   out      E4M3 [M,K], 16-byte aligned
  *   K % 16 == 0, 1 <= K <= 65536
  *
- * Per row: ss = sum x^2 in binary64; r = fp32(1 / sqrt(ss/K + eps)) in
- * binary64; h = bf16_rne((x * r) * gamma) in binary32; q = e4m3_rne_sat(h / s)
- * with an IEEE binary32 division.  The bytes equal "RMSNorm to bf16, then
- * quant_fp8_static" exactly. */
+ * Per row: ss = the exact sum of the squares of the row's bf16 values, rounded
+ * once to binary32 (round to nearest even); then mean = ss / K, t = mean + eps,
+ * d = sqrt(t), r = 1 / d, each one IEEE binary32 operation rounded to nearest
+ * even; h = bf16_rne((x * r) * gamma) with two binary32 multiplies (no fused
+ * multiply-add); q = e4m3_rne_sat(h / s) with an IEEE binary32 division.  The
+ * bytes equal "RMSNorm to bf16, then quant_fp8_static" exactly.  With eps = 0
+ * a row whose mean square underflows to zero in binary32 has r = inf: its
+ * nonzero elements saturate to +-448 and its zero elements give NaN codes. */
 fp8_status rmsnorm_quant_fp8(const void *x, const void *gamma, float eps, const float *scale, void *out,
                              int64_t M, int64_t K, void *stream);
 

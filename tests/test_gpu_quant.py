@@ -170,6 +170,22 @@ def test_rmsnorm_quant_shapes(fp8, orc, M, K, eps, s):
     assert np.array_equal(q, want)
 
 
+def test_rmsnorm_eps0_underflow_row(fp8, orc):
+    """eps = 0 and rows whose mean square underflows binary32 (elements +-2^-126
+    or 0, at two row lengths): r = inf, nonzero elements saturate to +-448
+    and zero elements give a NaN code, as in the oracle (any NaN code for
+    NaN)."""
+    for K in (64, 5120):
+        rows = np.full((2, K), 0x0080, np.uint16)
+        rows[0, 3] = 0x0000
+        rows[1, 5::7] = 0x8080
+        gamma = np.full(K, 0x3FC0, np.uint16)
+        q = host_bits(fp8.rmsnorm_quant_fp8(to_dev_bf16(rows), to_dev_bf16(gamma), 0.0, to_dev_f32(1 / 56)))
+        want = orc.rmsnorm_quant(rows, gamma, 0.0, float(np.float32(1 / 56)))
+        nan = (want & 0x7F) == 0x7F
+        assert np.array_equal(q[~nan], want[~nan]) and np.all((q[nan] & 0x7F) == 0x7F)
+
+
 def test_rmsnorm_fused_equals_unfused(fp8, orc):
     """Fused norm-quant == static quant of the bf16 norm output, byte for byte
     (the norm output comes from the oracle; the quant runs on the GPU)."""

@@ -109,14 +109,33 @@ def test_rmsnorm_closed_forms(orc):
     spike[7] = 0x40A0                                   # 5.0
     cases.append(spike)
     gamma = np.full(K, 0x3FC0, np.uint16)               # 1.5
+    # 2^-126: the squares (2^-252) underflow binary32 and the sum of squares
+    # rounds to zero; with eps > 0 the chain is defined and lands within one
+    # bf16 rounding of the exact value, whose mean square is negligible next to eps
+    tiny = np.full(K, 0x0080, np.uint16)
     for eps in (1e-6, 0.0, 0.25):
-        for row in cases:
+        for row in cases + ([tiny] if eps > 0 else []):
             h = orc.rmsnorm_bf16(row[None, :], gamma, eps)[0]
             hv = _as_f32(h)
             for k in (0, 7):
                 want = _rms_exact(_as_f32(row), eps, 1.5, k)
                 ulp = 2.0 ** (math.floor(math.log2(abs(want))) - 7) if want != 0 else 0.0
                 assert abs(float(hv[k]) - want) <= ulp, (row[:2], eps, k, hv[k], want)
+    assert orc.sum_squares_bf16(tiny) == 0.0
+
+
+def test_rmsnorm_eps0_underflow_row(orc):
+    """eps = 0 and a row whose mean square underflows binary32 (every element
+    +-2^-126 or 0): the sum of squares rounds to 0, r = 1/sqrt(0) = +inf, so
+    a nonzero element becomes +-inf and saturates to +-448 and a zero element
+    becomes 0 * inf = NaN (the NaN code) -- IEEE semantics of the stated chain."""
+    row = np.full((1, 64), 0x0080, np.uint16)
+    row[0, 3] = 0x0000
+    row[0, 5] = 0x8080
+    gamma = np.full(64, 0x3FC0, np.uint16)
+    q = orc.rmsnorm_quant(row, gamma, 0.0, float(np.float32(1 / 56)))[0]
+    assert q[0] == 0x7E and q[5] == 0xFE and (q[3] & 0x7F) == 0x7F
+    assert np.all(q[[1, 2, 4, 6, 63]] == 0x7E)
 
 
 def test_rmsnorm_scale_invariance(orc):
