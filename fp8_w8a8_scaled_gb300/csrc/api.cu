@@ -40,17 +40,25 @@ __global__ void bounded_wait_probe_kernel(uint32_t *err, unsigned long long time
 constexpr int kMaxDevices = 64;
 constexpr int64_t kI32Max = 2147483647;
 
-// Scratch of the decode kernel, allocated once per device on the first GEMM
-// call: arrival counters (zero between launches) and partial-sum slots.
+// Scratch of the split-K kernels' stream-K mode (arrival counters, zero
+// between launches, and partial-sum slots), one per stream that runs such a
+// launch, allocated on that stream's first one: launches on different streams
+// never share it, so they may overlap.
 constexpr size_t kWsCounters = size_t(1) << 20;
+constexpr int kMaxStreamWorkspaces = 64;
+
+struct StreamWorkspace {
+    cudaStream_t stream = nullptr;
+    uint32_t *counters = nullptr;
+    float *slots = nullptr;
+};
 
 struct DeviceState {
     bool ready = false;
     int num_sms = 0;
     uint32_t *err = nullptr;
-    uint32_t *counters = nullptr;
-    float *slots = nullptr;
-    size_t n_slots = 0;
+    StreamWorkspace ws[kMaxStreamWorkspaces];
+    int n_ws = 0;
     void *w16 = nullptr;  // the weight-only large-M branch's bf16 weight (grow-only)
     size_t w16_bytes = 0;
     cublasHandle_t blas = nullptr;
@@ -178,42 +186,53 @@ fp8_status w16_buffer(DeviceState *st, size_t bytes, void **out) {
     return FP8_OK;
 }
 
-// The decode kernel's workspace for this device: sized for the largest plan
-// (two CTAs per SM, 32-token tiles), allocated and zeroed on first use.
-fp8_status decode_workspace(DeviceState *st, const fp8k::DecodePlan &plan, fp8k::DecodeWorkspace *ws) {
+// The stream-K scratch of `stream` on this device (none for cluster plans):
+// sized for the largest plan (two CTAs per SM, 32-token tiles, 64-bit parts),
+// allocated on the stream's first stream-K launch with its counters zeroed on
+// that stream (no device-wide synchronisation).
+fp8_status decode_workspace(DeviceState *st, const fp8k::DecodePlan &plan, cudaStream_t stream,
+                            fp8k::DecodeWorkspace *ws) {
+    ws->counters = nullptr;
+    ws->slots = nullptr;
+    if (plan.split > 0) return FP8_OK;  // cluster mode: parts summed in distributed shared memory
     if (fp8k::decode_counters_needed(plan) > kWsCounters) return FP8_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (st->counters == nullptr) {
-        const size_t n_slots = 2u * 2u * static_cast<size_t>(st->num_sms) * fp8k::kDecodeMaxTokens * fp8k::kDecodeRows;
+    const size_t n_slots = 2u * 2u * 2u * static_cast<size_t>(st->num_sms) * fp8k::kDecodeMaxTokens * fp8k::kDecodeRows;
+    if (fp8k::decode_slot_floats(plan) > n_slots) return FP8_ERR_UNSUPPORTED;
+    StreamWorkspace *w = nullptr;
+    for (int i = 0; i < st->n_ws; ++i)
+        if (st->ws[i].stream == stream) w = &st->ws[i];
+    if (w == nullptr) {
+        if (st->n_ws == kMaxStreamWorkspaces) return FP8_ERR_UNSUPPORTED;
         void *c = nullptr, *sl = nullptr;
         if (cudaMalloc(&c, kWsCounters * sizeof(uint32_t)) != cudaSuccess) return FP8_ERR_CUDA;
         if (cudaMalloc(&sl, n_slots * sizeof(float)) != cudaSuccess) {
             cudaFree(c);
             return FP8_ERR_CUDA;
         }
-        if (cudaMemset(c, 0, kWsCounters * sizeof(uint32_t)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        if (cudaMemsetAsync(c, 0, kWsCounters * sizeof(uint32_t), stream) != cudaSuccess) {
             cudaFree(c);
             cudaFree(sl);
             return FP8_ERR_CUDA;
         }
-        st->counters = static_cast<uint32_t *>(c);
-        st->slots = static_cast<float *>(sl);
-        st->n_slots = n_slots;
+        w = &st->ws[st->n_ws++];
+        w->stream = stream;
+        w->counters = static_cast<uint32_t *>(c);
+        w->slots = static_cast<float *>(sl);
     }
-    if (fp8k::decode_slot_floats(plan) > st->n_slots) return FP8_ERR_UNSUPPORTED;
-    ws->counters = st->counters;
-    ws->slots = st->slots;
+    ws->counters = w->counters;
+    ws->slots = w->slots;
     return FP8_OK;
 }
-
 // ---------------------------------------------------------------- fixed scratch
 // Scratch of fp8_scaled_mm_noalloc: arrival counters then partial-sum slots
 // of the decode kernel, in one file-scope device array.  The module holds one
 // copy per device that loads the library, from load until the process exits.
 // In host code the array's name is only a host-side stand-in: its device
 // address comes from cudaGetSymbolAddress with the device current.
-constexpr size_t kNoAllocCounters = 16384;                 // output tiles
-constexpr size_t kNoAllocSlotFloats = 384u * 2u * 16u * 128u;  // 384 CTAs x 2 slots x 16 tokens x 128 rows
+constexpr size_t kNoAllocCounters = 16384;  // output tiles
+// 384 CTAs x 2 slots x 16 tokens x 128 rows of 64-bit exact parts (two floats' room each)
+constexpr size_t kNoAllocSlotFloats = 384u * 2u * 16u * 128u * 2u;
 constexpr size_t kNoAllocBytes = kNoAllocCounters * sizeof(uint32_t) + kNoAllocSlotFloats * sizeof(float);
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
@@ -232,6 +251,21 @@ fp8_status noalloc_scratch(void **out) {
     }
     *out = g_noalloc_ptr[dev];
     return FP8_OK;
+}
+
+// The tile (large-M) kernel's launch for fp8_scaled_mm's arguments (already
+// validated); it uses no scratch.
+fp8_status tile_gemm(DeviceState *st, const void *A, const void *B, const float *scale_a, const float *scale_b,
+                     int granularity, int64_t M, int64_t N, int64_t K, void *out, const fp8k::LaunchOpts &opts,
+                     cudaStream_t stream) {
+    const fp8k::PrefillPlan plan = fp8k::plan_prefill(M, N, K, st->num_sms);
+    if (static_cast<int64_t>(plan.m_tiles) * plan.n_tiles > kI32Max) return FP8_ERR_UNSUPPORTED;
+    CUtensorMap ta, tb;
+    fp8_status s;
+    if ((s = make_tmap_e4m3(&ta, A, M, K, fp8k::kPrefillBM)) != FP8_OK) return s;
+    if ((s = make_tmap_e4m3(&tb, B, N, K, static_cast<uint32_t>(plan.bn))) != FP8_OK) return s;
+    return from_cuda(fp8k::launch_prefill_gemm(ta, tb, scale_a, scale_b, granularity, M, N, K, out, st->err, plan,
+                                               opts, stream));
 }
 
 }  // namespace
@@ -305,18 +339,11 @@ fp8_status fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, 
     fp8k::LaunchOpts opts;
     opts.pdl = (flags & FP8_FLAG_NO_PDL) == 0;
     opts.weights_static = (flags & FP8_FLAG_WEIGHTS_STATIC) != 0;
-    if (fp8_describe_dispatch(M, N, K, granularity) == FP8_KERNEL_PREFILL) {
-        const fp8k::PrefillPlan plan = fp8k::plan_prefill(M, N, K, st->num_sms);
-        if (static_cast<int64_t>(plan.m_tiles) * plan.n_tiles > kI32Max) return FP8_ERR_UNSUPPORTED;
-        CUtensorMap ta, tb;
-        if ((s = make_tmap_e4m3(&ta, A, M, K, fp8k::kPrefillBM)) != FP8_OK) return s;
-        if ((s = make_tmap_e4m3(&tb, B, N, K, static_cast<uint32_t>(plan.bn))) != FP8_OK) return s;
-        return from_cuda(fp8k::launch_prefill_gemm(ta, tb, scale_a, scale_b, granularity, M, N, K, out, st->err,
-                                                   plan, opts, static_cast<cudaStream_t>(stream)));
-    }
+    if (fp8_describe_dispatch(M, N, K, granularity) == FP8_KERNEL_PREFILL)
+        return tile_gemm(st, A, B, scale_a, scale_b, granularity, M, N, K, out, opts, static_cast<cudaStream_t>(stream));
     const fp8k::DecodePlan plan = fp8k::plan_decode(M, N, K, st->num_sms, granularity == FP8_GRAN_BLOCK_128);
     fp8k::DecodeWorkspace ws;
-    if ((s = decode_workspace(st, plan, &ws)) != FP8_OK) return s;
+    if ((s = decode_workspace(st, plan, static_cast<cudaStream_t>(stream), &ws)) != FP8_OK) return s;
     CUtensorMap tw, ta;
     if ((s = make_tmap_e4m3(&tw, B, N, K, fp8k::kDecodeRows)) != FP8_OK) return s;
     if ((s = make_tmap_e4m3(&ta, A, M, K, decode_token_box_rows(plan, M))) != FP8_OK) return s;
@@ -345,6 +372,11 @@ fp8_status fp8_scaled_mm_noalloc(const void *A, const void *B, const float *scal
     DeviceState *st = nullptr;
     fp8_status s = device_state(&st);
     if (s != FP8_OK) return s;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // a K too long for the decode kernel's exact sums: the tile kernel, which
+    // uses no scratch
+    if (fp8_describe_dispatch(M, N, K, granularity) == FP8_KERNEL_PREFILL)
+        return tile_gemm(st, A, B, scale_a, scale_b, granularity, M, N, K, out, fp8k::LaunchOpts{}, cs);
     const fp8k::DecodePlan plan = fp8k::plan_decode(M, N, K, st->num_sms, granularity == FP8_GRAN_BLOCK_128);
     const size_t n_counters = fp8k::decode_counters_needed(plan);
     if (n_counters > kNoAllocCounters || fp8k::decode_slot_floats(plan) > kNoAllocSlotFloats)
@@ -354,9 +386,9 @@ fp8_status fp8_scaled_mm_noalloc(const void *A, const void *B, const float *scal
     fp8k::DecodeWorkspace ws;
     ws.counters = static_cast<uint32_t *>(scratch);
     ws.slots = reinterpret_cast<float *>(static_cast<unsigned char *>(scratch) + kNoAllocCounters * sizeof(uint32_t));
-    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     // the counters must start at zero; the previous call may have been cut short
-    if (cudaMemsetAsync(ws.counters, 0, n_counters * sizeof(uint32_t), cs) != cudaSuccess) return FP8_ERR_CUDA;
+    if (n_counters > 0 && cudaMemsetAsync(ws.counters, 0, n_counters * sizeof(uint32_t), cs) != cudaSuccess)
+        return FP8_ERR_CUDA;
     CUtensorMap tw, ta;
     if ((s = make_tmap_e4m3(&tw, B, N, K, fp8k::kDecodeRows)) != FP8_OK) return s;
     if ((s = make_tmap_e4m3(&ta, A, M, K, decode_token_box_rows(plan, M))) != FP8_OK) return s;
@@ -534,7 +566,7 @@ fp8_status fp8_w8a16_mm_ex(const void *x, const void *W, const float *scale_b, i
     }
     const fp8k::DecodePlan plan = fp8k::plan_w8a16(M, N, K, st->num_sms);
     fp8k::DecodeWorkspace ws;
-    if ((s = decode_workspace(st, plan, &ws)) != FP8_OK) return s;
+    if ((s = decode_workspace(st, plan, cs, &ws)) != FP8_OK) return s;
     CUtensorMap tw, tx;
     if ((s = make_tmap_e4m3(&tw, W, N, K, fp8k::kDecodeRows)) != FP8_OK) return s;
     if ((s = make_tmap_bf16(&tx, x, M, K, static_cast<uint32_t>(plan.tok_pad))) != FP8_OK) return s;
@@ -618,7 +650,11 @@ fp8_status fp8_clear_device_error(void) {
     if (s != FP8_OK) return s;
     if (cudaMemset(st->err, 0, sizeof(uint32_t)) != cudaSuccess) return FP8_ERR_CUDA;
     // a kernel that gave up may have left arrival counters behind
-    if (st->counters && cudaMemset(st->counters, 0, kWsCounters * sizeof(uint32_t)) != cudaSuccess) return FP8_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        for (int i = 0; i < st->n_ws; ++i)
+            if (cudaMemset(st->ws[i].counters, 0, kWsCounters * sizeof(uint32_t)) != cudaSuccess) return FP8_ERR_CUDA;
+    }
     return cudaDeviceSynchronize() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

@@ -114,11 +114,17 @@ typedef enum {
  * pure function of (M, N, K, granularity), see fp8_describe_dispatch, so a
  * captured CUDA graph replays the same kernel the eager call would run:
  * M <= 32 the weight-streaming decode kernel (16-token tile for M <= 16,
- * 32-token tile above; its stream-K mode uses the library's scratch area),
- * M >= 33 the tensor-core tile kernel (uses no scratch).  For a fixed M the
- * result is deterministic (bitwise the same on every run); on the tile kernel
- * row m does not depend on the other rows of A, and on the decode kernel
- * neither within one token tile size (M <= 16, or 17 <= M <= 32).
+ * 32-token tile above), M >= 33 the tensor-core tile kernel.  The decode
+ * kernel's stream-K mode (few 128-row tiles with a long K, see
+ * fp8_decode_split_for_sms) uses scratch memory: one area per stream, about
+ * 20 MB, allocated on that stream's first stream-K call (cudaMalloc, counters
+ * zeroed with cudaMemsetAsync on the stream), for at most 64 streams per device
+ * (FP8_ERR_UNSUPPORTED beyond); calls on different streams may overlap.  Its
+ * cluster mode and the tile kernel use none.  The result is deterministic
+ * (bitwise the same on every run); row m does not depend on the other rows of
+ * A (on the decode kernel for any M <= 32, on the tile kernel for any M >= 33),
+ * and, with exact sums (every granularity but blockwise), a projection split
+ * along N gives the same bits as the merged one.
  * Errors: FP8_ERR_INVALID_ARG, FP8_ERR_ALIGNMENT, FP8_ERR_UNSUPPORTED,
  * FP8_ERR_CUDA. */
 fp8_status fp8_scaled_mm(const void *A, const void *B, const float *scale_a, const float *scale_b,
@@ -151,25 +157,30 @@ fp8_status fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, 
  * not call cudaMalloc at all: code running inside a memory pool or arena
  * that must own every device allocation, hosts whose allocator is locked
  * while a CUDA graph is being built, or embedders that forbid hidden
- * allocations.  fp8_scaled_mm allocates its ~9 MB scratch on first use; this
- * entry point instead uses a fixed scratch area compiled into the library (a
- * file-scope device array of 6 MB + 64 KB that every GPU which loads the
- * library holds until the process exits), and never calls cudaMalloc,
- * cudaFree or any allocating routine.
+ * allocations.  fp8_scaled_mm allocates a per-stream scratch area on a
+ * stream's first stream-K call; this entry point instead uses a fixed scratch
+ * area compiled into the library (a file-scope device array of 12 MB + 64 KB
+ * that every GPU which loads the library holds until the process exits), and
+ * never calls cudaMalloc, cudaFree or any allocating routine.
  *
- * Arguments, layouts and results are those of fp8_scaled_mm (same kernel, so
- * the same bytes).  Limits of the fixed area: M <= 16, at most 16384 output
- * tiles of 128 rows (N <= 2,097,152), and at most 384 streaming CTAs (any
- * GPU with up to 192 SMs); larger problems return FP8_ERR_TOO_LARGE without
- * launching anything.
+ * Arguments, layouts and results are those of fp8_scaled_mm (same kernel,
+ * same plan, so the same bytes).  Limits: M <= 16 (else FP8_ERR_TOO_LARGE).
+ * Only the decode kernel's stream-K mode uses the fixed area: it needs one
+ * arrival counter per 128-row output tile (at most 16384 tiles) and two slots
+ * of 16 x 128 partial sums per CTA (at most 384 CTAs: its grid has at most
+ * two CTAs per SM, so any GPU with up to 192 SMs); beyond that it returns
+ * FP8_ERR_TOO_LARGE without launching anything.  Cluster-mode shapes (most
+ * shapes, see fp8_decode_split_for_sms) use none of it and have no further
+ * limit.
  *
  * The first call on a device looks up the device address of the scratch area
  * for that device (cudaGetSymbolAddress), so make the first call on each
- * device before capturing a CUDA graph.  Every call zeroes the area's arrival
- * counters on `stream` before its kernel.  All calls share the one area and
- * it keeps the last call's contents: calls that may run at the same time on
- * the GPU (different streams, no ordering) race and give wrong results;
- * order them.  Errors: those of fp8_scaled_mm, plus FP8_ERR_TOO_LARGE. */
+ * device before capturing a CUDA graph.  Every stream-K call zeroes the area's
+ * arrival counters on `stream` before its kernel.  All calls share the one
+ * area and it keeps the last call's contents: calls that may run at the same
+ * time on the GPU (different streams, no ordering) race and give wrong
+ * results; order them.  Errors: those of fp8_scaled_mm, plus
+ * FP8_ERR_TOO_LARGE. */
 fp8_status fp8_scaled_mm_noalloc(const void *A, const void *B, const float *scale_a, const float *scale_b,
                                  int granularity, int out_dtype, int64_t M, int64_t N, int64_t K, void *out,
                                  void *stream);

@@ -332,6 +332,30 @@ def test_batch_rows_independent_across_token_tiles(fp8):
         assert np.array_equal(one[0], full[m]), m
 
 
+def test_stream_k_on_two_streams(fp8):
+    """Stream-K launches (few 128-row tiles with a long K: the mode that uses
+    scratch) issued back to back on two streams at once: each stream has its
+    own scratch, so every result equals the serial one bit for bit."""
+    cases = []
+    for i, (M, N, K) in enumerate([(16, 2048, 5120), (9, 1032, 17408)]):
+        assert fp8.decode_split(M, N, K, granularity=2) == 0
+        c = workloads.random_gemm(65 + i, M, N, K, 2)
+        args = (to_dev_e4m3(c["A"]), to_dev_e4m3(c["B"]), to_dev_f32(c["sa"]), to_dev_f32(c["sb"]), 2)
+        cases.append((args, run_mm(fp8, *args)))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    outs = [[], []]
+    for _ in range(8):
+        for j, s in enumerate(streams):
+            with torch.cuda.stream(s):
+                outs[j].append(fp8.fp8_scaled_mm(*cases[j][0]))
+    torch.cuda.synchronize()
+    for j in range(2):
+        for o in outs[j]:
+            assert np.array_equal(host_bits(o), cases[j][1]), j
+
+
 def test_m_zero_is_noop(fp8):
     A = torch.empty((0, 64), dtype=torch.float8_e4m3fn, device="cuda")
     B = torch.zeros((64, 64), dtype=torch.float8_e4m3fn, device="cuda")
