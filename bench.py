@@ -472,15 +472,16 @@ def decode_step_weights(torch, device):
     return Wl
 
 
-def decode_step_fn(torch, fp8, device, Wl, M):
+def decode_step_fn(torch, fp8, device, Wl, M, buffers=None):
     """One synthetic decode step at M tokens over the layers' weights Wl:
     per layer RMSNorm -> static quant -> QKV, per-token quant of an [M, 8192]
     stub (the attention output, not on this path) -> O, gate_up on the same
     normalised input, SiLU(gate) * up -> per-token quant -> down (7 launches
-    per layer)."""
+    per layer).  If `buffers` is a dict, the step's inputs, intermediates and
+    outputs are put in it (for checking one layer against the oracle)."""
     shapes = workloads.LayerShapes()
     K = K_HID
-    gamma = workloads.device_bf16_normal(torch, (K,), seed=30000, device=device, std=0.1)
+    gamma = workloads.device_bf16_normal(torch, (K,), seed=30000, device=device, std=0.1, mean=1.0)
     s_a = torch.tensor([float(workloads.STATIC_INPUT_SCALE)], dtype=torch.float32, device=device)
     x = workloads.device_bf16_normal(torch, (M, K), seed=30001, device=device)
     o_in = workloads.device_bf16_normal(torch, (M, workloads.O_K), seed=30002, device=device)
@@ -492,6 +493,8 @@ def decode_step_fn(torch, fp8, device, Wl, M):
     y = [torch.empty((M, n), dtype=torch.bfloat16, device=device)
          for (n, _) in (shapes.qkv, shapes.o, shapes.gate_up, shapes.down)]
     st = fp8.FLAG_WEIGHTS_STATIC
+    if buffers is not None:
+        buffers.update(x=x, gamma=gamma, s_a=s_a, o_in=o_in, a=a, a_o=a_o, s_o=s_o, a_d=a_d, s_d=s_d, y=y)
 
     def step(_i):
         for ws in Wl:

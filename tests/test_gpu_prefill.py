@@ -1,7 +1,8 @@
 """GPU parity of the large-M (prefill) GEMM kernel against the CPU oracle:
 prefill-chunk data at the acceptance bound (ragged shapes and the largest
-workload shape), stress inputs (outlier-free activations, uniformly random
-codes) at the acceptance bound plus the binary32 accumulation bound, more
+workload shape), outlier-free quantised data at the acceptance bound (and,
+at M 2048, where a few near-zero outputs exceed it, at the acceptance bound
+plus the binary32 accumulation bound), uniformly random codes at the latter, more
 tiles than SMs (each persistent CTA walks several tiles through both TMEM
 accumulators), every scale granularity, the decode/prefill dispatch
 boundary, and the invariants the kernel's fixed accumulation order gives
@@ -33,10 +34,42 @@ SHAPES = [(40, 136, 272), (33, 136, 272), (65, 264, 400), (128, 256, 128), (300,
 @pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("gran", [0, 1, 2, 3])
 def test_prefill_quantised_operands(fp8, orc, M, N, K, gran):
+    """Quantised N(0, 1) activations x N(0, 0.02) weights (no outliers) on
+    ragged shapes: every output at the acceptance bound for M <= 128 (the
+    tile kernel's 2-k-block accumulation groups), at the acceptance bound
+    plus the binary32 accumulation bound above (see
+    test_prefill_outlier_free_large_m)."""
     assert fp8.describe_dispatch(M, N, K, gran) == fp8.KERNEL_PREFILL
     qa, qb, sa, sb, wa, wb, wsa, wsb = quantised_operands(fp8, orc, M, N, K, gran, 5000 + M + N + K + gran)
     y = run_mm(fp8, qa, qb, sa, sb, gran)
-    full_check(orc, wa, wb, wsa, wsb, gran, y, f"prefill {M}x{N}x{K} gran {gran}", tc_bound=True)
+    full_check(orc, wa, wb, wsa, wsb, gran, y, f"prefill {M}x{N}x{K} gran {gran}", tc_bound=M > 128)
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 2048, 5120), (128, 2048, 5120), (64, 1024, 17408), (128, 1024, 17408)])
+def test_prefill_outlier_free_strict(fp8, orc, M, N, K):
+    """Outlier-free quantised data at K 5120 and 17408, M 64 and 128 (the
+    tile kernel accumulates 2 k-blocks in TMEM between binary32 adds at M <=
+    128): every output at the acceptance bound."""
+    qa, qb, sa, sb, wa, wb, wsa, wsb = quantised_operands(fp8, orc, M, N, K, 2, 5400 + M + K)
+    y = run_mm(fp8, qa, qb, sa, sb, 2)
+    full_check(orc, wa, wb, wsa, wsb, 2, y, f"outlier-free {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 2048, 5120), (200, 1024, 17408), (2048, 2048, 5120), (2048, 1024, 17408)])
+def test_prefill_outlier_free_large_m(fp8, orc, M, N, K):
+    """Outlier-free quantised data at M 200 and 2048 (10-k-block groups): an
+    output's partial sums reach ~1e6 code units^2 while the acceptance
+    bound's absolute term is 1e-3 sqrt(K) (0.07-0.13), below one binary32 ulp
+    of such a partial, so about one output in a million, near zero, lands
+    beyond it (measured: up to 1.1x at 10-k-block groups; 1.5x / 1.8x even
+    with a binary32 add after every k-block, so shorter groups do not cure
+    it).  These data are held to the acceptance bound plus the binary32
+    accumulation bound; the prefill-chunk recipe (1% outliers) meets the
+    acceptance bound alone (test_prefill_chunk_data_full and the config-4
+    tests)."""
+    qa, qb, sa, sb, wa, wb, wsa, wsb = quantised_operands(fp8, orc, M, N, K, 2, 5500 + M + K)
+    y = run_mm(fp8, qa, qb, sa, sb, 2)
+    full_check(orc, wa, wb, wsa, wsb, 2, y, f"outlier-free {M}x{N}x{K}", tc_bound=True)
 
 
 @pytest.mark.parametrize("M,N,K", [(65, 264, 400), (300, 776, 1040)])
@@ -53,7 +86,7 @@ def test_prefill_more_tiles_than_sms(fp8, orc):
     M, N, K = 1024, 8192, 1024
     qa, qb, sa, sb, wa, wb, wsa, wsb = quantised_operands(fp8, orc, M, N, K, 2, 5200)
     y = run_mm(fp8, qa, qb, sa, sb, 2)
-    full_check(orc, wa, wb, wsa, wsb, 2, y, "1024x8192x1024", tc_bound=True)
+    full_check(orc, wa, wb, wsa, wsb, 2, y, "1024x8192x1024")
 
 
 @pytest.mark.parametrize("M", [16, 17, 32, 33])
@@ -65,7 +98,7 @@ def test_dispatch_boundary(fp8, orc, M):
     assert fp8.describe_dispatch(M, N, K, 2) == want
     qa, qb, sa, sb, wa, wb, wsa, wsb = quantised_operands(fp8, orc, M, N, K, 2, 5300)
     y = run_mm(fp8, qa, qb, sa, sb, 2)
-    full_check(orc, wa, wb, wsa, wsb, 2, y, f"boundary M={M}", tc_bound=M > 32)
+    full_check(orc, wa, wb, wsa, wsb, 2, y, f"boundary M={M}")
 
 
 @pytest.mark.parametrize("M,N", [(1000, 1288), (257, 10240)])

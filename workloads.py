@@ -174,11 +174,13 @@ def device_uniform_f32(torch, shape, lo: float, hi: float, seed: int, device):
     return torch.empty(shape, dtype=torch.float32, device=device).uniform_(lo, hi, generator=gen)
 
 
-def device_bf16_normal(torch, shape, seed: int, device, std: float = 1.0):
-    """Random bf16 values drawn around N(0, std^2) on the device (truncated draws)."""
+def device_bf16_normal(torch, shape, seed: int, device, std: float = 1.0, mean: float = 0.0):
+    """Random bf16 values drawn around N(mean, std^2) on the device (truncated draws)."""
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     v = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
     if std != 1.0:
         v.mul_(std)
+    if mean != 0.0:
+        v.add_(mean)
     return (v.view(torch.int32) >> 16).to(torch.int16).view(torch.bfloat16)
