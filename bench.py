@@ -412,8 +412,8 @@ def run_w8a16(torch, fp8, device, dist_barrier, dist_max, reps=40):
     """Weight-only FP8 GEMM on the merged QKV shape (N 10240, K 5120, bf16
     activations, per-channel weight scales): the widen-on-chip decode kernel at
     M in {1, 8, 16, 32} (weight bytes per launch / time, against the HBM peak;
-    20 launches per graph over eight 52.4 MB weights) and the large-M branch
-    (widen + dense bf16 GEMM + scale) at M 2048 in TFLOP/s."""
+    20 launches per graph over eight 52.4 MB weights) and the large-M tile
+    kernel (weight widened on chip, bf16 MMAs) at M 2048 in TFLOP/s."""
     N, K = N_QKV, K_HID
     W = [workloads.device_e4m3_codes(torch, (N, K), seed=900 + i, device=device).view(torch.float8_e4m3fn)
          for i in range(8)]
@@ -435,8 +435,8 @@ def run_w8a16(torch, fp8, device, dist_barrier, dist_max, reps=40):
     M = 2048
     x = workloads.device_bf16_normal(torch, (M, K), seed=910, device=device)
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
-    # eager launches (the branch calls cuBLAS): each call is ~100 us of GPU
-    # work, far above the host's enqueue time, so the events time the GPU
+    # eager launches: each call is ~100 us of GPU work, far above the host's
+    # enqueue time, so the events time the GPU
     for i in range(3):
         fp8.w8a16_mm(x, W[i % 8], sb, fp8.GRAN_PER_CHANNEL, out=Y)
     torch.cuda.synchronize(device)
@@ -449,7 +449,8 @@ def run_w8a16(torch, fp8, device, dist_barrier, dist_max, reps=40):
     torch.cuda.synchronize(device)
     us = dist_max(e0.elapsed_time(e1)) * 1e3 / 40
     dense = {"M": M, "us": round(us, 2), "tflops": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1),
-             "path": "widen (E4M3 -> bf16, exact) + cuBLAS bf16 GEMM + per-channel scale"}
+             "path": "tile kernel: E4M3 weight boxes widened to bf16 in TMEM, tcgen05 kind::f16 MMAs, "
+                     "per-channel scale in the epilogue"}
     del W
     return {"workload": "weight-only FP8 (W8A16) merged QKV N=10240 K=5120, bf16 activations, per-channel "
                         "weight scales, bf16 out; eight 52.4 MB weights rotated", "unit": "GB/s", "peak": peak,

@@ -2,11 +2,9 @@
 // TMA descriptor creation, the device error word.  Every entry point validates
 // everything before touching the GPU, so the validation paths run (and are
 // tested) on a machine without a GPU.
-#include <cublas_v2.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
-#include <dlfcn.h>
 
 #include <algorithm>
 #include <cstdint>
@@ -51,6 +49,7 @@ struct StreamWorkspace {
     cudaStream_t stream = nullptr;
     uint32_t *counters = nullptr;
     float *slots = nullptr;
+    bool zero_pending = false;  // made during capture: zeroed only inside that graph so far
 };
 
 struct DeviceState {
@@ -59,22 +58,7 @@ struct DeviceState {
     uint32_t *err = nullptr;
     StreamWorkspace ws[kMaxStreamWorkspaces];
     int n_ws = 0;
-    void *w16 = nullptr;  // the weight-only large-M branch's bf16 weight (grow-only)
-    size_t w16_bytes = 0;
-    cublasHandle_t blas = nullptr;
 };
-
-// cuBLAS, for the weight-only large-M branch's dense bf16 GEMM only, opened
-// on first use so that the library loads where cuBLAS is absent.
-struct Blas {
-    bool tried = false;
-    cublasStatus_t (*create)(cublasHandle_t *) = nullptr;
-    cublasStatus_t (*set_stream)(cublasHandle_t, cudaStream_t) = nullptr;
-    cublasStatus_t (*gemm_ex)(cublasHandle_t, cublasOperation_t, cublasOperation_t, int, int, int, const void *,
-                              const void *, cudaDataType, int, const void *, cudaDataType, int, const void *, void *,
-                              cudaDataType, int, cublasComputeType_t, cublasGemmAlgo_t) = nullptr;
-};
-Blas g_blas;
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -147,45 +131,6 @@ uint32_t decode_token_box_rows(const fp8k::DecodePlan &plan, int64_t M) {
     return static_cast<uint32_t>(std::min<int64_t>(M, plan.tok_pad));
 }
 
-// The cuBLAS handle of this device (cuBLAS opened on first use).
-fp8_status blas_handle(DeviceState *st, cublasHandle_t *h) {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_blas.tried) {
-        g_blas.tried = true;
-        void *lib = dlopen("libcublas.so.13", RTLD_NOW | RTLD_GLOBAL);
-        if (!lib) lib = dlopen("libcublas.so", RTLD_NOW | RTLD_GLOBAL);
-        if (lib) {
-            g_blas.create = reinterpret_cast<decltype(g_blas.create)>(dlsym(lib, "cublasCreate_v2"));
-            g_blas.set_stream = reinterpret_cast<decltype(g_blas.set_stream)>(dlsym(lib, "cublasSetStream_v2"));
-            g_blas.gemm_ex = reinterpret_cast<decltype(g_blas.gemm_ex)>(dlsym(lib, "cublasGemmEx"));
-        }
-    }
-    if (!g_blas.create || !g_blas.set_stream || !g_blas.gemm_ex) return FP8_ERR_UNSUPPORTED;
-    if (st->blas == nullptr && g_blas.create(&st->blas) != CUBLAS_STATUS_SUCCESS) {
-        st->blas = nullptr;
-        return FP8_ERR_CUDA;
-    }
-    *h = st->blas;
-    return FP8_OK;
-}
-
-// The bf16 weight buffer of the large-M branch, grown to `bytes` if needed.
-fp8_status w16_buffer(DeviceState *st, size_t bytes, void **out) {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (st->w16_bytes < bytes) {
-        if (st->w16 && cudaFree(st->w16) != cudaSuccess) return FP8_ERR_CUDA;
-        st->w16 = nullptr;
-        st->w16_bytes = 0;
-        if (cudaMalloc(&st->w16, bytes) != cudaSuccess) {
-            st->w16 = nullptr;
-            return FP8_ERR_CUDA;
-        }
-        st->w16_bytes = bytes;
-    }
-    *out = st->w16;
-    return FP8_OK;
-}
-
 // The stream-K scratch of `stream` on this device (none for cluster plans):
 // sized for the largest plan (two CTAs per SM, 32-token tiles, 64-bit parts),
 // allocated on the stream's first stream-K launch with its counters zeroed on
@@ -202,23 +147,35 @@ fp8_status decode_workspace(DeviceState *st, const fp8k::DecodePlan &plan, cudaS
     StreamWorkspace *w = nullptr;
     for (int i = 0; i < st->n_ws; ++i)
         if (st->ws[i].stream == stream) w = &st->ws[i];
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return FP8_ERR_CUDA;
+    const bool capturing = cap == cudaStreamCaptureStatusActive;
     if (w == nullptr) {
         if (st->n_ws == kMaxStreamWorkspaces) return FP8_ERR_UNSUPPORTED;
+        // On a stream that is being captured into a CUDA graph the allocation
+        // is made with this thread's capture mode relaxed for the two calls
+        // (cudaMalloc enqueues nothing); the counters' zeroing is then part of
+        // the graph and runs before the kernel on every replay, and the first
+        // call on the stream outside a capture zeroes them once more.
+        cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+        if (capturing && cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess) return FP8_ERR_CUDA;
         void *c = nullptr, *sl = nullptr;
-        if (cudaMalloc(&c, kWsCounters * sizeof(uint32_t)) != cudaSuccess) return FP8_ERR_CUDA;
-        if (cudaMalloc(&sl, n_slots * sizeof(float)) != cudaSuccess) {
-            cudaFree(c);
-            return FP8_ERR_CUDA;
+        cudaError_t e = cudaMalloc(&c, kWsCounters * sizeof(uint32_t));
+        if (e == cudaSuccess) {
+            e = cudaMalloc(&sl, n_slots * sizeof(float));
+            if (e != cudaSuccess) cudaFree(c);
         }
-        if (cudaMemsetAsync(c, 0, kWsCounters * sizeof(uint32_t), stream) != cudaSuccess) {
-            cudaFree(c);
-            cudaFree(sl);
-            return FP8_ERR_CUDA;
-        }
+        if (capturing && cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess) return FP8_ERR_CUDA;
+        if (e != cudaSuccess) return FP8_ERR_CUDA;
+        if (cudaMemsetAsync(c, 0, kWsCounters * sizeof(uint32_t), stream) != cudaSuccess) return FP8_ERR_CUDA;
         w = &st->ws[st->n_ws++];
         w->stream = stream;
         w->counters = static_cast<uint32_t *>(c);
         w->slots = static_cast<float *>(sl);
+        w->zero_pending = capturing;
+    } else if (w->zero_pending && !capturing) {
+        if (cudaMemsetAsync(w->counters, 0, kWsCounters * sizeof(uint32_t), stream) != cudaSuccess) return FP8_ERR_CUDA;
+        w->zero_pending = false;
     }
     ws->counters = w->counters;
     ws->slots = w->slots;
@@ -543,26 +500,16 @@ fp8_status fp8_w8a16_mm_ex(const void *x, const void *W, const float *scale_b, i
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int per_channel = granularity == FP8_GRAN_PER_CHANNEL ? 1 : 0;
     if (fp8_w8a16_describe_dispatch(M, N, K) == FP8_KERNEL_W16_DENSE) {
-        // Large M: the weight widened to bf16 (exact: every E4M3 value is a
-        // bf16 value), a dense bf16 GEMM (cuBLAS; y^T [N,M] = W16 [N,K] x^T,
-        // column-major) into out, then the scale applied in place.
-        cublasHandle_t h = nullptr;
-        if ((s = blas_handle(st, &h)) != FP8_OK) return s;
-        void *w16 = nullptr;
-        if ((s = w16_buffer(st, static_cast<size_t>(N) * static_cast<size_t>(K) * 2u, &w16)) != FP8_OK) return s;
-        if ((s = from_cuda(fp8k::launch_widen_weight(W, nullptr, 0, N, K, w16, cs, st->num_sms, opts))) != FP8_OK)
-            return s;
-        {
-            std::lock_guard<std::mutex> lock(g_mu);
-            const float one = 1.0f, zero = 0.0f;
-            if (g_blas.set_stream(h, cs) != CUBLAS_STATUS_SUCCESS) return FP8_ERR_CUDA;
-            const cublasStatus_t b = g_blas.gemm_ex(
-                h, CUBLAS_OP_T, CUBLAS_OP_N, static_cast<int>(N), static_cast<int>(M), static_cast<int>(K), &one, w16,
-                CUDA_R_16BF, static_cast<int>(K), x, CUDA_R_16BF, static_cast<int>(K), &zero, out, CUDA_R_16BF,
-                static_cast<int>(N), CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-            if (b != CUBLAS_STATUS_SUCCESS) return FP8_ERR_CUDA;
-        }
-        return from_cuda(fp8k::launch_scale_columns(out, scale_b, per_channel, M, N, cs, st->num_sms, opts));
+        // Large M: the tile kernel, widening each E4M3 weight box to bf16 on
+        // chip (exact: every E4M3 value is a bf16 value) for dense bf16 MMAs,
+        // the weight scale applied to the fp32 accumulator before the bf16
+        // rounding; no widened copy of the weight, no scratch.
+        const fp8k::W16TilePlan plan = fp8k::plan_w8a16_tile(M, N, K, st->num_sms);
+        if (plan.tiles > kI32Max) return FP8_ERR_UNSUPPORTED;
+        CUtensorMap tw, tx;
+        if ((s = make_tmap_e4m3(&tw, W, N, K, fp8k::kDecodeRows)) != FP8_OK) return s;
+        if ((s = make_tmap_bf16(&tx, x, M, K, static_cast<uint32_t>(fp8k::kW16TileTokens))) != FP8_OK) return s;
+        return from_cuda(fp8k::launch_w8a16_tile(tw, tx, scale_b, per_channel, M, N, out, st->err, plan, opts, cs));
     }
     const fp8k::DecodePlan plan = fp8k::plan_w8a16(M, N, K, st->num_sms);
     fp8k::DecodeWorkspace ws;

@@ -4,8 +4,8 @@
 // Sources: "[Kernel] add Flashinfer cutedsl w4a16 linear" (vllm #53014): the
 // FP8 channelwise half of the weight-only path (the weight stays E4M3 in HBM
 // and is widened on chip; at decode M the kernel is bound by the weight
-// bytes), and its large-M branch (widen the weight to 16 bits once, then a
-// dense 16-bit GEMM), which lives in api.cu.
+// bytes), and its large-M branch (a dense 16-bit GEMM over the widened
+// weight), here a tile kernel that widens the weight on chip too.
 //
 // Design (GB300, sm_103a).  The tensor core's kind::f16 takes both operands in
 // one 16-bit type, so the E4M3 weight tile is widened to bf16 (exact: every
@@ -38,6 +38,8 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "splitk.cuh"
+
+#include <algorithm>
 
 namespace fp8k {
 namespace {
@@ -435,6 +437,268 @@ cudaError_t launch_w16(const CUtensorMap &tw, const CUtensorMap &tx, const Decod
                             dim3(W16Cfg<TOK>::kThreads), p.smem_bytes, stream, o, tw, tx, a);
 }
 
+// ------------------------------------------------------------- large-M tile kernel
+//
+// The weight-only GEMM's large-M branch (the pages' branch widens the weight to
+// 16 bits for a dense 16-bit GEMM; here the widening happens on chip, tile by
+// tile, so HBM holds and streams only the E4M3 weight and nothing is
+// allocated).  Output tiles of 128 weight rows x 128 tokens, the whole K range
+// each, walked by persistent CTAs (one per SM), token tile fastest, so that
+// the CTAs running at the same time read each weight box from L2 many times.
+// Inside a CTA: warp 0 / lane 0 loads the weight boxes (128 x 128 bytes E4M3)
+// and token boxes (128 tokens x 64 bf16, two per k-block) with TMA into two
+// rings; warps 6-9 widen each weight box into one of two A tiles in tensor
+// memory (one row per thread, as in the decode kernel) and release the weight
+// stage; warp 1 / lane 0 issues eight tcgen05.mma kind::f16 per k-block (M =
+// 128 weight rows from TMEM, N = 128 tokens from shared memory, K = 16) into
+// one of two fp32 accumulators in TMEM; warps 2-5 (one weight row per thread)
+// read a finished accumulator, apply the weight scale in binary32, round to
+// bf16 and store, while the MMAs of the next tile fill the other accumulator.
+struct W16TileCfg {
+    static constexpr int kThreads = 320;  // producer, MMA, epilogue warpgroup (warps 2-5), widening warpgroup (6-9)
+    static constexpr int TN = kW16TileTokens;
+    static constexpr uint32_t kXRegion = TN * 128;          // 64 bf16 of K for TN tokens
+    static constexpr uint32_t kXStageBytes = 2 * kXRegion;  // one k-block of the token tile
+    static constexpr int kDBufs = 2;                         // accumulators, TN columns each
+    static constexpr int kABufs = 2;                         // widened weight tiles, 64 columns each
+    static constexpr uint32_t kACol0 = kDBufs * TN;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(kDecodeRows, TN);
+    static_assert(kACol0 + kABufs * 64 <= kTmemCols, "accumulators and widened tiles fit the allocation");
+};
+
+__global__ void __launch_bounds__(W16TileCfg::kThreads, 1)
+    w8a16_tile_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                      const W16TileArgs args) {
+    using Cfg = W16TileCfg;
+    constexpr int TN = Cfg::TN;
+    constexpr int ND = Cfg::kDBufs, NA = Cfg::kABufs;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem_base;
+    __shared__ uint32_t s_w_issued, s_w_consumed, s_x_issued, s_x_consumed;  // loads requested / used
+    __shared__ volatile uint32_t s_abort;
+
+    const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int WS = args.wstages, XS = args.xstages;
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    // [weight ring: WS x 16 KB][token ring: XS x 32 KB][barriers]
+    const uint32_t xbase = base + static_cast<uint32_t>(WS) * kW16WeightBytes;
+    const uint32_t bar0 = xbase + static_cast<uint32_t>(XS) * Cfg::kXStageBytes;
+    auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
+    auto wempty_bar = [&](int s) { return bar0 + 8u * (WS + s); };
+    auto xfull_bar = [&](int s) { return bar0 + 8u * (2 * WS + s); };
+    auto xempty_bar = [&](int s) { return bar0 + 8u * (2 * WS + XS + s); };
+    auto dfull_bar = [&](int b) { return bar0 + 8u * (2 * WS + 2 * XS + b); };
+    auto dempty_bar = [&](int b) { return bar0 + 8u * (2 * WS + 2 * XS + ND + b); };
+    auto afull_bar = [&](int a) { return bar0 + 8u * (2 * WS + 2 * XS + 2 * ND + a); };
+    auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * WS + 2 * XS + 2 * ND + NA + a); };
+    const uint32_t final_bar = bar0 + 8u * (2 * WS + 2 * XS + 2 * ND + 2 * NA);
+
+    const int kbt = args.kb_total, G = static_cast<int>(gridDim.x), me = static_cast<int>(blockIdx.x);
+    const int my_tiles = args.tiles > me ? (args.tiles - me + G - 1) / G : 0;  // tiles me, me + G, ...
+    const int total = my_tiles * kbt;                                           // k-block steps of this CTA
+    uint32_t *const err = args.err;
+
+    if (tid == 0) {
+        tma_prefetch_desc(&tmap_w);
+        tma_prefetch_desc(&tmap_x);
+        for (int s = 0; s < WS; ++s) {
+            mbar_init(wfull_bar(s), 1);
+            mbar_init(wempty_bar(s), 4);  // one arrive per widening warp
+        }
+        for (int s = 0; s < XS; ++s) {
+            mbar_init(xfull_bar(s), 1);
+            mbar_init(xempty_bar(s), 1);  // the MMA's commit
+        }
+        for (int b = 0; b < ND; ++b) {
+            mbar_init(dfull_bar(b), 1);   // the MMA's commit after a tile's last k-block
+            mbar_init(dempty_bar(b), 4);  // one arrive per epilogue warp
+        }
+        for (int a = 0; a < NA; ++a) {
+            mbar_init(afull_bar(a), 4);   // one arrive per widening warp
+            mbar_init(aempty_bar(a), 1);  // the MMA's commit
+        }
+        mbar_init(final_bar, 1);
+        fence_mbar_init();
+        s_w_issued = s_w_consumed = s_x_issued = s_x_consumed = 0;
+        s_abort = 0;
+    }
+    if (warp == 1) tmem_alloc(smem_u32(&s_tmem_base), Cfg::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem_base;
+
+    // tile of step q: t = me + (q / kbt) * G, token tile fastest
+    auto tile_of = [&](int q, int &m_tile, int &n_tile) {
+        const int t = me + (q / kbt) * G;
+        m_tile = t % args.m_tiles;
+        n_tile = t / args.m_tiles;
+    };
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------------------- producer
+        int wi = 0, xi = 0;  // steps whose weights / tokens are requested
+        // Weights that no earlier kernel in the stream writes may be fetched
+        // before the dependency wait; the tokens always wait.
+        const int pre = args.weights_static ? min(total, WS) : 0;
+        for (; wi < pre; ++wi) {
+            int mt, nt;
+            tile_of(wi, mt, nt);
+            mbar_arrive_expect_tx(wfull_bar(wi), kW16WeightBytes);
+            tma_load_2d(base + static_cast<uint32_t>(wi) * kW16WeightBytes, &tmap_w, wfull_bar(wi),
+                        (wi % kbt) * kBlockK, nt * kDecodeRows);
+        }
+        s_w_issued = static_cast<uint32_t>(wi);
+        grid_dependency_wait();
+        bool ok = true;
+        while (ok && (wi < total || xi < total)) {
+            // tokens first while they trail the weights (the MMA needs both)
+            if (xi < total && (xi < wi || wi == total)) {
+                const int s = xi % XS;
+                if (!cta_wait(xempty_bar(s), (static_cast<uint32_t>(xi / XS) & 1u) ^ 1u, err, kErrDecodeEmptyWait,
+                              &s_abort)) {
+                    ok = false;
+                    break;
+                }
+                int mt, nt;
+                tile_of(xi, mt, nt);
+                const int kb = xi % kbt;
+                const uint32_t xs = xbase + static_cast<uint32_t>(s) * Cfg::kXStageBytes;
+                mbar_arrive_expect_tx(xfull_bar(s), Cfg::kXStageBytes);
+                tma_load_2d(xs, &tmap_x, xfull_bar(s), kb * kBlockK, mt * TN);
+                tma_load_2d(xs + Cfg::kXRegion, &tmap_x, xfull_bar(s), kb * kBlockK + 64, mt * TN);
+                ++xi;
+                s_x_issued = static_cast<uint32_t>(xi);
+            } else {
+                const int s = wi % WS;
+                if (!cta_wait(wempty_bar(s), (static_cast<uint32_t>(wi / WS) & 1u) ^ 1u, err, kErrDecodeEmptyWait,
+                              &s_abort)) {
+                    ok = false;
+                    break;
+                }
+                int mt, nt;
+                tile_of(wi, mt, nt);
+                mbar_arrive_expect_tx(wfull_bar(s), kW16WeightBytes);
+                tma_load_2d(base + static_cast<uint32_t>(s) * kW16WeightBytes, &tmap_w, wfull_bar(s),
+                            (wi % kbt) * kBlockK, nt * kDecodeRows);
+                ++wi;
+                s_w_issued = static_cast<uint32_t>(wi);
+            }
+        }
+        grid_launch_dependents();
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------------------- MMA issuer
+        int q = 0;
+        for (; q < total; ++q) {
+            const int s = q % XS, a = q % NA, j = q / kbt, kb = q % kbt, b = j % ND;
+            if (!cta_wait(xfull_bar(s), static_cast<uint32_t>(q / XS) & 1u, err, kErrDecodeFullWait, &s_abort)) break;
+            if (!cta_wait(afull_bar(a), static_cast<uint32_t>(q / NA) & 1u, err, kErrW16AFullWait, &s_abort)) break;
+            if (kb == 0 && !cta_wait(dempty_bar(b), (static_cast<uint32_t>(j / ND) & 1u) ^ 1u, err,
+                                     kErrDecodeTmemEmptyWait, &s_abort))
+                break;
+            tc_fence_after();
+            const uint32_t xs = xbase + static_cast<uint32_t>(s) * Cfg::kXStageBytes;
+            const uint32_t at = tmem + Cfg::kACol0 + static_cast<uint32_t>(a) * 64u;
+            const uint32_t d = tmem + static_cast<uint32_t>(b * TN);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {  // K = 16 bf16 per MMA: 8 TMEM columns of A, 32 bytes of the token tile
+                const uint32_t h = static_cast<uint32_t>(kk >> 2), o = 2u * static_cast<uint32_t>(kk & 3);
+                mma_bf16_tmem_a(d, at + 8u * static_cast<uint32_t>(kk), sw128_kmajor_desc(xs + h * Cfg::kXRegion) + o,
+                                Cfg::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(xempty_bar(s));
+            mma_commit(aempty_bar(a));
+            if (kb == kbt - 1) mma_commit(dfull_bar(b));
+        }
+        s_x_consumed = static_cast<uint32_t>(q);
+        mma_commit(final_bar);  // arrives when every MMA issued above has completed
+    } else if (warp >= 6) {
+        // ---------------------------------------------------------------- widening
+        const int row = static_cast<int>((warp & 3u) * 32u + lane);
+        int q = 0;
+        for (; q < total; ++q) {
+            const int s = q % WS, a = q % NA;
+            // the TMEM stores below are warp-collective: the warp goes on only
+            // if every lane's wait succeeded
+            bool ok = cta_wait(wfull_bar(s), static_cast<uint32_t>(q / WS) & 1u, err, kErrW16FullWait, &s_abort);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            ok = cta_wait(aempty_bar(a), (static_cast<uint32_t>(q / NA) & 1u) ^ 1u, err, kErrW16AEmptyWait, &s_abort);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            widen_row_tmem<8>(smem_raw + (base + static_cast<uint32_t>(s) * kW16WeightBytes - raw),
+                              tmem + ((static_cast<uint32_t>(warp & 3u) * 32u) << 16) + Cfg::kACol0 +
+                                  static_cast<uint32_t>(a) * 64u,
+                              row, 0);
+            tmem_st_wait();  // the stores, before the tensor core reads them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(afull_bar(a));
+                mbar_arrive(wempty_bar(s));
+            }
+        }
+        if (warp == 6 && lane == 0) s_w_consumed = static_cast<uint32_t>(q);
+    } else if (warp >= 2) {
+        // ---------------------------------------------------------------- epilogue
+        const uint32_t quarter = warp & 3u;                      // TMEM lanes 32*(warp%4) .. +31
+        const int row = static_cast<int>(quarter * 32u + lane);  // weight row within the tile
+        grid_dependency_wait();  // outputs and scales are touched below
+        const float sb0 = __ldg(args.scale_b);
+        for (int j = 0; j < my_tiles; ++j) {
+            const int b = j % ND;
+            const bool ok = cta_wait(dfull_bar(b), static_cast<uint32_t>(j / ND) & 1u, err, kErrDecodeTmemFullWait,
+                                     &s_abort);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            int mt, nt;
+            tile_of(j * kbt, mt, nt);
+            const int n = nt * kDecodeRows + row, m0 = mt * TN;
+            const float sb = (args.per_channel && n < args.N) ? __ldg(args.scale_b + n) : sb0;
+            const uint32_t taddr = tmem + ((quarter * 32u) << 16) + static_cast<uint32_t>(b * TN);
+#pragma unroll 1
+            for (int c0 = 0; c0 < TN; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(taddr + static_cast<uint32_t>(c0), r);
+                tmem_ld_wait();
+                if (c0 + 16 >= TN) {  // last chunk read: the accumulator is free for the next tile
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(dempty_bar(b));
+                }
+                if (n < args.N) {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int m = m0 + c0 + jj;
+                        if (m < args.M)
+                            args.out[static_cast<int64_t>(m) * args.N + n] =
+                                __float2bfloat16_rn(__fmul_rn(__uint_as_float(r[jj]), sb));
+                    }
+                }
+            }
+        }
+    }
+    __syncwarp();
+    grid_dependency_wait();
+    grid_launch_dependents();
+    __syncthreads();
+
+    if (tid == 0) {
+        // Loads issued but never consumed (only after a timeout): let them land
+        // before the CTA exits.
+        for (uint32_t i = s_w_consumed; i < s_w_issued; ++i)
+            mbar_wait(wfull_bar(static_cast<int>(i % WS)), (i / WS) & 1u, err, kErrW16FullWait);
+        for (uint32_t i = s_x_consumed; i < s_x_issued; ++i)
+            mbar_wait(xfull_bar(static_cast<int>(i % XS)), (i / XS) & 1u, err, kErrDecodeFullWait);
+    }
+    if (warp == 1) {
+        mbar_wait(final_bar, 0, err, kErrDecodeAccumWait);  // every MMA has completed
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+}
+
 // w16[n,k] = bf16_rne(fp32(dec(W[n,k]) * s)), one binary32 multiply rounded
 // to nearest, then rounded to bf16 (s = 1 when `scale` is null: the exact
 // E4M3 value); 16 codes per thread, grid-stride.
@@ -460,31 +724,6 @@ __global__ void __launch_bounds__(256) widen_weight_kernel(const uint4 *__restri
         }
         out[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
         out[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-    }
-}
-
-// y[m,n] = bf16_rne(fp32(y[m,n]) * s), s = scale[n] (per channel) or
-// scale[0], in place over a bf16 [M,N] matrix; 8 elements per thread.
-__global__ void __launch_bounds__(256) scale_columns_kernel(uint4 *__restrict__ y, const float *__restrict__ scale,
-                                                            int per_channel, int64_t n8, int N8) {
-    grid_dependency_wait();
-    grid_launch_dependents();
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int n0 = static_cast<int>(i % N8) * 8;
-        const uint4 v = y[i];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const float s0 = __ldg(scale + (per_channel ? n0 + 2 * t : 0));
-            const float s1 = __ldg(scale + (per_channel ? n0 + 2 * t + 1 : 0));
-            const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(w[t] << 16), s0),
-                                                           __fmul_rn(__uint_as_float(w[t] & 0xFFFF0000u), s1));
-            o[t] = static_cast<uint32_t>(__bfloat16_as_ushort(b.x)) |
-                   (static_cast<uint32_t>(__bfloat16_as_ushort(b.y)) << 16);
-        }
-        y[i] = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -548,15 +787,52 @@ cudaError_t launch_w8a16_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap
     return launch_w16<16>(tmap_w, tmap_x, a, plan, opts, stream);
 }
 
-cudaError_t launch_scale_columns(void *y, const float *scale, int per_channel, int64_t M, int64_t N,
-                                 cudaStream_t stream, int num_sms, const LaunchOpts &opts) {
-    const int64_t n8 = M * N / 8;
-    int64_t blocks = (n8 + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    return launch_with_opts(scale_columns_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, opts,
-                            static_cast<uint4 *>(y), scale, per_channel, n8, static_cast<int>(N / 8));
+// The large-M tile kernel's plan: 128 x 128 output tiles, one persistent CTA
+// per SM (at most one per tile), 4 weight and 4 token stages (~193 KB).
+W16TilePlan plan_w8a16_tile(int64_t M, int64_t N, int64_t K, int num_sms) {
+    W16TilePlan p{};
+    p.m_tiles = static_cast<int>((M + kW16TileTokens - 1) / kW16TileTokens);
+    p.n_tiles = static_cast<int>((N + kDecodeRows - 1) / kDecodeRows);
+    p.kb_total = static_cast<int>((K + kBlockK - 1) / kBlockK);
+    p.tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    p.ctas = static_cast<int>(std::min<int64_t>(p.tiles, num_sms));
+    if (p.ctas < 1) p.ctas = 1;
+    p.wstages = 4;
+    p.xstages = 4;
+    const size_t barriers = 8u * static_cast<size_t>(2 * p.wstages + 2 * p.xstages + 2 * W16TileCfg::kDBufs +
+                                                     2 * W16TileCfg::kABufs + 1);
+    p.smem_bytes = 1024 + static_cast<size_t>(p.wstages) * kW16WeightBytes +
+                   static_cast<size_t>(p.xstages) * W16TileCfg::kXStageBytes + ((barriers + 127) / 128) * 128;
+    return p;
+}
+
+cudaError_t launch_w8a16_tile(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, const float *scale_b,
+                              int per_channel, int64_t M, int64_t N, void *out, uint32_t *err,
+                              const W16TilePlan &plan, const LaunchOpts &opts, cudaStream_t stream) {
+    W16TileArgs a{};
+    a.scale_b = scale_b;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.err = err;
+    a.per_channel = per_channel;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.kb_total = plan.kb_total;
+    a.m_tiles = plan.m_tiles;
+    a.tiles = static_cast<int>(plan.tiles);
+    a.wstages = plan.wstages;
+    a.xstages = plan.xstages;
+    a.weights_static = opts.weights_static ? 1 : 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool attr_done[64] = {};  // benign race: the attribute call is idempotent
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(w8a16_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    return launch_with_opts(w8a16_tile_kernel, dim3(static_cast<unsigned>(plan.ctas)), dim3(W16TileCfg::kThreads),
+                            plan.smem_bytes, stream, opts, tmap_w, tmap_x, a);
 }
 
 cudaError_t launch_widen_weight(const void *w, const float *scale, int per_channel, int64_t N, int64_t K, void *out,

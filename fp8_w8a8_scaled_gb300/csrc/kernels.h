@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include <cstdint>
 
 namespace fp8k {
@@ -140,13 +141,29 @@ cudaError_t launch_w8a16_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap
                               int per_channel, int64_t M, int64_t N, int64_t K, void *out, uint32_t *err,
                               const DecodePlan &plan, const DecodeWorkspace &ws, const LaunchOpts &opts,
                               cudaStream_t stream);
+// The weight-only large-M tile kernel (M >= 33): output tiles of 128 weight
+// rows x kW16TileTokens tokens, the E4M3 weight widened to bf16 on chip.
+constexpr int kW16TileTokens = 128;
+struct W16TileArgs {
+    const float *scale_b;
+    __nv_bfloat16 *out;
+    uint32_t *err;
+    int per_channel, M, N, kb_total, m_tiles, tiles, wstages, xstages, weights_static;
+};
+struct W16TilePlan {
+    int m_tiles, n_tiles, kb_total;
+    int64_t tiles;
+    int ctas, wstages, xstages;
+    size_t smem_bytes;
+};
+W16TilePlan plan_w8a16_tile(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_w8a16_tile(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, const float *scale_b,
+                              int per_channel, int64_t M, int64_t N, void *out, uint32_t *err,
+                              const W16TilePlan &plan, const LaunchOpts &opts, cudaStream_t stream);
 // w16 [N,K] bf16 = bf16_rne(fp32(dec(W) * s)) (K % 16 == 0); scale == nullptr
 // gives the exact E4M3 values (the large-M branch's weight).
 cudaError_t launch_widen_weight(const void *w, const float *scale, int per_channel, int64_t N, int64_t K, void *out,
                                 cudaStream_t stream, int num_sms, const LaunchOpts &opts);
-// y [M,N] bf16 <- bf16_rne(fp32(y) * s[n]) in place (N % 8 == 0).
-cudaError_t launch_scale_columns(void *y, const float *scale, int per_channel, int64_t M, int64_t N,
-                                 cudaStream_t stream, int num_sms, const LaunchOpts &opts);
 
 // ------------------------------------------------------------ prefill GEMM --
 

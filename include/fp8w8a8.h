@@ -89,7 +89,7 @@ typedef enum {
     FP8_KERNEL_DECODE_SPLITK = 1, /* weight-streaming split-K kernel (small M) */
     FP8_KERNEL_PREFILL = 2,       /* persistent tensor-core tile kernel (large M) */
     FP8_KERNEL_W16_DECODE = 3,    /* weight-only: widen-on-chip split-K kernel (M <= 32) */
-    FP8_KERNEL_W16_DENSE = 4      /* weight-only: widened bf16 weight + dense bf16 GEMM (M >= 33) */
+    FP8_KERNEL_W16_DENSE = 4      /* weight-only: tile kernel, weight widened on chip, dense bf16 MMAs (M >= 33) */
 } fp8_kernel_id;
 
 /* fp8_scaled_mm -- the FP8 W8A8 scaled GEMM.
@@ -118,8 +118,12 @@ typedef enum {
  * kernel's stream-K mode (few 128-row tiles with a long K, see
  * fp8_decode_split_for_sms) uses scratch memory: one area per stream, about
  * 20 MB, allocated on that stream's first stream-K call (cudaMalloc, counters
- * zeroed with cudaMemsetAsync on the stream), for at most 64 streams per device
- * (FP8_ERR_UNSUPPORTED beyond); calls on different streams may overlap.  Its
+ * zeroed with cudaMemsetAsync on the stream; during graph capture the
+ * allocation is made with the thread's capture mode relaxed and the zeroing
+ * becomes part of the graph), for at most 64 streams per device
+ * (FP8_ERR_UNSUPPORTED beyond); calls on different streams may overlap.  A
+ * captured graph uses its capture stream's area: graphs captured on one
+ * stream must not be replayed at the same time as each other.  Its
  * cluster mode and the tile kernel use none.  The result is deterministic
  * (bitwise the same on every run); row m does not depend on the other rows of
  * A (on the decode kernel for any M <= 32, on the tile kernel for any M >= 33),
@@ -353,7 +357,8 @@ fp8_status fp8_quant_weight_block(const void *w, void *out, float *scale_out, in
  *
  * Source: [P4] "[Kernel] add Flashinfer cutedsl w4a16 linear" (vllm #53014):
  * the FP8 channelwise half of the weight-only path, and its large-M branch
- * that widens the weight to 16 bits for a dense 16-bit GEMM.
+ * (a dense 16-bit GEMM over the weight widened to 16 bits; here the widening
+ * is done on chip, tile by tile).
  *
  *   x        bf16 [M,K] row-major, 16-byte aligned
  *   W        E4M3 [N,K] row-major (K contiguous), 16-byte aligned
@@ -362,17 +367,17 @@ fp8_status fp8_quant_weight_block(const void *w, void *out, float *scale_out, in
  *   M, N, K  as fp8_scaled_mm (K % 16 == 0, N % 8 == 0)
  *
  * y[m,n] = bf16( (sum_k x[m,k] * dec(W[n,k])) * sb ).  M <= 32: a split-K
- * kernel that widens each E4M3 weight tile to bf16 in shared memory (exact)
+ * kernel that widens each E4M3 weight tile to bf16 in tensor memory (exact)
  * and multiplies on the tensor core (fp32 accumulation inside 128-wide
- * k-blocks, TwoSum across them, the scale in binary32 at the end); it shares
- * the decode kernel's scratch area.  M >= 33: the weight widened to bf16
- * (exact) into a library-owned buffer of N*K*2 bytes (grown on demand, one per
- * device, so overlapping large-M calls on different streams race on it), a
- * dense bf16 GEMM from cuBLAS (fp32 accumulation, bf16 result; cuBLAS is
- * opened on first use, FP8_ERR_UNSUPPORTED where it is absent), then
- * y = bf16(fp32(y) * sb) in place.  fp8_w8a16_describe_dispatch tells which.
- * Errors: FP8_ERR_INVALID_ARG (also a granularity other than per-tensor /
- * per-channel), FP8_ERR_ALIGNMENT, FP8_ERR_UNSUPPORTED, FP8_ERR_CUDA. */
+ * k-blocks, TwoSum across them, the scale in binary32 at the end); its
+ * stream-K mode uses the per-stream scratch of fp8_scaled_mm.  M >= 33: a tile
+ * kernel (128 weight rows x 128 tokens per tile, the whole K) that widens each
+ * E4M3 weight box to bf16 in tensor memory on chip for dense bf16 MMAs (fp32
+ * accumulation over K in tensor memory), then y = bf16(fp32(acc * sb)); no
+ * widened copy of the weight is made and nothing is allocated.
+ * fp8_w8a16_describe_dispatch tells which.  Errors: FP8_ERR_INVALID_ARG (also
+ * a granularity other than per-tensor / per-channel), FP8_ERR_ALIGNMENT,
+ * FP8_ERR_UNSUPPORTED, FP8_ERR_CUDA. */
 fp8_status fp8_w8a16_mm(const void *x, const void *W, const float *scale_b, int granularity, int out_dtype,
                         int64_t M, int64_t N, int64_t K, void *out, void *stream);
 

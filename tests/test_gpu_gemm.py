@@ -355,6 +355,34 @@ def test_stream_k_on_two_streams(fp8):
             assert np.array_equal(host_bits(o), cases[j][1]), j
 
 
+def test_stream_k_first_call_inside_graph_capture(fp8):
+    """A stream whose first stream-K call is made while it is captured into a
+    CUDA graph: the scratch is allocated during the capture, the graph's
+    replays and a later eager call on the same stream all give the serial
+    result bit for bit."""
+    M, N, K = 16, 2048, 5120
+    assert fp8.decode_split(M, N, K, granularity=2) == 0
+    c = workloads.random_gemm(67, M, N, K, 2)
+    args = (to_dev_e4m3(c["A"]), to_dev_e4m3(c["B"]), to_dev_f32(c["sa"]), to_dev_f32(c["sb"]), 2)
+    ref = run_mm(fp8, *args)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fp8.fp8_scaled_mm(*args, out=out)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(out), ref)
+    with torch.cuda.stream(s):
+        eager = fp8.fp8_scaled_mm(*args)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(eager), ref)
+    assert fp8.get_device_error() == 0
+
+
 def test_m_zero_is_noop(fp8):
     A = torch.empty((0, 64), dtype=torch.float8_e4m3fn, device="cuda")
     B = torch.zeros((64, 64), dtype=torch.float8_e4m3fn, device="cuda")
