@@ -505,7 +505,7 @@ fp8_status fp8_w8a16_mm_ex(const void *x, const void *W, const float *scale_b, i
         // the weight scale applied to the fp32 accumulator before the bf16
         // rounding; no widened copy of the weight, no scratch.
         const fp8k::W16TilePlan plan = fp8k::plan_w8a16_tile(M, N, K, st->num_sms);
-        if (plan.tiles > kI32Max) return FP8_ERR_UNSUPPORTED;
+        if (plan.units > kI32Max) return FP8_ERR_UNSUPPORTED;
         CUtensorMap tw, tx;
         if ((s = make_tmap_e4m3(&tw, W, N, K, fp8k::kDecodeRows)) != FP8_OK) return s;
         if ((s = make_tmap_bf16(&tx, x, M, K, static_cast<uint32_t>(fp8k::kW16TileTokens))) != FP8_OK) return s;

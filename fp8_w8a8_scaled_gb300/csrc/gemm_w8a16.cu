@@ -79,6 +79,38 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t pair) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(b.x)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b.y)) << 16);
 }
 
+// Four E4M3 codes (code i in byte i of w) -> four bf16 (codes 0, 1 in `lo`,
+// 2, 3 in `hi`, the first of each pair in the low half), with integer
+// operations and one bf16 multiply per pair instead of the conversion pipe.
+// A code's seven magnitude bits are placed at bits 4..10 of a bf16 pattern and
+// its sign at bit 15: the E4M3 exponent lands in the low four bits of the bf16
+// exponent and the three mantissa bits at the top of the bf16 mantissa, a bf16
+// number equal to the code's value times 2^-120 (exponent 0 gives the bf16
+// subnormal with the same mantissa, as E4M3's subnormals).  The placement:
+// a byte permute puts code c in the low byte of a 16-bit lane and its sign
+// replicated in the high byte (0x00 or 0xFF), a shift by 4 moves the magnitude
+// to bits 4..10 and the sign copies to bits 11..15 (those of the low lane
+// spill into bits 16..19), and one mask keeps bits 4..10 and 15 of each lane.
+// Multiplying by 2^120 in bf16 is exact, the product being a bf16 number, so
+// the result is the decoded value.  The NaN codes (magnitude 0x7F) come out as
+// 480: bit 7 of each byte of (magnitude + 1), OR-ed into `nan`, is set exactly
+// for them, and the caller converts such chunks again with e4m3x2_to_bf16x2.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(a), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t &lo, uint32_t &hi, uint32_t &nan) {
+    nan |= ((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+    constexpr uint32_t kKeep = 0x87F087F0u, kTwo120 = 0x7B807B80u;  // bf16 2^120 in both halves
+    // selector nibbles: byte c copied (c), byte c's sign replicated (8 + c)
+    const uint32_t plo = (prmt(w, 0x9180u) << 4) & kKeep;
+    const uint32_t phi = (prmt(w, 0xB3A2u) << 4) & kKeep;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(plo), "r"(kTwo120));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(phi), "r"(kTwo120));
+}
+
 // Row r of a 128 x 128-byte E4M3 box (128-byte swizzle: 16-byte chunk j of
 // row r sits at chunk j ^ (r % 8)), chunks [J0, J0 + NJ), widened into the
 // calling thread's TMEM lane: K elements 2c, 2c + 1 in column c of the tile
@@ -91,17 +123,30 @@ __device__ __forceinline__ void widen_row_tmem(const uint8_t *src, uint32_t trow
 #pragma unroll
     for (int h = 0; h < NJ / 4; ++h) {
         uint32_t o[32];
+        uint32_t nan = 0;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             const int j = J0 + 4 * h + jj;
             const uint4 q = *reinterpret_cast<const uint4 *>(srow + ((j ^ sw) << 4));
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+            e4m3x4_to_bf16x4(q.x, o[8 * jj + 0], o[8 * jj + 1], nan);
+            e4m3x4_to_bf16x4(q.y, o[8 * jj + 2], o[8 * jj + 3], nan);
+            e4m3x4_to_bf16x4(q.z, o[8 * jj + 4], o[8 * jj + 5], nan);
+            e4m3x4_to_bf16x4(q.w, o[8 * jj + 6], o[8 * jj + 7], nan);
+        }
+        if (nan & 0x80808080u) {  // a NaN code in these 64: convert them again, NaN-preserving
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                o[8 * jj + 2 * t] = e4m3x2_to_bf16x2(w[t] & 0xFFFFu);
-                o[8 * jj + 2 * t + 1] = e4m3x2_to_bf16x2(w[t] >> 16);
+            for (int jj = 0; jj < 4; ++jj) {
+                const int j = J0 + 4 * h + jj;
+                const uint4 q = *reinterpret_cast<const uint4 *>(srow + ((j ^ sw) << 4));
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    o[8 * jj + 2 * t] = e4m3x2_to_bf16x2(w[t] & 0xFFFFu);
+                    o[8 * jj + 2 * t + 1] = e4m3x2_to_bf16x2(w[t] >> 16);
+                }
             }
         }
+        __syncwarp();  // the TMEM store is warp-collective
         tmem_st32(trow + static_cast<uint32_t>(J0 * 8 + 32 * h), o);
     }
 }
@@ -440,31 +485,42 @@ cudaError_t launch_w16(const CUtensorMap &tw, const CUtensorMap &tx, const Decod
 // ------------------------------------------------------------- large-M tile kernel
 //
 // The weight-only GEMM's large-M branch (the pages' branch widens the weight to
-// 16 bits for a dense 16-bit GEMM; here the widening happens on chip, tile by
-// tile, so HBM holds and streams only the E4M3 weight and nothing is
-// allocated).  Output tiles of 128 weight rows x 128 tokens, the whole K range
-// each, walked by persistent CTAs (one per SM), token tile fastest, so that
-// the CTAs running at the same time read each weight box from L2 many times.
-// Inside a CTA: warp 0 / lane 0 loads the weight boxes (128 x 128 bytes E4M3)
-// and token boxes (128 tokens x 64 bf16, two per k-block) with TMA into two
-// rings; warps 6-9 widen each weight box into one of two A tiles in tensor
-// memory (one row per thread, as in the decode kernel) and release the weight
-// stage; warp 1 / lane 0 issues eight tcgen05.mma kind::f16 per k-block (M =
-// 128 weight rows from TMEM, N = 128 tokens from shared memory, K = 16) into
-// one of two fp32 accumulators in TMEM; warps 2-5 (one weight row per thread)
-// read a finished accumulator, apply the weight scale in binary32, round to
-// bf16 and store, while the MMAs of the next tile fill the other accumulator.
+// 16 bits for a dense 16-bit GEMM; here the widening happens on chip, box by
+// box, so HBM holds and streams only the E4M3 weight and nothing is
+// allocated).  Output tiles of 256 weight rows (two 128-row halves) x 128
+// tokens, the whole K range each, walked by persistent CTAs (one per SM),
+// token tile fastest, so that the CTAs running at the same time read each
+// weight box and token box from L2 many times.  When the last round of tiles
+// would leave more than half of the CTAs idle, its tiles run as half tiles
+// (one 128-row half each) on twice as many CTAs.  Inside a CTA:
+//   * warp 0 / lane 0 loads each k-block's E4M3 weight boxes (128 x 128 bytes
+//     per half) and its token boxes (128 tokens x 64 bf16, two) with TMA into
+//     two rings;
+//   * warps 6-13, one weight row per thread (warps 6-9 the first half, 10-13
+//     the second), widen the k-block's E4M3 rows into one of two A tiles in
+//     tensor memory (128 lanes x 64 columns per half) and release the weight
+//     stage (sixteen widening warps, a half row each, were slower);
+//   * warp 1 / lane 0 issues eight tcgen05.mma kind::f16 per half and k-block
+//     (M = 128 weight rows from TMEM, N = 128 tokens from shared memory,
+//     K = 16) into the half's fp32 accumulator in TMEM;
+//   * warps 2-5 (one weight row per thread and half) read the finished
+//     accumulator, apply the weight scale in binary32, round to bf16 and
+//     store.
+// Tensor memory: the accumulator (2 x 128 columns) and two widened k-blocks
+// (2 x 2 x 64 columns) fill the 512 columns, so the accumulator is single:
+// the next tile's MMAs wait for the drain (a few percent of a tile's time).
 struct W16TileCfg {
-    static constexpr int kThreads = 320;  // producer, MMA, epilogue warpgroup (warps 2-5), widening warpgroup (6-9)
+    static constexpr int kThreads = 448;  // producer, MMA, epilogue warpgroup (2-5), two widening warpgroups (6-13)
+    static constexpr int kWidenWarps = 8;
     static constexpr int TN = kW16TileTokens;
-    static constexpr uint32_t kXRegion = TN * 128;          // 64 bf16 of K for TN tokens
-    static constexpr uint32_t kXStageBytes = 2 * kXRegion;  // one k-block of the token tile
-    static constexpr int kDBufs = 2;                         // accumulators, TN columns each
-    static constexpr int kABufs = 2;                         // widened weight tiles, 64 columns each
-    static constexpr uint32_t kACol0 = kDBufs * TN;
+    static constexpr uint32_t kWStageBytes = 2 * kW16WeightBytes;  // both halves of one k-block
+    static constexpr uint32_t kXRegion = TN * 128;                  // 64 bf16 of K for TN tokens
+    static constexpr uint32_t kXStageBytes = 2 * kXRegion;          // one k-block of the token tile
+    static constexpr int kABufs = 2;                                 // widened k-blocks, 2 x 64 columns each
+    static constexpr uint32_t kACol0 = 2 * TN;                       // after the accumulator's two halves
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kDecodeRows, TN);
-    static_assert(kACol0 + kABufs * 64 <= kTmemCols, "accumulators and widened tiles fit the allocation");
+    static_assert(kACol0 + kABufs * 128 <= kTmemCols, "accumulator and widened tiles fit the allocation");
 };
 
 __global__ void __launch_bounds__(W16TileCfg::kThreads, 1)
@@ -472,7 +528,7 @@ __global__ void __launch_bounds__(W16TileCfg::kThreads, 1)
                       const W16TileArgs args) {
     using Cfg = W16TileCfg;
     constexpr int TN = Cfg::TN;
-    constexpr int ND = Cfg::kDBufs, NA = Cfg::kABufs;
+    constexpr int NA = Cfg::kABufs;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t s_tmem_base;
     __shared__ uint32_t s_w_issued, s_w_consumed, s_x_issued, s_x_consumed;  // loads requested / used
@@ -482,22 +538,22 @@ __global__ void __launch_bounds__(W16TileCfg::kThreads, 1)
     const int WS = args.wstages, XS = args.xstages;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    // [weight ring: WS x 16 KB][token ring: XS x 32 KB][barriers]
-    const uint32_t xbase = base + static_cast<uint32_t>(WS) * kW16WeightBytes;
+    // [weight ring: WS x 32 KB][token ring: XS x 32 KB][barriers]
+    const uint32_t xbase = base + static_cast<uint32_t>(WS) * Cfg::kWStageBytes;
     const uint32_t bar0 = xbase + static_cast<uint32_t>(XS) * Cfg::kXStageBytes;
     auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
     auto wempty_bar = [&](int s) { return bar0 + 8u * (WS + s); };
     auto xfull_bar = [&](int s) { return bar0 + 8u * (2 * WS + s); };
     auto xempty_bar = [&](int s) { return bar0 + 8u * (2 * WS + XS + s); };
-    auto dfull_bar = [&](int b) { return bar0 + 8u * (2 * WS + 2 * XS + b); };
-    auto dempty_bar = [&](int b) { return bar0 + 8u * (2 * WS + 2 * XS + ND + b); };
-    auto afull_bar = [&](int a) { return bar0 + 8u * (2 * WS + 2 * XS + 2 * ND + a); };
-    auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * WS + 2 * XS + 2 * ND + NA + a); };
-    const uint32_t final_bar = bar0 + 8u * (2 * WS + 2 * XS + 2 * ND + 2 * NA);
+    const uint32_t dfull_bar = bar0 + 8u * (2 * WS + 2 * XS);
+    const uint32_t dempty_bar = dfull_bar + 8u;
+    auto afull_bar = [&](int a) { return dempty_bar + 8u * (1 + a); };
+    auto aempty_bar = [&](int a) { return dempty_bar + 8u * (1 + NA + a); };
+    const uint32_t final_bar = dempty_bar + 8u * (1 + 2 * NA);
 
     const int kbt = args.kb_total, G = static_cast<int>(gridDim.x), me = static_cast<int>(blockIdx.x);
-    const int my_tiles = args.tiles > me ? (args.tiles - me + G - 1) / G : 0;  // tiles me, me + G, ...
-    const int total = my_tiles * kbt;                                           // k-block steps of this CTA
+    const int my_units = args.units > me ? (args.units - me + G - 1) / G : 0;  // units me, me + G, ...
+    const int total = my_units * kbt;                                          // k-block steps of this CTA
     uint32_t *const err = args.err;
 
     if (tid == 0) {
@@ -505,18 +561,16 @@ __global__ void __launch_bounds__(W16TileCfg::kThreads, 1)
         tma_prefetch_desc(&tmap_x);
         for (int s = 0; s < WS; ++s) {
             mbar_init(wfull_bar(s), 1);
-            mbar_init(wempty_bar(s), 4);  // one arrive per widening warp
+            mbar_init(wempty_bar(s), Cfg::kWidenWarps);  // one arrive per widening warp
         }
         for (int s = 0; s < XS; ++s) {
             mbar_init(xfull_bar(s), 1);
             mbar_init(xempty_bar(s), 1);  // the MMA's commit
         }
-        for (int b = 0; b < ND; ++b) {
-            mbar_init(dfull_bar(b), 1);   // the MMA's commit after a tile's last k-block
-            mbar_init(dempty_bar(b), 4);  // one arrive per epilogue warp
-        }
+        mbar_init(dfull_bar, 1);   // the MMA's commit after a tile's last k-block
+        mbar_init(dempty_bar, 4);  // one arrive per epilogue warp
         for (int a = 0; a < NA; ++a) {
-            mbar_init(afull_bar(a), 4);   // one arrive per widening warp
+            mbar_init(afull_bar(a), Cfg::kWidenWarps);  // one arrive per widening warp
             mbar_init(aempty_bar(a), 1);  // the MMA's commit
         }
         mbar_init(final_bar, 1);
@@ -530,26 +584,44 @@ __global__ void __launch_bounds__(W16TileCfg::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = s_tmem_base;
 
-    // tile of step q: t = me + (q / kbt) * G, token tile fastest
-    auto tile_of = [&](int q, int &m_tile, int &n_tile) {
-        const int t = me + (q / kbt) * G;
+    // Unit j of this CTA: u = me + j * G.  Units below full_units are whole
+    // tiles (both halves), the rest half tiles of the last tiles, two per
+    // tile; a half that starts at or beyond N is dropped.  Token tile fastest.
+    auto unit_of = [&](int j, int &m_tile, int &n_tile, uint32_t &halves) {
+        const int u = me + j * G;
+        int t;
+        if (u < args.full_units) {
+            t = u;
+            halves = 3u;
+        } else {
+            const int v = u - args.full_units;
+            t = args.full_units + (v >> 1);
+            halves = 1u << (v & 1);
+        }
         m_tile = t % args.m_tiles;
         n_tile = t / args.m_tiles;
+        if (n_tile * (2 * kDecodeRows) + kDecodeRows >= args.N) halves &= 1u;
     };
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------------- producer
+        auto load_w = [&](int q, int s) {
+            int mt, nt;
+            uint32_t hm;
+            unit_of(q / kbt, mt, nt, hm);
+            const int kx = (q % kbt) * kBlockK;
+            const uint32_t ws = base + static_cast<uint32_t>(s) * Cfg::kWStageBytes;
+            mbar_arrive_expect_tx(wfull_bar(s), static_cast<uint32_t>(__popc(hm)) * kW16WeightBytes);
+            for (int h = 0; h < 2; ++h)
+                if ((hm >> h) & 1u)
+                    tma_load_2d(ws + static_cast<uint32_t>(h) * kW16WeightBytes, &tmap_w, wfull_bar(s), kx,
+                                (2 * nt + h) * kDecodeRows);
+        };
         int wi = 0, xi = 0;  // steps whose weights / tokens are requested
         // Weights that no earlier kernel in the stream writes may be fetched
         // before the dependency wait; the tokens always wait.
         const int pre = args.weights_static ? min(total, WS) : 0;
-        for (; wi < pre; ++wi) {
-            int mt, nt;
-            tile_of(wi, mt, nt);
-            mbar_arrive_expect_tx(wfull_bar(wi), kW16WeightBytes);
-            tma_load_2d(base + static_cast<uint32_t>(wi) * kW16WeightBytes, &tmap_w, wfull_bar(wi),
-                        (wi % kbt) * kBlockK, nt * kDecodeRows);
-        }
+        for (; wi < pre; ++wi) load_w(wi, wi);
         s_w_issued = static_cast<uint32_t>(wi);
         grid_dependency_wait();
         bool ok = true;
@@ -563,12 +635,13 @@ __global__ void __launch_bounds__(W16TileCfg::kThreads, 1)
                     break;
                 }
                 int mt, nt;
-                tile_of(xi, mt, nt);
-                const int kb = xi % kbt;
+                uint32_t hm;
+                unit_of(xi / kbt, mt, nt, hm);
+                const int kx = (xi % kbt) * kBlockK;
                 const uint32_t xs = xbase + static_cast<uint32_t>(s) * Cfg::kXStageBytes;
                 mbar_arrive_expect_tx(xfull_bar(s), Cfg::kXStageBytes);
-                tma_load_2d(xs, &tmap_x, xfull_bar(s), kb * kBlockK, mt * TN);
-                tma_load_2d(xs + Cfg::kXRegion, &tmap_x, xfull_bar(s), kb * kBlockK + 64, mt * TN);
+                tma_load_2d(xs, &tmap_x, xfull_bar(s), kx, mt * TN);
+                tma_load_2d(xs + Cfg::kXRegion, &tmap_x, xfull_bar(s), kx + 64, mt * TN);
                 ++xi;
                 s_x_issued = static_cast<uint32_t>(xi);
             } else {
@@ -578,11 +651,7 @@ __global__ void __launch_bounds__(W16TileCfg::kThreads, 1)
                     ok = false;
                     break;
                 }
-                int mt, nt;
-                tile_of(wi, mt, nt);
-                mbar_arrive_expect_tx(wfull_bar(s), kW16WeightBytes);
-                tma_load_2d(base + static_cast<uint32_t>(s) * kW16WeightBytes, &tmap_w, wfull_bar(s),
-                            (wi % kbt) * kBlockK, nt * kDecodeRows);
+                load_w(wi, s);
                 ++wi;
                 s_w_issued = static_cast<uint32_t>(wi);
             }
@@ -592,31 +661,39 @@ __global__ void __launch_bounds__(W16TileCfg::kThreads, 1)
         // ---------------------------------------------------------------- MMA issuer
         int q = 0;
         for (; q < total; ++q) {
-            const int s = q % XS, a = q % NA, j = q / kbt, kb = q % kbt, b = j % ND;
+            const int s = q % XS, a = q % NA, j = q / kbt, kb = q % kbt;
             if (!cta_wait(xfull_bar(s), static_cast<uint32_t>(q / XS) & 1u, err, kErrDecodeFullWait, &s_abort)) break;
             if (!cta_wait(afull_bar(a), static_cast<uint32_t>(q / NA) & 1u, err, kErrW16AFullWait, &s_abort)) break;
-            if (kb == 0 && !cta_wait(dempty_bar(b), (static_cast<uint32_t>(j / ND) & 1u) ^ 1u, err,
-                                     kErrDecodeTmemEmptyWait, &s_abort))
+            if (kb == 0 && !cta_wait(dempty_bar, (static_cast<uint32_t>(j) & 1u) ^ 1u, err, kErrDecodeTmemEmptyWait,
+                                     &s_abort))
                 break;
             tc_fence_after();
+            int mt, nt;
+            uint32_t hm;
+            unit_of(j, mt, nt, hm);
             const uint32_t xs = xbase + static_cast<uint32_t>(s) * Cfg::kXStageBytes;
-            const uint32_t at = tmem + Cfg::kACol0 + static_cast<uint32_t>(a) * 64u;
-            const uint32_t d = tmem + static_cast<uint32_t>(b * TN);
+            for (int h = 0; h < 2; ++h) {
+                if (!((hm >> h) & 1u)) continue;
+                const uint32_t at = tmem + Cfg::kACol0 + static_cast<uint32_t>(a * 128 + h * 64);
+                const uint32_t d = tmem + static_cast<uint32_t>(h * TN);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {  // K = 16 bf16 per MMA: 8 TMEM columns of A, 32 bytes of the token tile
-                const uint32_t h = static_cast<uint32_t>(kk >> 2), o = 2u * static_cast<uint32_t>(kk & 3);
-                mma_bf16_tmem_a(d, at + 8u * static_cast<uint32_t>(kk), sw128_kmajor_desc(xs + h * Cfg::kXRegion) + o,
-                                Cfg::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk) {  // K = 16 bf16 per MMA: 8 TMEM columns of A, 32 bytes of the tokens
+                    const uint32_t r = static_cast<uint32_t>(kk >> 2), o = 2u * static_cast<uint32_t>(kk & 3);
+                    mma_bf16_tmem_a(d, at + 8u * static_cast<uint32_t>(kk),
+                                    sw128_kmajor_desc(xs + r * Cfg::kXRegion) + o, Cfg::kIdesc,
+                                    (kb > 0 || kk > 0) ? 1u : 0u);
+                }
             }
             mma_commit(xempty_bar(s));
             mma_commit(aempty_bar(a));
-            if (kb == kbt - 1) mma_commit(dfull_bar(b));
+            if (kb == kbt - 1) mma_commit(dfull_bar);
         }
         s_x_consumed = static_cast<uint32_t>(q);
         mma_commit(final_bar);  // arrives when every MMA issued above has completed
     } else if (warp >= 6) {
         // ---------------------------------------------------------------- widening
-        const int row = static_cast<int>((warp & 3u) * 32u + lane);
+        const uint32_t quarter = warp & 3u, half = (warp - 6u) >> 2;
+        const int row = static_cast<int>(quarter * 32u + lane);
         int q = 0;
         for (; q < total; ++q) {
             const int s = q % WS, a = q % NA;
@@ -627,11 +704,17 @@ __global__ void __launch_bounds__(W16TileCfg::kThreads, 1)
             ok = cta_wait(aempty_bar(a), (static_cast<uint32_t>(q / NA) & 1u) ^ 1u, err, kErrW16AEmptyWait, &s_abort);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after();
-            widen_row_tmem<8>(smem_raw + (base + static_cast<uint32_t>(s) * kW16WeightBytes - raw),
-                              tmem + ((static_cast<uint32_t>(warp & 3u) * 32u) << 16) + Cfg::kACol0 +
-                                  static_cast<uint32_t>(a) * 64u,
-                              row, 0);
-            tmem_st_wait();  // the stores, before the tensor core reads them
+            int mt, nt;
+            uint32_t hm;
+            unit_of(q / kbt, mt, nt, hm);
+            if ((hm >> half) & 1u) {
+                widen_row_tmem<8>(smem_raw + (base + static_cast<uint32_t>(s) * Cfg::kWStageBytes +
+                                              half * kW16WeightBytes - raw),
+                                  tmem + ((quarter * 32u) << 16) + Cfg::kACol0 + static_cast<uint32_t>(a) * 128u +
+                                      half * 64u,
+                                  row, 0);
+                tmem_st_wait();  // the stores, before the tensor core reads them
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -642,38 +725,41 @@ __global__ void __launch_bounds__(W16TileCfg::kThreads, 1)
         if (warp == 6 && lane == 0) s_w_consumed = static_cast<uint32_t>(q);
     } else if (warp >= 2) {
         // ---------------------------------------------------------------- epilogue
-        const uint32_t quarter = warp & 3u;                      // TMEM lanes 32*(warp%4) .. +31
-        const int row = static_cast<int>(quarter * 32u + lane);  // weight row within the tile
-        grid_dependency_wait();  // outputs and scales are touched below
+        const uint32_t quarter = warp & 3u;  // TMEM lanes 32*(warp%4) .. +31
+        grid_dependency_wait();              // outputs and scales are touched below
         const float sb0 = __ldg(args.scale_b);
-        for (int j = 0; j < my_tiles; ++j) {
-            const int b = j % ND;
-            const bool ok = cta_wait(dfull_bar(b), static_cast<uint32_t>(j / ND) & 1u, err, kErrDecodeTmemFullWait,
-                                     &s_abort);
+        for (int j = 0; j < my_units; ++j) {
+            const bool ok = cta_wait(dfull_bar, static_cast<uint32_t>(j) & 1u, err, kErrDecodeTmemFullWait, &s_abort);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after();
             int mt, nt;
-            tile_of(j * kbt, mt, nt);
-            const int n = nt * kDecodeRows + row, m0 = mt * TN;
-            const float sb = (args.per_channel && n < args.N) ? __ldg(args.scale_b + n) : sb0;
-            const uint32_t taddr = tmem + ((quarter * 32u) << 16) + static_cast<uint32_t>(b * TN);
+            uint32_t hm;
+            unit_of(j, mt, nt, hm);
+            const int m0 = mt * TN;
+            const int h_last = (hm >> 1) & 1u;
+            for (int h = 0; h < 2; ++h) {
+                if (!((hm >> h) & 1u)) continue;
+                const int n = (2 * nt + h) * kDecodeRows + static_cast<int>(quarter * 32u + lane);
+                const float sb = (args.per_channel && n < args.N) ? __ldg(args.scale_b + n) : sb0;
+                const uint32_t taddr = tmem + ((quarter * 32u) << 16) + static_cast<uint32_t>(h * TN);
 #pragma unroll 1
-            for (int c0 = 0; c0 < TN; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(taddr + static_cast<uint32_t>(c0), r);
-                tmem_ld_wait();
-                if (c0 + 16 >= TN) {  // last chunk read: the accumulator is free for the next tile
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(dempty_bar(b));
-                }
-                if (n < args.N) {
+                for (int c0 = 0; c0 < TN; c0 += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(taddr + static_cast<uint32_t>(c0), r);
+                    tmem_ld_wait();
+                    if (h == h_last && c0 + 16 >= TN) {  // last read: the accumulator is free for the next tile
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(dempty_bar);
+                    }
+                    if (n < args.N) {
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int m = m0 + c0 + jj;
-                        if (m < args.M)
-                            args.out[static_cast<int64_t>(m) * args.N + n] =
-                                __float2bfloat16_rn(__fmul_rn(__uint_as_float(r[jj]), sb));
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int m = m0 + c0 + jj;
+                            if (m < args.M)
+                                args.out[static_cast<int64_t>(m) * args.N + n] =
+                                    __float2bfloat16_rn(__fmul_rn(__uint_as_float(r[jj]), sb));
+                        }
                     }
                 }
             }
@@ -787,21 +873,28 @@ cudaError_t launch_w8a16_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap
     return launch_w16<16>(tmap_w, tmap_x, a, plan, opts, stream);
 }
 
-// The large-M tile kernel's plan: 128 x 128 output tiles, one persistent CTA
-// per SM (at most one per tile), 4 weight and 4 token stages (~193 KB).
+// The large-M tile kernel's plan: 256 x 128 output tiles, one persistent CTA
+// per SM (at most one per unit), 3 weight and 3 token stages (~193 KB).  When
+// the tiles' last round would fill at most half of the CTAs, its tiles are
+// split into half tiles (128 weight rows each), unless the last weight tile
+// has a single half, to keep every unit non-empty.
 W16TilePlan plan_w8a16_tile(int64_t M, int64_t N, int64_t K, int num_sms) {
     W16TilePlan p{};
     p.m_tiles = static_cast<int>((M + kW16TileTokens - 1) / kW16TileTokens);
-    p.n_tiles = static_cast<int>((N + kDecodeRows - 1) / kDecodeRows);
+    p.n_tiles = static_cast<int>((N + 2 * kDecodeRows - 1) / (2 * kDecodeRows));
     p.kb_total = static_cast<int>((K + kBlockK - 1) / kBlockK);
     p.tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-    p.ctas = static_cast<int>(std::min<int64_t>(p.tiles, num_sms));
-    if (p.ctas < 1) p.ctas = 1;
-    p.wstages = 4;
-    p.xstages = 4;
-    const size_t barriers = 8u * static_cast<size_t>(2 * p.wstages + 2 * p.xstages + 2 * W16TileCfg::kDBufs +
-                                                     2 * W16TileCfg::kABufs + 1);
-    p.smem_bytes = 1024 + static_cast<size_t>(p.wstages) * kW16WeightBytes +
+    const int64_t sms = num_sms > 0 ? num_sms : 1;
+    const int64_t tail = p.tiles % sms;
+    const int64_t last_rows = N - static_cast<int64_t>(p.n_tiles - 1) * 2 * kDecodeRows;
+    const bool split = p.tiles > sms && tail > 0 && 2 * tail <= sms && last_rows > kDecodeRows;
+    p.full_units = split ? p.tiles - tail : p.tiles;
+    p.units = split ? p.tiles + tail : p.tiles;
+    p.ctas = static_cast<int>(std::min<int64_t>(p.units, sms));
+    p.wstages = 3;
+    p.xstages = 3;
+    const size_t barriers = 8u * static_cast<size_t>(2 * p.wstages + 2 * p.xstages + 2 + 2 * W16TileCfg::kABufs + 1);
+    p.smem_bytes = 1024 + static_cast<size_t>(p.wstages) * W16TileCfg::kWStageBytes +
                    static_cast<size_t>(p.xstages) * W16TileCfg::kXStageBytes + ((barriers + 127) / 128) * 128;
     return p;
 }
@@ -818,7 +911,8 @@ cudaError_t launch_w8a16_tile(const CUtensorMap &tmap_w, const CUtensorMap &tmap
     a.N = static_cast<int>(N);
     a.kb_total = plan.kb_total;
     a.m_tiles = plan.m_tiles;
-    a.tiles = static_cast<int>(plan.tiles);
+    a.full_units = static_cast<int>(plan.full_units);
+    a.units = static_cast<int>(plan.units);
     a.wstages = plan.wstages;
     a.xstages = plan.xstages;
     a.weights_static = opts.weights_static ? 1 : 0;

@@ -141,18 +141,19 @@ cudaError_t launch_w8a16_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap
                               int per_channel, int64_t M, int64_t N, int64_t K, void *out, uint32_t *err,
                               const DecodePlan &plan, const DecodeWorkspace &ws, const LaunchOpts &opts,
                               cudaStream_t stream);
-// The weight-only large-M tile kernel (M >= 33): output tiles of 128 weight
-// rows x kW16TileTokens tokens, the E4M3 weight widened to bf16 on chip.
+// The weight-only large-M tile kernel (M >= 33): output tiles of 2 x 128
+// weight rows x kW16TileTokens tokens (or one 128-row half in a split last
+// round), the E4M3 weight widened to bf16 on chip.
 constexpr int kW16TileTokens = 128;
 struct W16TileArgs {
     const float *scale_b;
     __nv_bfloat16 *out;
     uint32_t *err;
-    int per_channel, M, N, kb_total, m_tiles, tiles, wstages, xstages, weights_static;
+    int per_channel, M, N, kb_total, m_tiles, full_units, units, wstages, xstages, weights_static;
 };
 struct W16TilePlan {
     int m_tiles, n_tiles, kb_total;
-    int64_t tiles;
+    int64_t tiles, full_units, units;  // units: whole tiles below full_units, then half tiles
     int ctas, wstages, xstages;
     size_t smem_bytes;
 };

@@ -142,6 +142,40 @@ def test_w16_nan_weight_code(fp8, orc):
     assert not np.any(np.isnan(bf16_bits_to_f64(np.delete(y, 7, axis=1))))
 
 
+@pytest.mark.parametrize("M", [32, 256])
+@pytest.mark.parametrize("per_channel", [True, False])
+def test_w16_every_code_exact(fp8, orc, M, per_channel):
+    """Every non-NaN E4M3 weight code through the on-chip widening, exactly:
+    token m is one-hot at k = m, so y[m, n] = bf16(dec(W[n, m]) * 1) is the
+    decoded code itself (subnormal codes and signed zeros included); over the
+    256 rows n the codes (n + 8 m) mod 256 cover all 254 non-NaN codes for
+    every m.  M 32 runs the decode kernel, M 256 the tile kernel."""
+    N, K = 256, 256
+    x = np.zeros((M, K), np.uint16)
+    x[np.arange(M), np.arange(M)] = 0x3F80  # bf16 1.0
+    n, k = np.meshgrid(np.arange(N), np.arange(K), indexing="ij")
+    W = ((n + 8 * k) % 256).astype(np.uint8)
+    W[(W & 0x7F) == 0x7F] = 0x00  # NaN codes would turn a whole row into NaN
+    sb = np.ones(N if per_channel else 1, np.float32)
+    y = _dec_bf16(run_w16(fp8, to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb), 1 if per_channel else 0))
+    want = orc.e4m3_decode(W[:, :M]).T
+    assert np.array_equal(y, want)
+    y64, _ = orc.w8a16_mm(x, W, sb, per_channel)
+    assert np.array_equal(y64, want)
+
+
+def test_w16_nan_weight_code_tile_kernel(fp8, orc):
+    """A NaN weight code through the tile kernel's widening: that output
+    channel is NaN for every token, the others finite."""
+    x, W, sb = operands(9410, 40, 296, 528)
+    W[7, 100] = 0x7F
+    W[290, 517] = 0xFF
+    assert fp8.w8a16_describe_dispatch(40, 296, 528) == fp8.KERNEL_W16_DENSE
+    y = _dec_bf16(run_w16(fp8, to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb), 1))
+    assert np.all(np.isnan(y[:, [7, 290]]))
+    assert not np.any(np.isnan(np.delete(y, [7, 290], axis=1)))
+
+
 def test_w16_m_zero(fp8):
     x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
     W = torch.zeros((64, 64), dtype=torch.float8_e4m3fn, device="cuda")
@@ -167,14 +201,17 @@ def test_widen_weight_bitexact(fp8, orc, per_channel):
     assert np.all((got[nan_w] & 0x7F80) == 0x7F80) and np.all((got[nan_w] & 0x7F) != 0)
 
 
-@pytest.mark.parametrize("M,N,K", [(33, 136, 272), (64, 1032, 2064), (300, 520, 1040), (129, 8, 5136)])
+@pytest.mark.parametrize("M,N,K", [(33, 136, 272), (64, 1032, 2064), (300, 520, 1040), (129, 8, 5136),
+                                   (1100, 4504, 272), (200, 392, 400)])
 @pytest.mark.parametrize("per_channel", [True, False])
 def test_w16_dense_branch(fp8, orc, M, N, K, per_channel):
     """Large M: the tile kernel (weight widened on chip, bf16 MMAs with fp32
     accumulation over the whole K in tensor memory, the scale in binary32
     before the one bf16 rounding) against the method's exact result: the
     acceptance bound plus the binary32 accumulation bound of the tensor
-    core's 16-wide chunks; ragged M, N and K."""
+    core's 16-wide chunks; ragged M, N and K.  1100 x 4504 has more tiles
+    than SMs and a short last round, which runs as half tiles; 300 x 520 ends
+    in a weight tile of one half, 200 x 392 in one whose second half has 8 rows."""
     assert fp8.w8a16_describe_dispatch(M, N, K) == fp8.KERNEL_W16_DENSE
     x, W, sb = operands(9600 + M, M, N, K, per_channel, weights="quant")
     y = bf16_bits_to_f64(run_w16(fp8, to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb), 1 if per_channel else 0))
