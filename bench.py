@@ -18,6 +18,7 @@ Under torchrun (N > 1) every rank runs the same workload on its own GPU
 import argparse
 import json
 import os
+import platform
 import subprocess
 import sys
 import time
@@ -243,6 +244,46 @@ def time_graph(torch, graph, reps, dist_barrier):
     return t0.elapsed_time(t1)
 
 
+def time_graph_segments(torch, graph, reps, segments, dist_barrier):
+    """Like time_graph, with CUDA events also between `segments` equal runs of
+    replays (no synchronisation inside the timed region): returns the total
+    and each segment's time in ms."""
+    stream = torch.cuda.current_stream()
+    segments = max(1, min(segments, reps))
+    bounds = [reps * i // segments for i in range(segments + 1)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(segments + 1)]
+    dist_barrier()
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(segments):
+        for _ in range(bounds[i + 1] - bounds[i]):
+            graph.replay()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    dist_barrier()
+    seg = [ev[i].elapsed_time(ev[i + 1]) / (bounds[i + 1] - bounds[i]) for i in range(segments)]
+    return ev[0].elapsed_time(ev[-1]), seg
+
+
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (model name, or implementer and
+    part on Arm), with the machine type and the logical CPU count."""
+    name = ""
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+        name = fields.get("model name") or ""
+        if not name and "CPU part" in fields:
+            name = f"implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    except OSError:
+        pass
+    return f"{name or platform.processor() or 'unknown'} ({platform.machine()}, {os.cpu_count()} logical CPUs)"
+
+
 def cpu_baseline_sample(budget_s=10.0):
     """The oracle, as it stands, on the decode fused step (all six M values,
     full N), repeated until about `budget_s` seconds of wall time."""
@@ -258,9 +299,22 @@ def cpu_baseline_sample(budget_s=10.0):
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
+    # the same oracle on one thread, over a quarter of the budget
+    steps1, t1 = 0, time.perf_counter()
+    while True:
+        for m in MS:
+            A = oracle.rmsnorm_quant(d["x"][:m], d["gamma"], d["eps"], float(d["s_a"]))
+            oracle.scaled_mm(A, d["B"], d["s_a"], d["sb"], 1, nthreads=1)
+        steps1 += 1
+        el1 = time.perf_counter() - t1
+        if el1 >= budget_s / 4:
+            break
     return {"value": steps * step_bytes() / el / 1e12, "unit": "TB/s", "cores": nthreads, "kind": "oracle",
             "sample": f"{steps} full decode-fused steps (6 norm-quants + 6 GEMMs 10240x5120, M=1..32), "
-                      f"{el:.1f} s wall"}
+                      f"{el:.1f} s wall",
+            "one_thread": {"value": steps1 * step_bytes() / el1 / 1e12, "unit": "TB/s", "cores": 1,
+                           "sample": f"{steps1} steps, {el1:.1f} s wall"},
+            "cpu_model": cpu_model()}
 
 
 PREFILL_SHAPES = [(m, n) for m in workloads.PREFILL_MS for n in workloads.PREFILL_NS]
@@ -325,7 +379,8 @@ def run_prefill(torch, fp8, device, dist_barrier, dist_max, seconds_per_shape=0.
             res[name] = dist_max(time_graph(torch, graph, reps, dist_barrier)) / (reps * per)
             launches += reps * per
         ms = res["gemm"]
-        shapes.append({"M": M, "N": N, "K": K, "ms": round(ms, 5), "tflops": round(flop / ms / 1e9, 1)})
+        shapes.append({"M": M, "N": N, "K": K, "ms": round(ms, 5), "tflops": round(flop / ms / 1e9, 1),
+                       "frac": round(flop / ms / 1e9 / fp8_dense_peak()[0], 4)})
         quant.append({"M": M, "K": K, "us": round(res["quant"] * 1e3, 2),
                       "tbps": round(3.0 * M * K / (res["quant"] * 1e-3) / 1e12, 3)})
         tot_flop += flop
@@ -576,9 +631,11 @@ def run_ours(args, rank, world, dist_barrier, dist_max):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    ms = dist_max(time_graph(torch, step_graph, reps, dist_barrier))
+    ms, seg = time_graph_segments(torch, step_graph, reps, 5, dist_barrier)
+    ms = dist_max(ms)
     clk = clocks.stop()
     ms_step = ms / steps
+    seg_steps = [dist_max(t) / INNER for t in seg]  # ms per step of each fifth of the timed replays
     value = whole_job_tbps(world, step_bytes(), ms_step)
 
     # roofline of the dominant kernel: the GEMM launches alone, same rotation
@@ -658,6 +715,10 @@ def run_ours(args, rank, world, dist_barrier, dist_max):
         "metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": world, "steps": steps,
         "warmup": warm * INNER, "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
+        "spread": {"segments": len(seg_steps), "min_ms_per_step": round(min(seg_steps), 6),
+                   "max_ms_per_step": round(max(seg_steps), 6),
+                   "min_value": round(whole_job_tbps(world, step_bytes(), max(seg_steps)), 4),
+                   "max_value": round(whole_job_tbps(world, step_bytes(), min(seg_steps)), 4)},
         "config": {"workload": WORKLOAD, "bytes_per_step": step_bytes(), "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: six distinct 52.4 MB weights per step (315 MB)",
                    "graph": f"{INNER} steps per CUDA graph replay"},
@@ -736,7 +797,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
         "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
         "cpu_baseline": {"value": round(value, 8), "unit": "TB/s", "cores": nthreads, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 8), "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

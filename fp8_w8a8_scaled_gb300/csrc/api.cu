@@ -216,11 +216,11 @@ fp8_status tile_gemm(DeviceState *st, const void *A, const void *B, const float 
                      int granularity, int64_t M, int64_t N, int64_t K, void *out, const fp8k::LaunchOpts &opts,
                      cudaStream_t stream) {
     const fp8k::PrefillPlan plan = fp8k::plan_prefill(M, N, K, st->num_sms);
-    if (static_cast<int64_t>(plan.m_tiles) * plan.n_tiles > kI32Max) return FP8_ERR_UNSUPPORTED;
+    if (plan.units > kI32Max) return FP8_ERR_UNSUPPORTED;
     CUtensorMap ta, tb;
     fp8_status s;
     if ((s = make_tmap_e4m3(&ta, A, M, K, fp8k::kPrefillBM)) != FP8_OK) return s;
-    if ((s = make_tmap_e4m3(&tb, B, N, K, static_cast<uint32_t>(plan.bn))) != FP8_OK) return s;
+    if ((s = make_tmap_e4m3(&tb, B, N, K, 128u)) != FP8_OK) return s;  // 128-channel weight boxes
     return from_cuda(fp8k::launch_prefill_gemm(ta, tb, scale_a, scale_b, granularity, M, N, K, out, st->err, plan,
                                                opts, stream));
 }

@@ -16,10 +16,14 @@
 // idle: there the time goes into streaming the weights, and twice the CTAs
 // stream them twice as fast)
 // (token tile fastest, so the CTAs resident at one time share their weight
-// rows through L2 and the whole token matrix stays L2-resident):
+// rows through L2 and the whole token matrix stays L2-resident).  When the
+// tiles' last round would fill at most half of the SMs, its tiles run as two
+// 128-channel halves each (N = 128 MMAs into the half's accumulator columns),
+// on twice as many CTAs:
 //   * warp 0 / lane 0 loads, per 128-byte k-block, the 128 x 128-byte token box
-//     and the 256 x 128-byte weight box with TMA (128-byte swizzle) into a ring
-//     of 48 KB shared-memory stages;
+//     and the weight boxes (128 x 128 bytes each, one per 128 channels of the
+//     tile) with TMA (128-byte swizzle) into a ring of 48 KB shared-memory
+//     stages;
 //   * warp 1 / lane 0 issues four tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32)
 //     per k-block.  A tile's K range is cut into groups of kPrefillDrainKb
 //     k-blocks; each group accumulates from zero into one of two 256-column
@@ -74,7 +78,7 @@ struct PrefillArgs {
     const float *scale_b;
     __nv_bfloat16 *out;
     uint32_t *err;
-    int gran, M, N, kb_total, m_tiles, tiles, stages, drain_kb;
+    int gran, M, N, kb_total, m_tiles, full_units, units, stages, drain_kb;
 };
 
 // Bounded wait of one thread; gives up at once once the CTA has given up.
@@ -124,9 +128,25 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * stages + 2 + b); };
     const uint32_t final_bar = bar0 + 8u * (2 * stages + 4);
 
-    const int kbt = args.kb_total, m_tiles = args.m_tiles, tiles = args.tiles, dkb = args.drain_kb;
+    const int kbt = args.kb_total, m_tiles = args.m_tiles, units = args.units, dkb = args.drain_kb;
     const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
     uint32_t *const err = args.err;
+    // Unit u (u = c, c + G, ...): units below full_units are whole tiles
+    // (halves = 3), the rest 128-channel halves of the last tiles, two per
+    // tile (halves = 1 or 2; only with BN = 256).  A half that starts at or
+    // beyond N is dropped.  Token tile fastest.
+    auto unit_of = [&](int u, int &m_tile, int &n_tile, uint32_t &halves) {
+        int t = u;
+        halves = 3u;
+        if (u >= args.full_units) {
+            const int v = u - args.full_units;
+            t = args.full_units + (v >> 1);
+            halves = 1u << (v & 1);
+        }
+        m_tile = t % m_tiles;
+        n_tile = t / m_tiles;
+        if (BN == 256 && n_tile * BN + 128 >= args.N) halves &= 1u;
+    };
 
     if (tid == 0) {
         tma_prefetch_desc(&tmap_a);
@@ -158,17 +178,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int t = c; t < tiles && ok; t += G) {
-            const int m_tile = t % m_tiles, n_tile = t / m_tiles;
+        for (int u = c; u < units && ok; u += G) {
+            int m_tile, n_tile;
+            uint32_t halves;
+            unit_of(u, m_tile, n_tile, halves);
+            const uint32_t bytes = kPrefillATile + (BN == 256 ? static_cast<uint32_t>(__popc(halves)) * 128u * kBlockK
+                                                               : Cfg::kBTile);
             for (int kb = 0; kb < kbt; ++kb) {
                 if (!pf_wait(empty_bar(s), ph ^ 1u, err, kErrPrefillEmptyWait, &s_abort)) {
                     ok = false;
                     break;
                 }
                 const uint32_t stage = base + static_cast<uint32_t>(s) * Cfg::kStageBytes;
-                mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
+                mbar_arrive_expect_tx(full_bar(s), bytes);
                 tma_load_2d(stage, &tmap_a, full_bar(s), kb * kBlockK, m_tile * kPrefillBM);
-                tma_load_2d(stage + kPrefillATile, &tmap_b, full_bar(s), kb * kBlockK, n_tile * BN);
+                for (int h = 0; h < BN / 128; ++h)  // 128-channel weight boxes
+                    if ((halves >> h) & 1u)
+                        tma_load_2d(stage + kPrefillATile + static_cast<uint32_t>(h) * 128u * kBlockK, &tmap_b,
+                                    full_bar(s), kb * kBlockK, n_tile * BN + 128 * h);
                 ++it;
                 if (++s == stages) {
                     s = 0;
@@ -189,7 +216,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         uint32_t ph = 0;
         uint32_t dc = 0;  // groups issued so far (accumulator = dc & 1)
         bool ok = true;
-        for (int t = c; t < tiles && ok; t += G) {
+        for (int u = c; u < units && ok; u += G) {
+            int m_tile, n_tile;
+            uint32_t halves;
+            unit_of(u, m_tile, n_tile, halves);
+            // a half unit: N = 128 MMAs on its weight box, into its half of the accumulator
+            const uint32_t hoff = (halves == 2u) ? 128u : 0u;
+            const uint32_t idesc = halves == 3u ? Cfg::kIdesc : idesc_e4m3_f32(kPrefillBM, 128);
             for (int kb0 = 0; kb0 < kbt && ok; kb0 += dkb, ++dc) {
                 const int acc = static_cast<int>(dc & 1u);
                 if (!pf_wait(tempty_bar(acc), ((dc >> 1) & 1u) ^ 1u, err, kErrPrefillAccumEmptyWait, &s_abort)) {
@@ -197,7 +230,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * BN) + hoff;
                 const int kb1 = min(kb0 + dkb, kbt);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!pf_wait(full_bar(s), ph, err, kErrPrefillFullWait, &s_abort)) {
@@ -206,10 +239,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t stage = base + static_cast<uint32_t>(s) * Cfg::kStageBytes;
-                    const uint64_t da = sw128_kmajor_desc(stage), db = sw128_kmajor_desc(stage + kPrefillATile);
+                    const uint64_t da = sw128_kmajor_desc(stage),
+                                   db = sw128_kmajor_desc(stage + kPrefillATile + hoff * kBlockK);
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 32; ++kk)  // +32 bytes along K = +2 in the address field
-                        mma_e4m3(d, da + 2u * kk, db + 2u * kk, Cfg::kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        mma_e4m3(d, da + 2u * kk, db + 2u * kk, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
                     mma_commit(empty_bar(s));
                     ++it;
                     if (++s == stages) {
@@ -235,15 +269,19 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         constexpr int kCols = BN / 2;  // columns of one thread
         uint32_t dc = 0;
         bool ok = true;
-        for (int t = c; t < tiles && ok; t += G) {
+        for (int u = c; u < units && ok; u += G) {
+            int m_tile, n_tile;
+            uint32_t halves;
+            unit_of(u, m_tile, n_tile, halves);
             float y[kCols];
 #pragma unroll
             for (int j = 0; j < kCols; ++j) y[j] = 0.0f;
-            // a warp whose 32 token rows all lie beyond M (small M) only takes
-            // part in the hand-shake
-            const bool live = (t % m_tiles) * kPrefillBM + static_cast<int>(quarter * 32u) < M;
-            const int m_row = (t % m_tiles) * kPrefillBM + row;                  // this thread's token row
-            const int n_col = (t / m_tiles) * BN + half * kCols;                 // its first channel
+            // a warp whose 32 token rows all lie beyond M (small M), or whose
+            // channel half is not in this unit, only takes part in the hand-shake
+            const bool mine = BN == 128 || ((halves >> half) & 1u);
+            const bool live = mine && m_tile * kPrefillBM + static_cast<int>(quarter * 32u) < M;
+            const int m_row = m_tile * kPrefillBM + row;                  // this thread's token row
+            const int n_col = n_tile * BN + half * kCols;                 // its first channel
             // Blockwise: the scales of k-block kb (sa of this row, sb of this
             // column block) are requested two k-blocks ahead of their use, so
             // that their latency hides behind the epilogue's work.
@@ -304,9 +342,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 if (lane == 0) mbar_arrive(tempty_bar(acc));
             }
             if (!ok) break;
-            const int m_tile = t % m_tiles, n_tile = t / m_tiles;
             const int m = m_tile * kPrefillBM + row;
-            if (m < M) {
+            if (mine && m < M) {
                 const float sa = sa_vec ? __ldg(args.scale_a + m) : sa0;
                 const int nbase = n_tile * BN + half * kCols;
                 __nv_bfloat16 *const yrow = args.out + static_cast<int64_t>(m) * N;
@@ -370,7 +407,16 @@ PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms) {
     p.n_tiles = static_cast<int>((N + p.bn - 1) / p.bn);
     p.kb_total = static_cast<int>((K + kBlockK - 1) / kBlockK);
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-    p.ctas = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    // A last round that would fill at most half of the SMs runs as half tiles
+    // (256-channel tiles whose last one has two halves only).
+    const int64_t sms = num_sms > 0 ? num_sms : 1;
+    const int64_t tail = tiles % sms;
+    const int64_t last_rows = N - static_cast<int64_t>(p.n_tiles - 1) * p.bn;
+    const bool split = p.bn == 256 && tiles > sms && tail > 0 && 2 * tail <= sms && last_rows > 128;
+    p.tiles = tiles;
+    p.full_units = split ? tiles - tail : tiles;
+    p.units = split ? tiles + tail : tiles;
+    p.ctas = static_cast<int>(p.units < sms ? p.units : sms);
     if (p.ctas < 1) p.ctas = 1;
     p.stages = p.bn == 256 ? PrefillCfg<256>::kStages : PrefillCfg<128>::kStages;
     const int dkb = M <= kPrefillSmallM ? kPrefillDrainKbSmall : kPrefillDrainKb;
@@ -411,7 +457,8 @@ cudaError_t launch_prefill_gemm(const CUtensorMap &tmap_a, const CUtensorMap &tm
     a.N = static_cast<int>(N);
     a.kb_total = plan.kb_total;
     a.m_tiles = plan.m_tiles;
-    a.tiles = plan.m_tiles * plan.n_tiles;
+    a.full_units = static_cast<int>(plan.full_units);
+    a.units = static_cast<int>(plan.units);
     a.stages = plan.stages;
     a.drain_kb = plan.drain_kb;
     if (granularity == kGranBlock128) {

@@ -177,6 +177,7 @@ constexpr int64_t kPrefillMinM = 33;  // fp8_scaled_mm sends M >= this to the pr
 struct PrefillPlan {
     int bn;  // output channels per tile: 256, or 128 for small M with few tiles
     int m_tiles, n_tiles, kb_total;
+    int64_t tiles, full_units, units;  // units: whole tiles below full_units, then 128-channel halves
     int ctas;       // persistent CTAs (one per SM at most)
     int stages;
     int drain_kb;   // k-blocks accumulated in TMEM before the epilogue folds them into registers

@@ -140,7 +140,8 @@ def test_quantisers_empty(fp8):
 # ------------------------------------------------------------------ GEMM, random codes
 
 SHAPES = [(1, 136, 400), (3, 8, 16), (5, 1032, 5120), (16, 264, 272), (16, 128, 128),
-          (17, 264, 400), (32, 10240, 1040), (33, 1000, 272), (129, 520, 1040), (200, 8, 4096), (300, 1032, 2064)]
+          (17, 264, 400), (32, 10240, 1040), (33, 1000, 272), (129, 520, 1040), (200, 8, 4096), (300, 1032, 2064),
+          (1100, 4504, 400)]  # the last: a short last round split into 128-channel half tiles
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)

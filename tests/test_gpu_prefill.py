@@ -89,6 +89,18 @@ def test_prefill_more_tiles_than_sms(fp8, orc):
     full_check(orc, wa, wb, wsa, wsb, 2, y, "1024x8192x1024")
 
 
+@pytest.mark.parametrize("gran", [0, 1, 2, 3])
+def test_prefill_split_last_round(fp8, orc, gran):
+    """1100 x 4504: 9 x 18 = 162 tiles of 128 x 256, more than the SMs, with a
+    short last round that runs as 128-channel half tiles (N = 128 MMAs into
+    one half of the accumulator), and a last weight tile whose second half
+    holds 152 channels; every output against the oracle."""
+    M, N, K = 1100, 4504, 1040
+    qa, qb, sa, sb, wa, wb, wsa, wsb = quantised_operands(fp8, orc, M, N, K, gran, 5250 + gran)
+    y = run_mm(fp8, qa, qb, sa, sb, gran)
+    full_check(orc, wa, wb, wsa, wsb, gran, y, f"split last round gran {gran}", tc_bound=True)
+
+
 @pytest.mark.parametrize("M", [16, 17, 32, 33])
 def test_dispatch_boundary(fp8, orc, M):
     """The token tiles' boundary (16 / 17) and the last decode M and the first
@@ -118,11 +130,12 @@ def test_prefill_chunk_data_full(fp8, orc, M, N):
     print(f"prefill chunk {M}x{N}: max err/bound {worst:.4f}")
 
 
-@pytest.mark.parametrize("M,N", [(8192, 34816)])
+@pytest.mark.parametrize("M,N", [(8192, 34816), (2048, 10240)])
 def test_prefill_gate_up_sampled(fp8, orc, M, N):
-    """The largest prefill shape: per-token activations (1% outliers x20) into
-    the merged gate_up weight, per-channel scales; 3 full rows plus 20000
-    random outputs against the oracle."""
+    """The largest prefill shape and the QKV prefill chunk (both end in a
+    split last round): per-token activations (1% outliers x20) into the
+    merged weight, per-channel scales; 3 full rows plus 20000 random outputs
+    against the oracle."""
     d = workloads.prefill(seed=1, m=M, n=N)
     qa, sa = fp8.quant_fp8_per_token(to_dev_bf16(d["x"]))
     qb, sb = fp8.quant_fp8_per_token(to_dev_bf16(d["w"]))
