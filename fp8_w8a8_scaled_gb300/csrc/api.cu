@@ -221,8 +221,10 @@ fp8_status tile_gemm(DeviceState *st, const void *A, const void *B, const float 
     fp8_status s;
     if ((s = make_tmap_e4m3(&ta, A, M, K, fp8k::kPrefillBM)) != FP8_OK) return s;
     if ((s = make_tmap_e4m3(&tb, B, N, K, 128u)) != FP8_OK) return s;  // 128-channel weight boxes
-    return from_cuda(fp8k::launch_prefill_gemm(ta, tb, scale_a, scale_b, granularity, M, N, K, out, st->err, plan,
-                                               opts, stream));
+    CUtensorMap to;  // the output, stored in 128-token x 64-channel boxes
+    if ((s = make_tmap_bf16(&to, out, M, N, fp8k::kPrefillBM)) != FP8_OK) return s;
+    return from_cuda(fp8k::launch_prefill_gemm(ta, tb, to, scale_a, scale_b, granularity, M, N, K, out, st->err,
+                                               plan, opts, stream));
 }
 
 }  // namespace

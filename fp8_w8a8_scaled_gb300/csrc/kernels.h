@@ -186,7 +186,8 @@ struct PrefillPlan {
 
 PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms);
 
-cudaError_t launch_prefill_gemm(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b, const float *scale_a,
+cudaError_t launch_prefill_gemm(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b, const CUtensorMap &tmap_out,
+                                const float *scale_a,
                                 const float *scale_b, int granularity, int64_t M, int64_t N, int64_t K, void *out,
                                 uint32_t *err, const PrefillPlan &plan, const LaunchOpts &opts, cudaStream_t stream);
 

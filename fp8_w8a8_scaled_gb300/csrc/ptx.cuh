@@ -138,6 +138,29 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// Bulk tensor store of a 2-D box from this CTA's shared memory to global
+// memory, in the calling thread's current bulk group (elements outside the
+// tensor are not written).
+__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until the calling thread's bulk groups have finished reading their
+// shared-memory sources (the buffers may be written again).
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Waits until the calling thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Barrier `id` (1..15) of `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 // Orders this thread's earlier generic-proxy writes to shared memory before
 // later async-proxy accesses (TMA, tcgen05.mma operand reads) of it.
 __device__ __forceinline__ void fence_proxy_async_smem() {
