@@ -278,7 +278,11 @@ def cpu_model():
                     fields.setdefault(k.strip(), v.strip())
         name = fields.get("model name") or ""
         if not name and "CPU part" in fields:
-            name = f"implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+            arm = {"0xd40": "Neoverse V1", "0xd4f": "Neoverse V2", "0xd84": "Neoverse V3", "0xd0c": "Neoverse N1",
+                   "0xd49": "Neoverse N2", "0xd8e": "Neoverse N3"}
+            part = fields["CPU part"].lower()
+            known = arm.get(part, "") if fields.get("CPU implementer", "").lower() == "0x41" else ""
+            name = f"{known + ' ' if known else ''}(implementer {fields.get('CPU implementer', '?')} part {part})"
     except OSError:
         pass
     return f"{name or platform.processor() or 'unknown'} ({platform.machine()}, {os.cpu_count()} logical CPUs)"
