@@ -10,7 +10,13 @@
 // must be written as bf16, not F32).
 //
 // Design (GB300, sm_103a).  At prefill M every weight byte feeds >= 128 tokens
-// and the kernel is bound by the FP8 tensor-core rate.  One persistent CTA per
+// and the kernel is bound by the FP8 tensor-core rate.  Above 128 tokens the
+// CTAs work in pairs (thread-block clusters of two, cta_group::2 MMAs of 256
+// tokens x 256 channels issued by the pair's leader, each CTA loading its own
+// 128 tokens and 128 channels per stage: half the weight bytes per SM of a
+// one-CTA 128 x 256 tile; measured 1-3% faster, the kernel being bound by the
+// tensor pipe under the power cap rather than by its loads); at most 128
+// tokens, single CTAs.  One persistent CTA per
 // SM walks the 128-token x 256-channel output tiles t = blockIdx.x + i*gridDim.x
 // (128-channel tiles when M is small and 256-channel ones would leave most SMs
 // idle: there the time goes into streaming the weights, and twice the CTAs
@@ -45,6 +51,8 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+#include <algorithm>
+
 namespace fp8k {
 namespace {
 
@@ -53,13 +61,16 @@ constexpr int kPrefillEpiWarps = 8;
 constexpr uint32_t kPrefillATile = kPrefillBM * kBlockK;  // 16 KB of tokens per stage
 // The output tile is 128 tokens x BN channels, BN = 256 (the largest MMA N) or
 // 128 (twice the CTAs for small M, whose time goes into streaming weights).
-template <int BN>
+// kPair: a CTA pair (cta_group::2) computes a 256-token x 256-channel tile;
+// each CTA loads its own 128 tokens and 128 of the channels per stage.
+template <int BN, bool kPair = false>
 struct PrefillCfg {
-    static constexpr uint32_t kBTile = BN * kBlockK;             // weights per stage
+    static constexpr uint32_t kBTile = (kPair ? 128 : BN) * kBlockK;  // weights per stage
     static constexpr uint32_t kStageBytes = kPrefillATile + kBTile;
-    static constexpr uint32_t kTmemCols = 2 * BN;                 // two accumulators
-    static constexpr uint32_t kIdesc = idesc_e4m3_f32(kPrefillBM, BN);
-    static constexpr int kStages = BN == 256 ? 4 : 6;             // 192 KB of stages either way
+    static constexpr uint32_t kTmemCols = 2 * BN;                      // two accumulators
+    static constexpr uint32_t kIdesc = idesc_e4m3_f32(kPair ? 2 * kPrefillBM : kPrefillBM, BN);
+    static constexpr int kStages = kPair ? 6 : (BN == 256 ? 4 : 6);    // 192 KB of stages
+    static constexpr int kTileM = kPair ? 2 * kPrefillBM : kPrefillBM; // tokens per output tile
 };
 // Output staging: one 128-row x 64-column bf16 box (128-byte swizzle) per
 // epilogue half.
@@ -116,7 +127,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // (drain_kb == 1) and each k-block's partial sum is multiplied by its scale
 // product sa[m, kb] * sb[n / 128, kb] as it is added into the registers; the
 // tile's output then takes no further scale.
-template <int BN, bool kBlk>
+// kPair: clusters of two CTAs; rank 0 (the leader) issues cta_group::2 MMAs
+// of M = 256 tokens (its 128 and the peer's 128) x N = 256 channels (its
+// 128 and the peer's 128), whose accumulator rows land in each CTA's own
+// TMEM.  Both CTAs' loads signal the leader's full barrier; the leader's
+// commits arrive on both CTAs' barriers (multicast); both CTAs' epilogues
+// arrive on the leader's accumulator-empty barrier.
+template <int BN, bool kBlk, bool kPair>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_out, const PrefillArgs args) {
@@ -128,7 +145,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int stages = args.stages;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    using Cfg = PrefillCfg<BN>;
+    using Cfg = PrefillCfg<BN, kPair>;
+    constexpr int kTileM = Cfg::kTileM;
     const uint32_t staging = base + static_cast<uint32_t>(stages) * Cfg::kStageBytes;  // 2 output boxes
     const uint32_t bar0 = staging + 2u * kPrefillOutBox;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -138,7 +156,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const uint32_t final_bar = bar0 + 8u * (2 * stages + 4);
 
     const int kbt = args.kb_total, m_tiles = args.m_tiles, units = args.units, dkb = args.drain_kb;
-    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    // the pair's rank (0 = leader) and its cluster index among the clusters
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const int G = static_cast<int>(kPair ? gridDim.x / 2 : gridDim.x);
+    const int c = static_cast<int>(kPair ? blockIdx.x / 2 : blockIdx.x);
+    const bool leader = !kPair || rank == 0;
     uint32_t *const err = args.err;
     // Unit u (u = c, c + G, ...): units below full_units are whole tiles
     // (halves = 3), the rest 128-channel halves of the last tiles, two per
@@ -154,7 +176,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         m_tile = t % m_tiles;
         n_tile = t / m_tiles;
-        if (BN == 256 && n_tile * BN + 128 >= args.N) halves &= 1u;
+        if (!kPair && BN == 256 && n_tile * BN + 128 >= args.N) halves &= 1u;
     };
 
     if (tid == 0) {
@@ -167,7 +189,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), kPrefillEpiWarps);  // one arrive per epilogue warp
+            mbar_init(tempty_bar(b), kPair ? 2 * kPrefillEpiWarps : kPrefillEpiWarps);  // per epilogue warp
         }
         mbar_init(final_bar, 1);
         fence_mbar_init();
@@ -175,9 +197,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         s_consumed = 0;
         s_abort = 0;
     }
-    if (warp == 1) tmem_alloc(smem_u32(&s_tmem_base), Cfg::kTmemCols);
+    if (warp == 1) {
+        if constexpr (kPair)
+            tmem_alloc_pair(smem_u32(&s_tmem_base), Cfg::kTmemCols);
+        else
+            tmem_alloc(smem_u32(&s_tmem_base), Cfg::kTmemCols);
+    }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (kPair)
+        cluster_sync();  // both CTAs' barriers initialised before any remote arrive or commit
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem_base;
 
@@ -192,20 +222,28 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             int m_tile, n_tile;
             uint32_t halves;
             unit_of(u, m_tile, n_tile, halves);
-            const uint32_t bytes = kPrefillATile + (BN == 256 ? static_cast<uint32_t>(__popc(halves)) * 128u * kBlockK
-                                                               : Cfg::kBTile);
+            const uint32_t bytes =
+                kPair ? 2u * Cfg::kStageBytes  // both CTAs' boxes, on the leader's barrier
+                      : kPrefillATile + (BN == 256 ? static_cast<uint32_t>(__popc(halves)) * 128u * kBlockK : Cfg::kBTile);
             for (int kb = 0; kb < kbt; ++kb) {
                 if (!pf_wait(empty_bar(s), ph ^ 1u, err, kErrPrefillEmptyWait, &s_abort)) {
                     ok = false;
                     break;
                 }
                 const uint32_t stage = base + static_cast<uint32_t>(s) * Cfg::kStageBytes;
-                mbar_arrive_expect_tx(full_bar(s), bytes);
-                tma_load_2d(stage, &tmap_a, full_bar(s), kb * kBlockK, m_tile * kPrefillBM);
-                for (int h = 0; h < BN / 128; ++h)  // 128-channel weight boxes
-                    if ((halves >> h) & 1u)
-                        tma_load_2d(stage + kPrefillATile + static_cast<uint32_t>(h) * 128u * kBlockK, &tmap_b,
-                                    full_bar(s), kb * kBlockK, n_tile * BN + 128 * h);
+                if (leader) mbar_arrive_expect_tx(full_bar(s), bytes);
+                if constexpr (kPair) {
+                    const uint32_t fb = map_to_rank(full_bar(s), 0);  // the leader's barrier
+                    tma_load_2d_pair(stage, &tmap_a, fb, kb * kBlockK, m_tile * kTileM + static_cast<int>(rank) * 128);
+                    tma_load_2d_pair(stage + kPrefillATile, &tmap_b, fb, kb * kBlockK,
+                                     n_tile * BN + static_cast<int>(rank) * 128);
+                } else {
+                    tma_load_2d(stage, &tmap_a, full_bar(s), kb * kBlockK, m_tile * kPrefillBM);
+                    for (int h = 0; h < BN / 128; ++h)  // 128-channel weight boxes
+                        if ((halves >> h) & 1u)
+                            tma_load_2d(stage + kPrefillATile + static_cast<uint32_t>(h) * 128u * kBlockK, &tmap_b,
+                                        full_bar(s), kb * kBlockK, n_tile * BN + 128 * h);
+                }
                 ++it;
                 if (++s == stages) {
                     s = 0;
@@ -215,7 +253,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         s_issued = it;
         grid_launch_dependents();
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && leader) {
         // ---------------------------------------------------------------- MMA issuer
         // Each tile's K range is cut into groups of drain_kb k-blocks; every
         // group accumulates from zero into the next TMEM accumulator (two in
@@ -252,20 +290,36 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     const uint64_t da = sw128_kmajor_desc(stage),
                                    db = sw128_kmajor_desc(stage + kPrefillATile + hoff * kBlockK);
 #pragma unroll
-                    for (int kk = 0; kk < kBlockK / 32; ++kk)  // +32 bytes along K = +2 in the address field
-                        mma_e4m3(d, da + 2u * kk, db + 2u * kk, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
-                    mma_commit(empty_bar(s));
+                    for (int kk = 0; kk < kBlockK / 32; ++kk) {  // +32 bytes along K = +2 in the address field
+                        if constexpr (kPair)
+                            mma_e4m3_pair(d, da + 2u * kk, db + 2u * kk, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        else
+                            mma_e4m3(d, da + 2u * kk, db + 2u * kk, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    if constexpr (kPair)
+                        mma_commit_pair(empty_bar(s), 0x3);  // both CTAs' stages are free
+                    else
+                        mma_commit(empty_bar(s));
                     ++it;
                     if (++s == stages) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
-                if (ok) mma_commit(tfull_bar(acc));
+                if (ok) {
+                    if constexpr (kPair)
+                        mma_commit_pair(tfull_bar(acc), 0x3);
+                    else
+                        mma_commit(tfull_bar(acc));
+                }
             }
         }
         s_consumed = it;
-        mma_commit(final_bar);  // arrives when every MMA issued above has completed
+        // arrives when every MMA issued above has completed (on both CTAs of a pair)
+        if constexpr (kPair)
+            mma_commit_pair(final_bar, 0x3);
+        else
+            mma_commit(final_bar);
     } else if (warp >= 2) {
         // ---------------------------------------------------------------- epilogue
         grid_dependency_wait();  // scales may come from the previous kernel; the output may be read by it
@@ -291,8 +345,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             // a warp whose 32 token rows all lie beyond M (small M), or whose
             // channel half is not in this unit, only takes part in the hand-shake
             const bool mine = BN == 128 || ((halves >> half) & 1u);
-            const bool live = mine && m_tile * kPrefillBM + static_cast<int>(quarter * 32u) < M;
-            const int m_row = m_tile * kPrefillBM + row;                  // this thread's token row
+            const int m0 = m_tile * kTileM + static_cast<int>(rank) * kPrefillBM;  // this CTA's token rows
+            const bool live = mine && m0 + static_cast<int>(quarter * 32u) < M;
+            const int m_row = m0 + row;                                           // this thread's token row
             const int n_col = n_tile * BN + half * kCols;                 // its first channel
             // Blockwise: the scales of k-block kb (sa of this row, sb of this
             // column block) are requested two k-blocks ahead of their use, so
@@ -351,10 +406,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(acc));
+                if (lane == 0) {
+                    if constexpr (kPair)
+                        mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));  // the leader's barrier
+                    else
+                        mbar_arrive(tempty_bar(acc));
+                }
             }
             if (!ok) break;
-            const int m = m_tile * kPrefillBM + row;
+            const int m = m0 + row;
             if (mine) {  // the whole half (4 warps) alike: every warp reaches the named barriers
                 const float sa = (sa_vec && m < M) ? __ldg(args.scale_a + m) : sa0;
                 const int nbase = n_tile * BN + half * kCols;
@@ -383,7 +443,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     fence_proxy_async_smem();
                     named_bar_sync(1u + static_cast<uint32_t>(half), 128u);
                     if (issuer) {
-                        tma_store_2d(&tmap_out, stg, nbase + b * 64, m_tile * kPrefillBM);
+                        tma_store_2d(&tmap_out, stg, nbase + b * 64, m0);
                         bulk_commit_group();
                     }
                 }
@@ -395,21 +455,42 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
     // Every thread triggers only here, after the producer's dependency wait
     // (the producer triggered once more right after its last load).
-    __syncthreads();
+    __syncwarp();
+    if constexpr (kPair)
+        cluster_sync();  // no CTA of the pair arrives remotely after this
+    else
+        __syncthreads();
     grid_launch_dependents();
 
-    if (tid == 0) {
+    if (tid == 0 && leader) {
         // Loads issued but never consumed (only after a timeout): let them land
-        // before the CTA exits.
-        const uint32_t issued = s_issued, consumed = s_consumed;
+        // before the CTAs exit.  A pair's loads all signal the leader's
+        // barriers; the peer's count is read from its shared memory.
+        uint32_t issued = s_issued;
+        if constexpr (kPair) {
+            uint32_t peer;
+            asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                         : "=r"(peer)
+                         : "r"(map_to_rank(smem_u32(&s_issued), 1))
+                         : "memory");
+            issued = max(issued, peer);
+        }
+        const uint32_t consumed = s_consumed;
         for (uint32_t i = consumed; i < issued; ++i)
             mbar_wait(full_bar(static_cast<int>(i % static_cast<uint32_t>(stages))),
                       (i / static_cast<uint32_t>(stages)) & 1u, err, kErrPrefillFullWait);
     }
+    if constexpr (kPair) {
+        __syncwarp();
+        cluster_sync();  // the peer stays until the leader's check of its loads
+    }
     if (warp == 1) {
         mbar_wait(final_bar, 0, err, kErrPrefillAccumWait);  // every MMA has completed
         tc_fence_after();
-        tmem_dealloc(tmem, Cfg::kTmemCols);
+        if constexpr (kPair)
+            tmem_dealloc_pair(tmem, Cfg::kTmemCols);
+        else
+            tmem_dealloc(tmem, Cfg::kTmemCols);
     }
 }
 
@@ -417,9 +498,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
 // Shared memory of one CTA: alignment slack, the stages, the mbarriers
 // (full/empty per stage, full/empty per accumulator, one final), rounded up.
-static size_t prefill_smem_bytes(int stages, int bn) {
+static size_t prefill_smem_bytes(int stages, int bn, bool pair) {
     const size_t barriers = 8u * static_cast<size_t>(2 * stages + 5);
-    const size_t stage = static_cast<size_t>(kPrefillBM + bn) * kBlockK;
+    const size_t stage = static_cast<size_t>(kPrefillBM + (pair ? 128 : bn)) * kBlockK;
     return 1024 + static_cast<size_t>(stages) * stage + 2u * kPrefillOutBox + ((barriers + 127) / 128) * 128;
 }
 
@@ -432,6 +513,20 @@ PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms) {
     p.bn = (M <= kPrefillSmallM && 2 * tiles256 <= num_sms) ? 128 : 256;
     p.n_tiles = static_cast<int>((N + p.bn - 1) / p.bn);
     p.kb_total = static_cast<int>((K + kBlockK - 1) / kBlockK);
+    // CTA pairs (256-token tiles) once there are two token tiles of 128
+    p.pair = (p.bn == 256 && M > kPrefillBM && num_sms >= 2) ? 1 : 0;
+    if (p.pair) {
+        p.m_tiles = static_cast<int>((M + 2 * kPrefillBM - 1) / (2 * kPrefillBM));
+        const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+        const int64_t clusters = std::min<int64_t>(tiles, num_sms / 2);
+        p.tiles = tiles;
+        p.full_units = p.units = tiles;
+        p.ctas = static_cast<int>(2 * clusters);
+        p.stages = PrefillCfg<256, true>::kStages;
+        p.drain_kb = (kPrefillDrainKb > 0 && kPrefillDrainKb < p.kb_total) ? kPrefillDrainKb : p.kb_total;
+        p.smem_bytes = prefill_smem_bytes(p.stages, p.bn, true);
+        return p;
+    }
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     // A last round that would fill at most half of the SMs runs as half tiles
     // (256-channel tiles whose last one has two halves only).
@@ -447,26 +542,54 @@ PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms) {
     p.stages = p.bn == 256 ? PrefillCfg<256>::kStages : PrefillCfg<128>::kStages;
     const int dkb = M <= kPrefillSmallM ? kPrefillDrainKbSmall : kPrefillDrainKb;
     p.drain_kb = (dkb > 0 && dkb < p.kb_total) ? dkb : p.kb_total;
-    p.smem_bytes = prefill_smem_bytes(p.stages, p.bn);
+    p.smem_bytes = prefill_smem_bytes(p.stages, p.bn, false);
     return p;
 }
 
-template <int BN, bool kBlk>
+template <int BN, bool kBlk, bool kPair>
 static cudaError_t launch_bn(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b, const CUtensorMap &tmap_out,
-                             const PrefillArgs &a, const PrefillPlan &plan, const LaunchOpts &opts,
+                             const PrefillArgs &a, const PrefillPlan &plan, const LaunchOpts &opts_in,
                              cudaStream_t stream) {
+    LaunchOpts opts = opts_in;
+    opts.cluster_x = kPair ? 2 : 1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     static bool attr_done[64] = {};  // benign race: the attribute call is idempotent
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(prefill_gemm_kernel<BN, kBlk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(prefill_smem_bytes(PrefillCfg<BN>::kStages, BN)));
+        e = cudaFuncSetAttribute(prefill_gemm_kernel<BN, kBlk, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(prefill_smem_bytes(PrefillCfg<BN, kPair>::kStages, BN, kPair)));
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
-    return launch_with_opts(prefill_gemm_kernel<BN, kBlk>, dim3(static_cast<unsigned>(plan.ctas)), dim3(kPrefillThreads),
-                            plan.smem_bytes, stream, opts, tmap_a, tmap_b, tmap_out, a);
+    int ctas = plan.ctas;
+    if constexpr (kPair) {
+        // A persistent grid of pairs only works if every pair is resident at
+        // once: at most as many clusters as the GPU can hold together (SMs
+        // that have no partner in their GPC hold none).
+        static int max_clusters[64] = {};  // benign race: the query is idempotent
+        int mc = (dev >= 0 && dev < 64) ? max_clusters[dev] : 0;
+        if (mc == 0) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(plan.ctas));
+            cfg.blockDim = dim3(kPrefillThreads);
+            cfg.dynamicSmemBytes = plan.smem_bytes;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&mc, prefill_gemm_kernel<BN, kBlk, kPair>, &cfg);
+            if (e != cudaSuccess) return e;
+            if (mc < 1) return cudaErrorInvalidConfiguration;
+            if (dev >= 0 && dev < 64) max_clusters[dev] = mc;
+        }
+        ctas = std::min(ctas, 2 * mc);
+    }
+    return launch_with_opts(prefill_gemm_kernel<BN, kBlk, kPair>, dim3(static_cast<unsigned>(ctas)),
+                            dim3(kPrefillThreads), plan.smem_bytes, stream, opts, tmap_a, tmap_b, tmap_out, a);
 }
 
 cudaError_t launch_prefill_gemm(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b, const CUtensorMap &tmap_out,
@@ -492,11 +615,13 @@ cudaError_t launch_prefill_gemm(const CUtensorMap &tmap_a, const CUtensorMap &tm
     if (granularity == kGranBlock128) {
         // every k-block has its own scales: drain after each one
         a.drain_kb = 1;
-        if (plan.bn == 128) return launch_bn<128, true>(tmap_a, tmap_b, tmap_out, a, plan, opts, stream);
-        return launch_bn<256, true>(tmap_a, tmap_b, tmap_out, a, plan, opts, stream);
+        if (plan.bn == 128) return launch_bn<128, true, false>(tmap_a, tmap_b, tmap_out, a, plan, opts, stream);
+        if (plan.pair) return launch_bn<256, true, true>(tmap_a, tmap_b, tmap_out, a, plan, opts, stream);
+        return launch_bn<256, true, false>(tmap_a, tmap_b, tmap_out, a, plan, opts, stream);
     }
-    if (plan.bn == 128) return launch_bn<128, false>(tmap_a, tmap_b, tmap_out, a, plan, opts, stream);
-    return launch_bn<256, false>(tmap_a, tmap_b, tmap_out, a, plan, opts, stream);
+    if (plan.bn == 128) return launch_bn<128, false, false>(tmap_a, tmap_b, tmap_out, a, plan, opts, stream);
+    if (plan.pair) return launch_bn<256, false, true>(tmap_a, tmap_b, tmap_out, a, plan, opts, stream);
+    return launch_bn<256, false, false>(tmap_a, tmap_b, tmap_out, a, plan, opts, stream);
 }
 
 }  // namespace fp8k

@@ -175,7 +175,8 @@ constexpr int kPrefillBN = 256;
 constexpr int64_t kPrefillMinM = 33;  // fp8_scaled_mm sends M >= this to the prefill kernel
 
 struct PrefillPlan {
-    int bn;  // output channels per tile: 256, or 128 for small M with few tiles
+    int bn;    // output channels per tile: 256, or 128 for small M with few tiles
+    int pair;  // 1: CTA pairs (cta_group::2) on 256-token x 256-channel tiles
     int m_tiles, n_tiles, kb_total;
     int64_t tiles, full_units, units;  // units: whole tiles below full_units, then 128-channel halves
     int ctas;       // persistent CTAs (one per SM at most)
