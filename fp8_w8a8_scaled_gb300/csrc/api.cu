@@ -215,7 +215,7 @@ fp8_status noalloc_scratch(void **out) {
 fp8_status tile_gemm(DeviceState *st, const void *A, const void *B, const float *scale_a, const float *scale_b,
                      int granularity, int64_t M, int64_t N, int64_t K, void *out, const fp8k::LaunchOpts &opts,
                      cudaStream_t stream) {
-    const fp8k::PrefillPlan plan = fp8k::plan_prefill(M, N, K, st->num_sms);
+    const fp8k::PrefillPlan plan = fp8k::plan_prefill(M, N, K, st->num_sms, granularity == FP8_GRAN_BLOCK_128);
     if (plan.units > kI32Max) return FP8_ERR_UNSUPPORTED;
     CUtensorMap ta, tb;
     fp8_status s;

@@ -504,7 +504,7 @@ static size_t prefill_smem_bytes(int stages, int bn, bool pair) {
     return 1024 + static_cast<size_t>(stages) * stage + 2u * kPrefillOutBox + ((barriers + 127) / 128) * 128;
 }
 
-PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms) {
+PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms, bool blockwise) {
     PrefillPlan p{};
     p.m_tiles = static_cast<int>((M + kPrefillBM - 1) / kPrefillBM);
     // 256-channel tiles, unless they would leave most SMs idle while the
@@ -513,8 +513,11 @@ PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms) {
     p.bn = (M <= kPrefillSmallM && 2 * tiles256 <= num_sms) ? 128 : 256;
     p.n_tiles = static_cast<int>((N + p.bn - 1) / p.bn);
     p.kb_total = static_cast<int>((K + kBlockK - 1) / kBlockK);
-    // CTA pairs (256-token tiles) once there are two token tiles of 128
-    p.pair = (p.bn == 256 && M > kPrefillBM && num_sms >= 2) ? 1 : 0;
+    // CTA pairs (256-token tiles) once there are two token tiles of 128, but
+    // not for blockwise scaling: its per-k-block drains would hand each
+    // accumulator back across the pair (measured 239 against 142 us on
+    // 2048 x 10240 x 5120)
+    p.pair = (!blockwise && p.bn == 256 && M > kPrefillBM && num_sms >= 2) ? 1 : 0;
     if (p.pair) {
         p.m_tiles = static_cast<int>((M + 2 * kPrefillBM - 1) / (2 * kPrefillBM));
         const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -614,6 +617,7 @@ cudaError_t launch_prefill_gemm(const CUtensorMap &tmap_a, const CUtensorMap &tm
     a.drain_kb = plan.drain_kb;
     if (granularity == kGranBlock128) {
         // every k-block has its own scales: drain after each one
+        if (plan.pair) return cudaErrorInvalidValue;  // the plan must be made for blockwise scaling
         a.drain_kb = 1;
         if (plan.bn == 128) return launch_bn<128, true, false>(tmap_a, tmap_b, tmap_out, a, plan, opts, stream);
         if (plan.pair) return launch_bn<256, true, true>(tmap_a, tmap_b, tmap_out, a, plan, opts, stream);

@@ -185,7 +185,7 @@ struct PrefillPlan {
     size_t smem_bytes;
 };
 
-PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms);
+PrefillPlan plan_prefill(int64_t M, int64_t N, int64_t K, int num_sms, bool blockwise);
 
 cudaError_t launch_prefill_gemm(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b, const CUtensorMap &tmap_out,
                                 const float *scale_a,
