@@ -28,7 +28,8 @@ def fp8():
 
 # (M, N, K): ragged M (not a multiple of 128), ragged N (not a multiple of 256,
 # and N % 16 == 8 for a half 16-column chunk), ragged K (not a multiple of 128).
-SHAPES = [(40, 136, 272), (33, 136, 272), (65, 264, 400), (128, 256, 128), (300, 776, 1040), (257, 1288, 2064), (1000, 520, 5120)]
+SHAPES = [(40, 136, 272), (33, 136, 272), (65, 264, 400), (128, 256, 128), (129, 520, 1040), (300, 776, 1040),
+          (257, 1288, 2064), (1000, 520, 5120)]  # 129: the CTA pair's second CTA holds one token row
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -180,3 +181,53 @@ def test_prefill_invariants(fp8):
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(host_bits(out), y1)
+
+
+_FIRST_CALL_CAPTURED = r"""
+import sys
+sys.path.insert(0, %r)
+import numpy as np, torch
+import fp8_w8a8_scaled_gb300 as fp8
+import workloads
+# the library's first GEMM calls of the process are made inside CUDA-graph
+# capture: the tile kernels' one-time attribute and occupancy set-up runs there
+M, N, K = 300, 776, 1040
+c = workloads.random_gemm(5600, M, N, K, 2)
+A = torch.from_numpy(c["A"]).view(torch.float8_e4m3fn).cuda()
+B = torch.from_numpy(c["B"]).view(torch.float8_e4m3fn).cuda()
+sa = torch.from_numpy(np.ascontiguousarray(c["sa"])).cuda()
+sb = torch.from_numpy(np.ascontiguousarray(c["sb"])).cuda()
+x = torch.from_numpy(workloads.bf16_normal(workloads.rng(5601), (M, K)).view(np.int16)).view(torch.bfloat16).cuda()
+out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+out16 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+torch.cuda.synchronize()
+s = torch.cuda.Stream()
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):
+    fp8.fp8_scaled_mm(A, B, sa, sb, 2, out=out)
+    fp8.w8a16_mm(x, B, sb, fp8.GRAN_PER_CHANNEL, out=out16)
+out.fill_(0); out16.fill_(0)
+g.replay()
+torch.cuda.synchronize()
+ref = fp8.fp8_scaled_mm(A, B, sa, sb, 2)
+ref16 = fp8.w8a16_mm(x, B, sb, fp8.GRAN_PER_CHANNEL)
+torch.cuda.synchronize()
+assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+assert torch.equal(out16.view(torch.int16), ref16.view(torch.int16))
+assert fp8.get_device_error() == 0
+print("first-call-captured-ok")
+"""
+
+
+def test_tile_kernels_first_called_inside_graph_capture():
+    """A fresh process whose first tile-kernel calls (the CTA-pair prefill
+    GEMM and the weight-only tile GEMM) are made inside CUDA-graph capture:
+    the replay equals eager calls bit for bit."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FIRST_CALL_CAPTURED % root], capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "first-call-captured-ok" in r.stdout
