@@ -371,7 +371,7 @@ fp8_status fp8_quant_weight_block(const void *w, void *out, float *scale_out, in
  * and multiplies on the tensor core (fp32 accumulation inside 128-wide
  * k-blocks, TwoSum across them, the scale in binary32 at the end); its
  * stream-K mode uses the per-stream scratch of fp8_scaled_mm.  M >= 33: a tile
- * kernel (128 weight rows x 128 tokens per tile, the whole K) that widens each
+ * kernel (256 weight rows x 128 tokens per tile, the whole K) that widens each
  * E4M3 weight box to bf16 in tensor memory on chip for dense bf16 MMAs (fp32
  * accumulation over K in tensor memory), then y = bf16(fp32(acc * sb)); no
  * widened copy of the weight is made and nothing is allocated.
