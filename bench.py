@@ -244,13 +244,20 @@ def time_graph(torch, graph, reps, dist_barrier):
     return t0.elapsed_time(t1)
 
 
+def segment_bounds(reps, segments):
+    """Replay counts at the segment boundaries: `segments` (at most `reps`,
+    at least one) runs of replays whose lengths differ by at most one."""
+    segments = max(1, min(segments, reps))
+    return [reps * i // segments for i in range(segments + 1)]
+
+
 def time_graph_segments(torch, graph, reps, segments, dist_barrier):
     """Like time_graph, with CUDA events also between `segments` equal runs of
     replays (no synchronisation inside the timed region): returns the total
     and each segment's time in ms."""
     stream = torch.cuda.current_stream()
-    segments = max(1, min(segments, reps))
-    bounds = [reps * i // segments for i in range(segments + 1)]
+    bounds = segment_bounds(reps, segments)
+    segments = len(bounds) - 1
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(segments + 1)]
     dist_barrier()
     torch.cuda.synchronize()
@@ -265,13 +272,13 @@ def time_graph_segments(torch, graph, reps, segments, dist_barrier):
     return ev[0].elapsed_time(ev[-1]), seg
 
 
-def cpu_model():
+def cpu_model(cpuinfo="/proc/cpuinfo"):
     """The host CPU as /proc/cpuinfo names it (model name, or implementer and
     part on Arm), with the machine type and the logical CPU count."""
     name = ""
     try:
         fields = {}
-        with open("/proc/cpuinfo") as f:
+        with open(cpuinfo) as f:
             for line in f:
                 if ":" in line:
                     k, v = line.split(":", 1)

@@ -1,6 +1,7 @@
 """Host-side pieces of the bench (CPU): the clock sampler's parsing of
 nvidia-smi samples, the recorded-traffic lookup that is tied to the decode
-kernel's sources, the algorithmic byte counts, and the whole-job rate."""
+kernel's sources, the algorithmic byte counts, the whole-job rate, the
+timed-region segments of the spread and the CPU model string."""
 import os
 import sys
 
@@ -75,3 +76,28 @@ def test_whole_job_rate_sums_the_replicas():
     one = bench.whole_job_tbps(1, 317_460_528, 0.11)
     assert abs(one - 317_460_528 / 0.11e-3 / 1e12) < 1e-12
     assert abs(bench.whole_job_tbps(4, 317_460_528, 0.11) - 4 * one) < 1e-12
+
+
+def test_segment_bounds_split_the_replays_evenly():
+    for reps in (1, 2, 5, 7, 10, 103):
+        for segments in (1, 3, 5, 8):
+            b = bench.segment_bounds(reps, segments)
+            assert b[0] == 0 and b[-1] == reps
+            lengths = [b[i + 1] - b[i] for i in range(len(b) - 1)]
+            assert len(lengths) == min(segments, reps)
+            assert min(lengths) >= 1 and max(lengths) - min(lengths) <= 1
+    assert bench.segment_bounds(4, 0) == [0, 4]
+
+
+def test_cpu_model_names_arm_and_x86_parts(tmp_path):
+    arm = tmp_path / "arm"
+    arm.write_text("processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU architecture: 8\n"
+                   "CPU part\t: 0xd4f\n\nprocessor\t: 1\nCPU implementer\t: 0x41\nCPU part\t: 0xd4f\n")
+    assert bench.cpu_model(str(arm)).startswith("Neoverse V2 (implementer 0x41 part 0xd4f) (")
+    other = tmp_path / "other"
+    other.write_text("processor\t: 0\nCPU implementer\t: 0x4e\nCPU part\t: 0x004\n")
+    assert bench.cpu_model(str(other)).startswith("(implementer 0x4e part 0x004) (")
+    x86 = tmp_path / "x86"
+    x86.write_text("processor\t: 0\nvendor_id\t: GenuineIntel\nmodel name\t: Example CPU @ 2.00GHz\n")
+    assert bench.cpu_model(str(x86)).startswith("Example CPU @ 2.00GHz (")
+    assert "logical CPUs)" in bench.cpu_model(str(tmp_path / "missing"))
