@@ -476,17 +476,18 @@ def run_gate_up(torch, fp8, device, dist_barrier, dist_max, reps=40):
 
 def run_w8a16(torch, fp8, device, dist_barrier, dist_max, reps=40):
     """Weight-only FP8 GEMM on the merged QKV shape (N 10240, K 5120, bf16
-    activations, per-channel weight scales): the widen-on-chip decode kernel at
-    M in {1, 8, 16, 32} (weight bytes per launch / time, against the HBM peak;
-    20 launches per graph over eight 52.4 MB weights) and the large-M tile
-    kernel (weight widened on chip, bf16 MMAs) at M 2048 in TFLOP/s."""
+    activations, per-channel weight scales): the CUDA-core GEMV at M in {1, 4}
+    and the widen-on-chip decode kernel at M in {8, 16, 32} (weight bytes per
+    launch / time, against the HBM peak; 20 launches per graph over eight 52.4
+    MB weights) and the large-M tile kernel (weight widened on chip, bf16
+    MMAs) at M 2048 in TFLOP/s."""
     N, K = N_QKV, K_HID
     W = [workloads.device_e4m3_codes(torch, (N, K), seed=900 + i, device=device).view(torch.float8_e4m3fn)
          for i in range(8)]
     sb = workloads.device_uniform_f32(torch, (N,), 0.5e-3, 2e-3, seed=908, device=device)
     peak, _ = measured_peaks()
     rows, launches = [], 0
-    for M in (1, 8, 16, 32):
+    for M in (1, 4, 8, 16, 32):
         x = workloads.device_bf16_normal(torch, (M, K), seed=909, device=device)
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
         g = graph_of(torch, device, lambda i: fp8.w8a16_mm(x, W[i % 8], sb, fp8.GRAN_PER_CHANNEL, out=Y,
@@ -497,7 +498,9 @@ def run_w8a16(torch, fp8, device, dist_barrier, dist_max, reps=40):
         launches += 20 * reps
         b = N * K + 2 * M * K + 2 * M * N + 4 * N
         gbps = b / (us * 1e-6) / 1e9
-        rows.append({"M": M, "us": round(us, 3), "GBps": round(gbps, 1), "frac": round(gbps / peak, 4)})
+        kind = fp8.w8a16_describe_dispatch(M, N, K)
+        rows.append({"M": M, "us": round(us, 3), "GBps": round(gbps, 1), "frac": round(gbps / peak, 4),
+                     "kernel": "gemv" if kind == fp8.KERNEL_W16_GEMV else "decode"})
     M = 2048
     x = workloads.device_bf16_normal(torch, (M, K), seed=910, device=device)
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)

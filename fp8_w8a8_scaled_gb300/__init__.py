@@ -43,6 +43,7 @@ KERNEL_DECODE_SPLITK = 1
 KERNEL_PREFILL = 2
 KERNEL_W16_DECODE = 3
 KERNEL_W16_DENSE = 4
+KERNEL_W16_GEMV = 5
 
 E4M3 = torch.float8_e4m3fn
 

@@ -465,6 +465,7 @@ fp8_status quant_fp8_per_token(const void *x, void *out, float *scale_out, int64
 int fp8_w8a16_describe_dispatch(int64_t M, int64_t N, int64_t K) {
     if (M < 0 || N < 1 || K < 1 || M > kI32Max || N > kI32Max || K > kI32Max) return -1;
     if (M == 0) return FP8_KERNEL_NONE;
+    if (fp8k::w8a16_gemv_fits(M, K)) return FP8_KERNEL_W16_GEMV;
     return M >= fp8k::kPrefillMinM ? FP8_KERNEL_W16_DENSE : FP8_KERNEL_W16_DECODE;
 }
 
@@ -501,7 +502,14 @@ fp8_status fp8_w8a16_mm_ex(const void *x, const void *W, const float *scale_b, i
     opts.weights_static = (flags & FP8_FLAG_WEIGHTS_STATIC) != 0;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int per_channel = granularity == FP8_GRAN_PER_CHANNEL ? 1 : 0;
-    if (fp8_w8a16_describe_dispatch(M, N, K) == FP8_KERNEL_W16_DENSE) {
+    const int kind = fp8_w8a16_describe_dispatch(M, N, K);
+    if (kind == FP8_KERNEL_W16_GEMV) {
+        // One to four tokens: the CUDA-core GEMV (whole weight rows per warp,
+        // no split of K, no scratch).
+        return from_cuda(
+            fp8k::launch_w8a16_gemv(W, x, scale_b, per_channel, M, N, K, out, st->err, st->num_sms, opts, cs));
+    }
+    if (kind == FP8_KERNEL_W16_DENSE) {
         // Large M: the tile kernel, widening each E4M3 weight box to bf16 on
         // chip (exact: every E4M3 value is a bf16 value) for dense bf16 MMAs,
         // the weight scale applied to the fp32 accumulator before the bf16

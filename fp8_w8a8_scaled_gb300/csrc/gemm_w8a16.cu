@@ -814,6 +814,194 @@ __global__ void __launch_bounds__(256) widen_weight_kernel(const uint4 *__restri
     }
 }
 
+// ------------------------------------------------------------------ GEMV --
+// One to four tokens: y[m,n] = bf16(fp32(acc[m,n] * sb)) with acc the binary32
+// sum over K of x[m,k] * dec(W[n,k]), on the CUDA cores.  At this M the
+// kernel is bound by the weight bytes and the contraction is too small to pay
+// for a tensor-core hand-off per k-block (the widening into TMEM, the MMA
+// hand-shakes and the cross-CTA fix-up of the split-K kernel cost more than
+// the stream; see the W8A16 decode kernel above).  One CTA per SM takes a
+// contiguous range of weight rows and each of its kGemvWarps warps an equal
+// share of those, whole rows (no split of K: nothing is shared between warps
+// or CTAs, and a row's sum stays in its warp's registers).  Each warp streams
+// its rows in kGemvSeg-byte segments through its own ring of kGemvWarpStages
+// shared-memory stages: lane 0 issues one 1-D bulk copy per segment (the
+// first ones before the dependency wait when the weights are static, so the
+// whole CTA has its ring in flight while the previous kernel finishes) and
+// refills a stage as soon as the warp has read it.  Lane l multiplies the
+// segment's 16-byte vectors l, l + 32, ...: each E4M3 code is widened exactly
+// to bf16 (e4m3x4_to_bf16x4) and multiplied with the bf16 token into one
+// binary32 accumulator per token (mixed-precision fused multiply-adds, bf16
+// operands and binary32 accumulator, in k order within the lane); at the
+// row's end the warp adds the lanes' sums in a fixed butterfly order and lane
+// m stores token m.  A row holding a NaN code gives NaN outputs.  The tokens
+// are read once per CTA into shared memory as bf16, half-vector-transposed
+// ([token][8-value half h][vector v]) so that the 32 lanes' 16-byte reads of
+// one half are consecutive.  (Tokens held as binary32, read once per weight
+// value and token, made shared memory the bound at ~5 us per token on the
+// QKV shape; multiplying several rows per warp to share those reads kept
+// fewer bytes in flight per warp and was slower at one token.  Measured on
+// QKV at M = 1 over the ring's shape: 24 warps x 3 stages of 2560 or 2048
+// bytes 13.6-13.9 us, 32 warps x 2 x 2048 15.2, 32 x 3 x 1536 17.2, 16 x 4 x
+// 2048 16.1; the 2560-byte segments win on the longer weights, gate_up 35.6
+// against 38.9 us.)
+// acc + w.lo * x.lo, then + w.hi * x.hi: bf16 operands, a binary32
+// accumulator, each product exact and the sum rounded once to nearest (the
+// same bits as widening both to binary32 and using __fmaf_rn).
+__device__ __forceinline__ float fma_bf16x2_acc(uint32_t w, uint32_t x, float acc) {
+    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+        "mov.b32 {wl, wh}, %1;\n\t"
+        "mov.b32 {xl, xh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w), "r"(x));
+    return acc;
+}
+
+constexpr int kGemvWarps = 24;
+constexpr int kGemvThreads = 32 * kGemvWarps;
+constexpr int kGemvSeg = 2560;      // bytes of one weight-row segment (one stage; 5 x 32 x 16)
+constexpr int kGemvWarpStages = 3;  // stages per warp
+constexpr uint32_t kGemvRingBytes = static_cast<uint32_t>(kGemvWarps * kGemvWarpStages * kGemvSeg);
+constexpr uint32_t kGemvBarBytes = 8u * kGemvWarps * kGemvWarpStages;
+
+template <int MT>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+    w8a16_gemv_kernel(const uint8_t *__restrict__ W, const __nv_bfloat16 *__restrict__ x,
+                      const float *__restrict__ scale_b, int per_channel, int N, int K,
+                      __nv_bfloat16 *__restrict__ out, uint32_t *err, int weights_static) {
+    extern __shared__ __align__(128) uint8_t gsm[];
+    // [ring: kGemvWarps x kGemvWarpStages x kGemvSeg][barriers][tokens: MT x K bf16]
+    const uint32_t ring = smem_u32(gsm);
+    const uint32_t bars = ring + kGemvRingBytes;
+    uint8_t *const xs = gsm + kGemvRingBytes + kGemvBarBytes;
+    const int NV = K >> 4;  // 16-byte vectors per row
+    const int segs = (K + kGemvSeg - 1) / kGemvSeg;
+    const int tid = static_cast<int>(threadIdx.x), lane = tid & 31, warp = tid >> 5;
+    const int r0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * N / gridDim.x);
+    const int n = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * N / gridDim.x) - r0;
+    const int wr0 = r0 + (warp * n) / kGemvWarps, wr1 = r0 + ((warp + 1) * n) / kGemvWarps;
+    const int items = (wr1 - wr0) * segs;  // (row, segment) pairs of this warp, row-major
+    const uint32_t stage0 = ring + static_cast<uint32_t>(warp * kGemvWarpStages * kGemvSeg);
+    const uint32_t bar0 = bars + 8u * static_cast<uint32_t>(warp * kGemvWarpStages);
+    const uint64_t evict_first = policy_evict_first();
+
+    auto seg_bytes = [&](int j) { return min(kGemvSeg, K - (j % segs) * kGemvSeg); };
+    // lane 0: segment j of this warp's rows into stage j % kGemvWarpStages
+    auto issue = [&](int j) {
+        const int s = j % kGemvWarpStages;
+        const int r = wr0 + j / segs, sg = j % segs;
+        const uint32_t bytes = static_cast<uint32_t>(seg_bytes(j));
+        mbar_arrive_expect_tx(bar0 + 8u * s, bytes);
+        const uint8_t *src = W + static_cast<int64_t>(r) * K + static_cast<int64_t>(sg) * kGemvSeg;
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+            " [%0], [%1], %2, [%3], %4;" ::"r"(stage0 + static_cast<uint32_t>(s * kGemvSeg)),
+            "l"(src), "r"(bytes), "r"(bar0 + 8u * s), "l"(evict_first)
+            : "memory");
+    };
+
+    if (lane == 0) {
+        for (int s = 0; s < kGemvWarpStages; ++s) mbar_init(bar0 + 8u * s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const int pre = min(items, kGemvWarpStages);
+    // Weights that no earlier kernel in the stream writes may be fetched
+    // before the dependency wait; the tokens always wait.
+    if (weights_static && lane == 0)
+        for (int j = 0; j < pre; ++j) issue(j);
+    grid_dependency_wait();
+    {
+        // tokens -> shared memory, 8 bf16 (one 16-byte half of a 16-value
+        // vector) per thread and step, at [token][half h][vector v]
+        const int chunks = MT * (K >> 3);
+        for (int c = tid; c < chunks; c += kGemvThreads) {
+            const int m = c / (K >> 3), k = (c - m * (K >> 3)) << 3;
+            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(m) * K + k));
+            *reinterpret_cast<uint4 *>(xs + ((((m * 2 + ((k >> 3) & 1)) * NV) + (k >> 4)) << 4)) = q;
+        }
+    }
+    __syncthreads();
+    // nothing of this grid is read by the next kernel before it completes:
+    // let it launch, so that its prologue overlaps this grid's stream
+    grid_launch_dependents();
+    if (!weights_static && lane == 0)
+        for (int j = 0; j < pre; ++j) issue(j);
+
+    float acc[MT];
+    uint32_t nan = 0;
+    int j = 0;
+    for (; j < items; ++j) {
+        const int s = j % kGemvWarpStages, sg = j % segs;
+        const bool ok =
+            mbar_wait(bar0 + 8u * s, static_cast<uint32_t>(j / kGemvWarpStages) & 1u, err, kErrW16FullWait);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        if (sg == 0) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
+            nan = 0;
+        }
+        const int nvec = seg_bytes(j) >> 4;
+        const uint8_t *stage = gsm + (warp * kGemvWarpStages + s) * kGemvSeg;
+#pragma unroll
+        for (int u = 0; u < kGemvSeg / 16 / 32; ++u) {
+            const int lv = u * 32 + lane;  // vector within the segment
+            if (lv < nvec) {
+                const uint4 q = *reinterpret_cast<const uint4 *>(stage + 16 * lv);
+                const int v = sg * (kGemvSeg / 16) + lv;  // vector within the row
+                const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // k = 16 v + 8 h + 0..7: weight words 2h, 2h + 1
+                    uint4 xq[MT];
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+                        xq[m] = *reinterpret_cast<const uint4 *>(xs + ((((m * 2 + h) * NV) + v) << 4));
+#pragma unroll
+                    for (int t2 = 0; t2 < 2; ++t2) {
+                        uint32_t lo, hi;  // bf16 pairs (k, k + 1), (k + 2, k + 3), k = 16 v + 8 h + 4 t2
+                        e4m3x4_to_bf16x4(wd[2 * h + t2], lo, hi, nan);
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            acc[m] = fma_bf16x2_acc(lo, t2 == 0 ? xq[m].x : xq[m].z, acc[m]);
+                            acc[m] = fma_bf16x2_acc(hi, t2 == 0 ? xq[m].y : xq[m].w, acc[m]);
+                        }
+                    }
+                }
+            }
+        }
+        // every lane has read the stage: refill it with segment j + stages
+        __syncwarp();
+        if (lane == 0 && j + kGemvWarpStages < items) {
+            fence_proxy_async_smem();
+            issue(j + kGemvWarpStages);
+        }
+        if (sg == segs - 1) {
+            const int r = wr0 + j / segs;
+            const bool has_nan = __any_sync(0xffffffffu, (nan & 0x80808080u) != 0u);
+            const float sb = __ldg(scale_b + (per_channel ? r : 0));
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                float y = acc[m];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) y = __fadd_rn(y, __shfl_xor_sync(0xffffffffu, y, o));
+                if (lane == m)
+                    out[static_cast<int64_t>(m) * N + r] = has_nan ? __float2bfloat16_rn(__int_as_float(0x7fffffff))
+                                                                   : __float2bfloat16_rn(__fmul_rn(y, sb));
+            }
+        }
+    }
+    if (j < items && lane == 0) {
+        // gave up after a timed-out wait: let the copies already issued land
+        // (bounded) before the CTA's shared memory is released
+        const int issued = min(items, j + kGemvWarpStages);
+        for (int i = j; i < issued; ++i)
+            mbar_wait(bar0 + 8u * (i % kGemvWarpStages), static_cast<uint32_t>(i / kGemvWarpStages) & 1u, err,
+                      kErrW16FullWait);
+    }
+}
+
 }  // namespace
 
 // Shared memory of one CTA: alignment slack, the weight ring, the token ring
@@ -940,6 +1128,43 @@ cudaError_t launch_widen_weight(const void *w, const float *scale, int per_chann
     return launch_with_opts(widen_weight_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, opts,
                             static_cast<const uint4 *>(w), static_cast<uint4 *>(out), scale, per_channel, n16,
                             static_cast<int>(K / 16));
+}
+
+
+template <int MT>
+static cudaError_t launch_gemv_mt(const void *W, const void *x, const float *scale_b, int per_channel, int64_t N,
+                                  int64_t K, void *out, uint32_t *err, int num_sms, const LaunchOpts &opts,
+                                  cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool attr_done[64] = {};  // benign race: the attribute call is idempotent
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(w8a16_gemv_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kGemvRingBytes + kGemvBarBytes + kW16GemvMaxXBytes));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    // one CTA per SM (its ring and token copy fill most of the shared
+    // memory), no more CTAs than rows
+    const int64_t ctas = std::min<int64_t>(static_cast<int64_t>(num_sms > 0 ? num_sms : 1), N);
+    const size_t smem = kGemvRingBytes + kGemvBarBytes + static_cast<size_t>(MT) * static_cast<size_t>(K) * 2u;
+    return launch_with_opts(w8a16_gemv_kernel<MT>, dim3(static_cast<unsigned>(ctas)), dim3(kGemvThreads), smem,
+                            stream, opts, static_cast<const uint8_t *>(W), static_cast<const __nv_bfloat16 *>(x),
+                            scale_b, per_channel, static_cast<int>(N), static_cast<int>(K),
+                            static_cast<__nv_bfloat16 *>(out), err, opts.weights_static ? 1 : 0);
+}
+
+cudaError_t launch_w8a16_gemv(const void *W, const void *x, const float *scale_b, int per_channel, int64_t M,
+                              int64_t N, int64_t K, void *out, uint32_t *err, int num_sms, const LaunchOpts &opts,
+                              cudaStream_t stream) {
+    if (!w8a16_gemv_fits(M, K)) return cudaErrorInvalidValue;
+    switch (M) {
+        case 1: return launch_gemv_mt<1>(W, x, scale_b, per_channel, N, K, out, err, num_sms, opts, stream);
+        case 2: return launch_gemv_mt<2>(W, x, scale_b, per_channel, N, K, out, err, num_sms, opts, stream);
+        case 3: return launch_gemv_mt<3>(W, x, scale_b, per_channel, N, K, out, err, num_sms, opts, stream);
+        default: return launch_gemv_mt<4>(W, x, scale_b, per_channel, N, K, out, err, num_sms, opts, stream);
+    }
 }
 
 }  // namespace fp8k

@@ -141,6 +141,19 @@ cudaError_t launch_w8a16_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap
                               int per_channel, int64_t M, int64_t N, int64_t K, void *out, uint32_t *err,
                               const DecodePlan &plan, const DecodeWorkspace &ws, const LaunchOpts &opts,
                               cudaStream_t stream);
+// The weight-only GEMV for one to kW16GemvMaxTokens tokens on the CUDA cores
+// (no tensor core, no split of K, nothing shared between CTAs): one CTA per
+// SM, whole weight rows per warp streamed through a per-warp ring of bulk
+// copies, the tokens staged in shared memory as bf16 (M * K * 2 bytes, at
+// most kW16GemvMaxXBytes beside the 180 KB ring).
+constexpr int kW16GemvMaxTokens = 4;
+constexpr int64_t kW16GemvMaxXBytes = 40 * 1024;
+inline bool w8a16_gemv_fits(int64_t M, int64_t K) {
+    return M >= 1 && M <= kW16GemvMaxTokens && M * K * 2 <= kW16GemvMaxXBytes;
+}
+cudaError_t launch_w8a16_gemv(const void *W, const void *x, const float *scale_b, int per_channel, int64_t M,
+                              int64_t N, int64_t K, void *out, uint32_t *err, int num_sms, const LaunchOpts &opts,
+                              cudaStream_t stream);
 // The weight-only large-M tile kernel (M >= 33): output tiles of 2 x 128
 // weight rows x kW16TileTokens tokens (or one 128-row half in a split last
 // round), the E4M3 weight widened to bf16 on chip.

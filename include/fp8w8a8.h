@@ -89,7 +89,8 @@ typedef enum {
     FP8_KERNEL_DECODE_SPLITK = 1, /* weight-streaming split-K kernel (small M) */
     FP8_KERNEL_PREFILL = 2,       /* persistent tensor-core tile kernel (large M) */
     FP8_KERNEL_W16_DECODE = 3,    /* weight-only: widen-on-chip split-K kernel (M <= 32) */
-    FP8_KERNEL_W16_DENSE = 4      /* weight-only: tile kernel, weight widened on chip, dense bf16 MMAs (M >= 33) */
+    FP8_KERNEL_W16_DENSE = 4,     /* weight-only: tile kernel, weight widened on chip, dense bf16 MMAs (M >= 33) */
+    FP8_KERNEL_W16_GEMV = 5       /* weight-only: CUDA-core GEMV, whole weight rows per warp (M <= 4) */
 } fp8_kernel_id;
 
 /* fp8_scaled_mm -- the FP8 W8A8 scaled GEMM.
@@ -366,7 +367,13 @@ fp8_status fp8_quant_weight_block(const void *w, void *out, float *scale_out, in
  *   out      bf16 [M,N], 16-byte aligned, written in full
  *   M, N, K  as fp8_scaled_mm (K % 16 == 0, N % 8 == 0)
  *
- * y[m,n] = bf16( (sum_k x[m,k] * dec(W[n,k])) * sb ).  M <= 32: a split-K
+ * y[m,n] = bf16( (sum_k x[m,k] * dec(W[n,k])) * sb ).  M <= 4 (and M * K <=
+ * 20480): a GEMV on the CUDA cores, each warp whole weight rows, the weight
+ * widened exactly to bf16 and multiplied with the bf16 tokens into binary32
+ * (one fused multiply-add per product, k order within a lane, the lanes added
+ * in a fixed order), so a token's row is the same alone or among up to four;
+ * nothing is shared between CTAs and no scratch is used.  Otherwise
+ * M <= 32: a split-K
  * kernel that widens each E4M3 weight tile to bf16 in tensor memory (exact)
  * and multiplies on the tensor core (fp32 accumulation inside 128-wide
  * k-blocks, TwoSum across them, the scale in binary32 at the end); its
@@ -385,8 +392,10 @@ fp8_status fp8_w8a16_mm(const void *x, const void *W, const float *scale_b, int 
 fp8_status fp8_w8a16_mm_ex(const void *x, const void *W, const float *scale_b, int granularity, int out_dtype,
                            int64_t M, int64_t N, int64_t K, void *out, void *stream, unsigned flags);
 
-/* FP8_KERNEL_W16_DECODE for 1 <= M <= 32, FP8_KERNEL_W16_DENSE for M >= 33,
- * FP8_KERNEL_NONE for M == 0, -1 for sizes fp8_w8a16_mm rejects.  Pure. */
+/* FP8_KERNEL_W16_GEMV for 1 <= M <= 4 with M * K <= 20480 (the GEMV keeps the
+ * tokens in 40 KB of shared memory as bf16), otherwise FP8_KERNEL_W16_DECODE
+ * for 1 <= M <= 32 and FP8_KERNEL_W16_DENSE for M >= 33; FP8_KERNEL_NONE for
+ * M == 0, -1 for sizes fp8_w8a16_mm rejects.  Pure. */
 int fp8_w8a16_describe_dispatch(int64_t M, int64_t N, int64_t K);
 
 /* fp8_widen_weight -- out[n,k] = bf16_rne( fp32(dec(W[n,k]) * s) ), s =

@@ -205,7 +205,11 @@ def test_w8a16_validation(L):
     assert L.fp8_w8a16_mm(GOOD, GOOD2, SC, 0, 0, 0, 64, 64, GOOD3, None) == 0
     d = L.fp8_w8a16_describe_dispatch
     assert d(0, 64, 64) == 0 and d(-1, 64, 64) == -1 and d(4, 0, 64) == -1
-    assert all(d(M, 10240, 5120) == 3 for M in (1, 16, 17, 32))
+    # one to four tokens whose binary32 copy fits 96 KB: the GEMV (5)
+    assert all(d(M, 10240, 5120) == 5 for M in (1, 2, 3, 4))
+    assert d(4, 10240, 5120) == 5 and d(4, 10240, 5136) == 3 and d(1, 5120, 17408) == 5
+    assert d(1, 10240, 20480) == 5 and d(1, 10240, 20496) == 3 and d(2, 10240, 17408) == 3
+    assert all(d(M, 10240, 5120) == 3 for M in (5, 16, 17, 32))
     assert all(d(M, 10240, 5120) == 4 for M in (33, 64, 2048))
     wd = L.fp8_widen_weight
     assert wd(GOOD, SC, 1, 0, 64, GOOD3, None) == 0

@@ -1,6 +1,7 @@
 """GPU parity of the weight-only FP8 GEMM (W8A16: bf16 activations, E4M3
-weights) against the CPU oracle: the widen-on-chip decode kernel (M <= 32,
-every output), the weight widening entry point (byte-exact), the large-M
+weights) against the CPU oracle: the CUDA-core GEMV (M <= 4, every output),
+the widen-on-chip decode kernel (M <= 32, every output), the weight widening
+entry point (byte-exact), the large-M
 tile kernel (ragged shapes, every output; a 2048 x 10240 x 5120 prefill
 chunk, sampled outputs), and the invariants (determinism, dispatch, NaN
 codes)."""
@@ -89,7 +90,9 @@ SHAPES = [(1, 8, 16), (3, 136, 272), (16, 128, 128), (5, 1032, 5120), (16, 264, 
 @pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("per_channel", [True, False])
 def test_w16_decode_random_codes(fp8, orc, M, N, K, per_channel):
-    assert fp8.w8a16_describe_dispatch(M, N, K) == fp8.KERNEL_W16_DECODE
+    # M <= 4 runs the GEMV, the others the decode kernel
+    want = fp8.KERNEL_W16_GEMV if M <= 4 else fp8.KERNEL_W16_DECODE
+    assert fp8.w8a16_describe_dispatch(M, N, K) == want
     x, W, sb = operands(9000 + M + N + K, M, N, K, per_channel)
     check(fp8, orc, x, W, sb, per_channel, f"w16 {M}x{N}x{K} pc={per_channel}")
 
@@ -108,7 +111,7 @@ def test_w16_decode_tile_counts(fp8, orc, M, N, K):
     assert np.array_equal(run_w16(fp8, to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb), 1), y)
 
 
-@pytest.mark.parametrize("M", [1, 8, 16, 32])
+@pytest.mark.parametrize("M", [1, 4, 8, 16, 32])
 def test_w16_decode_qkv(fp8, orc, M):
     """Merged QKV (N 10240, K 5120), per-channel quantised N(0, 0.02) weights,
     every output."""
@@ -125,31 +128,69 @@ def test_w16_decode_rerun_bitwise(fp8):
 
 
 def test_w16_rows_independent(fp8):
-    """Row m of an M=16 call against the same row alone: same tile, same K
-    division, so bitwise."""
+    """Row m of an M=16 call against the same row in a 5-token call: same
+    16-token tile of the decode kernel, same K division, so bitwise."""
     x, W, sb = operands(9300, 16, 1032, 2064)
     xd, Wd, sbd = to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb)
     full = run_w16(fp8, xd, Wd, sbd, 1)
-    for m in (0, 9, 15):
+    for m in (0, 9, 11):
+        assert fp8.w8a16_describe_dispatch(5, 1032, 2064) == fp8.KERNEL_W16_DECODE
+        assert np.array_equal(run_w16(fp8, xd[m:m + 5].contiguous(), Wd, sbd, 1)[0], full[m])
+
+
+def test_w16_gemv_rows_independent(fp8):
+    """The GEMV: each token's sum runs in its own registers in a fixed order,
+    so a row alone, in a pair and among four gives the same bits."""
+    x, W, sb = operands(9310, 4, 2056, 5120)
+    xd, Wd, sbd = to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb)
+    assert fp8.w8a16_describe_dispatch(4, 2056, 5120) == fp8.KERNEL_W16_GEMV
+    full = run_w16(fp8, xd, Wd, sbd, 1)
+    for m in range(4):
         assert np.array_equal(run_w16(fp8, xd[m:m + 1].contiguous(), Wd, sbd, 1)[0], full[m])
+    assert np.array_equal(run_w16(fp8, xd[1:3].contiguous(), Wd, sbd, 1), full[1:3])
 
 
-def test_w16_nan_weight_code(fp8, orc):
-    x, W, sb = operands(9400, 4, 136, 272)
+# (M, N, K) for the GEMV: one 16-byte vector per row (K 16), rows fewer than
+# the CTAs (N 8, 24), 512-byte segments with a ragged last one (K 4112, 272),
+# the largest K for one and for four tokens (the bf16 token copy at its 40 KB
+# limit), a long K (the down projection), warps with one to several rows
+# (N 20000: 132 rows per CTA, 5 or 6 per warp)
+GEMV_SHAPES = [(1, 8, 16), (2, 24, 4112), (3, 1032, 5120), (4, 2056, 5120), (1, 5120, 17408), (1, 600, 20480),
+               (4, 304, 272), (2, 20000, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMV_SHAPES)
+@pytest.mark.parametrize("per_channel", [True, False])
+def test_w16_gemv(fp8, orc, M, N, K, per_channel):
+    """Every output of the GEMV against the oracle at the acceptance bound
+    (its binary32 sums are well inside the tensor-core accumulation allowance
+    the bound carries), and a rerun bitwise."""
+    assert fp8.w8a16_describe_dispatch(M, N, K) == fp8.KERNEL_W16_GEMV
+    x, W, sb = operands(9320 + M + N + K, M, N, K, per_channel, weights="codes" if K <= 5120 else "quant")
+    y = check(fp8, orc, x, W, sb, per_channel, f"w16 gemv {M}x{N}x{K} pc={per_channel}")
+    assert np.array_equal(run_w16(fp8, to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb), 1 if per_channel else 0), y)
+
+
+@pytest.mark.parametrize("M", [4, 8])
+def test_w16_nan_weight_code(fp8, orc, M):
+    """A NaN weight code: that output channel is NaN for every token, the
+    others finite (M 4: the GEMV; M 8: the decode kernel)."""
+    x, W, sb = operands(9400, M, 136, 272)
     W[7, 100] = 0x7F
     y = run_w16(fp8, to_dev_bf16(x), to_dev_e4m3(W), to_dev_f32(sb), 1)
     assert np.all(np.isnan(bf16_bits_to_f64(y[:, 7])))
     assert not np.any(np.isnan(bf16_bits_to_f64(np.delete(y, 7, axis=1))))
 
 
-@pytest.mark.parametrize("M", [32, 256])
+@pytest.mark.parametrize("M", [4, 32, 256])
 @pytest.mark.parametrize("per_channel", [True, False])
 def test_w16_every_code_exact(fp8, orc, M, per_channel):
     """Every non-NaN E4M3 weight code through the on-chip widening, exactly:
     token m is one-hot at k = m, so y[m, n] = bf16(dec(W[n, m]) * 1) is the
     decoded code itself (subnormal codes and signed zeros included); over the
     256 rows n the codes (n + 8 m) mod 256 cover all 254 non-NaN codes for
-    every m.  M 32 runs the decode kernel, M 256 the tile kernel."""
+    every m.  M 4 runs the GEMV, M 32 the decode kernel, M 256 the tile
+    kernel."""
     N, K = 256, 256
     x = np.zeros((M, K), np.uint16)
     x[np.arange(M), np.arange(M)] = 0x3F80  # bf16 1.0
