@@ -1,10 +1,12 @@
 """Host checks of the integer and binary32 recipes the kernels compute with,
 each against an independent definition (the oracle's E4M3 decode, exact
-integer arithmetic): the E4M3 -> bf16 widening of the weight-only kernels
-and its NaN test, and the decode GEMM's exact split of a k-block partial
-into integer parts.  The recipes are restated here in numpy so that a wrong
-constant or shift fails on the CPU; the GPU tests run the kernels themselves
-(test_w16_every_code_exact, the exact-sum decode tests).  No GPU needed."""
+integer arithmetic, exact rationals): the E4M3 -> bf16 widening of the
+weight-only kernels and its NaN test, the decode GEMM's exact split of a
+k-block partial into integer parts, and the TwoSum accumulation of the
+blockwise paths.  The recipes are restated here in numpy so that a wrong
+constant, shift or sign fails on the CPU; the GPU tests run the kernels
+themselves (test_w16_every_code_exact, the exact-sum decode tests, the
+blockwise tests).  No GPU needed."""
 import numpy as np
 
 import oracle
@@ -128,3 +130,47 @@ def test_exact_split_sums_are_order_free():
     perm = g.permutation(len(p))
     hi2, lo2 = exact_split(p[perm])
     assert int(np.sum(hi2)) * (1 << 23) + int(np.sum(lo2)) == total
+
+
+def two_sum_acc(hi, lo, v):
+    """The blockwise paths' TwoSum accumulation (Knuth's error-free sum: s =
+    hi + v and err with s + err == hi + v exactly, err folded into lo), every
+    operation binary32 round to nearest."""
+    f = np.float32
+    s = f(hi + v)
+    bv = f(s - hi)
+    av = f(s - bv)
+    err = f(f(hi - av) + f(v - bv))
+    return s, f(lo + err)
+
+
+def test_two_sum_is_error_free():
+    """One step: s + err equals hi + v exactly (binary64 holds both sums
+    exactly for exponents this close)."""
+    g = np.random.default_rng(8400)
+    a = (g.standard_normal(100000) * np.exp2(g.integers(-20, 20, 100000))).astype(np.float32)
+    b = (g.standard_normal(100000) * np.exp2(g.integers(-20, 20, 100000))).astype(np.float32)
+    for x, y in zip(a[:20000], b[:20000]):
+        s, err = two_sum_acc(x, np.float32(0.0), y)
+        assert float(s) + float(err) == float(x) + float(y)
+
+
+def test_two_sum_accumulation_of_k_block_partials():
+    """A tile's 40 scaled k-block partials (K 5120) folded into (hi, lo) and
+    rounded once: within a few units of 2^-48 of the partials' absolute sum
+    from the exact sum, where a plain binary32 sum is ~2^-24 away."""
+    from fractions import Fraction
+    g = np.random.default_rng(8500)
+    worst_ts, worst_plain = 0.0, 0.0
+    for _ in range(200):
+        x = (g.standard_normal(40) * np.exp2(g.integers(-6, 6, 40))).astype(np.float32)
+        hi, lo, plain = np.float32(0.0), np.float32(0.0), np.float32(0.0)
+        for v in x:
+            hi, lo = two_sum_acc(hi, lo, v)
+            plain = np.float32(plain + v)
+        exact = sum(Fraction(float(v)) for v in x)
+        scale = float(sum(abs(Fraction(float(v))) for v in x))
+        worst_ts = max(worst_ts, abs(float(Fraction(float(hi)) + Fraction(float(lo)) - exact)) / scale)
+        worst_plain = max(worst_plain, abs(float(Fraction(float(plain)) - exact)) / scale)
+    assert worst_ts <= 64 * 2.0 ** -48
+    assert worst_plain > 2.0 ** -30  # the comparison has teeth: plain binary32 loses far more
