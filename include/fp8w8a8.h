@@ -88,7 +88,7 @@ typedef enum {
     FP8_KERNEL_NONE = 0,          /* M == 0: nothing is launched */
     FP8_KERNEL_DECODE_SPLITK = 1, /* weight-streaming split-K kernel (small M) */
     FP8_KERNEL_PREFILL = 2,       /* persistent tensor-core tile kernel (large M) */
-    FP8_KERNEL_W16_DECODE = 3,    /* weight-only: widen-on-chip split-K kernel (M <= 32) */
+    FP8_KERNEL_W16_DECODE = 3,    /* weight-only: widen-on-chip split-K kernel (M <= 32, where the GEMV does not apply) */
     FP8_KERNEL_W16_DENSE = 4,     /* weight-only: tile kernel, weight widened on chip, dense bf16 MMAs (M >= 33) */
     FP8_KERNEL_W16_GEMV = 5       /* weight-only: CUDA-core GEMV, whole weight rows per warp (M <= 4) */
 } fp8_kernel_id;
