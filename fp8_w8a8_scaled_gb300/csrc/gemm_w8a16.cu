@@ -845,6 +845,7 @@ __global__ void __launch_bounds__(256) widen_weight_kernel(const uint4 *__restri
 // bytes 13.6-13.9 us, 32 warps x 2 x 2048 15.2, 32 x 3 x 1536 17.2, 16 x 4 x
 // 2048 16.1; the 2560-byte segments win on the longer weights, gate_up 35.6
 // against 38.9 us.)
+
 // acc + w.lo * x.lo, then + w.hi * x.hi: bf16 operands, a binary32
 // accumulator, each product exact and the sum rounded once to nearest (the
 // same bits as widening both to binary32 and using __fmaf_rn).
